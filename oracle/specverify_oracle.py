@@ -1,0 +1,284 @@
+"""Float64 CPU oracle for the batched speculative-decoding verify-and-commit step.
+
+TEST INFRASTRUCTURE.  Only tests/, __graft_entry__.smoke() and bench.py's CPU
+baseline leg may import or run this module.  The product path (the CUDA library
+and its Python binding) never imports it and shares no code with it.
+
+It is a plain, slow, deliberately unoptimised restatement of what the step
+computes, one sequence at a time, in float64 (bf16 and fp32 inputs widen to
+float64 exactly).  Sources, by page title and section:
+
+  [KB]  "M013" card of the ai-infra knowledge base (xuujii.github.io), §02-§06:
+        greedy table (§03), acceptance min(1,p/q) with p, q the real sampling
+        distributions after temperature (§04), the three-token worked example and
+        the residual max(p-q,0)/R with the R = 0 remark (§05), commit and KV
+        rollback pseudocode (§06).
+  [TUT] "投机解码教程：从概率保持、KV Cache 回滚到性能盈亏平衡" (richardf123.github.io),
+        §2 (contiguous prefix), §3 (greedy), §4 (logit alignment), §5.2-§5.3 (trim
+        to t+m, then t+m+1; bonus), §7.1-§7.3 (acceptance, residual, multi-token).
+  [APP] "学徒的草稿：推测解码与大模型的加速哲学" (carrie-l.github.io), part 2,
+        Steps 3-4 (accept when p >= q, else with probability p/q; residual; bonus).
+  [NXM] nxmr.cn news 151309: the same three-token example, exact-fraction check,
+        "R = 0 must not produce NaN", temperature/top-p must be reflected in p and q.
+
+Readings where the pages leave a step open (each also listed in the design doc):
+  * Rows arrive pre-aligned: target row i judges draft i, row 0 is the saved
+    boundary prediction, row gamma_b is the bonus row ([TUT] §4 table).
+  * Acceptance is the strict test u < min(1, r) with r = p(d)/q(d); when q(d) = 0,
+    r = +inf if p(d) > 0, and r = 0 whenever p(d) = 0.
+  * Greedy ties resolve to the lowest token id ([KB] §03 asks for a fixed rule).
+  * Inverse CDF in ascending id order: the token is the smallest v with
+    C_v > u * C_{V-1}, C the running sum of the weights; if none qualifies
+    (only possible when u >= 1) the last id with positive weight is taken.
+  * A rejection whose residual mass R is exactly 0 (unreachable in exact maths,
+    [KB] §05, [NXM]) samples from p_m instead and sets status bit 2.
+  * A draft id outside [0, V) is a rejection at that row (status bit 1); a
+    num_draft outside [0, gmax] is clamped (status bit 4).
+  * Temperature T <= 0 (or NaN) marks a greedy sequence; otherwise p = softmax(P/T)
+    and q = softmax(Q/T), the same T on both sides.
+
+Parity pins: see tests/test_oracle_pins.py.  Every function below is pinned by at
+least one test against values the pages print, closed forms, or brute force.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import List, Optional
+
+import numpy as np
+
+# status bits reported per sequence
+ST_BAD_DRAFT = 1
+ST_R_ZERO = 2
+ST_CLAMPED_GAMMA = 4
+ST_HISTORY_FULL = 8
+
+
+def widen(row: np.ndarray, dtype: str) -> np.ndarray:
+    """bf16 bit patterns (uint16) or float32 -> float64, exactly."""
+    if dtype == "bf16":
+        return (row.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    return np.asarray(row, dtype=np.float32).astype(np.float64)
+
+
+def softmax_at_temperature(logits: np.ndarray, T: float) -> np.ndarray:
+    """p_v = exp(L_v/T - max_u L_u/T) / sum_w exp(L_w/T - max_u L_u/T).
+
+    [KB] §04 and [NXM]: p and q are the distributions actually sampled from, after
+    temperature; the same T divides both sides.
+    """
+    z = logits / T
+    z = z - np.max(z)
+    e = np.exp(z)
+    return e / np.sum(e)
+
+
+def greedy_argmax(logits: np.ndarray) -> int:
+    """g = argmax_v L_v, the lowest id among equal maxima ([TUT] §3, [KB] §03)."""
+    best = np.max(logits)
+    return int(np.flatnonzero(logits == best)[0])
+
+
+def acceptance_ratio(p_d: float, q_d: float) -> float:
+    """r = p(d)/q(d), with q(d) = 0 read as +inf when p(d) > 0 and 0 when p(d) = 0."""
+    if p_d == 0.0:
+        return 0.0
+    if q_d == 0.0:
+        return math.inf
+    return p_d / q_d
+
+
+def accept_draft(p_d: float, q_d: float, u: float) -> bool:
+    """Accept draft d iff u < min(1, p(d)/q(d)) ([TUT] §7.1; [APP] Step 3: a draft
+    with p >= q is always kept, otherwise kept with probability p/q)."""
+    return u < min(1.0, acceptance_ratio(p_d, q_d))
+
+
+def residual_weights(p: np.ndarray, q: np.ndarray) -> np.ndarray:
+    """w_v = max(p_v - q_v, 0); R = sum_v w_v = 1 - sum_v min(p_v, q_v) ([TUT] §7.2)."""
+    return np.maximum(p - q, 0.0)
+
+
+def inverse_cdf(weights: np.ndarray, u: float):
+    """Sample an id from weights/sum(weights) with the explicit uniform u.
+
+    C_v = sum_{k<=v} w_k in ascending id order; the token is the smallest v with
+    C_v > u * C_{V-1}.  Returns (token, margin, total) where margin =
+    min(u - C_{v-1}/C_{V-1}, C_v/C_{V-1} - u) is how far u sits from the nearest
+    decision boundary (used only to flag near-ties in parity tests).
+    """
+    C = np.cumsum(weights)
+    total = float(C[-1])
+    target = u * total
+    hits = np.flatnonzero(C > target)
+    if hits.size:
+        v = int(hits[0])
+    else:
+        v = int(np.flatnonzero(weights > 0)[-1])
+    lo = float(C[v - 1]) if v > 0 else 0.0
+    hi = float(C[v])
+    margin = min(u - lo / total, hi / total - u) if total > 0 else 0.0
+    return v, margin, total
+
+
+@dataclasses.dataclass
+class SequenceResult:
+    tokens: List[int]               # the m+1 emitted tokens: d_0..d_{m-1}, then correction/bonus
+    m: int                          # accepted drafts
+    status: int
+    gamma: int                      # num_draft after clamping
+    greedy: bool
+    p_draft: List[float]            # p_i(d_i) for i < gamma (sampling), NaN where undefined
+    q_draft: List[float]
+    mass: float                     # mass the last token was drawn from (R, or sum p on bonus)
+    accept_margins: List[float]     # |u_i - r_i| for the decisions actually taken (i <= m)
+    sample_margin: float            # inverse-CDF margin (inf for greedy)
+
+    def flagged(self, tol: float = 1e-5) -> bool:
+        return any(a < tol for a in self.accept_margins) or self.sample_margin < tol
+
+
+def verify_greedy_sequence(target: np.ndarray, drafts: np.ndarray, gamma: int) -> SequenceResult:
+    """Greedy verification of one sequence ([TUT] §3.3, §4, §5.3; [KB] §03).
+
+    target: float64 [>= gamma+1, V] aligned rows.  m is the first i < gamma with
+    d_i != argmax(row i), else gamma; the emitted token is argmax(row m), which is the
+    target's replacement on a mismatch and the bonus token on full acceptance.
+    """
+    V = target.shape[1]
+    status = 0
+    m = gamma
+    for i in range(gamma):
+        d = int(drafts[i])
+        if not (0 <= d < V):
+            status |= ST_BAD_DRAFT
+        if d != greedy_argmax(target[i]):
+            m = i
+            break
+    tok = greedy_argmax(target[m])
+    toks = [int(x) for x in drafts[:m]] + [tok]
+    nan = [math.nan] * gamma
+    return SequenceResult(toks, m, status, gamma, True, nan, list(nan), math.nan, [], math.inf)
+
+
+def verify_sample_sequence(target: np.ndarray, draft: np.ndarray, drafts: np.ndarray,
+                           gamma: int, T: float, u_accept: np.ndarray, u_sample: float) -> SequenceResult:
+    """Sampling verification of one sequence ([TUT] §7.1-§7.3; [APP] Steps 3-4; [KB] §05-§06).
+
+    For i = 0..gamma-1, left to right: p_i = softmax(P_i/T), q_i = softmax(Q_i/T),
+    accept d_i iff u_accept[i] < min(1, p_i(d_i)/q_i(d_i)); stop at the first rejection
+    m.  On a rejection the correction is drawn from max(p_m - q_m, 0)/R with u_sample; on
+    full acceptance the bonus token is drawn from p_gamma with u_sample.
+    """
+    V = target.shape[1]
+    status = 0
+    m = gamma
+    p_d: List[float] = []
+    q_d: List[float] = []
+    margins: List[float] = []
+    p_m = q_m = None
+    for i in range(gamma):
+        p = softmax_at_temperature(target[i], T)
+        q = softmax_at_temperature(draft[i], T)
+        d = int(drafts[i])
+        if 0 <= d < V:
+            pd, qd = float(p[d]), float(q[d])
+            p_d.append(pd)
+            q_d.append(qd)
+            margins.append(abs(float(u_accept[i]) - acceptance_ratio(pd, qd)))
+            ok = accept_draft(pd, qd, float(u_accept[i]))
+        else:
+            status |= ST_BAD_DRAFT
+            p_d.append(math.nan)
+            q_d.append(math.nan)
+            ok = False
+        if not ok:
+            m = i
+            p_m, q_m = p, q
+            break
+    p_d += [math.nan] * (gamma - len(p_d))
+    q_d += [math.nan] * (gamma - len(q_d))
+    if m < gamma:
+        w = residual_weights(p_m, q_m)
+        if np.sum(w) > 0.0:
+            tok, smargin, mass = inverse_cdf(w, float(u_sample))
+        else:
+            status |= ST_R_ZERO
+            tok, smargin, mass = inverse_cdf(p_m, float(u_sample))
+            mass = 0.0
+    else:
+        p_bonus = softmax_at_temperature(target[gamma], T)
+        tok, smargin, mass = inverse_cdf(p_bonus, float(u_sample))
+    toks = [int(x) for x in drafts[:m]] + [tok]
+    return SequenceResult(toks, m, status, gamma, False, p_d, q_d, mass, margins, smargin)
+
+
+def verify_batch(target: np.ndarray, draft: Optional[np.ndarray], dtype: str,
+                 draft_tokens: np.ndarray, num_draft: np.ndarray, temperature: Optional[np.ndarray],
+                 u_accept: Optional[np.ndarray], u_sample: Optional[np.ndarray],
+                 seqs=None) -> List[SequenceResult]:
+    """Verify every sequence (or the listed ones) of a batch.
+
+    target [B, gmax+1, V], draft [B, gmax, V] (bf16 bits or float32); a sequence whose
+    temperature is not > 0, or every sequence when temperature is None, is greedy.
+    """
+    B, gp1, V = target.shape
+    gmax = gp1 - 1
+    out = []
+    for b in (range(B) if seqs is None else seqs):
+        g = int(num_draft[b])
+        clamped = 0
+        if g < 0 or g > gmax:
+            g = min(max(g, 0), gmax)
+            clamped = ST_CLAMPED_GAMMA
+        P = widen(target[b, : g + 1], dtype)
+        T = None if temperature is None else float(temperature[b])
+        if T is None or not (T > 0.0):
+            r = verify_greedy_sequence(P, draft_tokens[b], g)
+        else:
+            Q = widen(draft[b, :g], dtype) if g > 0 else np.zeros((0, V))
+            r = verify_sample_sequence(P, Q, draft_tokens[b], g, T, u_accept[b], float(u_sample[b]))
+        r.status |= clamped
+        out.append(r)
+    return out
+
+
+def emitted_rows(results: List[SequenceResult], gmax: int) -> np.ndarray:
+    """out_tokens layout [B, gmax+1]: the m+1 emitted tokens, then -1."""
+    out = np.full((len(results), gmax + 1), -1, dtype=np.int64)
+    for b, r in enumerate(results):
+        out[b, : len(r.tokens)] = r.tokens
+    return out
+
+
+def commit_kv_lengths(kv_len: np.ndarray, m: np.ndarray, correction_processed: bool,
+                      draft_kv_len: Optional[np.ndarray] = None, out_tokens: Optional[np.ndarray] = None,
+                      history: Optional[np.ndarray] = None, committed_len: Optional[np.ndarray] = None):
+    """Commit one round ([TUT] §5.1-§5.2; [KB] §06).
+
+    Both caches are trimmed to t + m (the accepted prefix); once the correction or bonus
+    token has been fed through both models they hold t + m + 1.  When a token history is
+    given, the m+1 emitted tokens are appended at committed_len; a sequence whose history
+    would overflow is left untouched and flagged (bit 8).
+    Returns (kv_len, draft_kv_len, history, committed_len, status) as new arrays.
+    """
+    kv = np.array(kv_len, dtype=np.int64)
+    dkv = None if draft_kv_len is None else np.array(draft_kv_len, dtype=np.int64)
+    hist = None if history is None else np.array(history)
+    clen = None if committed_len is None else np.array(committed_len, dtype=np.int64)
+    status = np.zeros(len(kv), dtype=np.int64)
+    add = 1 if correction_processed else 0
+    for b in range(len(kv)):
+        n = int(m[b]) + 1
+        if hist is not None:
+            cap = hist.shape[1]
+            if clen[b] + n > cap:
+                status[b] |= ST_HISTORY_FULL
+                continue
+            hist[b, clen[b]: clen[b] + n] = out_tokens[b, :n]
+            clen[b] += n
+        kv[b] += int(m[b]) + add
+        if dkv is not None:
+            dkv[b] += int(m[b]) + add
+    return kv, dkv, hist, clen, status

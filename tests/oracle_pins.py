@@ -1,0 +1,289 @@
+"""Pin checks for the float64 oracle, shared by the pin tests and the mutation tests.
+
+Each function raises AssertionError when the oracle disagrees with something the
+pages or plain mathematics fix.  The mutation tests plant plausible mistakes in
+the oracle and require that at least one of these checks then fails.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+
+from oracle import specverify_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
+        return json.load(f)
+
+
+def frac_list(xs):
+    return [Fraction(x) for x in xs]
+
+
+# ---------------------------------------------------------------------------------------
+# Black-box integration of the oracle's step over its explicit uniforms.
+#
+# For fixed drafts the step is a function of (u_accept[0..g-1], u_sample).  Row i is kept
+# iff u_accept[i] lies below a threshold t_i, and the sampled token is a non-decreasing step
+# function of u_sample (ascending-id inverse CDF).  Thresholds and breakpoints are located
+# by bisection on the oracle itself; the law of the emitted tokens is then the sum over the
+# cells of the resulting product partition of [0,1)^(g+1), each evaluated at its centre.
+# ---------------------------------------------------------------------------------------
+
+_BISECT = 64
+
+
+def _bisect(pred, lo=0.0, hi=1.0):
+    """sup{u in [lo,hi] : pred(u)} for a predicate true on [lo, t) and false on [t, hi]."""
+    if not pred(lo):
+        return lo
+    if pred(np.nextafter(hi, 0.0)):
+        return hi
+    for _ in range(_BISECT):
+        mid = 0.5 * (lo + hi)
+        if pred(mid):
+            lo = mid
+        else:
+            hi = mid
+    return 0.5 * (lo + hi)
+
+
+def step(P, Q, d, T, ua, us):
+    g = len(d)
+    return O.verify_sample_sequence(P, Q, np.asarray(d, dtype=np.int64), g, T,
+                                    np.asarray(ua, dtype=np.float64), us)
+
+
+def emitted_law(P, Q, d, T):
+    """{tuple(emitted tokens): probability} of one step with drafts d, integrating over
+    the uniforms by probing the oracle."""
+    g = len(d)
+    V = P.shape[1]
+    thr = []
+    for i in range(g):
+        # make rows < i pass (u = 0) so that row i's decision is observable
+        base = [0.0] * g
+
+        def kept(u, i=i):
+            ua = list(base)
+            ua[i] = u
+            return step(P, Q, d, T, ua, 0.5).m > i
+
+        reachable = all(step(P, Q, d, T, [0.0] * g, 0.5).m > j for j in range(i))
+        thr.append(_bisect(kept) if reachable else 0.5)
+    law = {}
+    for cell in itertools.product((0, 1), repeat=g):
+        widths, centre = 1.0, []
+        for i, side in enumerate(cell):
+            lo, hi = (0.0, thr[i]) if side == 0 else (thr[i], 1.0)
+            widths *= hi - lo
+            centre.append(0.5 * (lo + hi))
+        if widths <= 0.0:
+            continue
+
+        def last_tok(us):
+            return step(P, Q, d, T, centre, us).tokens[-1]
+
+        prev = 0.0
+        for v in range(V):
+            b = _bisect(lambda us: last_tok(us) <= v)
+            if b > prev:
+                toks = tuple(step(P, Q, d, T, centre, 0.5 * (prev + b)).tokens)
+                assert toks[-1] == v
+                law[toks] = law.get(toks, 0.0) + widths * (b - prev)
+                prev = b
+    return law
+
+
+def softmax_T(logits, T):
+    """Textbook temperature softmax, used only to state the target's own law."""
+    z = np.asarray(logits, dtype=np.float64) / T
+    e = np.exp(z - z.max())
+    return e / e.sum()
+
+
+# ---------------------------------------------------------------------------------------
+# Pins
+# ---------------------------------------------------------------------------------------
+
+def check_three_token_example(tol=1e-12):
+    """The worked example: kept mass (0.2,0.3,0.2), rejection 0.3, residual (1,0,0),
+    output exactly p (M013 card §05; nxmr.cn 151309)."""
+    G = golden("three_token_example.json")
+    p = np.array([float(Fraction(x)) for x in G["p"]])
+    q = np.array([float(Fraction(x)) for x in G["q"]])
+    P = np.log(np.stack([p, p]))
+    Q = np.log(q)[None, :]
+    out = np.zeros(3)
+    kept = np.zeros(3)
+    for x in range(3):
+        law = emitted_law(P, Q, [x], 1.0)
+        for toks, pr in law.items():
+            if len(toks) == 2:               # x kept (then a bonus token follows)
+                kept[x] += q[x] * pr
+                out[toks[0]] += q[x] * pr
+            else:                            # rejected: the correction is the only token
+                out[toks[0]] += q[x] * pr
+    acc_prob = kept / q
+    assert np.allclose(acc_prob, [float(Fraction(a)) for a in G["accept_prob"]], atol=tol, rtol=0), acc_prob
+    assert np.allclose(kept, [float(Fraction(a)) for a in G["accepted_mass"]], atol=tol, rtol=0), kept
+    assert abs((1 - kept.sum()) - float(Fraction(G["reject_mass"]))) < tol
+    assert np.allclose(out, [float(Fraction(a)) for a in G["output"]], atol=tol, rtol=0), out
+    # the residual branch alone: reject x = B and read the law of the correction
+    res = np.zeros(3)
+    law = emitted_law(P, Q, [1], 1.0)
+    rej = sum(pr for t, pr in law.items() if len(t) == 1)
+    for t, pr in law.items():
+        if len(t) == 1:
+            res[t[0]] += pr / rej
+    assert np.allclose(res, [float(Fraction(a)) for a in G["residual"]], atol=tol, rtol=0), res
+    return out
+
+
+def check_greedy_tables():
+    """Page tables: the draft is kept up to the first mismatch with the target's greedy
+    choice, whose token replaces it (M013 card §03; tutorial §3.3)."""
+    for case in golden("greedy_tables.json")["cases"]:
+        vocab = sorted(set(case["draft"]) | set(case["target_greedy"]) | {"<other>"})
+        ids = {w: i for i, w in enumerate(vocab)}
+        V = len(vocab)
+        k = len(case["draft"])
+        rng = np.random.default_rng(7)
+        rows = rng.normal(0, 1, size=(k + 1, V))
+        for i, w in enumerate(case["target_greedy"]):
+            rows[i, ids[w]] = 10.0
+        d = np.array([ids[w] for w in case["draft"]])
+        r = O.verify_greedy_sequence(rows, d, k)
+        assert r.m == case["accepted"], (r.m, case)
+        assert r.tokens == [ids[w] for w in case["committed"]], (r.tokens, case)
+    # full agreement: k tokens plus the bonus argmax of row k (tutorial §5.3)
+    rows = np.zeros((4, 6))
+    for i, t in enumerate([3, 1, 4, 5]):
+        rows[i, t] = 1.0
+    r = O.verify_greedy_sequence(rows, np.array([3, 1, 4]), 3)
+    assert r.m == 3 and r.tokens == [3, 1, 4, 5], r.tokens
+
+
+def controlled_alpha_rows(alpha, gamma):
+    """p = (a, 1-a, 0), q = (a, 0, 1-a): sum_v min(p, q) = a exactly.  Draft 0 is always kept
+    (p = q), draft 2 always rejected (p = 0)."""
+    with np.errstate(divide="ignore"):
+        P = np.log(np.tile([alpha, 1 - alpha, 0.0], (gamma + 1, 1)))
+        Q = np.log(np.tile([alpha, 0.0, 1 - alpha], (gamma, 1)))
+    return P, Q
+
+
+def expected_emitted_exact(alpha, gamma):
+    """E[emitted per round] by exact enumeration of the draft patterns through the oracle,
+    and the law of m."""
+    P, Q = controlled_alpha_rows(alpha, gamma)
+    E = 0.0
+    pm = np.zeros(gamma + 1)
+    for pat in itertools.product((0, 2), repeat=gamma):
+        w = math.prod(alpha if x == 0 else 1 - alpha for x in pat)
+        r = O.verify_sample_sequence(P, Q, np.array(pat), gamma, 1.0, np.full(gamma, 0.5), 0.5)
+        E += w * len(r.tokens)
+        pm[r.m] += w
+    return E, pm
+
+
+def check_expected_tokens():
+    """Closed form (1 - a^(g+1))/(1 - a) and the values the pages print."""
+    G = golden("expected_tokens.json")
+    for row in G["printed"]:
+        a, g = row["alpha"], row["gamma"]
+        E, pm = expected_emitted_exact(a, g)
+        assert abs(E - row["value"]) <= 0.5 * 10 ** (-row["printed_decimals"]) + 1e-12, (row, E)
+        assert abs(E - (1 - a ** (g + 1)) / (1 - a)) < 1e-12
+        # P(m = j) = a^j (1 - a) for j < g, a^g at g (tutorial §8)
+        want = [a ** j * (1 - a) for j in range(g)] + [a ** g]
+        assert np.allclose(pm, want, atol=1e-14), pm
+        EM = sum(j * pm[j] for j in range(g + 1))
+        assert abs(EM - a * (1 - a ** g) / (1 - a)) < 1e-12
+    for row in G["misprinted"]:
+        E, _ = expected_emitted_exact(row["alpha"], row["gamma"])
+        assert abs(E - row["formula_on_same_page"]) < 1e-6, (row, E)
+
+
+def random_tables(V, depth, seed, scale=1.5, zero_frac=0.0):
+    """Conditional logits of a toy target and draft model: logits(prefix) per model."""
+    rng = np.random.default_rng(seed)
+    cache = {}
+
+    def logits(model, prefix):
+        key = (model, tuple(prefix))
+        if key not in cache:
+            x = rng.normal(0, scale, size=V)
+            if zero_frac and model == "target":
+                mask = rng.random(V) < zero_frac
+                mask[rng.integers(V)] = False
+                x[mask] = -np.inf
+            cache[key] = x
+        return cache[key]
+
+    return logits
+
+
+def check_joint_law(V, gamma, T, seed, zero_frac=0.0, tol=1e-9):
+    """Brute force: draft tokens drawn autoregressively from the toy draft model, target rows
+    aligned as in the tutorial's §4 table, the step's emitted prefix extended by the target's
+    own sampling up to gamma+1 tokens must have exactly the target's autoregressive law
+    (tutorial §7.3: every position keeps its conditional law)."""
+    logits = random_tables(V, gamma + 1, seed, zero_frac=zero_frac)
+    n = gamma + 1
+    ext = {}
+    for d in itertools.product(range(V), repeat=gamma):
+        qd = 1.0
+        for i in range(gamma):
+            qd *= softmax_T(logits("draft", d[:i]), T)[d[i]]
+        if qd == 0.0:
+            continue
+        P = np.stack([logits("target", d[:i]) for i in range(gamma + 1)])
+        Q = np.stack([logits("draft", d[:i]) for i in range(gamma)])
+        for toks, pr in emitted_law(P, Q, list(d), T).items():
+            # extend with the target's own sampling up to n tokens
+            frontier = {toks: qd * pr}
+            while True:
+                nxt = {}
+                for seq, w in frontier.items():
+                    if len(seq) == n:
+                        ext[seq] = ext.get(seq, 0.0) + w
+                        continue
+                    pt = softmax_T(logits("target", seq), T)
+                    for v in range(V):
+                        if pt[v] > 0:
+                            nxt[seq + (v,)] = nxt.get(seq + (v,), 0.0) + w * pt[v]
+                if not nxt:
+                    break
+                frontier = nxt
+    for seq in itertools.product(range(V), repeat=n):
+        want = 1.0
+        for j in range(n):
+            want *= softmax_T(logits("target", seq[:j]), T)[seq[j]]
+        got = ext.get(seq, 0.0)
+        assert abs(got - want) < tol, (seq, got, want)
+
+
+def check_inverse_cdf_convention():
+    """Ascending ids, strict C_v > u*R: zero-weight ids are never returned."""
+    w = np.array([0.0, 0.5, 0.0, 0.25, 0.25, 0.0])
+    assert O.inverse_cdf(w, 0.0)[0] == 1
+    assert O.inverse_cdf(w, 0.49999)[0] == 1
+    assert O.inverse_cdf(w, 0.5)[0] == 3
+    assert O.inverse_cdf(w, 0.75)[0] == 4
+    assert O.inverse_cdf(w, np.nextafter(1.0, 0.0))[0] == 4
+    assert O.inverse_cdf(w, 1.0)[0] == 4       # u outside [0,1): the last positive id
+
+
+def check_greedy_tie_rule():
+    row = np.array([1.0, 3.0, 2.0, 3.0, -np.inf, 3.0])
+    assert O.greedy_argmax(row) == 1
+    assert O.greedy_argmax(np.full(5, -np.inf)) == 0
