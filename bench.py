@@ -1,0 +1,400 @@
+#!/usr/bin/env python3
+"""Throughput of the batched verify-and-commit step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference] [--config 3]
+
+One step = one pass of the whole hot path over one batch: spec_verify_sample (row statistics,
+acceptance, first rejection, residual/bonus draw, emit) followed by spec_commit_kv_lengths.
+The default workload is sampling with B=128 sequences, gamma=4 drafts, V=128256, bf16 logits,
+T=0.8 (295.5 MB of logits per step).  Prints one JSON line (rank 0).
+
+Metric: verified draft rows per second (sum of gamma_b over the batch, per step) and the
+achieved HBM bandwidth of the verify kernel: algorithmic bytes (every valid logit row read
+once) divided by its CUDA-event duration, against the measured HBM copy bandwidth.
+
+--impl reference times the float64 CPU oracle on the host cores instead, on a bounded sample
+of the same workload per step (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified draft rows/sec and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "verify_sample_B128_g4_V128256_bf16_dram.txt")
+KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_verification_34_gb300", "csrc", "verify.cu")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--copies", type=int, default=4, help="resident input copies rotated per step")
+    ap.add_argument("--e2e-steps", type=int, default=40)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def workload_config(wl, l2_note):
+    return {"workload": wl.name, "B": wl.B, "gamma": wl.gmax, "V": wl.V, "logits": wl.dtype,
+            "temperature": float(wl.temperature.max()), "algorithmic_bytes_per_step": wl.algorithmic_bytes(),
+            "verified_rows_per_step": wl.verified_rows(), "l2": l2_note}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("hbm_gbs"):
+            return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs: STREAM-style copy)"
+    return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+def recorded_traffic(units_per_launch):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this exact
+    kernel source; else None."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    kv = {}
+    for line in open(TRAFFIC_FILE, encoding="utf-8"):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    sha = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
+    if kv.get("source_sha256") != sha:
+        return None
+    try:
+        return int(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id=None, period_ms=50):
+        self.rows, self.proc, self.err = [], None, None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               f"-lms", str(period_ms)]
+        if gpu_id is not None:
+            cmd += ["-i", str(gpu_id)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError as e:
+            self.err = str(e)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if self.err or not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": self.err or "no nvidia-smi samples"}
+        win = [r for t, r in self.rows if t0 <= t <= t1 + 0.05] or [r for _, r in self.rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, reasons = [], set()
+        smax = None
+        for r in win:
+            try:
+                sm.append(float(r[1]))
+                smax = float(r[2])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def smi_gpu_id(local_rank):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",")]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return local_rank
+
+
+def all_reduce_max(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_oracle_rate(wl, seconds, seqs_cap=None):
+    """Oracle throughput on a bounded sample of the same batch: rows/s, sequences used."""
+    from oracle import specverify_oracle as O
+    t0 = time.perf_counter()
+    n = rows = 0
+    order = list(range(wl.B))
+    while True:
+        b = order[n % wl.B]
+        O.verify_batch(wl.target, wl.draft, wl.dtype, wl.draft_tokens, wl.num_draft,
+                       None if wl.greedy_only else wl.temperature, wl.u_accept, wl.u_sample, seqs=[b])
+        rows += int(wl.num_draft[b])
+        n += 1
+        el = time.perf_counter() - t0
+        if (el >= seconds and n >= 2) or (seqs_cap and n >= seqs_cap):
+            return rows / el, n, rows, el
+
+
+# ------------------------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from speculative_decoding_verification_34_gb300 import workloads as W
+    from oracle import specverify_oracle as O
+    wl = W.WORKLOADS[args.config](seed=0)
+    temp = None if wl.greedy_only else wl.temperature
+
+    def one(b):
+        O.verify_batch(wl.target, wl.draft, wl.dtype, wl.draft_tokens, wl.num_draft, temp,
+                       wl.u_accept, wl.u_sample, seqs=[b])
+
+    # size each step so that the whole run stays within ~150 s: whole sequences, at least one
+    t0 = time.perf_counter()
+    one(0)
+    t_seq = time.perf_counter() - t0
+    per_step = max(1, int(150.0 / max(1, args.steps + args.warmup) / max(t_seq, 1e-6)))
+    per_step = min(per_step, wl.B)
+    nxt = [0]
+
+    def step():
+        r = 0
+        for _ in range(per_step):
+            b = nxt[0] % wl.B
+            one(b)
+            r += int(wl.num_draft[b])
+            nxt[0] += 1
+        return r
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    rows = sum(step() for _ in range(args.steps))
+    el = time.perf_counter() - t0
+    value = rows / el
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl, "CPU oracle: host memory"),
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{per_step} sequence(s) of the {wl.B}-sequence batch per step "
+                                       f"(cycling), float64 numpy oracle, single thread"},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_native(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from speculative_decoding_verification_34_gb300 import build
+    from speculative_decoding_verification_34_gb300 import specverify as sv
+    from speculative_decoding_verification_34_gb300 import workloads as W
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+    if rank == 0:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    sv.load_library()
+
+    wl = W.WORKLOADS[args.config](seed=rank)   # weak scaling: every rank verifies its own batch
+    B, g, V = wl.B, wl.gmax, wl.V
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+    ncopies = max(1, args.copies)
+    tgt = [to_dev(wl.target) for _ in range(ncopies)]
+    drf = [to_dev(wl.draft) for _ in range(ncopies)] if not wl.greedy_only else None
+    toks, nd = to_dev(wl.draft_tokens), to_dev(wl.num_draft)
+    temp, ua, us = to_dev(wl.temperature), to_dev(wl.u_accept), to_dev(wl.u_sample)
+    kv0 = to_dev(wl.kv_len)
+    out = torch.empty((B, g + 1), dtype=torch.int32, device=device)
+    macc = torch.empty(B, dtype=torch.int32, device=device)
+    st = torch.empty(B, dtype=torch.int32, device=device)
+    dg = torch.empty((B, 2 * g + 1), dtype=torch.float32, device=device)
+    kv = kv0.clone()
+    dkv = kv0.clone()
+    stream = torch.cuda.current_stream(device)
+    verify = [sv.prepare_verify_sample(tgt[c], drf[c], toks, nd, temp, ua, us, out, macc, dg, st,
+                                       stream=stream) for c in range(ncopies)]
+    commit = sv.prepare_commit_kv_lengths(macc, kv, dkv, True, stream=stream)
+
+    for i in range(args.warmup):
+        verify[i % ncopies]()
+        commit()
+    torch.cuda.synchronize(device)
+    mean_emit = float(macc.float().mean().item()) + 1.0
+
+    K = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(smi_gpu_id(local))
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    n0 = sv.spec_launch_count()
+    w0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        ev0[i].record(stream)
+        verify[i % ncopies]()
+        ev1[i].record(stream)
+        commit()
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    w1 = time.time()
+    launches = sv.spec_launch_count() - n0
+    if world > 1:
+        dist.barrier()
+    sampler.stop()
+    clocks = sampler.summary(w0, w1)
+
+    elapsed_ms = start.elapsed_time(end)
+    kern_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    kern_mean_ms = statistics.fmean(kern_ms)
+    kern_med_ms = statistics.median(kern_ms)
+    elapsed_ms = all_reduce_max(elapsed_ms, world, device)
+    kern_mean_ms = all_reduce_max(kern_mean_ms, world, device)
+
+    rows_step = wl.verified_rows()
+    value = world * rows_step * K / (elapsed_ms / 1e3)
+    abytes = wl.algorithmic_bytes()
+    peak, peak_src = measured_peak()
+    achieved = abytes / (kern_mean_ms / 1e3) / 1e9
+
+    # ---- end to end through the public binding, host buffers, copies inside the region ----
+    pin = lambda a: (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16
+                     else torch.from_numpy(np.ascontiguousarray(a))).pin_memory()
+    h_in = [pin(wl.target), pin(wl.draft), pin(wl.draft_tokens), pin(wl.num_draft),
+            pin(wl.temperature), pin(wl.u_accept), pin(wl.u_sample), pin(wl.kv_len)]
+    d_in = [tgt[0], drf[0], toks, nd, temp, ua, us, kv]
+    h_out = [torch.empty_like(out, device="cpu").pin_memory(), torch.empty_like(macc, device="cpu").pin_memory(),
+             torch.empty_like(kv, device="cpu").pin_memory()]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def e2e_step():
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+        sv.spec_verify_sample(d_in[0], d_in[1], d_in[2], d_in[3], d_in[4], d_in[5], d_in[6],
+                              out, macc, dg, st)
+        sv.spec_commit_kv_lengths(macc, kv, None, True)
+        h_out[0].copy_(out, non_blocking=True)
+        h_out[1].copy_(macc, non_blocking=True)
+        h_out[2].copy_(kv, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    if world > 1:
+        dist.barrier()
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    es.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    ee.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = all_reduce_max(es.elapsed_time(ee), world, device)
+    e2e_value = world * rows_step * args.e2e_steps / (e2e_ms / 1e3)
+
+    cpu = None
+    if rank == 0 and world == 1:
+        rate, nseq, rows, el = cpu_oracle_rate(wl, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "rows/s", "cores": 1, "kind": "oracle",
+               "sample": f"{nseq} of the {wl.B} sequences of the same batch ({rows} verified rows, "
+                         f"{el:.1f} s), float64 numpy oracle, single thread"}
+
+    if rank == 0:
+        traffic = recorded_traffic(1)
+        line = {
+            "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+            "data": "synthetic",
+            "config": workload_config(wl, f"inputs larger than L2 ({abytes / 1e6:.1f} MB of logits per step), "
+                                          f"rotated over {ncopies} resident copies"),
+            "hbm_gbs": achieved, "hbm_frac_of_measured_peak": achieved / peak,
+            "sequences_per_s": world * B * K / (elapsed_ms / 1e3), "mean_emitted_per_sequence": mean_emit,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "verify_kernel<bf16, vec, mixed> (spec_verify_sample)",
+                         "kernel_ms_mean": kern_mean_ms, "kernel_ms_median": kern_med_ms,
+                         "algorithmic_bytes_per_launch": abytes, "peak_source": peak_src},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+            "gpu_launches": launches, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,151 @@
+/*
+ * specverify — batched target-side verify-and-commit step of speculative decoding,
+ * as CUDA kernels for sm_103a behind a plain C ABI.
+ *
+ * One round of speculative decoding is "draft proposal -> target block verification ->
+ * accept/reject -> commit tokens and repair caches" (tutorial "投机解码教程：从概率保持、
+ * KV Cache 回滚到性能盈亏平衡", §2).  This library is the last two stages for a batch of
+ * B independent sequences, given the logits the two models already produced.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every data pointer is a DEVICE pointer owned by the caller.  The library allocates
+ *    nothing, keeps no state between calls and never synchronises the host: each call
+ *    enqueues its work on `stream` (a cudaStream_t passed as void*; NULL = the legacy
+ *    default stream) and returns.  Results are valid once the stream reaches that point.
+ *  - Arrays are row-major and contiguous:
+ *        target_logits [B][gmax+1][V]   row i judges draft i; row 0 is the target's saved
+ *                                       prediction for the position after the committed
+ *                                       context; row num_draft[b] is the bonus row
+ *                                       (the alignment table of the tutorial's §4)
+ *        draft_logits  [B][gmax][V]     row i is the draft distribution d_i was drawn from
+ *        draft_tokens  [B][gmax]        int32
+ *        u_accept      [B][gmax]        float32 uniforms in [0,1), one per acceptance test
+ *        u_sample      [B]              float32 uniform in [0,1) for the correction/bonus draw
+ *        out_tokens    [B][gmax+1]      int32: the m+1 emitted tokens, then -1
+ *    Rows past a sequence's num_draft are never read (they may hold anything).
+ *  - Logits are bf16 (SPEC_BF16, raw 16-bit patterns) or float32 (SPEC_F32).  They must be
+ *    finite or -inf, with at least one finite value per read row; NaN or +inf inputs give
+ *    unspecified (but memory-safe) results.
+ *  - Return value: SPEC_OK, or an spec_status_t for errors found on the host (bad
+ *    arguments, CUDA launch failure); spec_last_error() then describes it.  Nothing is
+ *    enqueued when a call fails its argument checks.
+ *  - Data-dependent problems never fault or trap the GPU: they set bits in the optional
+ *    per-sequence status[B] word (see SPEC_ST_*) and a defined fallback is taken.
+ *  - Limits: 0 <= B (B == 0 is a no-op), 0 <= gmax <= SPEC_MAX_GAMMA, 1 <= V <= 2^31-1.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_EINVAL = 1,   /* null required pointer, bad size, misuse */
+  SPEC_EDTYPE = 2,   /* unknown dtype code */
+  SPEC_ENOSPACE = 3, /* a size exceeds a documented maximum */
+  SPEC_ECUDA = 4     /* a CUDA runtime call or kernel launch failed */
+} spec_status_t;
+
+typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype_t;
+
+#define SPEC_MAX_GAMMA 32
+
+/* per-sequence status bits */
+#define SPEC_ST_BAD_DRAFT 1      /* the stopping draft id was outside [0,V): it counted as rejected */
+#define SPEC_ST_R_ZERO 2         /* a rejection met residual mass R == 0: the correction was drawn from p_m */
+#define SPEC_ST_CLAMPED_GAMMA 4  /* num_draft[b] was outside [0,gmax] and was clamped */
+#define SPEC_ST_HISTORY_FULL 8   /* commit: appending would overflow the history; sequence left untouched */
+
+/*
+ * Greedy verification (temperature 0).
+ * Tutorial §3.3-§4 and the greedy table of the "M013" knowledge-base card, §03: with
+ * g_i = argmax_v target[b][i][v] (lowest id among equal maxima), m_b is the first i <
+ * num_draft[b] with draft_tokens[b][i] != g_i, else num_draft[b]; the step emits
+ * draft_tokens[b][0..m-1] followed by g_m (the target's replacement on a mismatch, the
+ * bonus token when every draft matched, tutorial §5.3).
+ *
+ *   target_logits  [B][gmax+1][V], dtype `dtype`
+ *   draft_tokens   [B][gmax]
+ *   num_draft      [B] drafts per sequence, or NULL for gmax everywhere
+ *   out_tokens     [B][gmax+1] (written), num_accepted [B] = m (written)
+ *   status         [B] or NULL (written: SPEC_ST_* bits)
+ */
+int spec_verify_greedy(const void* target_logits, int dtype, const int32_t* draft_tokens,
+                       const int32_t* num_draft, int B, int gmax, int V, int32_t* out_tokens,
+                       int32_t* num_accepted, int32_t* status, void* stream);
+
+/*
+ * Sampling verification (tutorial §7.1-§7.3; card §04-§06; "学徒的草稿" part 2, Steps 3-4).
+ * For a sequence with temperature T > 0: p_i = softmax(target[b][i]/T) and
+ * q_i = softmax(draft[b][i]/T) (the same T on both sides).  Drafts are tested left to right:
+ * d_i is kept iff u_accept[b][i] < min(1, p_i(d_i)/q_i(d_i)); m is the first rejected i (or
+ * num_draft[b]).  On a rejection the correction is the inverse-CDF draw, in ascending id
+ * order, of max(p_m - q_m, 0)/R at u_sample[b]*R (R its total); if R == 0 it is drawn from
+ * p_m instead (SPEC_ST_R_ZERO).  On full acceptance the bonus token is the inverse-CDF draw
+ * of p at row num_draft[b].  A sequence with T <= 0 (or NaN) is verified greedily exactly
+ * as spec_verify_greedy does, and its draft rows are not read.
+ *
+ *   draft_logits   [B][gmax][V], same dtype as target_logits
+ *   temperature    [B] float32
+ *   u_accept       [B][gmax] float32, u_sample [B] float32
+ *   diag           NULL or [B][2*gmax+1] float32 (written): diag[b][2i] = p_i(d_i),
+ *                  diag[b][2i+1] = q_i(d_i) for every i < num_draft[b] (NaN when d_i is out
+ *                  of range, for i >= num_draft[b], and for greedy sequences);
+ *                  diag[b][2*gmax] = R on a rejection (0 when it underflowed), the total
+ *                  mass of p at the bonus row on full acceptance, NaN for greedy sequences.
+ *   The other arguments are as for spec_verify_greedy.
+ */
+int spec_verify_sample(const void* target_logits, const void* draft_logits, int dtype,
+                       const int32_t* draft_tokens, const int32_t* num_draft,
+                       const float* temperature, const float* u_accept, const float* u_sample,
+                       int B, int gmax, int V, int32_t* out_tokens, int32_t* num_accepted,
+                       float* diag, int32_t* status, void* stream);
+
+/*
+ * Commit one round and roll the KV lengths back (tutorial §5.1-§5.2; card §06).
+ * The caches are trimmed to t + m (the accepted prefix of the block the verifier wrote);
+ * after the correction or bonus token has been fed through both models they hold
+ * t + m + 1.  So, per sequence:
+ *     target_kv_len[b] += num_accepted[b] + (correction_processed ? 1 : 0)
+ * and the same for draft_kv_len when it is not NULL (invariant: target length == draft
+ * length == committed length, tutorial §5.1).  When `history` is not NULL, the m+1 emitted
+ * tokens out_tokens[b][0..m] are appended to history[b][committed_len[b]...] and
+ * committed_len[b] grows by m+1; a sequence whose append would pass `cap` is left entirely
+ * untouched (lengths included) and flagged SPEC_ST_HISTORY_FULL in status.
+ *
+ *   num_accepted   [B] int32 (m, as written by a verify call; values are clamped to
+ *                  [0, gmax])
+ *   target_kv_len  [B] int32, read and written; draft_kv_len [B] or NULL
+ *   out_tokens     [B][gmax+1] int32, history [B][cap] int32, committed_len [B] int32 —
+ *                  all three NULL, or all three given (cap >= 1)
+ *   status         [B] or NULL: bits are OR-ed in (not cleared)
+ */
+int spec_commit_kv_lengths(const int32_t* num_accepted, int B, int32_t* target_kv_len,
+                           int32_t* draft_kv_len, int correction_processed,
+                           const int32_t* out_tokens, int gmax, int32_t* history,
+                           int32_t* committed_len, int cap, int32_t* status, void* stream);
+
+/* Message for the calling thread's last non-OK return ("" if none). */
+const char* spec_last_error(void);
+
+/* Kernels this library has launched in this process (all threads, all devices). */
+uint64_t spec_launch_count(void);
+
+/*
+ * How a verify call splits the vocabulary for this V and dtype: each sequence is one
+ * thread-block cluster of *ctas_per_seq blocks, block c owning ids [c*chunk, (c+1)*chunk)
+ * of every row.  Host-only; returns SPEC_OK or SPEC_EINVAL.
+ */
+int spec_verify_plan(int V, int dtype, int* ctas_per_seq, int* chunk);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

@@ -1,0 +1,217 @@
+"""Python binding of libspecverify (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and does nothing but check
+tensor types, shapes and devices, take raw device pointers and the current CUDA stream from
+PyTorch, and forward them.  All of the verification runs in the library's CUDA kernels; if
+the shared library is missing this module raises instead of computing anything itself.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+SPEC_BF16 = 0
+SPEC_F32 = 1
+SPEC_MAX_GAMMA = 32
+ST_BAD_DRAFT, ST_R_ZERO, ST_CLAMPED_GAMMA, ST_HISTORY_FULL = 1, 2, 4, 8
+
+_lib = None
+
+
+class SpecVerifyError(RuntimeError):
+    pass
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libspecverify.so (built in-tree by build.build()); raises if it is absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _build.LIB
+    if not os.path.exists(p):
+        raise SpecVerifyError(f"{p} is missing: build it with "
+                              "speculative_decoding_verification_34_gb300.build.build()")
+    lib = ctypes.CDLL(p)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int
+    lib.spec_verify_greedy.argtypes = [vp, i32, vp, vp, sz, sz, sz, vp, vp, vp, vp]
+    lib.spec_verify_greedy.restype = i32
+    lib.spec_verify_sample.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, sz, sz, sz, vp, vp, vp, vp, vp]
+    lib.spec_verify_sample.restype = i32
+    lib.spec_commit_kv_lengths.argtypes = [vp, sz, vp, vp, i32, vp, sz, vp, vp, sz, vp, vp]
+    lib.spec_commit_kv_lengths.restype = i32
+    lib.spec_last_error.argtypes = []
+    lib.spec_last_error.restype = ctypes.c_char_p
+    lib.spec_launch_count.argtypes = []
+    lib.spec_launch_count.restype = ctypes.c_uint64
+    lib.spec_verify_plan.argtypes = [i32, i32, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
+    lib.spec_verify_plan.restype = i32
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(rc: int):
+    if rc != 0:
+        msg = load_library().spec_last_error().decode(errors="replace")
+        raise SpecVerifyError(f"specverify error {rc}: {msg}")
+
+
+def _ptr(t: Optional[torch.Tensor], name: str, dtype=None, shape=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def spec_verify_greedy(target_logits: torch.Tensor, draft_tokens: torch.Tensor,
+                       num_draft: Optional[torch.Tensor], out_tokens: torch.Tensor,
+                       num_accepted: torch.Tensor, status: Optional[torch.Tensor] = None,
+                       stream=None) -> None:
+    B, gp1, V = target_logits.shape
+    gmax = gp1 - 1
+    lib = load_library()
+    _check(lib.spec_verify_greedy(
+        _ptr(target_logits, "target_logits"), _dtype_code(target_logits),
+        _ptr(draft_tokens, "draft_tokens", torch.int32, (B, gmax)),
+        _ptr(num_draft, "num_draft", torch.int32, (B,)), B, gmax, V,
+        _ptr(out_tokens, "out_tokens", torch.int32, (B, gmax + 1)),
+        _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
+        _ptr(status, "status", torch.int32, (B,)), _stream(stream)))
+
+
+def spec_verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor,
+                       draft_tokens: torch.Tensor, num_draft: Optional[torch.Tensor],
+                       temperature: torch.Tensor, u_accept: torch.Tensor, u_sample: torch.Tensor,
+                       out_tokens: torch.Tensor, num_accepted: torch.Tensor,
+                       diag: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                       stream=None) -> None:
+    B, gp1, V = target_logits.shape
+    gmax = gp1 - 1
+    if draft_logits.dtype != target_logits.dtype:
+        raise TypeError("target and draft logits must have the same dtype")
+    lib = load_library()
+    _check(lib.spec_verify_sample(
+        _ptr(target_logits, "target_logits"),
+        _ptr(draft_logits, "draft_logits", None, (B, gmax, V)), _dtype_code(target_logits),
+        _ptr(draft_tokens, "draft_tokens", torch.int32, (B, gmax)),
+        _ptr(num_draft, "num_draft", torch.int32, (B,)),
+        _ptr(temperature, "temperature", torch.float32, (B,)),
+        _ptr(u_accept, "u_accept", torch.float32, (B, gmax)),
+        _ptr(u_sample, "u_sample", torch.float32, (B,)), B, gmax, V,
+        _ptr(out_tokens, "out_tokens", torch.int32, (B, gmax + 1)),
+        _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
+        _ptr(diag, "diag", torch.float32, (B, 2 * gmax + 1)),
+        _ptr(status, "status", torch.int32, (B,)), _stream(stream)))
+
+
+def spec_commit_kv_lengths(num_accepted: torch.Tensor, target_kv_len: torch.Tensor,
+                           draft_kv_len: Optional[torch.Tensor], correction_processed: bool,
+                           out_tokens: Optional[torch.Tensor] = None,
+                           history: Optional[torch.Tensor] = None,
+                           committed_len: Optional[torch.Tensor] = None,
+                           status: Optional[torch.Tensor] = None, stream=None) -> None:
+    B = num_accepted.shape[0]
+    gmax = out_tokens.shape[1] - 1 if out_tokens is not None else 0
+    cap = history.shape[1] if history is not None else 0
+    lib = load_library()
+    _check(lib.spec_commit_kv_lengths(
+        _ptr(num_accepted, "num_accepted", torch.int32, (B,)), B,
+        _ptr(target_kv_len, "target_kv_len", torch.int32, (B,)),
+        _ptr(draft_kv_len, "draft_kv_len", torch.int32, (B,)), int(bool(correction_processed)),
+        _ptr(out_tokens, "out_tokens", torch.int32), gmax,
+        _ptr(history, "history", torch.int32), _ptr(committed_len, "committed_len", torch.int32, (B,)),
+        cap, _ptr(status, "status", torch.int32, (B,)), _stream(stream)))
+
+
+def spec_launch_count() -> int:
+    return int(load_library().spec_launch_count())
+
+
+def spec_verify_plan(V: int, dtype: int = SPEC_BF16):
+    """(blocks per sequence, vocabulary ids per block) a verify call uses for this V."""
+    cl, ch = ctypes.c_int(), ctypes.c_int()
+    _check(load_library().spec_verify_plan(V, dtype, ctypes.byref(cl), ctypes.byref(ch)))
+    return cl.value, ch.value
+
+
+class _Prepared:
+    """A verify/commit call whose arguments were checked and marshalled once; calling it
+    re-issues the same C call (same buffers, same stream) with no per-call Python checks."""
+
+    def __init__(self, fn, args, keep):
+        self._fn, self._args, self._keep = fn, args, keep
+
+    def __call__(self):
+        _check(self._fn(*self._args))
+
+
+def prepare_verify_sample(target_logits, draft_logits, draft_tokens, num_draft, temperature,
+                          u_accept, u_sample, out_tokens, num_accepted, diag=None, status=None,
+                          stream=None) -> _Prepared:
+    B, gp1, V = target_logits.shape
+    gmax = gp1 - 1
+    lib = load_library()
+    args = (_ptr(target_logits, "target_logits"),
+            _ptr(draft_logits, "draft_logits", target_logits.dtype, (B, gmax, V)),
+            _dtype_code(target_logits),
+            _ptr(draft_tokens, "draft_tokens", torch.int32, (B, gmax)),
+            _ptr(num_draft, "num_draft", torch.int32, (B,)),
+            _ptr(temperature, "temperature", torch.float32, (B,)),
+            _ptr(u_accept, "u_accept", torch.float32, (B, gmax)),
+            _ptr(u_sample, "u_sample", torch.float32, (B,)), B, gmax, V,
+            _ptr(out_tokens, "out_tokens", torch.int32, (B, gmax + 1)),
+            _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
+            _ptr(diag, "diag", torch.float32, (B, 2 * gmax + 1)),
+            _ptr(status, "status", torch.int32, (B,)), _stream(stream))
+    keep = (target_logits, draft_logits, draft_tokens, num_draft, temperature, u_accept,
+            u_sample, out_tokens, num_accepted, diag, status)
+    return _Prepared(lib.spec_verify_sample, args, keep)
+
+
+def prepare_commit_kv_lengths(num_accepted, target_kv_len, draft_kv_len, correction_processed,
+                              out_tokens=None, history=None, committed_len=None, status=None,
+                              stream=None) -> _Prepared:
+    B = num_accepted.shape[0]
+    gmax = out_tokens.shape[1] - 1 if out_tokens is not None else 0
+    cap = history.shape[1] if history is not None else 0
+    lib = load_library()
+    args = (_ptr(num_accepted, "num_accepted", torch.int32, (B,)), B,
+            _ptr(target_kv_len, "target_kv_len", torch.int32, (B,)),
+            _ptr(draft_kv_len, "draft_kv_len", torch.int32, (B,)), int(bool(correction_processed)),
+            _ptr(out_tokens, "out_tokens", torch.int32), gmax, _ptr(history, "history", torch.int32),
+            _ptr(committed_len, "committed_len", torch.int32, (B,)), cap,
+            _ptr(status, "status", torch.int32, (B,)), _stream(stream))
+    keep = (num_accepted, target_kv_len, draft_kv_len, out_tokens, history, committed_len, status)
+    return _Prepared(lib.spec_commit_kv_lengths, args, keep)

@@ -1,0 +1,128 @@
+"""Helpers for GPU-vs-oracle parity tests: upload a workload, run the C-ABI through the
+binding, compare with the float64 oracle sequence by sequence."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from oracle import specverify_oracle as O
+from speculative_decoding_verification_34_gb300 import specverify as sv
+
+CANARY = 64
+SENT_I = -123456789
+PROB_TOL = 1e-5
+MARGIN_TOL = 1e-5
+
+
+def dev(a: np.ndarray, dtype: str = None) -> torch.Tensor:
+    """numpy -> CUDA tensor; uint16 arrays become bfloat16 (bit pattern preserved)."""
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def padded(shape, dtype, fill):
+    """A CUDA buffer with CANARY sentinel elements after the returned view."""
+    n = int(np.prod(shape))
+    buf = torch.full((n + CANARY,), fill, dtype=dtype, device="cuda")
+    return buf, buf[:n].view(*shape)
+
+
+def canary_ok(buf, n, fill) -> bool:
+    tail = buf[n:].cpu()
+    if tail.dtype.is_floating_point and math.isnan(fill):
+        return bool(torch.isnan(tail).all())
+    return bool((tail == fill).all())
+
+
+def run_gpu(wl, mode: str = "auto", target=None, draft=None, check_canary=True):
+    """Run one verify call on a Workload.  mode: 'greedy' (spec_verify_greedy) or 'sample'."""
+    if mode == "auto":
+        mode = "greedy" if wl.greedy_only else "sample"
+    B, g = wl.B, wl.gmax
+    tgt = dev(wl.target) if target is None else target
+    toks = dev(wl.draft_tokens)
+    nd = dev(wl.num_draft)
+    ob, out = padded((B, g + 1), torch.int32, SENT_I)
+    mb, macc = padded((B,), torch.int32, SENT_I)
+    sb, st = padded((B,), torch.int32, SENT_I)
+    db, dg = padded((B, 2 * g + 1), torch.float32, float("nan"))
+    if mode == "greedy":
+        sv.spec_verify_greedy(tgt, toks, nd, out, macc, st)
+    else:
+        drf = dev(wl.draft) if draft is None else draft
+        sv.spec_verify_sample(tgt, drf, toks, nd, dev(wl.temperature), dev(wl.u_accept),
+                              dev(wl.u_sample), out, macc, dg, st)
+    torch.cuda.synchronize()
+    if check_canary:
+        assert canary_ok(ob, B * (g + 1), SENT_I), "out_tokens overrun"
+        assert canary_ok(mb, B, SENT_I), "num_accepted overrun"
+        assert canary_ok(sb, B, SENT_I), "status overrun"
+        if mode == "sample":
+            assert canary_ok(db, B * (2 * g + 1), float("nan")), "diag overrun"
+    return {"out": out.cpu().numpy(), "m": macc.cpu().numpy(), "status": st.cpu().numpy(),
+            "diag": dg.cpu().numpy() if mode == "sample" else None}
+
+
+def oracle_results(wl, seqs=None, mode="auto"):
+    if mode == "auto":
+        mode = "greedy" if wl.greedy_only else "sample"
+    temp = None if mode == "greedy" else wl.temperature
+    return O.verify_batch(wl.target, wl.draft, wl.dtype, wl.draft_tokens, wl.num_draft, temp,
+                          wl.u_accept, wl.u_sample, seqs=seqs)
+
+
+def draft_probs(wl, b, g):
+    """p_i(d_i), q_i(d_i) for every i < g from the oracle's softmax (NaN for bad ids)."""
+    T = float(wl.temperature[b])
+    pd, qd = [], []
+    for i in range(g):
+        d = int(wl.draft_tokens[b, i])
+        if 0 <= d < wl.V:
+            p = O.softmax_at_temperature(O.widen(wl.target[b, i], wl.dtype), T)
+            q = O.softmax_at_temperature(O.widen(wl.draft[b, i], wl.dtype), T)
+            pd.append(p[d])
+            qd.append(q[d])
+        else:
+            pd.append(math.nan)
+            qd.append(math.nan)
+    return pd, qd
+
+
+def compare(wl, gpu, results, seqs=None, check_probs=True):
+    """Element-by-element comparison.  Returns (n_checked, flagged_list).  Raises on any
+    mismatch in a sequence whose oracle decision margins are all >= MARGIN_TOL."""
+    seqs = list(range(wl.B)) if seqs is None else list(seqs)
+    flagged = []
+    g_all = wl.gmax
+    for b, r in zip(seqs, results):
+        out, m, st = gpu["out"][b], int(gpu["m"][b]), int(gpu["status"][b])
+        want = np.full(g_all + 1, -1)
+        want[: len(r.tokens)] = r.tokens
+        if r.flagged(MARGIN_TOL):
+            flagged.append(b)
+            # several answers are correct here: check that this one is a valid step
+            assert 0 <= m <= r.gamma and out[m] >= 0 and out[m] < wl.V, (b, out, m)
+            assert list(out[:m]) == list(wl.draft_tokens[b, :m]), (b, out)
+            assert all(x == -1 for x in out[m + 1:]), (b, out)
+            continue
+        assert m == r.m, f"seq {b}: m gpu={m} oracle={r.m}"
+        assert list(out) == list(want), f"seq {b}: tokens gpu={list(out)} oracle={list(want)}"
+        assert st == r.status, f"seq {b}: status gpu={st} oracle={r.status}"
+        if gpu["diag"] is not None:
+            dg = gpu["diag"][b]
+            if r.greedy:
+                assert np.isnan(dg).all(), (b, dg)
+            elif check_probs:
+                pd, qd = draft_probs(wl, b, r.gamma)
+                for i in range(g_all):
+                    gp, gq = dg[2 * i], dg[2 * i + 1]
+                    if i < r.gamma and not math.isnan(pd[i]):
+                        assert abs(gp - pd[i]) <= PROB_TOL and abs(gq - qd[i]) <= PROB_TOL, \
+                            f"seq {b} row {i}: p {gp} vs {pd[i]}, q {gq} vs {qd[i]}"
+                    else:
+                        assert math.isnan(gp) and math.isnan(gq), (b, i, gp, gq)
+                assert abs(dg[2 * g_all] - r.mass) <= PROB_TOL, f"seq {b}: mass {dg[2 * g_all]} vs {r.mass}"
+    return len(seqs), flagged

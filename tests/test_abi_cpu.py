@@ -1,0 +1,86 @@
+"""The C-ABI library builds, loads and exports every symbol the header declares; host-side
+argument checks return their error codes without touching a GPU (CPU only)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from speculative_decoding_verification_34_gb300 import build
+from speculative_decoding_verification_34_gb300 import specverify as sv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = build.build()
+    return sv.load_library(path)
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h, encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(spec_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_symbols_exported(lib):
+    names = declared_functions()
+    assert {"spec_verify_greedy", "spec_verify_sample", "spec_commit_kv_lengths",
+            "spec_last_error"} <= set(names)
+    raw = ctypes.CDLL(build.LIB)
+    for n in names:
+        assert hasattr(raw, n), f"{n} declared in include/ but not exported"
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails its checks before any CUDA call
+
+
+def greedy(lib, target=FAKE, dtype=0, toks=FAKE, B=4, gmax=3, V=100, out=FAKE, macc=FAKE):
+    return lib.spec_verify_greedy(target, dtype, toks, None, B, gmax, V, out, macc, None, None)
+
+
+def sample(lib, target=FAKE, draft=FAKE, dtype=0, temp=FAKE, ua=FAKE, us=FAKE, B=4, gmax=3, V=100):
+    return lib.spec_verify_sample(target, draft, dtype, FAKE, None, temp, ua, us, B, gmax, V,
+                                  FAKE, FAKE, None, None, None)
+
+
+def test_host_argument_checks(lib):
+    n0 = lib.spec_launch_count()
+    assert greedy(lib, dtype=7) == 2 and b"dtype" in lib.spec_last_error()
+    assert greedy(lib, B=-1) == 1
+    assert greedy(lib, V=0) == 1
+    assert greedy(lib, V=(1 << 30) + 1) == 1
+    assert greedy(lib, gmax=-1) == 1
+    assert greedy(lib, gmax=33) == 3
+    assert greedy(lib, target=None) == 1
+    assert greedy(lib, toks=None) == 1
+    assert greedy(lib, out=None) == 1 and greedy(lib, macc=None) == 1
+    assert greedy(lib, B=0) == 0 and lib.spec_last_error() == b""
+    assert greedy(lib, toks=None, gmax=0, B=0) == 0
+    assert sample(lib, draft=None) == 1 and sample(lib, temp=None) == 1
+    assert sample(lib, ua=None) == 1 and sample(lib, us=None) == 1
+    assert sample(lib, B=0) == 0
+    assert sample(lib, draft=None, ua=None, gmax=0, B=0) == 0
+    c = lib.spec_commit_kv_lengths
+    assert c(FAKE, 4, FAKE, None, 1, FAKE, 3, None, None, 10, None, None) == 1   # partial history args
+    assert c(FAKE, 4, FAKE, None, 1, FAKE, 3, FAKE, FAKE, 0, None, None) == 1    # cap < 1
+    assert c(None, 4, FAKE, None, 1, None, 3, None, None, 0, None, None) == 1
+    assert c(FAKE, 4, FAKE, None, 1, None, 40, None, None, 0, None, None) == 3
+    assert c(FAKE, 0, FAKE, None, 1, None, 3, None, None, 0, None, None) == 0
+    assert lib.spec_launch_count() == n0      # nothing was launched
+
+
+def test_plan_splits_vocabulary(lib):
+    for V in [1, 3, 1024, 4096, 4097, 32000, 50000, 128256, 151936, 1 << 20]:
+        cl, chunk = sv.spec_verify_plan(V)
+        assert 1 <= cl <= 16 and chunk % 8 == 0
+        assert cl * chunk >= V and (cl - 1) * chunk < V, (V, cl, chunk)
+    assert sv.spec_verify_plan(128256) == (16, 8016)
+    assert sv.spec_verify_plan(151936) == (16, 9496)
+    with pytest.raises(sv.SpecVerifyError):
+        sv.spec_verify_plan(0)
