@@ -163,6 +163,18 @@ def all_reduce_max(x, world, device):
     return float(t.item())
 
 
+def shard_workload(config, rank):
+    """Weak scaling: sequences are independent, so every rank verifies its own batch of the
+    same shape (seeded by its rank); nothing is exchanged on the data path."""
+    from speculative_decoding_verification_34_gb300 import workloads as W
+    return W.WORKLOADS[config](seed=rank)
+
+
+def aggregate_rate(world, rows_per_step, steps, max_elapsed_ms):
+    """Whole-job rows/s: the rows all ranks verified over the slowest rank's time."""
+    return world * rows_per_step * steps / (max_elapsed_ms / 1e3)
+
+
 def cpu_oracle_rate(wl, seconds, seqs_cap=None):
     """Oracle throughput on a bounded sample of the same batch: rows/s, sequences used."""
     from oracle import specverify_oracle as O
@@ -250,7 +262,7 @@ def run_native(args):
         dist.barrier()
     sv.load_library()
 
-    wl = W.WORKLOADS[args.config](seed=rank)   # weak scaling: every rank verifies its own batch
+    wl = shard_workload(args.config, rank)
     B, g, V = wl.B, wl.gmax, wl.V
 
     def to_dev(a):
@@ -315,7 +327,7 @@ def run_native(args):
     kern_mean_ms = all_reduce_max(kern_mean_ms, world, device)
 
     rows_step = wl.verified_rows()
-    value = world * rows_step * K / (elapsed_ms / 1e3)
+    value = aggregate_rate(world, rows_step, K, elapsed_ms)
     abytes = wl.algorithmic_bytes()
     peak, peak_src = measured_peak()
     achieved = abytes / (kern_mean_ms / 1e3) / 1e9
@@ -353,7 +365,7 @@ def run_native(args):
     ee.record(stream)
     torch.cuda.synchronize(device)
     e2e_ms = all_reduce_max(es.elapsed_time(ee), world, device)
-    e2e_value = world * rows_step * args.e2e_steps / (e2e_ms / 1e3)
+    e2e_value = aggregate_rate(world, rows_step, args.e2e_steps, e2e_ms)
 
     cpu = None
     if rank == 0 and world == 1:

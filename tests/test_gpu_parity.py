@@ -25,12 +25,16 @@ def _lib():
     sv.load_library()
 
 
-def _check(wl, seqs=None, mode="auto", max_flag_frac=0.01, **kw):
+def _check(wl, seqs=None, mode="auto", max_differ_frac=0.01, **kw):
+    """Flagged sequences (an oracle decision within 1e-5 of its threshold) are counted and
+    reported; among them the GPU may legitimately take the other branch, which is bounded
+    here as a sanity check on the fp32 arithmetic (it is normally 0)."""
     gpu = parity.run_gpu(wl, mode=mode, **kw)
     res = parity.oracle_results(wl, seqs=seqs, mode=mode)
-    n, flagged = parity.compare(wl, gpu, res, seqs=seqs)
-    print(f"{wl.name}: {n} sequences checked, {len(flagged)} flagged within 1e-5 margin: {flagged[:10]}")
-    assert len(flagged) <= max(1, int(max_flag_frac * n))
+    n, flagged, differ = parity.compare(wl, gpu, res, seqs=seqs)
+    print(f"{wl.name}: {n} sequences checked, {len(flagged)} flagged within 1e-5 margin "
+          f"{flagged[:10]}, {len(differ)} of them differ {differ[:10]}")
+    assert len(differ) <= max(1, int(max_differ_frac * n))
     return gpu, res
 
 
@@ -50,7 +54,7 @@ def test_three_token_trials():
 
 def test_greedy_workload_both_entry_points():
     wl = W.greedy_32k(seed=0)
-    gpu, res = _check(wl, mode="greedy", max_flag_frac=0.0)
+    gpu, res = _check(wl, mode="greedy", max_differ_frac=0.0)
     # the same sequences through spec_verify_sample with temperature 0 give the same result
     wl2 = W.greedy_32k(seed=0)
     wl2.greedy_only = False
@@ -75,9 +79,9 @@ def test_large_batch_workload_sampled():
     seqs = sorted(set(range(0, 256, 16)) | set(rng.choice(wl.B, 48, replace=False).tolist()))
     gpu = parity.run_gpu(wl)
     res = parity.oracle_results(wl, seqs=seqs)
-    n, flagged = parity.compare(wl, gpu, res, seqs=seqs)
-    print(f"{wl.name}: {n} sampled sequences, {len(flagged)} flagged")
-    assert len(flagged) <= 1
+    n, flagged, differ = parity.compare(wl, gpu, res, seqs=seqs)
+    print(f"{wl.name}: {n} sampled sequences, {len(flagged)} flagged, {len(differ)} differ")
+    assert len(differ) <= 1
     eq = np.arange(wl.B) % 16 == 0
     # q == p: every draft kept (ratio exactly 1), the bonus drawn, no status bits
     assert (gpu["m"][eq] == 4).all() and (gpu["status"][eq] == 0).all()
@@ -145,7 +149,7 @@ def test_greedy_ties_resolve_to_lowest_id():
                     np.full(3, 3, np.int32), np.zeros(3, np.float32), np.zeros((3, 3), np.float32),
                     np.zeros(3, np.float32), np.zeros(3, np.int32), greedy_only=True)
     wl.draft_tokens[0] = [7 + chunk, chunk + 44, 16]
-    gpu, _ = _check(wl, mode="greedy", max_flag_frac=0.0)
+    gpu, _ = _check(wl, mode="greedy", max_differ_frac=0.0)
     assert list(gpu["out"][0]) == [7 + chunk, chunk + 44, 16, int(np.argmax(t32[0, 3]))]
 
 
