@@ -107,15 +107,25 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
   }
 }
 
-// Merge two (max, sum of 2^((x-max)k)) partials; (-inf, 0) is the empty partial.
+// Merge two (max, sum of 2^((x-max)k)) partials; (-inf, 0) is the empty partial.  Products
+// and sums are explicitly rounded (never contracted into FMAs) so that bit-identical target
+// and draft rows always give bit-identical statistics.
 __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2, float k) {
   const float M = fmaxf(m, m2);
   if (M == -INFINITY) return;
-  const float a = (m == -INFINITY) ? 0.f : s * ex2((m - M) * k);
-  const float b = (m2 == -INFINITY) ? 0.f : s2 * ex2((m2 - M) * k);
+  const float a = (m == -INFINITY) ? 0.f : __fmul_rn(s, ex2(__fmul_rn(m - M, k)));
+  const float b = (m2 == -INFINITY) ? 0.f : __fmul_rn(s2, ex2(__fmul_rn(m2 - M, k)));
   m = M;
-  s = a + b;
+  s = __fadd_rn(a, b);
 }
+
+// p_v = 2^((x_v - M) k) / S, evaluated as ex2(x*k - M*k) * (1/S) with a rounded product.
+__device__ __forceinline__ float prob(float x, float k, float mk, float inv_s) {
+  return __fmul_rn(ex2(fmaf(x, k, -mk)), inv_s);
+}
+
+// max(p - q, 0) with a rounded difference: exactly 0 wherever p == q.
+__device__ __forceinline__ float residual(float p, float q) { return fmaxf(__fsub_rn(p, q), 0.f); }
 
 // Element formats.  A 16-byte vector holds kPerVec elements; -inf fills vectors past the end.
 struct Bf16 {
@@ -181,7 +191,7 @@ __device__ __forceinline__ void tile_stats(const Tile<E, kVec>& t, float k, floa
   m = warp_max(m);
   float s = 0.f;
   if (m != -INFINITY) {
-    const float mk = m * k;
+    const float mk = __fmul_rn(m, k);
 #pragma unroll
     for (int a = 0; a < kVecPerPass; ++a)
 #pragma unroll
@@ -335,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Args a) {
       if (M != -INFINITY)
         for (int c = 0; c < CL; ++c) {
           const float2 p = sm.all[c][slot];
-          if (p.x != -INFINITY) S += p.y * ex2((p.x - M) * k);
+          if (p.x != -INFINITY) S = __fadd_rn(S, __fmul_rn(p.y, ex2(__fmul_rn(p.x - M, k))));
         }
       sm.rowM[slot] = M;
       sm.rowInvS[slot] = __frcp_rn(S);
@@ -363,11 +373,11 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Args a) {
         if (valid) {
           const float xp = E::at(P + int64_t(lane) * V, d);
           const float xq = E::at(Q + int64_t(lane) * V, d);
-          p = ex2(fmaf(xp, k, -(sm.rowM[lane] * k))) * sm.rowInvS[lane];
-          q = ex2(fmaf(xq, k, -(sm.rowM[kQSlot + lane] * k))) * sm.rowInvS[kQSlot + lane];
+          p = prob(xp, k, __fmul_rn(sm.rowM[lane], k), sm.rowInvS[lane]);
+          q = prob(xq, k, __fmul_rn(sm.rowM[kQSlot + lane], k), sm.rowInvS[kQSlot + lane]);
           const float u = a.u_accept[int64_t(b) * gmax + lane];
           // u < min(1, p/q): r = 0 when p = 0, r = +inf when q = 0 < p
-          acc = (p == 0.f) ? (u < 0.f) : (p >= q ? (u < 1.f) : (u * q < p));
+          acc = (p == 0.f) ? (u < 0.f) : (p >= q ? (u < 1.f) : (__fmul_rn(u, q) < p));
         }
         sm.pd[lane] = p;
         sm.qd[lane] = q;
@@ -412,8 +422,8 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Args a) {
   const bool pair = m < g;                 // rejection: residual of (p_m, q_m); else bonus p_g
   const raw* rp = P + int64_t(m) * V;
   const raw* rq = pair ? Q + int64_t(m) * V : nullptr;
-  const float mkp = sm.rowM[m] * k, invp = sm.rowInvS[m];
-  const float mkq = pair ? sm.rowM[kQSlot + m] * k : 0.f;
+  const float mkp = __fmul_rn(sm.rowM[m], k), invp = sm.rowInvS[m];
+  const float mkq = pair ? __fmul_rn(sm.rowM[kQSlot + m], k) : 0.f;
   const float invq = pair ? sm.rowInvS[kQSlot + m] : 0.f;
   float wsum = 0.f, psum = 0.f;
   for (int64_t e0 = lo; e0 < hi; e0 += kPass) {
@@ -424,9 +434,9 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Args a) {
     for (int x = 0; x < kVecPerPass; ++x)
 #pragma unroll
       for (int j = 0; j < E::kPerVec; ++j) {
-        const float p = ex2(fmaf(tp.x(x, j), k, -mkp)) * invp;
+        const float p = prob(tp.x(x, j), k, mkp, invp);
         psum += p;
-        if (pair) wsum += fmaxf(p - ex2(fmaf(tq.x(x, j), k, -mkq)) * invq, 0.f);
+        if (pair) wsum += residual(p, prob(tq.x(x, j), k, mkq, invq));
       }
   }
   if (!pair) wsum = psum;
@@ -481,9 +491,9 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Args a) {
   const int64_t s0 = lo + int64_t(tid) * seg;
   const int64_t s1 = (s0 + seg < hi) ? s0 + seg : hi;
   auto weight = [&](int64_t v) -> float {
-    const float p = ex2(fmaf(E::at(rp, v), k, -mkp)) * invp;
+    const float p = prob(E::at(rp, v), k, mkp, invp);
     if (draw_p) return p;
-    return fmaxf(p - ex2(fmaf(E::at(rq, v), k, -mkq)) * invq, 0.f);
+    return residual(p, prob(E::at(rq, v), k, mkq, invq));
   };
   float mysum = 0.f;
   int mylast = -1;
