@@ -77,6 +77,7 @@ extern "C" int spec_commit_kv_lengths(const int32_t* num_accepted, int B, int32_
     set_error("gmax=%d exceeds SPEC_MAX_GAMMA=%d", gmax, SPEC_MAX_GAMMA);
     return SPEC_ENOSPACE;
   }
+  if (B == 0) return SPEC_OK;   // empty batch: pointers may be null
   if (!num_accepted || !target_kv_len) {
     set_error("null required pointer (num_accepted or target_kv_len)");
     return SPEC_EINVAL;

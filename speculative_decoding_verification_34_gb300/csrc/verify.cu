@@ -626,6 +626,7 @@ int check_common(const void* target, int dtype, const int32_t* draft_tokens, int
     set_error("gmax=%d exceeds SPEC_MAX_GAMMA=%d", gmax, SPEC_MAX_GAMMA);
     return SPEC_ENOSPACE;
   }
+  if (B == 0) return SPEC_OK;   // empty batch: nothing is read or written, pointers may be null
   if (!target || !out_tokens || !num_accepted || (gmax > 0 && !draft_tokens)) {
     set_error("null required pointer");
     return SPEC_EINVAL;
@@ -682,7 +683,7 @@ extern "C" int spec_verify_sample(const void* target_logits, const void* draft_l
   clear_error();
   int rc = check_common(target_logits, dtype, draft_tokens, B, gmax, V, out_tokens, num_accepted);
   if (rc != SPEC_OK) return rc;
-  if (!temperature || !u_sample || (gmax > 0 && (!draft_logits || !u_accept))) {
+  if (B > 0 && (!temperature || !u_sample || (gmax > 0 && (!draft_logits || !u_accept)))) {
     set_error("null required pointer (draft_logits, temperature, u_accept or u_sample)");
     return SPEC_EINVAL;
   }

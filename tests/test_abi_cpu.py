@@ -72,6 +72,9 @@ def test_host_argument_checks(lib):
     assert c(None, 4, FAKE, None, 1, None, 3, None, None, 0, None, None) == 1
     assert c(FAKE, 4, FAKE, None, 1, None, 40, None, None, 0, None, None) == 3
     assert c(FAKE, 0, FAKE, None, 1, None, 3, None, None, 0, None, None) == 0
+    assert c(None, 0, None, None, 1, None, 3, None, None, 0, None, None) == 0
+    assert greedy(lib, target=None, toks=None, out=None, macc=None, B=0) == 0
+    assert sample(lib, target=None, draft=None, temp=None, ua=None, us=None, B=0) == 0
     assert lib.spec_launch_count() == n0      # nothing was launched
 
 
