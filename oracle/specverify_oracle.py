@@ -259,8 +259,9 @@ def commit_kv_lengths(kv_len: np.ndarray, m: np.ndarray, correction_processed: b
 
     Both caches are trimmed to t + m (the accepted prefix); once the correction or bonus
     token has been fed through both models they hold t + m + 1.  When a token history is
-    given, the m+1 emitted tokens are appended at committed_len; a sequence whose history
-    would overflow is left untouched and flagged (bit 8).
+    given, the m+1 emitted tokens are appended at committed_len; a sequence whose append
+    position is not legal (committed_len < 0, or the history would overflow) is left
+    untouched and flagged (bit 8).
     Returns (kv_len, draft_kv_len, history, committed_len, status) as new arrays.
     """
     kv = np.array(kv_len, dtype=np.int64)
@@ -273,7 +274,7 @@ def commit_kv_lengths(kv_len: np.ndarray, m: np.ndarray, correction_processed: b
         n = int(m[b]) + 1
         if hist is not None:
             cap = hist.shape[1]
-            if clen[b] + n > cap:
+            if clen[b] < 0 or clen[b] + n > cap:
                 status[b] |= ST_HISTORY_FULL
                 continue
             hist[b, clen[b]: clen[b] + n] = out_tokens[b, :n]

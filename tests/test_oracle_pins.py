@@ -145,6 +145,11 @@ def test_commit_kv_lengths():
     assert list(clen2) == [4, 1, 3] and list(st) == [0, 0, O.ST_HISTORY_FULL]
     assert list(hist2[0]) == [-1, 5, 6, 9, -1, -1] and list(hist2[1]) == [4, -1, -1, -1, -1, -1]
     assert list(kv) == [103, 8, 0]          # the overflowing sequence is left untouched
+    # a negative committed length is not a legal append position either
+    kv, _, hist3, clen3, st = O.commit_kv_lengths(t, m, True, out_tokens=out, history=hist,
+                                                  committed_len=np.array([-1, 0, 0]))
+    assert list(st) == [O.ST_HISTORY_FULL, 0, 0] and list(kv) == [100, 8, 5]
+    assert list(clen3) == [-1, 1, 5] and (hist3[0] == -1).all()
 
 
 def test_greedy_workload_closed_form():
