@@ -136,14 +136,26 @@ def spec_verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor,
         _ptr(status, "status", torch.int32, (B,)), _stream(stream)))
 
 
+def _commit_gmax(out_tokens, gmax):
+    if out_tokens is not None:
+        g = out_tokens.shape[1] - 1
+        if gmax is not None and gmax != g:
+            raise ValueError(f"gmax={gmax} disagrees with out_tokens width {g + 1}")
+        return g
+    if gmax is None:
+        raise ValueError("gmax is required when out_tokens is not given")
+    return int(gmax)
+
+
 def spec_commit_kv_lengths(num_accepted: torch.Tensor, target_kv_len: torch.Tensor,
                            draft_kv_len: Optional[torch.Tensor], correction_processed: bool,
                            out_tokens: Optional[torch.Tensor] = None,
                            history: Optional[torch.Tensor] = None,
                            committed_len: Optional[torch.Tensor] = None,
-                           status: Optional[torch.Tensor] = None, stream=None) -> None:
+                           status: Optional[torch.Tensor] = None, stream=None,
+                           gmax: Optional[int] = None) -> None:
     B = num_accepted.shape[0]
-    gmax = out_tokens.shape[1] - 1 if out_tokens is not None else 0
+    gmax = _commit_gmax(out_tokens, gmax)
     cap = history.shape[1] if history is not None else 0
     lib = load_library()
     _check(lib.spec_commit_kv_lengths(
@@ -202,9 +214,9 @@ def prepare_verify_sample(target_logits, draft_logits, draft_tokens, num_draft, 
 
 def prepare_commit_kv_lengths(num_accepted, target_kv_len, draft_kv_len, correction_processed,
                               out_tokens=None, history=None, committed_len=None, status=None,
-                              stream=None) -> _Prepared:
+                              stream=None, gmax=None) -> _Prepared:
     B = num_accepted.shape[0]
-    gmax = out_tokens.shape[1] - 1 if out_tokens is not None else 0
+    gmax = _commit_gmax(out_tokens, gmax)
     cap = history.shape[1] if history is not None else 0
     lib = load_library()
     args = (_ptr(num_accepted, "num_accepted", torch.int32, (B,)), B,

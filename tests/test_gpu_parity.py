@@ -241,7 +241,7 @@ def test_commit_kv_lengths_matches_oracle():
         assert np.array_equal(S_.cpu().numpy(), st)
     # lengths only
     T_ = dev(t)
-    sv.spec_commit_kv_lengths(dev(m), T_, None, True)
+    sv.spec_commit_kv_lengths(dev(m), T_, None, True, gmax=g)
     torch.cuda.synchronize()
     assert np.array_equal(T_.cpu().numpy(), t + np.clip(m, 0, g) + 1)
 
