@@ -6,23 +6,28 @@
 // R = 0 remark).  How it is computed is this library's own design for sm_103a:
 //
 //   * Cluster of C blocks per sequence b (C <= 16); block c owns the vocabulary chunk
-//     [c*chunk, (c+1)*chunk) of every row of b.  Phase A streams the chunk of every row the
-//     sequence needs once from HBM (128-bit loads, one exp2 per sampled element) and reduces
-//     it to a (max, sum-of-exp) pair, or to an (argmax value, id) pair for greedy rows.
-//   * Each block pushes its per-row partials into every block's shared memory (distributed
-//     shared memory); after one cluster barrier every block holds all C partials and derives
-//     the same row maxima/normalisers, the same acceptance flags and the same m.
-//   * Phase B (sampling only): each block re-reads its chunk of the one row (pair) the final
-//     draw needs -- row m of p and q after a rejection, the bonus row otherwise, normally
-//     still in L2 -- and reduces the residual mass max(p-q,0) (and the p mass for the R = 0
-//     fallback).  A second push + barrier gives every block all C chunk masses; the block
-//     whose chunk holds u*R runs an in-chunk prefix scan to find the token and writes the
-//     outputs.
+//     [c*chunk, (c+1)*chunk) of every row of b.
+//   * Phase A streams the chunk of every row the sequence needs exactly once from HBM.  Each
+//     thread keeps its own 16-byte vectors in flight through a kStages-deep ring in shared
+//     memory (cp.async, one commit group per tile), so loads of the next tiles overlap the
+//     arithmetic on the current one.  A tile reduces to a (max, sum 2^((x-max)k)) pair with one
+//     ex2 per element (bf16x2 max, f32x2 FMA/ADD), or to (max, lowest id) for greedy rows.
+//   * Exchange 1: every block pushes its per-row partials into every block's shared memory
+//     (distributed shared memory); after one cluster barrier all blocks derive, in the same
+//     order, the same row maxima/normalisers, acceptance flags and m.
+//   * Phase B (sampling only): every block re-reads its chunk of the row (pair) the last token
+//     is drawn from -- row m of p and q after a rejection, the bonus row otherwise; normally an
+//     L2 hit -- keeping one partial sum per (pass, vector slot, thread) in shared memory, and
+//     pushes its chunk mass (exchange 2, second cluster barrier).
+//   * The block whose chunk holds u*R finds the token from its per-vector sums (warp scans,
+//     one vector reloaded) and writes the outputs.
 //
-// No global workspace, no atomics, no spin-waits: the only cross-block synchronisation is
-// the hardware cluster barrier, reached by every block of a cluster the same number of times.
+// No global workspace, no atomics on global memory, no spin-waits: the only cross-block
+// synchronisation is the hardware cluster barrier, which every block of a cluster reaches the
+// same number of times.  cp.async groups are waited per thread (the thread's own copies).
 
 #include <cooperative_groups.h>
+#include <cuda_bf16.h>
 
 #include <climits>
 #include <cmath>
@@ -38,9 +43,11 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCluster = 16;
-constexpr int kQSlot = SPEC_MAX_GAMMA + 1;        // row slot of draft row i is kQSlot + i
-constexpr int kSlots = kQSlot + SPEC_MAX_GAMMA;   // target rows 0..gmax, draft rows 0..gmax-1
-constexpr int kVecPerPass = 4;                    // 16-byte vectors per thread per row per pass
+constexpr int kVecPerPass = 4;                         // 16-byte vectors per thread per tile
+constexpr int kStages = 3;                             // cp.async ring depth (tiles)
+constexpr int kTileBytes = kThreads * kVecPerPass * 16;
+constexpr int kMaxSlices = 64;                         // (pass, vector slot) pairs per chunk
+constexpr int kMaxDynSmem = 160 * 1024;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -71,12 +78,53 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Streaming 128-bit read-only load that does not allocate in L1.
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
+// Packed pairs of f32 (sm_100+ f32x2 arithmetic), all round-to-nearest, never contracted.
+using f2 = unsigned long long;
+__device__ __forceinline__ f2 pk(float a, float b) {
+  f2 r;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 upk(f2 r) {
+  float2 v;
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+  f2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+  f2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+  f2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2 ex2x2(f2 a) {
+  const float2 v = upk(a);
+  return pk(ex2(v.x), ex2(v.y));
+}
+
+// 16-byte global -> shared copy that bypasses L1; src_bytes = 0 zero-fills without reading.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_l2(const void* p) {
   uint4 v;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-      : "l"(p));
+  asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
 }
 
@@ -89,7 +137,7 @@ __device__ __forceinline__ float warp_max(float v) {
 // Tree sum into lane 0, then broadcast: every lane gets the same bits.
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(kFull, v, o);
+  for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_down_sync(kFull, v, o));
   return __shfl_sync(kFull, v, 0);
 }
 
@@ -108,8 +156,7 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
 }
 
 // Merge two (max, sum of 2^((x-max)k)) partials; (-inf, 0) is the empty partial.  Products
-// and sums are explicitly rounded (never contracted into FMAs) so that bit-identical target
-// and draft rows always give bit-identical statistics.
+// and sums are explicitly rounded so bit-identical rows always give bit-identical statistics.
 __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2, float k) {
   const float M = fmaxf(m, m2);
   if (M == -INFINITY) return;
@@ -120,25 +167,37 @@ __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2,
 }
 
 // p_v = 2^((x_v - M) k) / S, evaluated as ex2(x*k - M*k) * (1/S) with a rounded product.
+// prob() and prob2() give identical bits for the same element.
 __device__ __forceinline__ float prob(float x, float k, float mk, float inv_s) {
   return __fmul_rn(ex2(fmaf(x, k, -mk)), inv_s);
 }
+__device__ __forceinline__ f2 prob2(f2 x, f2 k2, f2 nmk2, f2 inv2) { return mul2(ex2x2(fma2(x, k2, nmk2)), inv2); }
 
 // max(p - q, 0) with a rounded difference: exactly 0 wherever p == q.
 __device__ __forceinline__ float residual(float p, float q) { return fmaxf(__fsub_rn(p, q), 0.f); }
 
-// Element formats.  A 16-byte vector holds kPerVec elements; -inf fills vectors past the end.
+// Element formats.  A 16-byte vector holds kPerVec elements.
 struct Bf16 {
   using raw = uint16_t;
   static constexpr int kPerVec = 8;
-  static constexpr uint32_t kNegInfPair = 0xff80ff80u;
   __device__ __forceinline__ static float at(const raw* row, int64_t i) {
     return __uint_as_float(uint32_t(__ldg(row + i)) << 16);
   }
-  __device__ __forceinline__ static uint4 neg_inf() { return make_uint4(kNegInfPair, kNegInfPair, kNegInfPair, kNegInfPair); }
+  // element pair j (0..3) of a vector, widened to f32x2 (lower id first)
+  __device__ __forceinline__ static f2 pair(const uint4& v, int j) {
+    const uint32_t w = j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+    return pk(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  }
   __device__ __forceinline__ static float get(const uint4& v, int j) {
     const uint32_t w = (j >> 1) == 0 ? v.x : (j >> 1) == 1 ? v.y : (j >> 1) == 2 ? v.z : v.w;
     return __uint_as_float((j & 1) ? (w & 0xffff0000u) : (w << 16));
+  }
+  __device__ __forceinline__ static float vmax(const uint4& v) {
+    __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
+    a = __hmax2(a, *reinterpret_cast<const __nv_bfloat162*>(&v.y));
+    a = __hmax2(a, *reinterpret_cast<const __nv_bfloat162*>(&v.z));
+    a = __hmax2(a, *reinterpret_cast<const __nv_bfloat162*>(&v.w));
+    return fmaxf(__low2float(a), __high2float(a));
   }
 };
 
@@ -146,56 +205,65 @@ struct F32 {
   using raw = float;
   static constexpr int kPerVec = 4;
   __device__ __forceinline__ static float at(const raw* row, int64_t i) { return __ldg(row + i); }
-  __device__ __forceinline__ static uint4 neg_inf() {
-    const uint32_t n = 0xff800000u;
-    return make_uint4(n, n, n, n);
+  __device__ __forceinline__ static f2 pair(const uint4& v, int j) {
+    return j == 0 ? pk(__uint_as_float(v.x), __uint_as_float(v.y)) : pk(__uint_as_float(v.z), __uint_as_float(v.w));
   }
   __device__ __forceinline__ static float get(const uint4& v, int j) {
     return __uint_as_float(j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w);
   }
+  __device__ __forceinline__ static float vmax(const uint4& v) {
+    return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)), fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+  }
 };
 
-// One pass of one row: kVecPerPass vectors per thread, vector k of thread t at element
-// e0 + (k*kThreads + t)*kPerVec (coalesced across the block for every k).
+// A tile is one pass of one row: vector k of thread t covers elements
+// e0 + (k*kThreads + t)*kPerVec .. +kPerVec-1 (coalesced across the block for every k).
+// Vector path: the vectors come from the shared-memory ring.  Scalar path (unaligned rows):
+// elements are loaded one by one.  Out-of-range elements read as -inf.
 template <class E, bool kVec>
 struct Tile {
+  static constexpr int N = E::kPerVec;
   uint4 v[kVecPerPass];
-  float s[kVec ? 1 : kVecPerPass * E::kPerVec];
+  bool ok[kVecPerPass];
+  float s[kVec ? 1 : kVecPerPass * N];
 
-  __device__ __forceinline__ void load(const typename E::raw* row, int64_t e0, int64_t hi, int tid) {
-#pragma unroll
-    for (int k = 0; k < kVecPerPass; ++k) {
-      const int64_t e = e0 + int64_t(k * kThreads + tid) * E::kPerVec;
-      if constexpr (kVec) {
-        v[k] = e < hi ? ld_stream(row + e) : E::neg_inf();
-      } else {
-#pragma unroll
-        for (int j = 0; j < E::kPerVec; ++j)
-          s[k * E::kPerVec + j] = (e + j < hi) ? E::at(row, e + j) : -INFINITY;
-      }
-    }
-  }
   __device__ __forceinline__ float x(int k, int j) const {
-    if constexpr (kVec) return E::get(v[k], j);
-    else return s[k * E::kPerVec + j];
+    if constexpr (kVec) return ok[k] ? E::get(v[k], j) : -INFINITY;
+    else return s[k * N + j];
   }
 };
 
 template <class E, bool kVec>
 __device__ __forceinline__ void tile_stats(const Tile<E, kVec>& t, float k, float& run_m, float& run_s) {
+  constexpr int N = E::kPerVec;
   float m = -INFINITY;
+  if constexpr (kVec) {
 #pragma unroll
-  for (int a = 0; a < kVecPerPass; ++a)
+    for (int a = 0; a < kVecPerPass; ++a)
+      if (t.ok[a]) m = fmaxf(m, E::vmax(t.v[a]));
+  } else {
 #pragma unroll
-    for (int j = 0; j < E::kPerVec; ++j) m = fmaxf(m, t.x(a, j));
+    for (int a = 0; a < kVecPerPass * N; ++a) m = fmaxf(m, t.s[a]);
+  }
   m = warp_max(m);
   float s = 0.f;
   if (m != -INFINITY) {
     const float mk = __fmul_rn(m, k);
+    if constexpr (kVec) {
+      const f2 k2 = pk(k, k), nmk2 = pk(-mk, -mk);
+      f2 acc = pk(0.f, 0.f);
 #pragma unroll
-    for (int a = 0; a < kVecPerPass; ++a)
+      for (int a = 0; a < kVecPerPass; ++a)
+        if (t.ok[a]) {
 #pragma unroll
-      for (int j = 0; j < E::kPerVec; ++j) s += ex2(fmaf(t.x(a, j), k, -mk));
+          for (int j = 0; j < N / 2; ++j) acc = add2(acc, ex2x2(fma2(E::pair(t.v[a], j), k2, nmk2)));
+        }
+      const float2 r = upk(acc);
+      s = __fadd_rn(r.x, r.y);
+    } else {
+#pragma unroll
+      for (int a = 0; a < kVecPerPass * N; ++a) s = __fadd_rn(s, ex2(fmaf(t.s[a], k, -mk)));
+    }
   }
   s = warp_sum(s);
   merge_ms(run_m, run_s, m, s, k);
@@ -213,20 +281,44 @@ __device__ __forceinline__ void tile_argmax(const Tile<E, kVec>& t, int64_t e0, 
     }
 }
 
-struct Shared {
-  float2 warp_part[kWarps][kSlots];   // per-warp partial of each row slot (this block)
-  float2 local[kSlots];               // this block's chunk partial per row slot
-  float2 all[kMaxCluster][kSlots];    // every block's chunk partials, pushed by their owners
+// Statically sized shared state.
+struct Fixed {
   float2 mass_warp[kWarps];
   float2 all_mass[kMaxCluster];       // (weight mass, p mass) of every block's chunk
-  float rowM[kSlots];                 // row max of the logits
-  float rowInvS[kSlots];              // 1 / sum_v 2^((x_v - M) k)
-  int rowArg[kSlots];                 // greedy argmax per target row
   float pd[SPEC_MAX_GAMMA], qd[SPEC_MAX_GAMMA];
-  float scan_warp[kWarps];
-  int m, g, flags, owner, cand, lastpos, token;
-  float target_local, mass_out;
+  float wsum[kMaxSlices][kWarps];     // owner: per-(slice, warp) weight sums
+  int m, flags, owner, token, slice, warp_sel;
+  float target_local, mass_out, run_sel;
 };
+
+// Dynamic shared memory, sized per launch (byte offsets).
+struct Layout {
+  int ring, vsw, vsp, all, wpart, local, rowM, rowInvS, rowArg, total;
+};
+
+__host__ __device__ inline Layout make_layout(int nslots, int cl, int slices) {
+  Layout L;
+  int off = 0;
+  L.ring = off;
+  L.vsw = off;                                          // phase B reuses the ring's space
+  L.vsp = off + slices * kThreads * 4;
+  const int need_a = kStages * kTileBytes, need_b = 2 * slices * kThreads * 4;
+  off += need_a > need_b ? need_a : need_b;
+  L.all = off;
+  off += cl * nslots * 8;
+  L.wpart = off;
+  off += kWarps * nslots * 8;
+  L.local = off;
+  off += nslots * 8;
+  L.rowM = off;
+  off += nslots * 4;
+  L.rowInvS = off;
+  off += nslots * 4;
+  L.rowArg = off;
+  off += nslots * 4;
+  L.total = (off + 15) & ~15;
+  return L;
+}
 
 // ------------------------------------------------------------------------------------------
 // the kernel
@@ -235,7 +327,10 @@ struct Shared {
 template <class E, bool kVec, bool kMixed>
 __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Args a) {
   using raw = typename E::raw;
-  __shared__ Shared sm;
+  constexpr int N = E::kPerVec;
+  constexpr int kPass = kThreads * kVecPerPass * N;     // elements per tile
+  extern __shared__ __align__(16) unsigned char dyn[];
+  __shared__ Fixed fx;
   cg::cluster_group cluster = cg::this_cluster();
   const int CL = int(cluster.num_blocks());
   const int rank = int(cluster.block_rank());
@@ -248,6 +343,8 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Args a) {
 
   const int64_t V = a.V;
   const int gmax = a.gmax;
+  const int nslots = 2 * gmax + 1;                      // target rows 0..gmax, draft rows after
+  const int qslot = gmax + 1;
   int g = a.num_draft ? a.num_draft[b] : gmax;
   int flags = 0;
   if (g < 0 || g > gmax) {
@@ -263,156 +360,222 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Args a) {
   const raw* Q = sampling ? static_cast<const raw*>(a.draft) + int64_t(b) * gmax * V : nullptr;
   const int64_t lo = int64_t(rank) * a.chunk;
   const int64_t hi = lo + a.chunk < V ? lo + a.chunk : V;
-  constexpr int kPass = kThreads * kVecPerPass * E::kPerVec;
+  const int npass = hi > lo ? int((hi - lo + kPass - 1) / kPass) : 0;
+  const int slices = npass * kVecPerPass;
+  // the layout must be identical in every block of the cluster (blocks write into each
+  // other's shared memory), so it is sized by the full chunk, not by this block's share
+  const int slices_max = int((a.chunk + kPass - 1) / kPass) * kVecPerPass;
+  const Layout L = make_layout(nslots, CL, slices_max);
+  float2* all = reinterpret_cast<float2*>(dyn + L.all);
+  float2* wpart = reinterpret_cast<float2*>(dyn + L.wpart);
+  float2* local = reinterpret_cast<float2*>(dyn + L.local);
+  float* rowM = reinterpret_cast<float*>(dyn + L.rowM);
+  float* rowInvS = reinterpret_cast<float*>(dyn + L.rowInvS);
+  int* rowArg = reinterpret_cast<int*>(dyn + L.rowArg);
+
+  // Prefetch what the decision needs (draft ids, their logits, uniforms): lane i of warp 0
+  // owns draft i; the loads complete while phase A streams.
+  int d = -1;
+  bool dvalid = false;
+  float xp = 0.f, xq = 0.f, ua = 0.f;
+  if (warp == 0 && lane < g) {
+    d = a.draft_tokens[int64_t(b) * gmax + lane];
+    dvalid = d >= 0 && int64_t(d) < V;
+    if (sampling) {
+      if (dvalid) {
+        xp = E::at(P + int64_t(lane) * V, d);
+        xq = E::at(Q + int64_t(lane) * V, d);
+      }
+      ua = a.u_accept[int64_t(b) * gmax + lane];
+    }
+  }
 
   // ---------------- phase A: one streaming pass over this block's chunk of every row -----
-  if (sampling) {
-    // bonus row alone, then (target_i, draft_i) pairs from i = g-1 down to 0 so that the
-    // rows a rejection most often needs (small m) are the most recently read.
-    for (int i = g; i >= 0; --i) {
-      const raw* rp = P + int64_t(i) * V;
-      const raw* rq = (i < g) ? Q + int64_t(i) * V : nullptr;
-      float pm = -INFINITY, ps = 0.f, qm = -INFINITY, qs = 0.f;
-      for (int64_t e0 = lo; e0 < hi; e0 += kPass) {
-        Tile<E, kVec> tp, tq;
-        tp.load(rp, e0, hi, tid);
-        if (rq) tq.load(rq, e0, hi, tid);
-        tile_stats(tp, k, pm, ps);
-        if (rq) tile_stats(tq, k, qm, qs);
+  // Row order: sampling [P_g, Q_{g-1}, P_{g-1}, ..., Q_0, P_0] (the rows a rejection most
+  // often needs -- small m -- are read last); greedy [P_g, ..., P_0].
+  const int nrows = sampling ? 2 * g + 1 : g + 1;
+  auto row_of = [&](int r, int& slot) -> const raw* {
+    if (!sampling || r == 0) {
+      const int i = g - r;
+      slot = i;
+      return P + int64_t(i) * V;
+    }
+    const int i = g - 1 - ((r - 1) >> 1);
+    if (r & 1) {
+      slot = qslot + i;
+      return Q + int64_t(i) * V;
+    }
+    slot = i;
+    return P + int64_t(i) * V;
+  };
+  const int ntiles = nrows * npass;
+  unsigned char* ring = dyn + L.ring;
+  auto issue = [&](int t) {
+    if constexpr (kVec) {
+      if (t < ntiles) {
+        const int r = t / npass, ps = t - r * npass;
+        int slot;
+        const raw* row = row_of(r, slot);
+        const int64_t e0 = lo + int64_t(ps) * kPass;
+        unsigned char* st = ring + (t % kStages) * kTileBytes;
+#pragma unroll
+        for (int q = 0; q < kVecPerPass; ++q) {
+          const int64_t e = e0 + int64_t(q * kThreads + tid) * N;
+          const bool in = e < hi;
+          cp_async16(st + (q * kThreads + tid) * 16,
+                     in ? static_cast<const void*>(row + e) : static_cast<const void*>(row), in ? 16 : 0);
+        }
       }
-      if (lane == 0) {
-        sm.warp_part[warp][i] = make_float2(pm, ps);
-        if (rq) sm.warp_part[warp][kQSlot + i] = make_float2(qm, qs);
+      cp_async_commit();
+    }
+  };
+  if constexpr (kVec) {
+#pragma unroll
+    for (int t = 0; t < kStages - 1; ++t) issue(t);
+  }
+  float rm = -INFINITY, rs = 0.f;   // running (max, sum) of a sampled row / argmax value
+  int ri = INT_MAX;                 // running argmax id of a greedy row
+  for (int t = 0; t < ntiles; ++t) {
+    const int r = t / npass, ps = t - r * npass;
+    int slot;
+    const raw* row = row_of(r, slot);
+    const int64_t e0 = lo + int64_t(ps) * kPass;
+    Tile<E, kVec> tile;
+    if constexpr (kVec) {
+      issue(t + kStages - 1);
+      cp_async_wait<kStages - 1>();
+      const unsigned char* st = ring + (t % kStages) * kTileBytes;
+#pragma unroll
+      for (int q = 0; q < kVecPerPass; ++q) {
+        tile.v[q] = *reinterpret_cast<const uint4*>(st + (q * kThreads + tid) * 16);
+        tile.ok[q] = e0 + int64_t(q * kThreads + tid) * N < hi;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < kVecPerPass; ++q) {
+        const int64_t e = e0 + int64_t(q * kThreads + tid) * N;
+#pragma unroll
+        for (int j = 0; j < N; ++j) tile.s[q * N + j] = (e + j < hi) ? E::at(row, e + j) : -INFINITY;
       }
     }
-  } else {
-    for (int i = g; i >= 0; i -= 2) {
-      const raw* r0 = P + int64_t(i) * V;
-      const raw* r1 = (i >= 1) ? P + int64_t(i - 1) * V : nullptr;
-      float v0 = -INFINITY, v1 = -INFINITY;
-      int i0 = INT_MAX, i1 = INT_MAX;
-      for (int64_t e0 = lo; e0 < hi; e0 += kPass) {
-        Tile<E, kVec> t0, t1;
-        t0.load(r0, e0, hi, tid);
-        if (r1) t1.load(r1, e0, hi, tid);
-        tile_argmax(t0, e0, tid, v0, i0);
-        if (r1) tile_argmax(t1, e0, tid, v1, i1);
-      }
-      warp_argmax(v0, i0);
-      if (r1) warp_argmax(v1, i1);
-      if (lane == 0) {
-        sm.warp_part[warp][i] = make_float2(v0, __int_as_float(i0));
-        if (r1) sm.warp_part[warp][i - 1] = make_float2(v1, __int_as_float(i1));
-      }
+    if (sampling) tile_stats(tile, k, rm, rs);
+    else tile_argmax(tile, e0, tid, rm, ri);
+    if (ps == npass - 1) {
+      if (!sampling) warp_argmax(rm, ri);
+      if (lane == 0) wpart[warp * nslots + slot] = make_float2(rm, sampling ? rs : __int_as_float(ri));
+      rm = -INFINITY;
+      rs = 0.f;
+      ri = INT_MAX;
+    }
+  }
+  if constexpr (kVec) cp_async_wait<0>();
+  if (npass == 0 && lane == 0) {
+    // empty chunk: empty partials
+    for (int r = 0; r < nrows; ++r) {
+      int slot;
+      row_of(r, slot);
+      wpart[warp * nslots + slot] = make_float2(-INFINITY, sampling ? 0.f : __int_as_float(INT_MAX));
     }
   }
   __syncthreads();
 
-  // block partial per row slot, warps merged in a fixed order
-  const int nP = g + 1, nQ = sampling ? g : 0, nSlots = nP + nQ;
-  for (int r = tid; r < nSlots; r += kThreads) {
-    const int slot = r < nP ? r : kQSlot + (r - nP);
-    float2 acc = sm.warp_part[0][slot];
+  // block partial per row, warps merged in a fixed order
+  for (int r = tid; r < nrows; r += kThreads) {
+    int slot;
+    row_of(r, slot);
+    float2 acc = wpart[slot];
     for (int w = 1; w < kWarps; ++w) {
-      const float2 p = sm.warp_part[w][slot];
-      if (sampling) {
-        merge_ms(acc.x, acc.y, p.x, p.y, k);
-      } else if (better(p.x, __float_as_int(p.y), acc.x, __float_as_int(acc.y))) {
-        acc = p;
-      }
+      const float2 p = wpart[w * nslots + slot];
+      if (sampling) merge_ms(acc.x, acc.y, p.x, p.y, k);
+      else if (better(p.x, __float_as_int(p.y), acc.x, __float_as_int(acc.y))) acc = p;
     }
-    sm.local[slot] = acc;
+    local[slot] = acc;
   }
   __syncthreads();
 
   // ---------------- exchange 1: push the partials into every block of the cluster --------
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-  for (int idx = tid; idx < CL * nSlots; idx += kThreads) {
-    const int c = idx / nSlots, r = idx - c * nSlots;
-    const int slot = r < nP ? r : kQSlot + (r - nP);
-    float2* dst = cluster.map_shared_rank(&sm.all[rank][slot], c);
-    *dst = sm.local[slot];
+  for (int idx = tid; idx < CL * nrows; idx += kThreads) {
+    const int c = idx / nrows, r = idx - c * nrows;
+    int slot;
+    row_of(r, slot);
+    float2* dst = cluster.map_shared_rank(&all[rank * nslots + slot], c);
+    *dst = local[slot];
   }
   cluster.sync();
 
   // every block combines the C partials of each row in the same order -> identical results
-  for (int r = tid; r < nSlots; r += kThreads) {
-    const int slot = r < nP ? r : kQSlot + (r - nP);
+  for (int r = tid; r < nrows; r += kThreads) {
+    int slot;
+    row_of(r, slot);
     if (sampling) {
       float M = -INFINITY;
-      for (int c = 0; c < CL; ++c) M = fmaxf(M, sm.all[c][slot].x);
+      for (int c = 0; c < CL; ++c) M = fmaxf(M, all[c * nslots + slot].x);
       float S = 0.f;
       if (M != -INFINITY)
         for (int c = 0; c < CL; ++c) {
-          const float2 p = sm.all[c][slot];
+          const float2 p = all[c * nslots + slot];
           if (p.x != -INFINITY) S = __fadd_rn(S, __fmul_rn(p.y, ex2(__fmul_rn(p.x - M, k))));
         }
-      sm.rowM[slot] = M;
-      sm.rowInvS[slot] = __frcp_rn(S);
+      rowM[slot] = M;
+      rowInvS[slot] = __frcp_rn(S);
     } else {
       float bv = -INFINITY;
       int bi = INT_MAX;
       for (int c = 0; c < CL; ++c) {
-        const float2 p = sm.all[c][slot];
+        const float2 p = all[c * nslots + slot];
         if (better(p.x, __float_as_int(p.y), bv, bi)) { bv = p.x; bi = __float_as_int(p.y); }
       }
-      sm.rowArg[slot] = bi;
+      rowArg[slot] = bi;
     }
   }
   __syncthreads();
 
   // ---------------- acceptance flags and the first rejection (warp 0) -----------------------
   if (warp == 0) {
-    bool acc = false, valid = false;
-    int d = -1;
+    bool acc = false;
     if (lane < g) {
-      d = a.draft_tokens[int64_t(b) * gmax + lane];
-      valid = d >= 0 && int64_t(d) < V;
       if (sampling) {
         float p = NAN, q = NAN;
-        if (valid) {
-          const float xp = E::at(P + int64_t(lane) * V, d);
-          const float xq = E::at(Q + int64_t(lane) * V, d);
-          p = prob(xp, k, __fmul_rn(sm.rowM[lane], k), sm.rowInvS[lane]);
-          q = prob(xq, k, __fmul_rn(sm.rowM[kQSlot + lane], k), sm.rowInvS[kQSlot + lane]);
-          const float u = a.u_accept[int64_t(b) * gmax + lane];
+        if (dvalid) {
+          p = prob(xp, k, __fmul_rn(rowM[lane], k), rowInvS[lane]);
+          q = prob(xq, k, __fmul_rn(rowM[qslot + lane], k), rowInvS[qslot + lane]);
           // u < min(1, p/q): r = 0 when p = 0, r = +inf when q = 0 < p
-          acc = (p == 0.f) ? (u < 0.f) : (p >= q ? (u < 1.f) : (__fmul_rn(u, q) < p));
+          acc = (p == 0.f) ? (ua < 0.f) : (p >= q ? (ua < 1.f) : (__fmul_rn(ua, q) < p));
         }
-        sm.pd[lane] = p;
-        sm.qd[lane] = q;
+        fx.pd[lane] = p;
+        fx.qd[lane] = q;
       } else {
-        acc = valid && d == sm.rowArg[lane];
+        acc = dvalid && d == rowArg[lane];
       }
     }
     const unsigned keep = __ballot_sync(kFull, acc);
     const unsigned rej = ~keep & (g >= 32 ? kFull : ((1u << g) - 1u));
     const int m = rej ? __ffs(rej) - 1 : g;
-    const unsigned badmask = __ballot_sync(kFull, lane < g && !valid);
+    const unsigned badmask = __ballot_sync(kFull, lane < g && !dvalid);
     if (lane == 0) {
       int f = flags;
       if (m < g && ((badmask >> m) & 1u)) f |= SPEC_ST_BAD_DRAFT;
-      sm.m = m;
-      sm.g = g;
-      sm.flags = f;
+      fx.m = m;
+      fx.flags = f;
     }
   }
   __syncthreads();
-  const int m = sm.m;
+  const int m = fx.m;
 
   if (!sampling) {
     if (rank == 0) {
       for (int i = tid; i <= gmax; i += kThreads) {
         int v = -1;
         if (i < m) v = a.draft_tokens[int64_t(b) * gmax + i];
-        else if (i == m) v = sm.rowArg[m];
+        else if (i == m) v = rowArg[m];
         a.out_tokens[int64_t(b) * (gmax + 1) + i] = v;
       }
       if (a.diag)
         for (int i = tid; i < 2 * gmax + 1; i += kThreads) a.diag[int64_t(b) * (2 * gmax + 1) + i] = NAN;
       if (tid == 0) {
         a.num_accepted[b] = m;
-        if (a.status) a.status[b] = sm.flags;
+        if (a.status) a.status[b] = fx.flags;
       }
     }
     return;
@@ -422,32 +585,84 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Args a) {
   const bool pair = m < g;                 // rejection: residual of (p_m, q_m); else bonus p_g
   const raw* rp = P + int64_t(m) * V;
   const raw* rq = pair ? Q + int64_t(m) * V : nullptr;
-  const float mkp = __fmul_rn(sm.rowM[m], k), invp = sm.rowInvS[m];
-  const float mkq = pair ? __fmul_rn(sm.rowM[kQSlot + m], k) : 0.f;
-  const float invq = pair ? sm.rowInvS[kQSlot + m] : 0.f;
-  float wsum = 0.f, psum = 0.f;
-  for (int64_t e0 = lo; e0 < hi; e0 += kPass) {
-    Tile<E, kVec> tp, tq;
-    tp.load(rp, e0, hi, tid);
-    if (pair) tq.load(rq, e0, hi, tid);
+  const float mkp = __fmul_rn(rowM[m], k), invp = rowInvS[m];
+  const float mkq = pair ? __fmul_rn(rowM[qslot + m], k) : 0.f;
+  const float invq = pair ? rowInvS[qslot + m] : 0.f;
+  float* vsw = reinterpret_cast<float*>(dyn + L.vsw);   // per (slice, thread) weight sums
+  float* vsp = reinterpret_cast<float*>(dyn + L.vsp);   // per (slice, thread) p sums
+  // weights w (residual, or p on the bonus row) and p of one vector; elements past hi are 0
+  auto vec_weights = [&](int64_t e, float (&w)[N], float (&p)[N]) {
+    if constexpr (kVec) {
+      if (e < hi) {
+        const uint4 vp = ld_l2(rp + e);
+        const f2 k2 = pk(k, k), nmkp = pk(-mkp, -mkp), ip = pk(invp, invp);
+        if (pair) {
+          const uint4 vq = ld_l2(rq + e);
+          const f2 nmkq = pk(-mkq, -mkq), iq = pk(invq, invq);
 #pragma unroll
-    for (int x = 0; x < kVecPerPass; ++x)
+          for (int j = 0; j < N / 2; ++j) {
+            const float2 pp = upk(prob2(E::pair(vp, j), k2, nmkp, ip));
+            const float2 qq = upk(prob2(E::pair(vq, j), k2, nmkq, iq));
+            p[2 * j] = pp.x;
+            p[2 * j + 1] = pp.y;
+            w[2 * j] = residual(pp.x, qq.x);
+            w[2 * j + 1] = residual(pp.y, qq.y);
+          }
+        } else {
 #pragma unroll
-      for (int j = 0; j < E::kPerVec; ++j) {
-        const float p = prob(tp.x(x, j), k, mkp, invp);
-        psum += p;
-        if (pair) wsum += residual(p, prob(tq.x(x, j), k, mkq, invq));
+          for (int j = 0; j < N / 2; ++j) {
+            const float2 pp = upk(prob2(E::pair(vp, j), k2, nmkp, ip));
+            p[2 * j] = w[2 * j] = pp.x;
+            p[2 * j + 1] = w[2 * j + 1] = pp.y;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < N; ++j) w[j] = p[j] = 0.f;
       }
+    } else {
+#pragma unroll
+      for (int j = 0; j < N; ++j) {
+        if (e + j < hi) {
+          p[j] = prob(E::at(rp, e + j), k, mkp, invp);
+          w[j] = pair ? residual(p[j], prob(E::at(rq, e + j), k, mkq, invq)) : p[j];
+        } else {
+          w[j] = p[j] = 0.f;
+        }
+      }
+    }
+  };
+  float wsum = 0.f, psum = 0.f;
+  for (int ps = 0; ps < npass; ++ps) {
+    const int64_t e0 = lo + int64_t(ps) * kPass;
+#pragma unroll
+    for (int q = 0; q < kVecPerPass; ++q) {
+      float w[N], p[N];
+      vec_weights(e0 + int64_t(q * kThreads + tid) * N, w, p);
+      float sw = 0.f, sp = 0.f;
+#pragma unroll
+      for (int j = 0; j < N; ++j) {
+        sw = __fadd_rn(sw, w[j]);
+        sp = __fadd_rn(sp, p[j]);
+      }
+      const int s = ps * kVecPerPass + q;
+      vsw[s * kThreads + tid] = sw;
+      vsp[s * kThreads + tid] = sp;
+      wsum = __fadd_rn(wsum, sw);
+      psum = __fadd_rn(psum, sp);
+    }
   }
-  if (!pair) wsum = psum;
   wsum = warp_sum(wsum);
   psum = warp_sum(psum);
-  if (lane == 0) sm.mass_warp[warp] = make_float2(wsum, psum);
+  if (lane == 0) fx.mass_warp[warp] = make_float2(wsum, psum);
   __syncthreads();
   if (tid < CL) {
-    float2 acc = sm.mass_warp[0];
-    for (int w = 1; w < kWarps; ++w) { acc.x += sm.mass_warp[w].x; acc.y += sm.mass_warp[w].y; }
-    float2* dst = cluster.map_shared_rank(&sm.all_mass[rank], tid);
+    float2 acc = fx.mass_warp[0];
+    for (int w = 1; w < kWarps; ++w) {
+      acc.x = __fadd_rn(acc.x, fx.mass_warp[w].x);
+      acc.y = __fadd_rn(acc.y, fx.mass_warp[w].y);
+    }
+    float2* dst = cluster.map_shared_rank(&fx.all_mass[rank], tid);
     *dst = acc;
   }
   cluster.sync();
@@ -455,82 +670,96 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Args a) {
   // ---------------- which chunk holds u * total (every block, same order) ------------------
   if (tid == 0) {
     float R = 0.f, Pm = 0.f;
-    for (int c = 0; c < CL; ++c) { R += sm.all_mass[c].x; Pm += sm.all_mass[c].y; }
-    const bool use_w = !pair || R > 0.f;   // bonus: w is p itself
-    int f = sm.flags;
+    for (int c = 0; c < CL; ++c) {
+      R = __fadd_rn(R, fx.all_mass[c].x);
+      Pm = __fadd_rn(Pm, fx.all_mass[c].y);
+    }
+    const bool use_w = !pair || R > 0.f;   // bonus: the weights are p itself
+    int f = fx.flags;
     if (!use_w) f |= SPEC_ST_R_ZERO;
     const float total = use_w ? R : Pm;
-    const float target = a.u_sample[b] * total;
+    const float target = __fmul_rn(a.u_sample[b], total);
     int owner = -1, last = 0;
-    float excl = 0.f, run = 0.f;
+    float excl = 0.f, run = 0.f, excl_last = 0.f;
     for (int c = 0; c < CL; ++c) {
-      const float w = use_w ? sm.all_mass[c].x : sm.all_mass[c].y;
-      if (w > 0.f) last = c;
-      if (owner < 0) {
-        excl = run;
-        run += w;
-        if (run > target && w > 0.f) owner = c;
+      const float w = use_w ? fx.all_mass[c].x : fx.all_mass[c].y;
+      if (w > 0.f) { last = c; excl_last = run; }
+      const float nr = __fadd_rn(run, w);
+      if (owner < 0 && nr > target && w > 0.f) { owner = c; excl = run; }
+      run = nr;
+    }
+    if (owner < 0) { owner = last; excl = excl_last; }
+    fx.owner = owner;
+    fx.flags = f | (use_w ? 0 : 0x100);   // 0x100: draw from p (internal)
+    fx.target_local = __fsub_rn(target, excl);
+    fx.mass_out = pair ? (use_w ? R : 0.f) : R;
+  }
+  __syncthreads();
+  if (rank != fx.owner) return;
+
+  // ---------------- owner block: locate the token from the per-vector sums -----------------
+  const bool draw_p = !pair || (fx.flags & 0x100);
+  const float* vs = draw_p ? vsp : vsw;
+  const float tl = fx.target_local;
+  // per-(slice, warp) sums; slice-major, warp-minor is ascending vocabulary order
+  for (int s = 0; s < slices; ++s) {
+    const float x = warp_sum(vs[s * kThreads + tid]);
+    if (lane == 0) fx.wsum[s][warp] = x;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int ss = -1, sw = 0, ls = 0, lw = 0;
+    float run = 0.f, base = 0.f, base_last = 0.f;
+    for (int s = 0; s < slices && ss < 0; ++s)
+      for (int w = 0; w < kWarps; ++w) {
+        const float x = fx.wsum[s][w];
+        if (x > 0.f) { ls = s; lw = w; base_last = run; }
+        const float nr = __fadd_rn(run, x);
+        if (nr > tl && x > 0.f) { ss = s; sw = w; base = run; break; }
+        run = nr;
       }
-    }
-    if (owner < 0) { owner = last; excl = 0.f; for (int c = 0; c < last; ++c) excl += use_w ? sm.all_mass[c].x : sm.all_mass[c].y; }
-    sm.owner = owner;
-    sm.flags = f | (use_w ? 0 : 0x100);   // 0x100: draw from p (internal)
-    sm.target_local = target - excl;
-    sm.mass_out = pair ? (use_w ? R : 0.f) : R;
-    sm.cand = INT_MAX;
-    sm.lastpos = -1;
+    if (ss < 0) { ss = ls; sw = lw; base = base_last; }
+    fx.slice = ss;
+    fx.warp_sel = sw;
+    fx.run_sel = base;
+    fx.token = int(lo);
   }
   __syncthreads();
-  if (rank != sm.owner) return;
-
-  // ---------------- owner block: prefix scan inside the chunk ------------------------------
-  const bool draw_p = !pair || (sm.flags & 0x100);
-  const float tl = sm.target_local;
-  int64_t seg = (hi - lo + kThreads - 1) / kThreads;
-  seg = (seg + E::kPerVec - 1) / E::kPerVec * E::kPerVec;
-  const int64_t s0 = lo + int64_t(tid) * seg;
-  const int64_t s1 = (s0 + seg < hi) ? s0 + seg : hi;
-  auto weight = [&](int64_t v) -> float {
-    const float p = prob(E::at(rp, v), k, mkp, invp);
-    if (draw_p) return p;
-    return residual(p, prob(E::at(rq, v), k, mkq, invq));
-  };
-  float mysum = 0.f;
-  int mylast = -1;
-  for (int64_t v = s0; v < s1; ++v) {
-    const float w = weight(v);
-    mysum += w;
-    if (w > 0.f) mylast = int(v);
-  }
-  // block exclusive scan of the per-thread sums (warp scan, then warp totals in order)
-  float incl = mysum;
+  if (warp == fx.warp_sel) {
+    const int s = fx.slice;
+    const float x = vs[s * kThreads + tid];
+    float incl = x;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float y = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) sm.scan_warp[warp] = incl;
-  __syncthreads();
-  float woff = 0.f;
-  for (int w = 0; w < warp; ++w) woff += sm.scan_warp[w];
-  const float excl = woff + incl - mysum;
-  if (mysum > 0.f && excl + mysum > tl) atomicMin(&sm.cand, tid);
-  if (mylast >= 0) atomicMax(&sm.lastpos, mylast);
-  __syncthreads();
-  if (tid == sm.cand) {
-    int tok = mylast;
-    float r = excl;
-    for (int64_t v = s0; v < s1; ++v) {
-      const float w = weight(v);
-      r += w;
-      if (w > 0.f && r > tl) { tok = int(v); break; }
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl = __fadd_rn(incl, y);
     }
-    sm.token = tok;
+    const float base = fx.run_sel;
+    const unsigned hit = __ballot_sync(kFull, x > 0.f && __fadd_rn(base, incl) > tl);
+    const unsigned pos = __ballot_sync(kFull, x > 0.f);
+    const int sel = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
+    if (lane == sel) {
+      const int ps = s / kVecPerPass, q = s - ps * kVecPerPass;
+      const int64_t e = lo + int64_t(ps) * kPass + int64_t(q * kThreads + tid) * N;
+      float w[N], p[N];
+      vec_weights(e, w, p);
+      float r = __fsub_rn(__fadd_rn(base, incl), x);
+      int tok = -1, lastpos = -1;
+#pragma unroll
+      for (int j = 0; j < N; ++j) {
+        const float wj = draw_p ? p[j] : w[j];
+        r = __fadd_rn(r, wj);
+        if (wj > 0.f) {
+          lastpos = int(e) + j;
+          if (tok < 0 && r > tl) tok = int(e) + j;
+        }
+      }
+      fx.token = tok >= 0 ? tok : (lastpos >= 0 ? lastpos : int(lo));
+    }
   }
-  if (tid == 0 && sm.cand == INT_MAX) sm.token = sm.lastpos >= 0 ? sm.lastpos : int(lo);
   __syncthreads();
 
-  const int tok = sm.token;
+  const int tok = fx.token;
   for (int i = tid; i <= gmax; i += kThreads) {
     int v = -1;
     if (i < m) v = a.draft_tokens[int64_t(b) * gmax + i];
@@ -540,14 +769,14 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Args a) {
   if (a.diag) {
     float* dg = a.diag + int64_t(b) * (2 * gmax + 1);
     for (int i = tid; i < gmax; i += kThreads) {
-      dg[2 * i] = i < g ? sm.pd[i] : NAN;
-      dg[2 * i + 1] = i < g ? sm.qd[i] : NAN;
+      dg[2 * i] = i < g ? fx.pd[i] : NAN;
+      dg[2 * i + 1] = i < g ? fx.qd[i] : NAN;
     }
-    if (tid == 0) dg[2 * gmax] = sm.mass_out;
+    if (tid == 0) dg[2 * gmax] = fx.mass_out;
   }
   if (tid == 0) {
     a.num_accepted[b] = m;
-    if (a.status) a.status[b] = sm.flags & 0xff;
+    if (a.status) a.status[b] = fx.flags & 0xff;
   }
 }
 
@@ -569,35 +798,54 @@ Plan make_plan(int64_t V) {
   return Plan{cl, int(c)};
 }
 
+int slices_for(int64_t chunk, int dtype) {
+  const int64_t per_pass = int64_t(kThreads) * kVecPerPass * (dtype == SPEC_BF16 ? 8 : 4);
+  return int((chunk + per_pass - 1) / per_pass) * kVecPerPass;
+}
+
 std::mutex g_attr_mu;
 
 template <class E, bool kVec, bool kMixed>
-int launch(const Args& args, int B, void* stream) {
+int launch(const Args& args, int B, int dtype, void* stream) {
   auto fn = verify_kernel<E, kVec, kMixed>;
   const Plan plan = make_plan(args.V);
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  {
-    // cluster sizes above 8 need an opt-in; done once per device and kernel
-    static bool done[64] = {};
-    std::lock_guard<std::mutex> lk(g_attr_mu);
-    if (dev < 64 && !done[dev]) {
-      e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(NonPortableClusterSizeAllowed)");
-      done[dev] = true;
-    }
+  const int slices = slices_for(plan.chunk, dtype);
+  if (slices > kMaxSlices) {
+    set_error("V=%lld too large: %d vocabulary slices per block (max %d)", (long long)args.V, slices,
+              kMaxSlices);
+    return SPEC_ENOSPACE;
+  }
+  const Layout L = make_layout(2 * args.gmax + 1, plan.cl, slices);
+  if (L.total > kMaxDynSmem) {
+    set_error("shared memory plan of %d bytes exceeds %d", L.total, kMaxDynSmem);
+    return SPEC_ENOSPACE;
   }
   if (int64_t(B) * plan.cl > INT_MAX) {
     set_error("B=%d too large for %d blocks per sequence", B, plan.cl);
     return SPEC_ENOSPACE;
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  {
+    // cluster sizes above 8 and dynamic shared memory above 48 KB need an opt-in; done once
+    // per device and kernel
+    static bool done[64] = {};
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if (dev >= 64 || !done[dev]) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(NonPortableClusterSizeAllowed)");
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)");
+      if (dev < 64) done[dev] = true;
+    }
   }
   Args a = args;
   a.chunk = plan.chunk;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(B * plan.cl), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = size_t(L.total);
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -639,20 +887,18 @@ bool vec_ok(const void* p, int dtype, int64_t V) {
   return p == nullptr || ((reinterpret_cast<uintptr_t>(p) % 16 == 0) && (V * es) % 16 == 0);
 }
 
-}  // namespace
-}  // namespace specverify
-
-using namespace specverify;
-
-namespace {
 template <bool kMixed>
 int dispatch_on(const Args& a, int dtype, int B, void* stream) {
   const bool vec = vec_ok(a.target, dtype, a.V) && vec_ok(a.draft, dtype, a.V);
   if (dtype == SPEC_BF16)
-    return vec ? launch<Bf16, true, kMixed>(a, B, stream) : launch<Bf16, false, kMixed>(a, B, stream);
-  return vec ? launch<F32, true, kMixed>(a, B, stream) : launch<F32, false, kMixed>(a, B, stream);
+    return vec ? launch<Bf16, true, kMixed>(a, B, dtype, stream) : launch<Bf16, false, kMixed>(a, B, dtype, stream);
+  return vec ? launch<F32, true, kMixed>(a, B, dtype, stream) : launch<F32, false, kMixed>(a, B, dtype, stream);
 }
+
 }  // namespace
+}  // namespace specverify
+
+using namespace specverify;
 
 extern "C" int spec_verify_greedy(const void* target_logits, int dtype, const int32_t* draft_tokens,
                                   const int32_t* num_draft, int B, int gmax, int V,
@@ -660,8 +906,7 @@ extern "C" int spec_verify_greedy(const void* target_logits, int dtype, const in
                                   void* stream) {
   clear_error();
   int rc = check_common(target_logits, dtype, draft_tokens, B, gmax, V, out_tokens, num_accepted);
-  if (rc != SPEC_OK) return rc;
-  if (B == 0) return SPEC_OK;
+  if (rc != SPEC_OK || B == 0) return rc;
   Args a = {};
   a.target = target_logits;
   a.draft_tokens = draft_tokens;
