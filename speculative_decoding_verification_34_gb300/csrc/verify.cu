@@ -40,13 +40,13 @@ namespace cg = cooperative_groups;
 namespace specverify {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCluster = 16;
-constexpr int kVecPerPass = 4;                         // 16-byte vectors per thread per tile
+constexpr int kVecPerPass = 8;                         // 16-byte vectors per thread per tile
 constexpr int kStages = 3;                             // cp.async ring depth (tiles)
 constexpr int kTileBytes = kThreads * kVecPerPass * 16;
-constexpr int kMaxSlices = 64;                         // (pass, vector slot) pairs per chunk
+constexpr int kMaxSlices = 128;                        // (pass, vector slot) pairs per chunk
 constexpr int kMaxDynSmem = 160 * 1024;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -128,10 +128,11 @@ __device__ __forceinline__ uint4 ld_l2(const void* p) {
   return v;
 }
 
+// Warp-wide max in one instruction (sm_100+ f32 redux); -inf is the identity.
 __device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
-  return v;
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
 }
 
 // Tree sum into lane 0, then broadcast: every lane gets the same bits.
@@ -192,12 +193,20 @@ struct Bf16 {
     const uint32_t w = (j >> 1) == 0 ? v.x : (j >> 1) == 1 ? v.y : (j >> 1) == 2 ? v.z : v.w;
     return __uint_as_float((j & 1) ? (w & 0xffff0000u) : (w << 16));
   }
-  __device__ __forceinline__ static float vmax(const uint4& v) {
-    __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
-    a = __hmax2(a, *reinterpret_cast<const __nv_bfloat162*>(&v.y));
-    a = __hmax2(a, *reinterpret_cast<const __nv_bfloat162*>(&v.z));
-    a = __hmax2(a, *reinterpret_cast<const __nv_bfloat162*>(&v.w));
-    return fmaxf(__low2float(a), __high2float(a));
+  static constexpr uint32_t kNegInf = 0xff80ff80u;   // two bf16 -inf
+  // max over kVecPerPass vectors: bf16x2 max tree, one widening at the end
+  __device__ __forceinline__ static float tmax(const uint4 (&v)[kVecPerPass]) {
+    __nv_bfloat162 a[kVecPerPass];
+#pragma unroll
+    for (int q = 0; q < kVecPerPass; ++q) {
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[q]);
+      a[q] = __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3]));
+    }
+#pragma unroll
+    for (int w = kVecPerPass / 2; w > 0; w >>= 1)
+#pragma unroll
+      for (int q = 0; q < w; ++q) a[q] = __hmax2(a[q], a[q + w]);
+    return fmaxf(__low2float(a[0]), __high2float(a[0]));
   }
 };
 
@@ -211,8 +220,18 @@ struct F32 {
   __device__ __forceinline__ static float get(const uint4& v, int j) {
     return __uint_as_float(j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w);
   }
-  __device__ __forceinline__ static float vmax(const uint4& v) {
-    return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)), fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+  static constexpr uint32_t kNegInf = 0xff800000u;
+  __device__ __forceinline__ static float tmax(const uint4 (&v)[kVecPerPass]) {
+    float a[kVecPerPass];
+#pragma unroll
+    for (int q = 0; q < kVecPerPass; ++q)
+      a[q] = fmaxf(fmaxf(__uint_as_float(v[q].x), __uint_as_float(v[q].y)),
+                   fmaxf(__uint_as_float(v[q].z), __uint_as_float(v[q].w)));
+#pragma unroll
+    for (int w = kVecPerPass / 2; w > 0; w >>= 1)
+#pragma unroll
+      for (int q = 0; q < w; ++q) a[q] = fmaxf(a[q], a[q + w]);
+    return a[0];
   }
 };
 
@@ -224,11 +243,18 @@ template <class E, bool kVec>
 struct Tile {
   static constexpr int N = E::kPerVec;
   uint4 v[kVecPerPass];
-  bool ok[kVecPerPass];
   float s[kVec ? 1 : kVecPerPass * N];
 
+  // vector path: vectors q >= nq of this thread lie past the chunk end -> -inf
+  __device__ __forceinline__ void mask_tail(int nq) {
+    if constexpr (kVec) {
+#pragma unroll
+      for (int q = 0; q < kVecPerPass; ++q)
+        if (q >= nq) v[q] = make_uint4(E::kNegInf, E::kNegInf, E::kNegInf, E::kNegInf);
+    }
+  }
   __device__ __forceinline__ float x(int k, int j) const {
-    if constexpr (kVec) return ok[k] ? E::get(v[k], j) : -INFINITY;
+    if constexpr (kVec) return E::get(v[k], j);
     else return s[k * N + j];
   }
 };
@@ -236,12 +262,11 @@ struct Tile {
 template <class E, bool kVec>
 __device__ __forceinline__ void tile_stats(const Tile<E, kVec>& t, float k, float& run_m, float& run_s) {
   constexpr int N = E::kPerVec;
-  float m = -INFINITY;
+  float m;
   if constexpr (kVec) {
-#pragma unroll
-    for (int a = 0; a < kVecPerPass; ++a)
-      if (t.ok[a]) m = fmaxf(m, E::vmax(t.v[a]));
+    m = E::tmax(t.v);
   } else {
+    m = -INFINITY;
 #pragma unroll
     for (int a = 0; a < kVecPerPass * N; ++a) m = fmaxf(m, t.s[a]);
   }
@@ -250,15 +275,15 @@ __device__ __forceinline__ void tile_stats(const Tile<E, kVec>& t, float k, floa
   if (m != -INFINITY) {
     const float mk = __fmul_rn(m, k);
     if constexpr (kVec) {
+      // four independent f32x2 accumulators, combined in a fixed order
       const f2 k2 = pk(k, k), nmk2 = pk(-mk, -mk);
-      f2 acc = pk(0.f, 0.f);
+      f2 acc[4] = {pk(0.f, 0.f), pk(0.f, 0.f), pk(0.f, 0.f), pk(0.f, 0.f)};
 #pragma unroll
       for (int a = 0; a < kVecPerPass; ++a)
-        if (t.ok[a]) {
 #pragma unroll
-          for (int j = 0; j < N / 2; ++j) acc = add2(acc, ex2x2(fma2(E::pair(t.v[a], j), k2, nmk2)));
-        }
-      const float2 r = upk(acc);
+        for (int j = 0; j < N / 2; ++j)
+          acc[(a * (N / 2) + j) & 3] = add2(acc[(a * (N / 2) + j) & 3], ex2x2(fma2(E::pair(t.v[a], j), k2, nmk2)));
+      const float2 r = upk(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])));
       s = __fadd_rn(r.x, r.y);
     } else {
 #pragma unroll
@@ -446,9 +471,13 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Args a) {
       cp_async_wait<kStages - 1>();
       const unsigned char* st = ring + (t % kStages) * kTileBytes;
 #pragma unroll
-      for (int q = 0; q < kVecPerPass; ++q) {
+      for (int q = 0; q < kVecPerPass; ++q)
         tile.v[q] = *reinterpret_cast<const uint4*>(st + (q * kThreads + tid) * 16);
-        tile.ok[q] = e0 + int64_t(q * kThreads + tid) * N < hi;
+      if (e0 + kPass > hi) {
+        // partial tile: vectors q with e0 + (q*kThreads + tid)*N >= hi hold zero fill
+        const int64_t left = hi - e0 - int64_t(tid) * N;
+        const int nq = left <= 0 ? 0 : int((left + int64_t(kThreads) * N - 1) / (int64_t(kThreads) * N));
+        tile.mask_tail(nq);
       }
     } else {
 #pragma unroll
