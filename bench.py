@@ -283,8 +283,9 @@ def run_native(args):
     kv = kv0.clone()
     dkv = kv0.clone()
     stream = torch.cuda.current_stream(device)
+    ws = sv.alloc_workspace(B, g, V, sv.SPEC_BF16 if wl.dtype == "bf16" else sv.SPEC_F32, device)
     verify = [sv.prepare_verify_sample(tgt[c], drf[c], toks, nd, temp, ua, us, out, macc, dg, st,
-                                       stream=stream) for c in range(ncopies)]
+                                       workspace=ws, stream=stream) for c in range(ncopies)]
     commit = sv.prepare_commit_kv_lengths(macc, kv, dkv, True, stream=stream, gmax=g)
 
     for i in range(args.warmup):
@@ -347,7 +348,7 @@ def run_native(args):
         for h, d in zip(h_in, d_in):
             d.copy_(h, non_blocking=True)
         sv.spec_verify_sample(d_in[0], d_in[1], d_in[2], d_in[3], d_in[4], d_in[5], d_in[6],
-                              out, macc, dg, st)
+                              out, macc, dg, st, workspace=ws)
         sv.spec_commit_kv_lengths(macc, kv, None, True, gmax=g)
         h_out[0].copy_(out, non_blocking=True)
         h_out[1].copy_(macc, non_blocking=True)

@@ -13,6 +13,12 @@
  *    nothing, keeps no state between calls and never synchronises the host: each call
  *    enqueues its work on `stream` (a cudaStream_t passed as void*; NULL = the legacy
  *    default stream) and returns.  Results are valid once the stream reaches that point.
+ *  - The verify calls take a caller-owned device WORKSPACE of at least
+ *    spec_verify_workspace_bytes(B, gmax, V, dtype) bytes, 64-byte aligned, which must be
+ *    zero-filled before its first use.  Every completed call leaves it zero-filled again, so
+ *    one workspace serves any number of successive calls; calls that may run at the same time
+ *    (different streams) need different workspaces.  A workspace is sized for (B, gmax, V):
+ *    a larger one may be passed for smaller calls.
  *  - Arrays are row-major and contiguous:
  *        target_logits [B][gmax+1][V]   row i judges draft i; row 0 is the target's saved
  *                                       prediction for the position after the committed
@@ -33,7 +39,7 @@
  *  - Data-dependent problems never fault or trap the GPU: they set bits in the optional
  *    per-sequence status[B] word (see SPEC_ST_*) and a defined fallback is taken.
  *  - Limits: 0 <= B, 0 <= gmax <= SPEC_MAX_GAMMA, 1 <= V <= 2^21 (bf16) or 2^20 (fp32);
- *    a larger V returns SPEC_ENOSPACE.  B == 0 is a no-op that enqueues nothing and accepts
+ *    a larger V, or a batch needing more than 2^31-1 thread blocks, returns SPEC_ENOSPACE.  B == 0 is a no-op that enqueues nothing and accepts
  *    null pointers (empty tensors have none).
  */
 #ifndef SPECVERIFY_H
@@ -63,6 +69,8 @@ typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype_t;
 #define SPEC_ST_R_ZERO 2         /* a rejection met residual mass R == 0: the correction was drawn from p_m */
 #define SPEC_ST_CLAMPED_GAMMA 4  /* num_draft[b] was outside [0,gmax] and was clamped */
 #define SPEC_ST_HISTORY_FULL 8   /* commit: appending would overflow the history; sequence left untouched */
+#define SPEC_ST_TIMEOUT 16       /* a bounded device-side wait ran out: outputs of the sequence not
+                                    written; zero-fill the workspace before reusing it */
 
 /*
  * Greedy verification (temperature 0).
@@ -77,10 +85,12 @@ typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype_t;
  *   num_draft      [B] drafts per sequence, or NULL for gmax everywhere
  *   out_tokens     [B][gmax+1] (written), num_accepted [B] = m (written)
  *   status         [B] or NULL (written: SPEC_ST_* bits)
+ *   workspace      device scratch of workspace_bytes bytes (see the conventions above)
  */
 int spec_verify_greedy(const void* target_logits, int dtype, const int32_t* draft_tokens,
                        const int32_t* num_draft, int B, int gmax, int V, int32_t* out_tokens,
-                       int32_t* num_accepted, int32_t* status, void* stream);
+                       int32_t* num_accepted, int32_t* status, void* workspace,
+                       size_t workspace_bytes, void* stream);
 
 /*
  * Sampling verification (tutorial §7.1-§7.3; card §04-§06; "学徒的草稿" part 2, Steps 3-4).
@@ -107,7 +117,14 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits, int 
                        const int32_t* draft_tokens, const int32_t* num_draft,
                        const float* temperature, const float* u_accept, const float* u_sample,
                        int B, int gmax, int V, int32_t* out_tokens, int32_t* num_accepted,
-                       float* diag, int32_t* status, void* stream);
+                       float* diag, int32_t* status, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/*
+ * Bytes of workspace a verify call with these sizes needs (either entry point); 0 for
+ * invalid sizes.  Host-only.
+ */
+size_t spec_verify_workspace_bytes(int B, int gmax, int V, int dtype);
 
 /*
  * Commit one round and roll the KV lengths back (tutorial §5.1-§5.2; card §06).
@@ -140,9 +157,9 @@ const char* spec_last_error(void);
 uint64_t spec_launch_count(void);
 
 /*
- * How a verify call splits the vocabulary for this V and dtype: each sequence is one
- * thread-block cluster of *ctas_per_seq blocks, block c owning ids [c*chunk, (c+1)*chunk)
- * of every row.  Host-only; returns SPEC_OK or SPEC_EINVAL.
+ * How a verify call splits the vocabulary for this V and dtype: every row is cut into
+ * *ctas_per_seq chunks of *chunk ids (the last one ragged), each streamed by one thread
+ * block.  Host-only; returns SPEC_OK or SPEC_EINVAL.
  */
 int spec_verify_plan(int V, int dtype, int* ctas_per_seq, int* chunk);
 

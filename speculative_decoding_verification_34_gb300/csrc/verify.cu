@@ -1,32 +1,32 @@
-// Fused greedy / sampling verification: one thread-block cluster per sequence.
+// Greedy / sampling verification as one grid of independent work units.
 //
 // What is computed follows the tutorial "投机解码教程：从概率保持、KV Cache 回滚到性能盈亏平衡"
 // (§3-§4 greedy verification and logit alignment, §7.1-§7.3 acceptance min(1,p/q), residual
 // max(p-q,0)/R and the bonus draw) and the "M013" knowledge-base card (§03-§05, including the
-// R = 0 remark).  How it is computed is this library's own design for sm_103a:
+// R = 0 remark).  How it is computed is this library's own design for sm_103a.
 //
-//   * Cluster of C blocks per sequence b (C <= 16); block c owns the vocabulary chunk
-//     [c*chunk, (c+1)*chunk) of every row of b.
-//   * Phase A streams the chunk of every row the sequence needs exactly once from HBM.  Each
-//     thread keeps its own 16-byte vectors in flight through a kStages-deep ring in shared
-//     memory (cp.async, one commit group per tile), so loads of the next tiles overlap the
-//     arithmetic on the current one.  A tile reduces to a (max, sum 2^((x-max)k)) pair with one
-//     ex2 per element (bf16x2 max, f32x2 FMA/ADD), or to (max, lowest id) for greedy rows.
-//   * Exchange 1: every block pushes its per-row partials into every block's shared memory
-//     (distributed shared memory); after one cluster barrier all blocks derive, in the same
-//     order, the same row maxima/normalisers, acceptance flags and m.
-//   * Phase B (sampling only): every block re-reads its chunk of the row (pair) the last token
-//     is drawn from -- row m of p and q after a rejection, the bonus row otherwise; normally an
-//     L2 hit -- keeping one partial sum per (pass, vector slot, thread) in shared memory, and
-//     pushes its chunk mass (exchange 2, second cluster barrier).
-//   * The block whose chunk holds u*R finds the token from its per-vector sums (warp scans,
-//     one vector reloaded) and writes the outputs.
+// The vocabulary of every row is cut into CL chunks of `chunk` ids.  One launch runs two kinds
+// of block-sized work units, in a logical order that every block draws from a ticket counter
+// (so a unit only ever waits for units with smaller tickets, which are already running or
+// finished -- forward progress does not depend on the hardware's dispatch order):
 //
-// No global workspace, no atomics on global memory, no spin-waits: the only cross-block
-// synchronisation is the hardware cluster barrier, which every block of a cluster reaches the
-// same number of times.  cp.async groups are waited per thread (the thread's own copies).
+//   A(b, row, c)  streams chunk c of one valid row of sequence b from HBM (128-bit loads, one
+//                 ex2 per sampled element) and writes a (max, sum 2^((x-max)k)) partial, or an
+//                 (argmax value, id) partial for greedy rows, to the workspace; the unit whose
+//                 chunk holds a draft id also records that logit.  The last A unit of b to
+//                 finish (an arrival counter) is the *decider*: it combines the partials in a
+//                 fixed order, takes the acceptance decisions, finds m, and either writes the
+//                 greedy result or publishes a plan for the final draw.
+//   B(b, c)       waits (bounded) for b's plan, re-reads chunk c of the row the last token is
+//                 drawn from -- row m of p and q after a rejection, the bonus row otherwise;
+//                 these units come about two scheduling waves after b's A units, so the rows
+//                 are normally still in L2 -- and writes the chunk's residual and p masses.
+//                 The last B unit of b to finish is the *selector*: it locates the chunk
+//                 holding u*R, rescans that chunk and writes the outputs.
+//
+// Every call leaves the workspace zero-filled again (each counter is reset by the unit that
+// consumed it last), so a zero-filled workspace can serve successive calls on one stream.
 
-#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 #include <climits>
@@ -35,21 +35,21 @@
 
 #include "common.cuh"
 
-namespace cg = cooperative_groups;
-
 namespace specverify {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxCluster = 16;
-constexpr int kVecPerPass = 8;                         // 16-byte vectors per thread per tile
-constexpr int kStages = 3;                             // cp.async ring depth (tiles)
-constexpr int kTileBytes = kThreads * kVecPerPass * 16;
-constexpr int kMaxSlices = 128;                        // (pass, vector slot) pairs per chunk
-constexpr int kMaxDynSmem = 160 * 1024;
+constexpr int kVecPerPass = 4;                         // 16-byte vectors per thread per pass
+constexpr int kMaxChunks = 64;                         // chunks per row
+constexpr int kMaxPasses = 4;                          // passes per chunk
+constexpr int kMaxSlices = kMaxPasses * kVecPerPass;
+constexpr int kChunkTarget = 8192;                     // ids per chunk before rounding
+constexpr unsigned kSpinLimit = 1u << 22;              // bounded wait for a plan (~seconds)
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kStTimeout = 16;                         // status bit: a bounded wait ran out
+constexpr int kInternalDrawP = 0x100;
 
 struct Args {
   const void* target;
@@ -60,12 +60,37 @@ struct Args {
   const float* u_accept;
   const float* u_sample;
   int64_t V;
+  int B;
   int gmax;
-  int chunk;
   int32_t* out_tokens;
   int32_t* num_accepted;
   float* diag;
   int32_t* status;
+};
+
+struct Geo {
+  int CL;      // chunks per row
+  int chunk;   // ids per chunk (multiple of 8)
+  int nslots;  // row slots per sequence: target rows 0..gmax, then draft rows 0..gmax-1
+  int NA;      // A units per sequence (nslots * CL)
+  int G;       // units per group: the A units of sequence g, then the B units of g - delta
+  int delta;   // B units of sequence b sit in group b + delta
+};
+
+struct PlanRec {   // per sequence, published by the decider for the B units
+  int m, g, flags, pair;
+  float mkp, invp, mkq, invq;
+};
+
+struct Work {      // views into the caller's workspace
+  int* ctrl;       // [0] ticket counter
+  int* cnt;        // [B] A arrivals
+  int* bdone;      // [B] B arrivals
+  int* ready;      // [B] plan published
+  PlanRec* plan;   // [B]
+  float2* part;    // [B][nslots][CL]
+  float* xd;       // [B][nslots] logit at the draft id of that row
+  float2* mass;    // [B][CL] (residual mass, p mass)
 };
 
 // ------------------------------------------------------------------------------------------
@@ -78,53 +103,16 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Packed pairs of f32 (sm_100+ f32x2 arithmetic), all round-to-nearest, never contracted.
-using f2 = unsigned long long;
-__device__ __forceinline__ f2 pk(float a, float b) {
-  f2 r;
-  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ float2 upk(f2 r) {
-  float2 v;
-  asm("mov.b64 {%0,%1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+// Streaming 128-bit read-only load that does not allocate in L1.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
 }
-__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
-  f2 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ f2 add2(f2 a, f2 b) {
-  f2 d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
-  f2 d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ f2 ex2x2(f2 a) {
-  const float2 v = upk(a);
-  return pk(ex2(v.x), ex2(v.y));
-}
 
-// 16-byte global -> shared copy that bypasses L1; src_bytes = 0 zero-fills without reading.
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
-  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ uint4 ld_l2(const void* p) {
-  uint4 v;
-  asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
@@ -150,8 +138,8 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
 __device__ __forceinline__ void warp_argmax(float& v, int& i) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    float v2 = __shfl_xor_sync(kFull, v, o);
-    int i2 = __shfl_xor_sync(kFull, i, o);
+    const float v2 = __shfl_xor_sync(kFull, v, o);
+    const int i2 = __shfl_xor_sync(kFull, i, o);
     if (better(v2, i2, v, i)) { v = v2; i = i2; }
   }
 }
@@ -168,11 +156,9 @@ __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2,
 }
 
 // p_v = 2^((x_v - M) k) / S, evaluated as ex2(x*k - M*k) * (1/S) with a rounded product.
-// prob() and prob2() give identical bits for the same element.
 __device__ __forceinline__ float prob(float x, float k, float mk, float inv_s) {
   return __fmul_rn(ex2(fmaf(x, k, -mk)), inv_s);
 }
-__device__ __forceinline__ f2 prob2(f2 x, f2 k2, f2 nmk2, f2 inv2) { return mul2(ex2x2(fma2(x, k2, nmk2)), inv2); }
 
 // max(p - q, 0) with a rounded difference: exactly 0 wherever p == q.
 __device__ __forceinline__ float residual(float p, float q) { return fmaxf(__fsub_rn(p, q), 0.f); }
@@ -181,20 +167,15 @@ __device__ __forceinline__ float residual(float p, float q) { return fmaxf(__fsu
 struct Bf16 {
   using raw = uint16_t;
   static constexpr int kPerVec = 8;
+  static constexpr uint32_t kNegInf = 0xff80ff80u;   // two bf16 -inf
   __device__ __forceinline__ static float at(const raw* row, int64_t i) {
     return __uint_as_float(uint32_t(__ldg(row + i)) << 16);
-  }
-  // element pair j (0..3) of a vector, widened to f32x2 (lower id first)
-  __device__ __forceinline__ static f2 pair(const uint4& v, int j) {
-    const uint32_t w = j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
-    return pk(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
   }
   __device__ __forceinline__ static float get(const uint4& v, int j) {
     const uint32_t w = (j >> 1) == 0 ? v.x : (j >> 1) == 1 ? v.y : (j >> 1) == 2 ? v.z : v.w;
     return __uint_as_float((j & 1) ? (w & 0xffff0000u) : (w << 16));
   }
-  static constexpr uint32_t kNegInf = 0xff80ff80u;   // two bf16 -inf
-  // max over kVecPerPass vectors: bf16x2 max tree, one widening at the end
+  // max over the vectors of one pass: bf16x2 max tree, one widening at the end
   __device__ __forceinline__ static float tmax(const uint4 (&v)[kVecPerPass]) {
     __nv_bfloat162 a[kVecPerPass];
 #pragma unroll
@@ -213,49 +194,45 @@ struct Bf16 {
 struct F32 {
   using raw = float;
   static constexpr int kPerVec = 4;
+  static constexpr uint32_t kNegInf = 0xff800000u;
   __device__ __forceinline__ static float at(const raw* row, int64_t i) { return __ldg(row + i); }
-  __device__ __forceinline__ static f2 pair(const uint4& v, int j) {
-    return j == 0 ? pk(__uint_as_float(v.x), __uint_as_float(v.y)) : pk(__uint_as_float(v.z), __uint_as_float(v.w));
-  }
   __device__ __forceinline__ static float get(const uint4& v, int j) {
     return __uint_as_float(j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w);
   }
-  static constexpr uint32_t kNegInf = 0xff800000u;
   __device__ __forceinline__ static float tmax(const uint4 (&v)[kVecPerPass]) {
-    float a[kVecPerPass];
+    float a = -INFINITY;
 #pragma unroll
     for (int q = 0; q < kVecPerPass; ++q)
-      a[q] = fmaxf(fmaxf(__uint_as_float(v[q].x), __uint_as_float(v[q].y)),
-                   fmaxf(__uint_as_float(v[q].z), __uint_as_float(v[q].w)));
-#pragma unroll
-    for (int w = kVecPerPass / 2; w > 0; w >>= 1)
-#pragma unroll
-      for (int q = 0; q < w; ++q) a[q] = fmaxf(a[q], a[q + w]);
-    return a[0];
+      a = fmaxf(a, fmaxf(fmaxf(__uint_as_float(v[q].x), __uint_as_float(v[q].y)),
+                         fmaxf(__uint_as_float(v[q].z), __uint_as_float(v[q].w))));
+    return a;
   }
 };
 
-// A tile is one pass of one row: vector k of thread t covers elements
-// e0 + (k*kThreads + t)*kPerVec .. +kPerVec-1 (coalesced across the block for every k).
-// Vector path: the vectors come from the shared-memory ring.  Scalar path (unaligned rows):
-// elements are loaded one by one.  Out-of-range elements read as -inf.
+// One pass of one row chunk: vector q of thread t covers ids e0 + (q*kThreads + t)*kPerVec
+// .. + kPerVec - 1, coalesced across the block for every q.  Ids at or past hi read as -inf
+// (vector path: whole vectors, since chunk ends are vector aligned there).
 template <class E, bool kVec>
 struct Tile {
   static constexpr int N = E::kPerVec;
   uint4 v[kVecPerPass];
   float s[kVec ? 1 : kVecPerPass * N];
 
-  // vector path: vectors q >= nq of this thread lie past the chunk end -> -inf
-  __device__ __forceinline__ void mask_tail(int nq) {
-    if constexpr (kVec) {
+  __device__ __forceinline__ void load(const typename E::raw* row, int64_t e0, int64_t hi, int tid) {
 #pragma unroll
-      for (int q = 0; q < kVecPerPass; ++q)
-        if (q >= nq) v[q] = make_uint4(E::kNegInf, E::kNegInf, E::kNegInf, E::kNegInf);
+    for (int q = 0; q < kVecPerPass; ++q) {
+      const int64_t e = e0 + int64_t(q * kThreads + tid) * N;
+      if constexpr (kVec) {
+        v[q] = e < hi ? ld_stream(row + e) : make_uint4(E::kNegInf, E::kNegInf, E::kNegInf, E::kNegInf);
+      } else {
+#pragma unroll
+        for (int j = 0; j < N; ++j) s[q * N + j] = (e + j < hi) ? E::at(row, e + j) : -INFINITY;
+      }
     }
   }
-  __device__ __forceinline__ float x(int k, int j) const {
-    if constexpr (kVec) return E::get(v[k], j);
-    else return s[k * N + j];
+  __device__ __forceinline__ float x(int q, int j) const {
+    if constexpr (kVec) return E::get(v[q], j);
+    else return s[q * N + j];
   }
 };
 
@@ -274,21 +251,12 @@ __device__ __forceinline__ void tile_stats(const Tile<E, kVec>& t, float k, floa
   float s = 0.f;
   if (m != -INFINITY) {
     const float mk = __fmul_rn(m, k);
-    if constexpr (kVec) {
-      // four independent f32x2 accumulators, combined in a fixed order
-      const f2 k2 = pk(k, k), nmk2 = pk(-mk, -mk);
-      f2 acc[4] = {pk(0.f, 0.f), pk(0.f, 0.f), pk(0.f, 0.f), pk(0.f, 0.f)};
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};   // independent chains, combined in a fixed order
 #pragma unroll
-      for (int a = 0; a < kVecPerPass; ++a)
+    for (int q = 0; q < kVecPerPass; ++q)
 #pragma unroll
-        for (int j = 0; j < N / 2; ++j)
-          acc[(a * (N / 2) + j) & 3] = add2(acc[(a * (N / 2) + j) & 3], ex2x2(fma2(E::pair(t.v[a], j), k2, nmk2)));
-      const float2 r = upk(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])));
-      s = __fadd_rn(r.x, r.y);
-    } else {
-#pragma unroll
-      for (int a = 0; a < kVecPerPass * N; ++a) s = __fadd_rn(s, ex2(fmaf(t.s[a], k, -mk)));
-    }
+      for (int j = 0; j < N; ++j) acc[j & 3] = __fadd_rn(acc[j & 3], ex2(fmaf(t.x(q, j), k, -mk)));
+    s = __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
   }
   s = warp_sum(s);
   merge_ms(run_m, run_s, m, s, k);
@@ -297,52 +265,340 @@ __device__ __forceinline__ void tile_stats(const Tile<E, kVec>& t, float k, floa
 template <class E, bool kVec>
 __device__ __forceinline__ void tile_argmax(const Tile<E, kVec>& t, int64_t e0, int tid, float& bv, int& bi) {
 #pragma unroll
-  for (int a = 0; a < kVecPerPass; ++a)
+  for (int q = 0; q < kVecPerPass; ++q)
 #pragma unroll
     for (int j = 0; j < E::kPerVec; ++j) {
-      const int idx = int(e0 + int64_t(a * kThreads + tid) * E::kPerVec + j);
-      const float v = t.x(a, j);
+      const int idx = int(e0 + int64_t(q * kThreads + tid) * E::kPerVec + j);
+      const float v = t.x(q, j);
       if (better(v, idx, bv, bi)) { bv = v; bi = idx; }
     }
 }
 
-// Statically sized shared state.
-struct Fixed {
-  float2 mass_warp[kWarps];
-  float2 all_mass[kMaxCluster];       // (weight mass, p mass) of every block's chunk
+struct Shared {
+  float2 warp_part[kWarps];
+  float rowM[2 * SPEC_MAX_GAMMA + 1];
+  float rowInvS[2 * SPEC_MAX_GAMMA + 1];
+  int rowArg[SPEC_MAX_GAMMA + 1];
   float pd[SPEC_MAX_GAMMA], qd[SPEC_MAX_GAMMA];
-  float wsum[kMaxSlices][kWarps];     // owner: per-(slice, warp) weight sums
-  int m, flags, owner, token, slice, warp_sel;
+  float vs[kMaxSlices][kThreads];   // selector: per (slice, thread) weight sums of one chunk
+  float wsum[kMaxSlices][kWarps];
+  int unit, last, ok, m, flags, owner, slice, warp_sel, token;
   float target_local, mass_out, run_sel;
+  PlanRec plan;
 };
 
-// Dynamic shared memory, sized per launch (byte offsets).
-struct Layout {
-  int ring, vsw, vsp, all, wpart, local, rowM, rowInvS, rowArg, total;
+// ------------------------------------------------------------------------------------------
+// per-sequence context
+// ------------------------------------------------------------------------------------------
+
+template <class E, bool kMixed>
+struct Seq {
+  using raw = typename E::raw;
+  int b, g, flags;
+  bool sampling;
+  float k;
+  const raw* P;
+  const raw* Q;
+
+  __device__ __forceinline__ Seq(const Args& a, int b_) : b(b_) {
+    g = a.num_draft ? a.num_draft[b] : a.gmax;
+    flags = 0;
+    if (g < 0 || g > a.gmax) {
+      g = g < 0 ? 0 : a.gmax;
+      flags = SPEC_ST_CLAMPED_GAMMA;
+    }
+    float T = 0.f;
+    if constexpr (kMixed) T = a.temperature[b];
+    sampling = kMixed && (T > 0.f);
+    k = sampling ? kLog2e / T : 0.f;
+    P = static_cast<const raw*>(a.target) + int64_t(b) * (a.gmax + 1) * a.V;
+    Q = sampling ? static_cast<const raw*>(a.draft) + int64_t(b) * a.gmax * a.V : nullptr;
+  }
+  // rows this sequence reads: target 0..g (slots 0..g), draft 0..g-1 (slots gmax+1+i)
+  __device__ __forceinline__ bool slot_valid(int slot, int gmax) const {
+    if (slot <= gmax) return slot <= g;
+    return sampling && slot - gmax - 1 < g;
+  }
+  __device__ __forceinline__ int units(int CL) const { return CL * (sampling ? 2 * g + 1 : g + 1); }
 };
 
-__host__ __device__ inline Layout make_layout(int nslots, int cl, int slices) {
-  Layout L;
-  int off = 0;
-  L.ring = off;
-  L.vsw = off;                                          // phase B reuses the ring's space
-  L.vsp = off + slices * kThreads * 4;
-  const int need_a = kStages * kTileBytes, need_b = 2 * slices * kThreads * 4;
-  off += need_a > need_b ? need_a : need_b;
-  L.all = off;
-  off += cl * nslots * 8;
-  L.wpart = off;
-  off += kWarps * nslots * 8;
-  L.local = off;
-  off += nslots * 8;
-  L.rowM = off;
-  off += nslots * 4;
-  L.rowInvS = off;
-  off += nslots * 4;
-  L.rowArg = off;
-  off += nslots * 4;
-  L.total = (off + 15) & ~15;
-  return L;
+// ------------------------------------------------------------------------------------------
+// decider: combine the partials of sequence b, decide, publish
+// ------------------------------------------------------------------------------------------
+
+template <class E, bool kMixed>
+__device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E, kMixed>& sq, Shared& sm) {
+  const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
+  const int b = sq.b, g = sq.g, gmax = a.gmax, CL = geo.CL;
+  const float k = sq.k;
+  __threadfence();
+  const float2* part = w.part + int64_t(b) * geo.nslots * CL;
+  for (int slot = tid; slot < geo.nslots; slot += kThreads) {
+    if (!sq.slot_valid(slot, gmax)) continue;
+    const float2* pp = part + slot * CL;
+    if (sq.sampling) {
+      float M = -INFINITY;
+      for (int c = 0; c < CL; ++c) M = fmaxf(M, __ldcg(&pp[c]).x);
+      float S = 0.f;
+      if (M != -INFINITY)
+        for (int c = 0; c < CL; ++c) {
+          const float2 p = __ldcg(&pp[c]);
+          if (p.x != -INFINITY) S = __fadd_rn(S, __fmul_rn(p.y, ex2(__fmul_rn(p.x - M, k))));
+        }
+      sm.rowM[slot] = M;
+      sm.rowInvS[slot] = __frcp_rn(S);
+    } else {
+      float bv = -INFINITY;
+      int bi = INT_MAX;
+      for (int c = 0; c < CL; ++c) {
+        const float2 p = __ldcg(&pp[c]);
+        if (better(p.x, __float_as_int(p.y), bv, bi)) { bv = p.x; bi = __float_as_int(p.y); }
+      }
+      sm.rowArg[slot] = bi;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    bool acc = false, valid = false;
+    if (lane < g) {
+      const int d = a.draft_tokens[int64_t(b) * gmax + lane];
+      valid = d >= 0 && int64_t(d) < a.V;
+      if (sq.sampling) {
+        float p = NAN, q = NAN;
+        if (valid) {
+          const float* xd = w.xd + int64_t(b) * geo.nslots;
+          const int qs = gmax + 1 + lane;
+          p = prob(__ldcg(&xd[lane]), k, __fmul_rn(sm.rowM[lane], k), sm.rowInvS[lane]);
+          q = prob(__ldcg(&xd[qs]), k, __fmul_rn(sm.rowM[qs], k), sm.rowInvS[qs]);
+          const float u = a.u_accept[int64_t(b) * gmax + lane];
+          // u < min(1, p/q): r = 0 when p = 0, r = +inf when q = 0 < p
+          acc = (p == 0.f) ? (u < 0.f) : (p >= q ? (u < 1.f) : (__fmul_rn(u, q) < p));
+        }
+        sm.pd[lane] = p;
+        sm.qd[lane] = q;
+      } else {
+        acc = valid && d == sm.rowArg[lane];
+      }
+    }
+    const unsigned keep = __ballot_sync(kFull, acc);
+    const unsigned rej = ~keep & (g >= 32 ? kFull : ((1u << g) - 1u));
+    const int m = rej ? __ffs(rej) - 1 : g;
+    const unsigned bad = __ballot_sync(kFull, lane < g && !valid);
+    if (lane == 0) {
+      int f = sq.flags;
+      if (m < g && ((bad >> m) & 1u)) f |= SPEC_ST_BAD_DRAFT;
+      sm.m = m;
+      sm.flags = f;
+    }
+  }
+  __syncthreads();
+  const int m = sm.m;
+  if (!sq.sampling) {
+    for (int i = tid; i <= gmax; i += kThreads) {
+      int v = -1;
+      if (i < m) v = a.draft_tokens[int64_t(b) * gmax + i];
+      else if (i == m) v = sm.rowArg[m];
+      a.out_tokens[int64_t(b) * (gmax + 1) + i] = v;
+    }
+    if (a.diag)
+      for (int i = tid; i < 2 * gmax + 1; i += kThreads) a.diag[int64_t(b) * (2 * gmax + 1) + i] = NAN;
+    if (tid == 0) {
+      a.num_accepted[b] = m;
+      if (a.status) a.status[b] = sm.flags;
+      w.cnt[b] = 0;
+    }
+    return;
+  }
+  if (a.diag) {
+    float* dg = a.diag + int64_t(b) * (2 * gmax + 1);
+    for (int i = tid; i < gmax; i += kThreads) {
+      dg[2 * i] = i < g ? sm.pd[i] : NAN;
+      dg[2 * i + 1] = i < g ? sm.qd[i] : NAN;
+    }
+  }
+  if (tid == 0) {
+    PlanRec pr;
+    pr.m = m;
+    pr.g = g;
+    pr.flags = sm.flags;
+    pr.pair = m < g ? 1 : 0;
+    pr.mkp = __fmul_rn(sm.rowM[m], k);
+    pr.invp = sm.rowInvS[m];
+    const int qs = gmax + 1 + m;
+    pr.mkq = pr.pair ? __fmul_rn(sm.rowM[qs], k) : 0.f;
+    pr.invq = pr.pair ? sm.rowInvS[qs] : 0.f;
+    w.plan[b] = pr;
+    w.cnt[b] = 0;
+    __threadfence();
+    atomicExch(&w.ready[b], 1);
+  }
+}
+
+// weights of one vector of the draw row: w = residual (or p on the bonus row), and p
+template <class E, bool kVec>
+__device__ __forceinline__ void vec_weights(const typename E::raw* rp, const typename E::raw* rq, bool pair, int64_t e,
+                                            int64_t hi, float k, const PlanRec& pl, float (&w)[E::kPerVec],
+                                            float (&p)[E::kPerVec]) {
+  constexpr int N = E::kPerVec;
+  if constexpr (kVec) {
+    if (e < hi) {
+      const uint4 vp = ld_stream(rp + e);
+      const uint4 vq = pair ? ld_stream(rq + e) : vp;
+#pragma unroll
+      for (int j = 0; j < N; ++j) {
+        p[j] = prob(E::get(vp, j), k, pl.mkp, pl.invp);
+        w[j] = pair ? residual(p[j], prob(E::get(vq, j), k, pl.mkq, pl.invq)) : p[j];
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < N; ++j) w[j] = p[j] = 0.f;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      if (e + j < hi) {
+        p[j] = prob(E::at(rp, e + j), k, pl.mkp, pl.invp);
+        w[j] = pair ? residual(p[j], prob(E::at(rq, e + j), k, pl.mkq, pl.invq)) : p[j];
+      } else {
+        w[j] = p[j] = 0.f;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// selector: locate u*R among the chunk masses, rescan that chunk, write the outputs
+// ------------------------------------------------------------------------------------------
+
+template <class E, bool kVec, bool kMixed>
+__device__ void select(const Args& a, const Geo& geo, const Work& w, const Seq<E, kMixed>& sq, Shared& sm) {
+  using raw = typename E::raw;
+  constexpr int N = E::kPerVec;
+  constexpr int kPass = kThreads * kVecPerPass * N;
+  const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
+  const int b = sq.b, gmax = a.gmax, CL = geo.CL;
+  __threadfence();
+  const PlanRec& pl = sm.plan;
+  const bool pair = pl.pair != 0;
+  if (tid == 0) {
+    const float2* ms = w.mass + int64_t(b) * CL;
+    float R = 0.f, Pm = 0.f;
+    for (int c = 0; c < CL; ++c) {
+      const float2 x = __ldcg(&ms[c]);
+      R = __fadd_rn(R, x.x);
+      Pm = __fadd_rn(Pm, x.y);
+    }
+    const bool use_w = !pair || R > 0.f;   // bonus: the weights are p itself
+    int f = pl.flags;
+    if (!use_w) f |= SPEC_ST_R_ZERO | kInternalDrawP;
+    const float total = use_w ? R : Pm;
+    const float target = __fmul_rn(a.u_sample[b], total);
+    int owner = -1, last = 0;
+    float excl = 0.f, run = 0.f, excl_last = 0.f;
+    for (int c = 0; c < CL; ++c) {
+      const float2 x = __ldcg(&ms[c]);
+      const float wc = use_w ? x.x : x.y;
+      if (wc > 0.f) { last = c; excl_last = run; }
+      const float nr = __fadd_rn(run, wc);
+      if (owner < 0 && nr > target && wc > 0.f) { owner = c; excl = run; }
+      run = nr;
+    }
+    if (owner < 0) { owner = last; excl = excl_last; }
+    sm.owner = owner;
+    sm.flags = f;
+    sm.target_local = __fsub_rn(target, excl);
+    sm.mass_out = pair ? (use_w ? R : 0.f) : R;
+  }
+  __syncthreads();
+  const bool draw_p = !pair || (sm.flags & kInternalDrawP);
+  const int64_t lo = int64_t(sm.owner) * geo.chunk;
+  const int64_t hi = lo + geo.chunk < a.V ? lo + geo.chunk : a.V;
+  const raw* rp = sq.P + int64_t(pl.m) * a.V;
+  const raw* rq = pair ? sq.Q + int64_t(pl.m) * a.V : nullptr;
+  const int npass = int((hi - lo + kPass - 1) / kPass);
+  const int slices = npass * kVecPerPass;
+  for (int ps = 0; ps < npass; ++ps)
+#pragma unroll
+    for (int q = 0; q < kVecPerPass; ++q) {
+      float wv[N], pv[N];
+      vec_weights<E, kVec>(rp, rq, pair, lo + int64_t(ps) * kPass + int64_t(q * kThreads + tid) * N, hi, sq.k, pl, wv, pv);
+      float s = 0.f;
+#pragma unroll
+      for (int j = 0; j < N; ++j) s = __fadd_rn(s, draw_p ? pv[j] : wv[j]);
+      sm.vs[ps * kVecPerPass + q][tid] = s;
+    }
+  // per-(slice, warp) sums; slice-major, warp-minor is ascending vocabulary order
+  for (int s = 0; s < slices; ++s) {
+    const float x = warp_sum(sm.vs[s][tid]);
+    if (lane == 0) sm.wsum[s][warp] = x;
+  }
+  __syncthreads();
+  const float tl = sm.target_local;
+  if (tid == 0) {
+    int ss = -1, sw = 0, ls = 0, lw = 0;
+    float run = 0.f, base = 0.f, base_last = 0.f;
+    for (int s = 0; s < slices && ss < 0; ++s)
+      for (int wi = 0; wi < kWarps; ++wi) {
+        const float x = sm.wsum[s][wi];
+        if (x > 0.f) { ls = s; lw = wi; base_last = run; }
+        const float nr = __fadd_rn(run, x);
+        if (nr > tl && x > 0.f) { ss = s; sw = wi; base = run; break; }
+        run = nr;
+      }
+    if (ss < 0) { ss = ls; sw = lw; base = base_last; }
+    sm.slice = ss;
+    sm.warp_sel = sw;
+    sm.run_sel = base;
+    sm.token = int(lo);
+  }
+  __syncthreads();
+  if (warp == sm.warp_sel) {
+    const int s = sm.slice;
+    const float x = sm.vs[s][tid];
+    float incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl = __fadd_rn(incl, y);
+    }
+    const float base = sm.run_sel;
+    const unsigned hit = __ballot_sync(kFull, x > 0.f && __fadd_rn(base, incl) > tl);
+    const unsigned pos = __ballot_sync(kFull, x > 0.f);
+    const int sel = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
+    if (lane == sel) {
+      const int ps = s / kVecPerPass, q = s - ps * kVecPerPass;
+      const int64_t e = lo + int64_t(ps) * kPass + int64_t(q * kThreads + tid) * N;
+      float wv[N], pv[N];
+      vec_weights<E, kVec>(rp, rq, pair, e, hi, sq.k, pl, wv, pv);
+      float r = __fsub_rn(__fadd_rn(base, incl), x);
+      int tok = -1, lastpos = -1;
+#pragma unroll
+      for (int j = 0; j < N; ++j) {
+        const float wj = draw_p ? pv[j] : wv[j];
+        r = __fadd_rn(r, wj);
+        if (wj > 0.f) {
+          lastpos = int(e) + j;
+          if (tok < 0 && r > tl) tok = int(e) + j;
+        }
+      }
+      sm.token = tok >= 0 ? tok : (lastpos >= 0 ? lastpos : int(lo));
+    }
+  }
+  __syncthreads();
+  const int m = pl.m, tok = sm.token;
+  for (int i = tid; i <= gmax; i += kThreads) {
+    int v = -1;
+    if (i < m) v = a.draft_tokens[int64_t(b) * gmax + i];
+    else if (i == m) v = tok;
+    a.out_tokens[int64_t(b) * (gmax + 1) + i] = v;
+  }
+  if (tid == 0) {
+    if (a.diag) a.diag[int64_t(b) * (2 * gmax + 1) + 2 * gmax] = sm.mass_out;
+    a.num_accepted[b] = m;
+    if (a.status) a.status[b] = sm.flags & 0xff;
+    w.ready[b] = 0;
+    w.bdone[b] = 0;
+  }
 }
 
 // ------------------------------------------------------------------------------------------
@@ -350,462 +606,125 @@ __host__ __device__ inline Layout make_layout(int nslots, int cl, int slices) {
 // ------------------------------------------------------------------------------------------
 
 template <class E, bool kVec, bool kMixed>
-__global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Args a) {
+__global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Args a, const Geo geo, const Work w) {
   using raw = typename E::raw;
   constexpr int N = E::kPerVec;
-  constexpr int kPass = kThreads * kVecPerPass * N;     // elements per tile
-  extern __shared__ __align__(16) unsigned char dyn[];
-  __shared__ Fixed fx;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int CL = int(cluster.num_blocks());
-  const int rank = int(cluster.block_rank());
-  const int b = int(blockIdx.x) / CL;
-  const int tid = int(threadIdx.x);
-  const int lane = tid & 31, warp = tid >> 5;
+  constexpr int kPass = kThreads * kVecPerPass * N;
+  __shared__ Shared sm;
+  const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
 
-  // Split arrive: every block must be running before anyone writes into its shared memory.
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-
-  const int64_t V = a.V;
-  const int gmax = a.gmax;
-  const int nslots = 2 * gmax + 1;                      // target rows 0..gmax, draft rows after
-  const int qslot = gmax + 1;
-  int g = a.num_draft ? a.num_draft[b] : gmax;
-  int flags = 0;
-  if (g < 0 || g > gmax) {
-    g = g < 0 ? 0 : gmax;
-    flags |= SPEC_ST_CLAMPED_GAMMA;
-  }
-  float T = 0.f;
-  if constexpr (kMixed) T = a.temperature[b];
-  const bool sampling = kMixed && (T > 0.f);
-  const float k = sampling ? kLog2e / T : 0.f;
-
-  const raw* P = static_cast<const raw*>(a.target) + int64_t(b) * (gmax + 1) * V;
-  const raw* Q = sampling ? static_cast<const raw*>(a.draft) + int64_t(b) * gmax * V : nullptr;
-  const int64_t lo = int64_t(rank) * a.chunk;
-  const int64_t hi = lo + a.chunk < V ? lo + a.chunk : V;
-  const int npass = hi > lo ? int((hi - lo + kPass - 1) / kPass) : 0;
-  const int slices = npass * kVecPerPass;
-  // the layout must be identical in every block of the cluster (blocks write into each
-  // other's shared memory), so it is sized by the full chunk, not by this block's share
-  const int slices_max = int((a.chunk + kPass - 1) / kPass) * kVecPerPass;
-  const Layout L = make_layout(nslots, CL, slices_max);
-  float2* all = reinterpret_cast<float2*>(dyn + L.all);
-  float2* wpart = reinterpret_cast<float2*>(dyn + L.wpart);
-  float2* local = reinterpret_cast<float2*>(dyn + L.local);
-  float* rowM = reinterpret_cast<float*>(dyn + L.rowM);
-  float* rowInvS = reinterpret_cast<float*>(dyn + L.rowInvS);
-  int* rowArg = reinterpret_cast<int*>(dyn + L.rowArg);
-
-  // Prefetch what the decision needs (draft ids, their logits, uniforms): lane i of warp 0
-  // owns draft i; the loads complete while phase A streams.
-  int d = -1;
-  bool dvalid = false;
-  float xp = 0.f, xq = 0.f, ua = 0.f;
-  if (warp == 0 && lane < g) {
-    d = a.draft_tokens[int64_t(b) * gmax + lane];
-    dvalid = d >= 0 && int64_t(d) < V;
-    if (sampling) {
-      if (dvalid) {
-        xp = E::at(P + int64_t(lane) * V, d);
-        xq = E::at(Q + int64_t(lane) * V, d);
-      }
-      ua = a.u_accept[int64_t(b) * gmax + lane];
-    }
-  }
-
-  // ---------------- phase A: one streaming pass over this block's chunk of every row -----
-  // Row order: sampling [P_g, Q_{g-1}, P_{g-1}, ..., Q_0, P_0] (the rows a rejection most
-  // often needs -- small m -- are read last); greedy [P_g, ..., P_0].
-  const int nrows = sampling ? 2 * g + 1 : g + 1;
-  auto row_of = [&](int r, int& slot) -> const raw* {
-    if (!sampling || r == 0) {
-      const int i = g - r;
-      slot = i;
-      return P + int64_t(i) * V;
-    }
-    const int i = g - 1 - ((r - 1) >> 1);
-    if (r & 1) {
-      slot = qslot + i;
-      return Q + int64_t(i) * V;
-    }
-    slot = i;
-    return P + int64_t(i) * V;
-  };
-  const int ntiles = nrows * npass;
-  unsigned char* ring = dyn + L.ring;
-  auto issue = [&](int t) {
-    if constexpr (kVec) {
-      if (t < ntiles) {
-        const int r = t / npass, ps = t - r * npass;
-        int slot;
-        const raw* row = row_of(r, slot);
-        const int64_t e0 = lo + int64_t(ps) * kPass;
-        unsigned char* st = ring + (t % kStages) * kTileBytes;
-#pragma unroll
-        for (int q = 0; q < kVecPerPass; ++q) {
-          const int64_t e = e0 + int64_t(q * kThreads + tid) * N;
-          const bool in = e < hi;
-          cp_async16(st + (q * kThreads + tid) * 16,
-                     in ? static_cast<const void*>(row + e) : static_cast<const void*>(row), in ? 16 : 0);
-        }
-      }
-      cp_async_commit();
-    }
-  };
-  if constexpr (kVec) {
-#pragma unroll
-    for (int t = 0; t < kStages - 1; ++t) issue(t);
-  }
-  float rm = -INFINITY, rs = 0.f;   // running (max, sum) of a sampled row / argmax value
-  int ri = INT_MAX;                 // running argmax id of a greedy row
-  for (int t = 0; t < ntiles; ++t) {
-    const int r = t / npass, ps = t - r * npass;
-    int slot;
-    const raw* row = row_of(r, slot);
-    const int64_t e0 = lo + int64_t(ps) * kPass;
-    Tile<E, kVec> tile;
-    if constexpr (kVec) {
-      issue(t + kStages - 1);
-      cp_async_wait<kStages - 1>();
-      const unsigned char* st = ring + (t % kStages) * kTileBytes;
-#pragma unroll
-      for (int q = 0; q < kVecPerPass; ++q)
-        tile.v[q] = *reinterpret_cast<const uint4*>(st + (q * kThreads + tid) * 16);
-      if (e0 + kPass > hi) {
-        // partial tile: vectors q with e0 + (q*kThreads + tid)*N >= hi hold zero fill
-        const int64_t left = hi - e0 - int64_t(tid) * N;
-        const int nq = left <= 0 ? 0 : int((left + int64_t(kThreads) * N - 1) / (int64_t(kThreads) * N));
-        tile.mask_tail(nq);
-      }
-    } else {
-#pragma unroll
-      for (int q = 0; q < kVecPerPass; ++q) {
-        const int64_t e = e0 + int64_t(q * kThreads + tid) * N;
-#pragma unroll
-        for (int j = 0; j < N; ++j) tile.s[q * N + j] = (e + j < hi) ? E::at(row, e + j) : -INFINITY;
-      }
-    }
-    if (sampling) tile_stats(tile, k, rm, rs);
-    else tile_argmax(tile, e0, tid, rm, ri);
-    if (ps == npass - 1) {
-      if (!sampling) warp_argmax(rm, ri);
-      if (lane == 0) wpart[warp * nslots + slot] = make_float2(rm, sampling ? rs : __int_as_float(ri));
-      rm = -INFINITY;
-      rs = 0.f;
-      ri = INT_MAX;
-    }
-  }
-  if constexpr (kVec) cp_async_wait<0>();
-  if (npass == 0 && lane == 0) {
-    // empty chunk: empty partials
-    for (int r = 0; r < nrows; ++r) {
-      int slot;
-      row_of(r, slot);
-      wpart[warp * nslots + slot] = make_float2(-INFINITY, sampling ? 0.f : __int_as_float(INT_MAX));
-    }
+  // logical unit = ticket order; the last ticket of the launch resets the counter
+  if (tid == 0) {
+    const int u = atomicAdd(&w.ctrl[0], 1);
+    if (u == int(gridDim.x) - 1) w.ctrl[0] = 0;
+    sm.unit = u;
   }
   __syncthreads();
+  const int u = sm.unit;
+  const int grp = u / geo.G, off = u - grp * geo.G;
 
-  // block partial per row, warps merged in a fixed order
-  for (int r = tid; r < nrows; r += kThreads) {
-    int slot;
-    row_of(r, slot);
-    float2 acc = wpart[slot];
-    for (int w = 1; w < kWarps; ++w) {
-      const float2 p = wpart[w * nslots + slot];
-      if (sampling) merge_ms(acc.x, acc.y, p.x, p.y, k);
-      else if (better(p.x, __float_as_int(p.y), acc.x, __float_as_int(acc.y))) acc = p;
+  if (off < geo.NA) {
+    // ---------------- A unit: one chunk of one row ----------------------------------------
+    const int b = grp;
+    if (b >= a.B) return;
+    const int slot = off / geo.CL, c = off - slot * geo.CL;
+    const Seq<E, kMixed> sq(a, b);
+    if (!sq.slot_valid(slot, a.gmax)) return;
+    const raw* row = slot <= a.gmax ? sq.P + int64_t(slot) * a.V : sq.Q + int64_t(slot - a.gmax - 1) * a.V;
+    const int64_t lo = int64_t(c) * geo.chunk;
+    const int64_t hi = lo + geo.chunk < a.V ? lo + geo.chunk : a.V;
+    float rm = -INFINITY, rs = 0.f;
+    int ri = INT_MAX;
+    for (int64_t e0 = lo; e0 < hi; e0 += kPass) {
+      Tile<E, kVec> t;
+      t.load(row, e0, hi, tid);
+      if (sq.sampling) tile_stats(t, sq.k, rm, rs);
+      else tile_argmax(t, e0, tid, rm, ri);
     }
-    local[slot] = acc;
-  }
-  __syncthreads();
-
-  // ---------------- exchange 1: push the partials into every block of the cluster --------
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-  for (int idx = tid; idx < CL * nrows; idx += kThreads) {
-    const int c = idx / nrows, r = idx - c * nrows;
-    int slot;
-    row_of(r, slot);
-    float2* dst = cluster.map_shared_rank(&all[rank * nslots + slot], c);
-    *dst = local[slot];
-  }
-  cluster.sync();
-
-  // every block combines the C partials of each row in the same order -> identical results
-  for (int r = tid; r < nrows; r += kThreads) {
-    int slot;
-    row_of(r, slot);
-    if (sampling) {
-      float M = -INFINITY;
-      for (int c = 0; c < CL; ++c) M = fmaxf(M, all[c * nslots + slot].x);
-      float S = 0.f;
-      if (M != -INFINITY)
-        for (int c = 0; c < CL; ++c) {
-          const float2 p = all[c * nslots + slot];
-          if (p.x != -INFINITY) S = __fadd_rn(S, __fmul_rn(p.y, ex2(__fmul_rn(p.x - M, k))));
-        }
-      rowM[slot] = M;
-      rowInvS[slot] = __frcp_rn(S);
-    } else {
-      float bv = -INFINITY;
-      int bi = INT_MAX;
-      for (int c = 0; c < CL; ++c) {
-        const float2 p = all[c * nslots + slot];
-        if (better(p.x, __float_as_int(p.y), bv, bi)) { bv = p.x; bi = __float_as_int(p.y); }
+    if (!sq.sampling) warp_argmax(rm, ri);
+    if (lane == 0) sm.warp_part[warp] = make_float2(rm, sq.sampling ? rs : __int_as_float(ri));
+    __syncthreads();
+    if (tid == 0) {
+      float2 acc = sm.warp_part[0];
+      for (int wi = 1; wi < kWarps; ++wi) {
+        const float2 p = sm.warp_part[wi];
+        if (sq.sampling) merge_ms(acc.x, acc.y, p.x, p.y, sq.k);
+        else if (better(p.x, __float_as_int(p.y), acc.x, __float_as_int(acc.y))) acc = p;
       }
-      rowArg[slot] = bi;
-    }
-  }
-  __syncthreads();
-
-  // ---------------- acceptance flags and the first rejection (warp 0) -----------------------
-  if (warp == 0) {
-    bool acc = false;
-    if (lane < g) {
-      if (sampling) {
-        float p = NAN, q = NAN;
-        if (dvalid) {
-          p = prob(xp, k, __fmul_rn(rowM[lane], k), rowInvS[lane]);
-          q = prob(xq, k, __fmul_rn(rowM[qslot + lane], k), rowInvS[qslot + lane]);
-          // u < min(1, p/q): r = 0 when p = 0, r = +inf when q = 0 < p
-          acc = (p == 0.f) ? (ua < 0.f) : (p >= q ? (ua < 1.f) : (__fmul_rn(ua, q) < p));
-        }
-        fx.pd[lane] = p;
-        fx.qd[lane] = q;
-      } else {
-        acc = dvalid && d == rowArg[lane];
+      w.part[(int64_t(b) * geo.nslots + slot) * geo.CL + c] = acc;
+      // the logit at this row's draft id, if it falls in this chunk (sampling rows only)
+      const int i = slot <= a.gmax ? slot : slot - a.gmax - 1;
+      if (sq.sampling && i < sq.g) {
+        const int d = a.draft_tokens[int64_t(b) * a.gmax + i];
+        if (int64_t(d) >= lo && int64_t(d) < hi) w.xd[int64_t(b) * geo.nslots + slot] = E::at(row, d);
       }
+      __threadfence();
+      sm.last = atomicAdd(&w.cnt[b], 1) == sq.units(geo.CL) - 1;
     }
-    const unsigned keep = __ballot_sync(kFull, acc);
-    const unsigned rej = ~keep & (g >= 32 ? kFull : ((1u << g) - 1u));
-    const int m = rej ? __ffs(rej) - 1 : g;
-    const unsigned badmask = __ballot_sync(kFull, lane < g && !dvalid);
-    if (lane == 0) {
-      int f = flags;
-      if (m < g && ((badmask >> m) & 1u)) f |= SPEC_ST_BAD_DRAFT;
-      fx.m = m;
-      fx.flags = f;
-    }
-  }
-  __syncthreads();
-  const int m = fx.m;
-
-  if (!sampling) {
-    if (rank == 0) {
-      for (int i = tid; i <= gmax; i += kThreads) {
-        int v = -1;
-        if (i < m) v = a.draft_tokens[int64_t(b) * gmax + i];
-        else if (i == m) v = rowArg[m];
-        a.out_tokens[int64_t(b) * (gmax + 1) + i] = v;
-      }
-      if (a.diag)
-        for (int i = tid; i < 2 * gmax + 1; i += kThreads) a.diag[int64_t(b) * (2 * gmax + 1) + i] = NAN;
-      if (tid == 0) {
-        a.num_accepted[b] = m;
-        if (a.status) a.status[b] = fx.flags;
-      }
-    }
+    __syncthreads();
+    if (sm.last) decide<E, kMixed>(a, geo, w, sq, sm);
     return;
   }
 
-  // ---------------- phase B: chunk mass of the distribution the last token is drawn from ---
-  const bool pair = m < g;                 // rejection: residual of (p_m, q_m); else bonus p_g
-  const raw* rp = P + int64_t(m) * V;
-  const raw* rq = pair ? Q + int64_t(m) * V : nullptr;
-  const float mkp = __fmul_rn(rowM[m], k), invp = rowInvS[m];
-  const float mkq = pair ? __fmul_rn(rowM[qslot + m], k) : 0.f;
-  const float invq = pair ? rowInvS[qslot + m] : 0.f;
-  float* vsw = reinterpret_cast<float*>(dyn + L.vsw);   // per (slice, thread) weight sums
-  float* vsp = reinterpret_cast<float*>(dyn + L.vsp);   // per (slice, thread) p sums
-  // weights w (residual, or p on the bonus row) and p of one vector; elements past hi are 0
-  auto vec_weights = [&](int64_t e, float (&w)[N], float (&p)[N]) {
-    if constexpr (kVec) {
-      if (e < hi) {
-        const uint4 vp = ld_l2(rp + e);
-        const f2 k2 = pk(k, k), nmkp = pk(-mkp, -mkp), ip = pk(invp, invp);
-        if (pair) {
-          const uint4 vq = ld_l2(rq + e);
-          const f2 nmkq = pk(-mkq, -mkq), iq = pk(invq, invq);
-#pragma unroll
-          for (int j = 0; j < N / 2; ++j) {
-            const float2 pp = upk(prob2(E::pair(vp, j), k2, nmkp, ip));
-            const float2 qq = upk(prob2(E::pair(vq, j), k2, nmkq, iq));
-            p[2 * j] = pp.x;
-            p[2 * j + 1] = pp.y;
-            w[2 * j] = residual(pp.x, qq.x);
-            w[2 * j + 1] = residual(pp.y, qq.y);
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < N / 2; ++j) {
-            const float2 pp = upk(prob2(E::pair(vp, j), k2, nmkp, ip));
-            p[2 * j] = w[2 * j] = pp.x;
-            p[2 * j + 1] = w[2 * j + 1] = pp.y;
-          }
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < N; ++j) w[j] = p[j] = 0.f;
+  if constexpr (kMixed) {
+    // ---------------- B unit: one chunk of the draw row of sequence grp - delta -----------
+    const int b = grp - geo.delta;
+    if (b < 0 || b >= a.B) return;
+    const int c = off - geo.NA;
+    const Seq<E, kMixed> sq(a, b);
+    if (!sq.sampling) return;
+    if (tid == 0) {
+      // bounded wait for the decider of b (an A unit with a smaller ticket)
+      unsigned it = 0, ns = 32;
+      while (ld_acquire(&w.ready[b]) == 0 && ++it < kSpinLimit) {
+        __nanosleep(ns);
+        if (ns < 1024) ns <<= 1;
       }
-    } else {
+      sm.ok = it < kSpinLimit;
+      if (sm.ok) {
+        __threadfence();
+        sm.plan = w.plan[b];
+      } else if (a.status) {
+        atomicOr(&a.status[b], kStTimeout);
+      }
+    }
+    __syncthreads();
+    if (!sm.ok) return;
+    const PlanRec pl = sm.plan;
+    const bool pair = pl.pair != 0;
+    const raw* rp = sq.P + int64_t(pl.m) * a.V;
+    const raw* rq = pair ? sq.Q + int64_t(pl.m) * a.V : nullptr;
+    const int64_t lo = int64_t(c) * geo.chunk;
+    const int64_t hi = lo + geo.chunk < a.V ? lo + geo.chunk : a.V;
+    float ws = 0.f, ps = 0.f;
+    for (int64_t e0 = lo; e0 < hi; e0 += kPass)
 #pragma unroll
-      for (int j = 0; j < N; ++j) {
-        if (e + j < hi) {
-          p[j] = prob(E::at(rp, e + j), k, mkp, invp);
-          w[j] = pair ? residual(p[j], prob(E::at(rq, e + j), k, mkq, invq)) : p[j];
-        } else {
-          w[j] = p[j] = 0.f;
+      for (int q = 0; q < kVecPerPass; ++q) {
+        float wv[N], pv[N];
+        vec_weights<E, kVec>(rp, rq, pair, e0 + int64_t(q * kThreads + tid) * N, hi, sq.k, pl, wv, pv);
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+          ws = __fadd_rn(ws, wv[j]);
+          ps = __fadd_rn(ps, pv[j]);
         }
       }
-    }
-  };
-  float wsum = 0.f, psum = 0.f;
-  for (int ps = 0; ps < npass; ++ps) {
-    const int64_t e0 = lo + int64_t(ps) * kPass;
-#pragma unroll
-    for (int q = 0; q < kVecPerPass; ++q) {
-      float w[N], p[N];
-      vec_weights(e0 + int64_t(q * kThreads + tid) * N, w, p);
-      float sw = 0.f, sp = 0.f;
-#pragma unroll
-      for (int j = 0; j < N; ++j) {
-        sw = __fadd_rn(sw, w[j]);
-        sp = __fadd_rn(sp, p[j]);
+    ws = warp_sum(ws);
+    ps = warp_sum(ps);
+    if (lane == 0) sm.warp_part[warp] = make_float2(ws, ps);
+    __syncthreads();
+    if (tid == 0) {
+      float2 acc = sm.warp_part[0];
+      for (int wi = 1; wi < kWarps; ++wi) {
+        acc.x = __fadd_rn(acc.x, sm.warp_part[wi].x);
+        acc.y = __fadd_rn(acc.y, sm.warp_part[wi].y);
       }
-      const int s = ps * kVecPerPass + q;
-      vsw[s * kThreads + tid] = sw;
-      vsp[s * kThreads + tid] = sp;
-      wsum = __fadd_rn(wsum, sw);
-      psum = __fadd_rn(psum, sp);
+      if (!pair) acc.x = acc.y;
+      w.mass[int64_t(b) * geo.CL + c] = acc;
+      __threadfence();
+      sm.last = atomicAdd(&w.bdone[b], 1) == geo.CL - 1;
     }
-  }
-  wsum = warp_sum(wsum);
-  psum = warp_sum(psum);
-  if (lane == 0) fx.mass_warp[warp] = make_float2(wsum, psum);
-  __syncthreads();
-  if (tid < CL) {
-    float2 acc = fx.mass_warp[0];
-    for (int w = 1; w < kWarps; ++w) {
-      acc.x = __fadd_rn(acc.x, fx.mass_warp[w].x);
-      acc.y = __fadd_rn(acc.y, fx.mass_warp[w].y);
-    }
-    float2* dst = cluster.map_shared_rank(&fx.all_mass[rank], tid);
-    *dst = acc;
-  }
-  cluster.sync();
-
-  // ---------------- which chunk holds u * total (every block, same order) ------------------
-  if (tid == 0) {
-    float R = 0.f, Pm = 0.f;
-    for (int c = 0; c < CL; ++c) {
-      R = __fadd_rn(R, fx.all_mass[c].x);
-      Pm = __fadd_rn(Pm, fx.all_mass[c].y);
-    }
-    const bool use_w = !pair || R > 0.f;   // bonus: the weights are p itself
-    int f = fx.flags;
-    if (!use_w) f |= SPEC_ST_R_ZERO;
-    const float total = use_w ? R : Pm;
-    const float target = __fmul_rn(a.u_sample[b], total);
-    int owner = -1, last = 0;
-    float excl = 0.f, run = 0.f, excl_last = 0.f;
-    for (int c = 0; c < CL; ++c) {
-      const float w = use_w ? fx.all_mass[c].x : fx.all_mass[c].y;
-      if (w > 0.f) { last = c; excl_last = run; }
-      const float nr = __fadd_rn(run, w);
-      if (owner < 0 && nr > target && w > 0.f) { owner = c; excl = run; }
-      run = nr;
-    }
-    if (owner < 0) { owner = last; excl = excl_last; }
-    fx.owner = owner;
-    fx.flags = f | (use_w ? 0 : 0x100);   // 0x100: draw from p (internal)
-    fx.target_local = __fsub_rn(target, excl);
-    fx.mass_out = pair ? (use_w ? R : 0.f) : R;
-  }
-  __syncthreads();
-  if (rank != fx.owner) return;
-
-  // ---------------- owner block: locate the token from the per-vector sums -----------------
-  const bool draw_p = !pair || (fx.flags & 0x100);
-  const float* vs = draw_p ? vsp : vsw;
-  const float tl = fx.target_local;
-  // per-(slice, warp) sums; slice-major, warp-minor is ascending vocabulary order
-  for (int s = 0; s < slices; ++s) {
-    const float x = warp_sum(vs[s * kThreads + tid]);
-    if (lane == 0) fx.wsum[s][warp] = x;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int ss = -1, sw = 0, ls = 0, lw = 0;
-    float run = 0.f, base = 0.f, base_last = 0.f;
-    for (int s = 0; s < slices && ss < 0; ++s)
-      for (int w = 0; w < kWarps; ++w) {
-        const float x = fx.wsum[s][w];
-        if (x > 0.f) { ls = s; lw = w; base_last = run; }
-        const float nr = __fadd_rn(run, x);
-        if (nr > tl && x > 0.f) { ss = s; sw = w; base = run; break; }
-        run = nr;
-      }
-    if (ss < 0) { ss = ls; sw = lw; base = base_last; }
-    fx.slice = ss;
-    fx.warp_sel = sw;
-    fx.run_sel = base;
-    fx.token = int(lo);
-  }
-  __syncthreads();
-  if (warp == fx.warp_sel) {
-    const int s = fx.slice;
-    const float x = vs[s * kThreads + tid];
-    float incl = x;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(kFull, incl, o);
-      if (lane >= o) incl = __fadd_rn(incl, y);
-    }
-    const float base = fx.run_sel;
-    const unsigned hit = __ballot_sync(kFull, x > 0.f && __fadd_rn(base, incl) > tl);
-    const unsigned pos = __ballot_sync(kFull, x > 0.f);
-    const int sel = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
-    if (lane == sel) {
-      const int ps = s / kVecPerPass, q = s - ps * kVecPerPass;
-      const int64_t e = lo + int64_t(ps) * kPass + int64_t(q * kThreads + tid) * N;
-      float w[N], p[N];
-      vec_weights(e, w, p);
-      float r = __fsub_rn(__fadd_rn(base, incl), x);
-      int tok = -1, lastpos = -1;
-#pragma unroll
-      for (int j = 0; j < N; ++j) {
-        const float wj = draw_p ? p[j] : w[j];
-        r = __fadd_rn(r, wj);
-        if (wj > 0.f) {
-          lastpos = int(e) + j;
-          if (tok < 0 && r > tl) tok = int(e) + j;
-        }
-      }
-      fx.token = tok >= 0 ? tok : (lastpos >= 0 ? lastpos : int(lo));
-    }
-  }
-  __syncthreads();
-
-  const int tok = fx.token;
-  for (int i = tid; i <= gmax; i += kThreads) {
-    int v = -1;
-    if (i < m) v = a.draft_tokens[int64_t(b) * gmax + i];
-    else if (i == m) v = tok;
-    a.out_tokens[int64_t(b) * (gmax + 1) + i] = v;
-  }
-  if (a.diag) {
-    float* dg = a.diag + int64_t(b) * (2 * gmax + 1);
-    for (int i = tid; i < gmax; i += kThreads) {
-      dg[2 * i] = i < g ? fx.pd[i] : NAN;
-      dg[2 * i + 1] = i < g ? fx.qd[i] : NAN;
-    }
-    if (tid == 0) dg[2 * gmax] = fx.mass_out;
-  }
-  if (tid == 0) {
-    a.num_accepted[b] = m;
-    if (a.status) a.status[b] = fx.flags & 0xff;
+    __syncthreads();
+    if (sm.last) select<E, kVec, kMixed>(a, geo, w, sq, sm);
   }
 }
 
@@ -813,77 +732,121 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Args a) {
 // host side
 // ------------------------------------------------------------------------------------------
 
-struct Plan {
+struct Split {
   int cl;
   int chunk;
 };
 
-Plan make_plan(int64_t V) {
-  int cl = int((V + 4095) / 4096);
+Split make_split(int64_t V) {
+  int cl = int((V + kChunkTarget - 1) / kChunkTarget);
   if (cl < 1) cl = 1;
-  if (cl > kMaxCluster) cl = kMaxCluster;
+  if (cl > kMaxChunks) cl = kMaxChunks;
   int64_t c = (V + cl - 1) / cl;
   c = (c + 7) / 8 * 8;
-  return Plan{cl, int(c)};
+  return Split{cl, int(c)};
 }
 
-int slices_for(int64_t chunk, int dtype) {
-  const int64_t per_pass = int64_t(kThreads) * kVecPerPass * (dtype == SPEC_BF16 ? 8 : 4);
-  return int((chunk + per_pass - 1) / per_pass) * kVecPerPass;
+size_t align64(size_t x) { return (x + 63) & ~size_t(63); }
+
+struct WsLayout {
+  size_t ctrl, cnt, bdone, ready, plan, part, xd, mass, total;
+};
+
+WsLayout ws_layout(int B, int gmax, int64_t V) {
+  const Split s = make_split(V);
+  const size_t nslots = size_t(2 * gmax + 1);
+  WsLayout L;
+  size_t off = 0;
+  L.ctrl = off;
+  off = align64(off + 64);
+  L.cnt = off;
+  off = align64(off + size_t(B) * 4);
+  L.bdone = off;
+  off = align64(off + size_t(B) * 4);
+  L.ready = off;
+  off = align64(off + size_t(B) * 4);
+  L.plan = off;
+  off = align64(off + size_t(B) * sizeof(PlanRec));
+  L.part = off;
+  off = align64(off + size_t(B) * nslots * s.cl * 8);
+  L.xd = off;
+  off = align64(off + size_t(B) * nslots * 4);
+  L.mass = off;
+  off = align64(off + size_t(B) * s.cl * 8);
+  L.total = off;
+  return L;
 }
 
-std::mutex g_attr_mu;
+Work ws_views(void* ws, const WsLayout& L) {
+  unsigned char* p = static_cast<unsigned char*>(ws);
+  Work w;
+  w.ctrl = reinterpret_cast<int*>(p + L.ctrl);
+  w.cnt = reinterpret_cast<int*>(p + L.cnt);
+  w.bdone = reinterpret_cast<int*>(p + L.bdone);
+  w.ready = reinterpret_cast<int*>(p + L.ready);
+  w.plan = reinterpret_cast<PlanRec*>(p + L.plan);
+  w.part = reinterpret_cast<float2*>(p + L.part);
+  w.xd = reinterpret_cast<float*>(p + L.xd);
+  w.mass = reinterpret_cast<float2*>(p + L.mass);
+  return w;
+}
+
+std::mutex g_occ_mu;
 
 template <class E, bool kVec, bool kMixed>
-int launch(const Args& args, int B, int dtype, void* stream) {
+int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream) {
   auto fn = verify_kernel<E, kVec, kMixed>;
-  const Plan plan = make_plan(args.V);
-  const int slices = slices_for(plan.chunk, dtype);
-  if (slices > kMaxSlices) {
-    set_error("V=%lld too large: %d vocabulary slices per block (max %d)", (long long)args.V, slices,
-              kMaxSlices);
+  const Split sp = make_split(args.V);
+  const int64_t per_pass = int64_t(kThreads) * kVecPerPass * (dtype == SPEC_BF16 ? 8 : 4);
+  const int npass = int((sp.chunk + per_pass - 1) / per_pass);
+  if (npass > kMaxPasses) {
+    set_error("V=%lld too large: %d passes per chunk (max %d)", (long long)args.V, npass, kMaxPasses);
     return SPEC_ENOSPACE;
   }
-  const Layout L = make_layout(2 * args.gmax + 1, plan.cl, slices);
-  if (L.total > kMaxDynSmem) {
-    set_error("shared memory plan of %d bytes exceeds %d", L.total, kMaxDynSmem);
+  // host-only checks first: nothing is enqueued when they fail
+  const WsLayout L = ws_layout(args.B, args.gmax, args.V);
+  if (!ws || ws_bytes < L.total) {
+    set_error("workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, L.total);
     return SPEC_ENOSPACE;
   }
-  if (int64_t(B) * plan.cl > INT_MAX) {
-    set_error("B=%d too large for %d blocks per sequence", B, plan.cl);
-    return SPEC_ENOSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) % 64 != 0) {
+    set_error("workspace must be 64-byte aligned");
+    return SPEC_EINVAL;
   }
-  int dev = 0;
+  Geo geo;
+  geo.CL = sp.cl;
+  geo.chunk = sp.chunk;
+  geo.nslots = kMixed ? 2 * args.gmax + 1 : args.gmax + 1;   // greedy-only reads no draft rows
+  geo.NA = geo.nslots * geo.CL;
+  geo.G = geo.NA + (kMixed ? geo.CL : 0);
+  // B units of a sequence come about two waves of resident blocks after its A units
+  int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   {
-    // cluster sizes above 8 and dynamic shared memory above 48 KB need an opt-in; done once
-    // per device and kernel
-    static bool done[64] = {};
-    std::lock_guard<std::mutex> lk(g_attr_mu);
-    if (dev >= 64 || !done[dev]) {
-      e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(NonPortableClusterSizeAllowed)");
-      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)");
-      if (dev < 64) done[dev] = true;
+    static int cached[64] = {};
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    if (dev < 64 && cached[dev]) {
+      per_sm = cached[dev];
+    } else {
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, 0);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+      if (dev < 64) cached[dev] = per_sm;
     }
   }
-  Args a = args;
-  a.chunk = plan.chunk;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(B * plan.cl), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = size_t(L.total);
-  cfg.stream = static_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = unsigned(plan.cl);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, fn, a);
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  const int64_t resident = int64_t(sms) * (per_sm > 0 ? per_sm : 1);
+  geo.delta = kMixed ? int((2 * resident + geo.G - 1) / geo.G) : 0;
+  if (kMixed && geo.delta < 1) geo.delta = 1;
+  const int64_t blocks = (int64_t(args.B) + geo.delta) * geo.G;
+  if (blocks > INT_MAX) {
+    set_error("batch too large: %lld work units", (long long)blocks);
+    return SPEC_ENOSPACE;
+  }
+  const Work w = ws_views(ws, L);
+  fn<<<unsigned(blocks), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(args, geo, w);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "verify kernel launch");
   count_launch();
   return SPEC_OK;
@@ -917,11 +880,13 @@ bool vec_ok(const void* p, int dtype, int64_t V) {
 }
 
 template <bool kMixed>
-int dispatch_on(const Args& a, int dtype, int B, void* stream) {
+int dispatch_on(const Args& a, int dtype, void* ws, size_t ws_bytes, void* stream) {
   const bool vec = vec_ok(a.target, dtype, a.V) && vec_ok(a.draft, dtype, a.V);
   if (dtype == SPEC_BF16)
-    return vec ? launch<Bf16, true, kMixed>(a, B, dtype, stream) : launch<Bf16, false, kMixed>(a, B, dtype, stream);
-  return vec ? launch<F32, true, kMixed>(a, B, dtype, stream) : launch<F32, false, kMixed>(a, B, dtype, stream);
+    return vec ? launch<Bf16, true, kMixed>(a, dtype, ws, ws_bytes, stream)
+               : launch<Bf16, false, kMixed>(a, dtype, ws, ws_bytes, stream);
+  return vec ? launch<F32, true, kMixed>(a, dtype, ws, ws_bytes, stream)
+             : launch<F32, false, kMixed>(a, dtype, ws, ws_bytes, stream);
 }
 
 }  // namespace
@@ -929,10 +894,15 @@ int dispatch_on(const Args& a, int dtype, int B, void* stream) {
 
 using namespace specverify;
 
+extern "C" size_t spec_verify_workspace_bytes(int B, int gmax, int V, int dtype) {
+  if (B < 0 || gmax < 0 || gmax > SPEC_MAX_GAMMA || V < 1 || (dtype != SPEC_BF16 && dtype != SPEC_F32)) return 0;
+  return ws_layout(B, gmax, V).total;
+}
+
 extern "C" int spec_verify_greedy(const void* target_logits, int dtype, const int32_t* draft_tokens,
                                   const int32_t* num_draft, int B, int gmax, int V,
                                   int32_t* out_tokens, int32_t* num_accepted, int32_t* status,
-                                  void* stream) {
+                                  void* workspace, size_t workspace_bytes, void* stream) {
   clear_error();
   int rc = check_common(target_logits, dtype, draft_tokens, B, gmax, V, out_tokens, num_accepted);
   if (rc != SPEC_OK || B == 0) return rc;
@@ -941,11 +911,12 @@ extern "C" int spec_verify_greedy(const void* target_logits, int dtype, const in
   a.draft_tokens = draft_tokens;
   a.num_draft = num_draft;
   a.V = V;
+  a.B = B;
   a.gmax = gmax;
   a.out_tokens = out_tokens;
   a.num_accepted = num_accepted;
   a.status = status;
-  return dispatch_on<false>(a, dtype, B, stream);
+  return dispatch_on<false>(a, dtype, workspace, workspace_bytes, stream);
 }
 
 extern "C" int spec_verify_sample(const void* target_logits, const void* draft_logits, int dtype,
@@ -953,7 +924,8 @@ extern "C" int spec_verify_sample(const void* target_logits, const void* draft_l
                                   const float* temperature, const float* u_accept,
                                   const float* u_sample, int B, int gmax, int V,
                                   int32_t* out_tokens, int32_t* num_accepted, float* diag,
-                                  int32_t* status, void* stream) {
+                                  int32_t* status, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
   clear_error();
   int rc = check_common(target_logits, dtype, draft_tokens, B, gmax, V, out_tokens, num_accepted);
   if (rc != SPEC_OK) return rc;
@@ -971,12 +943,13 @@ extern "C" int spec_verify_sample(const void* target_logits, const void* draft_l
   a.u_accept = u_accept;
   a.u_sample = u_sample;
   a.V = V;
+  a.B = B;
   a.gmax = gmax;
   a.out_tokens = out_tokens;
   a.num_accepted = num_accepted;
   a.diag = diag;
   a.status = status;
-  return dispatch_on<true>(a, dtype, B, stream);
+  return dispatch_on<true>(a, dtype, workspace, workspace_bytes, stream);
 }
 
 extern "C" int spec_verify_plan(int V, int dtype, int* ctas_per_seq, int* chunk) {
@@ -985,7 +958,7 @@ extern "C" int spec_verify_plan(int V, int dtype, int* ctas_per_seq, int* chunk)
     set_error("bad arguments to spec_verify_plan");
     return SPEC_EINVAL;
   }
-  const Plan p = make_plan(V);
+  const Split p = make_split(V);
   *ctas_per_seq = p.cl;
   *chunk = p.chunk;
   return SPEC_OK;

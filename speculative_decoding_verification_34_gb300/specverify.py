@@ -42,10 +42,13 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                               "speculative_decoding_verification_34_gb300.build.build()")
     lib = ctypes.CDLL(p)
     vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int
-    lib.spec_verify_greedy.argtypes = [vp, i32, vp, vp, sz, sz, sz, vp, vp, vp, vp]
+    size_t = ctypes.c_size_t
+    lib.spec_verify_greedy.argtypes = [vp, i32, vp, vp, sz, sz, sz, vp, vp, vp, vp, size_t, vp]
     lib.spec_verify_greedy.restype = i32
-    lib.spec_verify_sample.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, sz, sz, sz, vp, vp, vp, vp, vp]
+    lib.spec_verify_sample.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, sz, sz, sz, vp, vp, vp, vp, vp, size_t, vp]
     lib.spec_verify_sample.restype = i32
+    lib.spec_verify_workspace_bytes.argtypes = [sz, sz, sz, i32]
+    lib.spec_verify_workspace_bytes.restype = size_t
     lib.spec_commit_kv_lengths.argtypes = [vp, sz, vp, vp, i32, vp, sz, vp, vp, sz, vp, vp]
     lib.spec_commit_kv_lengths.restype = i32
     lib.spec_last_error.argtypes = []
@@ -95,20 +98,41 @@ def _stream(stream) -> Optional[int]:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def spec_verify_workspace_bytes(B: int, gmax: int, V: int, dtype: int = SPEC_BF16) -> int:
+    return int(load_library().spec_verify_workspace_bytes(B, gmax, V, dtype))
+
+
+def alloc_workspace(B: int, gmax: int, V: int, dtype: int = SPEC_BF16, device=None) -> torch.Tensor:
+    """A zero-filled device workspace for verify calls of these sizes (reusable: every call
+    leaves it zero-filled; one call at a time)."""
+    n = spec_verify_workspace_bytes(B, gmax, V, dtype)
+    return torch.zeros(max(n, 64), dtype=torch.uint8, device=device or "cuda")
+
+
+def _ws(workspace, B, gmax, V, code, device):
+    if workspace is None:
+        workspace = alloc_workspace(B, gmax, V, code, device)
+    if workspace.dtype != torch.uint8:
+        raise TypeError("workspace must be a uint8 tensor")
+    return workspace, _ptr(workspace, "workspace"), workspace.numel()
+
+
 def spec_verify_greedy(target_logits: torch.Tensor, draft_tokens: torch.Tensor,
                        num_draft: Optional[torch.Tensor], out_tokens: torch.Tensor,
                        num_accepted: torch.Tensor, status: Optional[torch.Tensor] = None,
-                       stream=None) -> None:
+                       workspace: Optional[torch.Tensor] = None, stream=None) -> None:
     B, gp1, V = target_logits.shape
     gmax = gp1 - 1
     lib = load_library()
+    code = _dtype_code(target_logits)
+    ws, wsp, wsn = _ws(workspace, B, gmax, V, code, target_logits.device)
     _check(lib.spec_verify_greedy(
-        _ptr(target_logits, "target_logits"), _dtype_code(target_logits),
+        _ptr(target_logits, "target_logits"), code,
         _ptr(draft_tokens, "draft_tokens", torch.int32, (B, gmax)),
         _ptr(num_draft, "num_draft", torch.int32, (B,)), B, gmax, V,
         _ptr(out_tokens, "out_tokens", torch.int32, (B, gmax + 1)),
         _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
-        _ptr(status, "status", torch.int32, (B,)), _stream(stream)))
+        _ptr(status, "status", torch.int32, (B,)), wsp, wsn, _stream(stream)))
 
 
 def spec_verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor,
@@ -116,15 +140,17 @@ def spec_verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor,
                        temperature: torch.Tensor, u_accept: torch.Tensor, u_sample: torch.Tensor,
                        out_tokens: torch.Tensor, num_accepted: torch.Tensor,
                        diag: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
-                       stream=None) -> None:
+                       workspace: Optional[torch.Tensor] = None, stream=None) -> None:
     B, gp1, V = target_logits.shape
     gmax = gp1 - 1
     if draft_logits.dtype != target_logits.dtype:
         raise TypeError("target and draft logits must have the same dtype")
     lib = load_library()
+    code = _dtype_code(target_logits)
+    ws, wsp, wsn = _ws(workspace, B, gmax, V, code, target_logits.device)
     _check(lib.spec_verify_sample(
         _ptr(target_logits, "target_logits"),
-        _ptr(draft_logits, "draft_logits", None, (B, gmax, V)), _dtype_code(target_logits),
+        _ptr(draft_logits, "draft_logits", None, (B, gmax, V)), code,
         _ptr(draft_tokens, "draft_tokens", torch.int32, (B, gmax)),
         _ptr(num_draft, "num_draft", torch.int32, (B,)),
         _ptr(temperature, "temperature", torch.float32, (B,)),
@@ -191,10 +217,11 @@ class _Prepared:
 
 def prepare_verify_sample(target_logits, draft_logits, draft_tokens, num_draft, temperature,
                           u_accept, u_sample, out_tokens, num_accepted, diag=None, status=None,
-                          stream=None) -> _Prepared:
+                          workspace=None, stream=None) -> _Prepared:
     B, gp1, V = target_logits.shape
     gmax = gp1 - 1
     lib = load_library()
+    ws, wsp, wsn = _ws(workspace, B, gmax, V, _dtype_code(target_logits), target_logits.device)
     args = (_ptr(target_logits, "target_logits"),
             _ptr(draft_logits, "draft_logits", target_logits.dtype, (B, gmax, V)),
             _dtype_code(target_logits),
@@ -206,9 +233,9 @@ def prepare_verify_sample(target_logits, draft_logits, draft_tokens, num_draft, 
             _ptr(out_tokens, "out_tokens", torch.int32, (B, gmax + 1)),
             _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
             _ptr(diag, "diag", torch.float32, (B, 2 * gmax + 1)),
-            _ptr(status, "status", torch.int32, (B,)), _stream(stream))
+            _ptr(status, "status", torch.int32, (B,)), wsp, wsn, _stream(stream))
     keep = (target_logits, draft_logits, draft_tokens, num_draft, temperature, u_accept,
-            u_sample, out_tokens, num_accepted, diag, status)
+            u_sample, out_tokens, num_accepted, diag, status, ws)
     return _Prepared(lib.spec_verify_sample, args, keep)
 
 

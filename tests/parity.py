@@ -37,6 +37,22 @@ def canary_ok(buf, n, fill) -> bool:
     return bool((tail == fill).all())
 
 
+_WS = {}
+
+
+def workspace(B, g, V, code):
+    """A zero-filled workspace reused across calls (each call must leave it zero-filled)."""
+    n = sv.spec_verify_workspace_bytes(B, g, V, code)
+    key = torch.cuda.current_device()
+    if key not in _WS or _WS[key].numel() < n:
+        _WS[key] = torch.zeros(max(n, 64), dtype=torch.uint8, device="cuda")
+    return _WS[key]
+
+
+def workspace_is_clean() -> bool:
+    return all(bool((w == 0).all()) for w in _WS.values())
+
+
 def run_gpu(wl, mode: str = "auto", target=None, draft=None, check_canary=True):
     """Run one verify call on a Workload.  mode: 'greedy' (spec_verify_greedy) or 'sample'."""
     if mode == "auto":
@@ -49,13 +65,17 @@ def run_gpu(wl, mode: str = "auto", target=None, draft=None, check_canary=True):
     mb, macc = padded((B,), torch.int32, SENT_I)
     sb, st = padded((B,), torch.int32, SENT_I)
     db, dg = padded((B, 2 * g + 1), torch.float32, float("nan"))
+    code = sv.SPEC_BF16 if wl.dtype == "bf16" else sv.SPEC_F32
+    ws = workspace(B, g, wl.V, code)
     if mode == "greedy":
-        sv.spec_verify_greedy(tgt, toks, nd, out, macc, st)
+        sv.spec_verify_greedy(tgt, toks, nd, out, macc, st, workspace=ws)
     else:
         drf = dev(wl.draft) if draft is None else draft
         sv.spec_verify_sample(tgt, drf, toks, nd, dev(wl.temperature), dev(wl.u_accept),
-                              dev(wl.u_sample), out, macc, dg, st)
+                              dev(wl.u_sample), out, macc, dg, st, workspace=ws)
     torch.cuda.synchronize()
+    if check_canary:
+        assert workspace_is_clean(), "the call did not leave its workspace zero-filled"
     if check_canary:
         assert canary_ok(ob, B * (g + 1), SENT_I), "out_tokens overrun"
         assert canary_ok(mb, B, SENT_I), "num_accepted overrun"

@@ -41,12 +41,12 @@ FAKE = 0x10000  # never dereferenced: every call below fails its checks before a
 
 
 def greedy(lib, target=FAKE, dtype=0, toks=FAKE, B=4, gmax=3, V=100, out=FAKE, macc=FAKE):
-    return lib.spec_verify_greedy(target, dtype, toks, None, B, gmax, V, out, macc, None, None)
+    return lib.spec_verify_greedy(target, dtype, toks, None, B, gmax, V, out, macc, None, FAKE, 1 << 30, None)
 
 
 def sample(lib, target=FAKE, draft=FAKE, dtype=0, temp=FAKE, ua=FAKE, us=FAKE, B=4, gmax=3, V=100):
     return lib.spec_verify_sample(target, draft, dtype, FAKE, None, temp, ua, us, B, gmax, V,
-                                  FAKE, FAKE, None, None, None)
+                                  FAKE, FAKE, None, None, FAKE, 1 << 30, None)
 
 
 def test_host_argument_checks(lib):
@@ -81,9 +81,22 @@ def test_host_argument_checks(lib):
 def test_plan_splits_vocabulary(lib):
     for V in [1, 3, 1024, 4096, 4097, 32000, 50000, 128256, 151936, 1 << 20]:
         cl, chunk = sv.spec_verify_plan(V)
-        assert 1 <= cl <= 16 and chunk % 8 == 0
+        assert 1 <= cl <= 64 and chunk % 8 == 0
         assert cl * chunk >= V and (cl - 1) * chunk < V, (V, cl, chunk)
     assert sv.spec_verify_plan(128256) == (16, 8016)
-    assert sv.spec_verify_plan(151936) == (16, 9496)
+    assert sv.spec_verify_plan(151936) == (19, 8000)
+
+
+def test_workspace_size(lib):
+    n = sv.spec_verify_workspace_bytes(128, 4, 128256)
+    # counters, plans, per-(row, chunk) partials, draft logits, chunk masses
+    assert n >= 128 * (9 * 16 * 8 + 16 * 8 + 9 * 4 + 3 * 4 + 32)
+    assert n < 1 << 20
+    assert sv.spec_verify_workspace_bytes(128, 4, 128256) == sv.spec_verify_workspace_bytes(128, 4, 128256, 1)
+    assert sv.spec_verify_workspace_bytes(-1, 4, 100) == 0
+    assert sv.spec_verify_workspace_bytes(4, 40, 100) == 0
+    # too small a workspace is refused on the host, before any CUDA call
+    assert lib.spec_verify_greedy(FAKE, 0, FAKE, None, 4, 3, 100, FAKE, FAKE, None, FAKE, 8, None) == 3
+    assert b"workspace" in lib.spec_last_error()
     with pytest.raises(sv.SpecVerifyError):
         sv.spec_verify_plan(0)
