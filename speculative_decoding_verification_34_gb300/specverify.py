@@ -159,7 +159,7 @@ def spec_verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor,
         _ptr(out_tokens, "out_tokens", torch.int32, (B, gmax + 1)),
         _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
         _ptr(diag, "diag", torch.float32, (B, 2 * gmax + 1)),
-        _ptr(status, "status", torch.int32, (B,)), _stream(stream)))
+        _ptr(status, "status", torch.int32, (B,)), wsp, wsn, _stream(stream)))
 
 
 def _commit_gmax(out_tokens, gmax):

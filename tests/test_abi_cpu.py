@@ -100,3 +100,19 @@ def test_workspace_size(lib):
     assert b"workspace" in lib.spec_last_error()
     with pytest.raises(sv.SpecVerifyError):
         sv.spec_verify_plan(0)
+
+
+def test_binding_arity_matches_header(lib):
+    """The ctypes argument lists of the binding match the parameter lists in include/."""
+    text = ""
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text += re.sub(r"/\*.*?\*/", "", open(h, encoding="utf-8").read(), flags=re.S)
+    for name in ("spec_verify_greedy", "spec_verify_sample", "spec_commit_kv_lengths",
+                 "spec_verify_workspace_bytes", "spec_verify_plan"):
+        m = re.search(r"\b" + name + r"\s*\(([^)]*)\)", text)
+        params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
+        assert len(getattr(lib, name).argtypes) == len(params), name
+    # the prepared call marshals the same argument list
+    import inspect
+    src = inspect.getsource(sv.prepare_verify_sample)
+    assert "wsp, wsn" in src
