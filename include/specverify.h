@@ -15,10 +15,11 @@
  *    default stream) and returns.  Results are valid once the stream reaches that point.
  *  - The verify calls take a caller-owned device WORKSPACE of at least
  *    spec_verify_workspace_bytes(B, gmax, V, dtype) bytes, 64-byte aligned, which must be
- *    zero-filled before its first use.  Every completed call leaves it zero-filled again, so
- *    one workspace serves any number of successive calls; calls that may run at the same time
- *    (different streams) need different workspaces.  A workspace is sized for (B, gmax, V):
- *    a larger one may be passed for smaller calls.
+ *    zero-filled before its first use.  Every completed call returns the workspace's counters
+ *    (its first bytes) to zero, so one workspace serves any number of successive calls; the
+ *    rest holds scratch values that each call overwrites before reading.  Calls that may run
+ *    at the same time (different streams) need different workspaces.  A workspace sized for
+ *    (B, gmax, V) also serves smaller calls.
  *  - Arrays are row-major and contiguous:
  *        target_logits [B][gmax+1][V]   row i judges draft i; row 0 is the target's saved
  *                                       prediction for the position after the committed

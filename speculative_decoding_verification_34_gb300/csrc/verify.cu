@@ -24,8 +24,8 @@
 //                 The last B unit of b to finish is the *selector*: it locates the chunk
 //                 holding u*R, rescans that chunk and writes the outputs.
 //
-// Every call leaves the workspace zero-filled again (each counter is reset by the unit that
-// consumed it last), so a zero-filled workspace can serve successive calls on one stream.
+// Every call returns the workspace's counters to zero (each is reset by the unit that consumed
+// it last), so a zero-filled workspace can serve successive calls on one stream.
 
 #include <cuda_bf16.h>
 

@@ -104,7 +104,7 @@ def spec_verify_workspace_bytes(B: int, gmax: int, V: int, dtype: int = SPEC_BF1
 
 def alloc_workspace(B: int, gmax: int, V: int, dtype: int = SPEC_BF16, device=None) -> torch.Tensor:
     """A zero-filled device workspace for verify calls of these sizes (reusable: every call
-    leaves it zero-filled; one call at a time)."""
+    returns its counters to zero; one call at a time)."""
     n = spec_verify_workspace_bytes(B, gmax, V, dtype)
     return torch.zeros(max(n, 64), dtype=torch.uint8, device=device or "cuda")
 

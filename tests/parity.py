@@ -41,7 +41,7 @@ _WS = {}
 
 
 def workspace(B, g, V, code):
-    """A zero-filled workspace reused across calls (each call must leave it zero-filled)."""
+    """A zero-filled workspace reused across calls (each call must return its counters to 0)."""
     n = sv.spec_verify_workspace_bytes(B, g, V, code)
     key = torch.cuda.current_device()
     if key not in _WS or _WS[key].numel() < n:
@@ -49,8 +49,14 @@ def workspace(B, g, V, code):
     return _WS[key]
 
 
-def workspace_is_clean() -> bool:
-    return all(bool((w == 0).all()) for w in _WS.values())
+def counter_bytes(B):
+    """Bytes at the start of a workspace holding its counters: a 64-byte control word, then
+    three 64-byte-aligned int32 arrays of length B (arrivals, draw arrivals, plan flags)."""
+    return 64 + 3 * ((4 * B + 63) // 64 * 64)
+
+
+def workspace_is_clean(B) -> bool:
+    return all(bool((w[: counter_bytes(B)] == 0).all()) for w in _WS.values())
 
 
 def run_gpu(wl, mode: str = "auto", target=None, draft=None, check_canary=True):
@@ -75,7 +81,7 @@ def run_gpu(wl, mode: str = "auto", target=None, draft=None, check_canary=True):
                               dev(wl.u_sample), out, macc, dg, st, workspace=ws)
     torch.cuda.synchronize()
     if check_canary:
-        assert workspace_is_clean(), "the call did not leave its workspace zero-filled"
+        assert workspace_is_clean(B), "the call did not return the workspace counters to zero"
     if check_canary:
         assert canary_ok(ob, B * (g + 1), SENT_I), "out_tokens overrun"
         assert canary_ok(mb, B, SENT_I), "num_accepted overrun"
