@@ -15,11 +15,11 @@
  *    default stream) and returns.  Results are valid once the stream reaches that point.
  *  - The verify calls take a caller-owned device WORKSPACE of at least
  *    spec_verify_workspace_bytes(B, gmax, V, dtype) bytes, 64-byte aligned, which must be
- *    zero-filled before its first use.  Every completed call returns the workspace's counters
- *    (its first bytes) to zero, so one workspace serves any number of successive calls; the
- *    rest holds scratch values that each call overwrites before reading.  Calls that may run
- *    at the same time (different streams) need different workspaces.  A workspace sized for
- *    (B, gmax, V) also serves smaller calls.
+ *    zero-filled before its first use.  Its first eighth holds counters that every completed
+ *    call returns to zero; the rest holds scratch values that each call writes before reading.
+ *    So one workspace serves any number of successive calls of any sizes it fits, provided
+ *    every call passes the same workspace_bytes for it.  Calls that may run at the same time
+ *    (different streams) need different workspaces.
  *  - Arrays are row-major and contiguous:
  *        target_logits [B][gmax+1][V]   row i judges draft i; row 0 is the target's saved
  *                                       prediction for the position after the committed

@@ -691,6 +691,10 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Args a, const
     __syncthreads();
     if (!sm.ok) return;
     const PlanRec pl = sm.plan;
+    if (pl.m < 0 || pl.m > sq.g || (pl.pair && pl.m >= sq.g)) {   // never for a well-formed workspace; keeps reads in bounds
+      if (tid == 0 && a.status) atomicOr(&a.status[b], kStTimeout);
+      return;
+    }
     const bool pair = pl.pair != 0;
     const raw* rp = sq.P + int64_t(pl.m) * a.V;
     const raw* rq = pair ? sq.Q + int64_t(pl.m) * a.V : nullptr;
@@ -748,33 +752,60 @@ Split make_split(int64_t V) {
 
 size_t align64(size_t x) { return (x + 63) & ~size_t(63); }
 
+// Workspace layout.  The counters live in a header, the first eighth of the workspace (a
+// function of workspace_bytes alone); the scratch lives after it.  Any call's scratch is
+// therefore disjoint from any call's counters, whatever sizes successive calls use, and the
+// counters (all zero between calls) stay valid.
 struct WsLayout {
-  size_t ctrl, cnt, bdone, ready, plan, part, xd, mass, total;
+  size_t ctrl, cnt, bdone, ready, plan, part, xd, mass, header, scratch_end;
 };
 
-WsLayout ws_layout(int B, int gmax, int64_t V) {
+size_t counter_bytes(int B) { return 64 + 3 * align64(size_t(B) * 4); }
+
+size_t scratch_bytes(int B, int gmax, int64_t V) {
+  const Split s = make_split(V);
+  const size_t nslots = size_t(2 * gmax + 1);
+  return align64(size_t(B) * sizeof(PlanRec)) + align64(size_t(B) * nslots * s.cl * 8) +
+         align64(size_t(B) * nslots * 4) + align64(size_t(B) * s.cl * 8);
+}
+
+size_t header_for(size_t ws_bytes) { return (ws_bytes / 8) & ~size_t(63); }
+
+WsLayout ws_layout(int B, int gmax, int64_t V, size_t ws_bytes) {
   const Split s = make_split(V);
   const size_t nslots = size_t(2 * gmax + 1);
   WsLayout L;
-  size_t off = 0;
-  L.ctrl = off;
-  off = align64(off + 64);
-  L.cnt = off;
-  off = align64(off + size_t(B) * 4);
-  L.bdone = off;
-  off = align64(off + size_t(B) * 4);
-  L.ready = off;
-  off = align64(off + size_t(B) * 4);
+  L.header = header_for(ws_bytes);
+  L.ctrl = 0;
+  L.cnt = 64;
+  L.bdone = L.cnt + align64(size_t(B) * 4);
+  L.ready = L.bdone + align64(size_t(B) * 4);
+  size_t off = L.header;
   L.plan = off;
-  off = align64(off + size_t(B) * sizeof(PlanRec));
+  off += align64(size_t(B) * sizeof(PlanRec));
   L.part = off;
-  off = align64(off + size_t(B) * nslots * s.cl * 8);
+  off += align64(size_t(B) * nslots * s.cl * 8);
   L.xd = off;
-  off = align64(off + size_t(B) * nslots * 4);
+  off += align64(size_t(B) * nslots * 4);
   L.mass = off;
-  off = align64(off + size_t(B) * s.cl * 8);
-  L.total = off;
+  off += align64(size_t(B) * s.cl * 8);
+  L.scratch_end = off;
   return L;
+}
+
+bool ws_fits(int B, int gmax, int64_t V, size_t ws_bytes) {
+  return counter_bytes(B) <= header_for(ws_bytes) &&
+         header_for(ws_bytes) + scratch_bytes(B, gmax, V) <= ws_bytes;
+}
+
+// smallest workspace (a multiple of 64 bytes) that fits a call of these sizes
+size_t ws_required(int B, int gmax, int64_t V) {
+  const size_t c = counter_bytes(B), sc = scratch_bytes(B, gmax, V);
+  size_t w = align64(8 * (c + 64));
+  const size_t w2 = align64((sc + 64) * 8 / 7 + 64);
+  if (w2 > w) w = w2;
+  while (!ws_fits(B, gmax, V, w)) w += 64;
+  return w;
 }
 
 Work ws_views(void* ws, const WsLayout& L) {
@@ -804,11 +835,12 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
     return SPEC_ENOSPACE;
   }
   // host-only checks first: nothing is enqueued when they fail
-  const WsLayout L = ws_layout(args.B, args.gmax, args.V);
-  if (!ws || ws_bytes < L.total) {
-    set_error("workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, L.total);
+  if (!ws || !ws_fits(args.B, args.gmax, args.V, ws_bytes)) {
+    set_error("workspace of %zu bytes is smaller than the %zu bytes needed", ws ? ws_bytes : size_t(0),
+              ws_required(args.B, args.gmax, args.V));
     return SPEC_ENOSPACE;
   }
+  const WsLayout L = ws_layout(args.B, args.gmax, args.V, ws_bytes);
   if (reinterpret_cast<uintptr_t>(ws) % 64 != 0) {
     set_error("workspace must be 64-byte aligned");
     return SPEC_EINVAL;
@@ -896,7 +928,7 @@ using namespace specverify;
 
 extern "C" size_t spec_verify_workspace_bytes(int B, int gmax, int V, int dtype) {
   if (B < 0 || gmax < 0 || gmax > SPEC_MAX_GAMMA || V < 1 || (dtype != SPEC_BF16 && dtype != SPEC_F32)) return 0;
-  return ws_layout(B, gmax, V).total;
+  return ws_required(B, gmax, V);
 }
 
 extern "C" int spec_verify_greedy(const void* target_logits, int dtype, const int32_t* draft_tokens,

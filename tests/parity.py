@@ -49,14 +49,9 @@ def workspace(B, g, V, code):
     return _WS[key]
 
 
-def counter_bytes(B):
-    """Bytes at the start of a workspace holding its counters: a 64-byte control word, then
-    three 64-byte-aligned int32 arrays of length B (arrivals, draw arrivals, plan flags)."""
-    return 64 + 3 * ((4 * B + 63) // 64 * 64)
-
-
-def workspace_is_clean(B) -> bool:
-    return all(bool((w[: counter_bytes(B)] == 0).all()) for w in _WS.values())
+def workspace_is_clean() -> bool:
+    """The counter header (the first eighth of a workspace) is zero again after a call."""
+    return all(bool((w[: (w.numel() // 8) // 64 * 64] == 0).all()) for w in _WS.values())
 
 
 def run_gpu(wl, mode: str = "auto", target=None, draft=None, check_canary=True):
@@ -81,7 +76,7 @@ def run_gpu(wl, mode: str = "auto", target=None, draft=None, check_canary=True):
                               dev(wl.u_sample), out, macc, dg, st, workspace=ws)
     torch.cuda.synchronize()
     if check_canary:
-        assert workspace_is_clean(B), "the call did not return the workspace counters to zero"
+        assert workspace_is_clean(), "the call did not return the workspace counters to zero"
     if check_canary:
         assert canary_ok(ob, B * (g + 1), SENT_I), "out_tokens overrun"
         assert canary_ok(mb, B, SENT_I), "num_accepted overrun"

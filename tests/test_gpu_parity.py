@@ -260,3 +260,32 @@ def test_binding_rejects_bad_tensors():
 
 def dev(a):
     return parity.dev(a)
+
+
+def test_workspace_reuse_across_sizes():
+    """One zero-filled workspace serves calls of different sizes in any order."""
+    big = W.sampling_workload("ws-big", cfg=15, seed=0, B=96, gmax=6, V=40000, dtype="bf16",
+                              target_sigma=3.0, draft_scale=1.0, draft_sigma=1.0, temperature=0.9)
+    small = W.sampling_workload("ws-small", cfg=16, seed=0, B=5, gmax=2, V=3000, dtype="bf16",
+                                target_sigma=3.0, draft_scale=1.0, draft_sigma=1.0, temperature=1.1)
+    mid = W.sampling_workload("ws-mid", cfg=17, seed=0, B=40, gmax=8, V=9000, dtype="bf16",
+                              target_sigma=3.0, draft_scale=1.0, draft_sigma=1.0, temperature=0.7,
+                              greedy_mask=(np.arange(40) % 3) == 0)
+    n = max(sv.spec_verify_workspace_bytes(w.B, w.gmax, w.V) for w in (big, small, mid))
+    ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    for wl in (small, big, mid, small, big):
+        B, g = wl.B, wl.gmax
+        out = torch.empty((B, g + 1), dtype=torch.int32, device="cuda")
+        macc = torch.empty(B, dtype=torch.int32, device="cuda")
+        st = torch.empty(B, dtype=torch.int32, device="cuda")
+        dg = torch.empty((B, 2 * g + 1), dtype=torch.float32, device="cuda")
+        sv.spec_verify_sample(dev(wl.target), dev(wl.draft), dev(wl.draft_tokens), dev(wl.num_draft),
+                              dev(wl.temperature), dev(wl.u_accept), dev(wl.u_sample), out, macc, dg, st,
+                              workspace=ws)
+        torch.cuda.synchronize()
+        assert bool((ws[: (n // 8) // 64 * 64] == 0).all())
+        gpu = {"out": out.cpu().numpy(), "m": macc.cpu().numpy(), "status": st.cpu().numpy(),
+               "diag": dg.cpu().numpy()}
+        res = parity.oracle_results(wl)
+        _, _, differ = parity.compare(wl, gpu, res)
+        assert len(differ) <= 1
