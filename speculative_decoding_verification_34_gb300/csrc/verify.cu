@@ -1005,6 +1005,9 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
     if (dev < 64 && cached[dev]) {
       per_sm = cached[dev];
     } else {
+      // ring + static shared memory exceed the 48 KB a block gets without this opt-in
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)");
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem);
       if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
       if (per_sm < 1) {
