@@ -1,27 +1,30 @@
-// Greedy / sampling verification as one persistent grid working through logical units.
+// Greedy / sampling verification as one grid of independent work units.
 //
 // What is computed follows the tutorial "投机解码教程：从概率保持、KV Cache 回滚到性能盈亏平衡"
 // (§3-§4 greedy verification and logit alignment, §7.1-§7.3 acceptance min(1,p/q), residual
 // max(p-q,0)/R and the bonus draw) and the "M013" knowledge-base card (§03-§05, including the
 // R = 0 remark).  How it is computed is this library's own design for sm_103a.
 //
-// The vocabulary of every row is cut into CL chunks of `chunk` ids.  The work is a list of
-// block-sized units in a fixed logical order:
+// The vocabulary of every row is cut into CL chunks of `chunk` ids.  One launch runs two kinds
+// of block-sized work units, in a logical order that every block draws from a ticket counter
+// (so a unit only ever waits for units with smaller tickets, which are already running or
+// finished -- forward progress does not depend on the hardware's dispatch order):
 //
-//   A(b, row, c)  streams chunk c of one valid row of sequence b from HBM (128-bit cp.async
-//                 into a shared-memory ring, one ex2 per sampled element) and writes a
-//                 (max, sum 2^((x-max)k)) partial, or an (argmax value, id) partial for greedy
-//                 rows, to the workspace; the unit whose chunk holds a draft id also records
-//                 that logit.  The last A unit of b to arrive (a counter) makes its block the
-//                 *decider* of b: it combines the partials in a fixed order, takes the
-//                 acceptance decisions, finds m, and either writes the greedy result or
-//                 publishes a plan for the final draw.
+//   A(b, c)       streams chunk c of every row sequence b reads, once, from HBM (tiles of
+//                 16 KB through a per-thread cp.async ring in shared memory, one ex2 per
+//                 sampled element) and writes, per row, a (max, sum 2^((x-max)k)) partial, or
+//                 an (argmax value, id) partial for greedy rows, to the workspace; the logit at
+//                 each draft id is taken from the registers that hold it.  The last A unit of b
+//                 to finish (an arrival counter) is the *decider*: it combines the partials in
+//                 a fixed order, takes the acceptance decisions, finds m, and either writes the
+//                 greedy result or publishes a plan for the final draw.
 //   B(b, c)       waits (bounded) for b's plan, re-reads chunk c of the row the last token is
 //                 drawn from -- row m of p and q after a rejection, the bonus row otherwise;
-//                 these units come about two rounds of the grid after b's A units, so the
-//                 rows are normally still in L2 -- and writes the chunk's residual and p
-//                 masses.  The last B unit of b to arrive makes its block the *selector*: it
-//                 locates the chunk holding u*R, rescans that chunk and writes the outputs.
+//                 these units come about one and a half scheduling waves after b's A units, so
+//                 the rows are normally still in L2 -- and writes the chunk's residual and p
+//                 masses.
+//                 The last B unit of b to finish is the *selector*: it locates the chunk
+//                 holding u*R, rescans that chunk and writes the outputs.
 //
 // Every call returns the workspace's counters to zero (each is reset by the unit that consumed
 // it last), so a zero-filled workspace can serve successive calls on one stream.
@@ -41,7 +44,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kVecPerPass = 4;                         // 16-byte vectors per thread per pass
 constexpr int kMaxChunks = 64;                         // chunks per row
-constexpr int kStages = 3;                             // cp.async ring depth (A-unit tiles)
+constexpr int kStages = 3;                             // cp.async ring depth (tiles)
 constexpr int kTileBytes = kThreads * kVecPerPass * 16;
 constexpr int kMaxPasses = 4;                          // passes per chunk
 constexpr int kMaxSlices = kMaxPasses * kVecPerPass;
@@ -70,11 +73,9 @@ struct Args {
 };
 
 struct Geo {
-  int total;   // logical units: (B + delta) groups of G
-  int CL;      // chunks per row
+  int CL;      // chunks per row (= A units per sequence)
   int chunk;   // ids per chunk (multiple of 8)
   int nslots;  // row slots per sequence: target rows 0..gmax, then draft rows 0..gmax-1
-  int NA;      // A units per sequence (nslots * CL)
   int G;       // units per group: the A units of sequence g, then the B units of g - delta
   int delta;   // B units of sequence b sit in group b + delta
 };
@@ -295,13 +296,14 @@ __device__ __forceinline__ void tile_argmax(const Tile<E, kVec>& t, int64_t e0, 
 }
 
 struct Shared {
-  float2 wp[kWarps];                       // per-warp partials of the current unit
+  float2 wpart[kWarps][2 * SPEC_MAX_GAMMA + 1];   // per-warp partial of every row slot
+  float2 wp[kWarps];
   float rowM[2 * SPEC_MAX_GAMMA + 1];
   float rowInvS[2 * SPEC_MAX_GAMMA + 1];
   int rowArg[SPEC_MAX_GAMMA + 1];
   float pd[SPEC_MAX_GAMMA], qd[SPEC_MAX_GAMMA];
-  float wsum[kMaxSlices][kWarps];          // selector: per-(slice, warp) weight sums
-  int decide_b, last, ok, m, flags, owner, slice, warp_sel, token;
+  float wsum[kMaxSlices][kWarps];                 // selector: per-(slice, warp) weight sums
+  int unit, last, ok, m, flags, owner, slice, warp_sel, token;
   float target_local, mass_out, run_sel;
   PlanRec plan;
 };
@@ -338,33 +340,18 @@ struct Seq {
     if (slot <= gmax) return slot <= g;
     return sampling && slot - gmax - 1 < g;
   }
-  __device__ __forceinline__ int units(int CL) const { return CL * (sampling ? 2 * g + 1 : g + 1); }
+  __device__ __forceinline__ int nrows() const { return sampling ? 2 * g + 1 : g + 1; }
+  // r-th row read, in the order [P_g, Q_{g-1}, P_{g-1}, ..., Q_0, P_0] (sampling) or
+  // [P_g, ..., P_0] (greedy): the rows a rejection most often needs (small m) come last
+  __device__ __forceinline__ int slot_of(int r, int gmax) const {
+    if (!sampling || r == 0) return g - r;
+    const int i = g - 1 - ((r - 1) >> 1);
+    return (r & 1) ? gmax + 1 + i : i;
+  }
   __device__ __forceinline__ const raw* row(int slot, int gmax, int64_t V) const {
     return slot <= gmax ? P + int64_t(slot) * V : Q + int64_t(slot - gmax - 1) * V;
   }
 };
-
-// A logical unit: kind 0 = nothing, 1 = A(b, slot, c), 2 = B(b, c).
-struct Unit {
-  int kind, b, slot, c;
-};
-
-__device__ __forceinline__ Unit decode(int u, const Geo& geo, int B) {
-  Unit x;
-  const int grp = u / geo.G, off = u - grp * geo.G;
-  if (off < geo.NA) {
-    x.kind = grp < B ? 1 : 0;
-    x.b = grp;
-    x.slot = off / geo.CL;
-    x.c = off - x.slot * geo.CL;
-  } else {
-    x.b = grp - geo.delta;
-    x.kind = (x.b >= 0 && x.b < B) ? 2 : 0;
-    x.slot = 0;
-    x.c = off - geo.NA;
-  }
-  return x;
-}
 
 // ------------------------------------------------------------------------------------------
 // decider: combine the partials of sequence b, decide, publish
@@ -647,16 +634,8 @@ __device__ void select(const Args& a, const Geo& geo, const Work& w, const Seq<E
 }
 
 // ------------------------------------------------------------------------------------------
-// the kernel: persistent blocks, static schedule
+// the kernel
 // ------------------------------------------------------------------------------------------
-//
-// Block j processes the logical units j, j + R, j + 2R, ... in order (R = blocks in the grid,
-// all co-resident: the launch is cooperative).  A unit waits only in B units, and only for A
-// units with smaller indices, so the smallest unfinished unit can always finish: forward
-// progress holds.  A units' tiles are fetched kStages-1 A units ahead through a per-thread
-// cp.async ring in shared memory (each thread reads back only what it copied itself, so the
-// ring needs no block barrier).  The arrival that may make a block the decider of a sequence
-// is resolved one unit later (hiding the atomic's latency), and always before any wait.
 
 template <class E, bool kVec, bool kMixed>
 __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Args a, const Geo geo, const Work w) {
@@ -666,213 +645,180 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Args a, const
   extern __shared__ __align__(16) unsigned char ring[];
   __shared__ Shared sm;
   const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
-  const int R = int(gridDim.x);
-  const int total = geo.total;
 
-  // next valid A unit at or after u on this block's stride
-  auto next_a = [&](int u) -> int {
-    for (; u < total; u += R) {
-      const Unit x = decode(u, geo, a.B);
-      if (x.kind != 1) continue;
-      const Seq<E, kMixed> sq(a, x.b);
-      if (sq.slot_valid(x.slot, a.gmax)) return u;
-    }
-    return total;
-  };
-  // issue the ring stage for A unit u (vector path); always commits one group
-  int issued = 0;
-  auto issue = [&](int u) {
-    if constexpr (kVec) {
-      if (u < total) {
-        const Unit x = decode(u, geo, a.B);
-        const Seq<E, kMixed> sq(a, x.b);
-        const raw* row = sq.row(x.slot, a.gmax, a.V);
-        const int64_t lo = int64_t(x.c) * geo.chunk;
-        const int64_t hi = lo + geo.chunk < a.V ? lo + geo.chunk : a.V;
-        unsigned char* st = ring + (issued % kStages) * kTileBytes;
-#pragma unroll
-        for (int q = 0; q < kVecPerPass; ++q) {
-          const int64_t e = lo + int64_t(q * kThreads + tid) * N;
-          const bool in = e < hi;
-          cp_async16(st + (q * kThreads + tid) * 16, in ? static_cast<const void*>(row + e) : static_cast<const void*>(row),
-                     in ? 16 : 0);
-        }
-      }
-      cp_async_commit();
-      ++issued;
-    }
-  };
-
-  int u_issue = blockIdx.x;
-  if constexpr (kVec) {
-    for (int s = 0; s < kStages - 1; ++s) {
-      u_issue = next_a(u_issue);
-      issue(u_issue);
-      if (u_issue < total) u_issue += R;
-    }
+  // logical unit = ticket order; the last ticket of the launch resets the counter
+  if (tid == 0) {
+    const int u = atomicAdd(&w.ctrl[0], 1);
+    if (u == int(gridDim.x) - 1) w.ctrl[0] = 0;
+    sm.unit = u;
   }
-  int consumed = 0;
-  // pending arrival of this block's last A unit (thread 0 only)
-  int pend_b = -1, pend_old = 0, pend_need = 0;
-  auto resolve = [&]() {   // thread 0: did the pending arrival make this block the decider?
-    int db = -1;
-    if (pend_b >= 0 && pend_old == pend_need - 1) db = pend_b;
-    pend_b = -1;
-    return db;
-  };
+  __syncthreads();
+  const int u = sm.unit;
+  const int grp = u / geo.G, off = u - grp * geo.G;
 
-  for (int u = blockIdx.x; u < total; u += R) {
-    const Unit x = decode(u, geo, a.B);
-    if (x.kind == 1) {
-      // ---------------- A unit: one chunk of one row ------------------------------------
-      const Seq<E, kMixed> sq(a, x.b);
-      if (!sq.slot_valid(x.slot, a.gmax)) continue;
-      const raw* row = sq.row(x.slot, a.gmax, a.V);
-      const int64_t lo = int64_t(x.c) * geo.chunk;
-      const int64_t hi = lo + geo.chunk < a.V ? lo + geo.chunk : a.V;
-      const int i = x.slot <= a.gmax ? x.slot : x.slot - a.gmax - 1;
-      const int d = (sq.sampling && i < sq.g) ? __ldg(&a.draft_tokens[int64_t(x.b) * a.gmax + i]) : -1;
-      float rm = -INFINITY, rs = 0.f;
-      int ri = INT_MAX;
-      for (int64_t e0 = lo; e0 < hi; e0 += kPass) {
-        Tile<E, kVec> t;
-        if constexpr (kVec) {
-          // one ring stage holds the unit's first pass; further passes (long chunks) are loaded directly
-          if (e0 == lo) {
-            u_issue = next_a(u_issue);
-            issue(u_issue);
-            if (u_issue < total) u_issue += R;
-            cp_async_wait<kStages - 1>();
-            const unsigned char* st = ring + (consumed % kStages) * kTileBytes;
-#pragma unroll
-            for (int q = 0; q < kVecPerPass; ++q) {
-              t.v[q] = *reinterpret_cast<const uint4*>(st + (q * kThreads + tid) * 16);
-              if (e0 + int64_t(q * kThreads + tid) * N >= hi) t.v[q] = make_uint4(E::kNegInf, E::kNegInf, E::kNegInf, E::kNegInf);
-            }
-            ++consumed;
-          } else {
-            t.load(row, e0, hi, tid);
-          }
-        } else {
-          t.load(row, e0, hi, tid);
-        }
-        // the logit at the draft id, taken from the registers that hold it
-        if (d >= 0) {
+  if (off < geo.CL) {
+    // ---------------- A unit: chunk c of every row sequence b reads -----------------------
+    const int b = grp;
+    if (b >= a.B) return;
+    const int c = off;
+    const Seq<E, kMixed> sq(a, b);
+    const int64_t lo = int64_t(c) * geo.chunk;
+    const int64_t hi = lo + geo.chunk < a.V ? lo + geo.chunk : a.V;
+    const int npass = int((hi - lo + kPass - 1) / kPass);
+    const int nrows = sq.nrows();
+    const int ntiles = nrows * npass;
+    // tiles stream through a per-thread cp.async ring: each thread reads back only the
+    // vectors it copied itself, so the ring needs no block barrier
+    auto issue = [&](int t) {
+      if constexpr (kVec) {
+        if (t < ntiles) {
+          const int r = t / npass, ps = t - r * npass;
+          const raw* row = sq.row(sq.slot_of(r, a.gmax), a.gmax, a.V);
+          const int64_t e0 = lo + int64_t(ps) * kPass;
+          unsigned char* st = ring + (t % kStages) * kTileBytes;
 #pragma unroll
           for (int q = 0; q < kVecPerPass; ++q) {
-            const int64_t off = int64_t(d) - (e0 + int64_t(q * kThreads + tid) * N);
-            if (off >= 0 && off < N && int64_t(d) < hi) {
-              w.xd[int64_t(x.b) * geo.nslots + x.slot] = t.x(q, int(off));
-              __threadfence();
+            const int64_t e = e0 + int64_t(q * kThreads + tid) * N;
+            const bool in = e < hi;
+            cp_async16(st + (q * kThreads + tid) * 16, in ? static_cast<const void*>(row + e) : static_cast<const void*>(row),
+                       in ? 16 : 0);
+          }
+        }
+        cp_async_commit();
+      }
+    };
+    if constexpr (kVec) {
+#pragma unroll
+      for (int t = 0; t < kStages - 1; ++t) issue(t);
+    }
+    float rm = -INFINITY, rs = 0.f;
+    int ri = INT_MAX;
+    for (int t = 0; t < ntiles; ++t) {
+      const int r = t / npass, ps = t - r * npass;
+      const int slot = sq.slot_of(r, a.gmax);
+      const raw* row = sq.row(slot, a.gmax, a.V);
+      const int64_t e0 = lo + int64_t(ps) * kPass;
+      Tile<E, kVec> tile;
+      if constexpr (kVec) {
+        issue(t + kStages - 1);
+        cp_async_wait<kStages - 1>();
+        const unsigned char* st = ring + (t % kStages) * kTileBytes;
+#pragma unroll
+        for (int q = 0; q < kVecPerPass; ++q) {
+          tile.v[q] = *reinterpret_cast<const uint4*>(st + (q * kThreads + tid) * 16);
+          if (e0 + int64_t(q * kThreads + tid) * N >= hi) tile.v[q] = make_uint4(E::kNegInf, E::kNegInf, E::kNegInf, E::kNegInf);
+        }
+      } else {
+        tile.load(row, e0, hi, tid);
+      }
+      if (sq.sampling) {
+        // the logit at this row's draft id, taken from the registers that hold it
+        const int i = slot <= a.gmax ? slot : slot - a.gmax - 1;
+        if (i < sq.g) {
+          const int d = __ldg(&a.draft_tokens[int64_t(b) * a.gmax + i]);
+          if (int64_t(d) >= e0 && int64_t(d) < hi) {
+#pragma unroll
+            for (int q = 0; q < kVecPerPass; ++q) {
+              const int64_t o = int64_t(d) - (e0 + int64_t(q * kThreads + tid) * N);
+              if (o >= 0 && o < N) w.xd[int64_t(b) * geo.nslots + slot] = tile.x(q, int(o));
             }
           }
         }
-        if (sq.sampling) tile_stats(t, sq.k, rm, rs);
-        else tile_argmax(t, e0, tid, rm, ri);
+        tile_stats(tile, sq.k, rm, rs);
+      } else {
+        tile_argmax(tile, e0, tid, rm, ri);
       }
-      if (!sq.sampling) warp_argmax(rm, ri);
-      if (lane == 0) sm.wp[warp] = make_float2(rm, sq.sampling ? rs : __int_as_float(ri));
-      if (tid == 0) sm.decide_b = resolve();
-      __syncthreads();
-      const int db = sm.decide_b;
-      if (tid == 0) {
-        float2 acc = sm.wp[0];
-        for (int wi = 1; wi < kWarps; ++wi) {
-          const float2 p = sm.wp[wi];
-          if (sq.sampling) merge_ms(acc.x, acc.y, p.x, p.y, sq.k);
-          else if (better(p.x, __float_as_int(p.y), acc.x, __float_as_int(acc.y))) acc = p;
-        }
-        w.part[(int64_t(x.b) * geo.nslots + x.slot) * geo.CL + x.c] = acc;
-        pend_old = atom_add_acq_rel(&w.cnt[x.b], 1);
-        pend_b = x.b;
-        pend_need = sq.units(geo.CL);
+      if (ps == npass - 1) {
+        if (!sq.sampling) warp_argmax(rm, ri);
+        if (lane == 0) sm.wpart[warp][slot] = make_float2(rm, sq.sampling ? rs : __int_as_float(ri));
+        rm = -INFINITY;
+        rs = 0.f;
+        ri = INT_MAX;
       }
-      __syncthreads();   // sm.wp and sm.decide_b are free again after this barrier
-      if (db >= 0) {
-        const Seq<E, kMixed> ds(a, db);
-        decide<E, kMixed>(a, geo, w, ds, sm);
-      }
-      continue;
     }
-    if constexpr (kMixed) {
-      if (x.kind != 2) continue;
-      // ---------------- B unit: one chunk of the draw row of sequence b --------------------
-      const Seq<E, kMixed> sq(a, x.b);
-      if (!sq.sampling) continue;
-      // settle this block's own pending arrival before waiting on anyone
-      if (tid == 0) sm.decide_b = resolve();
-      __syncthreads();
-      const int db = sm.decide_b;
-      __syncthreads();
-      if (db >= 0) {
-        const Seq<E, kMixed> ds(a, db);
-        decide<E, kMixed>(a, geo, w, ds, sm);
+    if constexpr (kVec) cp_async_wait<0>();
+    __threadfence();   // the draft-id logits written above, before the arrival below
+    __syncthreads();
+    // block partial per row (warps merged in a fixed order), then the arrival
+    for (int r = tid; r < nrows; r += kThreads) {
+      const int slot = sq.slot_of(r, a.gmax);
+      float2 acc = sm.wpart[0][slot];
+      for (int wi = 1; wi < kWarps; ++wi) {
+        const float2 p = sm.wpart[wi][slot];
+        if (sq.sampling) merge_ms(acc.x, acc.y, p.x, p.y, sq.k);
+        else if (better(p.x, __float_as_int(p.y), acc.x, __float_as_int(acc.y))) acc = p;
       }
-      const int b = x.b, c = x.c;
-      if (tid == 0) {
-        // bounded wait for the decider of b (finished A units with smaller indices)
-        unsigned it = 0, ns = 32;
-        while (ld_acquire(&w.ready[b]) == 0 && ++it < kSpinLimit) {
-          __nanosleep(ns);
-          if (ns < 1024) ns <<= 1;
-        }
-        sm.ok = it < kSpinLimit;
-        if (sm.ok) {
-          __threadfence();
-          sm.plan = w.plan[b];
-          const PlanRec& pl = sm.plan;
-          // never fails for a well-formed workspace; keeps every read in bounds
-          if (pl.m < 0 || pl.m > sq.g || (pl.pair && pl.m >= sq.g)) sm.ok = 0;
-        }
-        if (!sm.ok && a.status) atomicOr(&a.status[b], kStTimeout);
-      }
-      __syncthreads();
-      if (!sm.ok) continue;
-      const PlanRec pl = sm.plan;
-      const bool pair = pl.pair != 0;
-      const raw* rp = sq.P + int64_t(pl.m) * a.V;
-      const raw* rq = pair ? sq.Q + int64_t(pl.m) * a.V : nullptr;
-      const int64_t lo = int64_t(c) * geo.chunk;
-      const int64_t hi = lo + geo.chunk < a.V ? lo + geo.chunk : a.V;
-      float ws = 0.f, ps = 0.f;
-      for (int64_t e0 = lo; e0 < hi; e0 += kPass)
-#pragma unroll
-        for (int q = 0; q < kVecPerPass; ++q) {
-          float wv[N], pv[N];
-          vec_weights<E, kVec>(rp, rq, pair, e0 + int64_t(q * kThreads + tid) * N, hi, sq.k, pl, wv, pv);
-#pragma unroll
-          for (int j = 0; j < N; ++j) {
-            ws = __fadd_rn(ws, wv[j]);
-            ps = __fadd_rn(ps, pv[j]);
-          }
-        }
-      ws = warp_sum(ws);
-      ps = warp_sum(ps);
-      if (lane == 0) sm.wp[warp] = make_float2(ws, ps);
-      __syncthreads();
-      if (tid == 0) {
-        float2 acc = sm.wp[0];
-        for (int wi = 1; wi < kWarps; ++wi) {
-          acc.x = __fadd_rn(acc.x, sm.wp[wi].x);
-          acc.y = __fadd_rn(acc.y, sm.wp[wi].y);
-        }
-        if (!pair) acc.x = acc.y;
-        w.mass[int64_t(b) * geo.CL + c] = acc;
-        sm.last = atom_add_acq_rel(&w.bdone[b], 1) == geo.CL - 1;
-      }
-      __syncthreads();
-      if (sm.last) select<E, kVec, kMixed>(a, geo, w, sq, sm);
+      w.part[(int64_t(b) * geo.nslots + slot) * geo.CL + c] = acc;
     }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) sm.last = atom_add_acq_rel(&w.cnt[b], 1) == geo.CL - 1;
+    __syncthreads();
+    if (sm.last) decide<E, kMixed>(a, geo, w, sq, sm);
+    return;
   }
-  // settle the last pending arrival
-  if (tid == 0) sm.decide_b = resolve();
-  __syncthreads();
-  const int db = sm.decide_b;
-  if (db >= 0) {
-    const Seq<E, kMixed> ds(a, db);
-    decide<E, kMixed>(a, geo, w, ds, sm);
+
+  if constexpr (kMixed) {
+    // ---------------- B unit: one chunk of the draw row of sequence grp - delta -----------
+    const int b = grp - geo.delta;
+    if (b < 0 || b >= a.B) return;
+    const int c = off - geo.CL;
+    const Seq<E, kMixed> sq(a, b);
+    if (!sq.sampling) return;
+    if (tid == 0) {
+      // bounded wait for the decider of b (an A unit with a smaller ticket)
+      unsigned it = 0, ns = 32;
+      while (ld_acquire(&w.ready[b]) == 0 && ++it < kSpinLimit) {
+        __nanosleep(ns);
+        if (ns < 1024) ns <<= 1;
+      }
+      sm.ok = it < kSpinLimit;
+      if (sm.ok) {
+        __threadfence();
+        sm.plan = w.plan[b];
+        const PlanRec& pl = sm.plan;
+        // never fails for a well-formed workspace; keeps every read in bounds
+        if (pl.m < 0 || pl.m > sq.g || (pl.pair && pl.m >= sq.g)) sm.ok = 0;
+      }
+      if (!sm.ok && a.status) atomicOr(&a.status[b], kStTimeout);
+    }
+    __syncthreads();
+    if (!sm.ok) return;
+    const PlanRec pl = sm.plan;
+    const bool pair = pl.pair != 0;
+    const raw* rp = sq.P + int64_t(pl.m) * a.V;
+    const raw* rq = pair ? sq.Q + int64_t(pl.m) * a.V : nullptr;
+    const int64_t lo = int64_t(c) * geo.chunk;
+    const int64_t hi = lo + geo.chunk < a.V ? lo + geo.chunk : a.V;
+    float ws = 0.f, ps = 0.f;
+    for (int64_t e0 = lo; e0 < hi; e0 += kPass)
+#pragma unroll
+      for (int q = 0; q < kVecPerPass; ++q) {
+        float wv[N], pv[N];
+        vec_weights<E, kVec>(rp, rq, pair, e0 + int64_t(q * kThreads + tid) * N, hi, sq.k, pl, wv, pv);
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+          ws = __fadd_rn(ws, wv[j]);
+          ps = __fadd_rn(ps, pv[j]);
+        }
+      }
+    ws = warp_sum(ws);
+    ps = warp_sum(ps);
+    if (lane == 0) sm.wp[warp] = make_float2(ws, ps);
+    __syncthreads();
+    if (tid == 0) {
+      float2 acc = sm.wp[0];
+      for (int wi = 1; wi < kWarps; ++wi) {
+        acc.x = __fadd_rn(acc.x, sm.wp[wi].x);
+        acc.y = __fadd_rn(acc.y, sm.wp[wi].y);
+      }
+      if (!pair) acc.x = acc.y;
+      w.mass[int64_t(b) * geo.CL + c] = acc;
+      sm.last = atom_add_acq_rel(&w.bdone[b], 1) == geo.CL - 1;
+    }
+    __syncthreads();
+    if (sm.last) select<E, kVec, kMixed>(a, geo, w, sq, sm);
   }
-  if constexpr (kVec) cp_async_wait<0>();
 }
 
 // ------------------------------------------------------------------------------------------
@@ -983,19 +929,18 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
               ws_required(args.B, args.gmax, args.V));
     return SPEC_ENOSPACE;
   }
+  const WsLayout L = ws_layout(args.B, args.gmax, args.V, ws_bytes);
   if (reinterpret_cast<uintptr_t>(ws) % 64 != 0) {
     set_error("workspace must be 64-byte aligned");
     return SPEC_EINVAL;
   }
-  const WsLayout L = ws_layout(args.B, args.gmax, args.V, ws_bytes);
   Geo geo;
   geo.CL = sp.cl;
   geo.chunk = sp.chunk;
   geo.nslots = kMixed ? 2 * args.gmax + 1 : args.gmax + 1;   // greedy-only reads no draft rows
-  geo.NA = geo.nslots * geo.CL;
-  geo.G = geo.NA + (kMixed ? geo.CL : 0);
+  geo.G = geo.CL + (kMixed ? geo.CL : 0);
   const size_t smem = kVec ? size_t(kStages) * kTileBytes : 0;
-  // persistent grid: every block co-resident (cooperative launch)
+  // B units of a sequence come about one and a half waves of resident blocks after its A units
   int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -1010,37 +955,22 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
       if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)");
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem);
       if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-      if (per_sm < 1) {
-        set_error("verify kernel does not fit on a multiprocessor");
-        return SPEC_ECUDA;
-      }
       if (dev < 64) cached[dev] = per_sm;
     }
   }
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-  const int64_t resident = int64_t(sms) * per_sm;
-  // B units of sequence b sit delta groups after its A units: about two rounds of the grid
-  geo.delta = kMixed ? int((geo.NA + 2 * resident + geo.G - 1) / geo.G) : 0;
-  const int64_t total = (int64_t(args.B) + geo.delta) * geo.G;
-  if (total > INT_MAX) {
-    set_error("batch too large: %lld work units", (long long)total);
+  const int64_t resident = int64_t(sms) * (per_sm > 0 ? per_sm : 1);
+  geo.delta = kMixed ? int((3 * resident / 2 + geo.G - 1) / geo.G) : 0;
+  if (kMixed && geo.delta < 1) geo.delta = 1;
+  const int64_t blocks = (int64_t(args.B) + geo.delta) * geo.G;
+  if (blocks > INT_MAX) {
+    set_error("batch too large: %lld work units", (long long)blocks);
     return SPEC_ENOSPACE;
   }
-  geo.total = int(total);
-  const int grid = int(total < resident ? total : resident);
   const Work w = ws_views(ws, L);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(grid), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = static_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, fn, args, geo, w);
+  fn<<<unsigned(blocks), kThreads, smem, static_cast<cudaStream_t>(stream)>>>(args, geo, w);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "verify kernel launch");
   count_launch();
   return SPEC_OK;
