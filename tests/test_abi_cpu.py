@@ -89,8 +89,8 @@ def test_plan_splits_vocabulary(lib):
 
 def test_workspace_size(lib):
     n = sv.spec_verify_workspace_bytes(128, 4, 128256)
-    # counters, plans, per-(row, chunk) partials, draft logits, chunk masses
-    assert n >= 128 * (9 * 16 * 8 + 16 * 8 + 9 * 4 + 3 * 4 + 32)
+    # per-(row, chunk) partials and draft logits, after a counter header (one eighth)
+    assert n >= 128 * (9 * 16 * 8 + 9 * 4) * 8 // 7
     assert n < 1 << 20
     assert sv.spec_verify_workspace_bytes(128, 4, 128256) == sv.spec_verify_workspace_bytes(128, 4, 128256, 1)
     assert sv.spec_verify_workspace_bytes(-1, 4, 100) == 0
