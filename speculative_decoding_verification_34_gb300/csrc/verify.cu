@@ -1,28 +1,32 @@
-// Greedy / sampling verification: one grid of independent blocks, no inter-block waiting.
+// Greedy / sampling verification: one grid of independent blocks.
 //
 // What is computed follows the tutorial "投机解码教程：从概率保持、KV Cache 回滚到性能盈亏平衡"
 // (§3-§4 greedy verification and logit alignment, §7.1-§7.3 acceptance min(1,p/q), residual
 // max(p-q,0)/R and the bonus draw) and the "M013" knowledge-base card (§03-§05, including the
 // R = 0 remark).  How it is computed is this library's own design for sm_103a.
 //
-// The vocabulary of every row is cut into CL chunks of `chunk` ids; block (b, c) of the grid
-// streams chunk c of every row sequence b reads, exactly once, from HBM: 16 KB tiles flow
-// through a per-thread cp.async ring in shared memory (each thread reads back only the vectors
-// it copied itself, so the ring needs no block barrier) and reduce, per row, to a
-// (max, sum 2^((x-max)k)) partial with one ex2 per element, or to an (argmax value, id)
-// partial for greedy rows; the logit at each draft id is taken from the registers holding it.
-// Partials go to the caller's workspace and the block arrives on a per-sequence counter.
+// The vocabulary of every row is cut into CL chunks of `chunk` ids.  The grid is a list of
+// block-sized units in groups: group g holds the A units of sequence g, then the B units of
+// sequence g - delta (delta groups ~ two waves of resident blocks).
 //
-// The last block of sequence b to arrive is its *decider*: it combines the partials in a fixed
-// order (so every quantity is the same whichever block decides), takes the acceptance
-// decisions, finds m, and then draws the last token itself: it streams the row (pair) the
-// draw uses -- row m of p and q after a rejection, the bonus row otherwise; just read by the
-// grid, so normally an L2 hit -- through the same ring, keeping one residual mass per tile,
-// locates u*R among the tile masses, rescans that tile, and writes the outputs.  No block ever
-// waits for another, so there is no ordering requirement on the grid.
+//   A(b, row, c)  reads chunk c of one row of sequence b once from HBM (128-bit loads), one
+//                 ex2 per sampled element, and writes a (max, sum 2^((x-max)k)) partial, or an
+//                 (argmax value, id) partial for greedy rows, to the workspace; the unit whose
+//                 chunk holds a draft id also records that logit.  The last A unit of b to
+//                 arrive (a counter) is the *decider*: it combines the partials in a fixed
+//                 order, takes the acceptance decisions, finds m, and either writes the greedy
+//                 result or publishes a plan for the final draw.
+//   B(b, c)       draws on the plan: chunk c of the row the last token is drawn from -- row m
+//                 of p and q after a rejection, the bonus row otherwise; normally still in L2 --
+//                 reduced to its residual and p masses.  The last chunk of b to finish makes its
+//                 block the *selector*: it locates the chunk holding u*R, rescans that chunk
+//                 and writes the outputs.
 //
-// Every call returns the workspace's counters to zero (the decider resets its sequence's), so a
-// zero-filled workspace can serve successive calls on one stream.
+// No block ever has to wait for another.  A B unit may wait a short, bounded while for its
+// plan; each draw chunk then goes through a small state machine (untouched -> claimed by its B
+// unit, or untouched -> given up -> taken by the decider) so that exactly one block processes
+// it whatever the timing: the decider takes the chunks whose B units gave up before the plan
+// was out, B units take the rest.  Every call returns the workspace's counters to zero.
 
 #include <cuda_bf16.h>
 
@@ -37,18 +41,17 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kVecPerPass = 4;                         // 16-byte vectors per thread per tile
-constexpr int kStages = 3;                             // cp.async ring depth (tiles)
-constexpr int kTileBytes = kThreads * kVecPerPass * 16;
+constexpr int kVecPerPass = 4;                         // 16-byte vectors per thread per pass
 constexpr int kMaxChunks = 64;                         // chunks per row
-constexpr int kMaxPasses = 4;                          // tiles per row chunk
+constexpr int kMaxPasses = 4;                          // passes per chunk
+constexpr int kMaxSlices = kMaxPasses * kVecPerPass;
 constexpr int kChunkTarget = 8192;                     // ids per chunk before rounding
-constexpr int kDrawVec = kVecPerPass / 2;              // draw tiles: kDrawVec vectors of p, of q
-constexpr int kMaxDrawTiles = 512;                     // draw tiles per row
-constexpr int kMaxSlices = kDrawVec;
+constexpr int kPlanWaitIters = 32;                     // optional bounded wait of a B unit (~15 us)
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kInternalDrawP = 0x100;
+// draw-chunk states
+constexpr int kChunkFree = 0, kChunkMine = 1, kChunkGivenUp = 2, kChunkDecider = 3;
 
 struct Args {
   const void* target;
@@ -68,15 +71,28 @@ struct Args {
 };
 
 struct Geo {
-  int CL;      // chunks per row (= blocks per sequence)
+  int CL;      // chunks per row
   int chunk;   // ids per chunk (multiple of 8)
   int nslots;  // row slots per sequence: target rows 0..gmax, then draft rows 0..gmax-1
+  int NA;      // A units per group (nslots * CL)
+  int G;       // units per group (NA, plus CL B units when sampling is possible)
+  int delta;   // B units of sequence b sit in group b + delta
+};
+
+struct __align__(16) PlanRec {   // per sequence, published by the decider for the draw
+  int m, g, flags, pair;
+  float mkp, invp, mkq, invq;
 };
 
 struct Work {      // views into the caller's workspace
-  int* cnt;        // [B] arrivals (counter header)
-  float2* part;    // [B][nslots][CL] per-chunk partials
+  int* cnt;        // [B] A arrivals            (counter header)
+  int* bdone;      // [B] draw-chunk arrivals   (counter header)
+  int* ready;      // [B] plan published        (counter header)
+  int* state;      // [B][CL] draw-chunk states (counter header)
+  PlanRec* plan;   // [B]
+  float2* part;    // [B][nslots][CL]
   float* xd;       // [B][nslots] logit at the draft id of that row
+  float2* mass;    // [B][CL] (residual mass, p mass)
 };
 
 // ------------------------------------------------------------------------------------------
@@ -272,15 +288,28 @@ __device__ __forceinline__ void tile_argmax(const Tile<E, kVec>& t, int64_t e0, 
     }
 }
 
+__device__ __forceinline__ int atom_cas(int* p, int cmp, int val) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.cas.b32 %0, [%1], %2, %3;" : "=r"(old) : "l"(p), "r"(cmp), "r"(val) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 struct Shared {
-  float2 wpart[kWarps][2 * SPEC_MAX_GAMMA + 1];   // per-warp partial of every row slot
+  float2 wp[kWarps];
   float rowM[2 * SPEC_MAX_GAMMA + 1];
   float rowInvS[2 * SPEC_MAX_GAMMA + 1];
   int rowArg[SPEC_MAX_GAMMA + 1];
   float pd[SPEC_MAX_GAMMA], qd[SPEC_MAX_GAMMA];
-  float wsum[kMaxSlices][kWarps];                 // draw: per-(slice, warp) sums of one tile
-  int last, m, flags, owner, slice, warp_sel, token;
+  float wsum[kMaxSlices][kWarps];                 // selector: per-(slice, warp) weight sums
+  int last, go, m, flags, owner, slice, warp_sel, token;
   float target_local, mass_out, run_sel;
+  PlanRec plan;
 };
 
 // ------------------------------------------------------------------------------------------
@@ -327,10 +356,6 @@ struct Seq {
   }
 };
 
-// ------------------------------------------------------------------------------------------
-// the draw: inverse CDF of the residual of (p_m, q_m), or of p at the bonus row
-// ------------------------------------------------------------------------------------------
-
 // weights of the N elements of one vector: w = residual (or p on the bonus row), and p
 template <class E>
 __device__ __forceinline__ void weights(const uint4& vp, const uint4& vq, bool pair, float k, float mkp, float invp,
@@ -365,145 +390,67 @@ __device__ __forceinline__ uint4 vec_at(const typename E::raw* row, int64_t e, i
   }
 }
 
+// ------------------------------------------------------------------------------------------
+// the draw: chunk masses, then the selector
+// ------------------------------------------------------------------------------------------
+
 template <class E, bool kVec, bool kMixed>
-__device__ void draw(const Args& a, const Seq<E, kMixed>& sq, Shared& sm, unsigned char* ring, int m, int flags) {
+__device__ void select(const Args& a, const Geo& geo, const Work& w, const Seq<E, kMixed>& sq, const PlanRec pl,
+                       Shared& sm) {
   using raw = typename E::raw;
   constexpr int N = E::kPerVec;
-  constexpr int kTile = kThreads * kDrawVec * N;       // ids per draw tile
+  constexpr int kPass = kThreads * kVecPerPass * N;
   const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
-  const int b = sq.b, gmax = a.gmax;
-  const int64_t V = a.V;
-  const float k = sq.k;
-  const bool pair = m < sq.g;
-  const raw* rp = sq.P + int64_t(m) * V;
-  const raw* rq = pair ? sq.Q + int64_t(m) * V : rp;
-  const int qs = gmax + 1 + m;
-  const float mkp = __fmul_rn(sm.rowM[m], k), invp = sm.rowInvS[m];
-  const float mkq = pair ? __fmul_rn(sm.rowM[qs], k) : 0.f, invq = pair ? sm.rowInvS[qs] : 0.f;
-  const int ntiles = int((V + kTile - 1) / kTile);
-  // per-(tile, warp) (weight, p) masses, in the dynamic shared memory after the ring
-  float2 (*tmass)[kWarps] = reinterpret_cast<float2 (*)[kWarps]>(ring + kStages * kTileBytes);
-
-  // pass 1: the masses of every tile, streamed through the ring (p vectors in slots 0..,
-  // q vectors in slots kDrawVec..)
-  auto issue = [&](int t) {
-    if constexpr (kVec) {
-      if (t < ntiles) {
-        unsigned char* st = ring + (t % kStages) * kTileBytes;
-#pragma unroll
-        for (int s = 0; s < kDrawVec; ++s) {
-          const int64_t e = int64_t(t) * kTile + int64_t(s * kThreads + tid) * N;
-          const bool in = e < V;
-          cp_async16(st + (s * kThreads + tid) * 16, in ? static_cast<const void*>(rp + e) : static_cast<const void*>(rp),
-                     in ? 16 : 0);
-          if (pair)
-            cp_async16(st + ((kDrawVec + s) * kThreads + tid) * 16,
-                       in ? static_cast<const void*>(rq + e) : static_cast<const void*>(rq), in ? 16 : 0);
-        }
-      }
-      cp_async_commit();
+  const int b = sq.b, gmax = a.gmax, CL = geo.CL;
+  const bool pair = pl.pair != 0;
+  __threadfence();
+  if (tid == 0) {
+    const float2* ms = w.mass + int64_t(b) * CL;
+    float R = 0.f, Pm = 0.f;
+    for (int c = 0; c < CL; ++c) {
+      const float2 x = __ldcg(&ms[c]);
+      R = __fadd_rn(R, x.x);
+      Pm = __fadd_rn(Pm, x.y);
     }
-  };
-  if constexpr (kVec) {
-#pragma unroll
-    for (int t = 0; t < kStages - 1; ++t) issue(t);
-  }
-  for (int t = 0; t < ntiles; ++t) {
-    float ws = 0.f, ps = 0.f;
-#pragma unroll
-    for (int s = 0; s < kDrawVec; ++s) {
-      const int64_t e = int64_t(t) * kTile + int64_t(s * kThreads + tid) * N;
-      uint4 vp, vq;
-      if constexpr (kVec) {
-        if (s == 0) {
-          issue(t + kStages - 1);
-          cp_async_wait<kStages - 1>();
-        }
-        const unsigned char* st = ring + (t % kStages) * kTileBytes;
-        const uint4 neg = make_uint4(E::kNegInf, E::kNegInf, E::kNegInf, E::kNegInf);
-        vp = e < V ? *reinterpret_cast<const uint4*>(st + (s * kThreads + tid) * 16) : neg;
-        vq = (pair && e < V) ? *reinterpret_cast<const uint4*>(st + ((kDrawVec + s) * kThreads + tid) * 16) : neg;
-      } else {
-        vp = vec_at<E, kVec>(rp, e, V);
-        vq = pair ? vec_at<E, kVec>(rq, e, V) : vp;
-      }
-      float w[N], p[N];
-      weights<E>(vp, vq, pair, k, mkp, invp, mkq, invq, w, p);
-#pragma unroll
-      for (int j = 0; j < N; ++j) {
-        ws = __fadd_rn(ws, w[j]);
-        ps = __fadd_rn(ps, p[j]);
-      }
-    }
-    ws = warp_sum(ws);
-    ps = warp_sum(ps);
-    if (lane == 0) tmass[t][warp] = make_float2(ws, ps);
-  }
-  if constexpr (kVec) cp_async_wait<0>();
-  __syncthreads();
-
-  // which tile holds u * total: warp 0, lanes own contiguous runs of tiles, warp scan
-  if (warp == 0) {
-    const int per = (ntiles + 31) / 32;
-    const int t0 = lane * per, t1 = min(ntiles, t0 + per);
-    float lw = 0.f, lp = 0.f;
-    for (int t = t0; t < t1; ++t)
-      for (int wi = 0; wi < kWarps; ++wi) {
-        lw = __fadd_rn(lw, tmass[t][wi].x);
-        lp = __fadd_rn(lp, tmass[t][wi].y);
-      }
-    float iw = lw, ip = lp;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float yw = __shfl_up_sync(kFull, iw, o), yp = __shfl_up_sync(kFull, ip, o);
-      if (lane >= o) {
-        iw = __fadd_rn(iw, yw);
-        ip = __fadd_rn(ip, yp);
-      }
-    }
-    const float R = __shfl_sync(kFull, iw, 31), Pm = __shfl_sync(kFull, ip, 31);
     const bool use_w = !pair || R > 0.f;   // bonus: the weights are p itself
+    int f = pl.flags;
+    if (!use_w) f |= SPEC_ST_R_ZERO | kInternalDrawP;
     const float total = use_w ? R : Pm;
     const float target = __fmul_rn(a.u_sample[b], total);
-    const float mine = use_w ? lw : lp, incl = use_w ? iw : ip;
-    const float excl = __fsub_rn(incl, mine);
-    const unsigned hit = __ballot_sync(kFull, mine > 0.f && incl > target);
-    const unsigned pos = __ballot_sync(kFull, mine > 0.f);
-    const int sl = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
-    if (lane == sl) {
-      // walk this lane's tiles in order
-      float run = excl;
-      int owner = -1, last = t0;
-      float base = excl, base_last = excl;
-      for (int t = t0; t < t1; ++t) {
-        float x = 0.f;
-        for (int wi = 0; wi < kWarps; ++wi) x = __fadd_rn(x, use_w ? tmass[t][wi].x : tmass[t][wi].y);
-        if (x > 0.f) { last = t; base_last = run; }
-        const float nr = __fadd_rn(run, x);
-        if (owner < 0 && nr > target && x > 0.f) { owner = t; base = run; }
-        run = nr;
-      }
-      if (owner < 0) { owner = last; base = base_last; }
-      int f = flags;
-      if (!use_w) f |= SPEC_ST_R_ZERO | kInternalDrawP;
-      sm.owner = owner;
-      sm.flags = f;
-      sm.target_local = __fsub_rn(target, base);
-      sm.mass_out = pair ? (use_w ? R : 0.f) : R;
+    int owner = -1, last = 0;
+    float excl = 0.f, run = 0.f, excl_last = 0.f;
+    for (int c = 0; c < CL; ++c) {
+      const float2 x = __ldcg(&ms[c]);
+      const float wc = use_w ? x.x : x.y;
+      if (wc > 0.f) { last = c; excl_last = run; }
+      const float nr = __fadd_rn(run, wc);
+      if (owner < 0 && nr > target && wc > 0.f) { owner = c; excl = run; }
+      run = nr;
     }
+    if (owner < 0) { owner = last; excl = excl_last; }
+    sm.owner = owner;
+    sm.flags = f;
+    sm.target_local = __fsub_rn(target, excl);
+    sm.mass_out = pair ? (use_w ? R : 0.f) : R;
   }
   __syncthreads();
-
-  // pass 2: rescan the owner tile: per-(slice, warp) sums, then one warp, then one lane
   const bool draw_p = !pair || (sm.flags & kInternalDrawP);
-  const int64_t base_e = int64_t(sm.owner) * kTile;
-  for (int s = 0; s < kDrawVec; ++s) {
-    const int64_t e = base_e + int64_t(s * kThreads + tid) * N;
-    float w[N], p[N];
-    weights<E>(vec_at<E, kVec>(rp, e, V), vec_at<E, kVec>(rq, e, pair ? V : 0), pair, k, mkp, invp, mkq, invq, w, p);
+  const int64_t lo = int64_t(sm.owner) * geo.chunk;
+  const int64_t hi = lo + geo.chunk < a.V ? lo + geo.chunk : a.V;
+  const raw* rp = sq.P + int64_t(pl.m) * a.V;
+  const raw* rq = pair ? sq.Q + int64_t(pl.m) * a.V : rp;
+  const int npass = int((hi - lo + kPass - 1) / kPass);
+  const int slices = npass * kVecPerPass;
+  // per-(slice, warp) sums; slice-major, warp-minor is ascending vocabulary order
+  for (int s = 0; s < slices; ++s) {
+    const int ps = s / kVecPerPass, q = s - ps * kVecPerPass;
+    const int64_t e = lo + int64_t(ps) * kPass + int64_t(q * kThreads + tid) * N;
+    float wv[N], pv[N];
+    weights<E>(vec_at<E, kVec>(rp, e, hi), vec_at<E, kVec>(rq, e, pair ? hi : 0), pair, sq.k, pl.mkp, pl.invp, pl.mkq,
+               pl.invq, wv, pv);
     float x = 0.f;
 #pragma unroll
-    for (int j = 0; j < N; ++j) x = __fadd_rn(x, draw_p ? p[j] : w[j]);
+    for (int j = 0; j < N; ++j) x = __fadd_rn(x, draw_p ? pv[j] : wv[j]);
     x = warp_sum(x);
     if (lane == 0) sm.wsum[s][warp] = x;
   }
@@ -512,7 +459,7 @@ __device__ void draw(const Args& a, const Seq<E, kMixed>& sq, Shared& sm, unsign
   if (tid == 0) {
     int ss = -1, sw = 0, ls = 0, lw = 0;
     float run = 0.f, base = 0.f, base_last = 0.f;
-    for (int s = 0; s < kDrawVec && ss < 0; ++s)
+    for (int s = 0; s < slices && ss < 0; ++s)
       for (int wi = 0; wi < kWarps; ++wi) {
         const float x = sm.wsum[s][wi];
         if (x > 0.f) { ls = s; lw = wi; base_last = run; }
@@ -524,17 +471,19 @@ __device__ void draw(const Args& a, const Seq<E, kMixed>& sq, Shared& sm, unsign
     sm.slice = ss;
     sm.warp_sel = sw;
     sm.run_sel = base;
-    sm.token = int(base_e);
+    sm.token = int(lo);
   }
   __syncthreads();
   if (warp == sm.warp_sel) {
     const int s = sm.slice;
-    const int64_t e = base_e + int64_t(s * kThreads + tid) * N;
-    float w[N], p[N];
-    weights<E>(vec_at<E, kVec>(rp, e, V), vec_at<E, kVec>(rq, e, pair ? V : 0), pair, k, mkp, invp, mkq, invq, w, p);
+    const int ps = s / kVecPerPass, q = s - ps * kVecPerPass;
+    const int64_t e = lo + int64_t(ps) * kPass + int64_t(q * kThreads + tid) * N;
+    float wv[N], pv[N];
+    weights<E>(vec_at<E, kVec>(rp, e, hi), vec_at<E, kVec>(rq, e, pair ? hi : 0), pair, sq.k, pl.mkp, pl.invp, pl.mkq,
+               pl.invq, wv, pv);
     float x = 0.f;
 #pragma unroll
-    for (int j = 0; j < N; ++j) x = __fadd_rn(x, draw_p ? p[j] : w[j]);
+    for (int j = 0; j < N; ++j) x = __fadd_rn(x, draw_p ? pv[j] : wv[j]);
     float incl = x;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -550,38 +499,94 @@ __device__ void draw(const Args& a, const Seq<E, kMixed>& sq, Shared& sm, unsign
       int tok = -1, lastpos = -1;
 #pragma unroll
       for (int j = 0; j < N; ++j) {
-        const float wj = draw_p ? p[j] : w[j];
+        const float wj = draw_p ? pv[j] : wv[j];
         r = __fadd_rn(r, wj);
         if (wj > 0.f) {
           lastpos = int(e) + j;
           if (tok < 0 && r > tl) tok = int(e) + j;
         }
       }
-      sm.token = tok >= 0 ? tok : (lastpos >= 0 ? lastpos : int(base_e));
+      sm.token = tok >= 0 ? tok : (lastpos >= 0 ? lastpos : int(lo));
     }
   }
   __syncthreads();
-  const int tok = sm.token;
+  const int m = pl.m, tok = sm.token;
   for (int i = tid; i <= gmax; i += kThreads) {
     int v = -1;
     if (i < m) v = a.draft_tokens[int64_t(b) * gmax + i];
     else if (i == m) v = tok;
     a.out_tokens[int64_t(b) * (gmax + 1) + i] = v;
   }
+  for (int c = tid; c < CL; c += kThreads) w.state[int64_t(b) * CL + c] = kChunkFree;
   if (tid == 0) {
     if (a.diag) a.diag[int64_t(b) * (2 * gmax + 1) + 2 * gmax] = sm.mass_out;
     a.num_accepted[b] = m;
     if (a.status) a.status[b] = sm.flags & 0xff;
+    w.ready[b] = 0;
+    w.bdone[b] = 0;
   }
+  __syncthreads();
+}
+
+// one draw chunk: its residual and p masses; the last chunk of b to finish selects
+template <class E, bool kVec, bool kMixed>
+__device__ void draw_chunk(const Args& a, const Geo& geo, const Work& w, const Seq<E, kMixed>& sq, const PlanRec pl,
+                           int c, Shared& sm) {
+  using raw = typename E::raw;
+  constexpr int N = E::kPerVec;
+  const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
+  const int b = sq.b;
+  const bool pair = pl.pair != 0;
+  const raw* rp = sq.P + int64_t(pl.m) * a.V;
+  const raw* rq = pair ? sq.Q + int64_t(pl.m) * a.V : rp;
+  const int64_t lo = int64_t(c) * geo.chunk;
+  const int64_t hi = lo + geo.chunk < a.V ? lo + geo.chunk : a.V;
+  float ws = 0.f, ps = 0.f;
+  // two vectors of each row in flight per thread: the rows are normally still in L2
+  constexpr int kDrawStep = kThreads * 2 * N;
+  for (int64_t e0 = lo; e0 < hi; e0 += kDrawStep) {
+    uint4 vp[2], vq[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int64_t e = e0 + int64_t(q * kThreads + tid) * N;
+      vp[q] = vec_at<E, kVec>(rp, e, hi);
+      vq[q] = vec_at<E, kVec>(rq, e, pair ? hi : 0);
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      float wv[N], pv[N];
+      weights<E>(vp[q], vq[q], pair, sq.k, pl.mkp, pl.invp, pl.mkq, pl.invq, wv, pv);
+#pragma unroll
+      for (int j = 0; j < N; ++j) {
+        ws = __fadd_rn(ws, wv[j]);
+        ps = __fadd_rn(ps, pv[j]);
+      }
+    }
+  }
+  ws = warp_sum(ws);
+  ps = warp_sum(ps);
+  if (lane == 0) sm.wp[warp] = make_float2(ws, ps);
+  __syncthreads();
+  if (tid == 0) {
+    float2 acc = sm.wp[0];
+    for (int wi = 1; wi < kWarps; ++wi) {
+      acc.x = __fadd_rn(acc.x, sm.wp[wi].x);
+      acc.y = __fadd_rn(acc.y, sm.wp[wi].y);
+    }
+    if (!pair) acc.x = acc.y;
+    w.mass[int64_t(b) * geo.CL + c] = acc;
+    sm.last = atom_add_acq_rel(&w.bdone[b], 1) == geo.CL - 1;
+  }
+  __syncthreads();
+  if (sm.last) select<E, kVec, kMixed>(a, geo, w, sq, pl, sm);
 }
 
 // ------------------------------------------------------------------------------------------
-// decider: combine the partials of sequence b, decide, then greedy result or the draw
+// decider: combine the partials of sequence b, decide, then greedy result or the plan
 // ------------------------------------------------------------------------------------------
 
 template <class E, bool kVec, bool kMixed>
-__device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E, kMixed>& sq, Shared& sm,
-                       unsigned char* ring) {
+__device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E, kMixed>& sq, Shared& sm) {
   const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
   const int b = sq.b, g = sq.g, gmax = a.gmax, CL = geo.CL;
   const float k = sq.k;
@@ -646,8 +651,7 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
     }
   }
   __syncthreads();
-  const int m = sm.m, flags = sm.flags;
-  if (tid == 0) w.cnt[b] = 0;   // every block of b has arrived: ready for the next call
+  const int m = sm.m;
   if (!sq.sampling) {
     for (int i = tid; i <= gmax; i += kThreads) {
       int v = -1;
@@ -659,8 +663,10 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
       for (int i = tid; i < 2 * gmax + 1; i += kThreads) a.diag[int64_t(b) * (2 * gmax + 1) + i] = NAN;
     if (tid == 0) {
       a.num_accepted[b] = m;
-      if (a.status) a.status[b] = flags;
+      if (a.status) a.status[b] = sm.flags;
+      w.cnt[b] = 0;
     }
+    __syncthreads();
     return;
   }
   if (a.diag) {
@@ -670,128 +676,154 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
       dg[2 * i + 1] = i < g ? sm.qd[i] : NAN;
     }
   }
-  draw<E, kVec, kMixed>(a, sq, sm, ring, m, flags);
+  if (tid == 0) {
+    PlanRec pr;
+    pr.m = m;
+    pr.g = g;
+    pr.flags = sm.flags;
+    pr.pair = m < g ? 1 : 0;
+    pr.mkp = __fmul_rn(sm.rowM[m], k);
+    pr.invp = sm.rowInvS[m];
+    const int qs = gmax + 1 + m;
+    pr.mkq = pr.pair ? __fmul_rn(sm.rowM[qs], k) : 0.f;
+    pr.invq = pr.pair ? sm.rowInvS[qs] : 0.f;
+    w.plan[b] = pr;
+    sm.plan = pr;
+    w.cnt[b] = 0;
+    __threadfence();
+    atomicExch(&w.ready[b], 1);
+    __threadfence();
+  }
+  __syncthreads();
+  const PlanRec pl = sm.plan;
+  // the chunks whose B units gave up before the plan was out are the decider's
+  for (int c = 0; c < CL; ++c) {
+    if (tid == 0) {
+      int s = ld_acquire(&w.state[int64_t(b) * CL + c]);
+      sm.go = s == kChunkGivenUp && atom_cas(&w.state[int64_t(b) * CL + c], kChunkGivenUp, kChunkDecider) == kChunkGivenUp;
+    }
+    __syncthreads();
+    const bool go = sm.go;
+    __syncthreads();
+    if (go) draw_chunk<E, kVec, kMixed>(a, geo, w, sq, pl, c, sm);
+  }
 }
 
 // ------------------------------------------------------------------------------------------
-// the kernel: block (b, c)
+// the kernel
 // ------------------------------------------------------------------------------------------
 
 template <class E, bool kVec, bool kMixed>
-__global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Args a, const Geo geo, const Work w) {
+__global__ void __launch_bounds__(kThreads, 6) verify_kernel(const Args a, const Geo geo, const Work w) {
   using raw = typename E::raw;
   constexpr int N = E::kPerVec;
-  constexpr int kPass = kThreads * kVecPerPass * N;     // ids per tile
-  extern __shared__ __align__(16) unsigned char ring[];
+  constexpr int kPass = kThreads * kVecPerPass * N;
   __shared__ Shared sm;
   const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
-  const int b = int(blockIdx.x) / geo.CL, c = int(blockIdx.x) - b * geo.CL;
-  const int gmax = a.gmax;
-  const int64_t V = a.V;
-  const Seq<E, kMixed> sq(a, b);
-  const int64_t lo = int64_t(c) * geo.chunk;
-  const int64_t hi = lo + geo.chunk < V ? lo + geo.chunk : V;
-  const int npass = int((hi - lo + kPass - 1) / kPass);
-  const int nrows = sq.nrows();
+  const int grp = int(blockIdx.x) / geo.G, off = int(blockIdx.x) - grp * geo.G;
 
-  // producer cursor: the next tile to copy into the ring
-  int ir = 0, ip = 0;
-  const raw* irow = sq.row(sq.slot_of(0, gmax), gmax, V);
-  int istage = 0;
-  auto issue = [&]() {
-    if constexpr (kVec) {
-      if (ir < nrows) {
-        const int64_t e0 = lo + int64_t(ip) * kPass;
-        unsigned char* st = ring + istage * kTileBytes + tid * 16;
-        const raw* src = irow + e0 + int64_t(tid) * N;
-        if (e0 + kPass <= hi) {
-#pragma unroll
-          for (int q = 0; q < kVecPerPass; ++q) cp_async16(st + q * kThreads * 16, src + q * kThreads * N, 16);
-        } else {
-#pragma unroll
-          for (int q = 0; q < kVecPerPass; ++q) {
-            const bool in = e0 + int64_t(q * kThreads + tid) * N < hi;
-            cp_async16(st + q * kThreads * 16, in ? static_cast<const void*>(src + q * kThreads * N) : static_cast<const void*>(irow),
-                       in ? 16 : 0);
-          }
-        }
-        if (++ip == npass) {
-          ip = 0;
-          if (++ir < nrows) irow = sq.row(sq.slot_of(ir, gmax), gmax, V);
-        }
-      }
-      cp_async_commit();
-      istage = istage == kStages - 1 ? 0 : istage + 1;
-    }
-  };
-  if constexpr (kVec) {
-#pragma unroll
-    for (int t = 0; t < kStages - 1; ++t) issue();
-  }
-  int cstage = 0;
-  for (int r = 0; r < nrows; ++r) {
-    const int slot = sq.slot_of(r, gmax);
-    const raw* row = sq.row(slot, gmax, V);
-    const int i = slot <= gmax ? slot : slot - gmax - 1;
-    const int d = (sq.sampling && i < sq.g) ? __ldg(&a.draft_tokens[int64_t(b) * gmax + i]) : -1;
+  if (off < geo.NA) {
+    // ---------------- A unit: chunk c of one row -------------------------------------------
+    const int b = grp;
+    if (b >= a.B) return;
+    const int slot = off / geo.CL, c = off - slot * geo.CL;
+    const Seq<E, kMixed> sq(a, b);
+    if (!sq.slot_valid(slot, a.gmax)) return;
+    const raw* row = sq.row(slot, a.gmax, a.V);
+    const int64_t lo = int64_t(c) * geo.chunk;
+    const int64_t hi = lo + geo.chunk < a.V ? lo + geo.chunk : a.V;
+    const int i = slot <= a.gmax ? slot : slot - a.gmax - 1;
+    const int d = (sq.sampling && i < sq.g) ? __ldg(&a.draft_tokens[int64_t(b) * a.gmax + i]) : -1;
     float rm = -INFINITY, rs = 0.f;
     int ri = INT_MAX;
-    for (int ps = 0; ps < npass; ++ps) {
-      const int64_t e0 = lo + int64_t(ps) * kPass;
-      Tile<E, kVec> tile;
-      if constexpr (kVec) {
-        issue();
-        cp_async_wait<kStages - 1>();
-        const unsigned char* st = ring + cstage * kTileBytes + tid * 16;
-#pragma unroll
-        for (int q = 0; q < kVecPerPass; ++q) tile.v[q] = *reinterpret_cast<const uint4*>(st + q * kThreads * 16);
-        cstage = cstage == kStages - 1 ? 0 : cstage + 1;
-        if (e0 + kPass > hi) {
-#pragma unroll
-          for (int q = 0; q < kVecPerPass; ++q)
-            if (e0 + int64_t(q * kThreads + tid) * N >= hi) tile.v[q] = make_uint4(E::kNegInf, E::kNegInf, E::kNegInf, E::kNegInf);
-        }
-      } else {
-        tile.load(row, e0, hi, tid);
-      }
+    for (int64_t e0 = lo; e0 < hi; e0 += kPass) {
+      Tile<E, kVec> t;
+      t.load(row, e0, hi, tid);
       if (sq.sampling) {
-        // the logit at this row's draft id, taken from the registers that hold it
         if (int64_t(d) >= e0 && int64_t(d) < e0 + kPass && int64_t(d) < hi) {
+          // the logit at this row's draft id, from the registers that hold it
 #pragma unroll
           for (int q = 0; q < kVecPerPass; ++q) {
             const int64_t o = int64_t(d) - (e0 + int64_t(q * kThreads + tid) * N);
             if (o >= 0 && o < N) {
-              w.xd[int64_t(b) * geo.nslots + slot] = tile.x(q, int(o));
+              w.xd[int64_t(b) * geo.nslots + slot] = t.x(q, int(o));
               __threadfence();
             }
           }
         }
-        tile_stats(tile, sq.k, rm, rs);
+        tile_stats(t, sq.k, rm, rs);
       } else {
-        tile_argmax(tile, e0, tid, rm, ri);
+        tile_argmax(t, e0, tid, rm, ri);
       }
     }
     if (!sq.sampling) warp_argmax(rm, ri);
-    if (lane == 0) sm.wpart[warp][slot] = make_float2(rm, sq.sampling ? rs : __int_as_float(ri));
-  }
-  if constexpr (kVec) cp_async_wait<0>();
-  __syncthreads();
-  // block partial per row (warps merged in a fixed order), then one arrival per block
-  for (int r = tid; r < nrows; r += kThreads) {
-    const int slot = sq.slot_of(r, gmax);
-    float2 acc = sm.wpart[0][slot];
-    for (int wi = 1; wi < kWarps; ++wi) {
-      const float2 p = sm.wpart[wi][slot];
-      if (sq.sampling) merge_ms(acc.x, acc.y, p.x, p.y, sq.k);
-      else if (better(p.x, __float_as_int(p.y), acc.x, __float_as_int(acc.y))) acc = p;
+    if (lane == 0) sm.wp[warp] = make_float2(rm, sq.sampling ? rs : __int_as_float(ri));
+    __syncthreads();
+    if (tid == 0) {
+      float2 acc = sm.wp[0];
+      for (int wi = 1; wi < kWarps; ++wi) {
+        const float2 p = sm.wp[wi];
+        if (sq.sampling) merge_ms(acc.x, acc.y, p.x, p.y, sq.k);
+        else if (better(p.x, __float_as_int(p.y), acc.x, __float_as_int(acc.y))) acc = p;
+      }
+      w.part[(int64_t(b) * geo.nslots + slot) * geo.CL + c] = acc;
+      sm.last = atom_add_acq_rel(&w.cnt[b], 1) == geo.CL * sq.nrows() - 1;
     }
-    w.part[(int64_t(b) * geo.nslots + slot) * geo.CL + c] = acc;
-    __threadfence();
+    __syncthreads();
+    if (sm.last) decide<E, kVec, kMixed>(a, geo, w, sq, sm);
+    return;
   }
-  __syncthreads();
-  if (tid == 0) sm.last = atom_add_acq_rel(&w.cnt[b], 1) == geo.CL - 1;
-  __syncthreads();
-  if (sm.last) decide<E, kVec, kMixed>(a, geo, w, sq, sm, ring);
+
+  if constexpr (kMixed) {
+    // ---------------- B unit: draw chunk c of sequence grp - delta ------------------------
+    const int b = grp - geo.delta;
+    if (b < 0 || b >= a.B) return;
+    const int c = off - geo.NA;
+    const Seq<E, kMixed> sq(a, b);
+    if (!sq.sampling) return;
+    if (tid == 0) {
+      int* st = &w.state[int64_t(b) * geo.CL + c];
+      // optional, bounded wait for the plan; correctness does not depend on it
+      int it = 0, ns = 64;
+      while (ld_acquire(&w.ready[b]) == 0 && it < kPlanWaitIters) {
+        __nanosleep(ns);
+        if (ns < 512) ns <<= 1;
+        ++it;
+      }
+      bool mine = false;
+      if (ld_acquire(&w.ready[b]) != 0) {
+        mine = atom_cas(st, kChunkFree, kChunkMine) == kChunkFree;
+      } else if (atom_cas(st, kChunkFree, kChunkGivenUp) == kChunkFree) {
+        // given up; if the plan appeared meanwhile, take the chunk back unless the decider has
+        __threadfence();
+        if (ld_acquire(&w.ready[b]) != 0) mine = atom_cas(st, kChunkGivenUp, kChunkMine) == kChunkGivenUp;
+      }
+      if (mine) {
+        __threadfence();
+        // through L2: an earlier read of this line by the same SM may sit stale in L1
+        const int4* src = reinterpret_cast<const int4*>(&w.plan[b]);
+        const int4 h0 = __ldcg(src), h1 = __ldcg(src + 1);
+        sm.plan.m = h0.x;
+        sm.plan.g = h0.y;
+        sm.plan.flags = h0.z;
+        sm.plan.pair = h0.w;
+        sm.plan.mkp = __int_as_float(h1.x);
+        sm.plan.invp = __int_as_float(h1.y);
+        sm.plan.mkq = __int_as_float(h1.z);
+        sm.plan.invq = __int_as_float(h1.w);
+        const PlanRec& pl = sm.plan;
+        // never fails for a well-formed workspace; keeps every read in bounds
+        if (pl.m < 0 || pl.m > sq.g || (pl.pair && pl.m >= sq.g)) {
+          mine = false;
+          if (a.status) atomicOr(&a.status[b], SPEC_ST_TIMEOUT);
+        }
+      }
+      sm.go = mine;
+    }
+    __syncthreads();
+    if (!sm.go) return;
+    draw_chunk<E, kVec, kMixed>(a, geo, w, sq, sm.plan, c, sm);
+  }
 }
 
 // ------------------------------------------------------------------------------------------
@@ -819,15 +851,19 @@ size_t align64(size_t x) { return (x + 63) & ~size_t(63); }
 // therefore disjoint from any call's counters, whatever sizes successive calls use, and the
 // counters (all zero between calls) stay valid.
 struct WsLayout {
-  size_t cnt, part, xd, header, scratch_end;
+  size_t cnt, bdone, ready, state, plan, part, xd, mass, header, scratch_end;
 };
 
-size_t counter_bytes(int B) { return align64(size_t(B) * 4); }
+size_t counter_bytes(int B, int64_t V) {
+  const Split s = make_split(V);
+  return 3 * align64(size_t(B) * 4) + align64(size_t(B) * s.cl * 4);
+}
 
 size_t scratch_bytes(int B, int gmax, int64_t V) {
   const Split s = make_split(V);
   const size_t nslots = size_t(2 * gmax + 1);
-  return align64(size_t(B) * nslots * s.cl * 8) + align64(size_t(B) * nslots * 4);
+  return align64(size_t(B) * sizeof(PlanRec)) + align64(size_t(B) * nslots * s.cl * 8) +
+         align64(size_t(B) * nslots * 4) + align64(size_t(B) * s.cl * 8);
 }
 
 size_t header_for(size_t ws_bytes) { return (ws_bytes / 8) & ~size_t(63); }
@@ -838,23 +874,30 @@ WsLayout ws_layout(int B, int gmax, int64_t V, size_t ws_bytes) {
   WsLayout L;
   L.header = header_for(ws_bytes);
   L.cnt = 0;
+  L.bdone = L.cnt + align64(size_t(B) * 4);
+  L.ready = L.bdone + align64(size_t(B) * 4);
+  L.state = L.ready + align64(size_t(B) * 4);
   size_t off = L.header;
+  L.plan = off;
+  off += align64(size_t(B) * sizeof(PlanRec));
   L.part = off;
   off += align64(size_t(B) * nslots * s.cl * 8);
   L.xd = off;
   off += align64(size_t(B) * nslots * 4);
+  L.mass = off;
+  off += align64(size_t(B) * s.cl * 8);
   L.scratch_end = off;
   return L;
 }
 
 bool ws_fits(int B, int gmax, int64_t V, size_t ws_bytes) {
-  return counter_bytes(B) <= header_for(ws_bytes) &&
+  return counter_bytes(B, V) <= header_for(ws_bytes) &&
          header_for(ws_bytes) + scratch_bytes(B, gmax, V) <= ws_bytes;
 }
 
 // smallest workspace (a multiple of 64 bytes) that fits a call of these sizes
 size_t ws_required(int B, int gmax, int64_t V) {
-  const size_t c = counter_bytes(B), sc = scratch_bytes(B, gmax, V);
+  const size_t c = counter_bytes(B, V), sc = scratch_bytes(B, gmax, V);
   size_t w = align64(8 * (c + 64));
   const size_t w2 = align64((sc + 64) * 8 / 7 + 64);
   if (w2 > w) w = w2;
@@ -866,12 +909,17 @@ Work ws_views(void* ws, const WsLayout& L) {
   unsigned char* p = static_cast<unsigned char*>(ws);
   Work w;
   w.cnt = reinterpret_cast<int*>(p + L.cnt);
+  w.bdone = reinterpret_cast<int*>(p + L.bdone);
+  w.ready = reinterpret_cast<int*>(p + L.ready);
+  w.state = reinterpret_cast<int*>(p + L.state);
+  w.plan = reinterpret_cast<PlanRec*>(p + L.plan);
   w.part = reinterpret_cast<float2*>(p + L.part);
   w.xd = reinterpret_cast<float*>(p + L.xd);
+  w.mass = reinterpret_cast<float2*>(p + L.mass);
   return w;
 }
 
-std::mutex g_attr_mu;
+std::mutex g_occ_mu;
 
 template <class E, bool kVec, bool kMixed>
 int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream) {
@@ -879,9 +927,8 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
   const Split sp = make_split(args.V);
   const int64_t per_pass = int64_t(kThreads) * kVecPerPass * (dtype == SPEC_BF16 ? 8 : 4);
   const int npass = int((sp.chunk + per_pass - 1) / per_pass);
-  const int64_t draw_tile = int64_t(kThreads) * kDrawVec * (dtype == SPEC_BF16 ? 8 : 4);
-  if (npass > kMaxPasses || (args.V + draw_tile - 1) / draw_tile > kMaxDrawTiles) {
-    set_error("V=%lld too large for this build", (long long)args.V);
+  if (npass > kMaxPasses) {
+    set_error("V=%lld too large: %d passes per chunk (max %d)", (long long)args.V, npass, kMaxPasses);
     return SPEC_ENOSPACE;
   }
   // host-only checks first: nothing is enqueued when they fail
@@ -894,35 +941,40 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
     set_error("workspace must be 64-byte aligned");
     return SPEC_EINVAL;
   }
-  const int64_t blocks = int64_t(args.B) * sp.cl;
-  if (blocks > INT_MAX) {
-    set_error("batch too large: %lld blocks", (long long)blocks);
-    return SPEC_ENOSPACE;
-  }
   const WsLayout L = ws_layout(args.B, args.gmax, args.V, ws_bytes);
   Geo geo;
   geo.CL = sp.cl;
   geo.chunk = sp.chunk;
   geo.nslots = kMixed ? 2 * args.gmax + 1 : args.gmax + 1;   // greedy-only reads no draft rows
-  const int64_t ndraw = (args.V + draw_tile - 1) / draw_tile;
-  const size_t smem = size_t(kStages) * kTileBytes + size_t(kMixed ? ndraw : 0) * kWarps * sizeof(float2);
-  int dev = 0;
+  geo.NA = geo.nslots * geo.CL;
+  geo.G = geo.NA + (kMixed ? geo.CL : 0);
+  // B units of a sequence come about two waves of resident blocks after its A units
+  int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   {
-    // the ring plus the static shared memory exceed the 48 KB a block gets without opting in;
-    // the opt-in is raised to the largest size any V can need, once per device
-    static bool done[64] = {};
-    std::lock_guard<std::mutex> lk(g_attr_mu);
-    if (dev >= 64 || !done[dev]) {
-      const int most = int(size_t(kStages) * kTileBytes + size_t(kMaxDrawTiles) * kWarps * sizeof(float2));
-      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)");
-      if (dev < 64) done[dev] = true;
+    static int cached[64] = {};
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    if (dev < 64 && cached[dev]) {
+      per_sm = cached[dev];
+    } else {
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, 0);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+      if (per_sm < 1) per_sm = 1;
+      if (dev < 64) cached[dev] = per_sm;
     }
   }
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  const int64_t resident = int64_t(sms) * per_sm;
+  geo.delta = kMixed ? int((2 * resident + geo.G - 1) / geo.G) : 0;
+  const int64_t blocks = (int64_t(args.B) + geo.delta) * geo.G;
+  if (blocks > INT_MAX) {
+    set_error("batch too large: %lld blocks", (long long)blocks);
+    return SPEC_ENOSPACE;
+  }
   const Work w = ws_views(ws, L);
-  fn<<<unsigned(blocks), kThreads, smem, static_cast<cudaStream_t>(stream)>>>(args, geo, w);
+  fn<<<unsigned(blocks), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(args, geo, w);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "verify kernel launch");
   count_launch();
