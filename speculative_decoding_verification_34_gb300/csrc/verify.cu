@@ -45,7 +45,19 @@ constexpr int kVecPerPass = 4;                         // 16-byte vectors per th
 constexpr int kMaxChunks = 64;                         // chunks per row
 constexpr int kMaxPasses = 4;                          // passes per chunk
 constexpr int kMaxSlices = kMaxPasses * kVecPerPass;
-constexpr int kChunkTarget = 8192;                     // ids per chunk before rounding
+#ifndef SPEC_CHUNK_TARGET
+#define SPEC_CHUNK_TARGET 8192
+#endif
+#ifndef SPEC_DRAW_WAVES
+#define SPEC_DRAW_WAVES 2
+#endif
+#ifndef SPEC_MIN_BLOCKS
+#define SPEC_MIN_BLOCKS 6
+#endif
+constexpr int kChunkTarget = SPEC_CHUNK_TARGET;        // ids per chunk before rounding
+constexpr int kDrawWaves = SPEC_DRAW_WAVES;            // distance of the draw behind the rows
+constexpr int kMinBlocks = SPEC_MIN_BLOCKS;            // resident blocks per SM the registers allow
+constexpr int kMaxGroups = 65535;                      // grid z limit
 constexpr int kPlanWaitIters = 32;                     // optional bounded wait of a B unit (~15 us)
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -74,9 +86,8 @@ struct Geo {
   int CL;      // chunks per row
   int chunk;   // ids per chunk (multiple of 8)
   int nslots;  // row slots per sequence: target rows 0..gmax, then draft rows 0..gmax-1
-  int NA;      // A units per group (nslots * CL)
-  int G;       // units per group (NA, plus CL B units when sampling is possible)
   int delta;   // B units of sequence b sit in group b + delta
+  int b0, b1;  // sequences [b0, b1) of this launch
 };
 
 struct __align__(16) PlanRec {   // per sequence, published by the decider for the draw
@@ -177,6 +188,46 @@ __device__ __forceinline__ float prob(float x, float k, float mk, float inv_s) {
 // max(p - q, 0) with a rounded difference: exactly 0 wherever p == q.
 __device__ __forceinline__ float residual(float p, float q) { return fmaxf(__fsub_rn(p, q), 0.f); }
 
+// Packed pairs of f32 (sm_100+ .f32x2 forms): each lane of a pair is rounded exactly as the
+// scalar fma.rn / add.rn / mul.rn would round it, so packing changes no result bit.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "sub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 ex2x2(float2 a) { return make_float2(ex2(a.x), ex2(a.y)); }
+
 // Element formats.  A 16-byte vector holds kPerVec elements.
 struct Bf16 {
   using raw = uint16_t;
@@ -188,6 +239,11 @@ struct Bf16 {
   __device__ __forceinline__ static float get(const uint4& v, int j) {
     const uint32_t w = (j >> 1) == 0 ? v.x : (j >> 1) == 1 ? v.y : (j >> 1) == 2 ? v.z : v.w;
     return __uint_as_float((j & 1) ? (w & 0xffff0000u) : (w << 16));
+  }
+  // elements (2h, 2h+1) of a vector as a pair
+  __device__ __forceinline__ static float2 pair(const uint4& v, int h) {
+    const uint32_t w = h == 0 ? v.x : h == 1 ? v.y : h == 2 ? v.z : v.w;
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
   }
   // max over the vectors of one pass: bf16x2 max tree, one widening at the end
   __device__ __forceinline__ static float tmax(const uint4 (&v)[kVecPerPass]) {
@@ -212,6 +268,10 @@ struct F32 {
   __device__ __forceinline__ static float at(const raw* row, int64_t i) { return __ldg(row + i); }
   __device__ __forceinline__ static float get(const uint4& v, int j) {
     return __uint_as_float(j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w);
+  }
+  __device__ __forceinline__ static float2 pair(const uint4& v, int h) {
+    return h == 0 ? make_float2(__uint_as_float(v.x), __uint_as_float(v.y))
+                  : make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
   }
   __device__ __forceinline__ static float tmax(const uint4 (&v)[kVecPerPass]) {
     float a = -INFINITY;
@@ -248,6 +308,10 @@ struct Tile {
     if constexpr (kVec) return E::get(v[q], j);
     else return s[q * N + j];
   }
+  __device__ __forceinline__ float2 xp(int q, int h) const {
+    if constexpr (kVec) return E::pair(v[q], h);
+    else return make_float2(s[q * N + 2 * h], s[q * N + 2 * h + 1]);
+  }
 };
 
 template <class E, bool kVec>
@@ -265,12 +329,17 @@ __device__ __forceinline__ void tile_stats(const Tile<E, kVec>& t, float k, floa
   float s = 0.f;
   if (m != -INFINITY) {
     const float mk = __fmul_rn(m, k);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};   // independent chains, combined in a fixed order
+    const float2 kk = make_float2(k, k), nmk = make_float2(-mk, -mk);
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;   // four chains, combined in a fixed order
 #pragma unroll
     for (int q = 0; q < kVecPerPass; ++q)
 #pragma unroll
-      for (int j = 0; j < N; ++j) acc[j & 3] = __fadd_rn(acc[j & 3], ex2(fmaf(t.x(q, j), k, -mk)));
-    s = __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
+      for (int h = 0; h < N / 2; ++h) {
+        const float2 e = ex2x2(fma2(t.xp(q, h), kk, nmk));
+        if (h & 1) acc1 = add2(acc1, e);
+        else acc0 = add2(acc0, e);
+      }
+    s = __fadd_rn(__fadd_rn(acc0.x, acc0.y), __fadd_rn(acc1.x, acc1.y));
   }
   s = warp_sum(s);
   merge_ms(run_m, run_s, m, s, k);
@@ -308,6 +377,7 @@ struct Shared {
   float pd[SPEC_MAX_GAMMA], qd[SPEC_MAX_GAMMA];
   float wsum[kMaxSlices][kWarps];                 // selector: per-(slice, warp) weight sums
   int last, go, m, flags, owner, slice, warp_sel, token;
+  unsigned taken[2];
   float target_local, mass_out, run_sel;
   PlanRec plan;
 };
@@ -360,10 +430,22 @@ struct Seq {
 template <class E>
 __device__ __forceinline__ void weights(const uint4& vp, const uint4& vq, bool pair, float k, float mkp, float invp,
                                         float mkq, float invq, float (&w)[E::kPerVec], float (&p)[E::kPerVec]) {
+  // prob() and residual() on packed pairs: the same roundings lane by lane
+  const float2 kk = make_float2(k, k);
 #pragma unroll
-  for (int j = 0; j < E::kPerVec; ++j) {
-    p[j] = prob(E::get(vp, j), k, mkp, invp);
-    w[j] = pair ? residual(p[j], prob(E::get(vq, j), k, mkq, invq)) : p[j];
+  for (int h = 0; h < E::kPerVec / 2; ++h) {
+    const float2 pp = mul2(ex2x2(fma2(E::pair(vp, h), kk, make_float2(-mkp, -mkp))), make_float2(invp, invp));
+    p[2 * h] = pp.x;
+    p[2 * h + 1] = pp.y;
+    if (pair) {
+      const float2 qq = mul2(ex2x2(fma2(E::pair(vq, h), kk, make_float2(-mkq, -mkq))), make_float2(invq, invq));
+      const float2 d = sub2(pp, qq);
+      w[2 * h] = fmaxf(d.x, 0.f);
+      w[2 * h + 1] = fmaxf(d.y, 0.f);
+    } else {
+      w[2 * h] = pp.x;
+      w[2 * h + 1] = pp.y;
+    }
   }
 }
 
@@ -541,7 +623,7 @@ __device__ void draw_chunk(const Args& a, const Geo& geo, const Work& w, const S
   const raw* rq = pair ? sq.Q + int64_t(pl.m) * a.V : rp;
   const int64_t lo = int64_t(c) * geo.chunk;
   const int64_t hi = lo + geo.chunk < a.V ? lo + geo.chunk : a.V;
-  float ws = 0.f, ps = 0.f;
+  float2 ws2 = make_float2(0.f, 0.f), ps2 = ws2;
   // two vectors of each row in flight per thread: the rows are normally still in L2
   constexpr int kDrawStep = kThreads * 2 * N;
   for (int64_t e0 = lo; e0 < hi; e0 += kDrawStep) {
@@ -557,12 +639,13 @@ __device__ void draw_chunk(const Args& a, const Geo& geo, const Work& w, const S
       float wv[N], pv[N];
       weights<E>(vp[q], vq[q], pair, sq.k, pl.mkp, pl.invp, pl.mkq, pl.invq, wv, pv);
 #pragma unroll
-      for (int j = 0; j < N; ++j) {
-        ws = __fadd_rn(ws, wv[j]);
-        ps = __fadd_rn(ps, pv[j]);
+      for (int h = 0; h < N / 2; ++h) {
+        ws2 = add2(ws2, make_float2(wv[2 * h], wv[2 * h + 1]));
+        ps2 = add2(ps2, make_float2(pv[2 * h], pv[2 * h + 1]));
       }
     }
   }
+  float ws = __fadd_rn(ws2.x, ws2.y), ps = __fadd_rn(ps2.x, ps2.y);
   ws = warp_sum(ws);
   ps = warp_sum(ps);
   if (lane == 0) sm.wp[warp] = make_float2(ws, ps);
@@ -591,29 +674,32 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
   const int b = sq.b, g = sq.g, gmax = a.gmax, CL = geo.CL;
   const float k = sq.k;
   __threadfence();
+  // one warp per row: lanes take chunks c and c + 32 (at most 64 chunks)
   const float2* part = w.part + int64_t(b) * geo.nslots * CL;
-  for (int slot = tid; slot < geo.nslots; slot += kThreads) {
+  for (int slot = warp; slot < geo.nslots; slot += kWarps) {
     if (!sq.slot_valid(slot, gmax)) continue;
     const float2* pp = part + slot * CL;
+    const float2 none = make_float2(-INFINITY, sq.sampling ? 0.f : __int_as_float(INT_MAX));
+    const float2 p0 = lane < CL ? __ldcg(&pp[lane]) : none;
+    const float2 p1 = lane + 32 < CL ? __ldcg(&pp[lane + 32]) : none;
     if (sq.sampling) {
-      float M = -INFINITY;
-      for (int c = 0; c < CL; ++c) M = fmaxf(M, __ldcg(&pp[c]).x);
+      const float M = warp_max(fmaxf(p0.x, p1.x));
       float S = 0.f;
-      if (M != -INFINITY)
-        for (int c = 0; c < CL; ++c) {
-          const float2 p = __ldcg(&pp[c]);
-          if (p.x != -INFINITY) S = __fadd_rn(S, __fmul_rn(p.y, ex2(__fmul_rn(p.x - M, k))));
-        }
-      sm.rowM[slot] = M;
-      sm.rowInvS[slot] = __frcp_rn(S);
-    } else {
-      float bv = -INFINITY;
-      int bi = INT_MAX;
-      for (int c = 0; c < CL; ++c) {
-        const float2 p = __ldcg(&pp[c]);
-        if (better(p.x, __float_as_int(p.y), bv, bi)) { bv = p.x; bi = __float_as_int(p.y); }
+      if (M != -INFINITY) {
+        const float t0 = p0.x == -INFINITY ? 0.f : __fmul_rn(p0.y, ex2(__fmul_rn(p0.x - M, k)));
+        const float t1 = p1.x == -INFINITY ? 0.f : __fmul_rn(p1.y, ex2(__fmul_rn(p1.x - M, k)));
+        S = warp_sum(__fadd_rn(t0, t1));
       }
-      sm.rowArg[slot] = bi;
+      if (lane == 0) {
+        sm.rowM[slot] = M;
+        sm.rowInvS[slot] = __frcp_rn(S);
+      }
+    } else {
+      float bv = p0.x;
+      int bi = __float_as_int(p0.y);
+      if (better(p1.x, __float_as_int(p1.y), bv, bi)) { bv = p1.x; bi = __float_as_int(p1.y); }
+      warp_argmax(bv, bi);
+      if (lane == 0) sm.rowArg[slot] = bi;
     }
   }
   __syncthreads();
@@ -697,16 +783,17 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
   __syncthreads();
   const PlanRec pl = sm.plan;
   // the chunks whose B units gave up before the plan was out are the decider's
-  for (int c = 0; c < CL; ++c) {
-    if (tid == 0) {
-      int s = ld_acquire(&w.state[int64_t(b) * CL + c]);
-      sm.go = s == kChunkGivenUp && atom_cas(&w.state[int64_t(b) * CL + c], kChunkGivenUp, kChunkDecider) == kChunkGivenUp;
-    }
-    __syncthreads();
-    const bool go = sm.go;
-    __syncthreads();
-    if (go) draw_chunk<E, kVec, kMixed>(a, geo, w, sq, pl, c, sm);
+  if (tid < 2) sm.taken[tid] = 0u;
+  __syncthreads();
+  if (tid < CL) {
+    int* st = &w.state[int64_t(b) * CL + tid];
+    if (ld_acquire(st) == kChunkGivenUp && atom_cas(st, kChunkGivenUp, kChunkDecider) == kChunkGivenUp)
+      atomicOr(&sm.taken[tid >> 5], 1u << (tid & 31));
   }
+  __syncthreads();
+  const unsigned taken0 = sm.taken[0], taken1 = sm.taken[1];
+  for (int c = 0; c < CL; ++c)
+    if ((c < 32 ? taken0 >> c : taken1 >> (c - 32)) & 1u) draw_chunk<E, kVec, kMixed>(a, geo, w, sq, pl, c, sm);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -714,19 +801,20 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
 // ------------------------------------------------------------------------------------------
 
 template <class E, bool kVec, bool kMixed>
-__global__ void __launch_bounds__(kThreads, 6) verify_kernel(const Args a, const Geo geo, const Work w) {
+__global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args a, const Geo geo, const Work w) {
   using raw = typename E::raw;
   constexpr int N = E::kPerVec;
   constexpr int kPass = kThreads * kVecPerPass * N;
   __shared__ Shared sm;
   const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
-  const int grp = int(blockIdx.x) / geo.G, off = int(blockIdx.x) - grp * geo.G;
+  // blockIdx = (chunk c, row slot or nslots for the draw, group); blocks are dispatched in
+  // x-fastest order, so a group's A units come first and its B units last
+  const int c = int(blockIdx.x), slot = int(blockIdx.y), grp = geo.b0 + int(blockIdx.z);
 
-  if (off < geo.NA) {
+  if (slot < geo.nslots) {
     // ---------------- A unit: chunk c of one row -------------------------------------------
     const int b = grp;
-    if (b >= a.B) return;
-    const int slot = off / geo.CL, c = off - slot * geo.CL;
+    if (b >= geo.b1) return;
     const Seq<E, kMixed> sq(a, b);
     if (!sq.slot_valid(slot, a.gmax)) return;
     const raw* row = sq.row(slot, a.gmax, a.V);
@@ -759,15 +847,23 @@ __global__ void __launch_bounds__(kThreads, 6) verify_kernel(const Args a, const
     if (!sq.sampling) warp_argmax(rm, ri);
     if (lane == 0) sm.wp[warp] = make_float2(rm, sq.sampling ? rs : __int_as_float(ri));
     __syncthreads();
-    if (tid == 0) {
-      float2 acc = sm.wp[0];
-      for (int wi = 1; wi < kWarps; ++wi) {
-        const float2 p = sm.wp[wi];
-        if (sq.sampling) merge_ms(acc.x, acc.y, p.x, p.y, sq.k);
-        else if (better(p.x, __float_as_int(p.y), acc.x, __float_as_int(acc.y))) acc = p;
+    if (warp == 0) {
+      // the block's partial from the warps' partials, lanes in parallel
+      float2 p = lane < kWarps ? sm.wp[lane] : make_float2(-INFINITY, sq.sampling ? 0.f : __int_as_float(INT_MAX));
+      if (sq.sampling) {
+        const float M = warp_max(p.x);
+        float S = 0.f;
+        if (M != -INFINITY) S = warp_sum(p.x == -INFINITY ? 0.f : __fmul_rn(p.y, ex2(__fmul_rn(p.x - M, sq.k))));
+        p = make_float2(M, S);
+      } else {
+        int pi = __float_as_int(p.y);
+        warp_argmax(p.x, pi);
+        p.y = __int_as_float(pi);
       }
-      w.part[(int64_t(b) * geo.nslots + slot) * geo.CL + c] = acc;
-      sm.last = atom_add_acq_rel(&w.cnt[b], 1) == geo.CL * sq.nrows() - 1;
+      if (lane == 0) {
+        w.part[(int64_t(b) * geo.nslots + slot) * geo.CL + c] = p;
+        sm.last = atom_add_acq_rel(&w.cnt[b], 1) == geo.CL * sq.nrows() - 1;
+      }
     }
     __syncthreads();
     if (sm.last) decide<E, kVec, kMixed>(a, geo, w, sq, sm);
@@ -777,8 +873,7 @@ __global__ void __launch_bounds__(kThreads, 6) verify_kernel(const Args a, const
   if constexpr (kMixed) {
     // ---------------- B unit: draw chunk c of sequence grp - delta ------------------------
     const int b = grp - geo.delta;
-    if (b < 0 || b >= a.B) return;
-    const int c = off - geo.NA;
+    if (b < geo.b0 || b >= geo.b1) return;
     const Seq<E, kMixed> sq(a, b);
     if (!sq.sampling) return;
     if (tid == 0) {
@@ -946,9 +1041,8 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
   geo.CL = sp.cl;
   geo.chunk = sp.chunk;
   geo.nslots = kMixed ? 2 * args.gmax + 1 : args.gmax + 1;   // greedy-only reads no draft rows
-  geo.NA = geo.nslots * geo.CL;
-  geo.G = geo.NA + (kMixed ? geo.CL : 0);
-  // B units of a sequence come about two waves of resident blocks after its A units
+  const int G = geo.nslots * geo.CL + (kMixed ? geo.CL : 0);   // units per group
+  // B units of a sequence come about kDrawWaves waves of resident blocks after its A units
   int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -967,17 +1061,21 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
   const int64_t resident = int64_t(sms) * per_sm;
-  geo.delta = kMixed ? int((2 * resident + geo.G - 1) / geo.G) : 0;
-  const int64_t blocks = (int64_t(args.B) + geo.delta) * geo.G;
-  if (blocks > INT_MAX) {
-    set_error("batch too large: %lld blocks", (long long)blocks);
-    return SPEC_ENOSPACE;
-  }
+  geo.delta = kMixed ? int((kDrawWaves * resident + G - 1) / G) : 0;
+  if (geo.delta > kMaxGroups / 2) geo.delta = kMaxGroups / 2;
   const Work w = ws_views(ws, L);
-  fn<<<unsigned(blocks), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(args, geo, w);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "verify kernel launch");
-  count_launch();
+  // one launch covers at most kMaxGroups groups (the grid's z limit); larger batches take
+  // several launches over consecutive sequence ranges, each complete on its own
+  const int per_launch = kMaxGroups - geo.delta;
+  for (int b0 = 0; b0 < args.B; b0 += per_launch) {
+    geo.b0 = b0;
+    geo.b1 = b0 + per_launch < args.B ? b0 + per_launch : args.B;
+    const dim3 grid(unsigned(geo.CL), unsigned(geo.nslots + (kMixed ? 1 : 0)), unsigned(geo.b1 - b0 + geo.delta));
+    fn<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(args, geo, w);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "verify kernel launch");
+    count_launch();
+  }
   return SPEC_OK;
 }
 
