@@ -188,8 +188,9 @@ __device__ __forceinline__ float prob(float x, float k, float mk, float inv_s) {
 // max(p - q, 0) with a rounded difference: exactly 0 wherever p == q.
 __device__ __forceinline__ float residual(float p, float q) { return fmaxf(__fsub_rn(p, q), 0.f); }
 
-// Packed pairs of f32 (sm_100+ .f32x2 forms): each lane of a pair is rounded exactly as the
-// scalar fma.rn / add.rn / mul.rn would round it, so packing changes no result bit.
+// Packed pairs of f32 (sm_100+ .f32x2 forms): each lane is rounded as the scalar fma.rn /
+// add.rn would round it.  Only an explicit fma and sums of exponentials are packed: a packed
+// product may be fused by the code generator into a following packed add or subtract.
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
   float2 d;
   asm("{\n\t.reg .b64 a, b, c, d;\n\t"
@@ -204,24 +205,6 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
   asm("{\n\t.reg .b64 a, b, d;\n\t"
       "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
       "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
-  float2 d;
-  asm("{\n\t.reg .b64 a, b, d;\n\t"
-      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-      "sub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-  float2 d;
-  asm("{\n\t.reg .b64 a, b, d;\n\t"
-      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
       : "=f"(d.x), "=f"(d.y)
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return d;
@@ -430,21 +413,22 @@ struct Seq {
 template <class E>
 __device__ __forceinline__ void weights(const uint4& vp, const uint4& vq, bool pair, float k, float mkp, float invp,
                                         float mkq, float invq, float (&w)[E::kPerVec], float (&p)[E::kPerVec]) {
-  // prob() and residual() on packed pairs: the same roundings lane by lane
+  // prob() and residual() with the exponent argument as a packed fma.  The products and the
+  // difference stay scalar mul.rn / sub.rn, which are never fused: a product fused into the
+  // difference would leave its rounding error behind where p == q must give exactly 0.
   const float2 kk = make_float2(k, k);
 #pragma unroll
   for (int h = 0; h < E::kPerVec / 2; ++h) {
-    const float2 pp = mul2(ex2x2(fma2(E::pair(vp, h), kk, make_float2(-mkp, -mkp))), make_float2(invp, invp));
-    p[2 * h] = pp.x;
-    p[2 * h + 1] = pp.y;
+    const float2 ep = ex2x2(fma2(E::pair(vp, h), kk, make_float2(-mkp, -mkp)));
+    p[2 * h] = __fmul_rn(ep.x, invp);
+    p[2 * h + 1] = __fmul_rn(ep.y, invp);
     if (pair) {
-      const float2 qq = mul2(ex2x2(fma2(E::pair(vq, h), kk, make_float2(-mkq, -mkq))), make_float2(invq, invq));
-      const float2 d = sub2(pp, qq);
-      w[2 * h] = fmaxf(d.x, 0.f);
-      w[2 * h + 1] = fmaxf(d.y, 0.f);
+      const float2 eq = ex2x2(fma2(E::pair(vq, h), kk, make_float2(-mkq, -mkq)));
+      w[2 * h] = residual(p[2 * h], __fmul_rn(eq.x, invq));
+      w[2 * h + 1] = residual(p[2 * h + 1], __fmul_rn(eq.y, invq));
     } else {
-      w[2 * h] = pp.x;
-      w[2 * h + 1] = pp.y;
+      w[2 * h] = p[2 * h];
+      w[2 * h + 1] = p[2 * h + 1];
     }
   }
 }
