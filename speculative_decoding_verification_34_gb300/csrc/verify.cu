@@ -287,9 +287,28 @@ struct Tile {
       }
     }
   }
+  // a pass that lies entirely below hi: no bounds to check
+  __device__ __forceinline__ void load_full(const typename E::raw* row, int64_t e0, int tid) {
+    if constexpr (kVec) {
+#pragma unroll
+      for (int q = 0; q < kVecPerPass; ++q) v[q] = ld_stream(row + e0 + int64_t(q * kThreads + tid) * N);
+    } else {
+      load(row, e0, e0 + int64_t(kThreads) * kVecPerPass * N, tid);
+    }
+  }
   __device__ __forceinline__ float x(int q, int j) const {
     if constexpr (kVec) return E::get(v[q], j);
     else return s[q * N + j];
+  }
+  // element (q, j) for run-time q and j, through static indices only (no local memory)
+  __device__ __forceinline__ float pick(int q, int j) const {
+    float r = 0.f;
+#pragma unroll
+    for (int qq = 0; qq < kVecPerPass; ++qq)
+#pragma unroll
+      for (int jj = 0; jj < N; ++jj)
+        if (qq == q && jj == j) r = x(qq, jj);
+    return r;
   }
   __device__ __forceinline__ float2 xp(int q, int h) const {
     if constexpr (kVec) return E::pair(v[q], h);
@@ -326,6 +345,47 @@ __device__ __forceinline__ void tile_stats(const Tile<E, kVec>& t, float k, floa
   }
   s = warp_sum(s);
   merge_ms(run_m, run_s, m, s, k);
+}
+
+// Per-thread running (max m, sum of 2^((x-m)k)) over the passes of a chunk: the sum is rescaled
+// when the max grows, and the warp is reduced once at the end (warp_stats).  Rows of -inf
+// give (-inf, 0) without NaN.
+template <class E, bool kVec>
+__device__ __forceinline__ void thread_stats(const Tile<E, kVec>& t, float k, float& run_m, float& run_s) {
+  constexpr int N = E::kPerVec;
+  float m;
+  if constexpr (kVec) {
+    m = E::tmax(t.v);
+  } else {
+    m = -INFINITY;
+#pragma unroll
+    for (int a = 0; a < kVecPerPass * N; ++a) m = fmaxf(m, t.s[a]);
+  }
+  const float mn = fmaxf(run_m, m);
+  const bool fin = mn != -INFINITY;
+  const float mk = fin ? __fmul_rn(mn, k) : 0.f;
+  const float scale = fin ? ex2(__fmul_rn(run_m - mn, k)) : 1.f;
+  const float2 kk = make_float2(k, k), nmk = make_float2(-mk, -mk);
+  float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;   // four chains, combined in a fixed order
+#pragma unroll
+  for (int q = 0; q < kVecPerPass; ++q)
+#pragma unroll
+    for (int h = 0; h < N / 2; ++h) {
+      const float2 e = ex2x2(fma2(t.xp(q, h), kk, nmk));
+      if (h & 1) acc1 = add2(acc1, e);
+      else acc0 = add2(acc0, e);
+    }
+  run_s = __fadd_rn(__fmul_rn(run_s, scale), __fadd_rn(__fadd_rn(acc0.x, acc0.y), __fadd_rn(acc1.x, acc1.y)));
+  run_m = mn;
+}
+
+// the warp's (max, sum) from its threads' running statistics; every lane gets the result
+__device__ __forceinline__ void warp_stats(float& m, float& s, float k) {
+  const float M = warp_max(m);
+  float S = 0.f;
+  if (M != -INFINITY) S = warp_sum(m == -INFINITY ? 0.f : __fmul_rn(s, ex2(__fmul_rn(m - M, k))));
+  m = M;
+  s = S;
 }
 
 template <class E, bool kVec>
@@ -806,29 +866,37 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
     const int64_t hi = lo + geo.chunk < a.V ? lo + geo.chunk : a.V;
     const int i = slot <= a.gmax ? slot : slot - a.gmax - 1;
     const int d = (sq.sampling && i < sq.g) ? __ldg(&a.draft_tokens[int64_t(b) * a.gmax + i]) : -1;
+    // where this row's draft id sits: pass dp, vector dq of thread dt, element dj
+    int dp = -1, dq = 0, dt = -1, dj = 0;
+    if (int64_t(d) >= lo && int64_t(d) < hi) {
+      int off = int(int64_t(d) - lo);
+      dp = off / kPass;
+      off -= dp * kPass;
+      dq = off / (kThreads * N);
+      off -= dq * kThreads * N;
+      dt = off / N;
+      dj = off - dt * N;
+    }
     float rm = -INFINITY, rs = 0.f;
     int ri = INT_MAX;
-    for (int64_t e0 = lo; e0 < hi; e0 += kPass) {
+    int pass = 0;
+    for (int64_t e0 = lo; e0 < hi; e0 += kPass, ++pass) {
       Tile<E, kVec> t;
-      t.load(row, e0, hi, tid);
+      if (e0 + kPass <= hi) t.load_full(row, e0, tid);
+      else t.load(row, e0, hi, tid);
       if (sq.sampling) {
-        if (int64_t(d) >= e0 && int64_t(d) < e0 + kPass && int64_t(d) < hi) {
+        if (pass == dp && tid == dt) {
           // the logit at this row's draft id, from the registers that hold it
-#pragma unroll
-          for (int q = 0; q < kVecPerPass; ++q) {
-            const int64_t o = int64_t(d) - (e0 + int64_t(q * kThreads + tid) * N);
-            if (o >= 0 && o < N) {
-              w.xd[int64_t(b) * geo.nslots + slot] = t.x(q, int(o));
-              __threadfence();
-            }
-          }
+          w.xd[int64_t(b) * geo.nslots + slot] = t.pick(dq, dj);
+          __threadfence();
         }
-        tile_stats(t, sq.k, rm, rs);
+        thread_stats(t, sq.k, rm, rs);
       } else {
         tile_argmax(t, e0, tid, rm, ri);
       }
     }
-    if (!sq.sampling) warp_argmax(rm, ri);
+    if (sq.sampling) warp_stats(rm, rs, sq.k);
+    else warp_argmax(rm, ri);
     if (lane == 0) sm.wp[warp] = make_float2(rm, sq.sampling ? rs : __int_as_float(ri));
     __syncthreads();
     if (warp == 0) {
