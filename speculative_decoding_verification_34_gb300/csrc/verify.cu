@@ -5,22 +5,23 @@
 // max(p-q,0)/R and the bonus draw) and the "M013" knowledge-base card (§03-§05, including the
 // R = 0 remark).  How it is computed is this library's own design for sm_103a.
 //
-// The vocabulary of every row is cut into CL chunks of `chunk` ids.  The grid is a list of
-// block-sized units in groups: group g holds the A units of sequence g, then the B units of
-// sequence g - delta (delta groups ~ two waves of resident blocks).
+// Every row is cut into CL row chunks of `chunk` ids for the statistics pass and into DCL
+// draw chunks of `dchunk` ids for the final draw.  The grid is a list of block-sized units
+// in groups: group g holds the A units of sequence g, then the B units of sequence
+// g - delta (delta groups ~ kDrawWaves waves of resident blocks).
 //
-//   A(b, row, c)  reads chunk c of one row of sequence b once from HBM (128-bit loads), one
-//                 ex2 per sampled element, and writes a (max, sum 2^((x-max)k)) partial, or an
-//                 (argmax value, id) partial for greedy rows, to the workspace; the unit whose
-//                 chunk holds a draft id also records that logit.  The last A unit of b to
-//                 arrive (a counter) is the *decider*: it combines the partials in a fixed
-//                 order, takes the acceptance decisions, finds m, and either writes the greedy
-//                 result or publishes a plan for the final draw.
-//   B(b, c)       draws on the plan: chunk c of the row the last token is drawn from -- row m
-//                 of p and q after a rejection, the bonus row otherwise; normally still in L2 --
-//                 reduced to its residual and p masses.  The last chunk of b to finish makes its
-//                 block the *selector*: it locates the chunk holding u*R, rescans that chunk
-//                 and writes the outputs.
+//   A(b, row, c)  reads row chunk c of one row of sequence b once from HBM (128-bit loads),
+//                 one ex2 per sampled element, and writes a (max, sum 2^((x-max)k)) partial, or
+//                 an (argmax value, id) partial for greedy rows, to the workspace; the unit
+//                 whose chunk holds the row's draft id also records that logit.  The last A
+//                 unit of b to arrive (a counter) is the *decider*: it combines the partials in
+//                 a fixed order, takes the acceptance decisions, finds m, and either writes the
+//                 greedy result or publishes a plan for the final draw.
+//   B(b, dc)      draws on the plan: draw chunk dc of the row the last token is drawn from --
+//                 row m of p and q after a rejection, the bonus row otherwise; normally still
+//                 in L2 -- reduced to its residual and p masses.  The last draw chunk of b to
+//                 finish makes its block the *selector*: it locates the chunk holding u*R,
+//                 rescans that chunk and writes the outputs.
 //
 // No block ever has to wait for another.  A B unit may wait a short, bounded while for its
 // plan; each draw chunk then goes through a small state machine (untouched -> claimed by its B
@@ -41,20 +42,24 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kVecPerPass = 4;                         // 16-byte vectors per thread per pass
-constexpr int kMaxChunks = 64;                         // chunks per row
-constexpr int kMaxPasses = 4;                          // passes per chunk
-constexpr int kMaxSlices = kMaxPasses * kVecPerPass;
+constexpr int kVecPerPass = 4;                         // 16-byte vectors per thread per row pass
+constexpr int kDrawVec = 2;                            // vectors of each row per thread per draw step
+constexpr int kMaxChunks = 64;                         // row chunks, and draw chunks, per row
+constexpr int kMaxSlices = 16;                         // kThreads-vector slices per draw chunk
 #ifndef SPEC_CHUNK_TARGET
-#define SPEC_CHUNK_TARGET 8192
+#define SPEC_CHUNK_TARGET 16384
+#endif
+#ifndef SPEC_DRAW_CHUNK_TARGET
+#define SPEC_DRAW_CHUNK_TARGET 4096
 #endif
 #ifndef SPEC_DRAW_WAVES
-#define SPEC_DRAW_WAVES 2
+#define SPEC_DRAW_WAVES 3
 #endif
 #ifndef SPEC_MIN_BLOCKS
 #define SPEC_MIN_BLOCKS 6
 #endif
-constexpr int kChunkTarget = SPEC_CHUNK_TARGET;        // ids per chunk before rounding
+constexpr int kChunkTarget = SPEC_CHUNK_TARGET;        // ids per row chunk before rounding
+constexpr int kDrawChunkTarget = SPEC_DRAW_CHUNK_TARGET;   // ids per draw chunk before rounding
 constexpr int kDrawWaves = SPEC_DRAW_WAVES;            // distance of the draw behind the rows
 constexpr int kMinBlocks = SPEC_MIN_BLOCKS;            // resident blocks per SM the registers allow
 constexpr int kMaxGroups = 65535;                      // grid z limit
@@ -83,11 +88,13 @@ struct Args {
 };
 
 struct Geo {
-  int CL;      // chunks per row
-  int chunk;   // ids per chunk (multiple of 8)
-  int nslots;  // row slots per sequence: target rows 0..gmax, then draft rows 0..gmax-1
-  int delta;   // B units of sequence b sit in group b + delta
-  int b0, b1;  // sequences [b0, b1) of this launch
+  int CL;       // row chunks per row
+  int chunk;    // ids per row chunk (multiple of 8)
+  int DCL;      // draw chunks per row
+  int dchunk;   // ids per draw chunk (multiple of 8)
+  int nslots;   // row slots per sequence: target rows 0..gmax, then draft rows 0..gmax-1
+  int delta;    // B units of sequence b sit in group b + delta
+  int b0, b1;   // sequences [b0, b1) of this launch
 };
 
 struct __align__(16) PlanRec {   // per sequence, published by the decider for the draw
@@ -96,14 +103,14 @@ struct __align__(16) PlanRec {   // per sequence, published by the decider for t
 };
 
 struct Work {      // views into the caller's workspace
-  int* cnt;        // [B] A arrivals            (counter header)
-  int* bdone;      // [B] draw-chunk arrivals   (counter header)
-  int* ready;      // [B] plan published        (counter header)
-  int* state;      // [B][CL] draw-chunk states (counter header)
+  int* cnt;        // [B] A arrivals               (counter header)
+  int* bdone;      // [B] draw-chunk arrivals      (counter header)
+  int* ready;      // [B] plan published           (counter header)
+  int* state;      // [B][DCL] draw-chunk states   (counter header)
   PlanRec* plan;   // [B]
   float2* part;    // [B][nslots][CL]
   float* xd;       // [B][nslots] logit at the draft id of that row
-  float2* mass;    // [B][CL] (residual mass, p mass)
+  float2* mass;    // [B][DCL] (residual mass, p mass)
 };
 
 // ------------------------------------------------------------------------------------------
@@ -127,18 +134,6 @@ __device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
   int old;
   asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
-}
-
-// 16-byte global -> shared copy that bypasses L1; src_bytes = 0 zero-fills without reading.
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
-  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Warp-wide max in one instruction (sm_100+ f32 redux); -inf is the identity.
@@ -167,17 +162,6 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
     const int i2 = __shfl_xor_sync(kFull, i, o);
     if (better(v2, i2, v, i)) { v = v2; i = i2; }
   }
-}
-
-// Merge two (max, sum of 2^((x-max)k)) partials; (-inf, 0) is the empty partial.  Products
-// and sums are explicitly rounded so bit-identical rows always give bit-identical statistics.
-__device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2, float k) {
-  const float M = fmaxf(m, m2);
-  if (M == -INFINITY) return;
-  const float a = (m == -INFINITY) ? 0.f : __fmul_rn(s, ex2(__fmul_rn(m - M, k)));
-  const float b = (m2 == -INFINITY) ? 0.f : __fmul_rn(s2, ex2(__fmul_rn(m2 - M, k)));
-  m = M;
-  s = __fadd_rn(a, b);
 }
 
 // p_v = 2^((x_v - M) k) / S, evaluated as ex2(x*k - M*k) * (1/S) with a rounded product.
@@ -300,52 +284,11 @@ struct Tile {
     if constexpr (kVec) return E::get(v[q], j);
     else return s[q * N + j];
   }
-  // element (q, j) for run-time q and j, through static indices only (no local memory)
-  __device__ __forceinline__ float pick(int q, int j) const {
-    float r = 0.f;
-#pragma unroll
-    for (int qq = 0; qq < kVecPerPass; ++qq)
-#pragma unroll
-      for (int jj = 0; jj < N; ++jj)
-        if (qq == q && jj == j) r = x(qq, jj);
-    return r;
-  }
   __device__ __forceinline__ float2 xp(int q, int h) const {
     if constexpr (kVec) return E::pair(v[q], h);
     else return make_float2(s[q * N + 2 * h], s[q * N + 2 * h + 1]);
   }
 };
-
-template <class E, bool kVec>
-__device__ __forceinline__ void tile_stats(const Tile<E, kVec>& t, float k, float& run_m, float& run_s) {
-  constexpr int N = E::kPerVec;
-  float m;
-  if constexpr (kVec) {
-    m = E::tmax(t.v);
-  } else {
-    m = -INFINITY;
-#pragma unroll
-    for (int a = 0; a < kVecPerPass * N; ++a) m = fmaxf(m, t.s[a]);
-  }
-  m = warp_max(m);
-  float s = 0.f;
-  if (m != -INFINITY) {
-    const float mk = __fmul_rn(m, k);
-    const float2 kk = make_float2(k, k), nmk = make_float2(-mk, -mk);
-    float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;   // four chains, combined in a fixed order
-#pragma unroll
-    for (int q = 0; q < kVecPerPass; ++q)
-#pragma unroll
-      for (int h = 0; h < N / 2; ++h) {
-        const float2 e = ex2x2(fma2(t.xp(q, h), kk, nmk));
-        if (h & 1) acc1 = add2(acc1, e);
-        else acc0 = add2(acc0, e);
-      }
-    s = __fadd_rn(__fadd_rn(acc0.x, acc0.y), __fadd_rn(acc1.x, acc1.y));
-  }
-  s = warp_sum(s);
-  merge_ms(run_m, run_s, m, s, k);
-}
 
 // Per-thread running (max m, sum of 2^((x-m)k)) over the passes of a chunk: the sum is rescaled
 // when the max grows, and the warp is reduced once at the end (warp_stats).  Rows of -inf
@@ -409,6 +352,17 @@ __device__ __forceinline__ int atom_cas(int* p, int cmp, int val) {
 __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// inclusive prefix sum over the warp's lanes, in a fixed association order
+__device__ __forceinline__ float warp_incl_scan(float v) {
+  const int lane = int(threadIdx.x) & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v = __fadd_rn(v, y);
+  }
   return v;
 }
 
@@ -517,60 +471,67 @@ __device__ __forceinline__ uint4 vec_at(const typename E::raw* row, int64_t e, i
 }
 
 // ------------------------------------------------------------------------------------------
-// the draw: chunk masses, then the selector
+// the draw: draw-chunk masses, then the selector
 // ------------------------------------------------------------------------------------------
 
+// Inverse CDF over the draw chunks of b: the owner chunk holds the smallest id whose running
+// weight exceeds u * total; that chunk is rescanned in ascending id order.  Slice s of a draw
+// chunk covers ids lo + s*kThreads*N .. + kThreads*N - 1, thread t the N ids from
+// lo + (s*kThreads + t)*N, so (slice, warp, lane, element) is ascending id order.
 template <class E, bool kVec, bool kMixed>
 __device__ void select(const Args& a, const Geo& geo, const Work& w, const Seq<E, kMixed>& sq, const PlanRec pl,
                        Shared& sm) {
   using raw = typename E::raw;
   constexpr int N = E::kPerVec;
-  constexpr int kPass = kThreads * kVecPerPass * N;
+  constexpr int kSlice = kThreads * N;
   const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
-  const int b = sq.b, gmax = a.gmax, CL = geo.CL;
+  const int b = sq.b, gmax = a.gmax, DCL = geo.DCL;
   const bool pair = pl.pair != 0;
-  __threadfence();
-  if (tid == 0) {
-    const float2* ms = w.mass + int64_t(b) * CL;
-    float R = 0.f, Pm = 0.f;
-    for (int c = 0; c < CL; ++c) {
-      const float2 x = __ldcg(&ms[c]);
-      R = __fadd_rn(R, x.x);
-      Pm = __fadd_rn(Pm, x.y);
-    }
+  if (warp == 0) {
+    // chunk masses, lanes c and c + 32, prefix sums in ascending chunk order
+    const float2* ms = w.mass + int64_t(b) * DCL;
+    const float2 x0 = lane < DCL ? __ldcg(&ms[lane]) : make_float2(0.f, 0.f);
+    const float2 x1 = lane + 32 < DCL ? __ldcg(&ms[lane + 32]) : make_float2(0.f, 0.f);
+    const float r0 = warp_incl_scan(x0.x), p0 = warp_incl_scan(x0.y);
+    const float rt0 = __shfl_sync(kFull, r0, 31), pt0 = __shfl_sync(kFull, p0, 31);
+    const float r1 = __fadd_rn(rt0, warp_incl_scan(x1.x)), p1 = __fadd_rn(pt0, warp_incl_scan(x1.y));
+    const float R = __shfl_sync(kFull, r1, 31), Pm = __shfl_sync(kFull, p1, 31);
     const bool use_w = !pair || R > 0.f;   // bonus: the weights are p itself
-    int f = pl.flags;
-    if (!use_w) f |= SPEC_ST_R_ZERO | kInternalDrawP;
+    const float w0 = use_w ? x0.x : x0.y, w1 = use_w ? x1.x : x1.y;
+    const float i0 = use_w ? r0 : p0, i1 = use_w ? r1 : p1;
     const float total = use_w ? R : Pm;
     const float target = __fmul_rn(a.u_sample[b], total);
-    int owner = -1, last = 0;
-    float excl = 0.f, run = 0.f, excl_last = 0.f;
-    for (int c = 0; c < CL; ++c) {
-      const float2 x = __ldcg(&ms[c]);
-      const float wc = use_w ? x.x : x.y;
-      if (wc > 0.f) { last = c; excl_last = run; }
-      const float nr = __fadd_rn(run, wc);
-      if (owner < 0 && nr > target && wc > 0.f) { owner = c; excl = run; }
-      run = nr;
+    // exclusive prefix of each chunk: the inclusive prefix of the one before it
+    float e0 = __shfl_up_sync(kFull, i0, 1), e1 = __shfl_up_sync(kFull, i1, 1);
+    const float t0 = __shfl_sync(kFull, i0, 31);
+    if (lane == 0) { e0 = 0.f; e1 = t0; }
+    const unsigned hit0 = __ballot_sync(kFull, w0 > 0.f && i0 > target);
+    const unsigned hit1 = __ballot_sync(kFull, w1 > 0.f && i1 > target);
+    const unsigned pos0 = __ballot_sync(kFull, w0 > 0.f), pos1 = __ballot_sync(kFull, w1 > 0.f);
+    int owner;
+    if (hit0) owner = __ffs(hit0) - 1;
+    else if (hit1) owner = 32 + __ffs(hit1) - 1;
+    else if (pos1) owner = 32 + 31 - __clz(pos1);   // rounding left u*total past the end
+    else owner = pos0 ? 31 - __clz(pos0) : 0;
+    const float excl = __shfl_sync(kFull, owner < 32 ? e0 : e1, owner & 31);
+    if (lane == 0) {
+      int f = pl.flags;
+      if (!use_w) f |= SPEC_ST_R_ZERO | kInternalDrawP;
+      sm.owner = owner;
+      sm.flags = f;
+      sm.target_local = __fsub_rn(target, excl);
+      sm.mass_out = pair ? (use_w ? R : 0.f) : Pm;
     }
-    if (owner < 0) { owner = last; excl = excl_last; }
-    sm.owner = owner;
-    sm.flags = f;
-    sm.target_local = __fsub_rn(target, excl);
-    sm.mass_out = pair ? (use_w ? R : 0.f) : R;
   }
   __syncthreads();
   const bool draw_p = !pair || (sm.flags & kInternalDrawP);
-  const int64_t lo = int64_t(sm.owner) * geo.chunk;
-  const int64_t hi = lo + geo.chunk < a.V ? lo + geo.chunk : a.V;
+  const int64_t lo = int64_t(sm.owner) * geo.dchunk;
+  const int64_t hi = lo + geo.dchunk < a.V ? lo + geo.dchunk : a.V;
   const raw* rp = sq.P + int64_t(pl.m) * a.V;
   const raw* rq = pair ? sq.Q + int64_t(pl.m) * a.V : rp;
-  const int npass = int((hi - lo + kPass - 1) / kPass);
-  const int slices = npass * kVecPerPass;
-  // per-(slice, warp) sums; slice-major, warp-minor is ascending vocabulary order
+  const int slices = int((hi - lo + kSlice - 1) / kSlice);
   for (int s = 0; s < slices; ++s) {
-    const int ps = s / kVecPerPass, q = s - ps * kVecPerPass;
-    const int64_t e = lo + int64_t(ps) * kPass + int64_t(q * kThreads + tid) * N;
+    const int64_t e = lo + int64_t(s) * kSlice + int64_t(tid) * N;
     float wv[N], pv[N];
     weights<E>(vec_at<E, kVec>(rp, e, hi), vec_at<E, kVec>(rq, e, pair ? hi : 0), pair, sq.k, pl.mkp, pl.invp, pl.mkq,
                pl.invq, wv, pv);
@@ -601,21 +562,14 @@ __device__ void select(const Args& a, const Geo& geo, const Work& w, const Seq<E
   }
   __syncthreads();
   if (warp == sm.warp_sel) {
-    const int s = sm.slice;
-    const int ps = s / kVecPerPass, q = s - ps * kVecPerPass;
-    const int64_t e = lo + int64_t(ps) * kPass + int64_t(q * kThreads + tid) * N;
+    const int64_t e = lo + int64_t(sm.slice) * kSlice + int64_t(tid) * N;
     float wv[N], pv[N];
     weights<E>(vec_at<E, kVec>(rp, e, hi), vec_at<E, kVec>(rq, e, pair ? hi : 0), pair, sq.k, pl.mkp, pl.invp, pl.mkq,
                pl.invq, wv, pv);
     float x = 0.f;
 #pragma unroll
     for (int j = 0; j < N; ++j) x = __fadd_rn(x, draw_p ? pv[j] : wv[j]);
-    float incl = x;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(kFull, incl, o);
-      if (lane >= o) incl = __fadd_rn(incl, y);
-    }
+    const float incl = warp_incl_scan(x);
     const float base = sm.run_sel;
     const unsigned hit = __ballot_sync(kFull, x > 0.f && __fadd_rn(base, incl) > tl);
     const unsigned pos = __ballot_sync(kFull, x > 0.f);
@@ -643,7 +597,7 @@ __device__ void select(const Args& a, const Geo& geo, const Work& w, const Seq<E
     else if (i == m) v = tok;
     a.out_tokens[int64_t(b) * (gmax + 1) + i] = v;
   }
-  for (int c = tid; c < CL; c += kThreads) w.state[int64_t(b) * CL + c] = kChunkFree;
+  for (int c = tid; c < DCL; c += kThreads) w.state[int64_t(b) * DCL + c] = kChunkFree;
   if (tid == 0) {
     if (a.diag) a.diag[int64_t(b) * (2 * gmax + 1) + 2 * gmax] = sm.mass_out;
     a.num_accepted[b] = m;
@@ -654,32 +608,31 @@ __device__ void select(const Args& a, const Geo& geo, const Work& w, const Seq<E
   __syncthreads();
 }
 
-// one draw chunk: its residual and p masses; the last chunk of b to finish selects
+// one draw chunk: its residual and p masses; the last draw chunk of b to finish selects
 template <class E, bool kVec, bool kMixed>
 __device__ void draw_chunk(const Args& a, const Geo& geo, const Work& w, const Seq<E, kMixed>& sq, const PlanRec pl,
-                           int c, Shared& sm) {
+                           int dc, Shared& sm) {
   using raw = typename E::raw;
   constexpr int N = E::kPerVec;
+  constexpr int kStep = kThreads * kDrawVec * N;
   const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
   const int b = sq.b;
   const bool pair = pl.pair != 0;
   const raw* rp = sq.P + int64_t(pl.m) * a.V;
   const raw* rq = pair ? sq.Q + int64_t(pl.m) * a.V : rp;
-  const int64_t lo = int64_t(c) * geo.chunk;
-  const int64_t hi = lo + geo.chunk < a.V ? lo + geo.chunk : a.V;
+  const int64_t lo = int64_t(dc) * geo.dchunk;
+  const int64_t hi = lo + geo.dchunk < a.V ? lo + geo.dchunk : a.V;
   float2 ws2 = make_float2(0.f, 0.f), ps2 = ws2;
-  // two vectors of each row in flight per thread: the rows are normally still in L2
-  constexpr int kDrawStep = kThreads * 2 * N;
-  for (int64_t e0 = lo; e0 < hi; e0 += kDrawStep) {
-    uint4 vp[2], vq[2];
+  for (int64_t e0 = lo; e0 < hi; e0 += kStep) {
+    uint4 vp[kDrawVec], vq[kDrawVec];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < kDrawVec; ++q) {
       const int64_t e = e0 + int64_t(q * kThreads + tid) * N;
       vp[q] = vec_at<E, kVec>(rp, e, hi);
       vq[q] = vec_at<E, kVec>(rq, e, pair ? hi : 0);
     }
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < kDrawVec; ++q) {
       float wv[N], pv[N];
       weights<E>(vp[q], vq[q], pair, sq.k, pl.mkp, pl.invp, pl.mkq, pl.invq, wv, pv);
 #pragma unroll
@@ -689,9 +642,8 @@ __device__ void draw_chunk(const Args& a, const Geo& geo, const Work& w, const S
       }
     }
   }
-  float ws = __fadd_rn(ws2.x, ws2.y), ps = __fadd_rn(ps2.x, ps2.y);
-  ws = warp_sum(ws);
-  ps = warp_sum(ps);
+  const float ws = warp_sum(__fadd_rn(ws2.x, ws2.y));
+  const float ps = warp_sum(__fadd_rn(ps2.x, ps2.y));
   if (lane == 0) sm.wp[warp] = make_float2(ws, ps);
   __syncthreads();
   if (tid == 0) {
@@ -701,8 +653,8 @@ __device__ void draw_chunk(const Args& a, const Geo& geo, const Work& w, const S
       acc.y = __fadd_rn(acc.y, sm.wp[wi].y);
     }
     if (!pair) acc.x = acc.y;
-    w.mass[int64_t(b) * geo.CL + c] = acc;
-    sm.last = atom_add_acq_rel(&w.bdone[b], 1) == geo.CL - 1;
+    w.mass[int64_t(b) * geo.DCL + dc] = acc;
+    sm.last = atom_add_acq_rel(&w.bdone[b], 1) == geo.DCL - 1;
   }
   __syncthreads();
   if (sm.last) select<E, kVec, kMixed>(a, geo, w, sq, pl, sm);
@@ -712,12 +664,24 @@ __device__ void draw_chunk(const Args& a, const Geo& geo, const Work& w, const S
 // decider: combine the partials of sequence b, decide, then greedy result or the plan
 // ------------------------------------------------------------------------------------------
 
+// Entered by every thread of the block whose A unit arrived last, after the arrival atomic
+// (acquire) and a block barrier: all partials and draft logits of b are visible.
 template <class E, bool kVec, bool kMixed>
 __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E, kMixed>& sq, Shared& sm) {
   const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
   const int b = sq.b, g = sq.g, gmax = a.gmax, CL = geo.CL;
   const float k = sq.k;
-  __threadfence();
+  // the per-draft inputs first: they do not depend on the combine below
+  int d = -1;
+  float u = 0.f, xp = 0.f, xq = 0.f;
+  if (warp == 0 && lane < g) {
+    d = __ldg(&a.draft_tokens[int64_t(b) * gmax + lane]);
+    if (sq.sampling) {
+      u = __ldg(&a.u_accept[int64_t(b) * gmax + lane]);
+      xp = __ldcg(&w.xd[int64_t(b) * geo.nslots + lane]);
+      xq = __ldcg(&w.xd[int64_t(b) * geo.nslots + gmax + 1 + lane]);
+    }
+  }
   // one warp per row: lanes take chunks c and c + 32 (at most 64 chunks)
   const float2* part = w.part + int64_t(b) * geo.nslots * CL;
   for (int slot = warp; slot < geo.nslots; slot += kWarps) {
@@ -746,20 +710,18 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
       if (lane == 0) sm.rowArg[slot] = bi;
     }
   }
+  if (tid < 2) sm.taken[tid] = 0u;
   __syncthreads();
   if (warp == 0) {
-    bool acc = false, valid = false;
+    bool acc = false;
+    const bool valid = lane < g && d >= 0 && int64_t(d) < a.V;
     if (lane < g) {
-      const int d = a.draft_tokens[int64_t(b) * gmax + lane];
-      valid = d >= 0 && int64_t(d) < a.V;
       if (sq.sampling) {
         float p = NAN, q = NAN;
         if (valid) {
-          const float* xd = w.xd + int64_t(b) * geo.nslots;
           const int qs = gmax + 1 + lane;
-          p = prob(__ldcg(&xd[lane]), k, __fmul_rn(sm.rowM[lane], k), sm.rowInvS[lane]);
-          q = prob(__ldcg(&xd[qs]), k, __fmul_rn(sm.rowM[qs], k), sm.rowInvS[qs]);
-          const float u = a.u_accept[int64_t(b) * gmax + lane];
+          p = prob(xp, k, __fmul_rn(sm.rowM[lane], k), sm.rowInvS[lane]);
+          q = prob(xq, k, __fmul_rn(sm.rowM[qs], k), sm.rowInvS[qs]);
           // u < min(1, p/q): r = 0 when p = 0, r = +inf when q = 0 < p
           acc = (p == 0.f) ? (u < 0.f) : (p >= q ? (u < 1.f) : (__fmul_rn(u, q) < p));
         }
@@ -820,23 +782,24 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
     w.plan[b] = pr;
     sm.plan = pr;
     w.cnt[b] = 0;
-    __threadfence();
+    __threadfence();                 // the plan before the flag
     atomicExch(&w.ready[b], 1);
-    __threadfence();
+    __threadfence();                 // the flag before the chunk states read below
   }
   __syncthreads();
   const PlanRec pl = sm.plan;
-  // the chunks whose B units gave up before the plan was out are the decider's
-  if (tid < 2) sm.taken[tid] = 0u;
-  __syncthreads();
-  if (tid < CL) {
-    int* st = &w.state[int64_t(b) * CL + tid];
+  // the draw chunks whose B units gave up before the plan was out are the decider's: with a
+  // fence between the flag and these reads here, and between the give-up and the flag read in
+  // the B unit, one of the two sides always sees the other
+  if (tid < geo.DCL) {
+    int* st = &w.state[int64_t(b) * geo.DCL + tid];
+    __threadfence();
     if (ld_acquire(st) == kChunkGivenUp && atom_cas(st, kChunkGivenUp, kChunkDecider) == kChunkGivenUp)
       atomicOr(&sm.taken[tid >> 5], 1u << (tid & 31));
   }
   __syncthreads();
   const unsigned taken0 = sm.taken[0], taken1 = sm.taken[1];
-  for (int c = 0; c < CL; ++c)
+  for (int c = 0; c < geo.DCL; ++c)
     if ((c < 32 ? taken0 >> c : taken1 >> (c - 32)) & 1u) draw_chunk<E, kVec, kMixed>(a, geo, w, sq, pl, c, sm);
 }
 
@@ -851,49 +814,37 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
   constexpr int kPass = kThreads * kVecPerPass * N;
   __shared__ Shared sm;
   const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
-  // blockIdx = (chunk c, row slot or nslots for the draw, group); blocks are dispatched in
-  // x-fastest order, so a group's A units come first and its B units last
-  const int c = int(blockIdx.x), slot = int(blockIdx.y), grp = geo.b0 + int(blockIdx.z);
+  // blockIdx = (x, y, group).  y < nslots: the A unit of row slot y, row chunk x.  y >= nslots:
+  // the B unit of draw chunk (y - nslots)*CL + x.  Blocks are dispatched in x-fastest order,
+  // so a group's A units come first and its B units last.
+  const int x = int(blockIdx.x), y = int(blockIdx.y), grp = geo.b0 + int(blockIdx.z);
 
-  if (slot < geo.nslots) {
-    // ---------------- A unit: chunk c of one row -------------------------------------------
-    const int b = grp;
+  if (y < geo.nslots) {
+    // ---------------- A unit: row chunk x of row slot y -------------------------------------
+    const int b = grp, slot = y, c = x;
     if (b >= geo.b1) return;
     const Seq<E, kMixed> sq(a, b);
     if (!sq.slot_valid(slot, a.gmax)) return;
     const raw* row = sq.row(slot, a.gmax, a.V);
     const int64_t lo = int64_t(c) * geo.chunk;
     const int64_t hi = lo + geo.chunk < a.V ? lo + geo.chunk : a.V;
+    // the logit at this row's draft id, if it lies in this chunk: fetched once, up front
     const int i = slot <= a.gmax ? slot : slot - a.gmax - 1;
-    const int d = (sq.sampling && i < sq.g) ? __ldg(&a.draft_tokens[int64_t(b) * a.gmax + i]) : -1;
-    // where this row's draft id sits: pass dp, vector dq of thread dt, element dj
-    int dp = -1, dq = 0, dt = -1, dj = 0;
-    if (int64_t(d) >= lo && int64_t(d) < hi) {
-      int off = int(int64_t(d) - lo);
-      dp = off / kPass;
-      off -= dp * kPass;
-      dq = off / (kThreads * N);
-      off -= dq * kThreads * N;
-      dt = off / N;
-      dj = off - dt * N;
+    bool has_d = false;
+    float xv = 0.f;
+    if (tid == 0 && sq.sampling && i < sq.g) {
+      const int d = __ldg(&a.draft_tokens[int64_t(b) * a.gmax + i]);
+      has_d = int64_t(d) >= lo && int64_t(d) < hi;
+      if (has_d) xv = E::at(row, d);
     }
     float rm = -INFINITY, rs = 0.f;
     int ri = INT_MAX;
-    int pass = 0;
-    for (int64_t e0 = lo; e0 < hi; e0 += kPass, ++pass) {
+    for (int64_t e0 = lo; e0 < hi; e0 += kPass) {
       Tile<E, kVec> t;
       if (e0 + kPass <= hi) t.load_full(row, e0, tid);
       else t.load(row, e0, hi, tid);
-      if (sq.sampling) {
-        if (pass == dp && tid == dt) {
-          // the logit at this row's draft id, from the registers that hold it
-          w.xd[int64_t(b) * geo.nslots + slot] = t.pick(dq, dj);
-          __threadfence();
-        }
-        thread_stats(t, sq.k, rm, rs);
-      } else {
-        tile_argmax(t, e0, tid, rm, ri);
-      }
+      if (sq.sampling) thread_stats(t, sq.k, rm, rs);
+      else tile_argmax(t, e0, tid, rm, ri);
     }
     if (sq.sampling) warp_stats(rm, rs, sq.k);
     else warp_argmax(rm, ri);
@@ -903,17 +854,16 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
       // the block's partial from the warps' partials, lanes in parallel
       float2 p = lane < kWarps ? sm.wp[lane] : make_float2(-INFINITY, sq.sampling ? 0.f : __int_as_float(INT_MAX));
       if (sq.sampling) {
-        const float M = warp_max(p.x);
-        float S = 0.f;
-        if (M != -INFINITY) S = warp_sum(p.x == -INFINITY ? 0.f : __fmul_rn(p.y, ex2(__fmul_rn(p.x - M, sq.k))));
-        p = make_float2(M, S);
+        warp_stats(p.x, p.y, sq.k);
       } else {
         int pi = __float_as_int(p.y);
         warp_argmax(p.x, pi);
         p.y = __int_as_float(pi);
       }
       if (lane == 0) {
+        if (has_d) w.xd[int64_t(b) * geo.nslots + slot] = xv;
         w.part[(int64_t(b) * geo.nslots + slot) * geo.CL + c] = p;
+        // release: this thread's partial and draft logit before the count
         sm.last = atom_add_acq_rel(&w.cnt[b], 1) == geo.CL * sq.nrows() - 1;
       }
     }
@@ -923,13 +873,14 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
   }
 
   if constexpr (kMixed) {
-    // ---------------- B unit: draw chunk c of sequence grp - delta ------------------------
+    // ---------------- B unit: draw chunk dc of sequence grp - delta -------------------------
+    const int dc = (y - geo.nslots) * geo.CL + x;
     const int b = grp - geo.delta;
-    if (b < geo.b0 || b >= geo.b1) return;
+    if (dc >= geo.DCL || b < geo.b0 || b >= geo.b1) return;
     const Seq<E, kMixed> sq(a, b);
     if (!sq.sampling) return;
     if (tid == 0) {
-      int* st = &w.state[int64_t(b) * geo.CL + c];
+      int* st = &w.state[int64_t(b) * geo.DCL + dc];
       // optional, bounded wait for the plan; correctness does not depend on it
       int it = 0, ns = 64;
       while (ld_acquire(&w.ready[b]) == 0 && it < kPlanWaitIters) {
@@ -969,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
     }
     __syncthreads();
     if (!sm.go) return;
-    draw_chunk<E, kVec, kMixed>(a, geo, w, sq, sm.plan, c, sm);
+    draw_chunk<E, kVec, kMixed>(a, geo, w, sq, sm.plan, dc, sm);
   }
 }
 
@@ -978,17 +929,25 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
 // ------------------------------------------------------------------------------------------
 
 struct Split {
-  int cl;
-  int chunk;
+  int cl, chunk;     // row chunks
+  int dcl, dchunk;   // draw chunks
 };
 
+void cut(int64_t V, int target, int& n, int& len) {
+  int64_t c = (V + target - 1) / target;
+  if (c < 1) c = 1;
+  if (c > kMaxChunks) c = kMaxChunks;
+  int64_t l = (V + c - 1) / c;
+  l = (l + 7) / 8 * 8;
+  n = int(c);
+  len = int(l);
+}
+
 Split make_split(int64_t V) {
-  int cl = int((V + kChunkTarget - 1) / kChunkTarget);
-  if (cl < 1) cl = 1;
-  if (cl > kMaxChunks) cl = kMaxChunks;
-  int64_t c = (V + cl - 1) / cl;
-  c = (c + 7) / 8 * 8;
-  return Split{cl, int(c)};
+  Split s;
+  cut(V, kChunkTarget, s.cl, s.chunk);
+  cut(V, kDrawChunkTarget, s.dcl, s.dchunk);
+  return s;
 }
 
 size_t align64(size_t x) { return (x + 63) & ~size_t(63); }
@@ -1003,14 +962,14 @@ struct WsLayout {
 
 size_t counter_bytes(int B, int64_t V) {
   const Split s = make_split(V);
-  return 3 * align64(size_t(B) * 4) + align64(size_t(B) * s.cl * 4);
+  return 3 * align64(size_t(B) * 4) + align64(size_t(B) * s.dcl * 4);
 }
 
 size_t scratch_bytes(int B, int gmax, int64_t V) {
   const Split s = make_split(V);
   const size_t nslots = size_t(2 * gmax + 1);
   return align64(size_t(B) * sizeof(PlanRec)) + align64(size_t(B) * nslots * s.cl * 8) +
-         align64(size_t(B) * nslots * 4) + align64(size_t(B) * s.cl * 8);
+         align64(size_t(B) * nslots * 4) + align64(size_t(B) * s.dcl * 8);
 }
 
 size_t header_for(size_t ws_bytes) { return (ws_bytes / 8) & ~size_t(63); }
@@ -1032,7 +991,7 @@ WsLayout ws_layout(int B, int gmax, int64_t V, size_t ws_bytes) {
   L.xd = off;
   off += align64(size_t(B) * nslots * 4);
   L.mass = off;
-  off += align64(size_t(B) * s.cl * 8);
+  off += align64(size_t(B) * s.dcl * 8);
   L.scratch_end = off;
   return L;
 }
@@ -1072,10 +1031,11 @@ template <class E, bool kVec, bool kMixed>
 int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream) {
   auto fn = verify_kernel<E, kVec, kMixed>;
   const Split sp = make_split(args.V);
-  const int64_t per_pass = int64_t(kThreads) * kVecPerPass * (dtype == SPEC_BF16 ? 8 : 4);
-  const int npass = int((sp.chunk + per_pass - 1) / per_pass);
-  if (npass > kMaxPasses) {
-    set_error("V=%lld too large: %d passes per chunk (max %d)", (long long)args.V, npass, kMaxPasses);
+  const int64_t slice = int64_t(kThreads) * (dtype == SPEC_BF16 ? 8 : 4);
+  const int64_t slices = (sp.dchunk + slice - 1) / slice;
+  if (slices > kMaxSlices) {
+    set_error("V=%lld too large: %lld slices per draw chunk (max %d)", (long long)args.V, (long long)slices,
+              kMaxSlices);
     return SPEC_ENOSPACE;
   }
   // host-only checks first: nothing is enqueued when they fail
@@ -1092,8 +1052,11 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
   Geo geo;
   geo.CL = sp.cl;
   geo.chunk = sp.chunk;
+  geo.DCL = sp.dcl;
+  geo.dchunk = sp.dchunk;
   geo.nslots = kMixed ? 2 * args.gmax + 1 : args.gmax + 1;   // greedy-only reads no draft rows
-  const int G = geo.nslots * geo.CL + (kMixed ? geo.CL : 0);   // units per group
+  const int brows = kMixed ? (geo.DCL + geo.CL - 1) / geo.CL : 0;   // grid rows of B units
+  const int G = geo.CL * (geo.nslots + brows);                       // units per group
   // B units of a sequence come about kDrawWaves waves of resident blocks after its A units
   int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1122,7 +1085,7 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
   for (int b0 = 0; b0 < args.B; b0 += per_launch) {
     geo.b0 = b0;
     geo.b1 = b0 + per_launch < args.B ? b0 + per_launch : args.B;
-    const dim3 grid(unsigned(geo.CL), unsigned(geo.nslots + (kMixed ? 1 : 0)), unsigned(geo.b1 - b0 + geo.delta));
+    const dim3 grid(unsigned(geo.CL), unsigned(geo.nslots + brows), unsigned(geo.b1 - b0 + geo.delta));
     fn<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(args, geo, w);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "verify kernel launch");

@@ -83,14 +83,15 @@ def test_plan_splits_vocabulary(lib):
         cl, chunk = sv.spec_verify_plan(V)
         assert 1 <= cl <= 64 and chunk % 8 == 0
         assert cl * chunk >= V and (cl - 1) * chunk < V, (V, cl, chunk)
-    assert sv.spec_verify_plan(128256) == (16, 8016)
-    assert sv.spec_verify_plan(151936) == (19, 8000)
+    assert sv.spec_verify_plan(128256) == (8, 16032)
+    assert sv.spec_verify_plan(151936) == (10, 15200)
 
 
 def test_workspace_size(lib):
     n = sv.spec_verify_workspace_bytes(128, 4, 128256)
+    cl, _ = sv.spec_verify_plan(128256)
     # per-(row, chunk) partials and draft logits, after a counter header (one eighth)
-    assert n >= 128 * (9 * 16 * 8 + 9 * 4) * 8 // 7
+    assert n >= 128 * (9 * cl * 8 + 9 * 4) * 8 // 7
     assert n < 1 << 20
     assert sv.spec_verify_workspace_bytes(128, 4, 128256) == sv.spec_verify_workspace_bytes(128, 4, 128256, 1)
     assert sv.spec_verify_workspace_bytes(-1, 4, 100) == 0
