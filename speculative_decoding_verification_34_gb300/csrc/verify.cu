@@ -43,7 +43,14 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kVecPerPass = 4;                         // 16-byte vectors per thread per row pass
-constexpr int kDrawVec = 2;                            // vectors of each row per thread per draw step
+#ifndef SPEC_DRAW_VEC
+#define SPEC_DRAW_VEC 2
+#endif
+#ifndef SPEC_PREFETCH
+#define SPEC_PREFETCH 0
+#endif
+constexpr int kDrawVec = SPEC_DRAW_VEC;                // vectors of each row per thread per draw step
+constexpr bool kPrefetch = SPEC_PREFETCH != 0;         // row passes double-buffered in registers
 constexpr int kMaxChunks = 64;                         // row chunks, and draw chunks, per row
 constexpr int kMaxSlices = 16;                         // kThreads-vector slices per draw chunk
 #ifndef SPEC_CHUNK_TARGET
@@ -67,7 +74,7 @@ constexpr int kPlanWaitIters = 32;                     // optional bounded wait 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kInternalDrawP = 0x100;
-// draw-chunk states
+// draw-chunk states (a chunk whose B unit saw the plan at once stays Free)
 constexpr int kChunkFree = 0, kChunkMine = 1, kChunkGivenUp = 2, kChunkDecider = 3;
 
 struct Args {
@@ -839,12 +846,31 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
     }
     float rm = -INFINITY, rs = 0.f;
     int ri = INT_MAX;
-    for (int64_t e0 = lo; e0 < hi; e0 += kPass) {
-      Tile<E, kVec> t;
+    auto fetch = [&](Tile<E, kVec>& t, int64_t e0) {
       if (e0 + kPass <= hi) t.load_full(row, e0, tid);
       else t.load(row, e0, hi, tid);
+    };
+    auto consume = [&](const Tile<E, kVec>& t, int64_t e0) {
       if (sq.sampling) thread_stats(t, sq.k, rm, rs);
       else tile_argmax(t, e0, tid, rm, ri);
+    };
+    if constexpr (kPrefetch) {
+      // two tiles in registers: the next pass is in flight while this one is reduced
+      Tile<E, kVec> t0, t1;
+      if (lo < hi) fetch(t0, lo);
+      for (int64_t e0 = lo; e0 < hi; e0 += 2 * kPass) {
+        if (e0 + kPass < hi) fetch(t1, e0 + kPass);
+        consume(t0, e0);
+        if (e0 + kPass >= hi) break;
+        if (e0 + 2 * kPass < hi) fetch(t0, e0 + 2 * kPass);
+        consume(t1, e0 + kPass);
+      }
+    } else {
+      for (int64_t e0 = lo; e0 < hi; e0 += kPass) {
+        Tile<E, kVec> t;
+        fetch(t, e0);
+        consume(t, e0);
+      }
     }
     if (sq.sampling) warp_stats(rm, rs, sq.k);
     else warp_argmax(rm, ri);
@@ -890,15 +916,17 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
       }
       bool mine = false;
       if (ld_acquire(&w.ready[b]) != 0) {
-        mine = atom_cas(st, kChunkFree, kChunkMine) == kChunkFree;
+        // the plan is out: the decider takes only given-up chunks, so this one stays ours
+        // without a claim
+        mine = true;
       } else if (atom_cas(st, kChunkFree, kChunkGivenUp) == kChunkFree) {
         // given up; if the plan appeared meanwhile, take the chunk back unless the decider has
         __threadfence();
         if (ld_acquire(&w.ready[b]) != 0) mine = atom_cas(st, kChunkGivenUp, kChunkMine) == kChunkGivenUp;
       }
       if (mine) {
-        __threadfence();
-        // through L2: an earlier read of this line by the same SM may sit stale in L1
+        // ordered after the acquire above; through L2: an earlier read of this line by the
+        // same SM may sit stale in L1
         const int4* src = reinterpret_cast<const int4*>(&w.plan[b]);
         const int4 h0 = __ldcg(src), h1 = __ldcg(src + 1);
         sm.plan.m = h0.x;
