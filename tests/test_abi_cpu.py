@@ -83,8 +83,8 @@ def test_plan_splits_vocabulary(lib):
         cl, chunk = sv.spec_verify_plan(V)
         assert 1 <= cl <= 64 and chunk % 8 == 0
         assert cl * chunk >= V and (cl - 1) * chunk < V, (V, cl, chunk)
-    assert sv.spec_verify_plan(128256) == (8, 16032)
-    assert sv.spec_verify_plan(151936) == (10, 15200)
+    assert sv.spec_verify_plan(128256) == (2, 64128)
+    assert sv.spec_verify_plan(151936) == (3, 50648)
 
 
 def test_workspace_size(lib):

@@ -132,7 +132,7 @@ def test_invalid_inputs_set_status():
 
 
 def test_greedy_ties_resolve_to_lowest_id():
-    V = 70000
+    V = 270000
     cl, chunk = sv.spec_verify_plan(V)
     assert cl > 3
     rng = np.random.default_rng(9)
