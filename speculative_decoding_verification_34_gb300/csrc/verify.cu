@@ -814,54 +814,6 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
 // the kernel
 // ------------------------------------------------------------------------------------------
 
-// Takes draw chunk dc of sequence b for this block, following the plan protocol: a chunk whose
-// plan was seen (ready != 0) is this block's; otherwise the chunk is given up to the decider,
-// unless the plan appears before the decider takes it.  Thread 0 only; returns whether the
-// chunk is this block's, with its plan in pl.
-template <class E, bool kMixed>
-__device__ bool claim_draw(const Args& a, const Geo& geo, const Work& w, int b, int g, int dc, bool seen,
-                           bool loaded, int4 h0, int4 h1, PlanRec& pl) {
-  int* st = &w.state[int64_t(b) * geo.DCL + dc];
-  bool mine = seen;
-  if (!mine) {
-    if (ld_acquire(&w.ready[b]) != 0) {
-      mine = true;
-    } else if (atom_cas(st, kChunkFree, kChunkGivenUp) == kChunkFree) {
-      // given up; if the plan appeared meanwhile, take the chunk back unless the decider has
-      __threadfence();
-      if (ld_acquire(&w.ready[b]) != 0) mine = atom_cas(st, kChunkGivenUp, kChunkMine) == kChunkGivenUp;
-    }
-  }
-  if (!mine) return false;
-  if (!loaded) {
-    // ordered after the acquire above; through L2: an earlier read of this line by the same
-    // SM may sit stale in L1
-    const int4* src = reinterpret_cast<const int4*>(&w.plan[b]);
-    h0 = __ldcg(src);
-    h1 = __ldcg(src + 1);
-  }
-  pl.m = h0.x;
-  pl.g = h0.y;
-  pl.flags = h0.z;
-  pl.pair = h0.w;
-  pl.mkp = __int_as_float(h1.x);
-  pl.invp = __int_as_float(h1.y);
-  pl.mkq = __int_as_float(h1.z);
-  pl.invq = __int_as_float(h1.w);
-  // never fails for a well-formed workspace; keeps every read in bounds
-  if (pl.m < 0 || pl.m > g || (pl.pair && pl.m >= g)) {
-    if (a.status) atomicOr(&a.status[b], SPEC_ST_TIMEOUT);
-    return false;
-  }
-  return true;
-}
-
-// blockIdx = (x, y, group z); unit u = y*CL + x of group grp = b0 + z.
-//   rows work:  for y < nslots, row chunk x of row slot y of sequence grp (if grp < b1);
-//   draw work:  for u < DCL, draw chunk u of sequence grp - delta (if that sequence is in
-//               [b0, b1) and sampled), done after the row work.
-// Blocks are dispatched in x-fastest order, so a sequence's draw chunks come about
-// kDrawWaves waves of resident blocks after its rows.
 template <class E, bool kVec, bool kMixed>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args a, const Geo geo, const Work w) {
   using raw = typename E::raw;
@@ -869,28 +821,17 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
   constexpr int kPass = kThreads * kVecPerPass * N;
   __shared__ Shared sm;
   const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
+  // blockIdx = (x, y, group).  y < nslots: the A unit of row slot y, row chunk x.  y >= nslots:
+  // the B unit of draw chunk (y - nslots)*CL + x.  Blocks are dispatched in x-fastest order,
+  // so a group's A units come first and its B units last.
   const int x = int(blockIdx.x), y = int(blockIdx.y), grp = geo.b0 + int(blockIdx.z);
-  const int u = y * geo.CL + x;
-  const int bA = grp, bD = grp - geo.delta;
-  bool rows = y < geo.nslots && bA < geo.b1;
-  bool draw = false;
-  if constexpr (kMixed) draw = u < geo.DCL && bD >= geo.b0 && bD < geo.b1 && __ldg(&a.temperature[bD]) > 0.f;
-  if (rows) {
-    const Seq<E, kMixed> sq(a, bA);
-    rows = sq.slot_valid(y, a.gmax);
-  }
-  if (!rows && !draw) return;
 
-  // is the draw's plan already out?  Read now; the plan itself is read near the end of the
-  // rows, so that its latency hides behind the block's reductions
-  const bool seen = draw && tid == 0 && ld_acquire(&w.ready[bD]) != 0;
-  bool loaded = false;
-  int4 h0 = make_int4(0, 0, 0, 0), h1 = h0;
-
-  if (rows) {
-    // ---------------- rows: row chunk x of row slot y of sequence bA ------------------------
-    const int b = bA, slot = y, c = x;
+  if (y < geo.nslots) {
+    // ---------------- A unit: row chunk x of row slot y -------------------------------------
+    const int b = grp, slot = y, c = x;
+    if (b >= geo.b1) return;
     const Seq<E, kMixed> sq(a, b);
+    if (!sq.slot_valid(slot, a.gmax)) return;
     const raw* row = sq.row(slot, a.gmax, a.V);
     const int64_t lo = int64_t(c) * geo.chunk;
     const int64_t hi = lo + geo.chunk < a.V ? lo + geo.chunk : a.V;
@@ -931,12 +872,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
         consume(t, e0);
       }
     }
-    if (seen) {
-      const int4* src = reinterpret_cast<const int4*>(&w.plan[bD]);
-      h0 = __ldcg(src);
-      h1 = __ldcg(src + 1);
-      loaded = true;
-    }
     if (sq.sampling) warp_stats(rm, rs, sq.k);
     else warp_argmax(rm, ri);
     if (lane == 0) sm.wp[warp] = make_float2(rm, sq.sampling ? rs : __int_as_float(ri));
@@ -960,16 +895,60 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
     }
     __syncthreads();
     if (sm.last) decide<E, kVec, kMixed>(a, geo, w, sq, sm);
+    return;
   }
 
   if constexpr (kMixed) {
-    if (!draw) return;
-    // ---------------- draw: draw chunk u of sequence bD -----------------------------------
-    const Seq<E, kMixed> sq(a, bD);
-    if (tid == 0) sm.go = claim_draw<E, kMixed>(a, geo, w, bD, sq.g, u, seen, loaded, h0, h1, sm.plan);
+    // ---------------- B unit: draw chunk dc of sequence grp - delta -------------------------
+    const int dc = (y - geo.nslots) * geo.CL + x;
+    const int b = grp - geo.delta;
+    if (dc >= geo.DCL || b < geo.b0 || b >= geo.b1) return;
+    const Seq<E, kMixed> sq(a, b);
+    if (!sq.sampling) return;
+    if (tid == 0) {
+      int* st = &w.state[int64_t(b) * geo.DCL + dc];
+      // optional, bounded wait for the plan; correctness does not depend on it
+      int it = 0, ns = 64;
+      while (ld_acquire(&w.ready[b]) == 0 && it < kPlanWaitIters) {
+        __nanosleep(ns);
+        if (ns < 512) ns <<= 1;
+        ++it;
+      }
+      bool mine = false;
+      if (ld_acquire(&w.ready[b]) != 0) {
+        // the plan is out: the decider takes only given-up chunks, so this one stays ours
+        // without a claim
+        mine = true;
+      } else if (atom_cas(st, kChunkFree, kChunkGivenUp) == kChunkFree) {
+        // given up; if the plan appeared meanwhile, take the chunk back unless the decider has
+        __threadfence();
+        if (ld_acquire(&w.ready[b]) != 0) mine = atom_cas(st, kChunkGivenUp, kChunkMine) == kChunkGivenUp;
+      }
+      if (mine) {
+        // ordered after the acquire above; through L2: an earlier read of this line by the
+        // same SM may sit stale in L1
+        const int4* src = reinterpret_cast<const int4*>(&w.plan[b]);
+        const int4 h0 = __ldcg(src), h1 = __ldcg(src + 1);
+        sm.plan.m = h0.x;
+        sm.plan.g = h0.y;
+        sm.plan.flags = h0.z;
+        sm.plan.pair = h0.w;
+        sm.plan.mkp = __int_as_float(h1.x);
+        sm.plan.invp = __int_as_float(h1.y);
+        sm.plan.mkq = __int_as_float(h1.z);
+        sm.plan.invq = __int_as_float(h1.w);
+        const PlanRec& pl = sm.plan;
+        // never fails for a well-formed workspace; keeps every read in bounds
+        if (pl.m < 0 || pl.m > sq.g || (pl.pair && pl.m >= sq.g)) {
+          mine = false;
+          if (a.status) atomicOr(&a.status[b], SPEC_ST_TIMEOUT);
+        }
+      }
+      sm.go = mine;
+    }
     __syncthreads();
     if (!sm.go) return;
-    draw_chunk<E, kVec, kMixed>(a, geo, w, sq, sm.plan, u, sm);
+    draw_chunk<E, kVec, kMixed>(a, geo, w, sq, sm.plan, dc, sm);
   }
 }
 
@@ -1104,11 +1083,9 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
   geo.DCL = sp.dcl;
   geo.dchunk = sp.dchunk;
   geo.nslots = kMixed ? 2 * args.gmax + 1 : args.gmax + 1;   // greedy-only reads no draft rows
-  // extra grid rows when a group has fewer row units than draw chunks
-  const int NA = geo.nslots * geo.CL;
-  const int brows = kMixed && geo.DCL > NA ? (geo.DCL - NA + geo.CL - 1) / geo.CL : 0;
+  const int brows = kMixed ? (geo.DCL + geo.CL - 1) / geo.CL : 0;   // grid rows of B units
   const int G = geo.CL * (geo.nslots + brows);                       // units per group
-  // a sequence's draw chunks come about kDrawWaves waves of resident blocks after its rows
+  // B units of a sequence come about kDrawWaves waves of resident blocks after its A units
   int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -1133,13 +1110,9 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
   // one launch covers at most kMaxGroups groups (the grid's z limit); larger batches take
   // several launches over consecutive sequence ranges, each complete on its own
   const int per_launch = kMaxGroups - geo.delta;
-  const int delta = geo.delta;
   for (int b0 = 0; b0 < args.B; b0 += per_launch) {
     geo.b0 = b0;
     geo.b1 = b0 + per_launch < args.B ? b0 + per_launch : args.B;
-    // small batches: the draw follows right after the last rows
-    geo.delta = delta < geo.b1 - b0 ? delta : geo.b1 - b0;
-    if (!kMixed) geo.delta = 0;
     const dim3 grid(unsigned(geo.CL), unsigned(geo.nslots + brows), unsigned(geo.b1 - b0 + geo.delta));
     fn<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(args, geo, w);
     e = cudaGetLastError();
