@@ -122,6 +122,34 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits, int 
                        void* stream);
 
 /*
+ * spec_verify_sample without a caller-owned workspace.  The pages have no counterpart: this
+ * is a convenience of this library for callers that cannot allocate device memory where they
+ * verify (a serving loop whose memory is fixed after start-up, or a step between a
+ * framework's allocations that must not add one).  It computes exactly what
+ * spec_verify_sample computes, with the same arguments minus the workspace.
+ *
+ * The workspace is an array of SPEC_STATIC_WORKSPACE_BYTES bytes compiled into the library,
+ * one per device, shared by every call of this function on that device:
+ *   - Calls whose sizes need more (about spec_verify_workspace_bytes(B, gmax, V, dtype)
+ *     above SPEC_STATIC_WORKSPACE_BYTES, which rounds up: the exact limits are B = 1724 at
+ *     gmax = 4, V = 128256 and B = 1488 at gmax = 4, V = 151936) return SPEC_ENOSPACE
+ *     before touching the device.
+ *   - The first call on a device looks the array up (cudaGetSymbolAddress), clears it and
+ *     waits for the clear, so its counters start at zero; make that call outside any stream
+ *     capture.  Later calls only launch the kernel.
+ *   - The array keeps the last call's scratch values; its counters are zero between calls.
+ *   - Calls that may overlap (different streams, or threads without ordering) race on the one
+ *     array: serialise them, e.g. on one stream.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define SPEC_STATIC_WORKSPACE_BYTES ((size_t)1 << 20)
+int spec_verify_sample_static(const void* target_logits, const void* draft_logits, int dtype,
+                              const int32_t* draft_tokens, const int32_t* num_draft,
+                              const float* temperature, const float* u_accept,
+                              const float* u_sample, int B, int gmax, int V, int32_t* out_tokens,
+                              int32_t* num_accepted, float* diag, int32_t* status, void* stream);
+
+/*
  * Bytes of workspace a verify call with these sizes needs (either entry point); 0 for
  * invalid sizes.  Host-only.
  */

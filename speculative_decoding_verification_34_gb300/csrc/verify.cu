@@ -1222,6 +1222,100 @@ extern "C" int spec_verify_sample(const void* target_logits, const void* draft_l
   return dispatch_on<true>(a, dtype, workspace, workspace_bytes, stream);
 }
 
+// ------------------------------------------------------------------------------------------
+// spec_verify_sample_static: the same verification with a workspace compiled into the library
+// ------------------------------------------------------------------------------------------
+//
+// For callers that cannot allocate device memory at the point of the call: a serving loop
+// whose memory is fixed after start-up, or code between a framework's allocations that must
+// not add one.  The workspace is one file-scope device array per device (every call of this
+// entry point on that device shares it); its address is looked up once per device with
+// cudaGetSymbolAddress.  Nothing is allocated, by this call or by any routine it calls.
+
+namespace specverify {
+namespace {
+
+constexpr size_t kStaticWsBytes = SPEC_STATIC_WORKSPACE_BYTES;
+static_assert(kStaticWsBytes % 64 == 0, "static workspace size");
+
+// The shared workspace: its first eighth holds the counters, which must be zero before the
+// first call and which every completed call leaves at zero; the scratch after it keeps the
+// last call's values.
+static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
+
+std::mutex g_static_mu;
+void* g_static_ptr[64] = {};
+
+// The device address of this device's array.  The first call on a device also clears the
+// whole array and waits for that to finish.
+int static_workspace(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) {
+    set_error("device %d: the static workspace serves devices 0..63", dev);
+    return SPEC_EINVAL;
+  }
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_ws);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the static workspace");
+    e = cudaMemset(p, 0, kStaticWsBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the static workspace");
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the static workspace");
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return SPEC_OK;
+}
+
+}  // namespace
+}  // namespace specverify
+
+extern "C" int spec_verify_sample_static(const void* target_logits, const void* draft_logits, int dtype,
+                                         const int32_t* draft_tokens, const int32_t* num_draft,
+                                         const float* temperature, const float* u_accept,
+                                         const float* u_sample, int B, int gmax, int V,
+                                         int32_t* out_tokens, int32_t* num_accepted, float* diag,
+                                         int32_t* status, void* stream) {
+  clear_error();
+  int rc = check_common(target_logits, dtype, draft_tokens, B, gmax, V, out_tokens, num_accepted);
+  if (rc != SPEC_OK) return rc;
+  if (B > 0 && (!temperature || !u_sample || (gmax > 0 && (!draft_logits || !u_accept)))) {
+    set_error("null required pointer (draft_logits, temperature, u_accept or u_sample)");
+    return SPEC_EINVAL;
+  }
+  if (B == 0) return SPEC_OK;
+  // sizes first, on the host: a call the array cannot hold touches nothing
+  if (!ws_fits(B, gmax, V, kStaticWsBytes)) {
+    set_error("B=%d gmax=%d V=%d needs a %zu-byte workspace; the static workspace holds %zu bytes "
+              "(use spec_verify_sample with a caller-owned workspace)",
+              B, gmax, V, ws_required(B, gmax, V), kStaticWsBytes);
+    return SPEC_ENOSPACE;
+  }
+  void* ws = nullptr;
+  rc = static_workspace(&ws);
+  if (rc != SPEC_OK) return rc;
+  Args a = {};
+  a.target = target_logits;
+  a.draft = draft_logits;
+  a.draft_tokens = draft_tokens;
+  a.num_draft = num_draft;
+  a.temperature = temperature;
+  a.u_accept = u_accept;
+  a.u_sample = u_sample;
+  a.V = V;
+  a.B = B;
+  a.gmax = gmax;
+  a.out_tokens = out_tokens;
+  a.num_accepted = num_accepted;
+  a.diag = diag;
+  a.status = status;
+  return dispatch_on<true>(a, dtype, ws, kStaticWsBytes, stream);
+}
+
 extern "C" int spec_verify_plan(int V, int dtype, int* ctas_per_seq, int* chunk) {
   clear_error();
   if (V < 1 || (dtype != SPEC_BF16 && dtype != SPEC_F32) || !ctas_per_seq || !chunk) {

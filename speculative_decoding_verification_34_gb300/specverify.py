@@ -47,6 +47,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.spec_verify_greedy.restype = i32
     lib.spec_verify_sample.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, sz, sz, sz, vp, vp, vp, vp, vp, size_t, vp]
     lib.spec_verify_sample.restype = i32
+    lib.spec_verify_sample_static.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, sz, sz, sz, vp, vp, vp, vp, vp]
+    lib.spec_verify_sample_static.restype = i32
     lib.spec_verify_workspace_bytes.argtypes = [sz, sz, sz, i32]
     lib.spec_verify_workspace_bytes.restype = size_t
     lib.spec_commit_kv_lengths.argtypes = [vp, sz, vp, vp, i32, vp, sz, vp, vp, sz, vp, vp]
@@ -160,6 +162,35 @@ def spec_verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor,
         _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
         _ptr(diag, "diag", torch.float32, (B, 2 * gmax + 1)),
         _ptr(status, "status", torch.int32, (B,)), wsp, wsn, _stream(stream)))
+
+
+def spec_verify_sample_static(target_logits: torch.Tensor, draft_logits: torch.Tensor,
+                              draft_tokens: torch.Tensor, num_draft: Optional[torch.Tensor],
+                              temperature: torch.Tensor, u_accept: torch.Tensor,
+                              u_sample: torch.Tensor, out_tokens: torch.Tensor,
+                              num_accepted: torch.Tensor, diag: Optional[torch.Tensor] = None,
+                              status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """spec_verify_sample on the library's per-device static workspace: allocates nothing.
+    Calls on one device share that workspace, so calls that may overlap must be serialised;
+    the first call on a device clears it and should come before any stream capture."""
+    B, gp1, V = target_logits.shape
+    gmax = gp1 - 1
+    if draft_logits.dtype != target_logits.dtype:
+        raise TypeError("target and draft logits must have the same dtype")
+    lib = load_library()
+    code = _dtype_code(target_logits)
+    _check(lib.spec_verify_sample_static(
+        _ptr(target_logits, "target_logits"),
+        _ptr(draft_logits, "draft_logits", None, (B, gmax, V)), code,
+        _ptr(draft_tokens, "draft_tokens", torch.int32, (B, gmax)),
+        _ptr(num_draft, "num_draft", torch.int32, (B,)),
+        _ptr(temperature, "temperature", torch.float32, (B,)),
+        _ptr(u_accept, "u_accept", torch.float32, (B, gmax)),
+        _ptr(u_sample, "u_sample", torch.float32, (B,)), B, gmax, V,
+        _ptr(out_tokens, "out_tokens", torch.int32, (B, gmax + 1)),
+        _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
+        _ptr(diag, "diag", torch.float32, (B, 2 * gmax + 1)),
+        _ptr(status, "status", torch.int32, (B,)), _stream(stream)))
 
 
 def _commit_gmax(out_tokens, gmax):

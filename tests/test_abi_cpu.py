@@ -109,7 +109,7 @@ def test_binding_arity_matches_header(lib):
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
         text += re.sub(r"/\*.*?\*/", "", open(h, encoding="utf-8").read(), flags=re.S)
     for name in ("spec_verify_greedy", "spec_verify_sample", "spec_commit_kv_lengths",
-                 "spec_verify_workspace_bytes", "spec_verify_plan"):
+                 "spec_verify_workspace_bytes", "spec_verify_plan", "spec_verify_sample_static"):
         m = re.search(r"\b" + name + r"\s*\(([^)]*)\)", text)
         params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
         assert len(getattr(lib, name).argtypes) == len(params), name
@@ -117,3 +117,15 @@ def test_binding_arity_matches_header(lib):
     import inspect
     src = inspect.getsource(sv.prepare_verify_sample)
     assert "wsp, wsn" in src
+
+
+def test_static_workspace_refuses_oversized_calls(lib):
+    """The static-workspace entry refuses, on the host, a batch whose counters alone exceed
+    the array (B = 100000 at gmax = 4, V = 128256: 6.4 MB of draw-chunk states)."""
+    n0 = lib.spec_launch_count()
+    rc = lib.spec_verify_sample_static(FAKE, FAKE, 0, FAKE, None, FAKE, FAKE, FAKE, 100000, 4, 128256,
+                                       FAKE, FAKE, None, None, None)
+    assert rc == 3 and b"static workspace" in lib.spec_last_error()
+    assert lib.spec_launch_count() == n0
+    assert lib.spec_verify_sample_static(FAKE, FAKE, 0, FAKE, None, FAKE, FAKE, FAKE, 0, 4, 128256,
+                                         FAKE, FAKE, None, None, None) == 0
