@@ -372,8 +372,8 @@ def run_native(args):
     if rank == 0 and world == 1:
         rate, nseq, rows, el = cpu_oracle_rate(wl, args.cpu_seconds)
         cpu = {"value": rate, "unit": "rows/s", "cores": 1, "kind": "oracle",
-               "sample": f"{nseq} of the {wl.B} sequences of the same batch ({rows} verified rows, "
-                         f"{el:.1f} s), float64 numpy oracle, single thread"}
+               "sample": f"{nseq} sequence verifications cycling over the batch's {wl.B} sequences "
+                         f"({rows} verified rows, {el:.1f} s), float64 numpy oracle, single thread"}
 
     if rank == 0:
         traffic = recorded_traffic(1)
