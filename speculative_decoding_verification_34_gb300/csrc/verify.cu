@@ -49,8 +49,15 @@ constexpr int kVecPerPass = 4;                         // 16-byte vectors per th
 #ifndef SPEC_PREFETCH
 #define SPEC_PREFETCH 1
 #endif
+#ifndef SPEC_RING
+#define SPEC_RING 0
+#endif
 constexpr int kDrawVec = SPEC_DRAW_VEC;                // vectors of each row per thread per draw step
 constexpr bool kPrefetch = SPEC_PREFETCH != 0;         // row passes double-buffered in registers
+constexpr int kRing = SPEC_RING;                       // >0: row passes staged through a ring of
+                                                       // this many 16 KB shared-memory stages
+constexpr int kStageBytes = 16384;                     // one pass of one row (bf16 or fp32)
+constexpr long long kMbarWaitNs = 2000000;             // bound on one stage wait (2 ms)
 constexpr int kMaxChunks = 64;                         // row chunks, and draw chunks, per row
 constexpr int kMaxSlices = 16;                         // kThreads-vector slices per draw chunk
 #ifndef SPEC_CHUNK_TARGET
@@ -362,6 +369,58 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
   return v;
 }
 
+// ---- bulk copies into shared memory, completed on an mbarrier -----------------------------
+
+__device__ __forceinline__ unsigned smem_addr(const void* p) {
+  return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n\tfence.proxy.async.shared::cta;" ::: "memory");
+}
+// one arrival that also announces `bytes` of transfer; the phase completes when they land
+__device__ __forceinline__ void mbar_expect(uint64_t* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+// global -> shared bulk copy (16-byte aligned addresses, size a multiple of 16)
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* bar, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ long long global_ns() {
+  long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// waits for the phase of the given parity; false if kMbarWaitNs passed first
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
+  if (mbar_try(bar, parity)) return true;
+  const long long t0 = global_ns();
+  for (;;) {
+    if (mbar_try(bar, parity)) return true;
+    if (global_ns() - t0 > kMbarWaitNs) return false;
+  }
+}
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(smem_addr(p)));
+  return v;
+}
+
 // inclusive prefix sum over the warp's lanes, in a fixed association order
 __device__ __forceinline__ float warp_incl_scan(float v) {
   const int lane = int(threadIdx.x) & 31;
@@ -382,8 +441,10 @@ struct Shared {
   float wsum[kMaxSlices][kWarps];                 // selector: per-(slice, warp) weight sums
   int last, go, m, flags, owner, slice, warp_sel, token;
   unsigned taken[2];
+  int err;
   float target_local, mass_out, run_sel;
   PlanRec plan;
+  uint64_t bars[kRing > 0 ? kRing : 1];
 };
 
 // ------------------------------------------------------------------------------------------
@@ -854,7 +915,52 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
       if (sq.sampling) thread_stats(t, sq.k, rm, rs);
       else tile_argmax(t, e0, tid, rm, ri);
     };
-    if constexpr (kPrefetch) {
+    if constexpr (kRing > 0 && kVec) {
+      // passes staged through a ring of kRing shared-memory stages by bulk copies: thread 0
+      // keeps kRing passes in flight; a stage is refilled once every thread has its tile
+      extern __shared__ __align__(128) unsigned char ring[];
+      const int npass = lo < hi ? int((hi - lo + kPass - 1) / kPass) : 0;
+      auto issue = [&](int p) {
+        const int st = p % kRing;
+        const int64_t e0 = lo + int64_t(p) * kPass;
+        const int64_t n = hi - e0 < kPass ? hi - e0 : kPass;
+        const unsigned bytes = unsigned(n * int64_t(sizeof(raw)));
+        mbar_expect(&sm.bars[st], bytes);
+        bulk_load(ring + st * kStageBytes, row + e0, bytes, &sm.bars[st]);
+      };
+      if (tid == 0) {
+        sm.err = 0;
+        for (int st = 0; st < kRing; ++st) mbar_init(&sm.bars[st]);
+        mbar_fence_init();
+        for (int p = 0; p < npass && p < kRing; ++p) issue(p);
+      }
+      __syncthreads();
+      for (int p = 0; p < npass; ++p) {
+        const int st = p % kRing;
+        const int64_t e0 = lo + int64_t(p) * kPass;
+        if (!mbar_wait(&sm.bars[st], unsigned(p / kRing) & 1u)) sm.err = 1;
+        Tile<E, kVec> t;
+#pragma unroll
+        for (int q = 0; q < kVecPerPass; ++q) {
+          const int off = q * kThreads + tid;
+          t.v[q] = e0 + int64_t(off) * N < hi ? lds128(ring + st * kStageBytes + off * 16)
+                                               : make_uint4(E::kNegInf, E::kNegInf, E::kNegInf, E::kNegInf);
+        }
+        __syncthreads();
+        if (tid == 0 && p + kRing < npass && !sm.err) issue(p + kRing);
+        consume(t, e0);
+      }
+      if (sm.err) {
+        // a stage wait ran out: wait, again bounded, for every copy this block issued, then
+        // report the sequence
+        if (tid == 0) {
+          for (int p = npass - kRing > 0 ? npass - kRing : 0; p < npass; ++p)
+            mbar_wait(&sm.bars[p % kRing], unsigned(p / kRing) & 1u);
+          if (a.status) atomicOr(&a.status[b], SPEC_ST_TIMEOUT);
+        }
+        __syncthreads();
+      }
+    } else if constexpr (kPrefetch) {
       // two tiles in registers: the next pass is in flight while this one is reduced
       Tile<E, kVec> t0, t1;
       if (lo < hi) fetch(t0, lo);
@@ -1086,6 +1192,8 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
   const int brows = kMixed ? (geo.DCL + geo.CL - 1) / geo.CL : 0;   // grid rows of B units
   const int G = geo.CL * (geo.nslots + brows);                       // units per group
   // B units of a sequence come about kDrawWaves waves of resident blocks after its A units
+  // the shared-memory ring of the row passes (vector path only)
+  const size_t dyn_smem = (kRing > 0 && kVec) ? size_t(kRing) * kStageBytes : 0;
   int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -1095,7 +1203,11 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
     if (dev < 64 && cached[dev]) {
       per_sm = cached[dev];
     } else {
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, 0);
+      if (dyn_smem > 0) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(dyn_smem));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute (ring size)");
+      }
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, dyn_smem);
       if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
       if (per_sm < 1) per_sm = 1;
       if (dev < 64) cached[dev] = per_sm;
@@ -1114,7 +1226,7 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
     geo.b0 = b0;
     geo.b1 = b0 + per_launch < args.B ? b0 + per_launch : args.B;
     const dim3 grid(unsigned(geo.CL), unsigned(geo.nslots + brows), unsigned(geo.b1 - b0 + geo.delta));
-    fn<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(args, geo, w);
+    fn<<<grid, kThreads, dyn_smem, static_cast<cudaStream_t>(stream)>>>(args, geo, w);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "verify kernel launch");
     count_launch();
