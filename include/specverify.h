@@ -30,7 +30,8 @@
  *        u_accept      [B][gmax]        float32 uniforms in [0,1), one per acceptance test
  *        u_sample      [B]              float32 uniform in [0,1) for the correction/bonus draw
  *        out_tokens    [B][gmax+1]      int32: the m+1 emitted tokens, then -1
- *    Rows past a sequence's num_draft are never read (they may hold anything).
+ *    Rows past a sequence's num_draft are never used (they may hold anything; the kernel may
+ *    read, and drop, up to 32 KB of such a row before it has loaded num_draft).
  *  - Logits are bf16 (SPEC_BF16, raw 16-bit patterns) or float32 (SPEC_F32).  They must be
  *    finite or -inf, with at least one finite value per read row; NaN or +inf inputs give
  *    unspecified (but memory-safe) results.
@@ -102,7 +103,7 @@ int spec_verify_greedy(const void* target_logits, int dtype, const int32_t* draf
  * order, of max(p_m - q_m, 0)/R at u_sample[b]*R (R its total); if R == 0 it is drawn from
  * p_m instead (SPEC_ST_R_ZERO).  On full acceptance the bonus token is the inverse-CDF draw
  * of p at row num_draft[b].  A sequence with T <= 0 (or NaN) is verified greedily exactly
- * as spec_verify_greedy does, and its draft rows are not read.
+ * as spec_verify_greedy does, and its draft rows are not used.
  *
  *   draft_logits   [B][gmax][V], same dtype as target_logits
  *   temperature    [B] float32

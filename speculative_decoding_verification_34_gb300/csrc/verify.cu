@@ -42,7 +42,10 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kVecPerPass = 4;                         // 16-byte vectors per thread per row pass
+#ifndef SPEC_VEC_PER_PASS
+#define SPEC_VEC_PER_PASS 4
+#endif
+constexpr int kVecPerPass = SPEC_VEC_PER_PASS;         // 16-byte vectors per thread per row pass
 #ifndef SPEC_DRAW_VEC
 #define SPEC_DRAW_VEC 4
 #endif
@@ -56,7 +59,7 @@ constexpr int kDrawVec = SPEC_DRAW_VEC;                // vectors of each row pe
 constexpr bool kPrefetch = SPEC_PREFETCH != 0;         // row passes double-buffered in registers
 constexpr int kRing = SPEC_RING;                       // >0: row passes staged through a ring of
                                                        // this many 16 KB shared-memory stages
-constexpr int kStageBytes = 16384;                     // one pass of one row (bf16 or fp32)
+constexpr int kStageBytes = kThreads * kVecPerPass * 16;   // one pass of one row (bf16 or fp32)
 constexpr long long kMbarWaitNs = 2000000;             // bound on one stage wait (2 ms)
 constexpr int kMaxChunks = 64;                         // row chunks, and draw chunks, per row
 constexpr int kMaxSlices = 16;                         // kThreads-vector slices per draw chunk
@@ -67,14 +70,14 @@ constexpr int kMaxSlices = 16;                         // kThreads-vector slices
 #define SPEC_DRAW_CHUNK_TARGET 8192
 #endif
 #ifndef SPEC_DRAW_WAVES
-#define SPEC_DRAW_WAVES 3
+#define SPEC_DRAW_WAVES 3.0
 #endif
 #ifndef SPEC_MIN_BLOCKS
 #define SPEC_MIN_BLOCKS 4
 #endif
 constexpr int kChunkTarget = SPEC_CHUNK_TARGET;        // ids per row chunk before rounding
 constexpr int kDrawChunkTarget = SPEC_DRAW_CHUNK_TARGET;   // ids per draw chunk before rounding
-constexpr int kDrawWaves = SPEC_DRAW_WAVES;            // distance of the draw behind the rows
+constexpr double kDrawWaves = SPEC_DRAW_WAVES;         // distance of the draw behind the rows
 constexpr int kMinBlocks = SPEC_MIN_BLOCKS;            // resident blocks per SM the registers allow
 constexpr int kMaxGroups = 65535;                      // grid z limit
 constexpr int kPlanWaitIters = 32;                     // optional bounded wait of a B unit (~15 us)
@@ -891,11 +894,26 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
     // ---------------- A unit: row chunk x of row slot y -------------------------------------
     const int b = grp, slot = y, c = x;
     if (b >= geo.b1) return;
-    const Seq<E, kMixed> sq(a, b);
-    if (!sq.slot_valid(slot, a.gmax)) return;
-    const raw* row = sq.row(slot, a.gmax, a.V);
+    // The row's address does not depend on the sequence's num_draft and temperature: its
+    // first two passes are started before those arrive.  A row past num_draft (or a draft
+    // row of a greedy sequence) is inside the caller's tensors; its passes are dropped.
+    const raw* row = slot <= a.gmax
+                         ? static_cast<const raw*>(a.target) + (int64_t(b) * (a.gmax + 1) + slot) * a.V
+                         : static_cast<const raw*>(a.draft) + (int64_t(b) * a.gmax + (slot - a.gmax - 1)) * a.V;
     const int64_t lo = int64_t(c) * geo.chunk;
     const int64_t hi = lo + geo.chunk < a.V ? lo + geo.chunk : a.V;
+    auto fetch = [&](Tile<E, kVec>& t, int64_t e0) {
+      if (e0 + kPass <= hi) t.load_full(row, e0, tid);
+      else t.load(row, e0, hi, tid);
+    };
+    constexpr bool kRegs = kPrefetch && !(kRing > 0 && kVec);
+    Tile<E, kVec> t0, t1;
+    if constexpr (kRegs) {
+      if (lo < hi) fetch(t0, lo);
+      if (lo + kPass < hi) fetch(t1, lo + kPass);
+    }
+    const Seq<E, kMixed> sq(a, b);
+    if (!sq.slot_valid(slot, a.gmax)) return;
     // the logit at this row's draft id, if it lies in this chunk: fetched once, up front
     const int i = slot <= a.gmax ? slot : slot - a.gmax - 1;
     bool has_d = false;
@@ -907,10 +925,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
     }
     float rm = -INFINITY, rs = 0.f;
     int ri = INT_MAX;
-    auto fetch = [&](Tile<E, kVec>& t, int64_t e0) {
-      if (e0 + kPass <= hi) t.load_full(row, e0, tid);
-      else t.load(row, e0, hi, tid);
-    };
     auto consume = [&](const Tile<E, kVec>& t, int64_t e0) {
       if (sq.sampling) thread_stats(t, sq.k, rm, rs);
       else tile_argmax(t, e0, tid, rm, ri);
@@ -960,16 +974,15 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
         }
         __syncthreads();
       }
-    } else if constexpr (kPrefetch) {
-      // two tiles in registers: the next pass is in flight while this one is reduced
-      Tile<E, kVec> t0, t1;
-      if (lo < hi) fetch(t0, lo);
+    } else if constexpr (kRegs) {
+      // two tiles in registers, both passes already in flight: each is refilled with the
+      // pass after next as soon as it has been reduced
       for (int64_t e0 = lo; e0 < hi; e0 += 2 * kPass) {
-        if (e0 + kPass < hi) fetch(t1, e0 + kPass);
         consume(t0, e0);
-        if (e0 + kPass >= hi) break;
         if (e0 + 2 * kPass < hi) fetch(t0, e0 + 2 * kPass);
+        if (e0 + kPass >= hi) break;
         consume(t1, e0 + kPass);
+        if (e0 + 3 * kPass < hi) fetch(t1, e0 + 3 * kPass);
       }
     } else {
       for (int64_t e0 = lo; e0 < hi; e0 += kPass) {
@@ -1010,18 +1023,22 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
     const int b = grp - geo.delta;
     if (dc >= geo.DCL || b < geo.b0 || b >= geo.b1) return;
     const Seq<E, kMixed> sq(a, b);
+    // the plan flag is read while the sequence's metadata loads are still in flight
+    int rdy = 0;
+    if (tid == 0) rdy = ld_acquire(&w.ready[b]);
     if (!sq.sampling) return;
     if (tid == 0) {
       int* st = &w.state[int64_t(b) * geo.DCL + dc];
       // optional, bounded wait for the plan; correctness does not depend on it
       int it = 0, ns = 64;
-      while (ld_acquire(&w.ready[b]) == 0 && it < kPlanWaitIters) {
+      while (rdy == 0 && it < kPlanWaitIters) {
         __nanosleep(ns);
         if (ns < 512) ns <<= 1;
         ++it;
+        rdy = ld_acquire(&w.ready[b]);
       }
       bool mine = false;
-      if (ld_acquire(&w.ready[b]) != 0) {
+      if (rdy != 0) {
         // the plan is out: the decider takes only given-up chunks, so this one stays ours
         // without a claim
         mine = true;
@@ -1216,7 +1233,7 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
   const int64_t resident = int64_t(sms) * per_sm;
-  geo.delta = kMixed ? int((kDrawWaves * resident + G - 1) / G) : 0;
+  geo.delta = kMixed ? int(std::ceil(kDrawWaves * double(resident) / double(G))) : 0;
   if (geo.delta > kMaxGroups / 2) geo.delta = kMaxGroups / 2;
   const Work w = ws_views(ws, L);
   // one launch covers at most kMaxGroups groups (the grid's z limit); larger batches take
