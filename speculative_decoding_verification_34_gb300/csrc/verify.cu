@@ -119,6 +119,13 @@ struct __align__(16) PlanRec {   // per sequence, published by the decider for t
   float mkp, invp, mkq, invq;
 };
 
+// The published flag carries what a draw unit needs to start its loads: 0 = not yet, else
+// bit 31 set, status flags in bits 20..27, pair in bit 16, m in bits 0..15.  The plan's
+// normalisers are read from the record alongside the row loads.
+__host__ __device__ inline int ready_word(const PlanRec& pr) {
+  return int(0x80000000u | (unsigned(pr.flags & 0xff) << 20) | (unsigned(pr.pair & 1) << 16) | unsigned(pr.m & 0xffff));
+}
+
 struct Work {      // views into the caller's workspace
   int* cnt;        // [B] A arrivals               (counter header)
   int* bdone;      // [B] draw-chunk arrivals      (counter header)
@@ -854,7 +861,7 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
     sm.plan = pr;
     w.cnt[b] = 0;
     __threadfence();                 // the plan before the flag
-    atomicExch(&w.ready[b], 1);
+    atomicExch(&w.ready[b], ready_word(pr));
     __threadfence();                 // the flag before the chunk states read below
   }
   __syncthreads();
@@ -1045,24 +1052,19 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
       } else if (atom_cas(st, kChunkFree, kChunkGivenUp) == kChunkFree) {
         // given up; if the plan appeared meanwhile, take the chunk back unless the decider has
         __threadfence();
-        if (ld_acquire(&w.ready[b]) != 0) mine = atom_cas(st, kChunkGivenUp, kChunkMine) == kChunkGivenUp;
+        const int r2 = ld_acquire(&w.ready[b]);
+        if (r2 != 0) {
+          mine = atom_cas(st, kChunkGivenUp, kChunkMine) == kChunkGivenUp;
+          rdy = r2;
+        }
       }
       if (mine) {
-        // ordered after the acquire above; through L2: an earlier read of this line by the
-        // same SM may sit stale in L1
-        const int4* src = reinterpret_cast<const int4*>(&w.plan[b]);
-        const int4 h0 = __ldcg(src), h1 = __ldcg(src + 1);
-        sm.plan.m = h0.x;
-        sm.plan.g = h0.y;
-        sm.plan.flags = h0.z;
-        sm.plan.pair = h0.w;
-        sm.plan.mkp = __int_as_float(h1.x);
-        sm.plan.invp = __int_as_float(h1.y);
-        sm.plan.mkq = __int_as_float(h1.z);
-        sm.plan.invq = __int_as_float(h1.w);
-        const PlanRec& pl = sm.plan;
+        sm.plan.m = rdy & 0xffff;
+        sm.plan.pair = (rdy >> 16) & 1;
+        sm.plan.flags = (rdy >> 20) & 0xff;
+        sm.plan.g = sq.g;
         // never fails for a well-formed workspace; keeps every read in bounds
-        if (pl.m < 0 || pl.m > sq.g || (pl.pair && pl.m >= sq.g)) {
+        if (sm.plan.m > sq.g || (sm.plan.pair && sm.plan.m >= sq.g)) {
           mine = false;
           if (a.status) atomicOr(&a.status[b], SPEC_ST_TIMEOUT);
         }
@@ -1071,7 +1073,16 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
     }
     __syncthreads();
     if (!sm.go) return;
-    draw_chunk<E, kVec, kMixed>(a, geo, w, sq, sm.plan, dc, sm);
+    // the normalisers, ordered after thread 0's acquire by the barrier; through L2 (an
+    // earlier read of this line by the same SM may sit stale in L1).  Their load and the
+    // rows' loads are in flight together.
+    PlanRec pl = sm.plan;
+    const float4 nf = __ldcg(reinterpret_cast<const float4*>(&w.plan[b]) + 1);
+    pl.mkp = nf.x;
+    pl.invp = nf.y;
+    pl.mkq = nf.z;
+    pl.invq = nf.w;
+    draw_chunk<E, kVec, kMixed>(a, geo, w, sq, pl, dc, sm);
   }
 }
 
