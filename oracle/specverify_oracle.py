@@ -36,6 +36,12 @@ Readings where the pages leave a step open (each also listed in the design doc):
     num_draft outside [0, gmax] is clamped (status bit 4).
   * Temperature T <= 0 (or NaN) marks a greedy sequence; otherwise p = softmax(P/T)
     and q = softmax(Q/T), the same T on both sides.
+  * Stops ([TUT] §5.2 "common mistakes": nothing after an EOS in the candidate block
+    may reach the cache; §12.3: EOS, maximum length and the rejection position must
+    agree with step-by-step decoding; [KB] §03: an end token or a length limit may end
+    the round early).  A round's emit d_0..d_{m-1}, tok is cut after its first EOS and
+    to the sequence's remaining token budget; the last emitted token is, as a
+    correction token is, not yet fed to the models, so m becomes (tokens emitted) - 1.
 
 Parity pins: see tests/test_oracle_pins.py.  Every function below is pinned by at
 least one test against values the pages print, closed forms, or brute force.
@@ -53,6 +59,7 @@ ST_BAD_DRAFT = 1
 ST_R_ZERO = 2
 ST_CLAMPED_GAMMA = 4
 ST_HISTORY_FULL = 8
+ST_STOPPED = 32
 
 
 def widen(row: np.ndarray, dtype: str) -> np.ndarray:
@@ -259,9 +266,10 @@ def commit_kv_lengths(kv_len: np.ndarray, m: np.ndarray, correction_processed: b
 
     Both caches are trimmed to t + m (the accepted prefix); once the correction or bonus
     token has been fed through both models they hold t + m + 1.  When a token history is
-    given, the m+1 emitted tokens are appended at committed_len; a sequence whose append
-    position is not legal (committed_len < 0, or the history would overflow) is left
-    untouched and flagged (bit 8).
+    given, the emitted tokens (out_tokens[b, :m+1] up to its first -1, which only a stop
+    leaves there) are appended at committed_len; a sequence whose append position is not
+    legal (committed_len < 0, or the history would overflow) is left untouched and flagged
+    (bit 8).
     Returns (kv_len, draft_kv_len, history, committed_len, status) as new arrays.
     """
     kv = np.array(kv_len, dtype=np.int64)
@@ -272,6 +280,11 @@ def commit_kv_lengths(kv_len: np.ndarray, m: np.ndarray, correction_processed: b
     add = 1 if correction_processed else 0
     for b in range(len(kv)):
         n = int(m[b]) + 1
+        if out_tokens is not None:
+            # only the emitted tokens: a round cut by a stop leaves -1 after them
+            lead = np.flatnonzero(np.asarray(out_tokens[b, :n]) < 0)
+            if lead.size:
+                n = int(lead[0])
         if hist is not None:
             cap = hist.shape[1]
             if clen[b] < 0 or clen[b] + n > cap:
@@ -283,3 +296,40 @@ def commit_kv_lengths(kv_len: np.ndarray, m: np.ndarray, correction_processed: b
         if dkv is not None:
             dkv[b] += int(m[b]) + add
     return kv, dkv, hist, clen, status
+
+
+def apply_stops(out_tokens: np.ndarray, m: np.ndarray, eos_id: int,
+                max_new: Optional[np.ndarray] = None):
+    """Cut each round's emit where step-by-step decoding would have stopped ([TUT] §5.2,
+    §12.3; [KB] §03).
+
+    The emit is out_tokens[b, :m+1] = d_0..d_{m-1}, tok.  It ends at its first token equal
+    to eos_id (kept; eos_id < 0 means no end token) and holds at most max_new[b] tokens
+    (the sequence's remaining budget; <= 0 emits nothing).  Emitted tokens stay, the rest
+    become -1, and m becomes (tokens emitted) - 1, at least 0: every emitted token but the
+    last has its cache entries kept, the last is fed next, as a correction token would be.
+    Bit 32 marks a sequence that must not continue: its last emitted token is the end
+    token, or its budget is used up.
+    Returns (out_tokens, m, status) as new arrays.
+    """
+    out = np.array(out_tokens, dtype=np.int64)
+    mm = np.array(m, dtype=np.int64)
+    status = np.zeros(len(mm), dtype=np.int64)
+    gmax = out.shape[1] - 1
+    for b in range(len(mm)):
+        n = min(max(int(mm[b]), 0), gmax) + 1
+        if eos_id >= 0:
+            hit = np.flatnonzero(out[b, :n] == eos_id)
+            if hit.size:
+                n = int(hit[0]) + 1
+        stop_budget = False
+        if max_new is not None:
+            budget = int(max_new[b])
+            n = min(n, max(budget, 0))
+            stop_budget = n >= budget
+        stop_eos = eos_id >= 0 and n >= 1 and out[b, n - 1] == eos_id
+        out[b, n:] = -1
+        mm[b] = max(n - 1, 0)
+        if stop_eos or stop_budget:
+            status[b] |= ST_STOPPED
+    return out, mm, status

@@ -287,3 +287,75 @@ def check_greedy_tie_rule():
     row = np.array([1.0, 3.0, 2.0, 3.0, -np.inf, 3.0])
     assert O.greedy_argmax(row) == 1
     assert O.greedy_argmax(np.full(5, -np.inf)) == 0
+
+
+# ------------------------------------------------------------------------------------------
+# stops: speculative rounds with the oracle's verify and stops reproduce step-by-step decoding
+# that ends at the first end token or at the length limit ([TUT] §12.3 asks exactly this of
+# EOS, maximum length and the rejection position; §5.2 forbids anything after an EOS in the
+# candidate block from reaching the cache)
+# ------------------------------------------------------------------------------------------
+
+def toy_model(seed, V, eos, eos_bias):
+    """A deterministic toy language model: the logits after any prefix come from a generator
+    seeded by (seed, prefix)."""
+    def logits(prefix):
+        x = np.random.default_rng([seed, len(prefix)] + [int(t) for t in prefix]).normal(0.0, 2.0, V)
+        x[eos] += eos_bias
+        return x
+    return logits
+
+
+def noisy_copy(model, seed, sigma):
+    """A draft model: the target's logits plus seeded noise (high but imperfect agreement)."""
+    def logits(prefix):
+        x = model(prefix)
+        return x + np.random.default_rng([seed, len(prefix)] + [int(t) for t in prefix]).normal(0.0, sigma, len(x))
+    return logits
+
+
+def ar_greedy_decode(target, prompt, eos, max_new):
+    """Step-by-step greedy decoding: one target argmax per token (first index on ties), stop
+    after the end token or after max_new tokens."""
+    out = []
+    while len(out) < max_new:
+        t = int(np.argmax(target(prompt + out)))
+        out.append(t)
+        if t == eos:
+            break
+    return out
+
+
+def spec_greedy_decode(target, draft, prompt, eos, max_new, gamma, max_rounds=200):
+    """Speculative greedy decoding through the oracle: draft gamma tokens greedily, verify
+    them against the target rows, cut the emit with apply_stops, append, repeat."""
+    from oracle import specverify_oracle as O
+    out = []
+    for _ in range(max_rounds):
+        prefix = prompt + out
+        ds = []
+        for _i in range(gamma):
+            ds.append(int(np.argmax(draft(prefix + ds))))
+        rows = np.stack([target(prefix + ds[:i]) for i in range(gamma + 1)])
+        r = O.verify_greedy_sequence(rows, np.array(ds), gamma)
+        toks = np.full((1, gamma + 1), -1, dtype=np.int64)
+        toks[0, : len(r.tokens)] = r.tokens
+        o2, _, st = O.apply_stops(toks, np.array([r.m]), eos, np.array([max_new - len(out)]))
+        out += [int(t) for t in o2[0] if t >= 0]
+        if st[0] & O.ST_STOPPED:
+            return out
+    raise AssertionError("speculative decoding did not stop")
+
+
+def check_stops_match_step_by_step(cases=None):
+    """Cases mix end tokens accepted inside a draft block, end tokens as the correction or
+    bonus token, and budgets that cut a block (V = 10, id 0 the end token)."""
+    cases = cases or [(seed, g, n, bias) for seed in range(10) for g in (1, 2, 4)
+                      for n in (1, 3, 9, 25) for bias in (-1.0, 0.5)]
+    for seed, gamma, max_new, bias in cases:
+        V, eos = 10, 0
+        target = toy_model(seed, V, eos, bias)
+        draft = noisy_copy(target, seed + 100, 1.0)
+        want = ar_greedy_decode(target, [3], eos, max_new)
+        got = spec_greedy_decode(target, draft, [3], eos, max_new, gamma)
+        assert got == want, (seed, gamma, max_new, bias, got, want)

@@ -26,6 +26,26 @@ def _icdf_ge(weights, u):
     return v, 1.0, total
 
 
+def _stops_last_token_only(out_tokens, m, eos_id, max_new=None):
+    # the tutorial's loop tests only output[-1] for the end token (an EOS accepted inside the
+    # block is emitted and followed by more tokens)
+    out = np.array(out_tokens)
+    mm = np.array(m)
+    st = np.zeros(len(mm), dtype=np.int64)
+    for b in range(len(mm)):
+        n = int(mm[b]) + 1
+        if max_new is not None:
+            n = min(n, max(int(max_new[b]), 0))
+        if (n >= 1 and out[b, n - 1] == eos_id) or (max_new is not None and n >= int(max_new[b])):
+            st[b] |= O.ST_STOPPED
+        out[b, n:] = -1
+        mm[b] = max(n - 1, 0)
+    return out, mm, st
+
+
+_apply_stops = O.apply_stops
+
+
 MUTATIONS = {
     "resample_from_p": ("residual_weights", lambda p, q: p.copy()),
     "residual_transposed": ("residual_weights", lambda p, q: np.maximum(q - p, 0.0)),
@@ -35,6 +55,8 @@ MUTATIONS = {
     "greedy_last_tie": ("greedy_argmax", _greedy_last_max),
     "inverse_cdf_ge": ("inverse_cdf", _icdf_ge),
     "row_shift": ("verify_sample_sequence", None),
+    "stops_last_token_only": ("apply_stops", _stops_last_token_only),
+    "stops_budget_ignored": ("apply_stops", lambda o, m, e, n=None: _apply_stops(o, m, e, None)),
 }
 
 
@@ -43,7 +65,8 @@ def _pins_pass():
               pins.check_expected_tokens, pins.check_inverse_cdf_convention,
               pins.check_greedy_tie_rule,
               lambda: pins.check_joint_law(3, 2, 0.7, 2),
-              lambda: pins.check_joint_law(3, 1, 1.0, 1)]
+              lambda: pins.check_joint_law(3, 1, 1.0, 1),
+              pins.check_stops_match_step_by_step]
     for c in checks:
         try:
             c()

@@ -166,3 +166,29 @@ def test_greedy_workload_closed_form():
     for b, r in enumerate(res):
         row = W.bf16_bits_to_f32(wl.target[b, r.m])
         assert r.tokens[-1] == int(np.argmax(row))
+
+
+def test_stops_match_step_by_step_decoding():
+    """Speculative rounds (oracle verify + stops) reproduce greedy step-by-step decoding that
+    ends at the first end token or at the length limit ([TUT] §12.3, §5.2)."""
+    pins.check_stops_match_step_by_step()
+
+
+def test_stops_special_cases():
+    out = np.array([[5, 0, 7, 9], [4, 6, -1, -1], [1, 2, 3, 4], [0, 8, 8, 8]])
+    m = np.array([3, 1, 3, 3])
+    o, mm, st = O.apply_stops(out, m, 0, None)
+    assert o.tolist() == [[5, 0, -1, -1], [4, 6, -1, -1], [1, 2, 3, 4], [0, -1, -1, -1]]
+    assert mm.tolist() == [1, 1, 3, 0] and st.tolist() == [O.ST_STOPPED, 0, 0, O.ST_STOPPED]
+    # budgets: 2 cuts a block (and stops), 5 does not bind, 0 emits nothing, -3 too
+    o, mm, st = O.apply_stops(out, m, -1, np.array([2, 5, 0, -3]))
+    assert o.tolist() == [[5, 0, -1, -1], [4, 6, -1, -1], [-1] * 4, [-1] * 4]
+    assert mm.tolist() == [1, 1, 0, 0] and st.tolist() == [O.ST_STOPPED, 0, O.ST_STOPPED, O.ST_STOPPED]
+    # a budget that lands exactly on the emit length stops the sequence, one above does not
+    o, mm, st = O.apply_stops(out, m, -1, np.array([4, 3, 4, 5]))
+    assert st.tolist() == [O.ST_STOPPED, 0, O.ST_STOPPED, 0] and mm.tolist() == [3, 1, 3, 3]
+    # commit appends only the emitted tokens of a cut round
+    kv, _, hist, clen, st = O.commit_kv_lengths(np.array([10, 10]), np.array([0, 1]), False,
+                                                out_tokens=np.array([[-1, -1], [4, 6]]),
+                                                history=np.full((2, 4), -9), committed_len=np.array([1, 1]))
+    assert clen.tolist() == [1, 3] and hist.tolist() == [[-9] * 4, [-9, 4, 6, -9]] and kv.tolist() == [10, 11]
