@@ -73,6 +73,7 @@ typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype_t;
 #define SPEC_ST_HISTORY_FULL 8   /* commit: appending would overflow the history; sequence left untouched */
 #define SPEC_ST_TIMEOUT 16       /* a bounded device-side wait ran out: outputs of the sequence not
                                     written; zero-fill the workspace before reusing it */
+#define SPEC_ST_STOPPED 32       /* stops: the sequence emitted its end token or used up its budget */
 
 /*
  * Greedy verification (temperature 0).
@@ -163,10 +164,11 @@ size_t spec_verify_workspace_bytes(int B, int gmax, int V, int dtype);
  * t + m + 1.  So, per sequence:
  *     target_kv_len[b] += num_accepted[b] + (correction_processed ? 1 : 0)
  * and the same for draft_kv_len when it is not NULL (invariant: target length == draft
- * length == committed length, tutorial §5.1).  When `history` is not NULL, the m+1 emitted
- * tokens out_tokens[b][0..m] are appended to history[b][committed_len[b]...] and
- * committed_len[b] grows by m+1; a sequence whose append would pass `cap` is left entirely
- * untouched (lengths included) and flagged SPEC_ST_HISTORY_FULL in status.
+ * length == committed length, tutorial §5.1).  When `history` is not NULL, the emitted
+ * tokens -- out_tokens[b][0..m] up to its first -1, which only spec_apply_stops leaves
+ * there, so normally all m+1 -- are appended to history[b][committed_len[b]...] and
+ * committed_len[b] grows by their count; a sequence whose append would pass `cap` is left
+ * entirely untouched (lengths included) and flagged SPEC_ST_HISTORY_FULL in status.
  *
  *   num_accepted   [B] int32 (m, as written by a verify call; values are clamped to
  *                  [0, gmax])
@@ -179,6 +181,29 @@ int spec_commit_kv_lengths(const int32_t* num_accepted, int B, int32_t* target_k
                            int32_t* draft_kv_len, int correction_processed,
                            const int32_t* out_tokens, int gmax, int32_t* history,
                            int32_t* committed_len, int cap, int32_t* status, void* stream);
+
+/*
+ * Stops: cut each round's emit where step-by-step decoding would have stopped (tutorial
+ * §5.2: nothing after an EOS in the candidate block may reach the cache; §12.3: EOS,
+ * maximum length and the rejection position must agree with step-by-step decoding; card §03:
+ * an end token or a length limit may end a round early).  Run it between a verify call and
+ * spec_commit_kv_lengths, on the same stream.
+ *
+ * Per sequence, the emit out_tokens[b][0..m] (m = num_accepted[b], clamped to [0, gmax])
+ * ends at its first token equal to eos_id (kept; eos_id < 0: no end token) and holds at most
+ * max_new[b] tokens (the sequence's remaining budget; <= 0 emits nothing; max_new NULL: no
+ * budget).  The tokens after the cut become -1 and num_accepted[b] becomes (tokens
+ * emitted) - 1, at least 0: every emitted token but the last keeps its cache entries, the
+ * last is fed next, as a correction token is.  status[b] (if not NULL) gets
+ * SPEC_ST_STOPPED when the last emitted token is eos_id or the budget is used up; such a
+ * sequence must not be continued (do not feed its last token).
+ *
+ *   out_tokens     [B][gmax+1] int32, read and written
+ *   num_accepted   [B] int32, read and written
+ *   max_new        [B] int32 or NULL
+ */
+int spec_apply_stops(int32_t* out_tokens, int32_t* num_accepted, int B, int gmax, int eos_id,
+                     const int32_t* max_new, int32_t* status, void* stream);
 
 /* Message for the calling thread's last non-OK return ("" if none). */
 const char* spec_last_error(void);

@@ -19,6 +19,7 @@ SPEC_BF16 = 0
 SPEC_F32 = 1
 SPEC_MAX_GAMMA = 32
 ST_BAD_DRAFT, ST_R_ZERO, ST_CLAMPED_GAMMA, ST_HISTORY_FULL = 1, 2, 4, 8
+ST_TIMEOUT, ST_STOPPED = 16, 32
 
 _lib = None
 
@@ -53,6 +54,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.spec_verify_workspace_bytes.restype = size_t
     lib.spec_commit_kv_lengths.argtypes = [vp, sz, vp, vp, i32, vp, sz, vp, vp, sz, vp, vp]
     lib.spec_commit_kv_lengths.restype = i32
+    lib.spec_apply_stops.argtypes = [vp, vp, sz, sz, i32, vp, vp, vp]
+    lib.spec_apply_stops.restype = i32
     lib.spec_last_error.argtypes = []
     lib.spec_last_error.restype = ctypes.c_char_p
     lib.spec_launch_count.argtypes = []
@@ -190,6 +193,19 @@ def spec_verify_sample_static(target_logits: torch.Tensor, draft_logits: torch.T
         _ptr(out_tokens, "out_tokens", torch.int32, (B, gmax + 1)),
         _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
         _ptr(diag, "diag", torch.float32, (B, 2 * gmax + 1)),
+        _ptr(status, "status", torch.int32, (B,)), _stream(stream)))
+
+
+def spec_apply_stops(out_tokens: torch.Tensor, num_accepted: torch.Tensor, eos_id: int,
+                     max_new: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                     stream=None) -> None:
+    """Cut each round's emit at its first end token and to the remaining budget, in place."""
+    B, gp1 = out_tokens.shape
+    lib = load_library()
+    _check(lib.spec_apply_stops(
+        _ptr(out_tokens, "out_tokens", torch.int32, (B, gp1)),
+        _ptr(num_accepted, "num_accepted", torch.int32, (B,)), B, gp1 - 1, int(eos_id),
+        _ptr(max_new, "max_new", torch.int32, (B,)),
         _ptr(status, "status", torch.int32, (B,)), _stream(stream)))
 
 

@@ -73,6 +73,10 @@ def test_host_argument_checks(lib):
     assert c(FAKE, 4, FAKE, None, 1, None, 40, None, None, 0, None, None) == 3
     assert c(FAKE, 0, FAKE, None, 1, None, 3, None, None, 0, None, None) == 0
     assert c(None, 0, None, None, 1, None, 3, None, None, 0, None, None) == 0
+    s = lib.spec_apply_stops
+    assert s(None, FAKE, 4, 3, 0, None, None, None) == 1 and s(FAKE, None, 4, 3, 0, None, None, None) == 1
+    assert s(FAKE, FAKE, -1, 3, 0, None, None, None) == 1 and s(FAKE, FAKE, 4, 40, 0, None, None, None) == 3
+    assert s(None, None, 0, 3, 0, None, None, None) == 0
     assert greedy(lib, target=None, toks=None, out=None, macc=None, B=0) == 0
     assert sample(lib, target=None, draft=None, temp=None, ua=None, us=None, B=0) == 0
     assert lib.spec_launch_count() == n0      # nothing was launched
@@ -109,7 +113,8 @@ def test_binding_arity_matches_header(lib):
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
         text += re.sub(r"/\*.*?\*/", "", open(h, encoding="utf-8").read(), flags=re.S)
     for name in ("spec_verify_greedy", "spec_verify_sample", "spec_commit_kv_lengths",
-                 "spec_verify_workspace_bytes", "spec_verify_plan", "spec_verify_sample_static"):
+                 "spec_verify_workspace_bytes", "spec_verify_plan", "spec_verify_sample_static",
+                 "spec_apply_stops"):
         m = re.search(r"\b" + name + r"\s*\(([^)]*)\)", text)
         params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
         assert len(getattr(lib, name).argtypes) == len(params), name
