@@ -324,6 +324,8 @@ def run_native(args):
     kern_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
     kern_mean_ms = statistics.fmean(kern_ms)
     kern_med_ms = statistics.median(kern_ms)
+    ks = sorted(kern_ms)
+    kern_p10, kern_p90 = ks[len(ks) // 10], ks[(9 * len(ks)) // 10]
     elapsed_ms = all_reduce_max(elapsed_ms, world, device)
     kern_mean_ms = all_reduce_max(kern_mean_ms, world, device)
 
@@ -332,6 +334,21 @@ def run_native(args):
     abytes = wl.algorithmic_bytes()
     peak, peak_src = measured_peak()
     achieved = abytes / (kern_mean_ms / 1e3) / 1e9
+
+    # ---- the post-verify kernels alone (stops, commit), per launch, on the same stream ----
+    budgets = torch.full((B,), 3, dtype=torch.int32, device=device)
+    def per_launch_us(fn, n=200):
+        for _ in range(10):
+            fn()
+        e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b_ in e:
+            a.record(stream)
+            fn()
+            b_.record(stream)
+        torch.cuda.synchronize(device)
+        return statistics.median(a.elapsed_time(b_) for a, b_ in e) * 1e3
+    post = {"spec_apply_stops_us": per_launch_us(lambda: sv.spec_apply_stops(out, macc, 0, budgets, st)),
+            "spec_commit_kv_lengths_us": per_launch_us(commit), "statistic": "median of 200 launches"}
 
     # ---- end to end through the public binding, host buffers, copies inside the region ----
     pin = lambda a: (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16
@@ -390,11 +407,12 @@ def run_native(args):
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": "verify_kernel<bf16, vec, mixed> (spec_verify_sample)",
                          "kernel_ms_mean": kern_mean_ms, "kernel_ms_median": kern_med_ms,
+                         "kernel_ms_p10": kern_p10, "kernel_ms_p90": kern_p90,
                          "algorithmic_bytes_per_launch": abytes, "peak_source": peak_src},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
-            "gpu_launches": launches, "clocks": clocks,
+            "gpu_launches": launches, "clocks": clocks, "post_kernels": post,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
