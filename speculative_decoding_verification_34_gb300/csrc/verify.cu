@@ -40,7 +40,10 @@
 namespace specverify {
 namespace {
 
-constexpr int kThreads = 256;
+#ifndef SPEC_THREADS
+#define SPEC_THREADS 256
+#endif
+constexpr int kThreads = SPEC_THREADS;
 constexpr int kWarps = kThreads / 32;
 #ifndef SPEC_VEC_PER_PASS
 #define SPEC_VEC_PER_PASS 4
@@ -61,16 +64,17 @@ constexpr int kRing = SPEC_RING;                       // >0: row passes staged 
                                                        // this many 16 KB shared-memory stages
 constexpr int kStageBytes = kThreads * kVecPerPass * 16;   // one pass of one row (bf16 or fp32)
 constexpr long long kMbarWaitNs = 2000000;             // bound on one stage wait (2 ms)
-constexpr int kMaxChunks = 64;                         // row chunks, and draw chunks, per row
-constexpr int kMaxSlices = 16;                         // kThreads-vector slices per draw chunk
+constexpr int kMaxChunks = 64;                         // row chunks per row
+constexpr int kMaxDrawChunks = 16;                     // draw chunks per row
+constexpr int kSubPerLane = kMaxDrawChunks * kWarps / 32;   // selector: sub-ranges per lane
 #ifndef SPEC_CHUNK_TARGET
 #define SPEC_CHUNK_TARGET 65536
 #endif
 #ifndef SPEC_DRAW_CHUNK_TARGET
-#define SPEC_DRAW_CHUNK_TARGET 8192
+#define SPEC_DRAW_CHUNK_TARGET 16384
 #endif
 #ifndef SPEC_DRAW_WAVES
-#define SPEC_DRAW_WAVES 3.0
+#define SPEC_DRAW_WAVES 1.5
 #endif
 #ifndef SPEC_MIN_BLOCKS
 #define SPEC_MIN_BLOCKS 4
@@ -78,12 +82,15 @@ constexpr int kMaxSlices = 16;                         // kThreads-vector slices
 constexpr int kChunkTarget = SPEC_CHUNK_TARGET;        // ids per row chunk before rounding
 constexpr int kDrawChunkTarget = SPEC_DRAW_CHUNK_TARGET;   // ids per draw chunk before rounding
 constexpr double kDrawWaves = SPEC_DRAW_WAVES;         // distance of the draw behind the rows
+#ifndef SPEC_DEFER_BYTES
+#define SPEC_DEFER_BYTES (64LL << 20)
+#endif
+constexpr long long kDeferBytes = SPEC_DEFER_BYTES;    // draw rows deferred to the end of a call
 constexpr int kMinBlocks = SPEC_MIN_BLOCKS;            // resident blocks per SM the registers allow
 constexpr int kMaxGroups = 65535;                      // grid z limit
 constexpr int kPlanWaitIters = 32;                     // optional bounded wait of a B unit (~15 us)
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kInternalDrawP = 0x100;
 // draw-chunk states (a chunk whose B unit saw the plan at once stays Free)
 constexpr int kChunkFree = 0, kChunkMine = 1, kChunkGivenUp = 2, kChunkDecider = 3;
 
@@ -110,9 +117,33 @@ struct Geo {
   int DCL;      // draw chunks per row
   int dchunk;   // ids per draw chunk (multiple of 8)
   int nslots;   // row slots per sequence: target rows 0..gmax, then draft rows 0..gmax-1
-  int delta;    // B units of sequence b sit in group b + delta
+  int delta;    // B units of sequence b sit in group b + delta (see draw_group_seq)
+  int ndefer;   // the first ndefer sequences of a launch draw after all of its row units
   int b0, b1;   // sequences [b0, b1) of this launch
 };
+
+// The sequence whose B units sit in group z of a launch of nb sequences (-1: none).  Groups
+// 0..nb-1 hold the row units of sequence z and, behind them by delta groups, the B units of the
+// sequences past the first ndefer.  After the last row unit come the B units of the first
+// ndefer sequences -- their plans are long out, and their draws keep HBM busy while the last
+// sequences are decided -- and then those of the last sequences.
+__host__ __device__ inline int draw_group_seq(int z, int nb, int delta, int ndefer) {
+  const int kd = ndefer < nb ? ndefer : nb;
+  if (z < nb) {
+    const int bl = z - delta;
+    return bl >= ndefer ? bl : -1;
+  }
+  if (z < nb + kd) return z - nb;
+  const int first = ndefer > nb - delta ? ndefer : nb - delta;
+  const int bl = first + (z - nb - kd);
+  return bl < nb ? bl : -1;
+}
+
+__host__ __device__ inline int draw_groups(int nb, int delta, int ndefer) {
+  const int kd = ndefer < nb ? ndefer : nb;
+  const int tail = nb > ndefer ? (nb - ndefer < delta ? nb - ndefer : delta) : 0;
+  return nb + kd + tail;
+}
 
 struct __align__(16) PlanRec {   // per sequence, published by the decider for the draw
   int m, g, flags, pair;
@@ -129,11 +160,10 @@ __host__ __device__ inline int ready_word(const PlanRec& pr) {
 struct Work {      // views into the caller's workspace
   int* cnt;        // [B] A arrivals               (counter header)
   int* bdone;      // [B] draw-chunk arrivals      (counter header)
-  int* ready;      // [B] plan published           (counter header)
+  uint64_t* planw; // [B][4] published plan words   (counter header)
   int* state;      // [B][DCL] draw-chunk states   (counter header)
-  PlanRec* plan;   // [B]
-  float2* part;    // [B][nslots][CL]
-  float* xd;       // [B][nslots] logit at the draft id of that row
+  uint64_t* part;  // [B][nslots][CL] published row partials (counter header: 0 when unwritten)
+  uint64_t* xd;    // [B][nslots] published logit at the draft id of that row (counter header)
   float2* mass;    // [B][DCL] (residual mass, p mass)
 };
 
@@ -152,6 +182,24 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
   uint4 v;
   asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
+}
+
+// 64-bit relaxed accesses at GPU scope: single-copy atomic, so a reader sees either the old
+// word or the whole new one.  A row unit publishes its partial this way, with no fence: the
+// word is nonzero by construction and the slot is zero until written, so the reader polls the
+// slot itself instead of relying on the order of the partial and the arrival count.
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ int atom_add_relaxed(int* p, int v) {
+  int old;
+  asm volatile("atom.relaxed.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 
 __device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
@@ -187,6 +235,13 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
     if (better(v2, i2, v, i)) { v = v2; i = i2; }
   }
 }
+
+// Published words.  A row partial is (M bits | S bits << 32) for sampling rows -- S >= 1 when M
+// is finite and M = -inf when S = 0, so the word is never 0 -- and (value bits | ~id << 32)
+// for greedy rows (~id != 0).  The logit at a draft id is (bits | 1 << 32).  NaN values are
+// stored as the canonical quiet NaN.
+__device__ __forceinline__ uint32_t canon_bits(float x) { return x != x ? 0x7fc00000u : __float_as_uint(x); }
+__device__ __forceinline__ uint64_t pack_word(uint32_t lo, uint32_t hi) { return uint64_t(lo) | (uint64_t(hi) << 32); }
 
 // p_v = 2^((x_v - M) k) / S, evaluated as ex2(x*k - M*k) * (1/S) with a rounded product.
 __device__ __forceinline__ float prob(float x, float k, float mk, float inv_s) {
@@ -448,11 +503,10 @@ struct Shared {
   float rowInvS[2 * SPEC_MAX_GAMMA + 1];
   int rowArg[SPEC_MAX_GAMMA + 1];
   float pd[SPEC_MAX_GAMMA], qd[SPEC_MAX_GAMMA];
-  float wsum[kMaxSlices][kWarps];                 // selector: per-(slice, warp) weight sums
-  int last, go, m, flags, owner, slice, warp_sel, token;
+  int last, go, m, flags, flags_extra, owner, token, lastpos;
   unsigned taken[2];
   int err;
-  float target_local, mass_out, run_sel;
+  float base, target, mass_out;
   PlanRec plan;
   uint64_t bars[kRing > 0 ? kRing : 1];
 };
@@ -549,163 +603,189 @@ __device__ __forceinline__ uint4 vec_at(const typename E::raw* row, int64_t e, i
 }
 
 // ------------------------------------------------------------------------------------------
-// the draw: draw-chunk masses, then the selector
+// the draw: per-warp masses of each draw chunk, then the selector
 // ------------------------------------------------------------------------------------------
+//
+// Draw chunk dc covers ids [dc*dchunk, (dc+1)*dchunk); warp w of the unit that reduces it owns
+// the contiguous sub-range [dc*dchunk + w*wlen, + wlen) with wlen = dchunk / kWarps, a whole
+// number of vectors.  Sub-range j = dc*kWarps + w is therefore the j-th slice of the row in
+// ascending id order, and its (residual, p) masses sit at mass[b][j].  In a warp step, vector
+// q of lane l covers the ids e0 + (q*32 + l)*N .. + N-1, so (step, q, lane, element) is
+// ascending id order too.
 
-// Inverse CDF over the draw chunks of b: the owner chunk holds the smallest id whose running
-// weight exceeds u * total; that chunk is rescanned in ascending id order.  Slice s of a draw
-// chunk covers ids lo + s*kThreads*N .. + kThreads*N - 1, thread t the N ids from
-// lo + (s*kThreads + t)*N, so (slice, warp, lane, element) is ascending id order.
+// Inverse CDF over the sub-range masses of b: warp 0 finds the owner sub-range (the one
+// holding the smallest id whose running weight exceeds u * total), then the block rescans it
+// in ascending id order, one 16-byte vector of p (and q) per thread per step.  Called by every
+// thread of the block.
 template <class E, bool kVec, bool kMixed>
 __device__ void select(const Args& a, const Geo& geo, const Work& w, const Seq<E, kMixed>& sq, const PlanRec pl,
                        Shared& sm) {
   using raw = typename E::raw;
   constexpr int N = E::kPerVec;
-  constexpr int kSlice = kThreads * N;
+  constexpr int kStep = kThreads * N;
   const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
-  const int b = sq.b, gmax = a.gmax, DCL = geo.DCL;
+  const int b = sq.b, gmax = a.gmax;
   const bool pair = pl.pair != 0;
   if (warp == 0) {
-    // chunk masses, lanes c and c + 32, prefix sums in ascending chunk order
-    const float2* ms = w.mass + int64_t(b) * DCL;
-    const float2 x0 = lane < DCL ? __ldcg(&ms[lane]) : make_float2(0.f, 0.f);
-    const float2 x1 = lane + 32 < DCL ? __ldcg(&ms[lane + 32]) : make_float2(0.f, 0.f);
-    const float r0 = warp_incl_scan(x0.x), p0 = warp_incl_scan(x0.y);
-    const float rt0 = __shfl_sync(kFull, r0, 31), pt0 = __shfl_sync(kFull, p0, 31);
-    const float r1 = __fadd_rn(rt0, warp_incl_scan(x1.x)), p1 = __fadd_rn(pt0, warp_incl_scan(x1.y));
-    const float R = __shfl_sync(kFull, r1, 31), Pm = __shfl_sync(kFull, p1, 31);
+    const int nsub = geo.DCL * kWarps;
+    const int per = (nsub + 31) / 32;   // consecutive sub-ranges per lane (at most kSubPerLane)
+    const float2* ms = w.mass + int64_t(b) * nsub;
+    float2 x[kSubPerLane];
+    float lr = 0.f, lp = 0.f;
+#pragma unroll
+    for (int i = 0; i < kSubPerLane; ++i) {
+      const int j = lane * per + i;
+      x[i] = (i < per && j < nsub) ? __ldcg(&ms[j]) : make_float2(0.f, 0.f);
+      lr = __fadd_rn(lr, x[i].x);
+      lp = __fadd_rn(lp, x[i].y);
+    }
+    const float ir = warp_incl_scan(lr), ip = warp_incl_scan(lp);
+    const float R = __shfl_sync(kFull, ir, 31), Pm = __shfl_sync(kFull, ip, 31);
     const bool use_w = !pair || R > 0.f;   // bonus: the weights are p itself
-    const float w0 = use_w ? x0.x : x0.y, w1 = use_w ? x1.x : x1.y;
-    const float i0 = use_w ? r0 : p0, i1 = use_w ? r1 : p1;
     const float total = use_w ? R : Pm;
     const float target = __fmul_rn(a.u_sample[b], total);
-    // exclusive prefix of each chunk: the inclusive prefix of the one before it
-    float e0 = __shfl_up_sync(kFull, i0, 1), e1 = __shfl_up_sync(kFull, i1, 1);
-    const float t0 = __shfl_sync(kFull, i0, 31);
-    if (lane == 0) { e0 = 0.f; e1 = t0; }
-    const unsigned hit0 = __ballot_sync(kFull, w0 > 0.f && i0 > target);
-    const unsigned hit1 = __ballot_sync(kFull, w1 > 0.f && i1 > target);
-    const unsigned pos0 = __ballot_sync(kFull, w0 > 0.f), pos1 = __ballot_sync(kFull, w1 > 0.f);
-    int owner;
-    if (hit0) owner = __ffs(hit0) - 1;
-    else if (hit1) owner = 32 + __ffs(hit1) - 1;
-    else if (pos1) owner = 32 + 31 - __clz(pos1);   // rounding left u*total past the end
-    else owner = pos0 ? 31 - __clz(pos0) : 0;
-    const float excl = __shfl_sync(kFull, owner < 32 ? e0 : e1, owner & 31);
-    if (lane == 0) {
-      int f = pl.flags;
-      if (!use_w) f |= SPEC_ST_R_ZERO | kInternalDrawP;
-      sm.owner = owner;
-      sm.flags = f;
-      sm.target_local = __fsub_rn(target, excl);
-      sm.mass_out = pair ? (use_w ? R : 0.f) : Pm;
-    }
-  }
-  __syncthreads();
-  const bool draw_p = !pair || (sm.flags & kInternalDrawP);
-  const int64_t lo = int64_t(sm.owner) * geo.dchunk;
-  const int64_t hi = lo + geo.dchunk < a.V ? lo + geo.dchunk : a.V;
-  const raw* rp = sq.P + int64_t(pl.m) * a.V;
-  const raw* rq = pair ? sq.Q + int64_t(pl.m) * a.V : rp;
-  const int slices = int((hi - lo + kSlice - 1) / kSlice);
-  for (int s = 0; s < slices; ++s) {
-    const int64_t e = lo + int64_t(s) * kSlice + int64_t(tid) * N;
-    float wv[N], pv[N];
-    weights<E>(vec_at<E, kVec>(rp, e, hi), vec_at<E, kVec>(rq, e, pair ? hi : 0), pair, sq.k, pl.mkp, pl.invp, pl.mkq,
-               pl.invq, wv, pv);
-    float x = 0.f;
+    const float incl = use_w ? ir : ip, mine = use_w ? lr : lp;
+    float excl = __shfl_up_sync(kFull, incl, 1);
+    if (lane == 0) excl = 0.f;
+    // owner lane: the first whose running total passes the target (else the last with weight)
+    const unsigned hit = __ballot_sync(kFull, mine > 0.f && incl > target);
+    const unsigned pos = __ballot_sync(kFull, mine > 0.f);
+    const int ol = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
+    if (lane == ol) {
+      float run = excl, base = excl, base_last = excl;
+      int found = -1, lastj = 0;
 #pragma unroll
-    for (int j = 0; j < N; ++j) x = __fadd_rn(x, draw_p ? pv[j] : wv[j]);
-    x = warp_sum(x);
-    if (lane == 0) sm.wsum[s][warp] = x;
-  }
-  __syncthreads();
-  const float tl = sm.target_local;
-  if (tid == 0) {
-    int ss = -1, sw = 0, ls = 0, lw = 0;
-    float run = 0.f, base = 0.f, base_last = 0.f;
-    for (int s = 0; s < slices && ss < 0; ++s)
-      for (int wi = 0; wi < kWarps; ++wi) {
-        const float x = sm.wsum[s][wi];
-        if (x > 0.f) { ls = s; lw = wi; base_last = run; }
-        const float nr = __fadd_rn(run, x);
-        if (nr > tl && x > 0.f) { ss = s; sw = wi; base = run; break; }
+      for (int i = 0; i < kSubPerLane; ++i) {
+        if (i >= per || found >= 0) continue;
+        const float wv = use_w ? x[i].x : x[i].y;
+        const float nr = __fadd_rn(run, wv);
+        if (wv > 0.f) {
+          lastj = i;
+          base_last = run;
+          if (nr > target) { found = i; base = run; }
+        }
         run = nr;
       }
-    if (ss < 0) { ss = ls; sw = lw; base = base_last; }
-    sm.slice = ss;
-    sm.warp_sel = sw;
-    sm.run_sel = base;
-    sm.token = int(lo);
-  }
-  __syncthreads();
-  if (warp == sm.warp_sel) {
-    const int64_t e = lo + int64_t(sm.slice) * kSlice + int64_t(tid) * N;
-    float wv[N], pv[N];
-    weights<E>(vec_at<E, kVec>(rp, e, hi), vec_at<E, kVec>(rq, e, pair ? hi : 0), pair, sq.k, pl.mkp, pl.invp, pl.mkq,
-               pl.invq, wv, pv);
-    float x = 0.f;
-#pragma unroll
-    for (int j = 0; j < N; ++j) x = __fadd_rn(x, draw_p ? pv[j] : wv[j]);
-    const float incl = warp_incl_scan(x);
-    const float base = sm.run_sel;
-    const unsigned hit = __ballot_sync(kFull, x > 0.f && __fadd_rn(base, incl) > tl);
-    const unsigned pos = __ballot_sync(kFull, x > 0.f);
-    const int sel = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
-    if (lane == sel) {
-      float r = __fsub_rn(__fadd_rn(base, incl), x);
-      int tok = -1, lastpos = -1;
-#pragma unroll
-      for (int j = 0; j < N; ++j) {
-        const float wj = draw_p ? pv[j] : wv[j];
-        r = __fadd_rn(r, wj);
-        if (wj > 0.f) {
-          lastpos = int(e) + j;
-          if (tok < 0 && r > tl) tok = int(e) + j;
-        }
-      }
-      sm.token = tok >= 0 ? tok : (lastpos >= 0 ? lastpos : int(lo));
+      if (found < 0) { found = lastj; base = base_last; }
+      int f = pl.flags;
+      if (!use_w) f |= SPEC_ST_R_ZERO;
+      sm.owner = lane * per + found;
+      sm.base = base;
+      sm.target = target;
+      sm.flags = f;
+      sm.mass_out = pair ? (use_w ? R : 0.f) : Pm;
+      sm.token = -1;
+      sm.lastpos = -1;
     }
   }
   __syncthreads();
-  const int m = pl.m, tok = sm.token;
+  const bool draw_p = (sm.flags & SPEC_ST_R_ZERO) != 0 || !pair;
+  const float target = sm.target;
+  const int oj = sm.owner;
+  const int wlen = geo.dchunk / kWarps;
+  const int64_t lo = int64_t(oj / kWarps) * geo.dchunk + int64_t(oj % kWarps) * wlen;
+  const int64_t hi = lo + wlen < a.V ? lo + wlen : a.V;
+  const raw* rp = sq.P + int64_t(pl.m) * a.V;
+  const raw* rq = pair ? sq.Q + int64_t(pl.m) * a.V : rp;
+  float run = sm.base;
+  for (int64_t e0 = lo; e0 < hi; e0 += kStep) {
+    const int64_t e = e0 + int64_t(tid) * N;
+    const uint4 vp = vec_at<E, kVec>(rp, e, hi), vq = vec_at<E, kVec>(rq, e, pair ? hi : 0);
+    float s = 0.f;
+    {
+      float wv[N], pv[N];
+      weights<E>(vp, vq, pair, sq.k, pl.mkp, pl.invp, pl.mkq, pl.invq, wv, pv);
+#pragma unroll
+      for (int j = 0; j < N; ++j) s = __fadd_rn(s, draw_p ? pv[j] : wv[j]);
+    }
+    const float inc = warp_incl_scan(s);
+    if (lane == 31) sm.wp[warp].x = inc;
+    __syncthreads();
+    float wex = run;   // running weight before this warp's first vector
+    for (int i = 0; i < warp; ++i) wex = __fadd_rn(wex, sm.wp[i].x);
+    float stot = run;
+    for (int i = 0; i < kWarps; ++i) stot = __fadd_rn(stot, sm.wp[i].x);
+    const float at = __fadd_rn(wex, inc);   // running weight through this vector
+    const unsigned h = __ballot_sync(kFull, s > 0.f && at > target);
+    const unsigned ps = __ballot_sync(kFull, s > 0.f);
+    __syncthreads();   // every warp has read sm.wp
+    if (lane == 0) sm.wp[warp] = make_float2(__int_as_float(int(h != 0)), __int_as_float(int(ps != 0)));
+    __syncthreads();
+    int hw = -1, pw = -1;
+    for (int i = 0; i < kWarps; ++i) {
+      if (hw < 0 && __float_as_int(sm.wp[i].x)) hw = i;
+      if (__float_as_int(sm.wp[i].y)) pw = i;
+    }
+    // the thread holding the target (the first hit), or the last with weight for the fallback
+    const int sel_w = hw >= 0 ? hw : pw;
+    if (sel_w == warp) {
+      const unsigned mask = hw >= 0 ? h : ps;
+      const int sl = hw >= 0 ? __ffs(mask) - 1 : 31 - __clz(mask);
+      if (lane == sl) {
+        // the same weights again, from the vectors kept in registers
+        float wv[N], pv[N];
+        weights<E>(vp, vq, pair, sq.k, pl.mkp, pl.invp, pl.mkq, pl.invq, wv, pv);
+        float r = __fsub_rn(at, s);
+        int t = -1, lp_ = -1;
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+          const float wj = draw_p ? pv[j] : wv[j];
+          r = __fadd_rn(r, wj);
+          if (wj > 0.f) {
+            lp_ = int(e) + j;
+            if (t < 0 && r > target) t = int(e) + j;
+          }
+        }
+        if (hw >= 0) sm.token = t >= 0 ? t : lp_;   // a hit vector holds the token up to rounding
+        else sm.lastpos = lp_;
+      }
+    }
+    run = stot;
+    __syncthreads();
+    if (sm.token >= 0) break;
+  }
+  const int m = pl.m;
+  const int tok = sm.token >= 0 ? sm.token : (sm.lastpos >= 0 ? sm.lastpos : int(lo));
   for (int i = tid; i <= gmax; i += kThreads) {
     int v = -1;
     if (i < m) v = a.draft_tokens[int64_t(b) * gmax + i];
     else if (i == m) v = tok;
     a.out_tokens[int64_t(b) * (gmax + 1) + i] = v;
   }
-  for (int c = tid; c < DCL; c += kThreads) w.state[int64_t(b) * DCL + c] = kChunkFree;
+  for (int c = tid; c < geo.DCL; c += kThreads) w.state[int64_t(b) * geo.DCL + c] = kChunkFree;
   if (tid == 0) {
     if (a.diag) a.diag[int64_t(b) * (2 * gmax + 1) + 2 * gmax] = sm.mass_out;
     a.num_accepted[b] = m;
     if (a.status) a.status[b] = sm.flags & 0xff;
-    w.ready[b] = 0;
+    uint64_t* pw = w.planw + int64_t(b) * 4;
+    for (int i = 0; i < 4; ++i) pw[i] = 0;
     w.bdone[b] = 0;
   }
   __syncthreads();
 }
 
-// one draw chunk: its residual and p masses; the last draw chunk of b to finish selects
+// one draw chunk: the (residual, p) masses of its kWarps sub-ranges; the last draw chunk of b
+// to finish selects
 template <class E, bool kVec, bool kMixed>
 __device__ void draw_chunk(const Args& a, const Geo& geo, const Work& w, const Seq<E, kMixed>& sq, const PlanRec pl,
                            int dc, Shared& sm) {
   using raw = typename E::raw;
   constexpr int N = E::kPerVec;
-  constexpr int kStep = kThreads * kDrawVec * N;
+  constexpr int kStep = 32 * kDrawVec * N;
   const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
   const int b = sq.b;
   const bool pair = pl.pair != 0;
   const raw* rp = sq.P + int64_t(pl.m) * a.V;
   const raw* rq = pair ? sq.Q + int64_t(pl.m) * a.V : rp;
-  const int64_t lo = int64_t(dc) * geo.dchunk;
-  const int64_t hi = lo + geo.dchunk < a.V ? lo + geo.dchunk : a.V;
+  const int wlen = geo.dchunk / kWarps;
+  const int64_t lo = int64_t(dc) * geo.dchunk + int64_t(warp) * wlen;
+  const int64_t hi = lo + wlen < a.V ? lo + wlen : a.V;
   float2 ws2 = make_float2(0.f, 0.f), ps2 = ws2;
   for (int64_t e0 = lo; e0 < hi; e0 += kStep) {
     uint4 vp[kDrawVec], vq[kDrawVec];
 #pragma unroll
     for (int q = 0; q < kDrawVec; ++q) {
-      const int64_t e = e0 + int64_t(q * kThreads + tid) * N;
+      const int64_t e = e0 + int64_t(q * 32 + lane) * N;
       vp[q] = vec_at<E, kVec>(rp, e, hi);
       vq[q] = vec_at<E, kVec>(rq, e, pair ? hi : 0);
     }
@@ -725,13 +805,11 @@ __device__ void draw_chunk(const Args& a, const Geo& geo, const Work& w, const S
   if (lane == 0) sm.wp[warp] = make_float2(ws, ps);
   __syncthreads();
   if (tid == 0) {
-    float2 acc = sm.wp[0];
-    for (int wi = 1; wi < kWarps; ++wi) {
-      acc.x = __fadd_rn(acc.x, sm.wp[wi].x);
-      acc.y = __fadd_rn(acc.y, sm.wp[wi].y);
-    }
-    if (!pair) acc.x = acc.y;
-    w.mass[int64_t(b) * geo.DCL + dc] = acc;
+    // the chunk's kWarps sub-range masses in four 16-byte stores, then the arrival (release)
+    float4* dst = reinterpret_cast<float4*>(w.mass + (int64_t(b) * geo.DCL + dc) * kWarps);
+#pragma unroll
+    for (int i = 0; i < kWarps / 2; ++i)
+      dst[i] = make_float4(sm.wp[2 * i].x, sm.wp[2 * i].y, sm.wp[2 * i + 1].x, sm.wp[2 * i + 1].y);
     sm.last = atom_add_acq_rel(&w.bdone[b], 1) == geo.DCL - 1;
   }
   __syncthreads();
@@ -742,32 +820,62 @@ __device__ void draw_chunk(const Args& a, const Geo& geo, const Work& w, const S
 // decider: combine the partials of sequence b, decide, then greedy result or the plan
 // ------------------------------------------------------------------------------------------
 
-// Entered by every thread of the block whose A unit arrived last, after the arrival atomic
-// (acquire) and a block barrier: all partials and draft logits of b are visible.
+// The published word at p, given a first read v of it: once it is there (it was stored before
+// its writer's arrival, which this block has seen), the slot returns to zero for the next
+// call.  Bounded: after kMbarWaitNs the sequence is flagged SPEC_ST_TIMEOUT and 0 is used.
+// First reads of several words are issued together, then settled one by one.
+__device__ __forceinline__ uint64_t settle_word(uint64_t* p, uint64_t v, Shared& sm) {
+  if (v == 0) {
+    const long long t0 = global_ns();
+    while ((v = ld_relaxed_u64(p)) == 0)
+      if (global_ns() - t0 > kMbarWaitNs) {
+        atomicOr(&sm.flags_extra, SPEC_ST_TIMEOUT);
+        break;
+      }
+  }
+  *p = 0;
+  return v;
+}
+
+// Entered by every thread of the block whose A unit arrived last (the arrival count reached
+// its total), after a block barrier.  The partials and draft logits are taken from their
+// published words.
 template <class E, bool kVec, bool kMixed>
 __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E, kMixed>& sq, Shared& sm) {
   const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
   const int b = sq.b, g = sq.g, gmax = a.gmax, CL = geo.CL;
   const float k = sq.k;
-  // the per-draft inputs first: they do not depend on the combine below
+  if (tid == 0) sm.flags_extra = 0;
+  __syncthreads();
+  // the per-draft inputs first: they do not depend on the combine below.  Every read is
+  // issued before any is waited on.
   int d = -1;
   float u = 0.f, xp = 0.f, xq = 0.f;
-  if (warp == 0 && lane < g) {
+  uint64_t* xdp = w.xd + int64_t(b) * geo.nslots + lane;
+  uint64_t* xdq = xdp + gmax + 1;
+  uint64_t vxp = 0, vxq = 0;
+  const bool drafts = warp == 0 && lane < g;
+  if (drafts) {
     d = __ldg(&a.draft_tokens[int64_t(b) * gmax + lane]);
     if (sq.sampling) {
       u = __ldg(&a.u_accept[int64_t(b) * gmax + lane]);
-      xp = __ldcg(&w.xd[int64_t(b) * geo.nslots + lane]);
-      xq = __ldcg(&w.xd[int64_t(b) * geo.nslots + gmax + 1 + lane]);
+      vxp = ld_relaxed_u64(xdp);
+      vxq = ld_relaxed_u64(xdq);
     }
   }
   // one warp per row: lanes take chunks c and c + 32 (at most 64 chunks)
-  const float2* part = w.part + int64_t(b) * geo.nslots * CL;
+  uint64_t* part = w.part + int64_t(b) * geo.nslots * CL;
   for (int slot = warp; slot < geo.nslots; slot += kWarps) {
     if (!sq.slot_valid(slot, gmax)) continue;
-    const float2* pp = part + slot * CL;
+    uint64_t* pp = part + slot * CL;
     const float2 none = make_float2(-INFINITY, sq.sampling ? 0.f : __int_as_float(INT_MAX));
-    const float2 p0 = lane < CL ? __ldcg(&pp[lane]) : none;
-    const float2 p1 = lane + 32 < CL ? __ldcg(&pp[lane + 32]) : none;
+    auto unpack = [&](uint64_t v) {
+      const uint32_t hi = uint32_t(v >> 32);
+      return make_float2(__uint_as_float(uint32_t(v)), sq.sampling ? __uint_as_float(hi) : __int_as_float(int(~hi)));
+    };
+    const uint64_t v0 = lane < CL ? ld_relaxed_u64(&pp[lane]) : 0, v1 = lane + 32 < CL ? ld_relaxed_u64(&pp[lane + 32]) : 0;
+    const float2 p0 = lane < CL ? unpack(settle_word(&pp[lane], v0, sm)) : none;
+    const float2 p1 = lane + 32 < CL ? unpack(settle_word(&pp[lane + 32], v1, sm)) : none;
     if (sq.sampling) {
       const float M = warp_max(fmaxf(p0.x, p1.x));
       float S = 0.f;
@@ -787,6 +895,11 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
       warp_argmax(bv, bi);
       if (lane == 0) sm.rowArg[slot] = bi;
     }
+  }
+  if (drafts && sq.sampling) {
+    // published for every draft row: the logit at d, or a marker when d is outside the row
+    xp = __uint_as_float(uint32_t(settle_word(xdp, vxp, sm)));
+    xq = __uint_as_float(uint32_t(settle_word(xdq, vxq, sm)));
   }
   if (tid < 2) sm.taken[tid] = 0u;
   __syncthreads();
@@ -814,7 +927,7 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
     const int m = rej ? __ffs(rej) - 1 : g;
     const unsigned bad = __ballot_sync(kFull, lane < g && !valid);
     if (lane == 0) {
-      int f = sq.flags;
+      int f = sq.flags | sm.flags_extra;
       if (m < g && ((bad >> m) & 1u)) f |= SPEC_ST_BAD_DRAFT;
       sm.m = m;
       sm.flags = f;
@@ -857,11 +970,14 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
     const int qs = gmax + 1 + m;
     pr.mkq = pr.pair ? __fmul_rn(sm.rowM[qs], k) : 0.f;
     pr.invq = pr.pair ? sm.rowInvS[qs] : 0.f;
-    w.plan[b] = pr;
     sm.plan = pr;
     w.cnt[b] = 0;
-    __threadfence();                 // the plan before the flag
-    atomicExch(&w.ready[b], ready_word(pr));
+    // four published words, no fence: a draw unit polls each (plan_words)
+    uint64_t* pw = w.planw + int64_t(b) * 4;
+    st_relaxed_u64(pw + 1, pack_word(__float_as_uint(pr.invp), 1u));
+    st_relaxed_u64(pw + 2, pack_word(__float_as_uint(pr.mkq), 1u));
+    st_relaxed_u64(pw + 3, pack_word(__float_as_uint(pr.invq), 1u));
+    st_relaxed_u64(pw, pack_word(uint32_t(ready_word(pr)), __float_as_uint(pr.mkp)));
     __threadfence();                 // the flag before the chunk states read below
   }
   __syncthreads();
@@ -923,11 +1039,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
     if (!sq.slot_valid(slot, a.gmax)) return;
     // the logit at this row's draft id, if it lies in this chunk: fetched once, up front
     const int i = slot <= a.gmax ? slot : slot - a.gmax - 1;
-    bool has_d = false;
+    bool has_d = false, no_d = false;
     float xv = 0.f;
     if (tid == 0 && sq.sampling && i < sq.g) {
       const int d = __ldg(&a.draft_tokens[int64_t(b) * a.gmax + i]);
       has_d = int64_t(d) >= lo && int64_t(d) < hi;
+      no_d = c == 0 && (d < 0 || int64_t(d) >= a.V);   // no chunk holds it: chunk 0 says so
       if (has_d) xv = E::at(row, d);
     }
     float rm = -INFINITY, rs = 0.f;
@@ -1013,10 +1130,14 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
         p.y = __int_as_float(pi);
       }
       if (lane == 0) {
-        if (has_d) w.xd[int64_t(b) * geo.nslots + slot] = xv;
-        w.part[(int64_t(b) * geo.nslots + slot) * geo.CL + c] = p;
-        // release: this thread's partial and draft logit before the count
-        sm.last = atom_add_acq_rel(&w.cnt[b], 1) == geo.CL * sq.nrows() - 1;
+        // published without a fence (see st_relaxed_u64); the arrival count only elects the
+        // decider, which polls the words themselves
+        if (has_d || no_d)
+          st_relaxed_u64(&w.xd[int64_t(b) * geo.nslots + slot], pack_word(canon_bits(has_d ? xv : NAN), has_d ? 1u : 2u));
+        st_relaxed_u64(&w.part[(int64_t(b) * geo.nslots + slot) * geo.CL + c],
+                       sq.sampling ? pack_word(canon_bits(p.x), __float_as_uint(p.y))
+                                   : pack_word(canon_bits(p.x), ~uint32_t(__float_as_int(p.y))));
+        sm.last = atom_add_relaxed(&w.cnt[b], 1) == geo.CL * sq.nrows() - 1;
       }
     }
     __syncthreads();
@@ -1025,46 +1146,63 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
   }
 
   if constexpr (kMixed) {
-    // ---------------- B unit: draw chunk dc of sequence grp - delta -------------------------
+    // ---------------- B unit: draw chunk dc of the sequence of this group --------------------
     const int dc = (y - geo.nslots) * geo.CL + x;
-    const int b = grp - geo.delta;
-    if (dc >= geo.DCL || b < geo.b0 || b >= geo.b1) return;
+    const int bl = draw_group_seq(int(blockIdx.z), geo.b1 - geo.b0, geo.delta, geo.ndefer);
+    if (dc >= geo.DCL || bl < 0) return;
+    const int b = geo.b0 + bl;
     const Seq<E, kMixed> sq(a, b);
-    // the plan flag is read while the sequence's metadata loads are still in flight
-    int rdy = 0;
-    if (tid == 0) rdy = ld_acquire(&w.ready[b]);
+    // the plan's first word is read while the sequence's metadata loads are still in flight
+    uint64_t* pw = w.planw + int64_t(b) * 4;
+    uint64_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
+    if (tid == 0) {
+      w0 = ld_relaxed_u64(pw);
+      w1 = ld_relaxed_u64(pw + 1);
+      w2 = ld_relaxed_u64(pw + 2);
+      w3 = ld_relaxed_u64(pw + 3);
+    }
     if (!sq.sampling) return;
     if (tid == 0) {
       int* st = &w.state[int64_t(b) * geo.DCL + dc];
       // optional, bounded wait for the plan; correctness does not depend on it
       int it = 0, ns = 64;
-      while (rdy == 0 && it < kPlanWaitIters) {
+      while (uint32_t(w0) == 0 && it < kPlanWaitIters) {
         __nanosleep(ns);
         if (ns < 512) ns <<= 1;
         ++it;
-        rdy = ld_acquire(&w.ready[b]);
+        w0 = ld_relaxed_u64(pw);
       }
       bool mine = false;
-      if (rdy != 0) {
+      if (uint32_t(w0) != 0) {
         // the plan is out: the decider takes only given-up chunks, so this one stays ours
         // without a claim
         mine = true;
       } else if (atom_cas(st, kChunkFree, kChunkGivenUp) == kChunkFree) {
         // given up; if the plan appeared meanwhile, take the chunk back unless the decider has
         __threadfence();
-        const int r2 = ld_acquire(&w.ready[b]);
-        if (r2 != 0) {
-          mine = atom_cas(st, kChunkGivenUp, kChunkMine) == kChunkGivenUp;
-          rdy = r2;
-        }
+        w0 = ld_relaxed_u64(pw);
+        if (uint32_t(w0) != 0) mine = atom_cas(st, kChunkGivenUp, kChunkMine) == kChunkGivenUp;
       }
       if (mine) {
+        // the other three words were stored before the first, in no guaranteed order: each
+        // is taken once it is there (bounded)
+        const long long t0 = global_ns();
+        while ((w1 == 0 || w2 == 0 || w3 == 0) && global_ns() - t0 < kMbarWaitNs) {
+          if (w1 == 0) w1 = ld_relaxed_u64(pw + 1);
+          if (w2 == 0) w2 = ld_relaxed_u64(pw + 2);
+          if (w3 == 0) w3 = ld_relaxed_u64(pw + 3);
+        }
+        const int rdy = int(uint32_t(w0));
         sm.plan.m = rdy & 0xffff;
         sm.plan.pair = (rdy >> 16) & 1;
         sm.plan.flags = (rdy >> 20) & 0xff;
         sm.plan.g = sq.g;
+        sm.plan.mkp = __uint_as_float(uint32_t(w0 >> 32));
+        sm.plan.invp = __uint_as_float(uint32_t(w1));
+        sm.plan.mkq = __uint_as_float(uint32_t(w2));
+        sm.plan.invq = __uint_as_float(uint32_t(w3));
         // never fails for a well-formed workspace; keeps every read in bounds
-        if (sm.plan.m > sq.g || (sm.plan.pair && sm.plan.m >= sq.g)) {
+        if (w1 == 0 || w2 == 0 || w3 == 0 || sm.plan.m > sq.g || (sm.plan.pair && sm.plan.m >= sq.g)) {
           mine = false;
           if (a.status) atomicOr(&a.status[b], SPEC_ST_TIMEOUT);
         }
@@ -1073,15 +1211,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
     }
     __syncthreads();
     if (!sm.go) return;
-    // the normalisers, ordered after thread 0's acquire by the barrier; through L2 (an
-    // earlier read of this line by the same SM may sit stale in L1).  Their load and the
-    // rows' loads are in flight together.
-    PlanRec pl = sm.plan;
-    const float4 nf = __ldcg(reinterpret_cast<const float4*>(&w.plan[b]) + 1);
-    pl.mkp = nf.x;
-    pl.invp = nf.y;
-    pl.mkq = nf.z;
-    pl.invq = nf.w;
+    const PlanRec pl = sm.plan;
     draw_chunk<E, kVec, kMixed>(a, geo, w, sq, pl, dc, sm);
   }
 }
@@ -1095,46 +1225,48 @@ struct Split {
   int dcl, dchunk;   // draw chunks
 };
 
-void cut(int64_t V, int target, int& n, int& len) {
+// n chunks of len ids (a multiple of `gran`) covering V, about `target` ids each, n <= nmax
+void cut(int64_t V, int target, int nmax, int gran, int& n, int& len) {
   int64_t c = (V + target - 1) / target;
   if (c < 1) c = 1;
-  if (c > kMaxChunks) c = kMaxChunks;
+  if (c > nmax) c = nmax;
   int64_t l = (V + c - 1) / c;
-  l = (l + 7) / 8 * 8;
-  n = int(c);
+  l = (l + gran - 1) / gran * gran;
+  n = int((V + l - 1) / l);
   len = int(l);
 }
 
 Split make_split(int64_t V) {
   Split s;
-  cut(V, kChunkTarget, s.cl, s.chunk);
-  cut(V, kDrawChunkTarget, s.dcl, s.dchunk);
+  cut(V, kChunkTarget, kMaxChunks, 8, s.cl, s.chunk);
+  // draw chunks split evenly into kWarps sub-ranges of whole 16-byte vectors
+  cut(V, kDrawChunkTarget, kMaxDrawChunks, kWarps * 8, s.dcl, s.dchunk);
   return s;
 }
 
 size_t align64(size_t x) { return (x + 63) & ~size_t(63); }
 
-// Workspace layout.  The counters live in a header, the first eighth of the workspace (a
-// function of workspace_bytes alone); the scratch lives after it.  Any call's scratch is
-// therefore disjoint from any call's counters, whatever sizes successive calls use, and the
-// counters (all zero between calls) stay valid.
+// Workspace layout.  The counters and the published words (all zero between calls) live in a
+// header, the first quarter of the workspace (a function of workspace_bytes alone); the
+// scratch lives after it.  Any call's scratch is therefore disjoint from any call's header,
+// whatever sizes successive calls use, and the header stays valid.
 struct WsLayout {
-  size_t cnt, bdone, ready, state, plan, part, xd, mass, header, scratch_end;
+  size_t cnt, bdone, planw, state, part, xd, mass, header, scratch_end;
 };
 
-size_t counter_bytes(int B, int64_t V) {
-  const Split s = make_split(V);
-  return 3 * align64(size_t(B) * 4) + align64(size_t(B) * s.dcl * 4);
-}
-
-size_t scratch_bytes(int B, int gmax, int64_t V) {
+size_t counter_bytes(int B, int gmax, int64_t V) {
   const Split s = make_split(V);
   const size_t nslots = size_t(2 * gmax + 1);
-  return align64(size_t(B) * sizeof(PlanRec)) + align64(size_t(B) * nslots * s.cl * 8) +
-         align64(size_t(B) * nslots * 4) + align64(size_t(B) * s.dcl * 8);
+  return 2 * align64(size_t(B) * 4) + align64(size_t(B) * 32) + align64(size_t(B) * s.dcl * 4) +
+         align64(size_t(B) * nslots * s.cl * 8) + align64(size_t(B) * nslots * 8);
 }
 
-size_t header_for(size_t ws_bytes) { return (ws_bytes / 8) & ~size_t(63); }
+size_t scratch_bytes(int B, int64_t V) {
+  const Split s = make_split(V);
+  return align64(size_t(B) * s.dcl * kWarps * 8);
+}
+
+size_t header_for(size_t ws_bytes) { return (ws_bytes / 4) & ~size_t(63); }
 
 WsLayout ws_layout(int B, int gmax, int64_t V, size_t ws_bytes) {
   const Split s = make_split(V);
@@ -1143,31 +1275,26 @@ WsLayout ws_layout(int B, int gmax, int64_t V, size_t ws_bytes) {
   L.header = header_for(ws_bytes);
   L.cnt = 0;
   L.bdone = L.cnt + align64(size_t(B) * 4);
-  L.ready = L.bdone + align64(size_t(B) * 4);
-  L.state = L.ready + align64(size_t(B) * 4);
+  L.planw = L.bdone + align64(size_t(B) * 4);
+  L.state = L.planw + align64(size_t(B) * 32);
+  L.part = L.state + align64(size_t(B) * s.dcl * 4);
+  L.xd = L.part + align64(size_t(B) * nslots * s.cl * 8);
   size_t off = L.header;
-  L.plan = off;
-  off += align64(size_t(B) * sizeof(PlanRec));
-  L.part = off;
-  off += align64(size_t(B) * nslots * s.cl * 8);
-  L.xd = off;
-  off += align64(size_t(B) * nslots * 4);
   L.mass = off;
-  off += align64(size_t(B) * s.dcl * 8);
+  off += align64(size_t(B) * s.dcl * kWarps * 8);
   L.scratch_end = off;
   return L;
 }
 
 bool ws_fits(int B, int gmax, int64_t V, size_t ws_bytes) {
-  return counter_bytes(B, V) <= header_for(ws_bytes) &&
-         header_for(ws_bytes) + scratch_bytes(B, gmax, V) <= ws_bytes;
+  return counter_bytes(B, gmax, V) <= header_for(ws_bytes) && header_for(ws_bytes) + scratch_bytes(B, V) <= ws_bytes;
 }
 
 // smallest workspace (a multiple of 64 bytes) that fits a call of these sizes
 size_t ws_required(int B, int gmax, int64_t V) {
-  const size_t c = counter_bytes(B, V), sc = scratch_bytes(B, gmax, V);
-  size_t w = align64(8 * (c + 64));
-  const size_t w2 = align64((sc + 64) * 8 / 7 + 64);
+  const size_t c = counter_bytes(B, gmax, V), sc = scratch_bytes(B, V);
+  size_t w = align64(4 * (c + 64));
+  const size_t w2 = align64((sc + 64) * 4 / 3 + 64);
   if (w2 > w) w = w2;
   while (!ws_fits(B, gmax, V, w)) w += 64;
   return w;
@@ -1178,11 +1305,10 @@ Work ws_views(void* ws, const WsLayout& L) {
   Work w;
   w.cnt = reinterpret_cast<int*>(p + L.cnt);
   w.bdone = reinterpret_cast<int*>(p + L.bdone);
-  w.ready = reinterpret_cast<int*>(p + L.ready);
+  w.planw = reinterpret_cast<uint64_t*>(p + L.planw);
   w.state = reinterpret_cast<int*>(p + L.state);
-  w.plan = reinterpret_cast<PlanRec*>(p + L.plan);
-  w.part = reinterpret_cast<float2*>(p + L.part);
-  w.xd = reinterpret_cast<float*>(p + L.xd);
+  w.part = reinterpret_cast<uint64_t*>(p + L.part);
+  w.xd = reinterpret_cast<uint64_t*>(p + L.xd);
   w.mass = reinterpret_cast<float2*>(p + L.mass);
   return w;
 }
@@ -1193,11 +1319,8 @@ template <class E, bool kVec, bool kMixed>
 int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream) {
   auto fn = verify_kernel<E, kVec, kMixed>;
   const Split sp = make_split(args.V);
-  const int64_t slice = int64_t(kThreads) * (dtype == SPEC_BF16 ? 8 : 4);
-  const int64_t slices = (sp.dchunk + slice - 1) / slice;
-  if (slices > kMaxSlices) {
-    set_error("V=%lld too large: %lld slices per draw chunk (max %d)", (long long)args.V, (long long)slices,
-              kMaxSlices);
+  if (args.V > (dtype == SPEC_BF16 ? (int64_t(1) << 21) : (int64_t(1) << 20))) {
+    set_error("V=%lld too large (at most 2^21 bf16 or 2^20 fp32 ids)", (long long)args.V);
     return SPEC_ENOSPACE;
   }
   // host-only checks first: nothing is enqueued when they fail
@@ -1245,15 +1368,21 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
   const int64_t resident = int64_t(sms) * per_sm;
   geo.delta = kMixed ? int(std::ceil(kDrawWaves * double(resident) / double(G))) : 0;
-  if (geo.delta > kMaxGroups / 2) geo.delta = kMaxGroups / 2;
+  if (geo.delta > kMaxGroups / 4) geo.delta = kMaxGroups / 4;
+  // sequences whose draws wait for the end: about as many as kDeferBytes of draw rows (the
+  // HBM the draw tail leaves idle), which miss L2 then but fill that idle time
+  const int64_t draw_row_bytes = 2 * args.V * (dtype == SPEC_BF16 ? 2 : 4);
+  geo.ndefer = kMixed ? int((kDeferBytes + draw_row_bytes - 1) / draw_row_bytes) : 0;
+  if (geo.ndefer > kMaxGroups / 4) geo.ndefer = kMaxGroups / 4;
   const Work w = ws_views(ws, L);
   // one launch covers at most kMaxGroups groups (the grid's z limit); larger batches take
   // several launches over consecutive sequence ranges, each complete on its own
-  const int per_launch = kMaxGroups - geo.delta;
+  const int per_launch = kMaxGroups - geo.delta - geo.ndefer;
   for (int b0 = 0; b0 < args.B; b0 += per_launch) {
     geo.b0 = b0;
     geo.b1 = b0 + per_launch < args.B ? b0 + per_launch : args.B;
-    const dim3 grid(unsigned(geo.CL), unsigned(geo.nslots + brows), unsigned(geo.b1 - b0 + geo.delta));
+    const int groups = kMixed ? draw_groups(geo.b1 - b0, geo.delta, geo.ndefer) : geo.b1 - b0;
+    const dim3 grid(unsigned(geo.CL), unsigned(geo.nslots + brows), unsigned(groups));
     fn<<<grid, kThreads, dyn_smem, static_cast<cudaStream_t>(stream)>>>(args, geo, w);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "verify kernel launch");
@@ -1378,7 +1507,7 @@ namespace {
 constexpr size_t kStaticWsBytes = SPEC_STATIC_WORKSPACE_BYTES;
 static_assert(kStaticWsBytes % 64 == 0, "static workspace size");
 
-// The shared workspace: its first eighth holds the counters, which must be zero before the
+// The shared workspace: its first quarter holds the counters, which must be zero before the
 // first call and which every completed call leaves at zero; the scratch after it keeps the
 // last call's values.
 static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
