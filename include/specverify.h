@@ -15,12 +15,10 @@
  *    default stream) and returns.  Results are valid once the stream reaches that point.
  *  - The verify calls take a caller-owned device WORKSPACE of at least
  *    spec_verify_workspace_bytes(B, gmax, V, dtype) bytes, 64-byte aligned, which must be
- *    zero-filled before its first use.  Its first quarter holds counters and hand-over slots
- *    that every completed call returns to zero; the rest holds scratch values that each call
- *    writes before reading.
- *    So one workspace serves any number of successive calls of any sizes it fits, provided
- *    every call passes the same workspace_bytes for it.  Calls that may run at the same time
- *    (different streams) need different workspaces.
+ *    zero-filled before its first use.  It holds counters and hand-over words only, and every
+ *    completed call returns all of it to zero, so one workspace serves any number of
+ *    successive calls of any sizes it fits.  Calls that may run at the same time (different
+ *    streams) need different workspaces.
  *  - Arrays are row-major and contiguous:
  *        target_logits [B][gmax+1][V]   row i judges draft i; row 0 is the target's saved
  *                                       prediction for the position after the committed
@@ -133,14 +131,14 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits, int 
  *
  * The workspace is an array of SPEC_STATIC_WORKSPACE_BYTES bytes compiled into the library,
  * one per device, shared by every call of this function on that device:
- *   - Calls whose sizes need more (about spec_verify_workspace_bytes(B, gmax, V, dtype)
- *     above SPEC_STATIC_WORKSPACE_BYTES, which rounds up: the exact limits are B = 744 at
- *     gmax = 4, V = 128256 and B = 720 at gmax = 4, V = 151936) return SPEC_ENOSPACE
- *     before touching the device.
+ *   - Calls whose sizes need more (spec_verify_workspace_bytes(B, gmax, V, dtype) above
+ *     SPEC_STATIC_WORKSPACE_BYTES: B = 1310 at gmax = 4, V = 128256 and B = 1040 at
+ *     gmax = 4, V = 151936 are the largest that fit) return SPEC_ENOSPACE before touching
+ *     the device.
  *   - The first call on a device looks the array up (cudaGetSymbolAddress), clears it and
  *     waits for the clear, so its counters start at zero; make that call outside any stream
  *     capture.  Later calls only launch the kernel.
- *   - The array keeps the last call's scratch values; its counters are zero between calls.
+ *   - Like any workspace, the array is all zero between calls.
  *   - Calls that may overlap (different streams, or threads without ordering) race on the one
  *     array: serialise them, e.g. on one stream.
  * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.

@@ -88,7 +88,7 @@ constexpr double kDrawWaves = SPEC_DRAW_WAVES;         // distance of the draw b
 constexpr long long kDeferBytes = SPEC_DEFER_BYTES;    // draw rows deferred to the end of a call
 constexpr int kMinBlocks = SPEC_MIN_BLOCKS;            // resident blocks per SM the registers allow
 constexpr int kMaxGroups = 65535;                      // grid z limit
-constexpr int kPlanWaitIters = 32;                     // optional bounded wait of a B unit (~15 us)
+constexpr int kPlanWaitIters = 64;                     // optional bounded wait of a B unit (~31 us)
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 // draw-chunk states (a chunk whose B unit saw the plan at once stays Free)
@@ -123,26 +123,28 @@ struct Geo {
 };
 
 // The sequence whose B units sit in group z of a launch of nb sequences (-1: none).  Groups
-// 0..nb-1 hold the row units of sequence z and, behind them by delta groups, the B units of the
-// sequences past the first ndefer.  After the last row unit come the B units of the first
-// ndefer sequences -- their plans are long out, and their draws keep HBM busy while the last
-// sequences are decided -- and then those of the last sequences.
+// 0..nb-1 hold the row units of sequence z and, delta groups behind them, the B units of the
+// sequences from ndefer on: their rows are still in L2 when they draw.  After the last row unit
+// come the B units of the last delta sequences, which cannot sit delta groups behind (their
+// plans come out as these units start), then those of the first ndefer sequences, whose plans
+// are long out: their draws keep HBM busy while the last sequences are decided.
 __host__ __device__ inline int draw_group_seq(int z, int nb, int delta, int ndefer) {
-  const int kd = ndefer < nb ? ndefer : nb;
+  const int nl = delta < nb ? delta : nb;   // the last sequences
   if (z < nb) {
     const int bl = z - delta;
     return bl >= ndefer ? bl : -1;
   }
-  if (z < nb + kd) return z - nb;
-  const int first = ndefer > nb - delta ? ndefer : nb - delta;
-  const int bl = first + (z - nb - kd);
-  return bl < nb ? bl : -1;
+  const int j = z - nb;
+  if (j < nl) return nb - nl + j;
+  const int bl = j - nl;
+  const int nd = ndefer < nb - nl ? ndefer : nb - nl;
+  return bl < nd ? bl : -1;
 }
 
 __host__ __device__ inline int draw_groups(int nb, int delta, int ndefer) {
-  const int kd = ndefer < nb ? ndefer : nb;
-  const int tail = nb > ndefer ? (nb - ndefer < delta ? nb - ndefer : delta) : 0;
-  return nb + kd + tail;
+  const int nl = delta < nb ? delta : nb;
+  const int nd = ndefer < nb - nl ? ndefer : nb - nl;
+  return nb + nl + nd;
 }
 
 struct __align__(16) PlanRec {   // per sequence, published by the decider for the draw
@@ -157,14 +159,14 @@ __host__ __device__ inline int ready_word(const PlanRec& pr) {
   return int(0x80000000u | (unsigned(pr.flags & 0xff) << 20) | (unsigned(pr.pair & 1) << 16) | unsigned(pr.m & 0xffff));
 }
 
-struct Work {      // views into the caller's workspace
-  int* cnt;        // [B] A arrivals               (counter header)
-  int* bdone;      // [B] draw-chunk arrivals      (counter header)
-  uint64_t* planw; // [B][4] published plan words   (counter header)
-  int* state;      // [B][DCL] draw-chunk states   (counter header)
-  uint64_t* part;  // [B][nslots][CL] published row partials (counter header: 0 when unwritten)
-  uint64_t* xd;    // [B][nslots] published logit at the draft id of that row (counter header)
-  float2* mass;    // [B][DCL] (residual mass, p mass)
+struct Work {      // views into the caller's workspace: every word is 0 between calls
+  int* cnt;        // [B] A arrivals
+  int* bdone;      // [B] draw-chunk arrivals
+  uint64_t* planw; // [B][4] published plan words
+  int* state;      // [B][DCL] draw-chunk states
+  uint64_t* part;  // [B][nslots][CL] published row partials (0 while unwritten)
+  uint64_t* xd;    // [B][nslots] published logit at the draft id of that row
+  uint64_t* mass;  // [B][DCL][kWarps] published sub-range masses (residual, -p)
 };
 
 // ------------------------------------------------------------------------------------------
@@ -602,6 +604,23 @@ __device__ __forceinline__ uint4 vec_at(const typename E::raw* row, int64_t e, i
   }
 }
 
+// The published word at p, given a first read v of it: once it is there (it was stored before
+// its writer's arrival, which this block has seen), the slot returns to zero for the next
+// call.  Bounded: after kMbarWaitNs the sequence is flagged SPEC_ST_TIMEOUT and 0 is used.
+// First reads of several words are issued together, then settled one by one.
+__device__ __forceinline__ uint64_t settle_word(uint64_t* p, uint64_t v, Shared& sm) {
+  if (v == 0) {
+    const long long t0 = global_ns();
+    while ((v = ld_relaxed_u64(p)) == 0)
+      if (global_ns() - t0 > kMbarWaitNs) {
+        atomicOr(&sm.flags_extra, SPEC_ST_TIMEOUT);
+        break;
+      }
+  }
+  *p = 0;
+  return v;
+}
+
 // ------------------------------------------------------------------------------------------
 // the draw: per-warp masses of each draw chunk, then the selector
 // ------------------------------------------------------------------------------------------
@@ -626,16 +645,28 @@ __device__ void select(const Args& a, const Geo& geo, const Work& w, const Seq<E
   const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
   const int b = sq.b, gmax = a.gmax;
   const bool pair = pl.pair != 0;
+  if (tid == 0) sm.flags_extra = 0;
+  __syncthreads();
   if (warp == 0) {
     const int nsub = geo.DCL * kWarps;
     const int per = (nsub + 31) / 32;   // consecutive sub-ranges per lane (at most kSubPerLane)
-    const float2* ms = w.mass + int64_t(b) * nsub;
+    uint64_t* ms = w.mass + int64_t(b) * nsub;
+    uint64_t raw_w[kSubPerLane];
+#pragma unroll
+    for (int i = 0; i < kSubPerLane; ++i) {
+      const int j = lane * per + i;
+      raw_w[i] = (i < per && j < nsub) ? ld_relaxed_u64(&ms[j]) : 0;
+    }
     float2 x[kSubPerLane];
     float lr = 0.f, lp = 0.f;
 #pragma unroll
     for (int i = 0; i < kSubPerLane; ++i) {
       const int j = lane * per + i;
-      x[i] = (i < per && j < nsub) ? __ldcg(&ms[j]) : make_float2(0.f, 0.f);
+      x[i] = make_float2(0.f, 0.f);
+      if (i < per && j < nsub) {
+        const uint64_t v = settle_word(&ms[j], raw_w[i], sm);
+        x[i] = make_float2(__uint_as_float(uint32_t(v)), -__uint_as_float(uint32_t(v >> 32)));
+      }
       lr = __fadd_rn(lr, x[i].x);
       lp = __fadd_rn(lp, x[i].y);
     }
@@ -667,7 +698,7 @@ __device__ void select(const Args& a, const Geo& geo, const Work& w, const Seq<E
         run = nr;
       }
       if (found < 0) { found = lastj; base = base_last; }
-      int f = pl.flags;
+      int f = pl.flags | sm.flags_extra;
       if (!use_w) f |= SPEC_ST_R_ZERO;
       sm.owner = lane * per + found;
       sm.base = base;
@@ -802,16 +833,12 @@ __device__ void draw_chunk(const Args& a, const Geo& geo, const Work& w, const S
   }
   const float ws = warp_sum(__fadd_rn(ws2.x, ws2.y));
   const float ps = warp_sum(__fadd_rn(ps2.x, ps2.y));
-  if (lane == 0) sm.wp[warp] = make_float2(ws, ps);
+  // each warp publishes its sub-range's word, (residual, -p): the sign bit of -p (p >= 0)
+  // makes it nonzero; the selector polls the words, so the arrival needs no fence
+  if (lane == 0)
+    st_relaxed_u64(&w.mass[(int64_t(b) * geo.DCL + dc) * kWarps + warp], pack_word(__float_as_uint(ws), __float_as_uint(-ps)));
   __syncthreads();
-  if (tid == 0) {
-    // the chunk's kWarps sub-range masses in four 16-byte stores, then the arrival (release)
-    float4* dst = reinterpret_cast<float4*>(w.mass + (int64_t(b) * geo.DCL + dc) * kWarps);
-#pragma unroll
-    for (int i = 0; i < kWarps / 2; ++i)
-      dst[i] = make_float4(sm.wp[2 * i].x, sm.wp[2 * i].y, sm.wp[2 * i + 1].x, sm.wp[2 * i + 1].y);
-    sm.last = atom_add_acq_rel(&w.bdone[b], 1) == geo.DCL - 1;
-  }
+  if (tid == 0) sm.last = atom_add_relaxed(&w.bdone[b], 1) == geo.DCL - 1;
   __syncthreads();
   if (sm.last) select<E, kVec, kMixed>(a, geo, w, sq, pl, sm);
 }
@@ -820,22 +847,6 @@ __device__ void draw_chunk(const Args& a, const Geo& geo, const Work& w, const S
 // decider: combine the partials of sequence b, decide, then greedy result or the plan
 // ------------------------------------------------------------------------------------------
 
-// The published word at p, given a first read v of it: once it is there (it was stored before
-// its writer's arrival, which this block has seen), the slot returns to zero for the next
-// call.  Bounded: after kMbarWaitNs the sequence is flagged SPEC_ST_TIMEOUT and 0 is used.
-// First reads of several words are issued together, then settled one by one.
-__device__ __forceinline__ uint64_t settle_word(uint64_t* p, uint64_t v, Shared& sm) {
-  if (v == 0) {
-    const long long t0 = global_ns();
-    while ((v = ld_relaxed_u64(p)) == 0)
-      if (global_ns() - t0 > kMbarWaitNs) {
-        atomicOr(&sm.flags_extra, SPEC_ST_TIMEOUT);
-        break;
-      }
-  }
-  *p = 0;
-  return v;
-}
 
 // Entered by every thread of the block whose A unit arrived last (the arrival count reached
 // its total), after a block barrier.  The partials and draft logits are taken from their
@@ -1246,58 +1257,33 @@ Split make_split(int64_t V) {
 
 size_t align64(size_t x) { return (x + 63) & ~size_t(63); }
 
-// Workspace layout.  The counters and the published words (all zero between calls) live in a
-// header, the first quarter of the workspace (a function of workspace_bytes alone); the
-// scratch lives after it.  Any call's scratch is therefore disjoint from any call's header,
-// whatever sizes successive calls use, and the header stays valid.
+// Workspace layout: counters and published words only, all zero between calls (each call
+// returns every word it used to zero), so calls of any sizes can share one workspace.
 struct WsLayout {
-  size_t cnt, bdone, planw, state, part, xd, mass, header, scratch_end;
+  size_t cnt, bdone, planw, state, part, xd, mass, end;
 };
 
-size_t counter_bytes(int B, int gmax, int64_t V) {
-  const Split s = make_split(V);
-  const size_t nslots = size_t(2 * gmax + 1);
-  return 2 * align64(size_t(B) * 4) + align64(size_t(B) * 32) + align64(size_t(B) * s.dcl * 4) +
-         align64(size_t(B) * nslots * s.cl * 8) + align64(size_t(B) * nslots * 8);
-}
-
-size_t scratch_bytes(int B, int64_t V) {
-  const Split s = make_split(V);
-  return align64(size_t(B) * s.dcl * kWarps * 8);
-}
-
-size_t header_for(size_t ws_bytes) { return (ws_bytes / 4) & ~size_t(63); }
-
-WsLayout ws_layout(int B, int gmax, int64_t V, size_t ws_bytes) {
+WsLayout ws_layout(int B, int gmax, int64_t V) {
   const Split s = make_split(V);
   const size_t nslots = size_t(2 * gmax + 1);
   WsLayout L;
-  L.header = header_for(ws_bytes);
   L.cnt = 0;
   L.bdone = L.cnt + align64(size_t(B) * 4);
   L.planw = L.bdone + align64(size_t(B) * 4);
   L.state = L.planw + align64(size_t(B) * 32);
   L.part = L.state + align64(size_t(B) * s.dcl * 4);
   L.xd = L.part + align64(size_t(B) * nslots * s.cl * 8);
-  size_t off = L.header;
-  L.mass = off;
-  off += align64(size_t(B) * s.dcl * kWarps * 8);
-  L.scratch_end = off;
+  L.mass = L.xd + align64(size_t(B) * nslots * 8);
+  L.end = L.mass + align64(size_t(B) * s.dcl * kWarps * 8);
   return L;
 }
 
-bool ws_fits(int B, int gmax, int64_t V, size_t ws_bytes) {
-  return counter_bytes(B, gmax, V) <= header_for(ws_bytes) && header_for(ws_bytes) + scratch_bytes(B, V) <= ws_bytes;
-}
+bool ws_fits(int B, int gmax, int64_t V, size_t ws_bytes) { return ws_layout(B, gmax, V).end <= ws_bytes; }
 
-// smallest workspace (a multiple of 64 bytes) that fits a call of these sizes
+// smallest workspace that fits a call of these sizes (a multiple of 64 bytes)
 size_t ws_required(int B, int gmax, int64_t V) {
-  const size_t c = counter_bytes(B, gmax, V), sc = scratch_bytes(B, V);
-  size_t w = align64(4 * (c + 64));
-  const size_t w2 = align64((sc + 64) * 4 / 3 + 64);
-  if (w2 > w) w = w2;
-  while (!ws_fits(B, gmax, V, w)) w += 64;
-  return w;
+  const size_t n = ws_layout(B, gmax, V).end;
+  return n > 64 ? n : 64;
 }
 
 Work ws_views(void* ws, const WsLayout& L) {
@@ -1309,7 +1295,7 @@ Work ws_views(void* ws, const WsLayout& L) {
   w.state = reinterpret_cast<int*>(p + L.state);
   w.part = reinterpret_cast<uint64_t*>(p + L.part);
   w.xd = reinterpret_cast<uint64_t*>(p + L.xd);
-  w.mass = reinterpret_cast<float2*>(p + L.mass);
+  w.mass = reinterpret_cast<uint64_t*>(p + L.mass);
   return w;
 }
 
@@ -1333,7 +1319,7 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
     set_error("workspace must be 64-byte aligned");
     return SPEC_EINVAL;
   }
-  const WsLayout L = ws_layout(args.B, args.gmax, args.V, ws_bytes);
+  const WsLayout L = ws_layout(args.B, args.gmax, args.V);
   Geo geo;
   geo.CL = sp.cl;
   geo.chunk = sp.chunk;
@@ -1507,9 +1493,8 @@ namespace {
 constexpr size_t kStaticWsBytes = SPEC_STATIC_WORKSPACE_BYTES;
 static_assert(kStaticWsBytes % 64 == 0, "static workspace size");
 
-// The shared workspace: its first quarter holds the counters, which must be zero before the
-// first call and which every completed call leaves at zero; the scratch after it keeps the
-// last call's values.
+// The shared workspace: all zero before the first call (the first call on a device clears it)
+// and after every completed call.
 static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
 
 std::mutex g_static_mu;

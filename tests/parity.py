@@ -50,9 +50,8 @@ def workspace(B, g, V, code):
 
 
 def workspace_is_clean() -> bool:
-    """The header (the first quarter of a workspace: counters and published words) is zero
-    again after a call."""
-    return all(bool((w[: (w.numel() // 4) // 64 * 64] == 0).all()) for w in _WS.values())
+    """The whole workspace (counters and hand-over words) is zero again after a call."""
+    return all(bool((w == 0).all()) for w in _WS.values())
 
 
 def run_gpu(wl, mode: str = "auto", target=None, draft=None, check_canary=True):

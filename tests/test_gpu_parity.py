@@ -283,7 +283,7 @@ def test_workspace_reuse_across_sizes():
                               dev(wl.temperature), dev(wl.u_accept), dev(wl.u_sample), out, macc, dg, st,
                               workspace=ws)
         torch.cuda.synchronize()
-        assert bool((ws[: (n // 4) // 64 * 64] == 0).all())
+        assert bool((ws == 0).all())
         gpu = {"out": out.cpu().numpy(), "m": macc.cpu().numpy(), "status": st.cpu().numpy(),
                "diag": dg.cpu().numpy()}
         res = parity.oracle_results(wl)
