@@ -284,8 +284,12 @@ def run_native(args):
     dkv = kv0.clone()
     stream = torch.cuda.current_stream(device)
     ws = sv.alloc_workspace(B, g, V, sv.SPEC_BF16 if wl.dtype == "bf16" else sv.SPEC_F32, device)
-    verify = [sv.prepare_verify_sample(tgt[c], drf[c], toks, nd, temp, ua, us, out, macc, dg, st,
-                                       workspace=ws, stream=stream) for c in range(ncopies)]
+    if wl.greedy_only:
+        verify = [sv.prepare_verify_greedy(tgt[c], toks, nd, out, macc, st, workspace=ws, stream=stream)
+                  for c in range(ncopies)]
+    else:
+        verify = [sv.prepare_verify_sample(tgt[c], drf[c], toks, nd, temp, ua, us, out, macc, dg, st,
+                                           workspace=ws, stream=stream) for c in range(ncopies)]
     commit = sv.prepare_commit_kv_lengths(macc, kv, dkv, True, stream=stream, gmax=g)
 
     for i in range(args.warmup):
@@ -336,26 +340,38 @@ def run_native(args):
     achieved = abytes / (kern_mean_ms / 1e3) / 1e9
 
     # ---- the post-verify kernels alone (stops, commit), per launch, on the same stream ----
+    # Each batch of launches is queued behind a verify call, so the GPU runs them back to back
+    # and the events around each one measure device time, not the host's launch gaps.
     budgets = torch.full((B,), 3, dtype=torch.int32, device=device)
-    def per_launch_us(fn, n=200):
+    stops = sv.prepare_apply_stops(out, macc, 0, budgets, st, stream=stream)
+
+    def per_launch_us(fn, batches=25, per=8):
         for _ in range(10):
             fn()
-        e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-        for a, b_ in e:
-            a.record(stream)
-            fn()
-            b_.record(stream)
-        torch.cuda.synchronize(device)
-        return statistics.median(a.elapsed_time(b_) for a, b_ in e) * 1e3
-    post = {"spec_apply_stops_us": per_launch_us(lambda: sv.spec_apply_stops(out, macc, 0, budgets, st)),
-            "spec_commit_kv_lengths_us": per_launch_us(commit), "statistic": "median of 200 launches"}
+        times = []
+        for _ in range(batches):
+            e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(per)]
+            verify[0]()
+            for a, b_ in e:
+                a.record(stream)
+                fn()
+                b_.record(stream)
+            torch.cuda.synchronize(device)
+            times += [a.elapsed_time(b_) for a, b_ in e]
+        return statistics.median(times) * 1e3
+    post = {"spec_apply_stops_us": per_launch_us(stops), "spec_commit_kv_lengths_us": per_launch_us(commit),
+            "statistic": "median of 200 launches queued behind a verify call"}
 
     # ---- end to end through the public binding, host buffers, copies inside the region ----
     pin = lambda a: (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16
                      else torch.from_numpy(np.ascontiguousarray(a))).pin_memory()
-    h_in = [pin(wl.target), pin(wl.draft), pin(wl.draft_tokens), pin(wl.num_draft),
-            pin(wl.temperature), pin(wl.u_accept), pin(wl.u_sample), pin(wl.kv_len)]
-    d_in = [tgt[0], drf[0], toks, nd, temp, ua, us, kv]
+    if wl.greedy_only:
+        h_in = [pin(wl.target), pin(wl.draft_tokens), pin(wl.num_draft), pin(wl.kv_len)]
+        d_in = [tgt[0], toks, nd, kv]
+    else:
+        h_in = [pin(wl.target), pin(wl.draft), pin(wl.draft_tokens), pin(wl.num_draft),
+                pin(wl.temperature), pin(wl.u_accept), pin(wl.u_sample), pin(wl.kv_len)]
+        d_in = [tgt[0], drf[0], toks, nd, temp, ua, us, kv]
     h_out = [torch.empty_like(out, device="cpu").pin_memory(), torch.empty_like(macc, device="cpu").pin_memory(),
              torch.empty_like(kv, device="cpu").pin_memory()]
     h2d = sum(t.numel() * t.element_size() for t in h_in)
@@ -364,8 +380,11 @@ def run_native(args):
     def e2e_step():
         for h, d in zip(h_in, d_in):
             d.copy_(h, non_blocking=True)
-        sv.spec_verify_sample(d_in[0], d_in[1], d_in[2], d_in[3], d_in[4], d_in[5], d_in[6],
-                              out, macc, dg, st, workspace=ws)
+        if wl.greedy_only:
+            sv.spec_verify_greedy(d_in[0], d_in[1], d_in[2], out, macc, st, workspace=ws)
+        else:
+            sv.spec_verify_sample(d_in[0], d_in[1], d_in[2], d_in[3], d_in[4], d_in[5], d_in[6],
+                                  out, macc, dg, st, workspace=ws)
         sv.spec_commit_kv_lengths(macc, kv, None, True, gmax=g)
         h_out[0].copy_(out, non_blocking=True)
         h_out[1].copy_(macc, non_blocking=True)
@@ -405,7 +424,8 @@ def run_native(args):
             "sequences_per_s": world * B * K / (elapsed_ms / 1e3), "mean_emitted_per_sequence": mean_emit,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "verify_kernel<bf16, vec, mixed> (spec_verify_sample)",
+                         "kernel": ("verify_kernel<bf16, vec, greedy> (spec_verify_greedy)" if wl.greedy_only
+                                    else "verify_kernel<bf16, vec, mixed> (spec_verify_sample)"),
                          "kernel_ms_mean": kern_mean_ms, "kernel_ms_median": kern_med_ms,
                          "kernel_ms_p10": kern_p10, "kernel_ms_p90": kern_p90,
                          "algorithmic_bytes_per_launch": abytes, "peak_source": peak_src},

@@ -286,6 +286,32 @@ def prepare_verify_sample(target_logits, draft_logits, draft_tokens, num_draft, 
     return _Prepared(lib.spec_verify_sample, args, keep)
 
 
+def prepare_verify_greedy(target_logits, draft_tokens, num_draft, out_tokens, num_accepted,
+                          status=None, workspace=None, stream=None) -> _Prepared:
+    B, gp1, V = target_logits.shape
+    gmax = gp1 - 1
+    lib = load_library()
+    ws, wsp, wsn = _ws(workspace, B, gmax, V, _dtype_code(target_logits), target_logits.device)
+    args = (_ptr(target_logits, "target_logits"), _dtype_code(target_logits),
+            _ptr(draft_tokens, "draft_tokens", torch.int32, (B, gmax)),
+            _ptr(num_draft, "num_draft", torch.int32, (B,)), B, gmax, V,
+            _ptr(out_tokens, "out_tokens", torch.int32, (B, gmax + 1)),
+            _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
+            _ptr(status, "status", torch.int32, (B,)), wsp, wsn, _stream(stream))
+    keep = (target_logits, draft_tokens, num_draft, out_tokens, num_accepted, status, ws)
+    return _Prepared(lib.spec_verify_greedy, args, keep)
+
+
+def prepare_apply_stops(out_tokens, num_accepted, eos_id, max_new=None, status=None, stream=None) -> _Prepared:
+    B, gp1 = out_tokens.shape
+    lib = load_library()
+    args = (_ptr(out_tokens, "out_tokens", torch.int32, (B, gp1)),
+            _ptr(num_accepted, "num_accepted", torch.int32, (B,)), B, gp1 - 1, int(eos_id),
+            _ptr(max_new, "max_new", torch.int32, (B,)), _ptr(status, "status", torch.int32, (B,)),
+            _stream(stream))
+    return _Prepared(lib.spec_apply_stops, args, (out_tokens, num_accepted, max_new, status))
+
+
 def prepare_commit_kv_lengths(num_accepted, target_kv_len, draft_kv_len, correction_processed,
                               out_tokens=None, history=None, committed_len=None, status=None,
                               stream=None, gmax=None) -> _Prepared:
