@@ -123,6 +123,31 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits, int 
                        void* stream);
 
 /*
+ * Both verify calls on the split layout of the target's logits, for engines that keep the
+ * prediction saved from the last round apart from the logits of the new block, so that they
+ * need not copy the two into one array first.  In the alignment table of the tutorial's §4,
+ * row 0 (the target's prediction for the position after the committed context) was produced
+ * by the previous round's forward and saved; rows 1..gmax come from this round's forward over
+ * the drafts.  The results are exactly those of spec_verify_greedy / spec_verify_sample on the
+ * concatenated array target[b] = [saved_logits[b], block_logits[b][0..gmax-1]]:
+ *   saved_logits   [B][V]        target row 0 of every sequence
+ *   block_logits   [B][gmax][V]  target rows 1..gmax (may be NULL when gmax == 0)
+ * The other arguments, the workspace and the status bits are as for those calls.  The 128-bit
+ * load path needs every logits array 16-byte aligned with V * element size a multiple of 16;
+ * otherwise a scalar path computes the same results.
+ */
+int spec_verify_greedy_split(const void* saved_logits, const void* block_logits, int dtype,
+                             const int32_t* draft_tokens, const int32_t* num_draft, int B, int gmax,
+                             int V, int32_t* out_tokens, int32_t* num_accepted, int32_t* status,
+                             void* workspace, size_t workspace_bytes, void* stream);
+int spec_verify_sample_split(const void* saved_logits, const void* block_logits,
+                             const void* draft_logits, int dtype, const int32_t* draft_tokens,
+                             const int32_t* num_draft, const float* temperature,
+                             const float* u_accept, const float* u_sample, int B, int gmax, int V,
+                             int32_t* out_tokens, int32_t* num_accepted, float* diag,
+                             int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * spec_verify_sample without a caller-owned workspace.  The pages have no counterpart: this
  * is a convenience of this library for callers that cannot allocate device memory where they
  * verify (a serving loop whose memory is fixed after start-up, or a step between a

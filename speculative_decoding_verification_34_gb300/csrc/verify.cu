@@ -95,7 +95,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kChunkFree = 0, kChunkMine = 1, kChunkGivenUp = 2, kChunkDecider = 3;
 
 struct Args {
-  const void* target;
+  const void* saved;    // split layout: target row 0 of every sequence, [B][V]; else null
+  const void* target;   // [B][gmax+1][V], or rows 1..gmax as [B][gmax][V] in the split layout
   const void* draft;
   const int32_t* draft_tokens;
   const int32_t* num_draft;
@@ -517,13 +518,26 @@ struct Shared {
 // per-sequence context
 // ------------------------------------------------------------------------------------------
 
+// Target row i of sequence b.  In the split layout row 0 (the prediction saved from the last
+// round) has an array of its own and rows 1..gmax are contiguous per sequence.
+template <class E>
+__device__ __forceinline__ const typename E::raw* target_row(const Args& a, int b, int i) {
+  using raw = typename E::raw;
+  if (a.saved) {
+    return i == 0 ? static_cast<const raw*>(a.saved) + int64_t(b) * a.V
+                  : static_cast<const raw*>(a.target) + (int64_t(b) * a.gmax + (i - 1)) * a.V;
+  }
+  return static_cast<const raw*>(a.target) + (int64_t(b) * (a.gmax + 1) + i) * a.V;
+}
+
 template <class E, bool kMixed>
 struct Seq {
   using raw = typename E::raw;
   int b, g, flags;
   bool sampling;
   float k;
-  const raw* P;
+  const raw* P0;   // target row 0
+  const raw* P1;   // target row 1; rows i >= 1 follow it V apart
   const raw* Q;
 
   __device__ __forceinline__ Seq(const Args& a, int b_) : b(b_) {
@@ -537,7 +551,8 @@ struct Seq {
     if constexpr (kMixed) T = __ldg(&a.temperature[b]);
     sampling = kMixed && (T > 0.f);
     k = sampling ? kLog2e / T : 0.f;
-    P = static_cast<const raw*>(a.target) + int64_t(b) * (a.gmax + 1) * a.V;
+    P0 = target_row<E>(a, b, 0);
+    P1 = target_row<E>(a, b, 1);
     Q = sampling ? static_cast<const raw*>(a.draft) + int64_t(b) * a.gmax * a.V : nullptr;
   }
   __device__ __forceinline__ bool slot_valid(int slot, int gmax) const {
@@ -552,9 +567,7 @@ struct Seq {
     const int i = g - 1 - ((r - 1) >> 1);
     return (r & 1) ? gmax + 1 + i : i;
   }
-  __device__ __forceinline__ const raw* row(int slot, int gmax, int64_t V) const {
-    return slot <= gmax ? P + int64_t(slot) * V : Q + int64_t(slot - gmax - 1) * V;
-  }
+  __device__ __forceinline__ const raw* prow(int i, int64_t V) const { return i == 0 ? P0 : P1 + int64_t(i - 1) * V; }
 };
 
 // weights of the N elements of one vector: w = residual (or p on the bonus row), and p
@@ -716,7 +729,7 @@ __device__ void select(const Args& a, const Geo& geo, const Work& w, const Seq<E
   const int wlen = geo.dchunk / kWarps;
   const int64_t lo = int64_t(oj / kWarps) * geo.dchunk + int64_t(oj % kWarps) * wlen;
   const int64_t hi = lo + wlen < a.V ? lo + wlen : a.V;
-  const raw* rp = sq.P + int64_t(pl.m) * a.V;
+  const raw* rp = sq.prow(pl.m, a.V);
   const raw* rq = pair ? sq.Q + int64_t(pl.m) * a.V : rp;
   float run = sm.base;
   for (int64_t e0 = lo; e0 < hi; e0 += kStep) {
@@ -806,7 +819,7 @@ __device__ void draw_chunk(const Args& a, const Geo& geo, const Work& w, const S
   const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
   const int b = sq.b;
   const bool pair = pl.pair != 0;
-  const raw* rp = sq.P + int64_t(pl.m) * a.V;
+  const raw* rp = sq.prow(pl.m, a.V);
   const raw* rq = pair ? sq.Q + int64_t(pl.m) * a.V : rp;
   const int wlen = geo.dchunk / kWarps;
   const int64_t lo = int64_t(dc) * geo.dchunk + int64_t(warp) * wlen;
@@ -1032,7 +1045,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
     // first two passes are started before those arrive.  A row past num_draft (or a draft
     // row of a greedy sequence) is inside the caller's tensors; its passes are dropped.
     const raw* row = slot <= a.gmax
-                         ? static_cast<const raw*>(a.target) + (int64_t(b) * (a.gmax + 1) + slot) * a.V
+                         ? target_row<E>(a, b, slot)
                          : static_cast<const raw*>(a.draft) + (int64_t(b) * a.gmax + (slot - a.gmax - 1)) * a.V;
     const int64_t lo = int64_t(c) * geo.chunk;
     const int64_t hi = lo + geo.chunk < a.V ? lo + geo.chunk : a.V;
@@ -1406,7 +1419,7 @@ bool vec_ok(const void* p, int dtype, int64_t V) {
 
 template <bool kMixed>
 int dispatch_on(const Args& a, int dtype, void* ws, size_t ws_bytes, void* stream) {
-  const bool vec = vec_ok(a.target, dtype, a.V) && vec_ok(a.draft, dtype, a.V);
+  const bool vec = vec_ok(a.target, dtype, a.V) && vec_ok(a.draft, dtype, a.V) && vec_ok(a.saved, dtype, a.V);
   if (dtype == SPEC_BF16)
     return vec ? launch<Bf16, true, kMixed>(a, dtype, ws, ws_bytes, stream)
                : launch<Bf16, false, kMixed>(a, dtype, ws, ws_bytes, stream);
@@ -1424,15 +1437,16 @@ extern "C" size_t spec_verify_workspace_bytes(int B, int gmax, int V, int dtype)
   return ws_required(B, gmax, V);
 }
 
-extern "C" int spec_verify_greedy(const void* target_logits, int dtype, const int32_t* draft_tokens,
-                                  const int32_t* num_draft, int B, int gmax, int V,
-                                  int32_t* out_tokens, int32_t* num_accepted, int32_t* status,
-                                  void* workspace, size_t workspace_bytes, void* stream) {
-  clear_error();
-  int rc = check_common(target_logits, dtype, draft_tokens, B, gmax, V, out_tokens, num_accepted);
-  if (rc != SPEC_OK || B == 0) return rc;
+namespace specverify {
+namespace {
+
+// The verify calls on either layout: saved == null is the one-array layout.
+int verify_greedy(const void* saved, const void* target, int dtype, const int32_t* draft_tokens,
+                  const int32_t* num_draft, int B, int gmax, int V, int32_t* out_tokens, int32_t* num_accepted,
+                  int32_t* status, void* workspace, size_t workspace_bytes, void* stream) {
   Args a = {};
-  a.target = target_logits;
+  a.saved = saved;
+  a.target = target;
   a.draft_tokens = draft_tokens;
   a.num_draft = num_draft;
   a.V = V;
@@ -1444,23 +1458,18 @@ extern "C" int spec_verify_greedy(const void* target_logits, int dtype, const in
   return dispatch_on<false>(a, dtype, workspace, workspace_bytes, stream);
 }
 
-extern "C" int spec_verify_sample(const void* target_logits, const void* draft_logits, int dtype,
-                                  const int32_t* draft_tokens, const int32_t* num_draft,
-                                  const float* temperature, const float* u_accept,
-                                  const float* u_sample, int B, int gmax, int V,
-                                  int32_t* out_tokens, int32_t* num_accepted, float* diag,
-                                  int32_t* status, void* workspace, size_t workspace_bytes,
-                                  void* stream) {
-  clear_error();
-  int rc = check_common(target_logits, dtype, draft_tokens, B, gmax, V, out_tokens, num_accepted);
-  if (rc != SPEC_OK) return rc;
-  if (B > 0 && (!temperature || !u_sample || (gmax > 0 && (!draft_logits || !u_accept)))) {
+int verify_sample(const void* saved, const void* target, const void* draft_logits, int dtype,
+                  const int32_t* draft_tokens, const int32_t* num_draft, const float* temperature,
+                  const float* u_accept, const float* u_sample, int B, int gmax, int V, int32_t* out_tokens,
+                  int32_t* num_accepted, float* diag, int32_t* status, void* workspace, size_t workspace_bytes,
+                  void* stream) {
+  if (!temperature || !u_sample || (gmax > 0 && (!draft_logits || !u_accept))) {
     set_error("null required pointer (draft_logits, temperature, u_accept or u_sample)");
     return SPEC_EINVAL;
   }
-  if (B == 0) return SPEC_OK;
   Args a = {};
-  a.target = target_logits;
+  a.saved = saved;
+  a.target = target;
   a.draft = draft_logits;
   a.draft_tokens = draft_tokens;
   a.num_draft = num_draft;
@@ -1475,6 +1484,71 @@ extern "C" int spec_verify_sample(const void* target_logits, const void* draft_l
   a.diag = diag;
   a.status = status;
   return dispatch_on<true>(a, dtype, workspace, workspace_bytes, stream);
+}
+
+// the split layout's extra check: the block rows are required when there are drafts
+int check_block(const void* block, int B, int gmax) {
+  if (B > 0 && gmax > 0 && !block) {
+    set_error("null required pointer (block_logits)");
+    return SPEC_EINVAL;
+  }
+  return SPEC_OK;
+}
+
+}  // namespace
+}  // namespace specverify
+
+extern "C" int spec_verify_greedy(const void* target_logits, int dtype, const int32_t* draft_tokens,
+                                  const int32_t* num_draft, int B, int gmax, int V,
+                                  int32_t* out_tokens, int32_t* num_accepted, int32_t* status,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  clear_error();
+  int rc = check_common(target_logits, dtype, draft_tokens, B, gmax, V, out_tokens, num_accepted);
+  if (rc != SPEC_OK || B == 0) return rc;
+  return verify_greedy(nullptr, target_logits, dtype, draft_tokens, num_draft, B, gmax, V, out_tokens, num_accepted,
+                       status, workspace, workspace_bytes, stream);
+}
+
+extern "C" int spec_verify_sample(const void* target_logits, const void* draft_logits, int dtype,
+                                  const int32_t* draft_tokens, const int32_t* num_draft,
+                                  const float* temperature, const float* u_accept,
+                                  const float* u_sample, int B, int gmax, int V,
+                                  int32_t* out_tokens, int32_t* num_accepted, float* diag,
+                                  int32_t* status, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  clear_error();
+  int rc = check_common(target_logits, dtype, draft_tokens, B, gmax, V, out_tokens, num_accepted);
+  if (rc != SPEC_OK || B == 0) return rc;
+  return verify_sample(nullptr, target_logits, draft_logits, dtype, draft_tokens, num_draft, temperature, u_accept,
+                       u_sample, B, gmax, V, out_tokens, num_accepted, diag, status, workspace, workspace_bytes,
+                       stream);
+}
+
+extern "C" int spec_verify_greedy_split(const void* saved_logits, const void* block_logits, int dtype,
+                                        const int32_t* draft_tokens, const int32_t* num_draft, int B, int gmax,
+                                        int V, int32_t* out_tokens, int32_t* num_accepted, int32_t* status,
+                                        void* workspace, size_t workspace_bytes, void* stream) {
+  clear_error();
+  int rc = check_common(saved_logits, dtype, draft_tokens, B, gmax, V, out_tokens, num_accepted);
+  if (rc == SPEC_OK) rc = check_block(block_logits, B, gmax);
+  if (rc != SPEC_OK || B == 0) return rc;
+  return verify_greedy(saved_logits, block_logits, dtype, draft_tokens, num_draft, B, gmax, V, out_tokens,
+                       num_accepted, status, workspace, workspace_bytes, stream);
+}
+
+extern "C" int spec_verify_sample_split(const void* saved_logits, const void* block_logits,
+                                        const void* draft_logits, int dtype, const int32_t* draft_tokens,
+                                        const int32_t* num_draft, const float* temperature,
+                                        const float* u_accept, const float* u_sample, int B, int gmax, int V,
+                                        int32_t* out_tokens, int32_t* num_accepted, float* diag,
+                                        int32_t* status, void* workspace, size_t workspace_bytes, void* stream) {
+  clear_error();
+  int rc = check_common(saved_logits, dtype, draft_tokens, B, gmax, V, out_tokens, num_accepted);
+  if (rc == SPEC_OK) rc = check_block(block_logits, B, gmax);
+  if (rc != SPEC_OK || B == 0) return rc;
+  return verify_sample(saved_logits, block_logits, draft_logits, dtype, draft_tokens, num_draft, temperature,
+                       u_accept, u_sample, B, gmax, V, out_tokens, num_accepted, diag, status, workspace,
+                       workspace_bytes, stream);
 }
 
 // ------------------------------------------------------------------------------------------

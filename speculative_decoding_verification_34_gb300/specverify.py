@@ -48,6 +48,11 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.spec_verify_greedy.restype = i32
     lib.spec_verify_sample.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, sz, sz, sz, vp, vp, vp, vp, vp, size_t, vp]
     lib.spec_verify_sample.restype = i32
+    lib.spec_verify_greedy_split.argtypes = [vp, vp, i32, vp, vp, sz, sz, sz, vp, vp, vp, vp, size_t, vp]
+    lib.spec_verify_greedy_split.restype = i32
+    lib.spec_verify_sample_split.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, sz, sz, sz, vp, vp, vp, vp, vp,
+                                             size_t, vp]
+    lib.spec_verify_sample_split.restype = i32
     lib.spec_verify_sample_static.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, sz, sz, sz, vp, vp, vp, vp, vp]
     lib.spec_verify_sample_static.restype = i32
     lib.spec_verify_workspace_bytes.argtypes = [sz, sz, sz, i32]
@@ -155,6 +160,65 @@ def spec_verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor,
     ws, wsp, wsn = _ws(workspace, B, gmax, V, code, target_logits.device)
     _check(lib.spec_verify_sample(
         _ptr(target_logits, "target_logits"),
+        _ptr(draft_logits, "draft_logits", None, (B, gmax, V)), code,
+        _ptr(draft_tokens, "draft_tokens", torch.int32, (B, gmax)),
+        _ptr(num_draft, "num_draft", torch.int32, (B,)),
+        _ptr(temperature, "temperature", torch.float32, (B,)),
+        _ptr(u_accept, "u_accept", torch.float32, (B, gmax)),
+        _ptr(u_sample, "u_sample", torch.float32, (B,)), B, gmax, V,
+        _ptr(out_tokens, "out_tokens", torch.int32, (B, gmax + 1)),
+        _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
+        _ptr(diag, "diag", torch.float32, (B, 2 * gmax + 1)),
+        _ptr(status, "status", torch.int32, (B,)), wsp, wsn, _stream(stream)))
+
+
+def _split_shapes(saved_logits, block_logits):
+    B, V = saved_logits.shape
+    if block_logits is None:
+        return B, 0, V
+    Bb, gmax, Vb = block_logits.shape
+    if (Bb, Vb) != (B, V) or block_logits.dtype != saved_logits.dtype:
+        raise ValueError(f"block_logits {tuple(block_logits.shape)} does not match saved_logits {(B, V)}")
+    return B, gmax, V
+
+
+def spec_verify_greedy_split(saved_logits: torch.Tensor, block_logits: Optional[torch.Tensor],
+                             draft_tokens: torch.Tensor, num_draft: Optional[torch.Tensor],
+                             out_tokens: torch.Tensor, num_accepted: torch.Tensor,
+                             status: Optional[torch.Tensor] = None,
+                             workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """spec_verify_greedy with target row 0 (saved_logits [B][V]) apart from rows 1..gmax
+    (block_logits [B][gmax][V])."""
+    B, gmax, V = _split_shapes(saved_logits, block_logits)
+    lib = load_library()
+    code = _dtype_code(saved_logits)
+    ws, wsp, wsn = _ws(workspace, B, gmax, V, code, saved_logits.device)
+    _check(lib.spec_verify_greedy_split(
+        _ptr(saved_logits, "saved_logits"), _ptr(block_logits, "block_logits"), code,
+        _ptr(draft_tokens, "draft_tokens", torch.int32, (B, gmax)),
+        _ptr(num_draft, "num_draft", torch.int32, (B,)), B, gmax, V,
+        _ptr(out_tokens, "out_tokens", torch.int32, (B, gmax + 1)),
+        _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
+        _ptr(status, "status", torch.int32, (B,)), wsp, wsn, _stream(stream)))
+
+
+def spec_verify_sample_split(saved_logits: torch.Tensor, block_logits: Optional[torch.Tensor],
+                             draft_logits: torch.Tensor, draft_tokens: torch.Tensor,
+                             num_draft: Optional[torch.Tensor], temperature: torch.Tensor,
+                             u_accept: torch.Tensor, u_sample: torch.Tensor, out_tokens: torch.Tensor,
+                             num_accepted: torch.Tensor, diag: Optional[torch.Tensor] = None,
+                             status: Optional[torch.Tensor] = None,
+                             workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """spec_verify_sample with target row 0 (saved_logits [B][V]) apart from rows 1..gmax
+    (block_logits [B][gmax][V])."""
+    B, gmax, V = _split_shapes(saved_logits, block_logits)
+    if draft_logits.dtype != saved_logits.dtype:
+        raise TypeError("target and draft logits must have the same dtype")
+    lib = load_library()
+    code = _dtype_code(saved_logits)
+    ws, wsp, wsn = _ws(workspace, B, gmax, V, code, saved_logits.device)
+    _check(lib.spec_verify_sample_split(
+        _ptr(saved_logits, "saved_logits"), _ptr(block_logits, "block_logits"),
         _ptr(draft_logits, "draft_logits", None, (B, gmax, V)), code,
         _ptr(draft_tokens, "draft_tokens", torch.int32, (B, gmax)),
         _ptr(num_draft, "num_draft", torch.int32, (B,)),

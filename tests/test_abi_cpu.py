@@ -82,6 +82,23 @@ def test_host_argument_checks(lib):
     assert lib.spec_launch_count() == n0      # nothing was launched
 
 
+def test_split_layout_argument_checks(lib):
+    """The split-layout calls check their two target arrays on the host: the saved row is
+    always required, the block rows only when there are drafts."""
+    n0 = lib.spec_launch_count()
+    g = lambda saved=FAKE, block=FAKE, B=4, gmax=3: lib.spec_verify_greedy_split(
+        saved, block, 0, FAKE, None, B, gmax, 100, FAKE, FAKE, None, FAKE, 8, None)
+    s = lambda saved=FAKE, block=FAKE, B=4, gmax=3: lib.spec_verify_sample_split(
+        saved, block, FAKE, 0, FAKE, None, FAKE, FAKE, FAKE, B, gmax, 100, FAKE, FAKE, None, None, FAKE, 8, None)
+    assert g(saved=None) == 1 and s(saved=None) == 1
+    assert g(block=None) == 1 and b"block_logits" in lib.spec_last_error()
+    assert s(block=None) == 1
+    # block may be null without drafts; the 8-byte workspace is then what is refused
+    assert g(block=None, gmax=0) == 3 and b"workspace" in lib.spec_last_error()
+    assert g(saved=None, block=None, B=0) == 0 and s(saved=None, block=None, B=0) == 0
+    assert lib.spec_launch_count() == n0
+
+
 def test_plan_splits_vocabulary(lib):
     for V in [1, 3, 1024, 4096, 4097, 32000, 50000, 128256, 151936, 1 << 20]:
         cl, chunk = sv.spec_verify_plan(V)
@@ -114,7 +131,7 @@ def test_binding_arity_matches_header(lib):
         text += re.sub(r"/\*.*?\*/", "", open(h, encoding="utf-8").read(), flags=re.S)
     for name in ("spec_verify_greedy", "spec_verify_sample", "spec_commit_kv_lengths",
                  "spec_verify_workspace_bytes", "spec_verify_plan", "spec_verify_sample_static",
-                 "spec_apply_stops"):
+                 "spec_apply_stops", "spec_verify_greedy_split", "spec_verify_sample_split"):
         m = re.search(r"\b" + name + r"\s*\(([^)]*)\)", text)
         params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
         assert len(getattr(lib, name).argtypes) == len(params), name
