@@ -36,6 +36,14 @@ Readings where the pages leave a step open (each also listed in the design doc):
     num_draft outside [0, gmax] is clamped (status bit 4).
   * Temperature T <= 0 (or NaN) marks a greedy sequence; otherwise p = softmax(P/T)
     and q = softmax(Q/T), the same T on both sides.
+  * Tree verification ([TUT] §5.3: the target checks every node of a draft tree in one
+    forward and keeps the longest accepted root-to-leaf path; [KB] §01, §06: a tree has its
+    own rules, and its branches need their own cache bookkeeping).  The pages give no
+    sampling rule for trees, so trees are verified greedily: node j is accepted iff its
+    parent is and its token equals the argmax of the parent's target row; the deepest
+    accepted node (the lowest index among equal depths) ends the path; the emitted tokens
+    are the path's, then the argmax of its last node's row.  A node whose parent index is
+    not smaller than its own is never accepted (status bit 64).
   * Stops ([TUT] §5.2 "common mistakes": nothing after an EOS in the candidate block
     may reach the cache; §12.3: EOS, maximum length and the rejection position must
     agree with step-by-step decoding; [KB] §03: an end token or a length limit may end
@@ -60,6 +68,7 @@ ST_R_ZERO = 2
 ST_CLAMPED_GAMMA = 4
 ST_HISTORY_FULL = 8
 ST_STOPPED = 32
+ST_BAD_TREE = 64
 
 
 def widen(row: np.ndarray, dtype: str) -> np.ndarray:
@@ -333,3 +342,76 @@ def apply_stops(out_tokens: np.ndarray, m: np.ndarray, eos_id: int,
         if stop_eos or stop_budget:
             status[b] |= ST_STOPPED
     return out, mm, status
+
+
+@dataclasses.dataclass
+class TreeResult:
+    tokens: List[int]   # the path's tokens, then the correction/bonus token
+    path: List[int]     # accepted node indices along the path, root (0) excluded
+    m: int              # path length = accepted drafts
+    status: int
+    n: int              # nodes after clamping
+
+
+def verify_tree_greedy_sequence(target: np.ndarray, node_tokens: np.ndarray, node_parents: np.ndarray,
+                                n: int) -> TreeResult:
+    """Greedy verification of a draft tree ([TUT] §5.3).
+
+    Nodes 1..n; node j carries token node_tokens[j-1] and has parent node_parents[j-1]
+    (0 is the root, the position after the committed context).  target: float64
+    [>= n+1, V]; row j is the target's prediction for the position after node j.  Node j
+    is accepted iff its parent is accepted (the root always is) and its token equals the
+    argmax of its parent's row.  The path ends at the deepest accepted node (lowest index
+    among equal depths); the step emits the path's tokens and then the argmax of that
+    node's row -- the target's replacement where the tree ran out of matching drafts, or
+    its bonus token at a leaf.
+    """
+    V = target.shape[1]
+    status = 0
+    accepted = [True] + [False] * n
+    depth = [0] * (n + 1)
+    best = 0
+    for j in range(1, n + 1):
+        par = int(node_parents[j - 1])
+        d = int(node_tokens[j - 1])
+        if not (0 <= par < j):
+            status |= ST_BAD_TREE
+            continue
+        depth[j] = depth[par] + 1
+        if not accepted[par]:
+            continue
+        if not (0 <= d < V):
+            status |= ST_BAD_DRAFT
+            continue
+        if d == greedy_argmax(target[par]):
+            accepted[j] = True
+            if depth[j] > depth[best]:
+                best = j
+    path = []
+    j = best
+    while j != 0:
+        path.append(j)
+        j = int(node_parents[j - 1])
+    path.reverse()
+    tokens = [int(node_tokens[c - 1]) for c in path] + [greedy_argmax(target[best])]
+    return TreeResult(tokens, path, len(path), status, n)
+
+
+def verify_tree_batch(target: np.ndarray, dtype: str, node_tokens: np.ndarray, node_parents: np.ndarray,
+                      num_nodes: Optional[np.ndarray], seqs=None) -> List[TreeResult]:
+    """Greedy tree verification of every sequence (or the listed ones): target
+    [B, nmax+1, V], node_tokens and node_parents [B, nmax]; num_nodes [B] (None: nmax),
+    clamped to [0, nmax] with status bit 4."""
+    B, np1, V = target.shape
+    nmax = np1 - 1
+    out = []
+    for b in (range(B) if seqs is None else seqs):
+        n = nmax if num_nodes is None else int(num_nodes[b])
+        clamped = 0
+        if n < 0 or n > nmax:
+            n = min(max(n, 0), nmax)
+            clamped = ST_CLAMPED_GAMMA
+        r = verify_tree_greedy_sequence(widen(target[b, : n + 1], dtype), node_tokens[b], node_parents[b], n)
+        r.status |= clamped
+        out.append(r)
+    return out

@@ -359,3 +359,113 @@ def check_stops_match_step_by_step(cases=None):
         want = ar_greedy_decode(target, [3], eos, max_new)
         got = spec_greedy_decode(target, draft, [3], eos, max_new, gamma)
         assert got == want, (seed, gamma, max_new, bias, got, want)
+
+
+# ---------------------------------------------------------------------------------------
+# tree verification (tutorial §5.3): greedy acceptance along a draft tree
+# ---------------------------------------------------------------------------------------
+
+def check_tree_figure():
+    """The tutorial's §5.3 tree, with three target continuations: the longer accepted
+    branch wins, a branch stops at its first mismatch, and nothing is accepted when the
+    first token already differs."""
+    G = golden("tree_figure.json")
+    names = G["nodes"]
+    words = sorted(set(names) | {"<bonus>", "<other>", "root"})
+    ids = {w: i for i, w in enumerate(words)}
+    V = len(words)
+    n = len(names)
+    toks = np.array([ids[w] for w in names])
+    par = np.array(G["parents"])
+    for case in G["cases"]:
+        rows = np.zeros((n + 1, V))
+        for after, nxt in case["target_greedy_after"].items():
+            r = 0 if after == "root" else names.index(after) + 1
+            rows[r, ids[nxt]] = 1.0
+        res = O.verify_tree_greedy_sequence(rows, toks, par, n)
+        assert [names[j - 1] for j in res.path] == case["path"], (res, case)
+        assert res.tokens == [ids[w] for w in case["emitted"]], (res, case)
+        assert res.m == len(case["path"]) and res.status == 0
+
+
+def check_tree_chain_equals_chain(cases=60, seed=5):
+    """A chain tree (node j's parent is j-1) is the chain verification of the same drafts."""
+    rng = np.random.default_rng(seed)
+    for _ in range(cases):
+        V = int(rng.integers(2, 9))
+        n = int(rng.integers(0, 7))
+        rows = rng.normal(0, 1, size=(n + 1, V)).round(1)
+        am = [int(np.argmax(r)) for r in rows]
+        d = np.array([am[i] if rng.random() < 0.7 else int(rng.integers(0, V)) for i in range(n)], dtype=np.int64)
+        if n and rng.random() < 0.2:
+            d[int(rng.integers(0, n))] = V + 3   # an id outside the row
+        chain = O.verify_greedy_sequence(rows, d, n)
+        tree = O.verify_tree_greedy_sequence(rows, d, np.arange(n), n)
+        assert tree.tokens == chain.tokens and tree.m == chain.m and tree.status == chain.status, (tree, chain)
+        assert tree.path == list(range(1, chain.m + 1))
+
+
+def _greedy_walk(rows, toks, par, n):
+    """The target's own greedy continuation, followed through the tree as long as the tree
+    holds the next token as a child: a second statement of 'the longest accepted path' for
+    trees whose siblings carry distinct tokens."""
+    children = {}
+    for j in range(1, n + 1):
+        children.setdefault(int(par[j - 1]), {})[int(toks[j - 1])] = j
+    node, path = 0, []
+    while True:
+        x = int(np.flatnonzero(rows[node] == rows[node].max())[0])
+        nxt = children.get(node, {}).get(x)
+        if nxt is None:
+            return path, [int(toks[c - 1]) for c in path] + [x]
+        path.append(nxt)
+        node = nxt
+
+
+def check_tree_matches_greedy_walk(cases=200, seed=11):
+    rng = np.random.default_rng(seed)
+    for _ in range(cases):
+        V = int(rng.integers(3, 8))
+        n = int(rng.integers(0, 12))
+        par = np.array([int(rng.integers(0, j)) for j in range(1, n + 1)], dtype=np.int64)
+        rows = rng.normal(0, 1, size=(n + 1, V)).round(1)
+        toks = np.zeros(n, dtype=np.int64)
+        used = {}
+        for j in range(1, n + 1):
+            p = int(par[j - 1])
+            free = [v for v in range(V) if v not in used.get(p, set())]
+            if not free:              # more children than ids: give the node up to the root
+                par[j - 1] = 0
+                p = 0
+                free = [v for v in range(V) if v not in used.get(0, set())] or [0]
+            am = int(np.flatnonzero(rows[p] == rows[p].max())[0])
+            t = am if (am in free and rng.random() < 0.6) else int(rng.choice(free))
+            toks[j - 1] = t
+            used.setdefault(p, set()).add(t)
+        if any(len(set(int(toks[c - 1]) for c in range(1, n + 1) if int(par[c - 1]) == p)) !=
+               sum(1 for c in range(1, n + 1) if int(par[c - 1]) == p) for p in range(n + 1)):
+            continue                  # duplicate siblings: the walk is not defined there
+        res = O.verify_tree_greedy_sequence(rows, toks, par, n)
+        path, emitted = _greedy_walk(rows, toks, par, n)
+        assert res.path == path and res.tokens == emitted, (res, path, emitted)
+
+
+def check_tree_ties_and_invalid_nodes():
+    """Equal-depth accepted paths (two siblings with the same token): the lower node index
+    wins.  A node whose parent index is not below its own is never accepted, nor is its
+    subtree (bit 64); a candidate id outside [0, V) is a rejection (bit 1)."""
+    V = 5
+    rows = np.zeros((5, V))
+    rows[0, 2] = 1.0      # root -> 2
+    rows[1, 3] = 1.0      # after node 1 -> 3
+    rows[2, 3] = 1.0      # after node 2 -> 3
+    rows[3, 4] = 1.0
+    rows[4, 1] = 1.0
+    # nodes: 1 = 2 (root), 2 = 2 (root), 3 = 3 (under 2), 4 = 3 (under 1)
+    res = O.verify_tree_greedy_sequence(rows, np.array([2, 2, 3, 3]), np.array([0, 0, 2, 1]), 4)
+    assert res.path == [2, 3] and res.tokens == [2, 3, 4] and res.status == 0, res
+    res = O.verify_tree_greedy_sequence(rows, np.array([2, 2, 3, 3]), np.array([0, 0, 1, 1]), 4)
+    assert res.path == [1, 3], res
+    # node 2 names itself as its parent; node 3 hangs below it
+    res = O.verify_tree_greedy_sequence(rows, np.array([7, 2, 3]), np.array([0, 2, 2]), 3)
+    assert res.status == O.ST_BAD_TREE | O.ST_BAD_DRAFT and res.path == [] and res.tokens == [2], res

@@ -46,6 +46,38 @@ def _stops_last_token_only(out_tokens, m, eos_id, max_new=None):
 _apply_stops = O.apply_stops
 
 
+def _tree_variant(own_row=False, last_tie=False):
+    # a copy of the tree verification with one planted mistake: the node's own row judged
+    # instead of its parent's, or the higher index winning equal depths
+    def run(target, node_tokens, node_parents, n):
+        V = target.shape[1]
+        status, acc, depth, best = 0, [True] + [False] * n, [0] * (n + 1), 0
+        for j in range(1, n + 1):
+            par, d = int(node_parents[j - 1]), int(node_tokens[j - 1])
+            if not (0 <= par < j):
+                status |= O.ST_BAD_TREE
+                continue
+            depth[j] = depth[par] + 1
+            if not acc[par]:
+                continue
+            if not (0 <= d < V):
+                status |= O.ST_BAD_DRAFT
+                continue
+            row = target[j] if own_row else target[par]
+            if d == O.greedy_argmax(row):
+                acc[j] = True
+                if depth[j] > depth[best] or (last_tie and depth[j] == depth[best]):
+                    best = j
+        path, j = [], best
+        while j != 0:
+            path.append(j)
+            j = int(node_parents[j - 1])
+        path.reverse()
+        return O.TreeResult([int(node_tokens[c - 1]) for c in path] + [O.greedy_argmax(target[best])],
+                            path, len(path), status, n)
+    return run
+
+
 MUTATIONS = {
     "resample_from_p": ("residual_weights", lambda p, q: p.copy()),
     "residual_transposed": ("residual_weights", lambda p, q: np.maximum(q - p, 0.0)),
@@ -57,6 +89,8 @@ MUTATIONS = {
     "row_shift": ("verify_sample_sequence", None),
     "stops_last_token_only": ("apply_stops", _stops_last_token_only),
     "stops_budget_ignored": ("apply_stops", lambda o, m, e, n=None: _apply_stops(o, m, e, None)),
+    "tree_own_row": ("verify_tree_greedy_sequence", _tree_variant(own_row=True)),
+    "tree_last_index_tie": ("verify_tree_greedy_sequence", _tree_variant(last_tie=True)),
 }
 
 
@@ -66,7 +100,9 @@ def _pins_pass():
               pins.check_greedy_tie_rule,
               lambda: pins.check_joint_law(3, 2, 0.7, 2),
               lambda: pins.check_joint_law(3, 1, 1.0, 1),
-              pins.check_stops_match_step_by_step]
+              pins.check_stops_match_step_by_step,
+              pins.check_tree_figure, pins.check_tree_chain_equals_chain,
+              pins.check_tree_matches_greedy_walk, pins.check_tree_ties_and_invalid_nodes]
     for c in checks:
         try:
             c()

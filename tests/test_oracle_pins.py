@@ -192,3 +192,29 @@ def test_stops_special_cases():
                                                 out_tokens=np.array([[-1, -1], [4, 6]]),
                                                 history=np.full((2, 4), -9), committed_len=np.array([1, 1]))
     assert clen.tolist() == [1, 3] and hist.tolist() == [[-9] * 4, [-9, 4, 6, -9]] and kv.tolist() == [10, 11]
+
+
+def test_tree_figure():
+    pins.check_tree_figure()
+
+
+def test_tree_chain_equals_chain_verification():
+    pins.check_tree_chain_equals_chain()
+
+
+def test_tree_matches_target_greedy_walk():
+    pins.check_tree_matches_greedy_walk()
+
+
+def test_tree_ties_and_invalid_nodes():
+    pins.check_tree_ties_and_invalid_nodes()
+
+
+def test_tree_batch_clamps_node_counts():
+    rows = np.zeros((2, 3, 4), dtype=np.float32)
+    rows[:, 0, 1] = 1.0
+    rows[:, 1, 2] = 1.0
+    res = O.verify_tree_batch(rows, "f32", np.array([[1, 2], [1, 3]]), np.array([[0, 1], [0, 1]]),
+                              np.array([5, -1]))
+    assert res[0].n == 2 and res[0].status == O.ST_CLAMPED_GAMMA and res[0].tokens == [1, 2, 0]
+    assert res[1].n == 0 and res[1].status == O.ST_CLAMPED_GAMMA and res[1].tokens == [1]
