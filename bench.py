@@ -42,17 +42,37 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=100)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6],
+                    help="1-5: the sampling/greedy workloads; 6: 63-node draft trees (greedy tree verify)")
     ap.add_argument("--copies", type=int, default=4, help="resident input copies rotated per step")
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
 
 
+def is_tree(wl):
+    return hasattr(wl, "node_parents")
+
+
 def workload_config(wl, l2_note):
+    if is_tree(wl):
+        return {"workload": wl.name, "B": wl.B, "tree_nodes": wl.nmax, "V": wl.V, "logits": wl.dtype,
+                "temperature": 0.0, "algorithmic_bytes_per_step": wl.algorithmic_bytes(),
+                "verified_rows_per_step": wl.verified_rows(), "l2": l2_note}
     return {"workload": wl.name, "B": wl.B, "gamma": wl.gmax, "V": wl.V, "logits": wl.dtype,
             "temperature": float(wl.temperature.max()), "algorithmic_bytes_per_step": wl.algorithmic_bytes(),
             "verified_rows_per_step": wl.verified_rows(), "l2": l2_note}
+
+
+def oracle_one(wl, b):
+    """The oracle on sequence b alone; returns the draft rows (or tree nodes) it judged."""
+    from oracle import specverify_oracle as O
+    if is_tree(wl):
+        O.verify_tree_batch(wl.target, wl.dtype, wl.node_tokens, wl.node_parents, wl.num_nodes, seqs=[b])
+        return int(wl.num_nodes[b])
+    O.verify_batch(wl.target, wl.draft, wl.dtype, wl.draft_tokens, wl.num_draft,
+                   None if wl.greedy_only else wl.temperature, wl.u_accept, wl.u_sample, seqs=[b])
+    return int(wl.num_draft[b])
 
 
 def dist_env():
@@ -177,15 +197,12 @@ def aggregate_rate(world, rows_per_step, steps, max_elapsed_ms):
 
 def cpu_oracle_rate(wl, seconds, seqs_cap=None):
     """Oracle throughput on a bounded sample of the same batch: rows/s, sequences used."""
-    from oracle import specverify_oracle as O
     t0 = time.perf_counter()
     n = rows = 0
     order = list(range(wl.B))
     while True:
         b = order[n % wl.B]
-        O.verify_batch(wl.target, wl.draft, wl.dtype, wl.draft_tokens, wl.num_draft,
-                       None if wl.greedy_only else wl.temperature, wl.u_accept, wl.u_sample, seqs=[b])
-        rows += int(wl.num_draft[b])
+        rows += oracle_one(wl, b)
         n += 1
         el = time.perf_counter() - t0
         if (el >= seconds and n >= 2) or (seqs_cap and n >= seqs_cap):
@@ -199,13 +216,10 @@ def run_reference(args):
     if rank != 0:
         return
     from speculative_decoding_verification_34_gb300 import workloads as W
-    from oracle import specverify_oracle as O
     wl = W.WORKLOADS[args.config](seed=0)
-    temp = None if wl.greedy_only else wl.temperature
 
     def one(b):
-        O.verify_batch(wl.target, wl.draft, wl.dtype, wl.draft_tokens, wl.num_draft, temp,
-                       wl.u_accept, wl.u_sample, seqs=[b])
+        return oracle_one(wl, b)
 
     # size each step so that the whole run stays within ~150 s: whole sequences, at least one
     t0 = time.perf_counter()
@@ -219,8 +233,7 @@ def run_reference(args):
         r = 0
         for _ in range(per_step):
             b = nxt[0] % wl.B
-            one(b)
-            r += int(wl.num_draft[b])
+            r += one(b)
             nxt[0] += 1
         return r
 
@@ -263,7 +276,8 @@ def run_native(args):
     sv.load_library()
 
     wl = shard_workload(args.config, rank)
-    B, g, V = wl.B, wl.gmax, wl.V
+    tree = is_tree(wl)
+    B, g, V = wl.B, (wl.nmax if tree else wl.gmax), wl.V
 
     def to_dev(a):
         if a.dtype == np.uint16:
@@ -272,9 +286,14 @@ def run_native(args):
 
     ncopies = max(1, args.copies)
     tgt = [to_dev(wl.target) for _ in range(ncopies)]
-    drf = [to_dev(wl.draft) for _ in range(ncopies)] if not wl.greedy_only else None
-    toks, nd = to_dev(wl.draft_tokens), to_dev(wl.num_draft)
-    temp, ua, us = to_dev(wl.temperature), to_dev(wl.u_accept), to_dev(wl.u_sample)
+    if tree:
+        drf, temp, ua, us = None, None, None, None
+        toks, nd, pars = to_dev(wl.node_tokens), to_dev(wl.num_nodes), to_dev(wl.node_parents)
+        path = torch.empty((B, g), dtype=torch.int32, device=device)
+    else:
+        drf = [to_dev(wl.draft) for _ in range(ncopies)] if not wl.greedy_only else None
+        toks, nd = to_dev(wl.draft_tokens), to_dev(wl.num_draft)
+        temp, ua, us = to_dev(wl.temperature), to_dev(wl.u_accept), to_dev(wl.u_sample)
     kv0 = to_dev(wl.kv_len)
     out = torch.empty((B, g + 1), dtype=torch.int32, device=device)
     macc = torch.empty(B, dtype=torch.int32, device=device)
@@ -284,7 +303,10 @@ def run_native(args):
     dkv = kv0.clone()
     stream = torch.cuda.current_stream(device)
     ws = sv.alloc_workspace(B, g, V, sv.SPEC_BF16 if wl.dtype == "bf16" else sv.SPEC_F32, device)
-    if wl.greedy_only:
+    if tree:
+        verify = [sv.prepare_verify_tree_greedy(tgt[c], toks, pars, nd, out, macc, path, st, workspace=ws,
+                                                stream=stream) for c in range(ncopies)]
+    elif wl.greedy_only:
         verify = [sv.prepare_verify_greedy(tgt[c], toks, nd, out, macc, st, workspace=ws, stream=stream)
                   for c in range(ncopies)]
     else:
@@ -365,7 +387,10 @@ def run_native(args):
     # ---- end to end through the public binding, host buffers, copies inside the region ----
     pin = lambda a: (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16
                      else torch.from_numpy(np.ascontiguousarray(a))).pin_memory()
-    if wl.greedy_only:
+    if tree:
+        h_in = [pin(wl.target), pin(wl.node_tokens), pin(wl.node_parents), pin(wl.num_nodes), pin(wl.kv_len)]
+        d_in = [tgt[0], toks, pars, nd, kv]
+    elif wl.greedy_only:
         h_in = [pin(wl.target), pin(wl.draft_tokens), pin(wl.num_draft), pin(wl.kv_len)]
         d_in = [tgt[0], toks, nd, kv]
     else:
@@ -380,7 +405,9 @@ def run_native(args):
     def e2e_step():
         for h, d in zip(h_in, d_in):
             d.copy_(h, non_blocking=True)
-        if wl.greedy_only:
+        if tree:
+            sv.spec_verify_tree_greedy(d_in[0], d_in[1], d_in[2], d_in[3], out, macc, path, st, workspace=ws)
+        elif wl.greedy_only:
             sv.spec_verify_greedy(d_in[0], d_in[1], d_in[2], out, macc, st, workspace=ws)
         else:
             sv.spec_verify_sample(d_in[0], d_in[1], d_in[2], d_in[3], d_in[4], d_in[5], d_in[6],
@@ -424,7 +451,8 @@ def run_native(args):
             "sequences_per_s": world * B * K / (elapsed_ms / 1e3), "mean_emitted_per_sequence": mean_emit,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": ("verify_kernel<bf16, vec, greedy> (spec_verify_greedy)" if wl.greedy_only
+                         "kernel": ("verify_kernel<bf16, vec, greedy> (spec_verify_tree_greedy)" if tree
+                                    else "verify_kernel<bf16, vec, greedy> (spec_verify_greedy)" if wl.greedy_only
                                     else "verify_kernel<bf16, vec, mixed> (spec_verify_sample)"),
                          "kernel_ms_mean": kern_mean_ms, "kernel_ms_median": kern_med_ms,
                          "kernel_ms_p10": kern_p10, "kernel_ms_p90": kern_p90,

@@ -29,8 +29,8 @@
  *        u_accept      [B][gmax]        float32 uniforms in [0,1), one per acceptance test
  *        u_sample      [B]              float32 uniform in [0,1) for the correction/bonus draw
  *        out_tokens    [B][gmax+1]      int32: the m+1 emitted tokens, then -1
- *    Rows past a sequence's num_draft are never used (they may hold anything; the kernel may
- *    read, and drop, up to 32 KB of such a row before it has loaded num_draft).
+ *    Rows past a sequence's num_draft, and the draft rows of a greedy sequence, are never
+ *    read (they may hold anything).
  *  - Logits are bf16 (SPEC_BF16, raw 16-bit patterns) or float32 (SPEC_F32).  They must be
  *    finite or -inf, with at least one finite value per read row; NaN or +inf inputs give
  *    unspecified (but memory-safe) results.
@@ -64,6 +64,7 @@ typedef enum {
 typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype_t;
 
 #define SPEC_MAX_GAMMA 32
+#define SPEC_MAX_TREE_NODES 63
 
 /* per-sequence status bits */
 #define SPEC_ST_BAD_DRAFT 1      /* the stopping draft id was outside [0,V): it counted as rejected */
@@ -73,6 +74,8 @@ typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype_t;
 #define SPEC_ST_TIMEOUT 16       /* a bounded device-side wait ran out: outputs of the sequence not
                                     written; zero-fill the workspace before reusing it */
 #define SPEC_ST_STOPPED 32       /* stops: the sequence emitted its end token or used up its budget */
+#define SPEC_ST_BAD_TREE 64      /* tree: a node's parent index was not below its own; it and its
+                                    subtree counted as rejected */
 
 /*
  * Greedy verification (temperature 0).
@@ -121,6 +124,37 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits, int 
                        int B, int gmax, int V, int32_t* out_tokens, int32_t* num_accepted,
                        float* diag, int32_t* status, void* workspace, size_t workspace_bytes,
                        void* stream);
+
+/*
+ * Greedy verification of a draft TREE (tutorial §5.3: the target checks every node of the
+ * tree in one forward and keeps the longest accepted root-to-leaf path; card §01: a tree
+ * follows its own rules).  Nodes 1..n (n = num_nodes[b], NULL: nmax) carry the draft token
+ * node_tokens[b][j-1] and hang below node_parents[b][j-1], which must be smaller than j
+ * (0 is the root: the position after the committed context).  Target row j is the target's
+ * prediction for the position after node j; row 0 is the saved prediction, as in the chain.
+ * Node j is accepted iff its parent is and its token is the argmax of the parent's row
+ * (lowest id among equal maxima).  The path ends at the deepest accepted node, the lowest
+ * index among equal depths; m is its depth.  The step emits the path's tokens and then the
+ * argmax of the last path node's row (the target's replacement, or its bonus token at a
+ * leaf), and path_nodes lists the path's node indices, so that the caller can keep the
+ * cache entries of exactly those nodes (card §06: trimming a length alone does not repair a
+ * tree's cache).  A chain tree (node j below j-1) gives spec_verify_greedy's results.
+ * The pages give no sampling rule for trees; this call is greedy only.
+ *
+ *   target_logits  [B][nmax+1][V]
+ *   node_tokens    [B][nmax] int32, node_parents [B][nmax] int32, num_nodes [B] or NULL
+ *   out_tokens     [B][nmax+1] (written): the m+1 emitted tokens, then -1
+ *   num_accepted   [B] = m (written); path_nodes [B][nmax] or NULL (written): the path's
+ *                  node indices in root-to-leaf order, then -1
+ *   status         [B] or NULL: SPEC_ST_BAD_TREE, SPEC_ST_BAD_DRAFT (a candidate id outside
+ *                  [0,V)), SPEC_ST_CLAMPED_GAMMA (num_nodes outside [0,nmax])
+ *   workspace      at least spec_verify_workspace_bytes(B, nmax, V, dtype) bytes
+ * Limits: 0 <= nmax <= SPEC_MAX_TREE_NODES (else SPEC_ENOSPACE).
+ */
+int spec_verify_tree_greedy(const void* target_logits, int dtype, const int32_t* node_tokens,
+                            const int32_t* node_parents, const int32_t* num_nodes, int B, int nmax, int V,
+                            int32_t* out_tokens, int32_t* num_accepted, int32_t* path_nodes,
+                            int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Both verify calls on the split layout of the target's logits, for engines that keep the
@@ -176,8 +210,8 @@ int spec_verify_sample_static(const void* target_logits, const void* draft_logit
                               int32_t* num_accepted, float* diag, int32_t* status, void* stream);
 
 /*
- * Bytes of workspace a verify call with these sizes needs (either entry point); 0 for
- * invalid sizes.  Host-only.
+ * Bytes of workspace a verify call with these sizes needs (any verify entry point; pass nmax
+ * as gmax for a tree call); 0 for invalid sizes.  Host-only.
  */
 size_t spec_verify_workspace_bytes(int B, int gmax, int V, int dtype);
 
@@ -195,7 +229,7 @@ size_t spec_verify_workspace_bytes(int B, int gmax, int V, int dtype);
  * entirely untouched (lengths included) and flagged SPEC_ST_HISTORY_FULL in status.
  *
  *   num_accepted   [B] int32 (m, as written by a verify call; values are clamped to
- *                  [0, gmax])
+ *                  [0, gmax]); gmax may be a tree call's nmax (up to SPEC_MAX_TREE_NODES)
  *   target_kv_len  [B] int32, read and written; draft_kv_len [B] or NULL
  *   out_tokens     [B][gmax+1] int32, history [B][cap] int32, committed_len [B] int32 —
  *                  all three NULL, or all three given (cap >= 1)
@@ -213,7 +247,8 @@ int spec_commit_kv_lengths(const int32_t* num_accepted, int B, int32_t* target_k
  * an end token or a length limit may end a round early).  Run it between a verify call and
  * spec_commit_kv_lengths, on the same stream.
  *
- * Per sequence, the emit out_tokens[b][0..m] (m = num_accepted[b], clamped to [0, gmax])
+ * Per sequence, the emit out_tokens[b][0..m] (m = num_accepted[b], clamped to [0, gmax];
+ * gmax up to SPEC_MAX_TREE_NODES, so a tree call's emit can be cut too)
  * ends at its first token equal to eos_id (kept; eos_id < 0: no end token) and holds at most
  * max_new[b] tokens (the sequence's remaining budget; <= 0 emits nothing; max_new NULL: no
  * budget).  The tokens after the cut become -1 and num_accepted[b] becomes (tokens

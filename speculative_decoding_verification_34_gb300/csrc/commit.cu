@@ -113,8 +113,8 @@ extern "C" int spec_commit_kv_lengths(const int32_t* num_accepted, int B, int32_
     set_error("bad sizes B=%d gmax=%d", B, gmax);
     return SPEC_EINVAL;
   }
-  if (gmax > SPEC_MAX_GAMMA) {
-    set_error("gmax=%d exceeds SPEC_MAX_GAMMA=%d", gmax, SPEC_MAX_GAMMA);
+  if (gmax > SPEC_MAX_TREE_NODES) {   // a chain's gmax, or a tree's nmax
+    set_error("gmax=%d exceeds SPEC_MAX_TREE_NODES=%d", gmax, SPEC_MAX_TREE_NODES);
     return SPEC_ENOSPACE;
   }
   if (B == 0) return SPEC_OK;   // empty batch: pointers may be null
@@ -150,8 +150,8 @@ extern "C" int spec_apply_stops(int32_t* out_tokens, int32_t* num_accepted, int 
     set_error("bad sizes B=%d gmax=%d", B, gmax);
     return SPEC_EINVAL;
   }
-  if (gmax > SPEC_MAX_GAMMA) {
-    set_error("gmax=%d exceeds SPEC_MAX_GAMMA=%d", gmax, SPEC_MAX_GAMMA);
+  if (gmax > SPEC_MAX_TREE_NODES) {   // a chain's gmax, or a tree's nmax
+    set_error("gmax=%d exceeds SPEC_MAX_TREE_NODES=%d", gmax, SPEC_MAX_TREE_NODES);
     return SPEC_ENOSPACE;
   }
   if (B == 0) return SPEC_OK;   // empty batch: pointers may be null

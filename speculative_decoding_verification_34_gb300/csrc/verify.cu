@@ -90,6 +90,8 @@ constexpr int kMinBlocks = SPEC_MIN_BLOCKS;            // resident blocks per SM
 constexpr int kMaxGroups = 65535;                      // grid z limit
 constexpr int kPlanWaitIters = 64;                     // optional bounded wait of a B unit (~31 us)
 constexpr unsigned kFull = 0xffffffffu;
+// target rows per sequence the greedy kernel handles: a chain's gmax+1, a tree's nmax+1
+constexpr int kMaxRows = (SPEC_MAX_TREE_NODES > SPEC_MAX_GAMMA ? SPEC_MAX_TREE_NODES : SPEC_MAX_GAMMA) + 1;
 constexpr float kLog2e = 1.4426950408889634f;
 // draw-chunk states (a chunk whose B unit saw the plan at once stays Free)
 constexpr int kChunkFree = 0, kChunkMine = 1, kChunkGivenUp = 2, kChunkDecider = 3;
@@ -110,6 +112,8 @@ struct Args {
   int32_t* num_accepted;
   float* diag;
   int32_t* status;
+  const int32_t* parents;   // tree verification: node parents [B][gmax]; else null
+  int32_t* path_nodes;      // tree verification: accepted path [B][gmax]
 };
 
 struct Geo {
@@ -425,6 +429,39 @@ __device__ __forceinline__ void tile_argmax(const Tile<E, kVec>& t, int64_t e0, 
     }
 }
 
+// The greedy-only kernel's cheaper form of the same running argmax (vector path).  A thread's
+// ids ascend with the pass, then q, then j, so a later element wins only with a strictly larger
+// value: per pass the tile's max comes from a packed max tree, and the whole tile is kept in
+// registers when that max beats the running one.  Once the chunk is done the kept tile is
+// searched for the first element holding the max.  A tile of NaN only is never kept.
+template <class E>
+struct KeptTile {
+  float m = -INFINITY;
+  int64_t e0 = -1;
+  uint4 v[kVecPerPass];
+
+  __device__ __forceinline__ void offer(const Tile<E, true>& t, int64_t te0) {
+    const float tm = E::tmax(t.v);
+    if (tm > m || (e0 < 0 && tm == tm)) {
+      m = tm;
+      e0 = te0;
+#pragma unroll
+      for (int q = 0; q < kVecPerPass; ++q) v[q] = t.v[q];
+    }
+  }
+  __device__ __forceinline__ void settle(int tid, float& bv, int& bi) const {
+    if (e0 < 0) return;
+    int found = INT_MAX;
+#pragma unroll
+    for (int q = 0; q < kVecPerPass; ++q)
+#pragma unroll
+      for (int j = 0; j < E::kPerVec; ++j)
+        if (found == INT_MAX && E::get(v[q], j) == m) found = int(e0 + int64_t(q * kThreads + tid) * E::kPerVec + j);
+    bv = m;
+    bi = found;
+  }
+};
+
 __device__ __forceinline__ int atom_cas(int* p, int cmp, int val) {
   int old;
   asm volatile("atom.acq_rel.gpu.global.cas.b32 %0, [%1], %2, %3;" : "=r"(old) : "l"(p), "r"(cmp), "r"(val) : "memory");
@@ -504,7 +541,10 @@ struct Shared {
   float2 wp[kWarps];
   float rowM[2 * SPEC_MAX_GAMMA + 1];
   float rowInvS[2 * SPEC_MAX_GAMMA + 1];
-  int rowArg[SPEC_MAX_GAMMA + 1];
+  int rowArg[kMaxRows];
+  int tpar[kMaxRows], ttok[kMaxRows], tpath[kMaxRows];   // tree verification
+  unsigned char tacc[kMaxRows], tdep[kMaxRows];
+  int tbest;
   float pd[SPEC_MAX_GAMMA], qd[SPEC_MAX_GAMMA];
   int last, go, m, flags, flags_extra, owner, token, lastpos;
   unsigned taken[2];
@@ -927,6 +967,72 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
   }
   if (tid < 2) sm.taken[tid] = 0u;
   __syncthreads();
+  if (!kMixed && a.parents) {
+    // Greedy tree verification (tutorial §5.3): node j (1..g) carries draft_tokens[b][j-1]
+    // and hangs below parents[b][j-1] (0 is the root); it is accepted iff its parent is and
+    // its token is the argmax of the parent's row.  The path ends at the deepest accepted
+    // node, the lowest index among equal depths.  Parents precede their children, so one
+    // pass in index order settles every node.
+    for (int j = tid; j < g; j += kThreads) {
+      sm.tpar[j + 1] = a.parents[int64_t(b) * gmax + j];
+      sm.ttok[j + 1] = a.draft_tokens[int64_t(b) * gmax + j];
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int f = sq.flags | sm.flags_extra;
+      sm.tacc[0] = 1;
+      sm.tdep[0] = 0;
+      int best = 0, bestd = 0;
+      for (int j = 1; j <= g; ++j) {
+        const int par = sm.tpar[j], d = sm.ttok[j];
+        sm.tacc[j] = 0;
+        sm.tdep[j] = 0;
+        if (par < 0 || par >= j) {
+          f |= SPEC_ST_BAD_TREE;
+          continue;
+        }
+        const int dep = sm.tdep[par] + 1;
+        sm.tdep[j] = (unsigned char)dep;
+        if (!sm.tacc[par]) continue;
+        if (d < 0 || int64_t(d) >= a.V) {
+          f |= SPEC_ST_BAD_DRAFT;
+          continue;
+        }
+        if (d == sm.rowArg[par]) {
+          sm.tacc[j] = 1;
+          if (dep > bestd) {
+            best = j;
+            bestd = dep;
+          }
+        }
+      }
+      int j = best;
+      for (int i = bestd - 1; i >= 0; --i) {
+        sm.tpath[i] = j;
+        j = sm.tpar[j];
+      }
+      sm.m = bestd;
+      sm.flags = f;
+      sm.tbest = best;
+    }
+    __syncthreads();
+    const int m = sm.m;
+    for (int i = tid; i <= gmax; i += kThreads) {
+      int v = -1;
+      if (i < m) v = sm.ttok[sm.tpath[i]];
+      else if (i == m) v = sm.rowArg[sm.tbest];
+      a.out_tokens[int64_t(b) * (gmax + 1) + i] = v;
+    }
+    if (a.path_nodes)
+      for (int i = tid; i < gmax; i += kThreads) a.path_nodes[int64_t(b) * gmax + i] = i < m ? sm.tpath[i] : -1;
+    if (tid == 0) {
+      a.num_accepted[b] = m;
+      if (a.status) a.status[b] = sm.flags;
+      w.cnt[b] = 0;
+    }
+    __syncthreads();
+    return;
+  }
   if (warp == 0) {
     bool acc = false;
     const bool valid = lane < g && d >= 0 && int64_t(d) < a.V;
@@ -1041,9 +1147,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
     // ---------------- A unit: row chunk x of row slot y -------------------------------------
     const int b = grp, slot = y, c = x;
     if (b >= geo.b1) return;
-    // The row's address does not depend on the sequence's num_draft and temperature: its
-    // first two passes are started before those arrive.  A row past num_draft (or a draft
-    // row of a greedy sequence) is inside the caller's tensors; its passes are dropped.
+    // A row past num_draft (or a draft row of a greedy sequence) is never read: in ragged or
+    // mixed batches such rows can be a large share of the grid.
     const raw* row = slot <= a.gmax
                          ? target_row<E>(a, b, slot)
                          : static_cast<const raw*>(a.draft) + (int64_t(b) * a.gmax + (slot - a.gmax - 1)) * a.V;
@@ -1055,12 +1160,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
     };
     constexpr bool kRegs = kPrefetch && !(kRing > 0 && kVec);
     Tile<E, kVec> t0, t1;
+    const Seq<E, kMixed> sq(a, b);
+    if (!sq.slot_valid(slot, a.gmax)) return;
     if constexpr (kRegs) {
       if (lo < hi) fetch(t0, lo);
       if (lo + kPass < hi) fetch(t1, lo + kPass);
     }
-    const Seq<E, kMixed> sq(a, b);
-    if (!sq.slot_valid(slot, a.gmax)) return;
     // the logit at this row's draft id, if it lies in this chunk: fetched once, up front
     const int i = slot <= a.gmax ? slot : slot - a.gmax - 1;
     bool has_d = false, no_d = false;
@@ -1073,9 +1178,15 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
     }
     float rm = -INFINITY, rs = 0.f;
     int ri = INT_MAX;
+    constexpr bool kKeep = kVec && !kMixed;   // the greedy-only kernel has the registers to spare
+    KeptTile<E> kept;
     auto consume = [&](const Tile<E, kVec>& t, int64_t e0) {
-      if (sq.sampling) thread_stats(t, sq.k, rm, rs);
-      else tile_argmax(t, e0, tid, rm, ri);
+      if constexpr (kKeep) {
+        kept.offer(t, e0);
+      } else {
+        if (sq.sampling) thread_stats(t, sq.k, rm, rs);
+        else tile_argmax(t, e0, tid, rm, ri);
+      }
     };
     if constexpr (kRing > 0 && kVec) {
       // passes staged through a ring of kRing shared-memory stages by bulk copies: thread 0
@@ -1139,6 +1250,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
         consume(t, e0);
       }
     }
+    if constexpr (kKeep) kept.settle(tid, rm, ri);
     if (sq.sampling) warp_stats(rm, rs, sq.k);
     else warp_argmax(rm, ri);
     if (lane == 0) sm.wp[warp] = make_float2(rm, sq.sampling ? rs : __int_as_float(ri));
@@ -1433,7 +1545,7 @@ int dispatch_on(const Args& a, int dtype, void* ws, size_t ws_bytes, void* strea
 using namespace specverify;
 
 extern "C" size_t spec_verify_workspace_bytes(int B, int gmax, int V, int dtype) {
-  if (B < 0 || gmax < 0 || gmax > SPEC_MAX_GAMMA || V < 1 || (dtype != SPEC_BF16 && dtype != SPEC_F32)) return 0;
+  if (B < 0 || gmax < 0 || gmax > SPEC_MAX_TREE_NODES || V < 1 || (dtype != SPEC_BF16 && dtype != SPEC_F32)) return 0;
   return ws_required(B, gmax, V);
 }
 
@@ -1549,6 +1661,43 @@ extern "C" int spec_verify_sample_split(const void* saved_logits, const void* bl
   return verify_sample(saved_logits, block_logits, draft_logits, dtype, draft_tokens, num_draft, temperature,
                        u_accept, u_sample, B, gmax, V, out_tokens, num_accepted, diag, status, workspace,
                        workspace_bytes, stream);
+}
+
+extern "C" int spec_verify_tree_greedy(const void* target_logits, int dtype, const int32_t* node_tokens,
+                                       const int32_t* node_parents, const int32_t* num_nodes, int B, int nmax,
+                                       int V, int32_t* out_tokens, int32_t* num_accepted, int32_t* path_nodes,
+                                       int32_t* status, void* workspace, size_t workspace_bytes, void* stream) {
+  clear_error();
+  if (dtype != SPEC_BF16 && dtype != SPEC_F32) {
+    set_error("unknown dtype code %d", dtype);
+    return SPEC_EDTYPE;
+  }
+  if (B < 0 || V < 1 || V > (1 << 30) || nmax < 0) {
+    set_error("bad sizes B=%d nmax=%d V=%d", B, nmax, V);
+    return SPEC_EINVAL;
+  }
+  if (nmax > SPEC_MAX_TREE_NODES) {
+    set_error("nmax=%d exceeds SPEC_MAX_TREE_NODES=%d", nmax, SPEC_MAX_TREE_NODES);
+    return SPEC_ENOSPACE;
+  }
+  if (B == 0) return SPEC_OK;
+  if (!target_logits || !out_tokens || !num_accepted || (nmax > 0 && (!node_tokens || !node_parents))) {
+    set_error("null required pointer");
+    return SPEC_EINVAL;
+  }
+  Args a = {};
+  a.target = target_logits;
+  a.draft_tokens = node_tokens;
+  a.parents = node_parents;
+  a.path_nodes = path_nodes;
+  a.num_draft = num_nodes;
+  a.V = V;
+  a.B = B;
+  a.gmax = nmax;
+  a.out_tokens = out_tokens;
+  a.num_accepted = num_accepted;
+  a.status = status;
+  return dispatch_on<false>(a, dtype, workspace, workspace_bytes, stream);
 }
 
 // ------------------------------------------------------------------------------------------

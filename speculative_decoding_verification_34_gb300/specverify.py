@@ -53,6 +53,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.spec_verify_sample_split.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, sz, sz, sz, vp, vp, vp, vp, vp,
                                              size_t, vp]
     lib.spec_verify_sample_split.restype = i32
+    lib.spec_verify_tree_greedy.argtypes = [vp, i32, vp, vp, vp, sz, sz, sz, vp, vp, vp, vp, vp, size_t, vp]
+    lib.spec_verify_tree_greedy.restype = i32
     lib.spec_verify_sample_static.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, sz, sz, sz, vp, vp, vp, vp, vp]
     lib.spec_verify_sample_static.restype = i32
     lib.spec_verify_workspace_bytes.argtypes = [sz, sz, sz, i32]
@@ -170,6 +172,47 @@ def spec_verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor,
         _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
         _ptr(diag, "diag", torch.float32, (B, 2 * gmax + 1)),
         _ptr(status, "status", torch.int32, (B,)), wsp, wsn, _stream(stream)))
+
+
+def spec_verify_tree_greedy(target_logits: torch.Tensor, node_tokens: torch.Tensor,
+                            node_parents: torch.Tensor, num_nodes: Optional[torch.Tensor],
+                            out_tokens: torch.Tensor, num_accepted: torch.Tensor,
+                            path_nodes: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                            workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Greedy verification of draft trees: target_logits [B][nmax+1][V] (row j after node j),
+    node_tokens and node_parents [B][nmax] (node j+1's token and parent, parent < j+1)."""
+    B, np1, V = target_logits.shape
+    nmax = np1 - 1
+    lib = load_library()
+    code = _dtype_code(target_logits)
+    ws, wsp, wsn = _ws(workspace, B, nmax, V, code, target_logits.device)
+    _check(lib.spec_verify_tree_greedy(
+        _ptr(target_logits, "target_logits"), code,
+        _ptr(node_tokens, "node_tokens", torch.int32, (B, nmax)),
+        _ptr(node_parents, "node_parents", torch.int32, (B, nmax)),
+        _ptr(num_nodes, "num_nodes", torch.int32, (B,)), B, nmax, V,
+        _ptr(out_tokens, "out_tokens", torch.int32, (B, nmax + 1)),
+        _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
+        _ptr(path_nodes, "path_nodes", torch.int32, (B, nmax)),
+        _ptr(status, "status", torch.int32, (B,)), wsp, wsn, _stream(stream)))
+
+
+def prepare_verify_tree_greedy(target_logits, node_tokens, node_parents, num_nodes, out_tokens, num_accepted,
+                               path_nodes=None, status=None, workspace=None, stream=None) -> "_Prepared":
+    B, np1, V = target_logits.shape
+    nmax = np1 - 1
+    lib = load_library()
+    ws, wsp, wsn = _ws(workspace, B, nmax, V, _dtype_code(target_logits), target_logits.device)
+    args = (_ptr(target_logits, "target_logits"), _dtype_code(target_logits),
+            _ptr(node_tokens, "node_tokens", torch.int32, (B, nmax)),
+            _ptr(node_parents, "node_parents", torch.int32, (B, nmax)),
+            _ptr(num_nodes, "num_nodes", torch.int32, (B,)), B, nmax, V,
+            _ptr(out_tokens, "out_tokens", torch.int32, (B, nmax + 1)),
+            _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
+            _ptr(path_nodes, "path_nodes", torch.int32, (B, nmax)),
+            _ptr(status, "status", torch.int32, (B,)), wsp, wsn, _stream(stream))
+    keep = (target_logits, node_tokens, node_parents, num_nodes, out_tokens, num_accepted, path_nodes, status, ws)
+    return _Prepared(lib.spec_verify_tree_greedy, args, keep)
 
 
 def _split_shapes(saved_logits, block_logits):

@@ -256,4 +256,75 @@ def large_batch_128k(seed: int = 0, B: int = 1024) -> Workload:
                              draft_sigma=sig, temperature=1.0, equal_mask=eq)
 
 
-WORKLOADS = {1: small_fp32, 2: greedy_32k, 3: sampling_128k, 4: mixed_152k, 5: large_batch_128k}
+@dataclasses.dataclass
+class TreeWorkload:
+    """Draft trees for greedy tree verification.  Node j (1..num_nodes[b]) carries
+    node_tokens[b][j-1] and hangs below node_parents[b][j-1] < j (0 is the root)."""
+    name: str
+    dtype: str
+    B: int
+    nmax: int
+    V: int
+    target: np.ndarray              # [B, nmax+1, V]: row j follows node j
+    node_tokens: np.ndarray         # int32 [B, nmax]
+    node_parents: np.ndarray        # int32 [B, nmax]
+    num_nodes: np.ndarray           # int32 [B]
+    kv_len: np.ndarray              # int32 [B]
+
+    def verified_rows(self) -> int:
+        """Draft nodes judged per call."""
+        return int(self.num_nodes.sum())
+
+    def algorithmic_bytes(self) -> int:
+        es = 2 if self.dtype == "bf16" else 4
+        return int((self.num_nodes.astype(np.int64) + 1).sum()) * self.V * es
+
+
+def tree_workload(name: str, *, cfg: int, seed: int, B: int, nmax: int, V: int, dtype: str = "bf16",
+                  sigma: float = 3.0, alpha: float = 0.7, width: int = 4, num_nodes=None) -> TreeWorkload:
+    """Draft trees with a planted target argmax.
+
+    Node j's parent is uniform among nodes max(0, j-width)..j-1, so trees branch and deepen
+    like the candidate trees of tree drafters.  Every target row is N(0, sigma^2) clipped to
+    +-6 sigma, with 6 sigma + 1 written at a uniformly chosen id (its argmax by
+    construction).  A node copies its parent row's planted id with probability alpha unless a
+    sibling already holds it; otherwise it takes a uniform id that no sibling holds.  Rows past
+    a sequence's node count are NaN.
+    """
+    (r_t, r_g, r_p, r_a, r_o, r_kv) = _streams(cfg, seed, 6)
+    hi = np.float32(6.0 * sigma)
+    n_arr = np.full(B, nmax, dtype=np.int32) if num_nodes is None else np.asarray(num_nodes, dtype=np.int32)
+    tgt = _alloc((B, nmax + 1, V), dtype)
+    toks = np.full((B, nmax), -1, dtype=np.int32)
+    pars = np.full((B, nmax), -1, dtype=np.int32)
+    for b in range(B):
+        n = int(n_arr[b])
+        t32 = np.clip(r_t.standard_normal((n + 1, V), dtype=np.float32) * np.float32(sigma), -hi, hi)
+        planted = r_g.integers(0, V, size=n + 1)
+        t32[np.arange(n + 1), planted] = hi + np.float32(1.0)
+        tgt[b, : n + 1] = _pack(t32, dtype)
+        taken = {}
+        for j in range(1, n + 1):
+            p = int(r_p.integers(max(0, j - width), j))
+            sib = taken.setdefault(p, set())
+            a = int(planted[p])
+            if a not in sib and r_a.random() < alpha:
+                t = a
+            else:
+                t = int(r_o.integers(0, V))
+                while t == a or t in sib:
+                    t = int(r_o.integers(0, V))
+            sib.add(t)
+            toks[b, j - 1] = t
+            pars[b, j - 1] = p
+    kv = r_kv.integers(512, 8193, size=B).astype(np.int32)
+    return TreeWorkload(name, dtype, B, nmax, V, tgt, toks, pars, n_arr, kv)
+
+
+def tree_63_128k(seed: int = 0) -> TreeWorkload:
+    """Tree workload: B=32 sequences, 63-node draft trees, V=128256, bf16 ~ N(0,3^2) with a
+    planted argmax per row; a node copies its parent's planted id with probability 0.7."""
+    return tree_workload("tree-B32-n63-V128256-bf16", cfg=6, seed=seed, B=32, nmax=63, V=128256)
+
+
+WORKLOADS = {1: small_fp32, 2: greedy_32k, 3: sampling_128k, 4: mixed_152k, 5: large_batch_128k, 6: tree_63_128k}

@@ -70,12 +70,12 @@ def test_host_argument_checks(lib):
     assert c(FAKE, 4, FAKE, None, 1, FAKE, 3, None, None, 10, None, None) == 1   # partial history args
     assert c(FAKE, 4, FAKE, None, 1, FAKE, 3, FAKE, FAKE, 0, None, None) == 1    # cap < 1
     assert c(None, 4, FAKE, None, 1, None, 3, None, None, 0, None, None) == 1
-    assert c(FAKE, 4, FAKE, None, 1, None, 40, None, None, 0, None, None) == 3
+    assert c(FAKE, 4, FAKE, None, 1, None, 64, None, None, 0, None, None) == 3
     assert c(FAKE, 0, FAKE, None, 1, None, 3, None, None, 0, None, None) == 0
     assert c(None, 0, None, None, 1, None, 3, None, None, 0, None, None) == 0
     s = lib.spec_apply_stops
     assert s(None, FAKE, 4, 3, 0, None, None, None) == 1 and s(FAKE, None, 4, 3, 0, None, None, None) == 1
-    assert s(FAKE, FAKE, -1, 3, 0, None, None, None) == 1 and s(FAKE, FAKE, 4, 40, 0, None, None, None) == 3
+    assert s(FAKE, FAKE, -1, 3, 0, None, None, None) == 1 and s(FAKE, FAKE, 4, 64, 0, None, None, None) == 3
     assert s(None, None, 0, 3, 0, None, None, None) == 0
     assert greedy(lib, target=None, toks=None, out=None, macc=None, B=0) == 0
     assert sample(lib, target=None, draft=None, temp=None, ua=None, us=None, B=0) == 0
@@ -99,6 +99,20 @@ def test_split_layout_argument_checks(lib):
     assert lib.spec_launch_count() == n0
 
 
+def test_tree_argument_checks(lib):
+    n0 = lib.spec_launch_count()
+    t = lambda tgt=FAKE, toks=FAKE, par=FAKE, B=4, nmax=7, V=100, dtype=0: lib.spec_verify_tree_greedy(
+        tgt, dtype, toks, par, None, B, nmax, V, FAKE, FAKE, None, None, FAKE, 8, None)
+    assert t(dtype=5) == 2
+    assert t(B=-1) == 1 and t(nmax=-1) == 1 and t(V=0) == 1
+    assert t(nmax=64) == 3 and b"SPEC_MAX_TREE_NODES" in lib.spec_last_error()
+    assert t(tgt=None) == 1 and t(toks=None) == 1 and t(par=None) == 1
+    assert t(toks=None, par=None, nmax=0) == 3 and b"workspace" in lib.spec_last_error()
+    assert t(tgt=None, toks=None, par=None, B=0) == 0
+    assert lib.spec_launch_count() == n0
+    assert sv.spec_verify_workspace_bytes(4, 63, 100) > 0 and sv.spec_verify_workspace_bytes(4, 64, 100) == 0
+
+
 def test_plan_splits_vocabulary(lib):
     for V in [1, 3, 1024, 4096, 4097, 32000, 50000, 128256, 151936, 1 << 20]:
         cl, chunk = sv.spec_verify_plan(V)
@@ -116,7 +130,7 @@ def test_workspace_size(lib):
     assert n < 1 << 20
     assert sv.spec_verify_workspace_bytes(128, 4, 128256) == sv.spec_verify_workspace_bytes(128, 4, 128256, 1)
     assert sv.spec_verify_workspace_bytes(-1, 4, 100) == 0
-    assert sv.spec_verify_workspace_bytes(4, 40, 100) == 0
+    assert sv.spec_verify_workspace_bytes(4, 64, 100) == 0   # beyond a tree call's 63 nodes
     # too small a workspace is refused on the host, before any CUDA call
     assert lib.spec_verify_greedy(FAKE, 0, FAKE, None, 4, 3, 100, FAKE, FAKE, None, FAKE, 8, None) == 3
     assert b"workspace" in lib.spec_last_error()
@@ -131,7 +145,8 @@ def test_binding_arity_matches_header(lib):
         text += re.sub(r"/\*.*?\*/", "", open(h, encoding="utf-8").read(), flags=re.S)
     for name in ("spec_verify_greedy", "spec_verify_sample", "spec_commit_kv_lengths",
                  "spec_verify_workspace_bytes", "spec_verify_plan", "spec_verify_sample_static",
-                 "spec_apply_stops", "spec_verify_greedy_split", "spec_verify_sample_split"):
+                 "spec_apply_stops", "spec_verify_greedy_split", "spec_verify_sample_split",
+                 "spec_verify_tree_greedy"):
         m = re.search(r"\b" + name + r"\s*\(([^)]*)\)", text)
         params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
         assert len(getattr(lib, name).argtypes) == len(params), name
