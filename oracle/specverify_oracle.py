@@ -36,6 +36,14 @@ Readings where the pages leave a step open (each also listed in the design doc):
     num_draft outside [0, gmax] is clamped (status bit 4).
   * Temperature T <= 0 (or NaN) marks a greedy sequence; otherwise p = softmax(P/T)
     and q = softmax(Q/T), the same T on both sides.
+  * Truncated sampling ([NXM] and [KB] §10: temperature, top-p or any other logits processing
+    that changes the distribution must show in p and q; [TUT] §7's pseudocode leaves top-p
+    out).  The same truncation is applied to both sides, each to its own distribution at T:
+    top-k keeps the ids whose logit is at least the k-th largest logit (ties kept; k <= 0 or
+    k >= V: off); top-p then keeps, of those, the ids whose logit is at least the largest
+    value t with mass(logit >= t) >= top_p * mass(kept by top-k) (ties kept; top_p outside
+    (0, 1): off); the kept probabilities are renormalised.  Acceptance, residual and the
+    bonus draw then use these p' and q'.
   * Tree verification ([TUT] §5.3: the target checks every node of a draft tree in one
     forward and keeps the longest accepted root-to-leaf path; [KB] §01, §06: a tree has its
     own rules, and its branches need their own cache bookkeeping).  The pages give no
@@ -88,6 +96,38 @@ def softmax_at_temperature(logits: np.ndarray, T: float) -> np.ndarray:
     z = z - np.max(z)
     e = np.exp(z)
     return e / np.sum(e)
+
+
+def truncated_distribution(logits: np.ndarray, T: float, top_k: int = 0, top_p: float = 1.0):
+    """p' = softmax(L/T) restricted to the ids top-k and then top-p keep, renormalised.
+
+    top-k (0 < k < V) keeps the ids whose logit is >= the k-th largest logit (ties kept).
+    top-p (0 < top_p < 1) keeps, of those, the ids whose logit is >= t*, the largest logit
+    value t among them with sum(p over kept ids with logit >= t) >= top_p * sum(p over kept
+    ids) (ties at t* kept).  Returns (p', margin): margin is how far the top-p crossing sits
+    from its target, |cum(t*) - target| and |cum(next value above t*) - target|, relative to
+    the kept mass (inf when top-p is off), used only to flag near-ties in parity tests.
+    """
+    p = softmax_at_temperature(logits, T)
+    V = len(logits)
+    keep = np.ones(V, dtype=bool)
+    if 0 < top_k < V:
+        tau_k = np.sort(logits)[::-1][top_k - 1]
+        keep &= logits >= tau_k
+    margin = math.inf
+    if 0.0 < top_p < 1.0:
+        vals, inv = np.unique(logits[keep], return_inverse=True)     # ascending distinct values
+        mass = np.bincount(inv, weights=p[keep], minlength=len(vals))
+        cum = np.cumsum(mass[::-1])                                   # from the largest value down
+        total = float(cum[-1])
+        target = top_p * total
+        j = int(np.flatnonzero(cum >= target)[0])
+        tau_p = vals[::-1][j]
+        keep &= logits >= tau_p
+        above = float(cum[j - 1]) if j > 0 else 0.0
+        margin = min(float(cum[j]) - target, target - above) / total
+    w = np.where(keep, p, 0.0)
+    return w / np.sum(w), margin
 
 
 def greedy_argmax(logits: np.ndarray) -> int:
@@ -179,13 +219,15 @@ def verify_greedy_sequence(target: np.ndarray, drafts: np.ndarray, gamma: int) -
 
 
 def verify_sample_sequence(target: np.ndarray, draft: np.ndarray, drafts: np.ndarray,
-                           gamma: int, T: float, u_accept: np.ndarray, u_sample: float) -> SequenceResult:
+                           gamma: int, T: float, u_accept: np.ndarray, u_sample: float,
+                           top_k: int = 0, top_p: float = 1.0) -> SequenceResult:
     """Sampling verification of one sequence ([TUT] §7.1-§7.3; [APP] Steps 3-4; [KB] §05-§06).
 
     For i = 0..gamma-1, left to right: p_i = softmax(P_i/T), q_i = softmax(Q_i/T),
     accept d_i iff u_accept[i] < min(1, p_i(d_i)/q_i(d_i)); stop at the first rejection
     m.  On a rejection the correction is drawn from max(p_m - q_m, 0)/R with u_sample; on
-    full acceptance the bonus token is drawn from p_gamma with u_sample.
+    full acceptance the bonus token is drawn from p_gamma with u_sample.  With top_k / top_p
+    set, p and q are the truncated distributions (truncated_distribution) on both sides.
     """
     V = target.shape[1]
     status = 0
@@ -194,9 +236,18 @@ def verify_sample_sequence(target: np.ndarray, draft: np.ndarray, drafts: np.nda
     q_d: List[float] = []
     margins: List[float] = []
     p_m = q_m = None
+    truncated = (0 < top_k < V) or (0.0 < top_p < 1.0)
+
+    def dist(row):
+        if not truncated:
+            return softmax_at_temperature(row, T)
+        d, tm = truncated_distribution(row, T, top_k, top_p)
+        margins.append(tm)
+        return d
+
     for i in range(gamma):
-        p = softmax_at_temperature(target[i], T)
-        q = softmax_at_temperature(draft[i], T)
+        p = dist(target[i])
+        q = dist(draft[i])
         d = int(drafts[i])
         if 0 <= d < V:
             pd, qd = float(p[d]), float(q[d])
@@ -224,7 +275,7 @@ def verify_sample_sequence(target: np.ndarray, draft: np.ndarray, drafts: np.nda
             tok, smargin, mass = inverse_cdf(p_m, float(u_sample))
             mass = 0.0
     else:
-        p_bonus = softmax_at_temperature(target[gamma], T)
+        p_bonus = dist(target[gamma])
         tok, smargin, mass = inverse_cdf(p_bonus, float(u_sample))
     toks = [int(x) for x in drafts[:m]] + [tok]
     return SequenceResult(toks, m, status, gamma, False, p_d, q_d, mass, margins, smargin)
@@ -233,7 +284,8 @@ def verify_sample_sequence(target: np.ndarray, draft: np.ndarray, drafts: np.nda
 def verify_batch(target: np.ndarray, draft: Optional[np.ndarray], dtype: str,
                  draft_tokens: np.ndarray, num_draft: np.ndarray, temperature: Optional[np.ndarray],
                  u_accept: Optional[np.ndarray], u_sample: Optional[np.ndarray],
-                 seqs=None) -> List[SequenceResult]:
+                 seqs=None, top_k: Optional[np.ndarray] = None,
+                 top_p: Optional[np.ndarray] = None) -> List[SequenceResult]:
     """Verify every sequence (or the listed ones) of a batch.
 
     target [B, gmax+1, V], draft [B, gmax, V] (bf16 bits or float32); a sequence whose
@@ -254,7 +306,9 @@ def verify_batch(target: np.ndarray, draft: Optional[np.ndarray], dtype: str,
             r = verify_greedy_sequence(P, draft_tokens[b], g)
         else:
             Q = widen(draft[b, :g], dtype) if g > 0 else np.zeros((0, V))
-            r = verify_sample_sequence(P, Q, draft_tokens[b], g, T, u_accept[b], float(u_sample[b]))
+            r = verify_sample_sequence(P, Q, draft_tokens[b], g, T, u_accept[b], float(u_sample[b]),
+                                       0 if top_k is None else int(top_k[b]),
+                                       1.0 if top_p is None else float(top_p[b]))
         r.status |= clamped
         out.append(r)
     return out

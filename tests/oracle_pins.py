@@ -62,7 +62,7 @@ def step(P, Q, d, T, ua, us):
                                     np.asarray(ua, dtype=np.float64), us)
 
 
-def emitted_law(P, Q, d, T):
+def emitted_law(P, Q, d, T, step=step):
     """{tuple(emitted tokens): probability} of one step with drafts d, integrating over
     the uniforms by probing the oracle."""
     g = len(d)
@@ -469,3 +469,115 @@ def check_tree_ties_and_invalid_nodes():
     # node 2 names itself as its parent; node 3 hangs below it
     res = O.verify_tree_greedy_sequence(rows, np.array([7, 2, 3]), np.array([0, 2, 2]), 3)
     assert res.status == O.ST_BAD_TREE | O.ST_BAD_DRAFT and res.path == [] and res.tokens == [2], res
+
+
+# ---------------------------------------------------------------------------------------
+# truncated sampling (NXM / KB §10: truncation must show in p and q): top-k, then top-p
+# ---------------------------------------------------------------------------------------
+
+def kept_by_counting(logits, T, top_k, top_p):
+    """The kept set stated element by element: v survives top-k iff fewer than k logits are
+    strictly larger; it survives top-p iff the top-k-kept mass strictly above its logit is
+    below top_p times the whole top-k-kept mass (it is needed to reach the target)."""
+    x = np.asarray(logits, dtype=np.float64)
+    V = len(x)
+    p = softmax_T(x, T)
+    keep = np.ones(V, dtype=bool)
+    if 0 < top_k < V:
+        keep = np.array([np.sum(x > x[v]) < top_k for v in range(V)])
+    if 0.0 < top_p < 1.0:
+        mass_k = np.sum(p[keep])
+        keep = keep & np.array([np.sum(p[keep & (x > x[v])]) < top_p * mass_k for v in range(V)])
+    return keep
+
+
+def check_truncation_against_counting(cases=300, seed=21):
+    rng = np.random.default_rng(seed)
+    for c in range(cases):
+        V = int(rng.integers(1, 40))
+        x = rng.normal(0, 2, size=V)
+        if c % 3 == 0:
+            x = np.round(x * 2) / 2            # many exact ties, as bf16 logits have
+        T = float(rng.choice([0.5, 1.0, 1.7]))
+        k = int(rng.choice([0, 1, 2, 5, V, V + 3, -1]))
+        tp = float(rng.choice([1.0, 0.0, 0.3, 0.75, 0.95, 0.999, 1.5]))
+        want = kept_by_counting(x, T, k, tp)
+        got, _ = O.truncated_distribution(x, T, k, tp)
+        assert np.array_equal(got > 0, want), (x, T, k, tp, got, want)
+        p = softmax_T(x, T)
+        assert np.allclose(got[want], p[want] / p[want].sum(), rtol=1e-12, atol=0)
+
+
+def check_top_k_one_is_greedy(cases=200, seed=22):
+    """top_k = 1 leaves one id on each side, so sampling verification with drafts from q'
+    (its argmax) is greedy verification, for any uniforms."""
+    rng = np.random.default_rng(seed)
+    for _ in range(cases):
+        V, g = int(rng.integers(2, 30)), int(rng.integers(0, 6))
+        P = rng.normal(0, 2, size=(g + 1, V))
+        Q = P[:g] + rng.normal(0, 1.0, size=(g, V))
+        d = np.argmax(Q, axis=1) if g else np.zeros(0, dtype=np.int64)
+        ua, us = rng.random(g), float(rng.random())
+        s1 = O.verify_sample_sequence(P, Q, d, g, float(rng.choice([0.6, 1.0])), ua, us, top_k=1)
+        s0 = O.verify_greedy_sequence(P, d, g)
+        assert s1.tokens == s0.tokens and s1.m == s0.m, (s1, s0)
+
+
+def check_truncation_off_switches(seed=23):
+    rng = np.random.default_rng(seed)
+    V, g = 17, 3
+    P = rng.normal(0, 2, size=(g + 1, V))
+    Q = P[:g] + rng.normal(0, 1.0, size=(g, V))
+    d = rng.integers(0, V, size=g)
+    ua, us = rng.random(g), 0.37
+    base = O.verify_sample_sequence(P, Q, d, g, 0.9, ua, us)
+    for k, tp in [(0, 1.0), (-3, 1.0), (V, 1.0), (V + 1, 2.0), (0, 0.0), (0, -0.5)]:
+        r = O.verify_sample_sequence(P, Q, d, g, 0.9, ua, us, top_k=k, top_p=tp)
+        assert r.tokens == base.tokens and r.m == base.m and r.p_draft == base.p_draft, (k, tp)
+
+
+def check_truncated_joint_law(V, gamma, T, top_k, top_p, seed, tol=1e-9):
+    """Brute force with truncation on both sides: drafts drawn from the draft's truncated
+    distribution, the step's emitted prefix extended by the target's truncated sampling,
+    gives exactly the truncated target's autoregressive law."""
+    logits = random_tables(V, gamma + 1, seed)
+
+    def tr(x):
+        keep = kept_by_counting(x, T, top_k, top_p)
+        p = softmax_T(x, T) * keep
+        return p / p.sum()
+
+    def tstep(P, Q, d, T_, ua, us):
+        return O.verify_sample_sequence(P, Q, np.asarray(d, dtype=np.int64), len(d), T_,
+                                        np.asarray(ua, dtype=np.float64), us, top_k=top_k, top_p=top_p)
+
+    n = gamma + 1
+    ext = {}
+    for d in itertools.product(range(V), repeat=gamma):
+        qd = 1.0
+        for i in range(gamma):
+            qd *= tr(logits("draft", d[:i]))[d[i]]
+        if qd == 0.0:
+            continue
+        P = np.stack([logits("target", d[:i]) for i in range(gamma + 1)])
+        Q = np.stack([logits("draft", d[:i]) for i in range(gamma)])
+        for toks, pr in emitted_law(P, Q, list(d), T, step=tstep).items():
+            frontier = {toks: qd * pr}
+            while True:
+                nxt = {}
+                for sq, w in frontier.items():
+                    if len(sq) == n:
+                        ext[sq] = ext.get(sq, 0.0) + w
+                        continue
+                    pt = tr(logits("target", sq))
+                    for v in range(V):
+                        if pt[v] > 0:
+                            nxt[sq + (v,)] = nxt.get(sq + (v,), 0.0) + w * pt[v]
+                if not nxt:
+                    break
+                frontier = nxt
+    for sq in itertools.product(range(V), repeat=n):
+        want = 1.0
+        for j in range(n):
+            want *= tr(logits("target", sq[:j]))[sq[j]]
+        assert abs(ext.get(sq, 0.0) - want) < tol, (sq, ext.get(sq, 0.0), want)

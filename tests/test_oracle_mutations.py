@@ -46,6 +46,34 @@ def _stops_last_token_only(out_tokens, m, eos_id, max_new=None):
 _apply_stops = O.apply_stops
 
 
+_truncated = O.truncated_distribution
+
+
+def _trunc_variant(full_mass=False, strict_k=False):
+    # a copy of the truncation with one planted mistake: top-p's target taken over the whole
+    # distribution instead of the top-k-kept mass, or top-k dropping the ties at its threshold
+    def run(logits, T, top_k=0, top_p=1.0):
+        p = O.softmax_at_temperature(logits, T)
+        V = len(logits)
+        keep = np.ones(V, dtype=bool)
+        if 0 < top_k < V:
+            tau = np.sort(logits)[::-1][top_k - 1]
+            keep &= (logits > tau) if strict_k else (logits >= tau)
+            if not keep.any():
+                keep[int(np.argmax(logits))] = True
+        if 0.0 < top_p < 1.0:
+            vals, inv = np.unique(logits[keep], return_inverse=True)
+            mass = np.bincount(inv, weights=p[keep], minlength=len(vals))
+            cum = np.cumsum(mass[::-1])
+            target = top_p * (1.0 if full_mass else float(cum[-1]))
+            hits = np.flatnonzero(cum >= target)
+            j = int(hits[0]) if hits.size else len(cum) - 1
+            keep &= logits >= vals[::-1][j]
+        w = np.where(keep, p, 0.0)
+        return w / np.sum(w), np.inf
+    return run
+
+
 def _tree_variant(own_row=False, last_tie=False):
     # a copy of the tree verification with one planted mistake: the node's own row judged
     # instead of its parent's, or the higher index winning equal depths
@@ -91,6 +119,8 @@ MUTATIONS = {
     "stops_budget_ignored": ("apply_stops", lambda o, m, e, n=None: _apply_stops(o, m, e, None)),
     "tree_own_row": ("verify_tree_greedy_sequence", _tree_variant(own_row=True)),
     "tree_last_index_tie": ("verify_tree_greedy_sequence", _tree_variant(last_tie=True)),
+    "top_p_full_mass": ("truncated_distribution", _trunc_variant(full_mass=True)),
+    "top_k_drops_ties": ("truncated_distribution", _trunc_variant(strict_k=True)),
 }
 
 
@@ -102,7 +132,9 @@ def _pins_pass():
               lambda: pins.check_joint_law(3, 1, 1.0, 1),
               pins.check_stops_match_step_by_step,
               pins.check_tree_figure, pins.check_tree_chain_equals_chain,
-              pins.check_tree_matches_greedy_walk, pins.check_tree_ties_and_invalid_nodes]
+              pins.check_tree_matches_greedy_walk, pins.check_tree_ties_and_invalid_nodes,
+              pins.check_truncation_against_counting, pins.check_top_k_one_is_greedy,
+              lambda: pins.check_truncated_joint_law(4, 2, 0.8, 0, 0.7, 32)]
     for c in checks:
         try:
             c()

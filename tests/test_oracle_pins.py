@@ -218,3 +218,21 @@ def test_tree_batch_clamps_node_counts():
                               np.array([5, -1]))
     assert res[0].n == 2 and res[0].status == O.ST_CLAMPED_GAMMA and res[0].tokens == [1, 2, 0]
     assert res[1].n == 0 and res[1].status == O.ST_CLAMPED_GAMMA and res[1].tokens == [1]
+
+
+def test_truncation_against_counting():
+    pins.check_truncation_against_counting()
+
+
+def test_top_k_one_is_greedy():
+    pins.check_top_k_one_is_greedy()
+
+
+def test_truncation_off_switches():
+    pins.check_truncation_off_switches()
+
+
+@pytest.mark.parametrize("V,gamma,T,k,tp,seed", [(4, 2, 1.0, 2, 1.0, 31), (4, 2, 0.8, 0, 0.7, 32),
+                                                  (4, 1, 1.3, 3, 0.6, 33), (3, 2, 1.0, 2, 0.9, 34)])
+def test_truncated_joint_law(V, gamma, T, k, tp, seed):
+    pins.check_truncated_joint_law(V, gamma, T, k, tp, seed)
