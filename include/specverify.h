@@ -126,6 +126,35 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits, int 
                        void* stream);
 
 /*
+ * Sampling verification with top-k / top-p truncation (the "M013" card §10 and the nxmr note:
+ * temperature, top-p or any other logits processing that changes the distribution must show
+ * in p and q).  Exactly spec_verify_sample, with p_i and q_i replaced by their truncated,
+ * renormalised versions, each side truncating its own distribution at T the same way:
+ *   top-k (0 < top_k[b] < V) keeps the ids whose logit is >= the k-th largest logit of the
+ *     row (ties kept);
+ *   top-p (0 < top_p[b] < 1) then keeps, of those, the ids whose logit is >= t*, the largest
+ *     logit t whose kept mass at or above t reaches top_p[b] times the top-k-kept mass (ties
+ *     at t* kept).
+ * Drafts should have been drawn from the truncated q (the proposer truncates too).  Acceptance,
+ * the residual max(p' - q', 0) and the bonus draw then use p' and q'; diag reports p'(d_i),
+ * q'(d_i) and the truncated residual mass.  top_k or top_p NULL (or a value outside its range)
+ * turns that truncation off for the batch (or the sequence); greedy sequences (T <= 0) are
+ * verified greedily.  bf16 logits only (SPEC_EDTYPE otherwise).
+ *
+ * Cost: the thresholds are found exactly, per row, by a radix search over the logits' 16-bit
+ * order-preserving keys: up to five passes over each row of a sampling sequence (max; one
+ * byte of the key per pass, for top-k and then for top-p), then the decisions and the draw,
+ * in three kernel launches.  The workspace is spec_verify_workspace_bytes(B, gmax, V, dtype)
+ * bytes, as for spec_verify_sample.
+ */
+int spec_verify_sample_truncated(const void* target_logits, const void* draft_logits, int dtype,
+                                 const int32_t* draft_tokens, const int32_t* num_draft,
+                                 const float* temperature, const int32_t* top_k, const float* top_p,
+                                 const float* u_accept, const float* u_sample, int B, int gmax, int V,
+                                 int32_t* out_tokens, int32_t* num_accepted, float* diag,
+                                 int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Greedy verification of a draft TREE (tutorial §5.3: the target checks every node of the
  * tree in one forward and keeps the longest accepted root-to-leaf path; card §01: a tree
  * follows its own rules).  Nodes 1..n (n = num_nodes[b], NULL: nmax) carry the draft token

@@ -155,6 +155,7 @@ __host__ __device__ inline int draw_groups(int nb, int delta, int ndefer) {
 struct __align__(16) PlanRec {   // per sequence, published by the decider for the draw
   int m, g, flags, pair;
   float mkp, invp, mkq, invq;
+  float taup, tauq;   // truncated sampling: the smallest kept logit of row m of p and of q
 };
 
 // The published flag carries what a draw unit needs to start its loads: 0 = not yet, else
@@ -610,23 +611,36 @@ struct Seq {
   __device__ __forceinline__ const raw* prow(int i, int64_t V) const { return i == 0 ? P0 : P1 + int64_t(i - 1) * V; }
 };
 
-// weights of the N elements of one vector: w = residual (or p on the bonus row), and p
-template <class E>
+// weights of the N elements of one vector: w = residual (or p on the bonus row), and p.
+// kTrunc: ids whose logit is below the row's kept threshold (taup, tauq) have probability 0.
+template <class E, bool kTrunc = false>
 __device__ __forceinline__ void weights(const uint4& vp, const uint4& vq, bool pair, float k, float mkp, float invp,
-                                        float mkq, float invq, float (&w)[E::kPerVec], float (&p)[E::kPerVec]) {
+                                        float mkq, float invq, float (&w)[E::kPerVec], float (&p)[E::kPerVec],
+                                        float taup = 0.f, float tauq = 0.f) {
   // prob() and residual() with the exponent argument as a packed fma.  The products and the
   // difference stay scalar mul.rn / sub.rn, which are never fused: a product fused into the
   // difference would leave its rounding error behind where p == q must give exactly 0.
   const float2 kk = make_float2(k, k);
 #pragma unroll
   for (int h = 0; h < E::kPerVec / 2; ++h) {
-    const float2 ep = ex2x2(fma2(E::pair(vp, h), kk, make_float2(-mkp, -mkp)));
+    const float2 xp = E::pair(vp, h);
+    const float2 ep = ex2x2(fma2(xp, kk, make_float2(-mkp, -mkp)));
     p[2 * h] = __fmul_rn(ep.x, invp);
     p[2 * h + 1] = __fmul_rn(ep.y, invp);
+    if constexpr (kTrunc) {
+      if (!(xp.x >= taup)) p[2 * h] = 0.f;
+      if (!(xp.y >= taup)) p[2 * h + 1] = 0.f;
+    }
     if (pair) {
-      const float2 eq = ex2x2(fma2(E::pair(vq, h), kk, make_float2(-mkq, -mkq)));
-      w[2 * h] = residual(p[2 * h], __fmul_rn(eq.x, invq));
-      w[2 * h + 1] = residual(p[2 * h + 1], __fmul_rn(eq.y, invq));
+      const float2 xq = E::pair(vq, h);
+      const float2 eq = ex2x2(fma2(xq, kk, make_float2(-mkq, -mkq)));
+      float q0 = __fmul_rn(eq.x, invq), q1 = __fmul_rn(eq.y, invq);
+      if constexpr (kTrunc) {
+        if (!(xq.x >= tauq)) q0 = 0.f;
+        if (!(xq.y >= tauq)) q1 = 0.f;
+      }
+      w[2 * h] = residual(p[2 * h], q0);
+      w[2 * h + 1] = residual(p[2 * h + 1], q1);
     } else {
       w[2 * h] = p[2 * h];
       w[2 * h + 1] = p[2 * h + 1];
@@ -689,7 +703,7 @@ __device__ __forceinline__ uint64_t settle_word(uint64_t* p, uint64_t v, Shared&
 // holding the smallest id whose running weight exceeds u * total), then the block rescans it
 // in ascending id order, one 16-byte vector of p (and q) per thread per step.  Called by every
 // thread of the block.
-template <class E, bool kVec, bool kMixed>
+template <class E, bool kVec, bool kMixed, bool kTrunc = false>
 __device__ void select(const Args& a, const Geo& geo, const Work& w, const Seq<E, kMixed>& sq, const PlanRec pl,
                        Shared& sm) {
   using raw = typename E::raw;
@@ -778,7 +792,7 @@ __device__ void select(const Args& a, const Geo& geo, const Work& w, const Seq<E
     float s = 0.f;
     {
       float wv[N], pv[N];
-      weights<E>(vp, vq, pair, sq.k, pl.mkp, pl.invp, pl.mkq, pl.invq, wv, pv);
+      weights<E, kTrunc>(vp, vq, pair, sq.k, pl.mkp, pl.invp, pl.mkq, pl.invq, wv, pv, pl.taup, pl.tauq);
 #pragma unroll
       for (int j = 0; j < N; ++j) s = __fadd_rn(s, draw_p ? pv[j] : wv[j]);
     }
@@ -808,7 +822,7 @@ __device__ void select(const Args& a, const Geo& geo, const Work& w, const Seq<E
       if (lane == sl) {
         // the same weights again, from the vectors kept in registers
         float wv[N], pv[N];
-        weights<E>(vp, vq, pair, sq.k, pl.mkp, pl.invp, pl.mkq, pl.invq, wv, pv);
+        weights<E, kTrunc>(vp, vq, pair, sq.k, pl.mkp, pl.invp, pl.mkq, pl.invq, wv, pv, pl.taup, pl.tauq);
         float r = __fsub_rn(at, s);
         int t = -1, lp_ = -1;
 #pragma unroll
@@ -850,7 +864,7 @@ __device__ void select(const Args& a, const Geo& geo, const Work& w, const Seq<E
 
 // one draw chunk: the (residual, p) masses of its kWarps sub-ranges; the last draw chunk of b
 // to finish selects
-template <class E, bool kVec, bool kMixed>
+template <class E, bool kVec, bool kMixed, bool kTrunc = false>
 __device__ void draw_chunk(const Args& a, const Geo& geo, const Work& w, const Seq<E, kMixed>& sq, const PlanRec pl,
                            int dc, Shared& sm) {
   using raw = typename E::raw;
@@ -876,7 +890,7 @@ __device__ void draw_chunk(const Args& a, const Geo& geo, const Work& w, const S
 #pragma unroll
     for (int q = 0; q < kDrawVec; ++q) {
       float wv[N], pv[N];
-      weights<E>(vp[q], vq[q], pair, sq.k, pl.mkp, pl.invp, pl.mkq, pl.invq, wv, pv);
+      weights<E, kTrunc>(vp[q], vq[q], pair, sq.k, pl.mkp, pl.invp, pl.mkq, pl.invq, wv, pv, pl.taup, pl.tauq);
 #pragma unroll
       for (int h = 0; h < N / 2; ++h) {
         ws2 = add2(ws2, make_float2(wv[2 * h], wv[2 * h + 1]));
@@ -893,7 +907,7 @@ __device__ void draw_chunk(const Args& a, const Geo& geo, const Work& w, const S
   __syncthreads();
   if (tid == 0) sm.last = atom_add_relaxed(&w.bdone[b], 1) == geo.DCL - 1;
   __syncthreads();
-  if (sm.last) select<E, kVec, kMixed>(a, geo, w, sq, pl, sm);
+  if (sm.last) select<E, kVec, kMixed, kTrunc>(a, geo, w, sq, pl, sm);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -1353,6 +1367,357 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
 }
 
 // ------------------------------------------------------------------------------------------
+// truncated sampling: per-row thresholds, then the decisions, then the draw
+// ------------------------------------------------------------------------------------------
+//
+// The same truncation on both sides (the "M013" card §10 and the nxmr note: temperature,
+// top-p or any other logits processing must show in p and q).  For every valid row of a
+// sampling sequence one block finds the row's max M, then the smallest kept logit tau: top-k
+// keeps the logits >= the k-th largest (ties kept), top-p then keeps those >= the largest t
+// whose kept mass at or above t reaches top_p times the top-k-kept mass.  Both thresholds are
+// found exactly by a radix search over order-preserving 16-bit keys of the bf16 logits, one
+// byte per pass, with counts and fixed-point masses (2^-40 units, summed in integers, so
+// every run gives the same bits).  The row's normaliser is the kept mass; p'(v) = 0 below tau.
+
+struct TruncArgs {
+  const int32_t* top_k;   // [B] or null
+  const float* top_p;     // [B] or null
+};
+
+struct __align__(16) RowInfo {
+  float mk;     // M * k
+  float invs;   // 1 / kept mass
+  float tau;    // smallest kept logit (-inf: everything kept)
+  int arg;      // greedy rows: lowest-id argmax
+};
+
+constexpr float kMassUnit = 1099511627776.0f;   // 2^40
+
+// order-preserving 16-bit key of a bf16 logit; -0 is taken as +0 so equal values share a key
+__device__ __forceinline__ uint32_t key16(uint32_t bits) {
+  bits &= 0xffffu;
+  if (bits == 0x8000u) bits = 0;
+  return (bits & 0x8000u) ? (~bits & 0xffffu) : (bits | 0x8000u);
+}
+__device__ __forceinline__ float key16_value(uint32_t key) {
+  const uint32_t bits = (key & 0x8000u) ? (key & 0x7fffu) : (~key & 0xffffu);
+  return __uint_as_float(bits << 16);
+}
+
+struct TruncShared {
+  unsigned cnt[256];
+  unsigned long long mass[256];
+  float wm[kWarps];
+  int wi[kWarps];
+  unsigned long long wtot[kWarps];
+};
+
+// Visits every id of a row once: fn(x, bits) per element, four 16-byte vectors per thread per
+// step, coalesced across the block.
+template <bool kVec, class Fn>
+__device__ __forceinline__ void for_each_bf16(const uint16_t* row, int64_t V, Fn fn) {
+  constexpr int kStep = kThreads * 8 * 4;
+  for (int64_t e0 = 0; e0 < V; e0 += kStep) {
+    uint4 v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = vec_at<Bf16, kVec>(row, e0 + int64_t(q * kThreads + int(threadIdx.x)) * 8, V);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int64_t e = e0 + int64_t(q * kThreads + int(threadIdx.x)) * 8;
+      const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (e + j >= V) break;
+        const uint32_t bits = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu);
+        fn(__uint_as_float(bits << 16), bits, int(e + j));
+      }
+    }
+  }
+}
+
+// One radix pass: for the elements whose key is >= kmin and whose high byte is `prefix`
+// (level 2; level 1 takes all), counts and masses per byte of the key.
+template <bool kVec>
+__device__ void trunc_hist(const uint16_t* row, int64_t V, int level, uint32_t prefix, uint32_t kmin, float k,
+                           float mk, TruncShared& ts) {
+  for (int i = int(threadIdx.x); i < 256; i += kThreads) {
+    ts.cnt[i] = 0;
+    ts.mass[i] = 0;
+  }
+  __syncthreads();
+  for_each_bf16<kVec>(row, V, [&](float x, uint32_t bits, int) {
+    const uint32_t key = key16(bits);
+    if (key < kmin) return;
+    if (level == 2 && (key >> 8) != prefix) return;
+    const uint32_t bin = level == 1 ? key >> 8 : key & 0xffu;
+    const float e = ex2(fmaf(x, k, -mk));
+    atomicAdd(&ts.cnt[bin], 1u);
+    atomicAdd(&ts.mass[bin], __float2ull_rn(e * kMassUnit));
+  });
+  __syncthreads();
+}
+
+// the mass (fixed point) of the elements with key >= kmin, all threads taking part
+template <bool kVec>
+__device__ unsigned long long trunc_total(const uint16_t* row, int64_t V, uint32_t kmin, float k, float mk,
+                                          TruncShared& ts) {
+  unsigned long long s = 0;
+  for_each_bf16<kVec>(row, V, [&](float x, uint32_t bits, int) {
+    if (key16(bits) >= kmin) s += __float2ull_rn(ex2(fmaf(x, k, -mk)) * kMassUnit);
+  });
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(kFull, s, o);
+  const int lane = int(threadIdx.x) & 31, warp = int(threadIdx.x) >> 5;
+  if (lane == 0) ts.wtot[warp] = s;
+  __syncthreads();
+  unsigned long long t = 0;
+  for (int i = 0; i < kWarps; ++i) t += ts.wtot[i];
+  __syncthreads();
+  return t;
+}
+
+// Per row: greedy rows get their argmax; sampling rows their max, threshold and kept mass.
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) trunc_rows_kernel(const Args a, const TruncArgs t, RowInfo* info,
+                                                              int nslots) {
+  __shared__ TruncShared ts;
+  __shared__ uint32_t s_key[2];
+  __shared__ unsigned long long s_mass;
+  const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
+  const int64_t idx = int64_t(blockIdx.x);
+  const int slot = int(idx % nslots), b = int(idx / nslots);
+  const Seq<Bf16, true> sq(a, b);
+  if (!sq.slot_valid(slot, a.gmax)) return;
+  const uint16_t* row = slot <= a.gmax ? target_row<Bf16>(a, b, slot)
+                                       : static_cast<const uint16_t*>(a.draft) + (int64_t(b) * a.gmax + (slot - a.gmax - 1)) * a.V;
+  RowInfo* out = info + int64_t(b) * nslots + slot;
+  const int64_t V = a.V;
+  if (!sq.sampling) {
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    for_each_bf16<kVec>(row, V, [&](float x, uint32_t, int id) {
+      if (better(x, id, bv, bi)) { bv = x; bi = id; }
+    });
+    warp_argmax(bv, bi);
+    if (lane == 0) { ts.wm[warp] = bv; ts.wi[warp] = bi; }
+    __syncthreads();
+    if (tid == 0) {
+      for (int i = 1; i < kWarps; ++i)
+        if (better(ts.wm[i], ts.wi[i], bv, bi)) { bv = ts.wm[i]; bi = ts.wi[i]; }
+      out->arg = bi;
+    }
+    return;
+  }
+  // pass 1: the row's max
+  float m = -INFINITY;
+  for_each_bf16<kVec>(row, V, [&](float x, uint32_t, int) { m = fmaxf(m, x); });
+  m = warp_max(m);
+  if (lane == 0) ts.wm[warp] = m;
+  __syncthreads();
+  float M = ts.wm[0];
+  for (int i = 1; i < kWarps; ++i) M = fmaxf(M, ts.wm[i]);
+  __syncthreads();
+  const float k = sq.k;
+  const float mk = __fmul_rn(M, k);
+  const int topk = t.top_k ? t.top_k[b] : 0;
+  const float topp = t.top_p ? t.top_p[b] : 1.f;
+  const bool dok = topk > 0 && int64_t(topk) < V;
+  const bool dop = topp > 0.f && topp < 1.f;
+  uint32_t kmin = 0;                       // smallest kept key so far (0: everything)
+  unsigned long long kept;                 // mass of the keys >= kmin
+  if (!dok && !dop) {
+    kept = trunc_total<kVec>(row, V, 0, k, mk, ts);
+  } else {
+    // level 1 over every element: the top-k search starts here, and so does top-p without top-k
+    trunc_hist<kVec>(row, V, 1, 0, 0, k, mk, ts);
+    if (dok) {
+      if (tid == 0) {
+        uint32_t acc = 0, b1 = 0;
+        unsigned long long above = 0;
+        for (int bin = 255; bin >= 0; --bin) {
+          if (acc + ts.cnt[bin] >= uint32_t(topk)) { b1 = uint32_t(bin); break; }
+          acc += ts.cnt[bin];
+          above += ts.mass[bin];
+        }
+        s_key[0] = b1;
+        s_key[1] = uint32_t(topk) - acc;   // still needed inside bin b1
+        s_mass = above;
+      }
+      __syncthreads();
+      const uint32_t b1 = s_key[0], need = s_key[1];
+      const unsigned long long above1 = s_mass;
+      __syncthreads();
+      trunc_hist<kVec>(row, V, 2, b1, 0, k, mk, ts);
+      if (tid == 0) {
+        uint32_t acc = 0, b2 = 0;
+        for (int bin = 255; bin >= 0; --bin) {
+          acc += ts.cnt[bin];
+          if (acc >= need) { b2 = uint32_t(bin); break; }
+        }
+        unsigned long long mk_mass = above1;
+        for (int bin = 255; bin >= int(b2); --bin) mk_mass += ts.mass[bin];
+        s_key[0] = (b1 << 8) | b2;
+        s_mass = mk_mass;
+      }
+      __syncthreads();
+      kmin = s_key[0];
+      kept = s_mass;
+      __syncthreads();
+    } else {
+      if (tid == 0) {
+        unsigned long long s = 0;
+        for (int bin = 0; bin < 256; ++bin) s += ts.mass[bin];
+        s_mass = s;
+      }
+      __syncthreads();
+      kept = s_mass;
+      __syncthreads();
+    }
+    if (dop) {
+      // top-p over the top-k-kept ids: the largest key whose kept mass at or above it reaches
+      // top_p times the kept mass
+      const unsigned long long target = (unsigned long long)ceil(double(topp) * double(kept));
+      if (dok) trunc_hist<kVec>(row, V, 1, 0, kmin, k, mk, ts);   // level 1 again, above tau_k only
+      if (tid == 0) {
+        unsigned long long acc = 0;
+        uint32_t c1 = 0;
+        for (int bin = 255; bin >= 0; --bin) {
+          if (acc + ts.mass[bin] >= target) { c1 = uint32_t(bin); break; }
+          acc += ts.mass[bin];
+        }
+        s_key[0] = c1;
+        s_mass = acc;
+      }
+      __syncthreads();
+      const uint32_t c1 = s_key[0];
+      const unsigned long long above = s_mass;
+      __syncthreads();
+      trunc_hist<kVec>(row, V, 2, c1, kmin, k, mk, ts);
+      if (tid == 0) {
+        unsigned long long acc = above;
+        uint32_t c2 = 0;
+        for (int bin = 255; bin >= 0; --bin) {
+          acc += ts.mass[bin];
+          if (acc >= target) { c2 = uint32_t(bin); break; }
+        }
+        s_key[0] = (c1 << 8) | c2;
+        s_mass = acc;
+      }
+      __syncthreads();
+      kmin = s_key[0];
+      kept = s_mass;
+    }
+  }
+  if (tid == 0) {
+    RowInfo r;
+    r.mk = mk;
+    r.invs = __frcp_rn(float(double(kept) / double(kMassUnit)));
+    r.tau = kmin == 0 ? -INFINITY : key16_value(kmin);
+    r.arg = 0;
+    *out = r;
+  }
+}
+
+// One warp per sequence: the acceptance decisions on the truncated p', q' (or the greedy
+// compare), the outputs of greedy sequences, and the plan of the draw.
+__global__ void __launch_bounds__(32) trunc_decide_kernel(const Args a, const RowInfo* info, int nslots,
+                                                          PlanRec* plans) {
+  const int lane = int(threadIdx.x);
+  const int b = int(blockIdx.x);
+  const Seq<Bf16, true> sq(a, b);
+  const int g = sq.g, gmax = a.gmax;
+  const RowInfo* ri = info + int64_t(b) * nslots;
+  bool acc = false, valid = false;
+  float p = NAN, q = NAN;
+  if (lane < g) {
+    const int d = __ldg(&a.draft_tokens[int64_t(b) * gmax + lane]);
+    valid = d >= 0 && int64_t(d) < a.V;
+    if (valid) {
+      if (sq.sampling) {
+        const RowInfo rp = ri[lane], rq = ri[gmax + 1 + lane];
+        const float xp = Bf16::at(target_row<Bf16>(a, b, lane), d);
+        const float xq = Bf16::at(static_cast<const uint16_t*>(a.draft) + (int64_t(b) * gmax + lane) * a.V, d);
+        p = xp >= rp.tau ? prob(xp, sq.k, rp.mk, rp.invs) : 0.f;
+        q = xq >= rq.tau ? prob(xq, sq.k, rq.mk, rq.invs) : 0.f;
+        const float u = __ldg(&a.u_accept[int64_t(b) * gmax + lane]);
+        acc = (p == 0.f) ? (u < 0.f) : (p >= q ? (u < 1.f) : (__fmul_rn(u, q) < p));
+      } else {
+        acc = d == ri[lane].arg;
+      }
+    }
+  }
+  const unsigned keep = __ballot_sync(kFull, acc);
+  const unsigned rej = ~keep & (g >= 32 ? kFull : ((1u << g) - 1u));
+  const int m = rej ? __ffs(rej) - 1 : g;
+  const unsigned bad = __ballot_sync(kFull, lane < g && !valid);
+  int flags = sq.flags;
+  if (m < g && ((bad >> m) & 1u)) flags |= SPEC_ST_BAD_DRAFT;
+  if (a.diag) {   // gmax <= 32: lane i writes draft i's p'(d_i), q'(d_i)
+    float* dg = a.diag + int64_t(b) * (2 * gmax + 1);
+    if (lane < gmax) {
+      dg[2 * lane] = (sq.sampling && lane < g) ? p : NAN;
+      dg[2 * lane + 1] = (sq.sampling && lane < g) ? q : NAN;
+    }
+    if (!sq.sampling && lane == 0) dg[2 * gmax] = NAN;
+  }
+  if (!sq.sampling) {
+    for (int i = lane; i <= gmax; i += 32) {
+      int v = -1;
+      if (i < m) v = a.draft_tokens[int64_t(b) * gmax + i];
+      else if (i == m) v = ri[m].arg;
+      a.out_tokens[int64_t(b) * (gmax + 1) + i] = v;
+    }
+    if (lane == 0) {
+      a.num_accepted[b] = m;
+      if (a.status) a.status[b] = flags;
+    }
+    return;
+  }
+  if (lane == 0) {
+    const RowInfo rp = ri[m];
+    PlanRec pr;
+    pr.m = m;
+    pr.g = g;
+    pr.flags = flags;
+    pr.pair = m < g ? 1 : 0;
+    pr.mkp = rp.mk;
+    pr.invp = rp.invs;
+    pr.taup = rp.tau;
+    if (pr.pair) {
+      const RowInfo rq = ri[gmax + 1 + m];
+      pr.mkq = rq.mk;
+      pr.invq = rq.invs;
+      pr.tauq = rq.tau;
+    } else {
+      pr.mkq = pr.invq = 0.f;
+      pr.tauq = 0.f;
+    }
+    plans[b] = pr;
+  }
+}
+
+// Draw chunk dc of sequence b (sampling sequences), on the plan the decisions left; the last
+// chunk to finish selects the token and writes the outputs.
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) trunc_draw_kernel(const Args a, const Geo geo, const Work w,
+                                                              PlanRec* plans, RowInfo* info, int nslots) {
+  __shared__ Shared sm;
+  const int64_t idx = int64_t(blockIdx.x);
+  const int dc = int(idx % geo.DCL), b = int(idx / geo.DCL);
+  const Seq<Bf16, true> sq(a, b);
+  if (sq.sampling) {
+    const PlanRec pl = plans[b];
+    draw_chunk<Bf16, kVec, true, true>(a, geo, w, sq, pl, dc, sm);
+  } else {
+    sm.last = dc == 0;   // one unit of a greedy sequence clears what the call used
+  }
+  __syncthreads();
+  if (!sm.last) return;
+  // the selector (or a greedy sequence's unit 0): every word of b returns to zero
+  for (int i = int(threadIdx.x); i < nslots; i += kThreads) info[int64_t(b) * nslots + i] = RowInfo{0.f, 0.f, 0.f, 0};
+  if (threadIdx.x == 0) plans[b] = PlanRec{};
+}
+
+// ------------------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------------------
 
@@ -1385,7 +1750,7 @@ size_t align64(size_t x) { return (x + 63) & ~size_t(63); }
 // Workspace layout: counters and published words only, all zero between calls (each call
 // returns every word it used to zero), so calls of any sizes can share one workspace.
 struct WsLayout {
-  size_t cnt, bdone, planw, state, part, xd, mass, end;
+  size_t cnt, bdone, planw, state, part, xd, mass, info, plans, end;
 };
 
 WsLayout ws_layout(int B, int gmax, int64_t V) {
@@ -1399,7 +1764,9 @@ WsLayout ws_layout(int B, int gmax, int64_t V) {
   L.part = L.state + align64(size_t(B) * s.dcl * 4);
   L.xd = L.part + align64(size_t(B) * nslots * s.cl * 8);
   L.mass = L.xd + align64(size_t(B) * nslots * 8);
-  L.end = L.mass + align64(size_t(B) * s.dcl * kWarps * 8);
+  L.info = L.mass + align64(size_t(B) * s.dcl * kWarps * 8);   // truncated sampling only
+  L.plans = L.info + align64(size_t(B) * nslots * sizeof(RowInfo));
+  L.end = L.plans + align64(size_t(B) * sizeof(PlanRec));
   return L;
 }
 
@@ -1499,6 +1866,49 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
     if (e != cudaSuccess) return cuda_fail(e, "verify kernel launch");
     count_launch();
   }
+  return SPEC_OK;
+}
+
+// truncated sampling: thresholds per row, decisions per sequence, then the draw; three launches
+template <bool kVec>
+int launch_truncated(const Args& args, const TruncArgs& t, void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || !ws_fits(args.B, args.gmax, args.V, ws_bytes)) {
+    set_error("workspace of %zu bytes is smaller than the %zu bytes needed", ws ? ws_bytes : size_t(0),
+              ws_required(args.B, args.gmax, args.V));
+    return SPEC_ENOSPACE;
+  }
+  if (reinterpret_cast<uintptr_t>(ws) % 64 != 0) {
+    set_error("workspace must be 64-byte aligned");
+    return SPEC_EINVAL;
+  }
+  const Split sp = make_split(args.V);
+  const WsLayout L = ws_layout(args.B, args.gmax, args.V);
+  const Work w = ws_views(ws, L);
+  unsigned char* base = static_cast<unsigned char*>(ws);
+  RowInfo* info = reinterpret_cast<RowInfo*>(base + L.info);
+  PlanRec* plans = reinterpret_cast<PlanRec*>(base + L.plans);
+  const int nslots = 2 * args.gmax + 1;
+  Geo geo = {};
+  geo.CL = sp.cl;
+  geo.chunk = sp.chunk;
+  geo.DCL = sp.dcl;
+  geo.dchunk = sp.dchunk;
+  geo.nslots = nslots;
+  geo.b0 = 0;
+  geo.b1 = args.B;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  trunc_rows_kernel<kVec><<<unsigned(int64_t(args.B) * nslots), kThreads, 0, s>>>(args, t, info, nslots);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "truncation rows kernel launch");
+  count_launch();
+  trunc_decide_kernel<<<unsigned(args.B), 32, 0, s>>>(args, info, nslots, plans);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "truncation decide kernel launch");
+  count_launch();
+  trunc_draw_kernel<kVec><<<unsigned(int64_t(args.B) * geo.DCL), kThreads, 0, s>>>(args, geo, w, plans, info, nslots);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "truncation draw kernel launch");
+  count_launch();
   return SPEC_OK;
 }
 
@@ -1661,6 +2071,49 @@ extern "C" int spec_verify_sample_split(const void* saved_logits, const void* bl
   return verify_sample(saved_logits, block_logits, draft_logits, dtype, draft_tokens, num_draft, temperature,
                        u_accept, u_sample, B, gmax, V, out_tokens, num_accepted, diag, status, workspace,
                        workspace_bytes, stream);
+}
+
+extern "C" int spec_verify_sample_truncated(const void* target_logits, const void* draft_logits, int dtype,
+                                            const int32_t* draft_tokens, const int32_t* num_draft,
+                                            const float* temperature, const int32_t* top_k, const float* top_p,
+                                            const float* u_accept, const float* u_sample, int B, int gmax, int V,
+                                            int32_t* out_tokens, int32_t* num_accepted, float* diag,
+                                            int32_t* status, void* workspace, size_t workspace_bytes, void* stream) {
+  clear_error();
+  int rc = check_common(target_logits, dtype, draft_tokens, B, gmax, V, out_tokens, num_accepted);
+  if (rc != SPEC_OK) return rc;
+  if (dtype != SPEC_BF16) {
+    set_error("truncated sampling takes bf16 logits");
+    return SPEC_EDTYPE;
+  }
+  if (V > (1 << 21)) {
+    set_error("V=%d too large (at most 2^21 bf16 ids)", V);
+    return SPEC_ENOSPACE;
+  }
+  if (B == 0) return SPEC_OK;
+  if (!temperature || !u_sample || (gmax > 0 && (!draft_logits || !u_accept))) {
+    set_error("null required pointer (draft_logits, temperature, u_accept or u_sample)");
+    return SPEC_EINVAL;
+  }
+  Args a = {};
+  a.target = target_logits;
+  a.draft = draft_logits;
+  a.draft_tokens = draft_tokens;
+  a.num_draft = num_draft;
+  a.temperature = temperature;
+  a.u_accept = u_accept;
+  a.u_sample = u_sample;
+  a.V = V;
+  a.B = B;
+  a.gmax = gmax;
+  a.out_tokens = out_tokens;
+  a.num_accepted = num_accepted;
+  a.diag = diag;
+  a.status = status;
+  TruncArgs t = {top_k, top_p};
+  const bool vec = vec_ok(target_logits, dtype, V) && vec_ok(draft_logits, dtype, V);
+  return vec ? launch_truncated<true>(a, t, workspace, workspace_bytes, stream)
+             : launch_truncated<false>(a, t, workspace, workspace_bytes, stream);
 }
 
 extern "C" int spec_verify_tree_greedy(const void* target_logits, int dtype, const int32_t* node_tokens,

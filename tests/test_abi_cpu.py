@@ -113,6 +113,18 @@ def test_tree_argument_checks(lib):
     assert sv.spec_verify_workspace_bytes(4, 63, 100) > 0 and sv.spec_verify_workspace_bytes(4, 64, 100) == 0
 
 
+def test_truncated_argument_checks(lib):
+    n0 = lib.spec_launch_count()
+    t = lambda dtype=0, draft=FAKE, temp=FAKE, B=4, V=100: lib.spec_verify_sample_truncated(
+        FAKE, draft, dtype, FAKE, None, temp, None, None, FAKE, FAKE, B, 3, V, FAKE, FAKE, None, None, FAKE, 8, None)
+    assert t(dtype=1) == 2 and b"bf16" in lib.spec_last_error()
+    assert t(draft=None) == 1 and t(temp=None) == 1
+    assert t(V=(1 << 21) + 8) == 3
+    assert t() == 3 and b"workspace" in lib.spec_last_error()
+    assert t(draft=None, temp=None, B=0) == 0
+    assert lib.spec_launch_count() == n0
+
+
 def test_plan_splits_vocabulary(lib):
     for V in [1, 3, 1024, 4096, 4097, 32000, 50000, 128256, 151936, 1 << 20]:
         cl, chunk = sv.spec_verify_plan(V)
@@ -146,7 +158,7 @@ def test_binding_arity_matches_header(lib):
     for name in ("spec_verify_greedy", "spec_verify_sample", "spec_commit_kv_lengths",
                  "spec_verify_workspace_bytes", "spec_verify_plan", "spec_verify_sample_static",
                  "spec_apply_stops", "spec_verify_greedy_split", "spec_verify_sample_split",
-                 "spec_verify_tree_greedy"):
+                 "spec_verify_tree_greedy", "spec_verify_sample_truncated"):
         m = re.search(r"\b" + name + r"\s*\(([^)]*)\)", text)
         params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
         assert len(getattr(lib, name).argtypes) == len(params), name

@@ -1,0 +1,104 @@
+"""Top-k / top-p truncated sampling on the GPU (spec_verify_sample_truncated) against the float64
+oracle: tokens and accepted counts bit-exact outside flagged margins (acceptance, inverse CDF
+and the top-p crossing), p'(d), q'(d) and the residual mass within 1e-5; workspace returned to
+zero; repeat runs bit-identical.  The "M013" card §10 and the nxmr note: truncation must show in
+both p and q."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import specverify_oracle as O
+from speculative_decoding_verification_34_gb300 import specverify as sv
+from speculative_decoding_verification_34_gb300 import workloads as W
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+def run_truncated(wl, top_k, top_p):
+    B, g = wl.B, wl.gmax
+    out = torch.full((B, g + 1), -7, dtype=torch.int32, device="cuda")
+    m = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    dg = torch.full((B, 2 * g + 1), 1234.5, dtype=torch.float32, device="cuda")
+    st = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(sv.spec_verify_workspace_bytes(B, g, wl.V, sv.SPEC_BF16), dtype=torch.uint8, device="cuda")
+    sv.spec_verify_sample_truncated(parity.dev(wl.target), parity.dev(wl.draft), parity.dev(wl.draft_tokens),
+                                    parity.dev(wl.num_draft), parity.dev(wl.temperature),
+                                    None if top_k is None else parity.dev(np.asarray(top_k, np.int32)),
+                                    None if top_p is None else parity.dev(np.asarray(top_p, np.float32)),
+                                    parity.dev(wl.u_accept), parity.dev(wl.u_sample), out, m, dg, st, workspace=ws)
+    torch.cuda.synchronize()
+    assert bool((ws == 0).all()), "workspace not returned to zero"
+    return {"out": out.cpu().numpy(), "m": m.cpu().numpy(), "status": st.cpu().numpy(), "diag": dg.cpu().numpy()}
+
+
+def check(wl, top_k, top_p, max_differ=1):
+    gpu = run_truncated(wl, top_k, top_p)
+    res = O.verify_batch(wl.target, wl.draft, wl.dtype, wl.draft_tokens, wl.num_draft, wl.temperature,
+                         wl.u_accept, wl.u_sample, top_k=None if top_k is None else np.asarray(top_k),
+                         top_p=None if top_p is None else np.asarray(top_p))
+    n, flagged, differ = parity.compare(wl, gpu, res, check_probs=False)
+    assert len(differ) <= max_differ, (flagged, differ)
+    # p'(d_i), q'(d_i) for the drafts the oracle judged
+    for b, r in enumerate(res):
+        if r.greedy:
+            continue
+        dg = gpu["diag"][b]
+        for i, (pd, qd) in enumerate(zip(r.p_draft, r.q_draft)):
+            if not math.isnan(pd) and b not in flagged:
+                assert abs(dg[2 * i] - pd) <= parity.PROB_TOL and abs(dg[2 * i + 1] - qd) <= parity.PROB_TOL, \
+                    (b, i, dg[2 * i], pd, dg[2 * i + 1], qd)
+    return gpu, res
+
+
+def test_truncation_settings_small_vocabulary():
+    B = 16
+    wl = W.sampling_workload("trunc-small", cfg=71, seed=0, B=B, gmax=4, V=5000, dtype="bf16",
+                             target_sigma=3.0, draft_scale=0.9, draft_sigma=0.7,
+                             temperature=[0.8, 1.0, 0.7, 1.2, 0.9, 1.0, 0.6, 1.1, 0.8, 1.0, 0.0, 0.9, 1.0, 0.7, 1.3, 0.8],
+                             num_draft=[4, 4, 3, 4, 2, 4, 4, 1, 4, 0, 4, 4, 3, 4, 4, 4],
+                             greedy_mask=[0] * 10 + [1] + [0] * 5)
+    top_k = [0, 1, 5, 200, 0, 0, 50, 4999, 5000, 30, 20, -3, 3, 100, 0, 1000]
+    top_p = [1.0, 1.0, 1.0, 1.0, 0.5, 0.9, 0.8, 0.95, 0.3, 0.7, 0.6, 2.0, 0.99, 0.0, 0.05, 0.999]
+    _, res = check(wl, top_k, top_p)
+    plain = O.verify_batch(wl.target, wl.draft, wl.dtype, wl.draft_tokens, wl.num_draft, wl.temperature,
+                           wl.u_accept, wl.u_sample)
+    assert sum(r.tokens != s.tokens for r, s in zip(res, plain)) >= 4   # the truncation matters here
+
+
+def test_truncation_full_vocabulary():
+    wl = W.sampling_workload("trunc-128k", cfg=72, seed=1, B=8, gmax=4, V=128256, dtype="bf16",
+                             target_sigma=3.0, draft_scale=0.7, draft_sigma=1.0, temperature=0.8,
+                             boost_frac=0.01, boost=8.0)
+    check(wl, [50, 50, 0, 0, 1000, 20, 1, 2000], [0.9, 1.0, 0.9, 0.5, 0.95, 0.7, 1.0, 0.8])
+
+
+def test_ties_at_the_threshold():
+    """Logits on a coarse grid: the k-th largest value is shared by many ids, all of them kept."""
+    wl = W.sampling_workload("trunc-ties", cfg=73, seed=2, B=10, gmax=3, V=3000, dtype="bf16",
+                             target_sigma=3.0, draft_scale=1.0, draft_sigma=0.5, temperature=1.0)
+    for arr in (wl.target, wl.draft):
+        f = W.bf16_bits_to_f32(arr)
+        arr[...] = W.f32_to_bf16_bits(np.round(f))
+    check(wl, [1, 2, 7, 40, 300, 5, 1, 60, 3, 10], [1.0, 0.8, 1.0, 0.9, 0.5, 1.0, 0.9, 0.99, 0.6, 1.0])
+
+
+def test_no_truncation_arrays():
+    wl = W.sampling_workload("trunc-off", cfg=74, seed=3, B=6, gmax=5, V=9000, dtype="bf16",
+                             target_sigma=3.0, draft_scale=1.0, draft_sigma=1.0, temperature=0.9)
+    check(wl, None, None)
+    check(wl, None, [0.8] * 6)
+    check(wl, [64] * 6, None)
+
+
+def test_repeat_runs_are_bit_identical():
+    wl = W.sampling_workload("trunc-repeat", cfg=75, seed=4, B=12, gmax=4, V=20000, dtype="bf16",
+                             target_sigma=3.0, draft_scale=0.8, draft_sigma=1.0, temperature=0.8)
+    k, p = [40] * 12, [0.9] * 12
+    a = run_truncated(wl, k, p)
+    b = run_truncated(wl, k, p)
+    for key in ("out", "m", "status"):
+        assert np.array_equal(a[key], b[key])
+    assert np.array_equal(a["diag"].view(np.int32), b["diag"].view(np.int32))
