@@ -45,6 +45,8 @@ def parse_args():
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6],
                     help="1-5: the sampling/greedy workloads; 6: 63-node draft trees (greedy tree verify)")
     ap.add_argument("--copies", type=int, default=4, help="resident input copies rotated per step")
+    ap.add_argument("--top-k", type=int, default=0, help="truncated sampling: top-k on every sequence (0: off)")
+    ap.add_argument("--top-p", type=float, default=1.0, help="truncated sampling: top-p on every sequence (1: off)")
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
@@ -59,9 +61,12 @@ def workload_config(wl, l2_note):
         return {"workload": wl.name, "B": wl.B, "tree_nodes": wl.nmax, "V": wl.V, "logits": wl.dtype,
                 "temperature": 0.0, "algorithmic_bytes_per_step": wl.algorithmic_bytes(),
                 "verified_rows_per_step": wl.verified_rows(), "l2": l2_note}
-    return {"workload": wl.name, "B": wl.B, "gamma": wl.gmax, "V": wl.V, "logits": wl.dtype,
-            "temperature": float(wl.temperature.max()), "algorithmic_bytes_per_step": wl.algorithmic_bytes(),
-            "verified_rows_per_step": wl.verified_rows(), "l2": l2_note}
+    c = {"workload": wl.name, "B": wl.B, "gamma": wl.gmax, "V": wl.V, "logits": wl.dtype,
+         "temperature": float(wl.temperature.max()), "algorithmic_bytes_per_step": wl.algorithmic_bytes(),
+         "verified_rows_per_step": wl.verified_rows(), "l2": l2_note}
+    if getattr(wl, "top_k", None) is not None:
+        c["top_k"], c["top_p"] = int(wl.top_k[0]), float(wl.top_p[0])
+    return c
 
 
 def oracle_one(wl, b):
@@ -71,8 +76,20 @@ def oracle_one(wl, b):
         O.verify_tree_batch(wl.target, wl.dtype, wl.node_tokens, wl.node_parents, wl.num_nodes, seqs=[b])
         return int(wl.num_nodes[b])
     O.verify_batch(wl.target, wl.draft, wl.dtype, wl.draft_tokens, wl.num_draft,
-                   None if wl.greedy_only else wl.temperature, wl.u_accept, wl.u_sample, seqs=[b])
+                   None if wl.greedy_only else wl.temperature, wl.u_accept, wl.u_sample, seqs=[b],
+                   top_k=getattr(wl, "top_k", None), top_p=getattr(wl, "top_p", None))
     return int(wl.num_draft[b])
+
+
+def apply_truncation(wl, args):
+    """--top-k / --top-p: the same truncation for every sequence of a sampling workload."""
+    import numpy as np
+    if is_tree(wl) or wl.greedy_only or (args.top_k <= 0 and not (0.0 < args.top_p < 1.0)):
+        return False
+    wl.top_k = np.full(wl.B, args.top_k, dtype=np.int32)
+    wl.top_p = np.full(wl.B, args.top_p, dtype=np.float32)
+    wl.name = f"{wl.name}-topk{args.top_k}-topp{args.top_p:g}"
+    return True
 
 
 def dist_env():
@@ -217,6 +234,7 @@ def run_reference(args):
         return
     from speculative_decoding_verification_34_gb300 import workloads as W
     wl = W.WORKLOADS[args.config](seed=0)
+    apply_truncation(wl, args)
 
     def one(b):
         return oracle_one(wl, b)
@@ -277,6 +295,7 @@ def run_native(args):
 
     wl = shard_workload(args.config, rank)
     tree = is_tree(wl)
+    trunc = apply_truncation(wl, args)
     B, g, V = wl.B, (wl.nmax if tree else wl.gmax), wl.V
 
     def to_dev(a):
@@ -309,6 +328,10 @@ def run_native(args):
     elif wl.greedy_only:
         verify = [sv.prepare_verify_greedy(tgt[c], toks, nd, out, macc, st, workspace=ws, stream=stream)
                   for c in range(ncopies)]
+    elif trunc:
+        tk, tp = to_dev(wl.top_k), to_dev(wl.top_p)
+        verify = [sv.prepare_verify_sample_truncated(tgt[c], drf[c], toks, nd, temp, tk, tp, ua, us, out, macc, dg, st,
+                                                     workspace=ws, stream=stream) for c in range(ncopies)]
     else:
         verify = [sv.prepare_verify_sample(tgt[c], drf[c], toks, nd, temp, ua, us, out, macc, dg, st,
                                            workspace=ws, stream=stream) for c in range(ncopies)]
@@ -409,6 +432,9 @@ def run_native(args):
             sv.spec_verify_tree_greedy(d_in[0], d_in[1], d_in[2], d_in[3], out, macc, path, st, workspace=ws)
         elif wl.greedy_only:
             sv.spec_verify_greedy(d_in[0], d_in[1], d_in[2], out, macc, st, workspace=ws)
+        elif trunc:
+            sv.spec_verify_sample_truncated(d_in[0], d_in[1], d_in[2], d_in[3], d_in[4], tk, tp, d_in[5], d_in[6],
+                                            out, macc, dg, st, workspace=ws)
         else:
             sv.spec_verify_sample(d_in[0], d_in[1], d_in[2], d_in[3], d_in[4], d_in[5], d_in[6],
                                   out, macc, dg, st, workspace=ws)
@@ -452,6 +478,8 @@ def run_native(args):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": ("verify_kernel<bf16, vec, greedy> (spec_verify_tree_greedy)" if tree
+                                    else "trunc_rows + trunc_decide + trunc_draw kernels (spec_verify_sample_truncated)"
+                                    if trunc
                                     else "verify_kernel<bf16, vec, greedy> (spec_verify_greedy)" if wl.greedy_only
                                     else "verify_kernel<bf16, vec, mixed> (spec_verify_sample)"),
                          "kernel_ms_mean": kern_mean_ms, "kernel_ms_median": kern_med_ms,

@@ -1435,26 +1435,36 @@ __device__ __forceinline__ void for_each_bf16(const uint16_t* row, int64_t V, Fn
   }
 }
 
-// One radix pass: for the elements whose key is >= kmin and whose high byte is `prefix`
-// (level 2; level 1 takes all), counts and masses per byte of the key.
+// One window pass: bin d holds the keys hi - d (d < 256).  Keys above hi are skipped; keys below
+// the window only add to the block's count and mass below it, without atomics, so the atomics
+// land on the few ids near the top of the row, where the thresholds are searched.
 template <bool kVec>
-__device__ void trunc_hist(const uint16_t* row, int64_t V, int level, uint32_t prefix, uint32_t kmin, float k,
-                           float mk, TruncShared& ts) {
+__device__ void trunc_window(const uint16_t* row, int64_t V, uint32_t hi, float k, float mk, TruncShared& ts,
+                             unsigned long long& below_mass) {
   for (int i = int(threadIdx.x); i < 256; i += kThreads) {
     ts.cnt[i] = 0;
     ts.mass[i] = 0;
   }
   __syncthreads();
+  unsigned long long om = 0;
   for_each_bf16<kVec>(row, V, [&](float x, uint32_t bits, int) {
     const uint32_t key = key16(bits);
-    if (key < kmin) return;
-    if (level == 2 && (key >> 8) != prefix) return;
-    const uint32_t bin = level == 1 ? key >> 8 : key & 0xffu;
-    const float e = ex2(fmaf(x, k, -mk));
-    atomicAdd(&ts.cnt[bin], 1u);
-    atomicAdd(&ts.mass[bin], __float2ull_rn(e * kMassUnit));
+    if (key > hi) return;
+    const unsigned long long e = __float2ull_rn(ex2(fmaf(x, k, -mk)) * kMassUnit);
+    const uint32_t d = hi - key;
+    if (d < 256) {
+      atomicAdd(&ts.cnt[d], 1u);
+      atomicAdd(&ts.mass[d], e);
+    } else {
+      om += e;
+    }
   });
+  for (int o = 16; o > 0; o >>= 1) om += __shfl_down_sync(kFull, om, o);
+  const int lane = int(threadIdx.x) & 31, warp = int(threadIdx.x) >> 5;
+  if (lane == 0) ts.wtot[warp] = om;
   __syncthreads();
+  below_mass = 0;
+  for (int i = 0; i < kWarps; ++i) below_mass += ts.wtot[i];
 }
 
 // the mass (fixed point) of the elements with key >= kmin, all threads taking part
@@ -1522,89 +1532,70 @@ __global__ void __launch_bounds__(kThreads) trunc_rows_kernel(const Args a, cons
   const float topp = t.top_p ? t.top_p[b] : 1.f;
   const bool dok = topk > 0 && int64_t(topk) < V;
   const bool dop = topp > 0.f && topp < 1.f;
-  uint32_t kmin = 0;                       // smallest kept key so far (0: everything)
-  unsigned long long kept;                 // mass of the keys >= kmin
+  // Windows of 256 keys from the row's max down.  top-k: the first key whose count from the
+  // top reaches k; top-p: then the first key whose kept mass from the top reaches top_p times
+  // the top-k-kept mass.  Both are exact: a window is searched key by key.
+  const uint32_t ktop = key16(__float_as_uint(M) >> 16);
+  uint32_t kmin = 0;                       // smallest kept key (0: everything)
+  unsigned long long kept = 0;             // mass of the keys >= kmin
   if (!dok && !dop) {
     kept = trunc_total<kVec>(row, V, 0, k, mk, ts);
   } else {
-    // level 1 over every element: the top-k search starts here, and so does top-p without top-k
-    trunc_hist<kVec>(row, V, 1, 0, 0, k, mk, ts);
     if (dok) {
-      if (tid == 0) {
-        uint32_t acc = 0, b1 = 0;
-        unsigned long long above = 0;
-        for (int bin = 255; bin >= 0; --bin) {
-          if (acc + ts.cnt[bin] >= uint32_t(topk)) { b1 = uint32_t(bin); break; }
-          acc += ts.cnt[bin];
-          above += ts.mass[bin];
+      uint32_t hi = ktop, need = uint32_t(topk);
+      for (;;) {
+        unsigned long long below;
+        trunc_window<kVec>(row, V, hi, k, mk, ts, below);
+        if (tid == 0) {
+          int found = -1;
+          uint32_t acc = 0;
+          unsigned long long m_acc = 0;
+          for (int d = 0; d < 256 && d <= int(hi); ++d) {
+            acc += ts.cnt[d];
+            m_acc += ts.mass[d];
+            if (acc >= need) { found = d; break; }
+          }
+          s_key[0] = found >= 0 ? hi - uint32_t(found) : 0xffffffffu;
+          s_key[1] = need - (found >= 0 ? 0u : acc);
+          s_mass = m_acc;
         }
-        s_key[0] = b1;
-        s_key[1] = uint32_t(topk) - acc;   // still needed inside bin b1
-        s_mass = above;
+        __syncthreads();
+        kept += s_mass;
+        const uint32_t res = s_key[0];
+        need = s_key[1];
+        __syncthreads();
+        if (res != 0xffffffffu) { kmin = res; break; }
+        if (hi < 256) break;   // no key left (cannot happen for k < V)
+        hi -= 256;
       }
-      __syncthreads();
-      const uint32_t b1 = s_key[0], need = s_key[1];
-      const unsigned long long above1 = s_mass;
-      __syncthreads();
-      trunc_hist<kVec>(row, V, 2, b1, 0, k, mk, ts);
-      if (tid == 0) {
-        uint32_t acc = 0, b2 = 0;
-        for (int bin = 255; bin >= 0; --bin) {
-          acc += ts.cnt[bin];
-          if (acc >= need) { b2 = uint32_t(bin); break; }
-        }
-        unsigned long long mk_mass = above1;
-        for (int bin = 255; bin >= int(b2); --bin) mk_mass += ts.mass[bin];
-        s_key[0] = (b1 << 8) | b2;
-        s_mass = mk_mass;
-      }
-      __syncthreads();
-      kmin = s_key[0];
-      kept = s_mass;
-      __syncthreads();
     } else {
-      if (tid == 0) {
-        unsigned long long s = 0;
-        for (int bin = 0; bin < 256; ++bin) s += ts.mass[bin];
-        s_mass = s;
-      }
-      __syncthreads();
-      kept = s_mass;
-      __syncthreads();
+      kept = trunc_total<kVec>(row, V, 0, k, mk, ts);
     }
     if (dop) {
-      // top-p over the top-k-kept ids: the largest key whose kept mass at or above it reaches
-      // top_p times the kept mass
       const unsigned long long target = (unsigned long long)ceil(double(topp) * double(kept));
-      if (dok) trunc_hist<kVec>(row, V, 1, 0, kmin, k, mk, ts);   // level 1 again, above tau_k only
-      if (tid == 0) {
-        unsigned long long acc = 0;
-        uint32_t c1 = 0;
-        for (int bin = 255; bin >= 0; --bin) {
-          if (acc + ts.mass[bin] >= target) { c1 = uint32_t(bin); break; }
-          acc += ts.mass[bin];
+      uint32_t hi = ktop;
+      unsigned long long acc = 0;
+      for (;;) {
+        unsigned long long below;
+        trunc_window<kVec>(row, V, hi, k, mk, ts, below);
+        if (tid == 0) {
+          int found = -1;
+          unsigned long long a2 = acc;
+          for (int d = 0; d < 256 && d <= int(hi) && hi - uint32_t(d) >= kmin; ++d) {
+            a2 += ts.mass[d];
+            if (a2 >= target) { found = d; break; }
+          }
+          s_key[0] = found >= 0 ? hi - uint32_t(found) : 0xffffffffu;
+          s_mass = a2;
         }
-        s_key[0] = c1;
-        s_mass = acc;
+        __syncthreads();
+        const uint32_t res = s_key[0];
+        acc = s_mass;
+        __syncthreads();
+        if (res != 0xffffffffu) { kmin = res; kept = acc; break; }
+        if (hi < 256 || hi - 256 < kmin) break;   // cannot happen: the kept mass reaches the target
+        hi -= 256;
       }
-      __syncthreads();
-      const uint32_t c1 = s_key[0];
-      const unsigned long long above = s_mass;
-      __syncthreads();
-      trunc_hist<kVec>(row, V, 2, c1, kmin, k, mk, ts);
-      if (tid == 0) {
-        unsigned long long acc = above;
-        uint32_t c2 = 0;
-        for (int bin = 255; bin >= 0; --bin) {
-          acc += ts.mass[bin];
-          if (acc >= target) { c2 = uint32_t(bin); break; }
-        }
-        s_key[0] = (c1 << 8) | c2;
-        s_mass = acc;
-      }
-      __syncthreads();
-      kmin = s_key[0];
-      kept = s_mass;
     }
   }
   if (tid == 0) {

@@ -427,6 +427,31 @@ def prepare_verify_sample(target_logits, draft_logits, draft_tokens, num_draft, 
     return _Prepared(lib.spec_verify_sample, args, keep)
 
 
+def prepare_verify_sample_truncated(target_logits, draft_logits, draft_tokens, num_draft, temperature, top_k,
+                                    top_p, u_accept, u_sample, out_tokens, num_accepted, diag=None, status=None,
+                                    workspace=None, stream=None) -> _Prepared:
+    B, gp1, V = target_logits.shape
+    gmax = gp1 - 1
+    lib = load_library()
+    ws, wsp, wsn = _ws(workspace, B, gmax, V, _dtype_code(target_logits), target_logits.device)
+    args = (_ptr(target_logits, "target_logits"),
+            _ptr(draft_logits, "draft_logits", target_logits.dtype, (B, gmax, V)),
+            _dtype_code(target_logits),
+            _ptr(draft_tokens, "draft_tokens", torch.int32, (B, gmax)),
+            _ptr(num_draft, "num_draft", torch.int32, (B,)),
+            _ptr(temperature, "temperature", torch.float32, (B,)),
+            _ptr(top_k, "top_k", torch.int32, (B,)), _ptr(top_p, "top_p", torch.float32, (B,)),
+            _ptr(u_accept, "u_accept", torch.float32, (B, gmax)),
+            _ptr(u_sample, "u_sample", torch.float32, (B,)), B, gmax, V,
+            _ptr(out_tokens, "out_tokens", torch.int32, (B, gmax + 1)),
+            _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
+            _ptr(diag, "diag", torch.float32, (B, 2 * gmax + 1)),
+            _ptr(status, "status", torch.int32, (B,)), wsp, wsn, _stream(stream))
+    keep = (target_logits, draft_logits, draft_tokens, num_draft, temperature, top_k, top_p, u_accept,
+            u_sample, out_tokens, num_accepted, diag, status, ws)
+    return _Prepared(lib.spec_verify_sample_truncated, args, keep)
+
+
 def prepare_verify_greedy(target_logits, draft_tokens, num_draft, out_tokens, num_accepted,
                           status=None, workspace=None, stream=None) -> _Prepared:
     B, gp1, V = target_logits.shape
