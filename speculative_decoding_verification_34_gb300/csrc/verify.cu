@@ -1412,24 +1412,31 @@ struct TruncShared {
   unsigned long long wtot[kWarps];
 };
 
-// Visits every id of a row once: fn(x, bits) per element, four 16-byte vectors per thread per
-// step, coalesced across the block.
+// Visits every id of a row once: fn(x, bits, id) per element, eight 16-byte vectors per thread
+// per step, coalesced across the block.
 template <bool kVec, class Fn>
 __device__ __forceinline__ void for_each_bf16(const uint16_t* row, int64_t V, Fn fn) {
-  constexpr int kStep = kThreads * 8 * 4;
+  constexpr int kVecs = 8;
+  constexpr int kStep = kThreads * 8 * kVecs;
   for (int64_t e0 = 0; e0 < V; e0 += kStep) {
-    uint4 v[4];
+    uint4 v[kVecs];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) v[q] = vec_at<Bf16, kVec>(row, e0 + int64_t(q * kThreads + int(threadIdx.x)) * 8, V);
+    for (int q = 0; q < kVecs; ++q) v[q] = vec_at<Bf16, kVec>(row, e0 + int64_t(q * kThreads + int(threadIdx.x)) * 8, V);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < kVecs; ++q) {
       const int64_t e = e0 + int64_t(q * kThreads + int(threadIdx.x)) * 8;
       const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+      if (e + 8 <= V) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (e + j >= V) break;
-        const uint32_t bits = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu);
-        fn(__uint_as_float(bits << 16), bits, int(e + j));
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t bits = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu);
+          fn(__uint_as_float(bits << 16), bits, int(e + j));
+        }
+      } else {
+        for (int j = 0; j < 8 && e + j < V; ++j) {
+          const uint32_t bits = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu);
+          fn(__uint_as_float(bits << 16), bits, int(e + j));
+        }
       }
     }
   }
@@ -1439,42 +1446,32 @@ __device__ __forceinline__ void for_each_bf16(const uint16_t* row, int64_t V, Fn
 // the window only add to the block's count and mass below it, without atomics, so the atomics
 // land on the few ids near the top of the row, where the thresholds are searched.
 template <bool kVec>
-__device__ void trunc_window(const uint16_t* row, int64_t V, uint32_t hi, float k, float mk, TruncShared& ts,
-                             unsigned long long& below_mass) {
+__device__ void trunc_window(const uint16_t* row, int64_t V, uint32_t hi, float k, float mk, TruncShared& ts) {
   for (int i = int(threadIdx.x); i < 256; i += kThreads) {
     ts.cnt[i] = 0;
     ts.mass[i] = 0;
   }
   __syncthreads();
-  unsigned long long om = 0;
   for_each_bf16<kVec>(row, V, [&](float x, uint32_t bits, int) {
-    const uint32_t key = key16(bits);
-    if (key > hi) return;
-    const unsigned long long e = __float2ull_rn(ex2(fmaf(x, k, -mk)) * kMassUnit);
-    const uint32_t d = hi - key;
+    const uint32_t d = hi - key16(bits);   // wraps for keys above hi
     if (d < 256) {
       atomicAdd(&ts.cnt[d], 1u);
-      atomicAdd(&ts.mass[d], e);
-    } else {
-      om += e;
+      atomicAdd(&ts.mass[d], __float2ull_rn(ex2(fmaf(x, k, -mk)) * kMassUnit));
     }
   });
-  for (int o = 16; o > 0; o >>= 1) om += __shfl_down_sync(kFull, om, o);
-  const int lane = int(threadIdx.x) & 31, warp = int(threadIdx.x) >> 5;
-  if (lane == 0) ts.wtot[warp] = om;
   __syncthreads();
-  below_mass = 0;
-  for (int i = 0; i < kWarps; ++i) below_mass += ts.wtot[i];
 }
 
 // the mass (fixed point) of the elements with key >= kmin, all threads taking part
 template <bool kVec>
 __device__ unsigned long long trunc_total(const uint16_t* row, int64_t V, uint32_t kmin, float k, float mk,
                                           TruncShared& ts) {
-  unsigned long long s = 0;
+  // per thread in float, in a fixed order (so in fixed bits); in fixed point across threads
+  float f = 0.f;
   for_each_bf16<kVec>(row, V, [&](float x, uint32_t bits, int) {
-    if (key16(bits) >= kmin) s += __float2ull_rn(ex2(fmaf(x, k, -mk)) * kMassUnit);
+    if (key16(bits) >= kmin) f = __fadd_rn(f, ex2(fmaf(x, k, -mk)));
   });
+  unsigned long long s = __float2ull_rn(f * kMassUnit);
   for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(kFull, s, o);
   const int lane = int(threadIdx.x) & 31, warp = int(threadIdx.x) >> 5;
   if (lane == 0) ts.wtot[warp] = s;
@@ -1544,8 +1541,7 @@ __global__ void __launch_bounds__(kThreads) trunc_rows_kernel(const Args a, cons
     if (dok) {
       uint32_t hi = ktop, need = uint32_t(topk);
       for (;;) {
-        unsigned long long below;
-        trunc_window<kVec>(row, V, hi, k, mk, ts, below);
+        trunc_window<kVec>(row, V, hi, k, mk, ts);
         if (tid == 0) {
           int found = -1;
           uint32_t acc = 0;
@@ -1576,8 +1572,7 @@ __global__ void __launch_bounds__(kThreads) trunc_rows_kernel(const Args a, cons
       uint32_t hi = ktop;
       unsigned long long acc = 0;
       for (;;) {
-        unsigned long long below;
-        trunc_window<kVec>(row, V, hi, k, mk, ts, below);
+        trunc_window<kVec>(row, V, hi, k, mk, ts);
         if (tid == 0) {
           int found = -1;
           unsigned long long a2 = acc;
