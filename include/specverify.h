@@ -141,11 +141,13 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits, int 
  * turns that truncation off for the batch (or the sequence); greedy sequences (T <= 0) are
  * verified greedily.  bf16 logits only (SPEC_EDTYPE otherwise).
  *
- * Cost: the thresholds are found exactly, per row, by a radix search over the logits' 16-bit
- * order-preserving keys: up to five passes over each row of a sampling sequence (max; one
- * byte of the key per pass, for top-k and then for top-p), then the decisions and the draw,
- * in three kernel launches.  The workspace is spec_verify_workspace_bytes(B, gmax, V, dtype)
- * bytes, as for spec_verify_sample.
+ * Cost: the thresholds are found exactly, per row, by counting the logits' 16-bit
+ * order-preserving keys in windows of 256 keys from the top.  Usually one pass over each row
+ * of a sampling sequence: a sample of the row places the window before the pass, which also
+ * takes the row's max.  A row whose max lies more than 96 keys above the sample's, or whose
+ * threshold lies below the window, is read again, once per further window.  Then come the
+ * decisions and the draw: three kernel launches in all.  The workspace is
+ * spec_verify_workspace_bytes(B, gmax, V, dtype) bytes, as for spec_verify_sample.
  */
 int spec_verify_sample_truncated(const void* target_logits, const void* draft_logits, int dtype,
                                  const int32_t* draft_tokens, const int32_t* num_draft,
@@ -220,7 +222,7 @@ int spec_verify_sample_split(const void* saved_logits, const void* block_logits,
  * The workspace is an array of SPEC_STATIC_WORKSPACE_BYTES bytes compiled into the library,
  * one per device, shared by every call of this function on that device:
  *   - Calls whose sizes need more (spec_verify_workspace_bytes(B, gmax, V, dtype) above
- *     SPEC_STATIC_WORKSPACE_BYTES: B = 1310 at gmax = 4, V = 128256 and B = 1040 at
+ *     SPEC_STATIC_WORKSPACE_BYTES: B = 1056 at gmax = 4, V = 128256 and B = 873 at
  *     gmax = 4, V = 151936 are the largest that fit) return SPEC_ENOSPACE before touching
  *     the device.
  *   - The first call on a device looks the array up (cudaGetSymbolAddress), clears it and

@@ -521,6 +521,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
     if (global_ns() - t0 > kMbarWaitNs) return false;
   }
 }
+
 __device__ __forceinline__ uint4 lds128(const void* p) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(smem_addr(p)));
@@ -1392,6 +1393,19 @@ struct __align__(16) RowInfo {
 };
 
 constexpr float kMassUnit = 1099511627776.0f;   // 2^40
+#ifndef SPEC_TRUNC_GUARD
+#define SPEC_TRUNC_GUARD 96
+#endif
+#ifndef SPEC_TRUNC_FUSED_WIDTH
+#define SPEC_TRUNC_FUSED_WIDTH 256
+#endif
+constexpr uint32_t kGuardKeys = SPEC_TRUNC_GUARD;        // fused window's top above the estimated max
+constexpr uint32_t kFusedWidth = SPEC_TRUNC_FUSED_WIDTH; // keys the fused pass counts (256 or 512)
+static_assert(kFusedWidth == 256 || kFusedWidth == 512, "one or two windows of 256 keys");
+#ifndef SPEC_TRUNC_SAMPLE_RUNS
+#define SPEC_TRUNC_SAMPLE_RUNS 4
+#endif
+constexpr int kSampleRuns = SPEC_TRUNC_SAMPLE_RUNS;     // runs of kThreads vectors the estimate reads
 
 // order-preserving 16-bit key of a bf16 logit; -0 is taken as +0 so equal values share a key
 __device__ __forceinline__ uint32_t key16(uint32_t bits) {
@@ -1405,12 +1419,29 @@ __device__ __forceinline__ float key16_value(uint32_t key) {
 }
 
 struct TruncShared {
-  unsigned cnt[256];
-  unsigned long long mass[256];
+  unsigned cnt[2][256];          // window counts: [0] a pass's window; [0], [1] the fused pass's
   float wm[kWarps];
   int wi[kWarps];
   unsigned long long wtot[kWarps];
+  int res_d;
+  uint32_t res_cnt;
+  unsigned long long res_mass;
 };
+
+// The key of -inf; smaller keys are NaN patterns, which no window counts.
+constexpr uint32_t kKeyNegInf = 0x7fu;
+
+// fixed-point sum over the block of one value per thread (a fixed order, so fixed bits)
+__device__ unsigned long long block_sum_u64(unsigned long long s, TruncShared& ts) {
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(kFull, s, o);
+  const int lane = int(threadIdx.x) & 31, warp = int(threadIdx.x) >> 5;
+  if (lane == 0) ts.wtot[warp] = s;
+  __syncthreads();
+  unsigned long long t = 0;
+  for (int i = 0; i < kWarps; ++i) t += ts.wtot[i];
+  __syncthreads();
+  return t;
+}
 
 // Visits every id of a row once: fn(x, bits, id) per element, eight 16-byte vectors per thread
 // per step, coalesced across the block.
@@ -1442,44 +1473,249 @@ __device__ __forceinline__ void for_each_bf16(const uint16_t* row, int64_t V, Fn
   }
 }
 
-// One window pass: bin d holds the keys hi - d (d < 256).  Keys above hi are skipped; keys below
-// the window only add to the block's count and mass below it, without atomics, so the atomics
-// land on the few ids near the top of the row, where the thresholds are searched.
+// Visits every 16-byte vector of a row once: fn(v, nvalid), nvalid = the ids of v inside the
+// row (8 but at a ragged tail), eight vectors per thread per step, coalesced across the block.
+// Vectors wholly past the row are skipped.
+template <bool kVec, class Fn>
+__device__ __forceinline__ void for_each_vec(const uint16_t* row, int64_t V, Fn fn) {
+  constexpr int kVecs = 8;
+  constexpr int kStep = kThreads * 8 * kVecs;
+  const int tid = int(threadIdx.x);
+  for (int64_t e0 = 0; e0 < V; e0 += kStep) {
+    uint4 v[kVecs];
+#pragma unroll
+    for (int q = 0; q < kVecs; ++q) v[q] = vec_at<Bf16, kVec>(row, e0 + int64_t(q * kThreads + tid) * 8, V);
+#pragma unroll
+    for (int q = 0; q < kVecs; ++q) {
+      const int64_t e = e0 + int64_t(q * kThreads + tid) * 8;
+      if (e < V) fn(v[q], V - e < 8 ? int(V - e) : 8);
+    }
+  }
+}
+
+// The window of one pass: keys hi-width+1..hi, bin d = hi - key.
+struct Window {
+  uint32_t hi;
+  uint32_t width;
+  uint32_t blo;    // fast form: the bf16 code of the lowest key
+  bool fast;       // the window lies above +0: bf16 codes order like the values there
+  float vlo, vhi;  // the window's lowest and highest values
+  __device__ Window(uint32_t h, uint32_t w) : hi(h), width(w) {
+    fast = h > 0x8000u + w - 1u;
+    blo = fast ? h - (w - 1u) - 0x8000u : 0u;
+    vhi = key16_value(h);
+    vlo = h >= w - 1u + kKeyNegInf ? key16_value(h - (w - 1u)) : -INFINITY;
+  }
+};
+
+// One vector's part of a window pass.  kFast: a logit is in the window iff its code minus blo is
+// below the width (unsigned; negative logits wrap far above), its bin is width-1 minus that, and padding
+// (-inf) is never in it; otherwise the order-preserving key decides, ids past nvalid skipped.
+// With kBelow, the ids under the window add their mass to f, in id order.
+// adds 1 to the shared word at addr when t < width, without a branch
+__device__ __forceinline__ void count_if(uint32_t t, uint32_t width, uint32_t addr) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.lt.u32 p, %0, %1;\n\t@p red.shared.add.u32 [%2], 1;\n\t}" ::"r"(t), "r"(width),
+               "r"(addr));
+}
+
+template <bool kFast, bool kBelow>
+__device__ __forceinline__ void window_vec(const uint4& v, int nvalid, const Window& win, float k, float mk,
+                                           unsigned* cnt, float& f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const uint32_t clast = smem_addr(cnt) + 4u * (win.width - 1u);   // bin width-1: code blo
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t bits = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu);
+    if constexpr (kFast) {
+      const uint32_t t = bits - win.blo;
+      count_if(t, win.width, clast - 4u * t);
+      if constexpr (kBelow) {
+        const float x = __uint_as_float(bits << 16);
+        f = __fadd_rn(f, x < win.vlo ? ex2(fmaf(x, k, -mk)) : 0.f);
+      }
+    } else {
+      if (j >= nvalid) break;
+      const float x = __uint_as_float(bits << 16);
+      if (kBelow && x < win.vlo) f = __fadd_rn(f, ex2(fmaf(x, k, -mk)));
+      else if (x >= win.vlo && x <= win.vhi) atomicAdd(&cnt[win.hi - key16(bits)], 1u);
+    }
+  }
+}
+
+// One window pass: bin d counts the ids of key hi - d (d < 256).  Every id of one key has the
+// same logit, so a bin's mass is its count times that logit's exp: counting is all the pass does
+// per id inside the window (one 32-bit shared atomic), ids above it are skipped, and with `below`
+// the ids under it add their mass to a per-thread float sum, returned as the block's fixed-point
+// total.
 template <bool kVec>
-__device__ void trunc_window(const uint16_t* row, int64_t V, uint32_t hi, float k, float mk, TruncShared& ts) {
-  for (int i = int(threadIdx.x); i < 256; i += kThreads) {
-    ts.cnt[i] = 0;
-    ts.mass[i] = 0;
+__device__ unsigned long long trunc_window(const uint16_t* row, int64_t V, uint32_t hi, bool below, float k,
+                                           float mk, TruncShared& ts) {
+  unsigned* cnt = ts.cnt[0];
+  for (int i = int(threadIdx.x); i < 256; i += kThreads) cnt[i] = 0;
+  __syncthreads();
+  const Window win(hi, 256u);
+  float f = 0.f;
+  if (win.fast) {
+    if (below) for_each_vec<kVec>(row, V, [&](const uint4& v, int nv) { window_vec<true, true>(v, nv, win, k, mk, cnt, f); });
+    else for_each_vec<kVec>(row, V, [&](const uint4& v, int nv) { window_vec<true, false>(v, nv, win, k, mk, cnt, f); });
+  } else {
+    if (below) for_each_vec<kVec>(row, V, [&](const uint4& v, int nv) { window_vec<false, true>(v, nv, win, k, mk, cnt, f); });
+    else for_each_vec<kVec>(row, V, [&](const uint4& v, int nv) { window_vec<false, false>(v, nv, win, k, mk, cnt, f); });
   }
   __syncthreads();
-  for_each_bf16<kVec>(row, V, [&](float x, uint32_t bits, int) {
-    const uint32_t d = hi - key16(bits);   // wraps for keys above hi
-    if (d < 256) {
-      atomicAdd(&ts.cnt[d], 1u);
-      atomicAdd(&ts.mass[d], __float2ull_rn(ex2(fmaf(x, k, -mk)) * kMassUnit));
+  return below ? block_sum_u64(__float2ull_rn(f * kMassUnit), ts) : 0ull;
+}
+
+// Warp 0 walks the window's bins d = 0..dmax from the top: the first bin at which the running
+// count (by_count) or the running fixed-point mass reaches `target`.  Each lane takes eight
+// bins, the lanes' sums are scanned, and the lane holding the crossing walks its own bins.
+// Leaves in ts: res_d (-1: not reached), and the count and mass of bins 0..res_d (of the whole
+// window when not reached).  count(d) gives bin d's count.
+template <class Count>
+__device__ void trunc_scan(TruncShared& ts, Count count, uint32_t hi, int dmax, float k, float mk, bool by_count,
+                           unsigned long long target) {
+  if (threadIdx.x < 32) {
+    const int lane = int(threadIdx.x);
+    uint32_t c[8];
+    unsigned long long w[8];
+    uint32_t lc = 0;
+    unsigned long long lw = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int d = lane * 8 + j;
+      c[j] = d <= dmax ? count(d) : 0u;
+      w[j] = c[j] ? c[j] * (unsigned long long)__float2ull_rn(ex2(fmaf(key16_value(hi - uint32_t(d)), k, -mk)) *
+                                                                kMassUnit)
+                  : 0ull;
+      lc += c[j];
+      lw += w[j];
     }
-  });
+    uint32_t ic = lc;
+    unsigned long long iw = lw;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t uc = __shfl_up_sync(kFull, ic, o);
+      const unsigned long long uw = __shfl_up_sync(kFull, iw, o);
+      if (lane >= o) { ic += uc; iw += uw; }
+    }
+    const unsigned hit = __ballot_sync(kFull, by_count ? uint64_t(ic) >= target : iw >= target);
+    if (hit == 0) {
+      if (lane == 31) { ts.res_d = -1; ts.res_cnt = ic; ts.res_mass = iw; }
+    } else if (lane == __ffs(hit) - 1) {
+      uint32_t rc = ic - lc;
+      unsigned long long rw = iw - lw;
+      int d = lane * 8;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        rc += c[j];
+        rw += w[j];
+        if (by_count ? uint64_t(rc) >= target : rw >= target) { d = lane * 8 + j; break; }
+      }
+      ts.res_d = d;
+      ts.res_cnt = rc;
+      ts.res_mass = rw;
+    }
+  }
   __syncthreads();
 }
 
-// the mass (fixed point) of the elements with key >= kmin, all threads taking part
+// the mass (fixed point) of the whole row, all threads taking part
 template <bool kVec>
-__device__ unsigned long long trunc_total(const uint16_t* row, int64_t V, uint32_t kmin, float k, float mk,
-                                          TruncShared& ts) {
+__device__ unsigned long long trunc_total(const uint16_t* row, int64_t V, float k, float mk, TruncShared& ts) {
   // per thread in float, in a fixed order (so in fixed bits); in fixed point across threads
   float f = 0.f;
-  for_each_bf16<kVec>(row, V, [&](float x, uint32_t bits, int) {
-    if (key16(bits) >= kmin) f = __fadd_rn(f, ex2(fmaf(x, k, -mk)));
+  for_each_bf16<kVec>(row, V, [&](float x, uint32_t, int) { f = __fadd_rn(f, ex2(fmaf(x, k, -mk))); });
+  return block_sum_u64(__float2ull_rn(f * kMassUnit), ts);
+}
+
+// the block's max of one value per thread, returned to every thread
+__device__ float block_max_f32(float m, TruncShared& ts) {
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) ts.wm[threadIdx.x >> 5] = m;
+  __syncthreads();
+  float r = ts.wm[0];
+  for (int i = 1; i < kWarps; ++i) r = fmaxf(r, ts.wm[i]);
+  __syncthreads();
+  return r;
+}
+
+// the fixed-point mass of 256 counted bins (bin d: key hi - d), all threads taking part
+__device__ unsigned long long bins_mass(const unsigned* cnt, uint32_t hi, float k, float mk, TruncShared& ts) {
+  const int d = int(threadIdx.x);
+  const unsigned c = cnt[d];
+  const unsigned long long w =
+      c ? c * (unsigned long long)__float2ull_rn(ex2(fmaf(key16_value(hi - uint32_t(d)), k, -mk)) * kMassUnit) : 0ull;
+  return block_sum_u64(w, ts);
+}
+
+// The one pass of the fused search: the row's max (packed bf16 maxima) and the counts of a window
+// fixed before the pass; with kBelow, the mass of the ids under the window relative to the
+// window's lowest value (vk = that value times k; every term is at most 1), so that no max is
+// needed during the pass.
+template <bool kVec, bool kFast, bool kBelow>
+__device__ __forceinline__ void fused_pass(const uint16_t* row, int64_t V, const Window& win, float k, float vk,
+                                           unsigned* cnt, __nv_bfloat162& h, float& f) {
+  for_each_vec<kVec>(row, V, [&](const uint4& v, int nv) {
+    const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+    h = __hmax2(h, __hmax2(__hmax2(p2[0], p2[1]), __hmax2(p2[2], p2[3])));
+    window_vec<kFast, kBelow>(v, nv, win, k, vk, cnt, f);
   });
-  unsigned long long s = __float2ull_rn(f * kMassUnit);
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(kFull, s, o);
-  const int lane = int(threadIdx.x) & 31, warp = int(threadIdx.x) >> 5;
-  if (lane == 0) ts.wtot[warp] = s;
-  __syncthreads();
-  unsigned long long t = 0;
-  for (int i = 0; i < kWarps; ++i) t += ts.wtot[i];
-  __syncthreads();
-  return t;
+}
+
+// The thresholds of one row, over windows of 256 keys from key `top` (the row's max, or a key
+// above it: the bins above the max are empty) down.
+// top-k: the first key whose count from the top reaches k; top-p: then the first key whose
+// kept mass from the top reaches top_p times the top-k-kept mass.  Both are exact: a window is
+// searched key by key.  The window at the max usually holds both crossings, and its counts
+// serve both searches.  window(hi, below) runs one window pass (returning the mass under the
+// window when `below`); count(d) reads bin d of the last one.  Every thread calls this with the
+// same arguments and takes the same branches.  Leaves kmin (smallest kept key, 0: all) and kept
+// (their fixed-point mass).
+template <class WindowFn, class Count>
+__device__ void trunc_search(TruncShared& ts, WindowFn window, Count count, uint32_t top, int topk, float topp,
+                             bool dok, bool dop, float k, float mk, uint32_t& kmin, unsigned long long& kept) {
+  kmin = 0;
+  kept = 0;
+  uint32_t hi = top;                       // the window `count` reads
+  if (dok) {
+    unsigned long long above = 0;          // mass of the windows above hi
+    uint32_t need = uint32_t(topk);        // ids still to count
+    for (;;) {
+      window(hi, false);
+      trunc_scan(ts, count, hi, 255, k, mk, true, need);
+      const int d = ts.res_d;
+      const uint32_t c = ts.res_cnt;
+      const unsigned long long w = ts.res_mass;
+      __syncthreads();
+      if (d >= 0) { kmin = hi - uint32_t(d); kept = above + w; break; }
+      above += w;
+      need -= c;
+      if (hi < 256u + kKeyNegInf) { kept = above; break; }   // only with NaN logits: fewer than k ids counted
+      hi -= 256u;
+    }
+  } else {
+    // the whole row's mass: the window at the max by counts, the rest by per-thread sums
+    const unsigned long long below = window(hi, true);
+    trunc_scan(ts, count, hi, 255, k, mk, true, ~0ull);
+    kept = ts.res_mass + below;
+    __syncthreads();
+  }
+  if (!dop) return;
+  const unsigned long long target = (unsigned long long)ceil(double(topp) * double(kept));
+  unsigned long long acc = 0;
+  uint32_t h = top;
+  for (;;) {
+    if (h != hi) { window(h, false); hi = h; }
+    const int dmax = kmin == 0 ? 255 : int(min(255u, h - kmin));
+    trunc_scan(ts, count, h, dmax, k, mk, false, target - acc);
+    const int d = ts.res_d;
+    const unsigned long long w = ts.res_mass;
+    __syncthreads();
+    if (d >= 0) { kmin = h - uint32_t(d); kept = acc + w; return; }
+    acc += w;
+    // cannot happen: the kept mass reaches the target
+    if (h < 256u + kKeyNegInf || h - 256u < kmin) return;
+    h -= 256u;
+  }
 }
 
 // Per row: greedy rows get their argmax; sampling rows their max, threshold and kept mass.
@@ -1487,8 +1723,6 @@ template <bool kVec>
 __global__ void __launch_bounds__(kThreads) trunc_rows_kernel(const Args a, const TruncArgs t, RowInfo* info,
                                                               int nslots) {
   __shared__ TruncShared ts;
-  __shared__ uint32_t s_key[2];
-  __shared__ unsigned long long s_mass;
   const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
   const int64_t idx = int64_t(blockIdx.x);
   const int slot = int(idx % nslots), b = int(idx / nslots);
@@ -1514,85 +1748,102 @@ __global__ void __launch_bounds__(kThreads) trunc_rows_kernel(const Args a, cons
     }
     return;
   }
-  // pass 1: the row's max
-  float m = -INFINITY;
-  for_each_bf16<kVec>(row, V, [&](float x, uint32_t, int) { m = fmaxf(m, x); });
-  m = warp_max(m);
-  if (lane == 0) ts.wm[warp] = m;
-  __syncthreads();
-  float M = ts.wm[0];
-  for (int i = 1; i < kWarps; ++i) M = fmaxf(M, ts.wm[i]);
-  __syncthreads();
   const float k = sq.k;
-  const float mk = __fmul_rn(M, k);
   const int topk = t.top_k ? t.top_k[b] : 0;
   const float topp = t.top_p ? t.top_p[b] : 1.f;
   const bool dok = topk > 0 && int64_t(topk) < V;
   const bool dop = topp > 0.f && topp < 1.f;
-  // Windows of 256 keys from the row's max down.  top-k: the first key whose count from the
-  // top reaches k; top-p: then the first key whose kept mass from the top reaches top_p times
-  // the top-k-kept mass.  Both are exact: a window is searched key by key.
-  const uint32_t ktop = key16(__float_as_uint(M) >> 16);
+  // An estimate of the row's max from kSampleRuns runs of kThreads vectors spread over the row fixes
+  // the window of the one pass: kFusedWidth keys from kGuardKeys keys above the estimate.
+  float ms;
+  {
+    const int64_t nvec = (V + 7) / 8;
+    const int64_t stride = nvec / kSampleRuns > kThreads ? nvec / kSampleRuns : int64_t(kThreads);
+    __nv_bfloat162 h = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+#pragma unroll
+    for (int q = 0; q < kSampleRuns; ++q) {
+      const int64_t vi = int64_t(q) * stride + tid;
+      if (vi < nvec) {
+        const uint4 v = vec_at<Bf16, kVec>(row, vi * 8, V);
+        const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+        h = __hmax2(h, __hmax2(__hmax2(p2[0], p2[1]), __hmax2(p2[2], p2[3])));
+      }
+    }
+    ms = block_max_f32(fmaxf(__low2float(h), __high2float(h)), ts);
+  }
+  const uint32_t top = key16(__float_as_uint(ms) >> 16) + kGuardKeys;
+  const bool fused = top <= 0xff7fu;       // the window stays among finite values
+  float M = -INFINITY;
   uint32_t kmin = 0;                       // smallest kept key (0: everything)
   unsigned long long kept = 0;             // mass of the keys >= kmin
-  if (!dok && !dop) {
-    kept = trunc_total<kVec>(row, V, 0, k, mk, ts);
-  } else {
-    if (dok) {
-      uint32_t hi = ktop, need = uint32_t(topk);
-      for (;;) {
-        trunc_window<kVec>(row, V, hi, k, mk, ts);
-        if (tid == 0) {
-          int found = -1;
-          uint32_t acc = 0;
-          unsigned long long m_acc = 0;
-          for (int d = 0; d < 256 && d <= int(hi); ++d) {
-            acc += ts.cnt[d];
-            m_acc += ts.mass[d];
-            if (acc >= need) { found = d; break; }
-          }
-          s_key[0] = found >= 0 ? hi - uint32_t(found) : 0xffffffffu;
-          s_key[1] = need - (found >= 0 ? 0u : acc);
-          s_mass = m_acc;
-        }
-        __syncthreads();
-        kept += s_mass;
-        const uint32_t res = s_key[0];
-        need = s_key[1];
-        __syncthreads();
-        if (res != 0xffffffffu) { kmin = res; break; }
-        if (hi < 256) break;   // no key left (cannot happen for k < V)
-        hi -= 256;
-      }
+  bool done = false;
+  if (fused) {
+    const Window win(top, kFusedWidth);
+    const bool below = !dok;               // the whole row's mass is wanted
+    const float vk = __fmul_rn(win.vlo, k);
+    unsigned* cnt = &ts.cnt[0][0];         // [0]: keys top..top-255, [1]: the next 256
+    for (int i = tid; i < 512; i += kThreads) cnt[i] = 0;
+    __syncthreads();
+    __nv_bfloat162 h = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+    float f = 0.f;
+    if (win.fast) {
+      if (below) fused_pass<kVec, true, true>(row, V, win, k, vk, cnt, h, f);
+      else fused_pass<kVec, true, false>(row, V, win, k, vk, cnt, h, f);
     } else {
-      kept = trunc_total<kVec>(row, V, 0, k, mk, ts);
+      if (below) fused_pass<kVec, false, true>(row, V, win, k, vk, cnt, h, f);
+      else fused_pass<kVec, false, false>(row, V, win, k, vk, cnt, h, f);
     }
-    if (dop) {
-      const unsigned long long target = (unsigned long long)ceil(double(topp) * double(kept));
-      uint32_t hi = ktop;
-      unsigned long long acc = 0;
-      for (;;) {
-        trunc_window<kVec>(row, V, hi, k, mk, ts);
-        if (tid == 0) {
-          int found = -1;
-          unsigned long long a2 = acc;
-          for (int d = 0; d < 256 && d <= int(hi) && hi - uint32_t(d) >= kmin; ++d) {
-            a2 += ts.mass[d];
-            if (a2 >= target) { found = d; break; }
-          }
-          s_key[0] = found >= 0 ? hi - uint32_t(found) : 0xffffffffu;
-          s_mass = a2;
-        }
-        __syncthreads();
-        const uint32_t res = s_key[0];
-        acc = s_mass;
-        __syncthreads();
-        if (res != 0xffffffffu) { kmin = res; kept = acc; break; }
-        if (hi < 256 || hi - 256 < kmin) break;   // cannot happen: the kept mass reaches the target
-        hi -= 256;
+    __syncthreads();
+    M = block_max_f32(fmaxf(__low2float(h), __high2float(h)), ts);
+    const float mk = __fmul_rn(M, k);
+    if (key16(__float_as_uint(M) >> 16) <= top) {
+      // the window holds the max: its counts serve the search's first windows
+      unsigned long long rest = 0, massb = 0;   // masses under both windows, of the second window
+      if (below) {
+        // per thread from the window's lowest value to the max (a factor at most 1), then fixed point
+        rest = block_sum_u64(__float2ull_rn(__fmul_rn(f, ex2(vk - mk)) * kMassUnit), ts);
+        if (kFusedWidth > 256) massb = bins_mass(cnt + 256, top - 256u, k, mk, ts);
       }
+      if (!dok && !dop) {
+        kept = bins_mass(cnt, top, k, mk, ts) + massb + rest;
+      } else {
+        int cur = 0;                        // which count array the last window is in
+        bool pre = true;                    // the fused counts are still there
+        trunc_search(
+            ts,
+            [&](uint32_t hi, bool blw) -> unsigned long long {
+              if (pre && hi == top) { cur = 0; return blw ? massb + rest : 0ull; }
+              if (pre && kFusedWidth > 256 && hi == top - 256u) { cur = 1; return blw ? rest : 0ull; }
+              pre = false;
+              cur = 0;
+              return trunc_window<kVec>(row, V, hi, blw, k, mk, ts);
+            },
+            [&](int d) { return ts.cnt[cur][d]; }, top, topk, topp, dok, dop, k, mk, kmin, kept);
+      }
+      done = true;
     }
   }
+  if (!done) {
+    // the estimate missed (or no window fits): the max, then windows from it down
+    if (!fused) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+      for_each_vec<kVec>(row, V, [&](const uint4& v, int) {
+        const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+        h = __hmax2(h, __hmax2(__hmax2(p2[0], p2[1]), __hmax2(p2[2], p2[3])));
+      });
+      M = block_max_f32(fmaxf(__low2float(h), __high2float(h)), ts);
+    }
+    const float mk = __fmul_rn(M, k);
+    const uint32_t ktop = key16(__float_as_uint(M) >> 16);
+    if (!dok && !dop) {
+      kept = trunc_total<kVec>(row, V, k, mk, ts);
+    } else {
+      trunc_search(
+          ts, [&](uint32_t hi, bool below) { return trunc_window<kVec>(row, V, hi, below, k, mk, ts); },
+          [&](int d) { return ts.cnt[0][d]; }, ktop, topk, topp, dok, dop, k, mk, kmin, kept);
+    }
+  }
+  const float mk = __fmul_rn(M, k);
   if (tid == 0) {
     RowInfo r;
     r.mk = mk;
@@ -1883,7 +2134,8 @@ int launch_truncated(const Args& args, const TruncArgs& t, void* ws, size_t ws_b
   geo.b0 = 0;
   geo.b1 = args.B;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  trunc_rows_kernel<kVec><<<unsigned(int64_t(args.B) * nslots), kThreads, 0, s>>>(args, t, info, nslots);
+  const int64_t rows = int64_t(args.B) * nslots;
+  trunc_rows_kernel<kVec><<<unsigned(rows), kThreads, 0, s>>>(args, t, info, nslots);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "truncation rows kernel launch");
   count_launch();

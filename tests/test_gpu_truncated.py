@@ -102,3 +102,33 @@ def test_repeat_runs_are_bit_identical():
     for key in ("out", "m", "status"):
         assert np.array_equal(a[key], b[key])
     assert np.array_equal(a["diag"].view(np.int32), b["diag"].view(np.int32))
+
+
+@pytest.mark.parametrize("V", [40000, 151936, 262144, 5001, 270000])
+def test_row_layouts(V):
+    """Rows split over 2, 5 and 8 CTAs' shared memory, a vocabulary that is not a multiple of
+    8 (the scalar load path) and rows longer than eight slices (searched from global memory)."""
+    wl = W.sampling_workload(f"trunc-V{V}", cfg=76, seed=5, B=6, gmax=3, V=V, dtype="bf16",
+                             target_sigma=3.0, draft_scale=0.8, draft_sigma=1.0,
+                             temperature=[0.8, 1.0, 0.0, 0.7, 1.2, 0.9], num_draft=[3, 3, 3, 2, 3, 0],
+                             greedy_mask=[0, 0, 1, 0, 0, 0])
+    check(wl, [50, 0, 10, 1000, 20, 0], [0.9, 0.8, 1.0, 1.0, 0.5, 0.95])
+
+
+def test_fused_window_edges():
+    """The one-pass search fixes its window from a sample of the row before the pass.  Rows where
+    that sample misses the max by far (a planted outlier: the row is searched again from the true
+    max), rows of negative logits (windows below zero compare keys), a top-k crossing below both
+    fused windows, a low temperature and logits near zero."""
+    B = 8
+    wl = W.sampling_workload("trunc-fused", cfg=77, seed=6, B=B, gmax=3, V=128256, dtype="bf16",
+                             target_sigma=3.0, draft_scale=0.8, draft_sigma=1.0,
+                             temperature=[0.8, 1.0, 0.9, 0.05, 1.0, 0.7, 0.8, 1.0], boost_frac=0.01, boost=8.0)
+    for arr in (wl.target, wl.draft):
+        f = W.bf16_bits_to_f32(arr).astype(np.float32)
+        f[0, :, 8003] = 60.0           # id 8003 lies outside the sampled runs
+        f[5, :, 77777] = 45.0
+        f[1] -= 40.0                   # every logit negative
+        f[4] *= 1e-3                   # logits near zero
+        arr[...] = W.f32_to_bf16_bits(f)
+    check(wl, [50, 0, 40000, 0, 100, 20, 0, 0], [0.9, 0.9, 1.0, 0.9, 0.95, 1.0, 1.0, 0.7])
