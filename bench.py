@@ -478,7 +478,7 @@ def run_native(args):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": ("verify_kernel<bf16, vec, greedy> (spec_verify_tree_greedy)" if tree
-                                    else "trunc_rows + trunc_decide + trunc_draw kernels (spec_verify_sample_truncated)"
+                                    else "trunc_rows + trunc_draw kernels (spec_verify_sample_truncated)"
                                     if trunc
                                     else "verify_kernel<bf16, vec, greedy> (spec_verify_greedy)" if wl.greedy_only
                                     else "verify_kernel<bf16, vec, mixed> (spec_verify_sample)"),

@@ -146,7 +146,7 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits, int 
  * of a sampling sequence: a sample of the row places the window before the pass, which also
  * takes the row's max.  A row whose max lies more than 96 keys above the sample's, or whose
  * threshold lies below the window, is read again, once per further window.  Then come the
- * decisions and the draw: three kernel launches in all.  The workspace is
+ * decisions and the draw: two kernel launches in all.  The workspace is
  * spec_verify_workspace_bytes(B, gmax, V, dtype) bytes, as for spec_verify_sample.
  */
 int spec_verify_sample_truncated(const void* target_logits, const void* draft_logits, int dtype,
@@ -222,7 +222,7 @@ int spec_verify_sample_split(const void* saved_logits, const void* block_logits,
  * The workspace is an array of SPEC_STATIC_WORKSPACE_BYTES bytes compiled into the library,
  * one per device, shared by every call of this function on that device:
  *   - Calls whose sizes need more (spec_verify_workspace_bytes(B, gmax, V, dtype) above
- *     SPEC_STATIC_WORKSPACE_BYTES: B = 1056 at gmax = 4, V = 128256 and B = 873 at
+ *     SPEC_STATIC_WORKSPACE_BYTES: B = 1110 at gmax = 4, V = 128256 and B = 910 at
  *     gmax = 4, V = 151936 are the largest that fit) return SPEC_ENOSPACE before touching
  *     the device.
  *   - The first call on a device looks the array up (cudaGetSymbolAddress), clears it and

@@ -1854,12 +1854,11 @@ __global__ void __launch_bounds__(kThreads) trunc_rows_kernel(const Args a, cons
   }
 }
 
-// One warp per sequence: the acceptance decisions on the truncated p', q' (or the greedy
-// compare), the outputs of greedy sequences, and the plan of the draw.
-__global__ void __launch_bounds__(32) trunc_decide_kernel(const Args a, const RowInfo* info, int nslots,
-                                                          PlanRec* plans) {
-  const int lane = int(threadIdx.x);
-  const int b = int(blockIdx.x);
+// One warp: sequence b's acceptance decisions on the truncated p', q' (or the greedy compare)
+// and the plan of its draw (returned in lane 0).  `writer`: also the diag entries and, for a
+// greedy sequence, its outputs (one warp per sequence does that).
+__device__ PlanRec trunc_decide(const Args& a, const RowInfo* info, int nslots, int b, bool writer) {
+  const int lane = int(threadIdx.x) & 31;
   const Seq<Bf16, true> sq(a, b);
   const int g = sq.g, gmax = a.gmax;
   const RowInfo* ri = info + int64_t(b) * nslots;
@@ -1888,7 +1887,7 @@ __global__ void __launch_bounds__(32) trunc_decide_kernel(const Args a, const Ro
   const unsigned bad = __ballot_sync(kFull, lane < g && !valid);
   int flags = sq.flags;
   if (m < g && ((bad >> m) & 1u)) flags |= SPEC_ST_BAD_DRAFT;
-  if (a.diag) {   // gmax <= 32: lane i writes draft i's p'(d_i), q'(d_i)
+  if (writer && a.diag) {   // gmax <= 32: lane i writes draft i's p'(d_i), q'(d_i)
     float* dg = a.diag + int64_t(b) * (2 * gmax + 1);
     if (lane < gmax) {
       dg[2 * lane] = (sq.sampling && lane < g) ? p : NAN;
@@ -1896,7 +1895,9 @@ __global__ void __launch_bounds__(32) trunc_decide_kernel(const Args a, const Ro
     }
     if (!sq.sampling && lane == 0) dg[2 * gmax] = NAN;
   }
+  PlanRec pr = {};
   if (!sq.sampling) {
+    if (!writer) return pr;
     for (int i = lane; i <= gmax; i += 32) {
       int v = -1;
       if (i < m) v = a.draft_tokens[int64_t(b) * gmax + i];
@@ -1907,11 +1908,10 @@ __global__ void __launch_bounds__(32) trunc_decide_kernel(const Args a, const Ro
       a.num_accepted[b] = m;
       if (a.status) a.status[b] = flags;
     }
-    return;
+    return pr;
   }
   if (lane == 0) {
     const RowInfo rp = ri[m];
-    PlanRec pr;
     pr.m = m;
     pr.g = g;
     pr.flags = flags;
@@ -1928,30 +1928,38 @@ __global__ void __launch_bounds__(32) trunc_decide_kernel(const Args a, const Ro
       pr.mkq = pr.invq = 0.f;
       pr.tauq = 0.f;
     }
-    plans[b] = pr;
   }
+  return pr;
 }
 
-// Draw chunk dc of sequence b (sampling sequences), on the plan the decisions left; the last
-// chunk to finish selects the token and writes the outputs.
+// Draw chunk dc of sequence b (sampling sequences): warp 0 first takes the sequence's decisions
+// (every chunk alike, so no plan is handed over; chunk 0 also writes the diag and a greedy
+// sequence's outputs), then the chunk's part of the draw; the last chunk to finish selects the
+// token and writes the outputs.
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads) trunc_draw_kernel(const Args a, const Geo geo, const Work w,
-                                                              PlanRec* plans, RowInfo* info, int nslots) {
+                                                              RowInfo* info, int nslots) {
   __shared__ Shared sm;
   const int64_t idx = int64_t(blockIdx.x);
   const int dc = int(idx % geo.DCL), b = int(idx / geo.DCL);
   const Seq<Bf16, true> sq(a, b);
+  if (!sq.sampling && dc != 0) return;
+  if (threadIdx.x < 32) {
+    const PlanRec pr = trunc_decide(a, info, nslots, b, dc == 0);
+    if (threadIdx.x == 0) sm.plan = pr;
+  }
+  __syncthreads();
   if (sq.sampling) {
-    const PlanRec pl = plans[b];
+    const PlanRec pl = sm.plan;
     draw_chunk<Bf16, kVec, true, true>(a, geo, w, sq, pl, dc, sm);
   } else {
-    sm.last = dc == 0;   // one unit of a greedy sequence clears what the call used
+    sm.last = true;   // unit 0 of a greedy sequence clears what the call used
   }
   __syncthreads();
   if (!sm.last) return;
-  // the selector (or a greedy sequence's unit 0): every word of b returns to zero
+  // the selector (or a greedy sequence's unit 0), after every chunk of b has read its rows'
+  // records: they return to zero
   for (int i = int(threadIdx.x); i < nslots; i += kThreads) info[int64_t(b) * nslots + i] = RowInfo{0.f, 0.f, 0.f, 0};
-  if (threadIdx.x == 0) plans[b] = PlanRec{};
 }
 
 // ------------------------------------------------------------------------------------------
@@ -1987,7 +1995,7 @@ size_t align64(size_t x) { return (x + 63) & ~size_t(63); }
 // Workspace layout: counters and published words only, all zero between calls (each call
 // returns every word it used to zero), so calls of any sizes can share one workspace.
 struct WsLayout {
-  size_t cnt, bdone, planw, state, part, xd, mass, info, plans, end;
+  size_t cnt, bdone, planw, state, part, xd, mass, info, end;
 };
 
 WsLayout ws_layout(int B, int gmax, int64_t V) {
@@ -2002,8 +2010,7 @@ WsLayout ws_layout(int B, int gmax, int64_t V) {
   L.xd = L.part + align64(size_t(B) * nslots * s.cl * 8);
   L.mass = L.xd + align64(size_t(B) * nslots * 8);
   L.info = L.mass + align64(size_t(B) * s.dcl * kWarps * 8);   // truncated sampling only
-  L.plans = L.info + align64(size_t(B) * nslots * sizeof(RowInfo));
-  L.end = L.plans + align64(size_t(B) * sizeof(PlanRec));
+  L.end = L.info + align64(size_t(B) * nslots * sizeof(RowInfo));
   return L;
 }
 
@@ -2106,7 +2113,7 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
   return SPEC_OK;
 }
 
-// truncated sampling: thresholds per row, decisions per sequence, then the draw; three launches
+// truncated sampling: thresholds per row, then decisions and the draw per sequence; two launches
 template <bool kVec>
 int launch_truncated(const Args& args, const TruncArgs& t, void* ws, size_t ws_bytes, void* stream) {
   if (!ws || !ws_fits(args.B, args.gmax, args.V, ws_bytes)) {
@@ -2123,7 +2130,6 @@ int launch_truncated(const Args& args, const TruncArgs& t, void* ws, size_t ws_b
   const Work w = ws_views(ws, L);
   unsigned char* base = static_cast<unsigned char*>(ws);
   RowInfo* info = reinterpret_cast<RowInfo*>(base + L.info);
-  PlanRec* plans = reinterpret_cast<PlanRec*>(base + L.plans);
   const int nslots = 2 * args.gmax + 1;
   Geo geo = {};
   geo.CL = sp.cl;
@@ -2139,11 +2145,7 @@ int launch_truncated(const Args& args, const TruncArgs& t, void* ws, size_t ws_b
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "truncation rows kernel launch");
   count_launch();
-  trunc_decide_kernel<<<unsigned(args.B), 32, 0, s>>>(args, info, nslots, plans);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "truncation decide kernel launch");
-  count_launch();
-  trunc_draw_kernel<kVec><<<unsigned(int64_t(args.B) * geo.DCL), kThreads, 0, s>>>(args, geo, w, plans, info, nslots);
+  trunc_draw_kernel<kVec><<<unsigned(int64_t(args.B) * geo.DCL), kThreads, 0, s>>>(args, geo, w, info, nslots);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "truncation draw kernel launch");
   count_launch();

@@ -154,7 +154,7 @@ def test_static_workspace_limits_in_header():
     """The largest batches the static workspace takes, as include/specverify.h states them."""
     text = open(os.path.join(ROOT, "include", "specverify.h"), encoding="utf-8").read()
     cap = 1 << 20
-    for B, V in ((1056, 128256), (873, 151936)):
+    for B, V in ((1110, 128256), (910, 151936)):
         assert f"B = {B} at" in text and f"V = {V}" in text
         assert sv.spec_verify_workspace_bytes(B, 4, V) <= cap < sv.spec_verify_workspace_bytes(B + 1, 4, V)
 
