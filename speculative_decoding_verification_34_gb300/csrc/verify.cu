@@ -62,6 +62,7 @@ constexpr int kDrawVec = SPEC_DRAW_VEC;                // vectors of each row pe
 constexpr bool kPrefetch = SPEC_PREFETCH != 0;         // row passes double-buffered in registers
 constexpr int kRing = SPEC_RING;                       // >0: row passes staged through a ring of
                                                        // this many 16 KB shared-memory stages
+constexpr int kRingSlots = kRing > 0 ? kRing : 1;       // the ring's modulus (1 when it is off)
 constexpr int kStageBytes = kThreads * kVecPerPass * 16;   // one pass of one row (bf16 or fp32)
 constexpr long long kMbarWaitNs = 2000000;             // bound on one stage wait (2 ms)
 constexpr int kMaxChunks = 64;                         // row chunks per row
@@ -207,12 +208,6 @@ __device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
 __device__ __forceinline__ int atom_add_relaxed(int* p, int v) {
   int old;
   asm volatile("atom.relaxed.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
-__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
 }
 
@@ -492,7 +487,7 @@ __device__ __forceinline__ void mbar_expect(uint64_t* bar, unsigned bytes) {
                : "memory");
 }
 // global -> shared bulk copy (16-byte aligned addresses, size a multiple of 16)
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+__device__ __forceinline__ __attribute__((unused)) void bulk_load(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                    smem_addr(dst)),
                "l"(src), "r"(bytes), "r"(smem_addr(bar))
@@ -1209,7 +1204,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
       extern __shared__ __align__(128) unsigned char ring[];
       const int npass = lo < hi ? int((hi - lo + kPass - 1) / kPass) : 0;
       auto issue = [&](int p) {
-        const int st = p % kRing;
+        const int st = p % kRingSlots;
         const int64_t e0 = lo + int64_t(p) * kPass;
         const int64_t n = hi - e0 < kPass ? hi - e0 : kPass;
         const unsigned bytes = unsigned(n * int64_t(sizeof(raw)));
@@ -1224,9 +1219,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
       }
       __syncthreads();
       for (int p = 0; p < npass; ++p) {
-        const int st = p % kRing;
+        const int st = p % kRingSlots;
         const int64_t e0 = lo + int64_t(p) * kPass;
-        if (!mbar_wait(&sm.bars[st], unsigned(p / kRing) & 1u)) sm.err = 1;
+        if (!mbar_wait(&sm.bars[st], unsigned(p / kRingSlots) & 1u)) sm.err = 1;
         Tile<E, kVec> t;
 #pragma unroll
         for (int q = 0; q < kVecPerPass; ++q) {
@@ -1243,7 +1238,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
         // report the sequence
         if (tid == 0) {
           for (int p = npass - kRing > 0 ? npass - kRing : 0; p < npass; ++p)
-            mbar_wait(&sm.bars[p % kRing], unsigned(p / kRing) & 1u);
+            mbar_wait(&sm.bars[p % kRingSlots], unsigned(p / kRingSlots) & 1u);
           if (a.status) atomicOr(&a.status[b], SPEC_ST_TIMEOUT);
         }
         __syncthreads();
@@ -1481,7 +1476,18 @@ __device__ __forceinline__ void for_each_vec(const uint16_t* row, int64_t V, Fn 
   constexpr int kVecs = 8;
   constexpr int kStep = kThreads * 8 * kVecs;
   const int tid = int(threadIdx.x);
-  for (int64_t e0 = 0; e0 < V; e0 += kStep) {
+  int64_t e0 = 0;
+  if constexpr (kVec) {
+    // whole steps: every vector inside the row (V is a multiple of 8 here), no checks
+    for (; e0 + kStep <= V; e0 += kStep) {
+      uint4 v[kVecs];
+#pragma unroll
+      for (int q = 0; q < kVecs; ++q) v[q] = ld_stream(row + e0 + int64_t(q * kThreads + tid) * 8);
+#pragma unroll
+      for (int q = 0; q < kVecs; ++q) fn(v[q], 8);
+    }
+  }
+  for (; e0 < V; e0 += kStep) {
     uint4 v[kVecs];
 #pragma unroll
     for (int q = 0; q < kVecs; ++q) v[q] = vec_at<Bf16, kVec>(row, e0 + int64_t(q * kThreads + tid) * 8, V);
