@@ -1950,6 +1950,8 @@ __global__ void __launch_bounds__(kThreads) trunc_draw_kernel(const Args a, cons
   const int dc = int(idx % geo.DCL), b = int(idx / geo.DCL);
   const Seq<Bf16, true> sq(a, b);
   if (!sq.sampling && dc != 0) return;
+  // launched while the row kernel finishes: its records are complete and visible after this
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (threadIdx.x < 32) {
     const PlanRec pr = trunc_decide(a, info, nslots, b, dc == 0);
     if (threadIdx.x == 0) sm.plan = pr;
@@ -2151,8 +2153,19 @@ int launch_truncated(const Args& args, const TruncArgs& t, void* ws, size_t ws_b
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "truncation rows kernel launch");
   count_launch();
-  trunc_draw_kernel<kVec><<<unsigned(int64_t(args.B) * geo.DCL), kThreads, 0, s>>>(args, geo, w, info, nslots);
-  e = cudaGetLastError();
+  {
+    // programmatic dependent launch: the draw's blocks start as the row kernel's drain
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(int64_t(args.B) * geo.DCL));
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, trunc_draw_kernel<kVec>, args, geo, w, info, nslots);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "truncation draw kernel launch");
   count_launch();
   return SPEC_OK;
