@@ -1401,6 +1401,10 @@ static_assert(kFusedWidth == 256 || kFusedWidth == 512, "one or two windows of 2
 #define SPEC_TRUNC_SAMPLE_RUNS 4
 #endif
 constexpr int kSampleRuns = SPEC_TRUNC_SAMPLE_RUNS;     // runs of kThreads vectors the estimate reads
+#ifndef SPEC_TRUNC_DRAW_CHUNK
+#define SPEC_TRUNC_DRAW_CHUNK 32768
+#endif
+constexpr int kTruncDrawChunk = SPEC_TRUNC_DRAW_CHUNK;  // ids per draw unit of the truncated draw
 
 // order-preserving 16-bit key of a bf16 logit; -0 is taken as +0 so equal values share a key
 __device__ __forceinline__ uint32_t key16(uint32_t bits) {
@@ -2142,8 +2146,8 @@ int launch_truncated(const Args& args, const TruncArgs& t, void* ws, size_t ws_b
   Geo geo = {};
   geo.CL = sp.cl;
   geo.chunk = sp.chunk;
-  geo.DCL = sp.dcl;
-  geo.dchunk = sp.dchunk;
+  // draw chunks of about kTruncDrawChunk ids, no more than the workspace layout holds
+  cut(args.V, kTruncDrawChunk, sp.dcl, kWarps * 8, geo.DCL, geo.dchunk);
   geo.nslots = nslots;
   geo.b0 = 0;
   geo.b1 = args.B;
