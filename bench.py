@@ -109,6 +109,33 @@ def measured_peak():
     return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
 
 
+def code_sha256(path):
+    """sha256 of a C/CUDA source with its comments removed and its whitespace collapsed, so that
+    an edit of comments alone keeps a recorded measurement of the compiled code valid."""
+    text = open(path, encoding="utf-8").read()
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":                       # string or character literal, escapes kept
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    code = " ".join("".join(out).split())
+    return hashlib.sha256(code.encode("utf-8")).hexdigest()
+
+
 def recorded_traffic(units_per_launch):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on this exact
     kernel source; else None."""
@@ -119,8 +146,7 @@ def recorded_traffic(units_per_launch):
         if ":" in line and not line.startswith("#"):
             k, v = line.split(":", 1)
             kv[k.strip()] = v.strip()
-    sha = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
-    if kv.get("source_sha256") != sha:
+    if kv.get("code_sha256") != code_sha256(KERNEL_SRC):
         return None
     try:
         return int(kv["dram_bytes_per_launch"])

@@ -1371,9 +1371,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
 // sampling sequence one block finds the row's max M, then the smallest kept logit tau: top-k
 // keeps the logits >= the k-th largest (ties kept), top-p then keeps those >= the largest t
 // whose kept mass at or above t reaches top_p times the top-k-kept mass.  Both thresholds are
-// found exactly by a radix search over order-preserving 16-bit keys of the bf16 logits, one
-// byte per pass, with counts and fixed-point masses (2^-40 units, summed in integers, so
-// every run gives the same bits).  The row's normaliser is the kept mass; p'(v) = 0 below tau.
+// found exactly by counting the ids of each order-preserving 16-bit key of the bf16 logits in
+// windows of 256 keys from the top: all ids of one key share one logit, so a key's mass is
+// its count times that logit's mass, in fixed point (2^-40 units, summed in integers, so every
+// run gives the same bits).  A sample of the row places the first window before the one pass
+// that also takes M; further windows, if any, are further passes.  The row's normaliser is the
+// kept mass; p'(v) = 0 below tau.
 
 struct TruncArgs {
   const int32_t* top_k;   // [B] or null
@@ -1518,16 +1521,16 @@ struct Window {
   }
 };
 
-// One vector's part of a window pass.  kFast: a logit is in the window iff its code minus blo is
-// below the width (unsigned; negative logits wrap far above), its bin is width-1 minus that, and padding
-// (-inf) is never in it; otherwise the order-preserving key decides, ids past nvalid skipped.
-// With kBelow, the ids under the window add their mass to f, in id order.
 // adds 1 to the shared word at addr when t < width, without a branch
 __device__ __forceinline__ void count_if(uint32_t t, uint32_t width, uint32_t addr) {
   asm volatile("{\n\t.reg .pred p;\n\tsetp.lt.u32 p, %0, %1;\n\t@p red.shared.add.u32 [%2], 1;\n\t}" ::"r"(t), "r"(width),
                "r"(addr));
 }
 
+// One vector's part of a window pass.  kFast: a logit is in the window iff its code minus blo
+// is below the width (unsigned; negative logits wrap far above), its bin is width-1 minus
+// that, and padding (-inf) is never in it; otherwise the order-preserving key decides, ids past
+// nvalid skipped.  With kBelow, the ids under the window add their mass to f, in id order.
 template <bool kFast, bool kBelow>
 __device__ __forceinline__ void window_vec(const uint4& v, int nvalid, const Window& win, float k, float mk,
                                            unsigned* cnt, float& f) {
@@ -1554,7 +1557,7 @@ __device__ __forceinline__ void window_vec(const uint4& v, int nvalid, const Win
 
 // One window pass: bin d counts the ids of key hi - d (d < 256).  Every id of one key has the
 // same logit, so a bin's mass is its count times that logit's exp: counting is all the pass does
-// per id inside the window (one 32-bit shared atomic), ids above it are skipped, and with `below`
+// per id inside the window (one 32-bit shared reduction), ids above it are skipped, and with `below`
 // the ids under it add their mass to a per-thread float sum, returned as the block's fixed-point
 // total.
 template <bool kVec>
@@ -1648,8 +1651,9 @@ __device__ float block_max_f32(float m, TruncShared& ts) {
   return r;
 }
 
-// the fixed-point mass of 256 counted bins (bin d: key hi - d), all threads taking part
+// the fixed-point mass of 256 counted bins (bin d: key hi - d), thread d taking bin d
 __device__ unsigned long long bins_mass(const unsigned* cnt, uint32_t hi, float k, float mk, TruncShared& ts) {
+  static_assert(kThreads == 256, "one bin per thread");
   const int d = int(threadIdx.x);
   const unsigned c = cnt[d];
   const unsigned long long w =

@@ -49,3 +49,4 @@ def test_two_rank_sharding_and_timing():
         assert (b0, g0, v0) == (b1, g1, v1) == (8, 4, 1024)
         assert d0 != d1                                # each rank has its own batch
         assert abs(value - 2 * 32 * 100 / 0.015) < 1e-6
+
