@@ -1445,6 +1445,17 @@ __device__ unsigned long long block_sum_u64(unsigned long long s, TruncShared& t
   return t;
 }
 
+// the block's max of one value per thread, returned to every thread
+__device__ float block_max_f32(float m, TruncShared& ts) {
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) ts.wm[threadIdx.x >> 5] = m;
+  __syncthreads();
+  float r = ts.wm[0];
+  for (int i = 1; i < kWarps; ++i) r = fmaxf(r, ts.wm[i]);
+  __syncthreads();
+  return r;
+}
+
 // Visits every id of a row once: fn(x, bits, id) per element, eight 16-byte vectors per thread
 // per step, coalesced across the block.
 template <bool kVec, class Fn>
@@ -1531,9 +1542,10 @@ __device__ __forceinline__ void count_if(uint32_t t, uint32_t width, uint32_t ad
 // is below the width (unsigned; negative logits wrap far above), its bin is width-1 minus
 // that, and padding (-inf) is never in it; otherwise the order-preserving key decides, ids past
 // nvalid skipped.  With kBelow, the ids under the window add their mass to f, in id order.
-template <bool kFast, bool kBelow>
+// With kNext, xb keeps the largest logit under the window (where the next window can start).
+template <bool kFast, bool kBelow, bool kNext = false>
 __device__ __forceinline__ void window_vec(const uint4& v, int nvalid, const Window& win, float k, float mk,
-                                           unsigned* cnt, float& f) {
+                                           unsigned* cnt, float& f, float& xb) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   const uint32_t clast = smem_addr(cnt) + 4u * (win.width - 1u);   // bin width-1: code blo
 #pragma unroll
@@ -1542,15 +1554,20 @@ __device__ __forceinline__ void window_vec(const uint4& v, int nvalid, const Win
     if constexpr (kFast) {
       const uint32_t t = bits - win.blo;
       count_if(t, win.width, clast - 4u * t);
-      if constexpr (kBelow) {
+      if constexpr (kBelow || kNext) {
         const float x = __uint_as_float(bits << 16);
-        f = __fadd_rn(f, x < win.vlo ? ex2(fmaf(x, k, -mk)) : 0.f);
+        if constexpr (kBelow) f = __fadd_rn(f, x < win.vlo ? ex2(fmaf(x, k, -mk)) : 0.f);
+        if constexpr (kNext) xb = fmaxf(xb, x < win.vlo ? x : -INFINITY);
       }
     } else {
       if (j >= nvalid) break;
       const float x = __uint_as_float(bits << 16);
-      if (kBelow && x < win.vlo) f = __fadd_rn(f, ex2(fmaf(x, k, -mk)));
-      else if (x >= win.vlo && x <= win.vhi) atomicAdd(&cnt[win.hi - key16(bits)], 1u);
+      if (x < win.vlo) {
+        if constexpr (kBelow) f = __fadd_rn(f, ex2(fmaf(x, k, -mk)));
+        if constexpr (kNext) xb = fmaxf(xb, x);
+      } else if (x <= win.vhi) {
+        atomicAdd(&cnt[win.hi - key16(bits)], 1u);
+      }
     }
   }
 }
@@ -1560,22 +1577,25 @@ __device__ __forceinline__ void window_vec(const uint4& v, int nvalid, const Win
 // per id inside the window (one 32-bit shared reduction), ids above it are skipped, and with `below`
 // the ids under it add their mass to a per-thread float sum, returned as the block's fixed-point
 // total.
+// `next` receives the key of the largest logit under the window (the key of -inf when there is
+// none): no key between it and the window holds an id, so the next window can start there.
 template <bool kVec>
 __device__ unsigned long long trunc_window(const uint16_t* row, int64_t V, uint32_t hi, bool below, float k,
-                                           float mk, TruncShared& ts) {
+                                           float mk, TruncShared& ts, uint32_t& next) {
   unsigned* cnt = ts.cnt[0];
   for (int i = int(threadIdx.x); i < 256; i += kThreads) cnt[i] = 0;
   __syncthreads();
   const Window win(hi, 256u);
-  float f = 0.f;
+  float f = 0.f, xb = -INFINITY;
   if (win.fast) {
-    if (below) for_each_vec<kVec>(row, V, [&](const uint4& v, int nv) { window_vec<true, true>(v, nv, win, k, mk, cnt, f); });
-    else for_each_vec<kVec>(row, V, [&](const uint4& v, int nv) { window_vec<true, false>(v, nv, win, k, mk, cnt, f); });
+    if (below) for_each_vec<kVec>(row, V, [&](const uint4& v, int nv) { window_vec<true, true, true>(v, nv, win, k, mk, cnt, f, xb); });
+    else for_each_vec<kVec>(row, V, [&](const uint4& v, int nv) { window_vec<true, false, true>(v, nv, win, k, mk, cnt, f, xb); });
   } else {
-    if (below) for_each_vec<kVec>(row, V, [&](const uint4& v, int nv) { window_vec<false, true>(v, nv, win, k, mk, cnt, f); });
-    else for_each_vec<kVec>(row, V, [&](const uint4& v, int nv) { window_vec<false, false>(v, nv, win, k, mk, cnt, f); });
+    if (below) for_each_vec<kVec>(row, V, [&](const uint4& v, int nv) { window_vec<false, true, true>(v, nv, win, k, mk, cnt, f, xb); });
+    else for_each_vec<kVec>(row, V, [&](const uint4& v, int nv) { window_vec<false, false, true>(v, nv, win, k, mk, cnt, f, xb); });
   }
   __syncthreads();
+  next = key16(__float_as_uint(block_max_f32(xb, ts)) >> 16);
   return below ? block_sum_u64(__float2ull_rn(f * kMassUnit), ts) : 0ull;
 }
 
@@ -1640,17 +1660,6 @@ __device__ unsigned long long trunc_total(const uint16_t* row, int64_t V, float 
   return block_sum_u64(__float2ull_rn(f * kMassUnit), ts);
 }
 
-// the block's max of one value per thread, returned to every thread
-__device__ float block_max_f32(float m, TruncShared& ts) {
-  m = warp_max(m);
-  if ((threadIdx.x & 31) == 0) ts.wm[threadIdx.x >> 5] = m;
-  __syncthreads();
-  float r = ts.wm[0];
-  for (int i = 1; i < kWarps; ++i) r = fmaxf(r, ts.wm[i]);
-  __syncthreads();
-  return r;
-}
-
 // the fixed-point mass of 256 counted bins (bin d: key hi - d), thread d taking bin d
 __device__ unsigned long long bins_mass(const unsigned* cnt, uint32_t hi, float k, float mk, TruncShared& ts) {
   static_assert(kThreads == 256, "one bin per thread");
@@ -1671,7 +1680,8 @@ __device__ __forceinline__ void fused_pass(const uint16_t* row, int64_t V, const
   for_each_vec<kVec>(row, V, [&](const uint4& v, int nv) {
     const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v);
     h = __hmax2(h, __hmax2(__hmax2(p2[0], p2[1]), __hmax2(p2[2], p2[3])));
-    window_vec<kFast, kBelow>(v, nv, win, k, vk, cnt, f);
+    float unused = 0.f;
+    window_vec<kFast, kBelow>(v, nv, win, k, vk, cnt, f, unused);
   });
 }
 
@@ -1681,12 +1691,14 @@ __device__ __forceinline__ void fused_pass(const uint16_t* row, int64_t V, const
 // kept mass from the top reaches top_p times the top-k-kept mass.  Both are exact: a window is
 // searched key by key.  The window at the max usually holds both crossings, and its counts
 // serve both searches.  window(hi, below) runs one window pass (returning the mass under the
-// window when `below`); count(d) reads bin d of the last one.  Every thread calls this with the
-// same arguments and takes the same branches.  Leaves kmin (smallest kept key, 0: all) and kept
-// (their fixed-point mass).
-template <class WindowFn, class Count>
-__device__ void trunc_search(TruncShared& ts, WindowFn window, Count count, uint32_t top, int topk, float topp,
-                             bool dok, bool dop, float k, float mk, uint32_t& kmin, unsigned long long& kept) {
+// window when `below`); count(d) reads bin d of the last one; step(hi) gives the top of the next
+// window below it (hi - 256, or the first key under the window that holds an id, skipping empty
+// keys).  Every thread calls this with the same arguments and takes the same branches.  Leaves
+// kmin (smallest kept key, 0: all) and kept (their fixed-point mass).
+template <class WindowFn, class Count, class StepFn>
+__device__ void trunc_search(TruncShared& ts, WindowFn window, Count count, StepFn step, uint32_t top, int topk,
+                             float topp, bool dok, bool dop, float k, float mk, uint32_t& kmin,
+                             unsigned long long& kept) {
   kmin = 0;
   kept = 0;
   uint32_t hi = top;                       // the window `count` reads
@@ -1704,7 +1716,7 @@ __device__ void trunc_search(TruncShared& ts, WindowFn window, Count count, uint
       above += w;
       need -= c;
       if (hi < 256u + kKeyNegInf) { kept = above; break; }   // only with NaN logits: fewer than k ids counted
-      hi -= 256u;
+      hi = step(hi);
     }
   } else {
     // the whole row's mass: the window at the max by counts, the rest by per-thread sums
@@ -1728,7 +1740,8 @@ __device__ void trunc_search(TruncShared& ts, WindowFn window, Count count, uint
     acc += w;
     // cannot happen: the kept mass reaches the target
     if (h < 256u + kKeyNegInf || h - 256u < kmin) return;
-    h -= 256u;
+    h = step(h);
+    if (h < kmin) return;
   }
 }
 
@@ -1823,16 +1836,18 @@ __global__ void __launch_bounds__(kThreads) trunc_rows_kernel(const Args a, cons
       } else {
         int cur = 0;                        // which count array the last window is in
         bool pre = true;                    // the fused counts are still there
+        uint32_t nxt = 0;                   // the next window's top after the last counted one
         trunc_search(
             ts,
             [&](uint32_t hi, bool blw) -> unsigned long long {
-              if (pre && hi == top) { cur = 0; return blw ? massb + rest : 0ull; }
-              if (pre && kFusedWidth > 256 && hi == top - 256u) { cur = 1; return blw ? rest : 0ull; }
+              if (pre && hi == top) { cur = 0; nxt = hi - 256u; return blw ? massb + rest : 0ull; }
+              if (pre && kFusedWidth > 256 && hi == top - 256u) { cur = 1; nxt = hi - 256u; return blw ? rest : 0ull; }
               pre = false;
               cur = 0;
-              return trunc_window<kVec>(row, V, hi, blw, k, mk, ts);
+              return trunc_window<kVec>(row, V, hi, blw, k, mk, ts, nxt);
             },
-            [&](int d) { return ts.cnt[cur][d]; }, top, topk, topp, dok, dop, k, mk, kmin, kept);
+            [&](int d) { return ts.cnt[cur][d]; }, [&](uint32_t) { return nxt; }, top, topk, topp, dok, dop, k,
+            mk, kmin, kept);
       }
       done = true;
     }
@@ -1852,9 +1867,11 @@ __global__ void __launch_bounds__(kThreads) trunc_rows_kernel(const Args a, cons
     if (!dok && !dop) {
       kept = trunc_total<kVec>(row, V, k, mk, ts);
     } else {
+      uint32_t nxt = 0;
       trunc_search(
-          ts, [&](uint32_t hi, bool below) { return trunc_window<kVec>(row, V, hi, below, k, mk, ts); },
-          [&](int d) { return ts.cnt[0][d]; }, ktop, topk, topp, dok, dop, k, mk, kmin, kept);
+          ts, [&](uint32_t hi, bool below) { return trunc_window<kVec>(row, V, hi, below, k, mk, ts, nxt); },
+          [&](int d) { return ts.cnt[0][d]; }, [&](uint32_t) { return nxt; }, ktop, topk, topp, dok, dop, k, mk,
+          kmin, kept);
     }
   }
   const float mk = __fmul_rn(M, k);

@@ -132,3 +132,26 @@ def test_fused_window_edges():
         f[4] *= 1e-3                   # logits near zero
         arr[...] = W.f32_to_bf16_bits(f)
     check(wl, [50, 0, 40000, 0, 100, 20, 0, 0], [0.9, 0.9, 1.0, 0.9, 0.95, 1.0, 1.0, 0.7])
+
+
+def test_deep_crossings():
+    """Thresholds far below the max in key space (flat logits near zero, where bf16 keys are
+    dense; flat negative logits; a top-k of most of the vocabulary): the search narrows the keys
+    left to one window in a few passes instead of walking them 256 at a time."""
+    B = 6
+    wl = W.sampling_workload("trunc-deep", cfg=78, seed=7, B=B, gmax=3, V=128256, dtype="bf16",
+                             target_sigma=1.0, draft_scale=0.9, draft_sigma=0.5, temperature=1.0)
+    for arr in (wl.target, wl.draft):
+        f = W.bf16_bits_to_f32(arr).astype(np.float32)
+        f[0:3] *= 1e-3                 # flat, around zero
+        f[3:5] = f[3:5] * 1e-2 - 5.0   # flat, negative
+        arr[...] = W.f32_to_bf16_bits(f)
+    check(wl, [0, 60000, 0, 0, 100000, 127000], [0.9, 1.0, 0.5, 0.95, 0.9, 0.99])
+
+
+def test_walks_over_empty_keys():
+    """Crossings below zero on spread logits: the keys near zero hold few ids or none, and the
+    search steps from a window straight to the next key that holds one."""
+    wl = W.sampling_workload("trunc-gaps", cfg=80, seed=8, B=4, gmax=2, V=128256, dtype="bf16",
+                             target_sigma=3.0, draft_scale=0.9, draft_sigma=0.5, temperature=[5.0, 5.0, 2.0, 1.0])
+    check(wl, [0, 125000, 0, 120000], [0.999, 1.0, 0.995, 0.99])
