@@ -145,8 +145,9 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits, int 
  * order-preserving keys in windows of 256 keys from the top.  Usually one pass over each row
  * of a sampling sequence: a sample of the row places the window before the pass, which also
  * takes the row's max.  A row whose max lies more than 96 keys above the sample's, or whose
- * threshold lies below the window, is read again, once per further window.  Then come the
- * decisions and the draw: two kernel launches in all.  The workspace is
+ * threshold lies below the window, is read again, once per further window that holds ids
+ * (runs of keys holding none are skipped).  Then come the decisions and the draw: two kernel
+ * launches in all, the second a programmatic dependent launch.  The workspace is
  * spec_verify_workspace_bytes(B, gmax, V, dtype) bytes, as for spec_verify_sample.
  */
 int spec_verify_sample_truncated(const void* target_logits, const void* draft_logits, int dtype,
