@@ -158,6 +158,18 @@ int spec_verify_sample_truncated(const void* target_logits, const void* draft_lo
                                  int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * spec_verify_sample_truncated on the split layout of spec_verify_sample_split: saved_logits
+ * [B][V] is target row 0 and block_logits [B][gmax][V] holds rows 1..gmax (NULL allowed only
+ * when gmax == 0).  Same results as the one-array call on their concatenation.
+ */
+int spec_verify_sample_truncated_split(const void* saved_logits, const void* block_logits,
+                                       const void* draft_logits, int dtype, const int32_t* draft_tokens,
+                                       const int32_t* num_draft, const float* temperature, const int32_t* top_k,
+                                       const float* top_p, const float* u_accept, const float* u_sample, int B,
+                                       int gmax, int V, int32_t* out_tokens, int32_t* num_accepted, float* diag,
+                                       int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Greedy verification of a draft TREE (tutorial §5.3: the target checks every node of the
  * tree in one forward and keeps the longest accepted root-to-leaf path; card §01: a tree
  * follows its own rules).  Nodes 1..n (n = num_nodes[b], NULL: nmax) carry the draft token

@@ -2357,15 +2357,16 @@ extern "C" int spec_verify_sample_split(const void* saved_logits, const void* bl
                        workspace_bytes, stream);
 }
 
-extern "C" int spec_verify_sample_truncated(const void* target_logits, const void* draft_logits, int dtype,
-                                            const int32_t* draft_tokens, const int32_t* num_draft,
-                                            const float* temperature, const int32_t* top_k, const float* top_p,
-                                            const float* u_accept, const float* u_sample, int B, int gmax, int V,
-                                            int32_t* out_tokens, int32_t* num_accepted, float* diag,
-                                            int32_t* status, void* workspace, size_t workspace_bytes, void* stream) {
-  clear_error();
-  int rc = check_common(target_logits, dtype, draft_tokens, B, gmax, V, out_tokens, num_accepted);
-  if (rc != SPEC_OK) return rc;
+namespace specverify {
+namespace {
+
+// The truncated call on either layout: saved == nullptr, target [B][gmax+1][V]; or saved
+// [B][V] (row 0) and target [B][gmax][V] (rows 1..gmax).
+int verify_truncated(const void* saved, const void* target, const void* draft_logits, int dtype,
+                     const int32_t* draft_tokens, const int32_t* num_draft, const float* temperature,
+                     const int32_t* top_k, const float* top_p, const float* u_accept, const float* u_sample, int B,
+                     int gmax, int V, int32_t* out_tokens, int32_t* num_accepted, float* diag, int32_t* status,
+                     void* workspace, size_t workspace_bytes, void* stream) {
   if (dtype != SPEC_BF16) {
     set_error("truncated sampling takes bf16 logits");
     return SPEC_EDTYPE;
@@ -2380,7 +2381,8 @@ extern "C" int spec_verify_sample_truncated(const void* target_logits, const voi
     return SPEC_EINVAL;
   }
   Args a = {};
-  a.target = target_logits;
+  a.saved = saved;
+  a.target = target;
   a.draft = draft_logits;
   a.draft_tokens = draft_tokens;
   a.num_draft = num_draft;
@@ -2395,9 +2397,42 @@ extern "C" int spec_verify_sample_truncated(const void* target_logits, const voi
   a.diag = diag;
   a.status = status;
   TruncArgs t = {top_k, top_p};
-  const bool vec = vec_ok(target_logits, dtype, V) && vec_ok(draft_logits, dtype, V);
+  const bool vec = vec_ok(target, dtype, V) && vec_ok(draft_logits, dtype, V) && vec_ok(saved, dtype, V);
   return vec ? launch_truncated<true>(a, t, workspace, workspace_bytes, stream)
              : launch_truncated<false>(a, t, workspace, workspace_bytes, stream);
+}
+
+}  // namespace
+}  // namespace specverify
+
+extern "C" int spec_verify_sample_truncated(const void* target_logits, const void* draft_logits, int dtype,
+                                            const int32_t* draft_tokens, const int32_t* num_draft,
+                                            const float* temperature, const int32_t* top_k, const float* top_p,
+                                            const float* u_accept, const float* u_sample, int B, int gmax, int V,
+                                            int32_t* out_tokens, int32_t* num_accepted, float* diag,
+                                            int32_t* status, void* workspace, size_t workspace_bytes, void* stream) {
+  clear_error();
+  const int rc = check_common(target_logits, dtype, draft_tokens, B, gmax, V, out_tokens, num_accepted);
+  if (rc != SPEC_OK) return rc;
+  return verify_truncated(nullptr, target_logits, draft_logits, dtype, draft_tokens, num_draft, temperature, top_k,
+                          top_p, u_accept, u_sample, B, gmax, V, out_tokens, num_accepted, diag, status, workspace,
+                          workspace_bytes, stream);
+}
+
+extern "C" int spec_verify_sample_truncated_split(const void* saved_logits, const void* block_logits,
+                                                  const void* draft_logits, int dtype, const int32_t* draft_tokens,
+                                                  const int32_t* num_draft, const float* temperature,
+                                                  const int32_t* top_k, const float* top_p, const float* u_accept,
+                                                  const float* u_sample, int B, int gmax, int V, int32_t* out_tokens,
+                                                  int32_t* num_accepted, float* diag, int32_t* status,
+                                                  void* workspace, size_t workspace_bytes, void* stream) {
+  clear_error();
+  int rc = check_common(saved_logits, dtype, draft_tokens, B, gmax, V, out_tokens, num_accepted);
+  if (rc == SPEC_OK) rc = check_block(block_logits, B, gmax);
+  if (rc != SPEC_OK) return rc;
+  return verify_truncated(saved_logits, block_logits, draft_logits, dtype, draft_tokens, num_draft, temperature,
+                          top_k, top_p, u_accept, u_sample, B, gmax, V, out_tokens, num_accepted, diag, status,
+                          workspace, workspace_bytes, stream);
 }
 
 extern "C" int spec_verify_tree_greedy(const void* target_logits, int dtype, const int32_t* node_tokens,

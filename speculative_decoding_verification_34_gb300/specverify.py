@@ -57,6 +57,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.spec_verify_sample_truncated.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, sz, sz, vp, vp, vp, vp,
                                                  vp, size_t, vp]
     lib.spec_verify_sample_truncated.restype = i32
+    lib.spec_verify_sample_truncated_split.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, sz, sz, vp,
+                                                       vp, vp, vp, vp, size_t, vp]
+    lib.spec_verify_sample_truncated_split.restype = i32
     lib.spec_verify_tree_greedy.restype = i32
     lib.spec_verify_sample_static.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, sz, sz, sz, vp, vp, vp, vp, vp]
     lib.spec_verify_sample_static.restype = i32
@@ -195,6 +198,37 @@ def spec_verify_sample_truncated(target_logits: torch.Tensor, draft_logits: torc
     ws, wsp, wsn = _ws(workspace, B, gmax, V, code, target_logits.device)
     _check(lib.spec_verify_sample_truncated(
         _ptr(target_logits, "target_logits"),
+        _ptr(draft_logits, "draft_logits", None, (B, gmax, V)), code,
+        _ptr(draft_tokens, "draft_tokens", torch.int32, (B, gmax)),
+        _ptr(num_draft, "num_draft", torch.int32, (B,)),
+        _ptr(temperature, "temperature", torch.float32, (B,)),
+        _ptr(top_k, "top_k", torch.int32, (B,)), _ptr(top_p, "top_p", torch.float32, (B,)),
+        _ptr(u_accept, "u_accept", torch.float32, (B, gmax)),
+        _ptr(u_sample, "u_sample", torch.float32, (B,)), B, gmax, V,
+        _ptr(out_tokens, "out_tokens", torch.int32, (B, gmax + 1)),
+        _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
+        _ptr(diag, "diag", torch.float32, (B, 2 * gmax + 1)),
+        _ptr(status, "status", torch.int32, (B,)), wsp, wsn, _stream(stream)))
+
+
+def spec_verify_sample_truncated_split(saved_logits: torch.Tensor, block_logits: Optional[torch.Tensor],
+                                       draft_logits: torch.Tensor, draft_tokens: torch.Tensor,
+                                       num_draft: Optional[torch.Tensor], temperature: torch.Tensor,
+                                       top_k: Optional[torch.Tensor], top_p: Optional[torch.Tensor],
+                                       u_accept: torch.Tensor, u_sample: torch.Tensor, out_tokens: torch.Tensor,
+                                       num_accepted: torch.Tensor, diag: Optional[torch.Tensor] = None,
+                                       status: Optional[torch.Tensor] = None,
+                                       workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """spec_verify_sample_truncated with target row 0 (saved_logits [B][V]) apart from rows
+    1..gmax (block_logits [B][gmax][V])."""
+    B, gmax, V = _split_shapes(saved_logits, block_logits)
+    if draft_logits.dtype != saved_logits.dtype:
+        raise TypeError("target and draft logits must have the same dtype")
+    lib = load_library()
+    code = _dtype_code(saved_logits)
+    ws, wsp, wsn = _ws(workspace, B, gmax, V, code, saved_logits.device)
+    _check(lib.spec_verify_sample_truncated_split(
+        _ptr(saved_logits, "saved_logits"), _ptr(block_logits, "block_logits"),
         _ptr(draft_logits, "draft_logits", None, (B, gmax, V)), code,
         _ptr(draft_tokens, "draft_tokens", torch.int32, (B, gmax)),
         _ptr(num_draft, "num_draft", torch.int32, (B,)),

@@ -122,6 +122,15 @@ def test_truncated_argument_checks(lib):
     assert t(V=(1 << 21) + 8) == 3
     assert t() == 3 and b"workspace" in lib.spec_last_error()
     assert t(draft=None, temp=None, B=0) == 0
+    # the split layout: the saved row always, the block rows when there are drafts
+    ts = lambda saved=FAKE, block=FAKE, dtype=0, B=4, gmax=3: lib.spec_verify_sample_truncated_split(
+        saved, block, FAKE, dtype, FAKE, None, FAKE, None, None, FAKE, FAKE, B, gmax, 100, FAKE, FAKE, None, None,
+        FAKE, 8, None)
+    assert ts(saved=None) == 1
+    assert ts(block=None) == 1 and b"block_logits" in lib.spec_last_error()
+    assert ts(dtype=1) == 2
+    assert ts(block=None, gmax=0) == 3 and b"workspace" in lib.spec_last_error()
+    assert ts(saved=None, block=None, B=0) == 0
     assert lib.spec_launch_count() == n0
 
 
@@ -167,7 +176,8 @@ def test_binding_arity_matches_header(lib):
     for name in ("spec_verify_greedy", "spec_verify_sample", "spec_commit_kv_lengths",
                  "spec_verify_workspace_bytes", "spec_verify_plan", "spec_verify_sample_static",
                  "spec_apply_stops", "spec_verify_greedy_split", "spec_verify_sample_split",
-                 "spec_verify_tree_greedy", "spec_verify_sample_truncated"):
+                 "spec_verify_tree_greedy", "spec_verify_sample_truncated",
+                 "spec_verify_sample_truncated_split"):
         m = re.search(r"\b" + name + r"\s*\(([^)]*)\)", text)
         params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
         assert len(getattr(lib, name).argtypes) == len(params), name

@@ -155,3 +155,45 @@ def test_walks_over_empty_keys():
     wl = W.sampling_workload("trunc-gaps", cfg=80, seed=8, B=4, gmax=2, V=128256, dtype="bf16",
                              target_sigma=3.0, draft_scale=0.9, draft_sigma=0.5, temperature=[5.0, 5.0, 2.0, 1.0])
     check(wl, [0, 125000, 0, 120000], [0.999, 1.0, 0.995, 0.99])
+
+
+@pytest.mark.parametrize("offset", [0, 1])
+def test_split_layout_matches_one_array(offset):
+    """spec_verify_sample_truncated_split (target row 0 in an array of its own) gives the
+    one-array call's bits, on the 128-bit path and (offset 1: misaligned) the scalar path, and
+    with gmax = 0."""
+    for gmax in (4, 0):
+        wl = W.sampling_workload(f"trunc-split-{gmax}", cfg=81, seed=9 + offset, B=6, gmax=gmax, V=20000,
+                                 dtype="bf16", target_sigma=3.0, draft_scale=0.8, draft_sigma=1.0,
+                                 temperature=[0.8, 1.0, 0.0, 0.7, 1.2, 0.9],
+                                 greedy_mask=[0, 0, 1, 0, 0, 0])
+        k = np.asarray([50, 0, 10, 1000, 20, 0], np.int32)
+        p = np.asarray([0.9, 0.8, 1.0, 1.0, 0.5, 0.95], np.float32)
+        one = run_truncated(wl, k, p)
+        tgt = parity.dev(wl.target)
+        B, g, V = wl.B, wl.gmax, wl.V
+
+        def place(t):
+            if offset == 0:
+                return t.contiguous()
+            buf = torch.empty(t.numel() + offset, dtype=t.dtype, device=t.device)
+            view = buf[offset:].view(t.shape)
+            view.copy_(t)
+            return view
+
+        saved = place(tgt[:, 0, :])
+        block = place(tgt[:, 1:, :]) if g > 0 else None
+        out = torch.full((B, g + 1), -7, dtype=torch.int32, device="cuda")
+        m = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+        dg = torch.full((B, 2 * g + 1), 1234.5, dtype=torch.float32, device="cuda")
+        st = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+        ws = torch.zeros(sv.spec_verify_workspace_bytes(B, g, V, sv.SPEC_BF16), dtype=torch.uint8, device="cuda")
+        sv.spec_verify_sample_truncated_split(saved, block, parity.dev(wl.draft), parity.dev(wl.draft_tokens),
+                                              parity.dev(wl.num_draft), parity.dev(wl.temperature),
+                                              parity.dev(k), parity.dev(p), parity.dev(wl.u_accept),
+                                              parity.dev(wl.u_sample), out, m, dg, st, workspace=ws)
+        torch.cuda.synchronize()
+        assert bool((ws == 0).all())
+        assert np.array_equal(out.cpu().numpy(), one["out"]) and np.array_equal(m.cpu().numpy(), one["m"])
+        assert np.array_equal(st.cpu().numpy(), one["status"])
+        assert np.array_equal(dg.cpu().numpy().view(np.int32), one["diag"].view(np.int32))
