@@ -238,9 +238,11 @@ int spec_verify_sample_split(const void* saved_logits, const void* block_logits,
  *     SPEC_STATIC_WORKSPACE_BYTES: B = 1110 at gmax = 4, V = 128256 and B = 910 at
  *     gmax = 4, V = 151936 are the largest that fit) return SPEC_ENOSPACE before touching
  *     the device.
- *   - The first call on a device looks the array up (cudaGetSymbolAddress), clears it and
+ *   - Every call looks the array's device address up (cudaGetSymbolAddress, which allocates
+ *     nothing).  The first call on a device, and the first after a device reset (which
+ *     reloads the library's code, possibly at another address), also clears the array and
  *     waits for the clear, so its counters start at zero; make that call outside any stream
- *     capture.  Later calls only launch the kernel.
+ *     capture.  Other calls only launch the kernel.
  *   - Like any workspace, the array is all zero between calls.
  *   - Calls that may overlap (different streams, or threads without ordering) race on the one
  *     array: serialise them, e.g. on one stream.

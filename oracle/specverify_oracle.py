@@ -21,7 +21,7 @@ float64 exactly).  Sources, by page title and section:
   [NXM] nxmr.cn news 151309: the same three-token example, exact-fraction check,
         "R = 0 must not produce NaN", temperature/top-p must be reflected in p and q.
 
-Readings where the pages leave a step open (each also listed in the design doc):
+Readings where the pages leave a step open:
   * Rows arrive pre-aligned: target row i judges draft i, row 0 is the saved
     boundary prediction, row gamma_b is the bonus row ([TUT] §4 table).
   * Acceptance is the strict test u < min(1, r) with r = p(d)/q(d); when q(d) = 0,

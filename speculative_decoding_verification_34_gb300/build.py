@@ -3,11 +3,16 @@
     python -m speculative_decoding_verification_34_gb300.build [--force] [-v]
 
 Each .cu file is compiled in parallel to an object under _build/, then linked into a
-shared library next to this file with the CUDA runtime linked statically.
+shared library next to this file with the CUDA runtime linked statically.  The library is
+rebuilt unless a stamp beside it records the same content hash of every source, header,
+this script and the compiler flags, and the same machine type: a library copied from
+elsewhere, or built from other sources, is never reused.
 """
 from __future__ import annotations
 
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -19,6 +24,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libspecverify.so")
+STAMP = os.path.join(BUILD, "libspecverify.stamp")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 
@@ -40,17 +46,30 @@ def _deps():
     return hdrs + [os.path.abspath(__file__)]
 
 
+def content_hash() -> str:
+    """sha256 over the sources, headers, this script, the flags and the machine type."""
+    h = hashlib.sha256()
+    for p in sorted(sources() + _deps()):
+        h.update(os.path.relpath(p, ROOT).encode())
+        with open(p, "rb") as f:
+            h.update(hashlib.sha256(f.read()).digest())
+    h.update(repr((ARCH, FLAGS[:-1], platform.machine())).encode())
+    return h.hexdigest()
+
+
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    if not (os.path.exists(LIB) and os.path.exists(STAMP)):
         return False
-    t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(p) <= t for p in sources() + _deps())
+    with open(STAMP) as f:
+        return f.read().strip() == content_hash()
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     if not force and up_to_date():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
+    if os.path.exists(STAMP):
+        os.remove(STAMP)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
@@ -72,6 +91,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(content_hash() + "\n")
     return LIB
 
 

@@ -40,54 +40,19 @@
 namespace specverify {
 namespace {
 
-#ifndef SPEC_THREADS
-#define SPEC_THREADS 256
-#endif
-constexpr int kThreads = SPEC_THREADS;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-#ifndef SPEC_VEC_PER_PASS
-#define SPEC_VEC_PER_PASS 4
-#endif
-constexpr int kVecPerPass = SPEC_VEC_PER_PASS;         // 16-byte vectors per thread per row pass
-#ifndef SPEC_DRAW_VEC
-#define SPEC_DRAW_VEC 4
-#endif
-#ifndef SPEC_PREFETCH
-#define SPEC_PREFETCH 1
-#endif
-#ifndef SPEC_RING
-#define SPEC_RING 0
-#endif
-constexpr int kDrawVec = SPEC_DRAW_VEC;                // vectors of each row per thread per draw step
-constexpr bool kPrefetch = SPEC_PREFETCH != 0;         // row passes double-buffered in registers
-constexpr int kRing = SPEC_RING;                       // >0: row passes staged through a ring of
-                                                       // this many 16 KB shared-memory stages
-constexpr int kRingSlots = kRing > 0 ? kRing : 1;       // the ring's modulus (1 when it is off)
-constexpr int kStageBytes = kThreads * kVecPerPass * 16;   // one pass of one row (bf16 or fp32)
-constexpr long long kMbarWaitNs = 2000000;             // bound on one stage wait (2 ms)
-constexpr int kMaxChunks = 64;                         // row chunks per row
-constexpr int kMaxDrawChunks = 16;                     // draw chunks per row
+constexpr int kVecPerPass = 4;                 // 16-byte vectors per thread per row pass
+constexpr int kDrawVec = 4;                    // vectors of each row per thread per draw step
+constexpr long long kWaitNs = 2000000;         // bound on any wait for another block (2 ms)
+constexpr int kMaxChunks = 64;                 // row chunks per row
+constexpr int kMaxDrawChunks = 16;             // draw chunks per row
 constexpr int kSubPerLane = kMaxDrawChunks * kWarps / 32;   // selector: sub-ranges per lane
-#ifndef SPEC_CHUNK_TARGET
-#define SPEC_CHUNK_TARGET 65536
-#endif
-#ifndef SPEC_DRAW_CHUNK_TARGET
-#define SPEC_DRAW_CHUNK_TARGET 16384
-#endif
-#ifndef SPEC_DRAW_WAVES
-#define SPEC_DRAW_WAVES 1.5
-#endif
-#ifndef SPEC_MIN_BLOCKS
-#define SPEC_MIN_BLOCKS 4
-#endif
-constexpr int kChunkTarget = SPEC_CHUNK_TARGET;        // ids per row chunk before rounding
-constexpr int kDrawChunkTarget = SPEC_DRAW_CHUNK_TARGET;   // ids per draw chunk before rounding
-constexpr double kDrawWaves = SPEC_DRAW_WAVES;         // distance of the draw behind the rows
-#ifndef SPEC_DEFER_BYTES
-#define SPEC_DEFER_BYTES (64LL << 20)
-#endif
-constexpr long long kDeferBytes = SPEC_DEFER_BYTES;    // draw rows deferred to the end of a call
-constexpr int kMinBlocks = SPEC_MIN_BLOCKS;            // resident blocks per SM the registers allow
+constexpr int kChunkTarget = 65536;            // ids per row chunk before rounding
+constexpr int kDrawChunkTarget = 16384;        // ids per draw chunk before rounding
+constexpr double kDrawWaves = 1.5;             // distance of the draw behind the rows
+constexpr long long kDeferBytes = 64LL << 20;  // draw rows deferred to the end of a call
+constexpr int kMinBlocks = 4;                  // resident blocks per SM the registers allow
 constexpr int kMaxGroups = 65535;                      // grid z limit
 constexpr int kPlanWaitIters = 64;                     // optional bounded wait of a B unit (~31 us)
 constexpr unsigned kFull = 0xffffffffu;
@@ -470,59 +435,14 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
   return v;
 }
 
-// ---- bulk copies into shared memory, completed on an mbarrier -----------------------------
-
 __device__ __forceinline__ unsigned smem_addr(const void* p) {
   return static_cast<unsigned>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ void mbar_fence_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;\n\tfence.proxy.async.shared::cta;" ::: "memory");
-}
-// one arrival that also announces `bytes` of transfer; the phase completes when they land
-__device__ __forceinline__ void mbar_expect(uint64_t* bar, unsigned bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-               : "memory");
-}
-// global -> shared bulk copy (16-byte aligned addresses, size a multiple of 16)
-__device__ __forceinline__ __attribute__((unused)) void bulk_load(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_addr(dst)),
-               "l"(src), "r"(bytes), "r"(smem_addr(bar))
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint64_t* bar, unsigned parity) {
-  unsigned ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
 }
 __device__ __forceinline__ long long global_ns() {
   long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// waits for the phase of the given parity; false if kMbarWaitNs passed first
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
-  if (mbar_try(bar, parity)) return true;
-  const long long t0 = global_ns();
-  for (;;) {
-    if (mbar_try(bar, parity)) return true;
-    if (global_ns() - t0 > kMbarWaitNs) return false;
-  }
-}
-
-__device__ __forceinline__ uint4 lds128(const void* p) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(smem_addr(p)));
-  return v;
-}
-
 // inclusive prefix sum over the warp's lanes, in a fixed association order
 __device__ __forceinline__ float warp_incl_scan(float v) {
   const int lane = int(threadIdx.x) & 31;
@@ -548,7 +468,6 @@ struct Shared {
   int err;
   float base, target, mass_out;
   PlanRec plan;
-  uint64_t bars[kRing > 0 ? kRing : 1];
 };
 
 // ------------------------------------------------------------------------------------------
@@ -669,13 +588,13 @@ __device__ __forceinline__ uint4 vec_at(const typename E::raw* row, int64_t e, i
 
 // The published word at p, given a first read v of it: once it is there (it was stored before
 // its writer's arrival, which this block has seen), the slot returns to zero for the next
-// call.  Bounded: after kMbarWaitNs the sequence is flagged SPEC_ST_TIMEOUT and 0 is used.
+// call.  Bounded: after kWaitNs the sequence is flagged SPEC_ST_TIMEOUT and 0 is used.
 // First reads of several words are issued together, then settled one by one.
 __device__ __forceinline__ uint64_t settle_word(uint64_t* p, uint64_t v, Shared& sm) {
   if (v == 0) {
     const long long t0 = global_ns();
     while ((v = ld_relaxed_u64(p)) == 0)
-      if (global_ns() - t0 > kMbarWaitNs) {
+      if (global_ns() - t0 > kWaitNs) {
         atomicOr(&sm.flags_extra, SPEC_ST_TIMEOUT);
         break;
       }
@@ -1168,14 +1087,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
       if (e0 + kPass <= hi) t.load_full(row, e0, tid);
       else t.load(row, e0, hi, tid);
     };
-    constexpr bool kRegs = kPrefetch && !(kRing > 0 && kVec);
     Tile<E, kVec> t0, t1;
     const Seq<E, kMixed> sq(a, b);
     if (!sq.slot_valid(slot, a.gmax)) return;
-    if constexpr (kRegs) {
-      if (lo < hi) fetch(t0, lo);
-      if (lo + kPass < hi) fetch(t1, lo + kPass);
-    }
+    if (lo < hi) fetch(t0, lo);
+    if (lo + kPass < hi) fetch(t1, lo + kPass);
     // the logit at this row's draft id, if it lies in this chunk: fetched once, up front
     const int i = slot <= a.gmax ? slot : slot - a.gmax - 1;
     bool has_d = false, no_d = false;
@@ -1198,52 +1114,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
         else tile_argmax(t, e0, tid, rm, ri);
       }
     };
-    if constexpr (kRing > 0 && kVec) {
-      // passes staged through a ring of kRing shared-memory stages by bulk copies: thread 0
-      // keeps kRing passes in flight; a stage is refilled once every thread has its tile
-      extern __shared__ __align__(128) unsigned char ring[];
-      const int npass = lo < hi ? int((hi - lo + kPass - 1) / kPass) : 0;
-      auto issue = [&](int p) {
-        const int st = p % kRingSlots;
-        const int64_t e0 = lo + int64_t(p) * kPass;
-        const int64_t n = hi - e0 < kPass ? hi - e0 : kPass;
-        const unsigned bytes = unsigned(n * int64_t(sizeof(raw)));
-        mbar_expect(&sm.bars[st], bytes);
-        bulk_load(ring + st * kStageBytes, row + e0, bytes, &sm.bars[st]);
-      };
-      if (tid == 0) {
-        sm.err = 0;
-        for (int st = 0; st < kRing; ++st) mbar_init(&sm.bars[st]);
-        mbar_fence_init();
-        for (int p = 0; p < npass && p < kRing; ++p) issue(p);
-      }
-      __syncthreads();
-      for (int p = 0; p < npass; ++p) {
-        const int st = p % kRingSlots;
-        const int64_t e0 = lo + int64_t(p) * kPass;
-        if (!mbar_wait(&sm.bars[st], unsigned(p / kRingSlots) & 1u)) sm.err = 1;
-        Tile<E, kVec> t;
-#pragma unroll
-        for (int q = 0; q < kVecPerPass; ++q) {
-          const int off = q * kThreads + tid;
-          t.v[q] = e0 + int64_t(off) * N < hi ? lds128(ring + st * kStageBytes + off * 16)
-                                               : make_uint4(E::kNegInf, E::kNegInf, E::kNegInf, E::kNegInf);
-        }
-        __syncthreads();
-        if (tid == 0 && p + kRing < npass && !sm.err) issue(p + kRing);
-        consume(t, e0);
-      }
-      if (sm.err) {
-        // a stage wait ran out: wait, again bounded, for every copy this block issued, then
-        // report the sequence
-        if (tid == 0) {
-          for (int p = npass - kRing > 0 ? npass - kRing : 0; p < npass; ++p)
-            mbar_wait(&sm.bars[p % kRingSlots], unsigned(p / kRingSlots) & 1u);
-          if (a.status) atomicOr(&a.status[b], SPEC_ST_TIMEOUT);
-        }
-        __syncthreads();
-      }
-    } else if constexpr (kRegs) {
+    {
       // two tiles in registers, both passes already in flight: each is refilled with the
       // pass after next as soon as it has been reduced
       for (int64_t e0 = lo; e0 < hi; e0 += 2 * kPass) {
@@ -1252,12 +1123,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
         if (e0 + kPass >= hi) break;
         consume(t1, e0 + kPass);
         if (e0 + 3 * kPass < hi) fetch(t1, e0 + 3 * kPass);
-      }
-    } else {
-      for (int64_t e0 = lo; e0 < hi; e0 += kPass) {
-        Tile<E, kVec> t;
-        fetch(t, e0);
-        consume(t, e0);
       }
     }
     if constexpr (kKeep) kept.settle(tid, rm, ri);
@@ -1333,7 +1198,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
         // the other three words were stored before the first, in no guaranteed order: each
         // is taken once it is there (bounded)
         const long long t0 = global_ns();
-        while ((w1 == 0 || w2 == 0 || w3 == 0) && global_ns() - t0 < kMbarWaitNs) {
+        while ((w1 == 0 || w2 == 0 || w3 == 0) && global_ns() - t0 < kWaitNs) {
           if (w1 == 0) w1 = ld_relaxed_u64(pw + 1);
           if (w2 == 0) w2 = ld_relaxed_u64(pw + 2);
           if (w3 == 0) w3 = ld_relaxed_u64(pw + 3);
@@ -1391,23 +1256,10 @@ struct __align__(16) RowInfo {
 };
 
 constexpr float kMassUnit = 1099511627776.0f;   // 2^40
-#ifndef SPEC_TRUNC_GUARD
-#define SPEC_TRUNC_GUARD 96
-#endif
-#ifndef SPEC_TRUNC_FUSED_WIDTH
-#define SPEC_TRUNC_FUSED_WIDTH 256
-#endif
-constexpr uint32_t kGuardKeys = SPEC_TRUNC_GUARD;        // fused window's top above the estimated max
-constexpr uint32_t kFusedWidth = SPEC_TRUNC_FUSED_WIDTH; // keys the fused pass counts (256 or 512)
-static_assert(kFusedWidth == 256 || kFusedWidth == 512, "one or two windows of 256 keys");
-#ifndef SPEC_TRUNC_SAMPLE_RUNS
-#define SPEC_TRUNC_SAMPLE_RUNS 4
-#endif
-constexpr int kSampleRuns = SPEC_TRUNC_SAMPLE_RUNS;     // runs of kThreads vectors the estimate reads
-#ifndef SPEC_TRUNC_DRAW_CHUNK
-#define SPEC_TRUNC_DRAW_CHUNK 32768
-#endif
-constexpr int kTruncDrawChunk = SPEC_TRUNC_DRAW_CHUNK;  // ids per draw unit of the truncated draw
+constexpr uint32_t kGuardKeys = 96;        // fused window's top above the estimated max
+constexpr uint32_t kFusedWidth = 256; // keys the fused pass counts: one window
+constexpr int kSampleRuns = 4;     // runs of kThreads vectors the estimate reads
+constexpr int kTruncDrawChunk = 32768;  // ids per draw unit of the truncated draw
 
 // order-preserving 16-bit key of a bf16 logit; -0 is taken as +0 so equal values share a key
 __device__ __forceinline__ uint32_t key16(uint32_t bits) {
@@ -1829,7 +1681,6 @@ __global__ void __launch_bounds__(kThreads) trunc_rows_kernel(const Args a, cons
       if (below) {
         // per thread from the window's lowest value to the max (a factor at most 1), then fixed point
         rest = block_sum_u64(__float2ull_rn(__fmul_rn(f, ex2(vk - mk)) * kMassUnit), ts);
-        if (kFusedWidth > 256) massb = bins_mass(cnt + 256, top - 256u, k, mk, ts);
       }
       if (!dok && !dop) {
         kept = bins_mass(cnt, top, k, mk, ts) + massb + rest;
@@ -1841,7 +1692,6 @@ __global__ void __launch_bounds__(kThreads) trunc_rows_kernel(const Args a, cons
             ts,
             [&](uint32_t hi, bool blw) -> unsigned long long {
               if (pre && hi == top) { cur = 0; nxt = hi - 256u; return blw ? massb + rest : 0ull; }
-              if (pre && kFusedWidth > 256 && hi == top - 256u) { cur = 1; nxt = hi - 256u; return blw ? rest : 0ull; }
               pre = false;
               cur = 0;
               return trunc_window<kVec>(row, V, hi, blw, k, mk, ts, nxt);
@@ -2098,8 +1948,7 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
   const int brows = kMixed ? (geo.DCL + geo.CL - 1) / geo.CL : 0;   // grid rows of B units
   const int G = geo.CL * (geo.nslots + brows);                       // units per group
   // B units of a sequence come about kDrawWaves waves of resident blocks after its A units
-  // the shared-memory ring of the row passes (vector path only)
-  const size_t dyn_smem = (kRing > 0 && kVec) ? size_t(kRing) * kStageBytes : 0;
+  const size_t dyn_smem = 0;
   int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -2109,10 +1958,6 @@ int launch(const Args& args, int dtype, void* ws, size_t ws_bytes, void* stream)
     if (dev < 64 && cached[dev]) {
       per_sm = cached[dev];
     } else {
-      if (dyn_smem > 0) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(dyn_smem));
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute (ring size)");
-      }
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, dyn_smem);
       if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
       if (per_sm < 1) per_sm = 1;
@@ -2479,8 +2324,10 @@ extern "C" int spec_verify_tree_greedy(const void* target_logits, int dtype, con
 // For callers that cannot allocate device memory at the point of the call: a serving loop
 // whose memory is fixed after start-up, or code between a framework's allocations that must
 // not add one.  The workspace is one file-scope device array per device (every call of this
-// entry point on that device shares it); its address is looked up once per device with
-// cudaGetSymbolAddress.  Nothing is allocated, by this call or by any routine it calls.
+// entry point on that device shares it).  Every call looks its address up with
+// cudaGetSymbolAddress (which allocates nothing); the first call on a device, and the first
+// after a device reset has reloaded the library's module at a new address, also clears the
+// array and waits for that.  Nothing is allocated, by this call or by any routine it calls.
 
 namespace specverify {
 namespace {
@@ -2493,10 +2340,9 @@ static_assert(kStaticWsBytes % 64 == 0, "static workspace size");
 static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
 
 std::mutex g_static_mu;
-void* g_static_ptr[64] = {};
+void* g_static_ptr[64] = {};   // the address this device's array was last cleared at
 
-// The device address of this device's array.  The first call on a device also clears the
-// whole array and waits for that to finish.
+// The device address of the current device's array, cleared first when it is new.
 int static_workspace(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -2505,18 +2351,18 @@ int static_workspace(void** out) {
     set_error("device %d: the static workspace serves devices 0..63", dev);
     return SPEC_EINVAL;
   }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_static_ws);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the static workspace");
   std::lock_guard<std::mutex> lk(g_static_mu);
-  if (!g_static_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_ws);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the static workspace");
+  if (g_static_ptr[dev] != p) {
     e = cudaMemset(p, 0, kStaticWsBytes);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the static workspace");
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "clearing the static workspace");
     g_static_ptr[dev] = p;
   }
-  *out = g_static_ptr[dev];
+  *out = p;
   return SPEC_OK;
 }
 
