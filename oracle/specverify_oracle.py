@@ -151,6 +151,14 @@ def accept_draft(p_d: float, q_d: float, u: float) -> bool:
     return u < min(1.0, acceptance_ratio(p_d, q_d))
 
 
+def accept_margin(u: float, r: float) -> float:
+    """|u - r|: how far the uniform of an acceptance test sits from the ratio it is compared
+    with.  The decision u < min(1, r) can only change where u crosses r (for r >= 1, u in
+    [0, 1) never does), so this is the distance to the decision boundary, used only to flag
+    near-ties in parity tests (a fp32 evaluation of p and q may put r on the other side)."""
+    return abs(u - r)
+
+
 def residual_weights(p: np.ndarray, q: np.ndarray) -> np.ndarray:
     """w_v = max(p_v - q_v, 0); R = sum_v w_v = 1 - sum_v min(p_v, q_v) ([TUT] §7.2)."""
     return np.maximum(p - q, 0.0)
@@ -253,7 +261,7 @@ def verify_sample_sequence(target: np.ndarray, draft: np.ndarray, drafts: np.nda
             pd, qd = float(p[d]), float(q[d])
             p_d.append(pd)
             q_d.append(qd)
-            margins.append(abs(float(u_accept[i]) - acceptance_ratio(pd, qd)))
+            margins.append(accept_margin(float(u_accept[i]), acceptance_ratio(pd, qd)))
             ok = accept_draft(pd, qd, float(u_accept[i]))
         else:
             status |= ST_BAD_DRAFT

@@ -581,3 +581,146 @@ def check_truncated_joint_law(V, gamma, T, top_k, top_p, seed, tol=1e-9):
         for j in range(n):
             want *= tr(logits("target", sq[:j]))[sq[j]]
         assert abs(ext.get(sq, 0.0) - want) < tol, (sq, ext.get(sq, 0.0), want)
+
+
+# ---------------------------------------------------------------------------------------
+# decision margins: every margin the oracle reports is the distance from its uniform (or
+# mass target) to the point where the decision it flags actually changes.  Parity tests
+# exempt sequences whose margin is below 1e-5 from the bit-exact check (the near-tied
+# decisions [TUT] §12.3 tells apart from real mismatches), so a margin computed too large
+# would hide a real mismatch and one computed too small would widen the exemption.
+# ---------------------------------------------------------------------------------------
+
+_IN, _OUT = 1.0 - 1e-6, 1.0 + 1e-6
+
+
+def _one_row_case(rng, V):
+    T = float(rng.choice([0.6, 1.0, 1.4]))
+    P = rng.normal(0, 1.5, size=(2, V))
+    Q = P[:1] + rng.normal(0, float(rng.choice([0.1, 0.5, 1.5])), size=(1, V))
+    d = np.array([int(rng.integers(0, V))])
+    return P, Q, d, T
+
+
+def check_accept_margin(cases=400, seed=31, need_flips=100):
+    """Moving u_accept toward p(d)/q(d) by the reported margin times (1 - 1e-6) keeps the
+    decision; by (1 + 1e-6) it flips it (where the moved u stays in [0, 1))."""
+    rng = np.random.default_rng(seed)
+    flips = 0
+    for _ in range(cases):
+        P, Q, d, T = _one_row_case(rng, int(rng.integers(2, 12)))
+        u = float(rng.random())
+        res = O.verify_sample_sequence(P, Q, d, 1, T, np.array([u]), 0.5)
+        kept = res.m == 1
+        a = res.accept_margins[0]
+        assert a >= 0.0
+        s = 1.0 if kept else -1.0             # kept: u < r, so r lies above u
+
+        def keeps(v):
+            return O.verify_sample_sequence(P, Q, d, 1, T, np.array([v]), 0.5).m == 1
+        if a < 1e-9:
+            continue
+        u_in, u_out = u + s * a * _IN, u + s * a * _OUT
+        if 0.0 <= u_in < 1.0:
+            assert keeps(u_in) == kept, (u, a, u_in, kept)
+        if 0.0 <= u_out < 1.0:
+            assert keeps(u_out) != kept, (u, a, u_out, kept)
+            flips += 1
+        elif kept:
+            # r >= 1: every u in [u, 1) keeps the draft
+            for v in (u, 0.5 * (u + 1.0), float(np.nextafter(1.0, 0.0))):
+                assert keeps(v)
+    assert flips >= need_flips, flips
+
+
+def check_inverse_cdf_margin(cases=400, seed=32, need_flips=150):
+    """Moving u by the reported inverse-CDF margin times (1 - 1e-6), either way, keeps the
+    token; by (1 + 1e-6) toward the nearer cell edge it changes it.  Checked on the function
+    itself and on the draw of a whole step (correction or bonus)."""
+    rng = np.random.default_rng(seed)
+    flips = 0
+    for c in range(cases):
+        V = int(rng.integers(1, 16))
+        w = rng.random(V) * (rng.random(V) < 0.7)
+        if not w.any():
+            w[int(rng.integers(0, V))] = 1.0
+        u = float(rng.random())
+        v, a, _ = O.inverse_cdf(w, u)
+        assert a >= 0.0
+        if a < 1e-9:
+            continue
+        for s in (-1.0, 1.0):
+            ui = u + s * a * _IN
+            if 0.0 <= ui < 1.0:
+                assert O.inverse_cdf(w, ui)[0] == v, (w, u, a, ui)
+        # the nearer cell edge is crossed on one side; when a moved u leaves [0, 1) that edge
+        # may be the end of the range itself, so only cases with both inside are required
+        outs = [u + s * a * _OUT for s in (-1.0, 1.0)]
+        if all(0.0 <= x < 1.0 for x in outs):
+            assert any(O.inverse_cdf(w, x)[0] != v for x in outs), (w, u, a)
+            flips += 1
+    assert flips >= need_flips, flips
+    # the same on whole steps: the sample margin is the margin of the draw actually made
+    step_flips = 0
+    for c in range(cases // 2):
+        P, Q, d, T = _one_row_case(rng, int(rng.integers(2, 10)))
+        ua = np.array([float(rng.random())])
+        us = float(rng.random())
+        res = O.verify_sample_sequence(P, Q, d, 1, T, ua, us)
+        a = res.sample_margin
+        if not (1e-9 <= a < 1.0):
+            continue
+
+        def tok(x):
+            r = O.verify_sample_sequence(P, Q, d, 1, T, ua, x)
+            assert r.m == res.m
+            return r.tokens[-1]
+        for s in (-1.0, 1.0):
+            x = us + s * a * _IN
+            if 0.0 <= x < 1.0:
+                assert tok(x) == res.tokens[-1]
+        outs = [us - a * _OUT, us + a * _OUT]
+        if all(0.0 <= x < 1.0 for x in outs):
+            assert any(tok(x) != res.tokens[-1] for x in outs)
+            step_flips += 1
+    assert step_flips >= need_flips // 3, step_flips
+
+
+def check_top_p_margin(cases=300, seed=33, need_flips=100):
+    """Moving top_p by the reported crossing margin times (1 - 1e-6), either way, keeps the
+    kept set; by (1 + 1e-6) toward the nearer crossing it changes it."""
+    rng = np.random.default_rng(seed)
+    flips = 0
+    for c in range(cases):
+        V = int(rng.integers(2, 30))
+        x = rng.normal(0, 2, size=V)
+        if c % 3 == 0:
+            x = np.round(x * 2) / 2
+        T = float(rng.choice([0.5, 1.0, 1.7]))
+        k = int(rng.choice([0, 3, 8]))
+        tp = float(rng.uniform(0.05, 0.95))
+        dist, a = O.truncated_distribution(x, T, k, tp)
+        assert a >= 0.0
+        kept = dist > 0
+        if a < 1e-9 or not math.isfinite(a):
+            continue
+        for s in (-1.0, 1.0):
+            t = tp + s * a * _IN
+            if 0.0 < t < 1.0:
+                assert np.array_equal(O.truncated_distribution(x, T, k, t)[0] > 0, kept), (x, tp, a, t)
+        outs = [tp - a * _OUT, tp + a * _OUT]
+        if all(0.0 < t < 1.0 for t in outs):
+            assert any(not np.array_equal(O.truncated_distribution(x, T, k, t)[0] > 0, kept) for t in outs)
+            flips += 1
+    assert flips >= need_flips, flips
+    # off: no crossing, no margin
+    assert O.truncated_distribution(np.array([0.0, 1.0]), 1.0, 0, 1.0)[1] == math.inf
+
+
+def check_flagged_uses_every_margin():
+    """flagged() looks at every acceptance margin of the step and at its draw's margin."""
+    r = O.SequenceResult([1], 0, 0, 2, False, [0.1, 0.1], [0.1, 0.1], 0.5, [0.5, 2e-6], 0.3)
+    assert r.flagged(1e-5) and not r.flagged(1e-6)
+    r.accept_margins = [0.5, 0.5]
+    r.sample_margin = 5e-6
+    assert r.flagged(1e-5) and not r.flagged(1e-6)

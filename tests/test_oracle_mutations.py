@@ -47,6 +47,23 @@ _apply_stops = O.apply_stops
 
 
 _truncated = O.truncated_distribution
+_inverse_cdf = O.inverse_cdf
+
+
+def _icdf_margin_scaled(f):
+    # the inverse CDF with its reported margin scaled by f (the token is unchanged)
+    def run(weights, u):
+        v, a, total = _inverse_cdf(weights, u)
+        return v, a * f, total
+    return run
+
+
+def _top_p_margin_scaled(f):
+    # the truncation with its top-p crossing margin scaled by f (the kept set is unchanged)
+    def run(logits, T, top_k=0, top_p=1.0):
+        d, a = _truncated(logits, T, top_k, top_p)
+        return d, a * f
+    return run
 
 
 def _trunc_variant(full_mass=False, strict_k=False):
@@ -121,6 +138,13 @@ MUTATIONS = {
     "tree_last_index_tie": ("verify_tree_greedy_sequence", _tree_variant(last_tie=True)),
     "top_p_full_mass": ("truncated_distribution", _trunc_variant(full_mass=True)),
     "top_k_drops_ties": ("truncated_distribution", _trunc_variant(strict_k=True)),
+    "accept_margin_halved": ("accept_margin", lambda u, r: abs(u - r) / 2),
+    "accept_margin_doubled": ("accept_margin", lambda u, r: abs(u - r) * 2),
+    "accept_margin_of_clamped_ratio_minus_u": ("accept_margin", lambda u, r: min(1.0, r) - u),
+    "inverse_cdf_margin_halved": ("inverse_cdf", _icdf_margin_scaled(0.5)),
+    "inverse_cdf_margin_doubled": ("inverse_cdf", _icdf_margin_scaled(2.0)),
+    "top_p_margin_halved": ("truncated_distribution", _top_p_margin_scaled(0.5)),
+    "top_p_margin_doubled": ("truncated_distribution", _top_p_margin_scaled(2.0)),
 }
 
 
@@ -134,7 +158,11 @@ def _pins_pass():
               pins.check_tree_figure, pins.check_tree_chain_equals_chain,
               pins.check_tree_matches_greedy_walk, pins.check_tree_ties_and_invalid_nodes,
               pins.check_truncation_against_counting, pins.check_top_k_one_is_greedy,
-              lambda: pins.check_truncated_joint_law(4, 2, 0.8, 0, 0.7, 32)]
+              lambda: pins.check_truncated_joint_law(4, 2, 0.8, 0, 0.7, 32),
+              lambda: pins.check_accept_margin(cases=200, need_flips=40),
+              lambda: pins.check_inverse_cdf_margin(cases=200, need_flips=60),
+              lambda: pins.check_top_p_margin(cases=150, need_flips=40),
+              pins.check_flagged_uses_every_margin]
     for c in checks:
         try:
             c()

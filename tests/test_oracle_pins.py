@@ -236,3 +236,19 @@ def test_truncation_off_switches():
                                                   (4, 1, 1.3, 3, 0.6, 33), (3, 2, 1.0, 2, 0.9, 34)])
 def test_truncated_joint_law(V, gamma, T, k, tp, seed):
     pins.check_truncated_joint_law(V, gamma, T, k, tp, seed)
+
+
+def test_accept_margin_is_distance_to_decision_flip():
+    pins.check_accept_margin()
+
+
+def test_inverse_cdf_margin_is_distance_to_token_change():
+    pins.check_inverse_cdf_margin()
+
+
+def test_top_p_margin_is_distance_to_kept_set_change():
+    pins.check_top_p_margin()
+
+
+def test_flagged_uses_every_margin():
+    pins.check_flagged_uses_every_margin()
