@@ -12,8 +12,10 @@ Metric: verified draft rows per second (sum of gamma_b over the batch, per step)
 achieved HBM bandwidth of the verify kernel: algorithmic bytes (every valid logit row read
 once) divided by its CUDA-event duration, against the measured HBM copy bandwidth.
 
---impl reference times the float64 CPU oracle on the host cores instead, on a bounded sample
-of the same workload per step (rank 0 only).
+--impl reference times the float64 CPU oracle on all host cores instead, on a bounded sample
+of the same workload per step (rank 0 only).  The native line's cpu_baseline times the same
+oracle on one core and on all cores; its parity field compares one call's outputs with the
+oracle on every sequence of the batch.
 """
 from __future__ import annotations
 
@@ -239,7 +241,7 @@ def aggregate_rate(world, rows_per_step, steps, max_elapsed_ms):
 
 
 def cpu_oracle_rate(wl, seconds, seqs_cap=None):
-    """Oracle throughput on a bounded sample of the same batch: rows/s, sequences used."""
+    """Oracle throughput on one core over a bounded sample of the batch: rows/s, sequences used."""
     t0 = time.perf_counter()
     n = rows = 0
     order = list(range(wl.B))
@@ -252,49 +254,216 @@ def cpu_oracle_rate(wl, seconds, seqs_cap=None):
             return rows / el, n, rows, el
 
 
+# ---- the oracle on all host cores: one spawned process per core, the logits shared ----------
+
+_POOL_STATE = {}
+_BIG = ("target", "draft")
+
+
+def _pool_init(root, meta, shm_specs):
+    if root not in sys.path:
+        sys.path.insert(0, root)
+    import types
+    from multiprocessing import shared_memory
+
+    import numpy as np
+    arrays = {}
+    for name, (shm_name, shape, dt) in shm_specs.items():
+        shm = shared_memory.SharedMemory(name=shm_name)   # the parent unlinks it
+        _POOL_STATE["shm_" + name] = shm
+        arrays[name] = np.ndarray(shape, dtype=np.dtype(dt), buffer=shm.buf)
+    _POOL_STATE["wl"] = types.SimpleNamespace(**meta, **arrays)
+
+
+def _pool_task(seqs):
+    wl = _POOL_STATE["wl"]
+    return sum(oracle_one(wl, b) for b in seqs)
+
+
+class OraclePool:
+    """A spawn-context process pool over the host cores with the workload's logits in shared
+    memory (spawn, not fork: the parent has already initialised CUDA)."""
+
+    def __init__(self, wl, procs=None):
+        import multiprocessing as mp
+        from multiprocessing import shared_memory
+
+        import numpy as np
+        self.procs = procs or len(os.sched_getaffinity(0))
+        self.shms, specs, meta = [], {}, {}
+        for k, v in vars(wl).items():
+            if k in _BIG and isinstance(v, np.ndarray):
+                shm = shared_memory.SharedMemory(create=True, size=max(1, v.nbytes))
+                np.ndarray(v.shape, dtype=v.dtype, buffer=shm.buf)[...] = v
+                self.shms.append(shm)
+                specs[k] = (shm.name, v.shape, v.dtype.str)
+            else:
+                meta[k] = v
+        from concurrent.futures import ProcessPoolExecutor
+        # an executor, not multiprocessing.Pool: a worker that dies raises here instead of being
+        # replaced forever
+        self.pool = ProcessPoolExecutor(self.procs, mp_context=mp.get_context("spawn"),
+                                        initializer=_pool_init, initargs=(ROOT, meta, specs))
+        list(self.pool.map(_pool_task, [[] for _ in range(self.procs)]))   # every worker started
+
+    def run(self, seqs):
+        """Verify the listed sequences over all workers; returns (rows, seconds)."""
+        chunks = [seqs[i::self.procs] for i in range(self.procs)]
+        t0 = time.perf_counter()
+        rows = sum(self.pool.map(_pool_task, chunks))
+        return rows, time.perf_counter() - t0
+
+    def close(self):
+        self.pool.shutdown(wait=True, cancel_futures=True)
+        for shm in self.shms:
+            shm.close()
+            shm.unlink()
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline(wl, seconds, runs=3):
+    """The oracle timed on one core and on all cores (processes over sequences), each as the
+    median of `runs` runs over a bounded sample of the batch, about `seconds` in total."""
+    per = max(0.2, seconds / (2 * runs))
+    single = [cpu_oracle_rate(wl, per)[0] for _ in range(runs)]
+    r1 = statistics.median(single)
+    rows_per_seq = max(1.0, wl.verified_rows() / wl.B)
+    pool = OraclePool(wl)
+    try:
+        n = max(pool.procs, int(round(per * r1 * pool.procs / rows_per_seq)))
+        seqs = [i % wl.B for i in range(n)]
+        allc = []
+        for _ in range(runs):
+            rows, el = pool.run(seqs)
+            allc.append(rows / el)
+    finally:
+        pool.close()
+    return {"value": r1, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "value_all": statistics.median(allc), "cores_all": pool.procs, "runs": runs,
+            "runs_single": single, "runs_all": allc, "cpu_model": cpu_model(), "nproc": os.cpu_count(),
+            "sample": f"median of {runs} runs per leg: one core cycling over the batch's {wl.B} sequences "
+                      f"for {per:.1f} s a run; {pool.procs} processes over {n} sequence verifications a run; "
+                      f"float64 numpy oracle"}
+
+
+def parity_record(wl, gpu, tol=1e-5):
+    """The GPU outputs of one call against the oracle on every sequence of the batch: decisions
+    whose oracle margin is below tol are flagged (either branch is correct there) and counted;
+    every other sequence must match exactly.  Also alpha = sum min(p, q) per draft row (the
+    acceptance rate of that row) and the closed-form expected emit 1 + sum_j prod_{i<j} alpha_i
+    beside the measured mean emit."""
+    import math
+
+    import numpy as np
+    from oracle import specverify_oracle as O
+    flagged = differ = mismatch = 0
+    perr = 0.0
+    if is_tree(wl):
+        res = O.verify_tree_batch(wl.target, wl.dtype, wl.node_tokens, wl.node_parents, wl.num_nodes)
+    else:
+        res = O.verify_batch(wl.target, wl.draft, wl.dtype, wl.draft_tokens, wl.num_draft,
+                             None if wl.greedy_only else wl.temperature, wl.u_accept, wl.u_sample,
+                             top_k=getattr(wl, "top_k", None), top_p=getattr(wl, "top_p", None))
+    g_all = gpu["out"].shape[1] - 1
+    for b, r in enumerate(res):
+        want = np.full(g_all + 1, -1)
+        want[: len(r.tokens)] = r.tokens
+        same = (int(gpu["m"][b]) == r.m and np.array_equal(gpu["out"][b], want)
+                and int(gpu["status"][b]) == r.status)
+        fl = (not is_tree(wl)) and r.flagged(tol)
+        flagged += fl
+        differ += fl and not same
+        mismatch += (not fl) and not same
+        if not is_tree(wl) and not r.greedy and gpu.get("diag") is not None:
+            for i in range(r.gamma):
+                if not math.isnan(r.p_draft[i]):
+                    perr = max(perr, abs(float(gpu["diag"][b][2 * i]) - r.p_draft[i]),
+                               abs(float(gpu["diag"][b][2 * i + 1]) - r.q_draft[i]))
+    rec = {"checked": len(res), "flagged": flagged, "differ": differ, "mismatch": mismatch,
+           "margin": tol, "prob_max_abs_err": perr,
+           "sample": f"every sequence of one call ({len(res)}), float64 oracle"}
+    if not is_tree(wl) and not wl.greedy_only:
+        alphas, expect = [], []
+        for b in range(wl.B):
+            T = float(wl.temperature[b])
+            g = min(max(int(wl.num_draft[b]), 0), wl.gmax)
+            if not T > 0:
+                continue
+            run, e = 1.0, 1.0
+            for i in range(g):
+                P = O.widen(wl.target[b, i], wl.dtype)
+                Q = O.widen(wl.draft[b, i], wl.dtype)
+                tk = int(wl.top_k[b]) if getattr(wl, "top_k", None) is not None else 0
+                tp = float(wl.top_p[b]) if getattr(wl, "top_p", None) is not None else 1.0
+                p = O.truncated_distribution(P, T, tk, tp)[0]
+                q = O.truncated_distribution(Q, T, tk, tp)[0]
+                a = float(np.minimum(p, q).sum())
+                alphas.append(a)
+                run *= a
+                e += run
+            expect.append(e)
+        m = gpu["m"][np.asarray(wl.temperature) > 0]
+        rec["alpha_mean"] = statistics.fmean(alphas) if alphas else None
+        rec["expected_emitted_per_sampling_sequence"] = statistics.fmean(expect) if expect else None
+        rec["measured_emitted_per_sampling_sequence"] = float(m.mean()) + 1.0 if len(m) else None
+    return rec
+
+
 # ------------------------------------------------------------------------------------------
 
 def run_reference(args):
+    """The float64 oracle as it stands, on all host cores (one spawned process per core, over
+    sequences), each step a bounded sample of the workload's sequences."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
     from speculative_decoding_verification_34_gb300 import workloads as W
     wl = W.WORKLOADS[args.config](seed=0)
     apply_truncation(wl, args)
+    pool = OraclePool(wl)
+    try:
+        # size each step so that the whole run stays within ~150 s: whole sequences, at least
+        # one per process
+        t0 = time.perf_counter()
+        oracle_one(wl, 0)
+        t_seq = time.perf_counter() - t0
+        per_step = int(150.0 / max(1, args.steps + args.warmup) / max(t_seq, 1e-6) * pool.procs)
+        per_step = max(pool.procs, min(per_step, wl.B * pool.procs))
+        nxt = [0]
 
-    def one(b):
-        return oracle_one(wl, b)
+        def step():
+            seqs = [(nxt[0] + i) % wl.B for i in range(per_step)]
+            nxt[0] += per_step
+            return pool.run(seqs)[0]
 
-    # size each step so that the whole run stays within ~150 s: whole sequences, at least one
-    t0 = time.perf_counter()
-    one(0)
-    t_seq = time.perf_counter() - t0
-    per_step = max(1, int(150.0 / max(1, args.steps + args.warmup) / max(t_seq, 1e-6)))
-    per_step = min(per_step, wl.B)
-    nxt = [0]
-
-    def step():
-        r = 0
-        for _ in range(per_step):
-            b = nxt[0] % wl.B
-            r += one(b)
-            nxt[0] += 1
-        return r
-
-    for _ in range(args.warmup):
-        step()
-    t0 = time.perf_counter()
-    rows = sum(step() for _ in range(args.steps))
-    el = time.perf_counter() - t0
+        for _ in range(args.warmup):
+            step()
+        t0 = time.perf_counter()
+        rows = sum(step() for _ in range(args.steps))
+        el = time.perf_counter() - t0
+    finally:
+        pool.close()
     value = rows / el
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(wl, "CPU oracle: host memory"),
-            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{per_step} sequence(s) of the {wl.B}-sequence batch per step "
-                                       f"(cycling), float64 numpy oracle, single thread"},
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": pool.procs, "kind": "oracle",
+                             "cpu_model": cpu_model(), "nproc": os.cpu_count(),
+                             "sample": f"{per_step} sequence verifications per step cycling over the batch's "
+                                       f"{wl.B} sequences, {pool.procs} processes, float64 numpy oracle"},
             "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -401,6 +570,7 @@ def run_native(args):
     kern_med_ms = statistics.median(kern_ms)
     ks = sorted(kern_ms)
     kern_p10, kern_p90 = ks[len(ks) // 10], ks[(9 * len(ks)) // 10]
+    outliers = sum(1 for x in ks if x > 1.05 * kern_med_ms)
     elapsed_ms = all_reduce_max(elapsed_ms, world, device)
     kern_mean_ms = all_reduce_max(kern_mean_ms, world, device)
 
@@ -483,12 +653,17 @@ def run_native(args):
     e2e_ms = all_reduce_max(es.elapsed_time(ee), world, device)
     e2e_value = aggregate_rate(world, rows_step, args.e2e_steps, e2e_ms)
 
-    cpu = None
+    # ---- the outputs of one call (every input copy holds the same data) against the oracle ----
+    verify[0]()
+    torch.cuda.synchronize(device)
+    gpu_out = {"out": out.cpu().numpy(), "m": macc.cpu().numpy(), "status": st.cpu().numpy(),
+               "diag": None if (tree or wl.greedy_only) else dg.cpu().numpy()}
+
+    cpu = parity = None
+    if rank == 0:
+        parity = parity_record(wl, gpu_out)
     if rank == 0 and world == 1:
-        rate, nseq, rows, el = cpu_oracle_rate(wl, args.cpu_seconds)
-        cpu = {"value": rate, "unit": "rows/s", "cores": 1, "kind": "oracle",
-               "sample": f"{nseq} sequence verifications cycling over the batch's {wl.B} sequences "
-                         f"({rows} verified rows, {el:.1f} s), float64 numpy oracle, single thread"}
+        cpu = cpu_baseline(wl, args.cpu_seconds)
 
     if rank == 0:
         traffic = recorded_traffic(1)
@@ -509,9 +684,13 @@ def run_native(args):
                                     else "verify_kernel<bf16, vec, greedy> (spec_verify_greedy)" if wl.greedy_only
                                     else "verify_kernel<bf16, vec, mixed> (spec_verify_sample)"),
                          "kernel_ms_mean": kern_mean_ms, "kernel_ms_median": kern_med_ms,
-                         "kernel_ms_p10": kern_p10, "kernel_ms_p90": kern_p90,
+                         "kernel_ms_p10": kern_p10, "kernel_ms_p90": kern_p90, "kernel_ms_max": ks[-1],
+                         "frac_of_median": abytes / (kern_med_ms / 1e3) / 1e9 / peak,
+                         "launches_timed": len(ks), "launches_above_1p05_median": outliers,
+                         "slowest_launches_ms": ks[-3:],
                          "algorithmic_bytes_per_launch": abytes, "peak_source": peak_src},
-            "cpu_baseline": cpu,
+            "step_minus_kernel_median_ms": elapsed_ms / K - kern_med_ms,
+            "cpu_baseline": cpu, "parity": parity,
             "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
             "gpu_launches": launches, "clocks": clocks, "post_kernels": post,

@@ -87,6 +87,7 @@ def test_split_sampling_matches_one_array_and_oracle(dtype, V, offset):
     two = _run(wl, split=True, greedy=False, offset_elems=offset)
     _same(one, two)
     n, flagged, differ = parity.compare(wl, two, parity.oracle_results(wl))
+    parity.record(wl.name, n, flagged, differ, entry="sample_split")
     assert n == B and len(differ) <= 1, (flagged, differ)
 
 

@@ -40,6 +40,7 @@ def check(wl, top_k, top_p, max_differ=1):
                          wl.u_accept, wl.u_sample, top_k=None if top_k is None else np.asarray(top_k),
                          top_p=None if top_p is None else np.asarray(top_p))
     n, flagged, differ = parity.compare(wl, gpu, res, check_probs=False)
+    parity.record(wl.name, n, flagged, differ, entry="sample_truncated")
     assert len(differ) <= max_differ, (flagged, differ)
     # p'(d_i), q'(d_i) for the drafts the oracle judged
     for b, r in enumerate(res):
