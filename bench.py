@@ -3,8 +3,10 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference] [--config 3]
 
-One step = one pass of the whole hot path over one batch: spec_verify_sample (row statistics,
-acceptance, first rejection, residual/bonus draw, emit) followed by spec_commit_kv_lengths.
+One step = one pass of the whole hot path over one batch: row statistics, acceptance, first
+rejection, residual/bonus draw, emit and the KV commit -- one spec_verify_sample_commit launch
+(spec_verify_greedy_commit for greedy batches; trees and truncated sampling are followed by a
+separate spec_commit_kv_lengths launch).
 The default workload is sampling with B=128 sequences, gamma=4 drafts, V=128256, bf16 logits,
 T=0.8 (295.5 MB of logits per step).  Prints one JSON line (rank 0).
 
@@ -521,20 +523,26 @@ def run_native(args):
         verify = [sv.prepare_verify_tree_greedy(tgt[c], toks, pars, nd, out, macc, path, st, workspace=ws,
                                                 stream=stream) for c in range(ncopies)]
     elif wl.greedy_only:
-        verify = [sv.prepare_verify_greedy(tgt[c], toks, nd, out, macc, st, workspace=ws, stream=stream)
-                  for c in range(ncopies)]
+        # verification and the commit of the round in one launch
+        verify = [sv.prepare_verify_greedy_commit(tgt[c], toks, nd, out, macc, kv, dkv, True, status=st,
+                                                  workspace=ws, stream=stream) for c in range(ncopies)]
     elif trunc:
         tk, tp = to_dev(wl.top_k), to_dev(wl.top_p)
         verify = [sv.prepare_verify_sample_truncated(tgt[c], drf[c], toks, nd, temp, tk, tp, ua, us, out, macc, dg, st,
                                                      workspace=ws, stream=stream) for c in range(ncopies)]
     else:
-        verify = [sv.prepare_verify_sample(tgt[c], drf[c], toks, nd, temp, ua, us, out, macc, dg, st,
-                                           workspace=ws, stream=stream) for c in range(ncopies)]
+        verify = [sv.prepare_verify_sample_commit(tgt[c], drf[c], toks, nd, temp, ua, us, out, macc, kv, dkv, True,
+                                                  diag=dg, status=st, workspace=ws, stream=stream)
+                  for c in range(ncopies)]
+    # a separate commit launch only where no fused call exists (trees, truncated sampling)
+    fused = not (tree or trunc)
     commit = sv.prepare_commit_kv_lengths(macc, kv, dkv, True, stream=stream, gmax=g)
+    step_commit = None if fused else commit
 
     for i in range(args.warmup):
         verify[i % ncopies]()
-        commit()
+        if step_commit:
+            step_commit()
     torch.cuda.synchronize(device)
     mean_emit = float(macc.float().mean().item()) + 1.0
 
@@ -554,7 +562,8 @@ def run_native(args):
         ev0[i].record(stream)
         verify[i % ncopies]()
         ev1[i].record(stream)
-        commit()
+        if step_commit:
+            step_commit()
     end.record(stream)
     torch.cuda.synchronize(device)
     w1 = time.time()
@@ -627,14 +636,16 @@ def run_native(args):
         if tree:
             sv.spec_verify_tree_greedy(d_in[0], d_in[1], d_in[2], d_in[3], out, macc, path, st, workspace=ws)
         elif wl.greedy_only:
-            sv.spec_verify_greedy(d_in[0], d_in[1], d_in[2], out, macc, st, workspace=ws)
+            sv.spec_verify_greedy_commit(d_in[0], d_in[1], d_in[2], out, macc, kv, None, True, status=st,
+                                         workspace=ws)
         elif trunc:
             sv.spec_verify_sample_truncated(d_in[0], d_in[1], d_in[2], d_in[3], d_in[4], tk, tp, d_in[5], d_in[6],
                                             out, macc, dg, st, workspace=ws)
         else:
-            sv.spec_verify_sample(d_in[0], d_in[1], d_in[2], d_in[3], d_in[4], d_in[5], d_in[6],
-                                  out, macc, dg, st, workspace=ws)
-        sv.spec_commit_kv_lengths(macc, kv, None, True, gmax=g)
+            sv.spec_verify_sample_commit(d_in[0], d_in[1], d_in[2], d_in[3], d_in[4], d_in[5], d_in[6],
+                                         out, macc, kv, None, True, diag=dg, status=st, workspace=ws)
+        if not fused:
+            sv.spec_commit_kv_lengths(macc, kv, None, True, gmax=g)
         h_out[0].copy_(out, non_blocking=True)
         h_out[1].copy_(macc, non_blocking=True)
         h_out[2].copy_(kv, non_blocking=True)
@@ -681,8 +692,9 @@ def run_native(args):
                          "kernel": ("verify_kernel<bf16, vec, greedy> (spec_verify_tree_greedy)" if tree
                                     else "trunc_rows + trunc_draw kernels (spec_verify_sample_truncated)"
                                     if trunc
-                                    else "verify_kernel<bf16, vec, greedy> (spec_verify_greedy)" if wl.greedy_only
-                                    else "verify_kernel<bf16, vec, mixed> (spec_verify_sample)"),
+                                    else "verify_kernel<bf16, vec, greedy> with the commit (spec_verify_greedy_commit)"
+                                    if wl.greedy_only
+                                    else "verify_kernel<bf16, vec, mixed> with the commit (spec_verify_sample_commit)"),
                          "kernel_ms_mean": kern_mean_ms, "kernel_ms_median": kern_med_ms,
                          "kernel_ms_p10": kern_p10, "kernel_ms_p90": kern_p90, "kernel_ms_max": ks[-1],
                          "frac_of_median": abytes / (kern_med_ms / 1e3) / 1e9 / peak,

@@ -287,6 +287,37 @@ int spec_commit_kv_lengths(const int32_t* num_accepted, int B, int32_t* target_k
                            int32_t* committed_len, int cap, int32_t* status, void* stream);
 
 /*
+ * Verification and the commit of the same round in one launch: spec_verify_greedy /
+ * spec_verify_sample followed by spec_commit_kv_lengths (with that call's out_tokens, gmax
+ * and status), fused.  The tutorial's §13.2 asks for the round's decision to stay on the GPU
+ * and for small kernels to be merged; here the thread that writes a sequence's outputs also
+ * rolls its KV lengths back (tutorial §5.1-§5.2; card §06), so a round costs one launch.
+ * Every output -- out_tokens, num_accepted, diag, status, the lengths, history and
+ * committed_len -- equals what the two separate calls leave, except that status carries
+ * SPEC_ST_HISTORY_FULL in the same word the verify call writes (the separate commit ORs it
+ * into the word the verify call wrote: the same value).
+ *
+ *   target_kv_len  [B] int32, required, read and written; draft_kv_len [B] or NULL
+ *   history [B][cap] and committed_len [B]: both NULL, or both given with cap >= 1
+ *
+ * Returns what the verify call returns, or SPEC_EINVAL for bad commit arguments (nothing is
+ * enqueued then).  Use a stops pass (spec_apply_stops) with the separate calls instead:
+ * the fused call commits every emitted token.
+ */
+int spec_verify_greedy_commit(const void* target_logits, int dtype, const int32_t* draft_tokens,
+                              const int32_t* num_draft, int B, int gmax, int V, int32_t* out_tokens,
+                              int32_t* num_accepted, int32_t* status, void* workspace, size_t workspace_bytes,
+                              int32_t* target_kv_len, int32_t* draft_kv_len, int correction_processed,
+                              int32_t* history, int32_t* committed_len, int cap, void* stream);
+int spec_verify_sample_commit(const void* target_logits, const void* draft_logits, int dtype,
+                              const int32_t* draft_tokens, const int32_t* num_draft,
+                              const float* temperature, const float* u_accept, const float* u_sample,
+                              int B, int gmax, int V, int32_t* out_tokens, int32_t* num_accepted,
+                              float* diag, int32_t* status, void* workspace, size_t workspace_bytes,
+                              int32_t* target_kv_len, int32_t* draft_kv_len, int correction_processed,
+                              int32_t* history, int32_t* committed_len, int cap, void* stream);
+
+/*
  * Stops: cut each round's emit where step-by-step decoding would have stopped (tutorial
  * §5.2: nothing after an EOS in the candidate block may reach the cache; §12.3: EOS,
  * maximum length and the rejection position must agree with step-by-step decoding; card §03:

@@ -80,6 +80,14 @@ struct Args {
   int32_t* status;
   const int32_t* parents;   // tree verification: node parents [B][gmax]; else null
   int32_t* path_nodes;      // tree verification: accepted path [B][gmax]
+  // the commit of the same round, done by the thread that writes the sequence's outputs
+  // (kv_target null: no commit)
+  int32_t* kv_target;       // [B] t, read and written
+  int32_t* kv_draft;        // [B] or null
+  int kv_add;               // 1 when the correction/bonus token counts as processed
+  int32_t* history;         // [B][cap] or null
+  int32_t* committed_len;   // [B] (with history)
+  int cap;
 };
 
 struct Geo {
@@ -603,6 +611,27 @@ __device__ __forceinline__ uint64_t settle_word(uint64_t* p, uint64_t v, Shared&
   return v;
 }
 
+// The commit of sequence b's round (tutorial §5.1-§5.2; card §06), when the call carries one:
+// the caches are trimmed to t + m and hold t + m + 1 once the last token has been fed; the m + 1
+// emitted tokens (the drafts d_0..d_{m-1}, then tok) are appended to the history at
+// committed_len, or, if they would pass its capacity, the sequence is left untouched.  Returns
+// the status bits to add.  Called by one thread.
+__device__ __forceinline__ int commit_round(const Args& a, int b, int m, int tok) {
+  if (!a.kv_target) return 0;
+  const int n = m + 1;
+  if (a.history) {
+    const int c = a.committed_len[b];
+    if (c < 0 || c > a.cap - n) return SPEC_ST_HISTORY_FULL;
+    int32_t* dst = a.history + int64_t(b) * a.cap + c;
+    for (int i = 0; i < m; ++i) dst[i] = a.draft_tokens[int64_t(b) * a.gmax + i];
+    dst[m] = tok;
+    a.committed_len[b] = c + n;
+  }
+  a.kv_target[b] += m + a.kv_add;
+  if (a.kv_draft) a.kv_draft[b] += m + a.kv_add;
+  return 0;
+}
+
 // ------------------------------------------------------------------------------------------
 // the draw: per-warp masses of each draw chunk, then the selector
 // ------------------------------------------------------------------------------------------
@@ -769,7 +798,8 @@ __device__ void select(const Args& a, const Geo& geo, const Work& w, const Seq<E
   if (tid == 0) {
     if (a.diag) a.diag[int64_t(b) * (2 * gmax + 1) + 2 * gmax] = sm.mass_out;
     a.num_accepted[b] = m;
-    if (a.status) a.status[b] = sm.flags & 0xff;
+    const int cf = commit_round(a, b, m, tok);
+    if (a.status) a.status[b] = (sm.flags | cf) & 0xff;
     uint64_t* pw = w.planw + int64_t(b) * 4;
     for (int i = 0; i < 4; ++i) pw[i] = 0;
     w.bdone[b] = 0;
@@ -1005,7 +1035,8 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
       for (int i = tid; i < 2 * gmax + 1; i += kThreads) a.diag[int64_t(b) * (2 * gmax + 1) + i] = NAN;
     if (tid == 0) {
       a.num_accepted[b] = m;
-      if (a.status) a.status[b] = sm.flags;
+      const int cf = commit_round(a, b, m, sm.rowArg[m]);
+      if (a.status) a.status[b] = sm.flags | cf;
       w.cnt[b] = 0;
     }
     __syncthreads();
@@ -2091,11 +2122,50 @@ extern "C" size_t spec_verify_workspace_bytes(int B, int gmax, int V, int dtype)
 namespace specverify {
 namespace {
 
+// The commit a fused verify-and-commit call carries (kv_target null: none).
+struct CommitArgs {
+  int32_t* kv_target;
+  int32_t* kv_draft;
+  int add;
+  int32_t* history;
+  int32_t* committed_len;
+  int cap;
+};
+
+// host checks of a fused call's commit arguments, the same as spec_commit_kv_lengths makes
+int check_commit(const CommitArgs& c) {
+  if (!c.kv_target) {
+    set_error("null required pointer (target_kv_len)");
+    return SPEC_EINVAL;
+  }
+  if ((c.history != nullptr) != (c.committed_len != nullptr)) {
+    set_error("history and committed_len must be given together");
+    return SPEC_EINVAL;
+  }
+  if (c.history && c.cap < 1) {
+    set_error("history capacity %d < 1", c.cap);
+    return SPEC_EINVAL;
+  }
+  return SPEC_OK;
+}
+
+void set_commit(Args& a, const CommitArgs* c) {
+  if (!c) return;
+  a.kv_target = c->kv_target;
+  a.kv_draft = c->kv_draft;
+  a.kv_add = c->add ? 1 : 0;
+  a.history = c->history;
+  a.committed_len = c->committed_len;
+  a.cap = c->cap;
+}
+
 // The verify calls on either layout: saved == null is the one-array layout.
 int verify_greedy(const void* saved, const void* target, int dtype, const int32_t* draft_tokens,
                   const int32_t* num_draft, int B, int gmax, int V, int32_t* out_tokens, int32_t* num_accepted,
-                  int32_t* status, void* workspace, size_t workspace_bytes, void* stream) {
+                  int32_t* status, void* workspace, size_t workspace_bytes, void* stream,
+                  const CommitArgs* ck = nullptr) {
   Args a = {};
+  set_commit(a, ck);
   a.saved = saved;
   a.target = target;
   a.draft_tokens = draft_tokens;
@@ -2113,12 +2183,13 @@ int verify_sample(const void* saved, const void* target, const void* draft_logit
                   const int32_t* draft_tokens, const int32_t* num_draft, const float* temperature,
                   const float* u_accept, const float* u_sample, int B, int gmax, int V, int32_t* out_tokens,
                   int32_t* num_accepted, float* diag, int32_t* status, void* workspace, size_t workspace_bytes,
-                  void* stream) {
+                  void* stream, const CommitArgs* ck = nullptr) {
   if (!temperature || !u_sample || (gmax > 0 && (!draft_logits || !u_accept))) {
     set_error("null required pointer (draft_logits, temperature, u_accept or u_sample)");
     return SPEC_EINVAL;
   }
   Args a = {};
+  set_commit(a, ck);
   a.saved = saved;
   a.target = target;
   a.draft = draft_logits;
@@ -2173,6 +2244,40 @@ extern "C" int spec_verify_sample(const void* target_logits, const void* draft_l
   return verify_sample(nullptr, target_logits, draft_logits, dtype, draft_tokens, num_draft, temperature, u_accept,
                        u_sample, B, gmax, V, out_tokens, num_accepted, diag, status, workspace, workspace_bytes,
                        stream);
+}
+
+extern "C" int spec_verify_greedy_commit(const void* target_logits, int dtype, const int32_t* draft_tokens,
+                                         const int32_t* num_draft, int B, int gmax, int V, int32_t* out_tokens,
+                                         int32_t* num_accepted, int32_t* status, void* workspace,
+                                         size_t workspace_bytes, int32_t* target_kv_len, int32_t* draft_kv_len,
+                                         int correction_processed, int32_t* history, int32_t* committed_len,
+                                         int cap, void* stream) {
+  clear_error();
+  int rc = check_common(target_logits, dtype, draft_tokens, B, gmax, V, out_tokens, num_accepted);
+  if (rc != SPEC_OK || B == 0) return rc;
+  const CommitArgs ck = {target_kv_len, draft_kv_len, correction_processed, history, committed_len, cap};
+  rc = check_commit(ck);
+  if (rc != SPEC_OK) return rc;
+  return verify_greedy(nullptr, target_logits, dtype, draft_tokens, num_draft, B, gmax, V, out_tokens, num_accepted,
+                       status, workspace, workspace_bytes, stream, &ck);
+}
+
+extern "C" int spec_verify_sample_commit(const void* target_logits, const void* draft_logits, int dtype,
+                                         const int32_t* draft_tokens, const int32_t* num_draft,
+                                         const float* temperature, const float* u_accept, const float* u_sample,
+                                         int B, int gmax, int V, int32_t* out_tokens, int32_t* num_accepted,
+                                         float* diag, int32_t* status, void* workspace, size_t workspace_bytes,
+                                         int32_t* target_kv_len, int32_t* draft_kv_len, int correction_processed,
+                                         int32_t* history, int32_t* committed_len, int cap, void* stream) {
+  clear_error();
+  int rc = check_common(target_logits, dtype, draft_tokens, B, gmax, V, out_tokens, num_accepted);
+  if (rc != SPEC_OK || B == 0) return rc;
+  const CommitArgs ck = {target_kv_len, draft_kv_len, correction_processed, history, committed_len, cap};
+  rc = check_commit(ck);
+  if (rc != SPEC_OK) return rc;
+  return verify_sample(nullptr, target_logits, draft_logits, dtype, draft_tokens, num_draft, temperature, u_accept,
+                       u_sample, B, gmax, V, out_tokens, num_accepted, diag, status, workspace, workspace_bytes,
+                       stream, &ck);
 }
 
 extern "C" int spec_verify_greedy_split(const void* saved_logits, const void* block_logits, int dtype,

@@ -177,7 +177,8 @@ def test_binding_arity_matches_header(lib):
                  "spec_verify_workspace_bytes", "spec_verify_plan", "spec_verify_sample_static",
                  "spec_apply_stops", "spec_verify_greedy_split", "spec_verify_sample_split",
                  "spec_verify_tree_greedy", "spec_verify_sample_truncated",
-                 "spec_verify_sample_truncated_split"):
+                 "spec_verify_sample_truncated_split", "spec_verify_greedy_commit",
+                 "spec_verify_sample_commit"):
         m = re.search(r"\b" + name + r"\s*\(([^)]*)\)", text)
         params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
         assert len(getattr(lib, name).argtypes) == len(params), name
@@ -197,3 +198,22 @@ def test_static_workspace_refuses_oversized_calls(lib):
     assert lib.spec_launch_count() == n0
     assert lib.spec_verify_sample_static(FAKE, FAKE, 0, FAKE, None, FAKE, FAKE, FAKE, 0, 4, 128256,
                                          FAKE, FAKE, None, None, None) == 0
+
+
+def test_fused_commit_argument_checks(lib):
+    """The fused verify-and-commit calls refuse bad commit arguments on the host, before any
+    CUDA call, the way spec_commit_kv_lengths does."""
+    n0 = lib.spec_launch_count()
+    g = lambda t=FAKE, h=None, c=None, cap=0: lib.spec_verify_greedy_commit(
+        FAKE, 0, FAKE, None, 4, 3, 100, FAKE, FAKE, None, FAKE, 8, t, None, 1, h, c, cap, None)
+    assert g(t=None) == 1 and b"target_kv_len" in lib.spec_last_error()
+    assert g(h=FAKE) == 1 and g(c=FAKE) == 1
+    assert g(h=FAKE, c=FAKE, cap=0) == 1 and b"capacity" in lib.spec_last_error()
+    s = lambda t=FAKE, h=None, c=None, cap=0, B=4: lib.spec_verify_sample_commit(
+        FAKE, FAKE, 0, FAKE, None, FAKE, FAKE, FAKE, B, 3, 100, FAKE, FAKE, None, None, FAKE, 8,
+        t, None, 1, h, c, cap, None)
+    assert s(t=None) == 1 and s(h=FAKE) == 1
+    assert s(t=None, B=0) == 0          # empty batch: nothing to check, nothing enqueued
+    # valid commit arguments reach the workspace check (8 bytes: refused) and stop there
+    assert g() == 3 and s() == 3 and b"workspace" in lib.spec_last_error()
+    assert lib.spec_launch_count() == n0

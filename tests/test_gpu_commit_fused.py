@@ -1,0 +1,83 @@
+"""The fused verify-and-commit calls leave exactly what the verify call followed by
+spec_commit_kv_lengths leaves: tokens, accepted counts, diag, status (history overflow
+included), both KV lengths, the history and the committed lengths."""
+import numpy as np
+import pytest
+import torch
+
+from speculative_decoding_verification_34_gb300 import specverify as sv
+from speculative_decoding_verification_34_gb300 import workloads as W
+from tests.parity import dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _state(wl, cap, seed):
+    rng = np.random.default_rng(seed)
+    B = wl.B
+    clen = rng.integers(0, cap, B).astype(np.int32)
+    clen[::7] = cap - 1            # no room for a whole round: left untouched, flagged
+    clen[3] = -1                   # an illegal append position: likewise
+    hist = np.full((B, cap), -5, np.int32)
+    t = wl.kv_len.astype(np.int32)
+    return {"t": dev(t), "d": dev(t + 1), "h": dev(hist), "c": dev(clen)}
+
+
+def _outs(wl):
+    B, g = wl.B, wl.gmax
+    return (torch.full((B, g + 1), -7, dtype=torch.int32, device="cuda"),
+            torch.full((B,), -7, dtype=torch.int32, device="cuda"),
+            torch.full((B, 2 * g + 1), 1.5, dtype=torch.float32, device="cuda"),
+            torch.full((B,), -7, dtype=torch.int32, device="cuda"))
+
+
+def _host(*ts):
+    return [t.cpu().numpy() for t in ts]
+
+
+@pytest.mark.parametrize("name", ["sampling", "mixed", "greedy"])
+def test_fused_commit_equals_separate_calls(name):
+    if name == "sampling":
+        wl = W.sampling_workload("fused-s", cfg=61, seed=0, B=96, gmax=4, V=128256, dtype="bf16",
+                                 target_sigma=3.0, draft_scale=0.7, draft_sigma=1.0, temperature=0.8)
+    elif name == "mixed":
+        wl = W.sampling_workload("fused-m", cfg=62, seed=0, B=64, gmax=6, V=50000, dtype="f32",
+                                 target_sigma=3.0, draft_scale=1.0, draft_sigma=1.5, temperature=0.7,
+                                 num_draft=np.arange(64) % 7, greedy_mask=(np.arange(64) % 2) == 0)
+    else:
+        wl = W.greedy_planted_workload("fused-g", cfg=63, seed=0, B=64, gmax=5, V=32000, alpha=0.8)
+    cap = 12
+    code = sv.SPEC_BF16 if wl.dtype == "bf16" else sv.SPEC_F32
+    ws = torch.zeros(sv.spec_verify_workspace_bytes(wl.B, wl.gmax, wl.V, code), dtype=torch.uint8, device="cuda")
+    tgt, toks, nd = dev(wl.target), dev(wl.draft_tokens), dev(wl.num_draft)
+    got = {}
+    for fused in (False, True):
+        for proc in (True, False):
+            st = _state(wl, cap, seed=5)
+            out, m, dg, status = _outs(wl)
+            if wl.greedy_only:
+                if fused:
+                    sv.spec_verify_greedy_commit(tgt, toks, nd, out, m, st["t"], st["d"], proc, st["h"], st["c"],
+                                                 status=status, workspace=ws)
+                else:
+                    sv.spec_verify_greedy(tgt, toks, nd, out, m, status, workspace=ws)
+                    sv.spec_commit_kv_lengths(m, st["t"], st["d"], proc, out, st["h"], st["c"], status)
+            else:
+                args = (tgt, dev(wl.draft), toks, nd, dev(wl.temperature), dev(wl.u_accept), dev(wl.u_sample),
+                        out, m)
+                if fused:
+                    sv.spec_verify_sample_commit(*args, st["t"], st["d"], proc, st["h"], st["c"], diag=dg,
+                                                 status=status, workspace=ws)
+                else:
+                    sv.spec_verify_sample(*args, diag=dg, status=status, workspace=ws)
+                    sv.spec_commit_kv_lengths(m, st["t"], st["d"], proc, out, st["h"], st["c"], status)
+            torch.cuda.synchronize()
+            got[(fused, proc)] = _host(out, m, dg.view(torch.int32), status, st["t"], st["d"], st["h"], st["c"])
+    assert bool((ws == 0).all())
+    names = ("out_tokens", "num_accepted", "diag", "status", "target_kv_len", "draft_kv_len", "history",
+             "committed_len")
+    for proc in (True, False):
+        for n, x, y in zip(names, got[(False, proc)], got[(True, proc)]):
+            assert np.array_equal(x, y), (name, proc, n)
+    status = got[(True, True)][3]
+    assert (status & sv.ST_HISTORY_FULL).any() and not (status & sv.ST_HISTORY_FULL).all()
