@@ -36,6 +36,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "schedule.h"
 
 namespace specverify {
 namespace {
@@ -51,7 +52,7 @@ constexpr int kSubPerLane = kMaxDrawChunks * kWarps / 32;   // selector: sub-ran
 constexpr int kChunkTarget = 65536;            // ids per row chunk before rounding
 constexpr int kDrawChunkTarget = 16384;        // ids per draw chunk before rounding
 constexpr double kDrawWaves = 1.5;             // distance of the draw behind the rows
-constexpr long long kDeferBytes = 64LL << 20;  // draw rows deferred to the end of a call
+constexpr long long kDeferBytes = 48LL << 20;  // draw rows deferred to the end of a call
 constexpr int kMinBlocks = 4;                  // resident blocks per SM the registers allow
 constexpr int kMaxGroups = 65535;                      // grid z limit
 constexpr int kPlanWaitIters = 64;                     // optional bounded wait of a B unit (~31 us)
@@ -100,31 +101,6 @@ struct Geo {
   int ndefer;   // the first ndefer sequences of a launch draw after all of its row units
   int b0, b1;   // sequences [b0, b1) of this launch
 };
-
-// The sequence whose B units sit in group z of a launch of nb sequences (-1: none).  Groups
-// 0..nb-1 hold the row units of sequence z and, delta groups behind them, the B units of the
-// sequences from ndefer on: their rows are still in L2 when they draw.  After the last row unit
-// come the B units of the last delta sequences, which cannot sit delta groups behind (their
-// plans come out as these units start), then those of the first ndefer sequences, whose plans
-// are long out: their draws keep HBM busy while the last sequences are decided.
-__host__ __device__ inline int draw_group_seq(int z, int nb, int delta, int ndefer) {
-  const int nl = delta < nb ? delta : nb;   // the last sequences
-  if (z < nb) {
-    const int bl = z - delta;
-    return bl >= ndefer ? bl : -1;
-  }
-  const int j = z - nb;
-  if (j < nl) return nb - nl + j;
-  const int bl = j - nl;
-  const int nd = ndefer < nb - nl ? ndefer : nb - nl;
-  return bl < nd ? bl : -1;
-}
-
-__host__ __device__ inline int draw_groups(int nb, int delta, int ndefer) {
-  const int nl = delta < nb ? delta : nb;
-  const int nd = ndefer < nb - nl ? ndefer : nb - nl;
-  return nb + nl + nd;
-}
 
 struct __align__(16) PlanRec {   // per sequence, published by the decider for the draw
   int m, g, flags, pair;
