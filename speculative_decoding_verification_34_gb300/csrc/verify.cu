@@ -49,6 +49,9 @@ constexpr long long kWaitNs = 2000000;         // bound on any wait for another 
 constexpr int kMaxChunks = 64;                 // row chunks per row
 constexpr int kMaxDrawChunks = 16;             // draw chunks per row
 constexpr int kSubPerLane = kMaxDrawChunks * kWarps / 32;   // selector: sub-ranges per lane
+constexpr int kPartBuf = 512;                  // decider: row partials staged in shared memory at once
+static_assert(kPartBuf % kThreads == 0 && kMaxChunks < kPartBuf, "partial batches");
+static_assert(SPEC_MAX_GAMMA < kThreads, "one output per thread");
 constexpr int kChunkTarget = 65536;            // ids per row chunk before rounding
 constexpr int kDrawChunkTarget = 16384;        // ids per draw chunk before rounding
 constexpr double kDrawWaves = 1.5;             // distance of the draw behind the rows
@@ -451,7 +454,9 @@ struct Shared {
   unsigned taken[2];
   int err;
   float base, target, mass_out;
+  int hist;                 // history slot of the round's first token, -1: no history write
   PlanRec plan;
+  float2 pbuf[kPartBuf];    // decider: one batch of rows' partials
 };
 
 // ------------------------------------------------------------------------------------------
@@ -589,23 +594,43 @@ __device__ __forceinline__ uint64_t settle_word(uint64_t* p, uint64_t v, Shared&
 
 // The commit of sequence b's round (tutorial §5.1-§5.2; card §06), when the call carries one:
 // the caches are trimmed to t + m and hold t + m + 1 once the last token has been fed; the m + 1
-// emitted tokens (the drafts d_0..d_{m-1}, then tok) are appended to the history at
-// committed_len, or, if they would pass its capacity, the sequence is left untouched.  Returns
-// the status bits to add.  Called by one thread.
-__device__ __forceinline__ int commit_round(const Args& a, int b, int m, int tok) {
+// emitted tokens (the drafts d_0..d_{m-1}, then the last token) are appended to the history at
+// committed_len, or, if they would pass its capacity, the sequence is left untouched.  The
+// current lengths are loaded when the thread that commits starts its part of the round
+// (commit_load), so that no load trails the outputs.
+struct CommitIn {
+  int kvt, kvd, clen;
+};
+
+__device__ __forceinline__ CommitIn commit_load(const Args& a, int b) {
+  CommitIn c = {0, 0, 0};
+  if (!a.kv_target) return c;
+  c.kvt = a.kv_target[b];
+  if (a.kv_draft) c.kvd = a.kv_draft[b];
+  if (a.history) c.clen = a.committed_len[b];
+  return c;
+}
+
+// Writes the new lengths; returns the status bits to add and, in *hist, the history slot the
+// m + 1 tokens go to (-1: none), which the output threads fill.  Called by one thread.
+__device__ __forceinline__ int commit_apply(const Args& a, int b, int m, const CommitIn& c, int* hist) {
+  *hist = -1;
   if (!a.kv_target) return 0;
   const int n = m + 1;
   if (a.history) {
-    const int c = a.committed_len[b];
-    if (c < 0 || c > a.cap - n) return SPEC_ST_HISTORY_FULL;
-    int32_t* dst = a.history + int64_t(b) * a.cap + c;
-    for (int i = 0; i < m; ++i) dst[i] = a.draft_tokens[int64_t(b) * a.gmax + i];
-    dst[m] = tok;
-    a.committed_len[b] = c + n;
+    if (c.clen < 0 || c.clen > a.cap - n) return SPEC_ST_HISTORY_FULL;
+    *hist = c.clen;
+    a.committed_len[b] = c.clen + n;
   }
-  a.kv_target[b] += m + a.kv_add;
-  if (a.kv_draft) a.kv_draft[b] += m + a.kv_add;
+  a.kv_target[b] = c.kvt + m + a.kv_add;
+  if (a.kv_draft) a.kv_draft[b] = c.kvd + m + a.kv_add;
   return 0;
+}
+
+// Output i of sequence b (i = 0..gmax): token v, and its history copy when the commit has one.
+__device__ __forceinline__ void put_output(const Args& a, int b, int i, int m, int v, int hist) {
+  a.out_tokens[int64_t(b) * (a.gmax + 1) + i] = v;
+  if (hist >= 0 && i <= m) a.history[int64_t(b) * a.cap + hist + i] = v;
 }
 
 // ------------------------------------------------------------------------------------------
@@ -632,6 +657,11 @@ __device__ void select(const Args& a, const Geo& geo, const Work& w, const Seq<E
   const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
   const int b = sq.b, gmax = a.gmax;
   const bool pair = pl.pair != 0;
+  // what the outputs and the commit need besides the token, loaded before the masses so that
+  // no round trip trails the draw: u, the accepted drafts (thread i holds d_i) and the lengths
+  const float us = warp == 0 ? __ldg(&a.u_sample[b]) : 0.f;
+  const int dtok = tid < pl.m ? __ldg(&a.draft_tokens[int64_t(b) * gmax + tid]) : -1;
+  const CommitIn cin = tid == 0 ? commit_load(a, b) : CommitIn{0, 0, 0};
   if (tid == 0) sm.flags_extra = 0;
   __syncthreads();
   if (warp == 0) {
@@ -661,7 +691,7 @@ __device__ void select(const Args& a, const Geo& geo, const Work& w, const Seq<E
     const float R = __shfl_sync(kFull, ir, 31), Pm = __shfl_sync(kFull, ip, 31);
     const bool use_w = !pair || R > 0.f;   // bonus: the weights are p itself
     const float total = use_w ? R : Pm;
-    const float target = __fmul_rn(a.u_sample[b], total);
+    const float target = __fmul_rn(us, total);
     const float incl = use_w ? ir : ip, mine = use_w ? lr : lp;
     float excl = __shfl_up_sync(kFull, incl, 1);
     if (lane == 0) excl = 0.f;
@@ -764,22 +794,21 @@ __device__ void select(const Args& a, const Geo& geo, const Work& w, const Seq<E
   }
   const int m = pl.m;
   const int tok = sm.token >= 0 ? sm.token : (sm.lastpos >= 0 ? sm.lastpos : int(lo));
-  for (int i = tid; i <= gmax; i += kThreads) {
-    int v = -1;
-    if (i < m) v = a.draft_tokens[int64_t(b) * gmax + i];
-    else if (i == m) v = tok;
-    a.out_tokens[int64_t(b) * (gmax + 1) + i] = v;
-  }
-  for (int c = tid; c < geo.DCL; c += kThreads) w.state[int64_t(b) * geo.DCL + c] = kChunkFree;
   if (tid == 0) {
+    int hist;
+    const int cf = commit_apply(a, b, m, cin, &hist);
+    sm.hist = hist;
     if (a.diag) a.diag[int64_t(b) * (2 * gmax + 1) + 2 * gmax] = sm.mass_out;
     a.num_accepted[b] = m;
-    const int cf = commit_round(a, b, m, tok);
     if (a.status) a.status[b] = (sm.flags | cf) & 0xff;
     uint64_t* pw = w.planw + int64_t(b) * 4;
     for (int i = 0; i < 4; ++i) pw[i] = 0;
     w.bdone[b] = 0;
   }
+  __syncthreads();
+  // gmax < kThreads: thread i writes output i
+  if (tid <= gmax) put_output(a, b, tid, m, tid < m ? dtok : (tid == m ? tok : -1), sm.hist);
+  for (int c = tid; c < geo.DCL; c += kThreads) w.state[int64_t(b) * geo.DCL + c] = kChunkFree;
   __syncthreads();
 }
 
@@ -862,19 +891,39 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
       vxq = ld_relaxed_u64(xdq);
     }
   }
-  // one warp per row: lanes take chunks c and c + 32 (at most 64 chunks)
+  // a greedy sequence is committed here: its lengths are loaded with the rest
+  const CommitIn cin = (tid == 0 && !sq.sampling && !a.parents) ? commit_load(a, b) : CommitIn{0, 0, 0};
+  // The row partials, a batch of rows at a time: every word of the batch is loaded at once (a
+  // thread per word) and staged in shared memory, then one warp per row combines them, lanes
+  // taking chunks c and c + 32 (at most 64 chunks).
   uint64_t* part = w.part + int64_t(b) * geo.nslots * CL;
-  for (int slot = warp; slot < geo.nslots; slot += kWarps) {
+  const float2 none = make_float2(-INFINITY, sq.sampling ? 0.f : __int_as_float(INT_MAX));
+  auto unpack = [&](uint64_t v) {
+    const uint32_t hi = uint32_t(v >> 32);
+    return make_float2(__uint_as_float(uint32_t(v)), sq.sampling ? __uint_as_float(hi) : __int_as_float(int(~hi)));
+  };
+  const int per_batch = kPartBuf / CL;   // rows per batch (CL <= kMaxChunks < kPartBuf)
+  for (int s0 = 0; s0 < geo.nslots; s0 += per_batch) {
+    const int s1 = s0 + per_batch < geo.nslots ? s0 + per_batch : geo.nslots;
+    const int nw = (s1 - s0) * CL;
+    uint64_t* pb = part + s0 * CL;
+    uint64_t v[kPartBuf / kThreads];
+#pragma unroll
+    for (int j = 0; j < kPartBuf / kThreads; ++j) {
+      const int i = tid + j * kThreads;
+      v[j] = (i < nw && sq.slot_valid(s0 + i / CL, gmax)) ? ld_relaxed_u64(&pb[i]) : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < kPartBuf / kThreads; ++j) {
+      const int i = tid + j * kThreads;
+      if (i < nw) sm.pbuf[i] = sq.slot_valid(s0 + i / CL, gmax) ? unpack(settle_word(&pb[i], v[j], sm)) : none;
+    }
+    __syncthreads();
+  for (int slot = s0 + warp; slot < s1; slot += kWarps) {
     if (!sq.slot_valid(slot, gmax)) continue;
-    uint64_t* pp = part + slot * CL;
-    const float2 none = make_float2(-INFINITY, sq.sampling ? 0.f : __int_as_float(INT_MAX));
-    auto unpack = [&](uint64_t v) {
-      const uint32_t hi = uint32_t(v >> 32);
-      return make_float2(__uint_as_float(uint32_t(v)), sq.sampling ? __uint_as_float(hi) : __int_as_float(int(~hi)));
-    };
-    const uint64_t v0 = lane < CL ? ld_relaxed_u64(&pp[lane]) : 0, v1 = lane + 32 < CL ? ld_relaxed_u64(&pp[lane + 32]) : 0;
-    const float2 p0 = lane < CL ? unpack(settle_word(&pp[lane], v0, sm)) : none;
-    const float2 p1 = lane + 32 < CL ? unpack(settle_word(&pp[lane + 32], v1, sm)) : none;
+    const float2* pp = sm.pbuf + (slot - s0) * CL;
+    const float2 p0 = lane < CL ? pp[lane] : none;
+    const float2 p1 = lane + 32 < CL ? pp[lane + 32] : none;
     if (sq.sampling) {
       const float M = warp_max(fmaxf(p0.x, p1.x));
       float S = 0.f;
@@ -894,6 +943,8 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
       warp_argmax(bv, bi);
       if (lane == 0) sm.rowArg[slot] = bi;
     }
+  }
+    __syncthreads();   // the buffer is refilled by the next batch
   }
   if (drafts && sq.sampling) {
     // published for every draft row: the logit at d, or a marker when d is outside the row
@@ -1001,20 +1052,19 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
   __syncthreads();
   const int m = sm.m;
   if (!sq.sampling) {
-    for (int i = tid; i <= gmax; i += kThreads) {
-      int v = -1;
-      if (i < m) v = a.draft_tokens[int64_t(b) * gmax + i];
-      else if (i == m) v = sm.rowArg[m];
-      a.out_tokens[int64_t(b) * (gmax + 1) + i] = v;
-    }
-    if (a.diag)
-      for (int i = tid; i < 2 * gmax + 1; i += kThreads) a.diag[int64_t(b) * (2 * gmax + 1) + i] = NAN;
     if (tid == 0) {
+      int hist;
+      const int cf = commit_apply(a, b, m, cin, &hist);
+      sm.hist = hist;
       a.num_accepted[b] = m;
-      const int cf = commit_round(a, b, m, sm.rowArg[m]);
       if (a.status) a.status[b] = sm.flags | cf;
       w.cnt[b] = 0;
     }
+    __syncthreads();
+    // thread i < m is lane i of warp 0, which holds d_i
+    if (tid <= gmax) put_output(a, b, tid, m, tid < m ? d : (tid == m ? sm.rowArg[m] : -1), sm.hist);
+    if (a.diag)
+      for (int i = tid; i < 2 * gmax + 1; i += kThreads) a.diag[int64_t(b) * (2 * gmax + 1) + i] = NAN;
     __syncthreads();
     return;
   }
