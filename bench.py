@@ -38,6 +38,8 @@ METRIC = "verified draft rows/sec and achieved HBM GB/s (% of GB300 peak), 1 GPU
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "verify_sample_B128_g4_V128256_bf16_dram.txt")
 KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_verification_34_gb300", "csrc", "verify.cu")
+# the verify kernel's sources: the kernel and the draw placement it compiles in
+KERNEL_SRCS = (KERNEL_SRC, os.path.join(ROOT, "speculative_decoding_verification_34_gb300", "csrc", "schedule.h"))
 
 
 def parse_args():
@@ -113,10 +115,11 @@ def measured_peak():
     return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
 
 
-def code_sha256(path):
-    """sha256 of a C/CUDA source with its comments removed and its whitespace collapsed, so that
-    an edit of comments alone keeps a recorded measurement of the compiled code valid."""
-    text = open(path, encoding="utf-8").read()
+def code_sha256(*paths):
+    """sha256 of C/CUDA sources (in order) with their comments removed and their whitespace
+    collapsed, so that an edit of comments alone keeps a recorded measurement of the compiled
+    code valid."""
+    text = "\n".join(open(p, encoding="utf-8").read() for p in paths)
     out, i, n = [], 0, len(text)
     while i < n:
         c = text[i]
@@ -150,7 +153,7 @@ def recorded_traffic(units_per_launch):
         if ":" in line and not line.startswith("#"):
             k, v = line.split(":", 1)
             kv[k.strip()] = v.strip()
-    if kv.get("code_sha256") != code_sha256(KERNEL_SRC):
+    if kv.get("code_sha256") != code_sha256(*KERNEL_SRCS):
         return None
     try:
         return int(kv["dram_bytes_per_launch"])
@@ -597,7 +600,23 @@ def run_native(args):
     value = aggregate_rate(world, rows_step, K, elapsed_ms)
     abytes = wl.algorithmic_bytes()
     peak, peak_src = measured_peak()
-    achieved = abytes / (kern_mean_ms / 1e3) / 1e9
+    # The kernel's average launch duration.  Where a step is exactly one verify launch (the
+    # fused calls), the timed region holds nothing else: its length over the launches in it is
+    # that average, the gap to the next launch included.  Otherwise (a separate commit or stops
+    # launch in the step) the per-launch event pairs give it.  An event pair around a launch
+    # adds its own time, measured here on an empty pair.
+    one_launch_per_step = fused and launches == K
+    region_ms = elapsed_ms / K
+    kern_avg_ms = region_ms if one_launch_per_step else kern_mean_ms
+    achieved = abytes / (kern_avg_ms / 1e3) / 1e9
+    torch.cuda.synchronize(device)
+    ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(200)]
+    torch.cuda._sleep(int(2e6))
+    for a_, b_ in ee:
+        a_.record(stream)
+        b_.record(stream)
+    torch.cuda.synchronize(device)
+    empty_pair_us = statistics.median(a_.elapsed_time(b_) for a_, b_ in ee) * 1e3
 
     # ---- the post-verify kernels alone (stops, commit), per launch, on the same stream ----
     # Each batch of launches is queued behind a verify call, so the GPU runs them back to back
@@ -705,12 +724,19 @@ def run_native(args):
                                     else "verify_kernel<bf16, vec, greedy> with the commit (spec_verify_greedy_commit)"
                                     if wl.greedy_only
                                     else "verify_kernel<bf16, vec, mixed> with the commit (spec_verify_sample_commit)"),
+                         "kernel_ms": kern_avg_ms,
+                         "kernel_ms_source": ("timed region / launches: one verify launch per step, back to back"
+                                              if one_launch_per_step else "mean of per-launch event pairs"),
                          "kernel_ms_mean": kern_mean_ms, "kernel_ms_median": kern_med_ms,
                          "kernel_ms_p10": kern_p10, "kernel_ms_p90": kern_p90, "kernel_ms_max": ks[-1],
+                         "frac_per_launch_events_mean": abytes / (kern_mean_ms / 1e3) / 1e9 / peak,
                          "frac_of_median": abytes / (kern_med_ms / 1e3) / 1e9 / peak,
+                         "empty_event_pair_us": empty_pair_us,
                          "launches_timed": len(ks), "launches_above_1p05_median": outliers,
                          "slowest_launches_ms": ks[-3:],
-                         "kernel_timing": "a second pass of the K steps with an event pair around each verify launch",
+                         "kernel_timing": "kernel_ms_mean/median/p10/p90/max: a second pass of the K steps with an "
+                                          "event pair around each verify launch (each pair adds its own time: "
+                                          "empty_event_pair_us)",
                          "algorithmic_bytes_per_launch": abytes, "peak_source": peak_src},
             "step_minus_kernel_median_ms": elapsed_ms / K - kern_med_ms,
             "step_minus_kernel_mean_ms": elapsed_ms / K - kern_mean_ms,

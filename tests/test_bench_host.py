@@ -19,3 +19,15 @@ def test_code_hash_ignores_comments_only(tmp_path):
     assert h("/* a block comment */\n" + src + "\n// trailing\n") == base
     assert h(src.replace("red.shared.add.u32", "red.shared.add.s32", 1)) != base
     assert h(src.replace("kThreads", "kThreads + 0", 1)) != base
+
+
+def test_code_hash_covers_the_schedule_header(tmp_path):
+    """The recorded figure is tied to the draw placement too (csrc/schedule.h)."""
+    base = bench.code_sha256(*bench.KERNEL_SRCS)
+    assert base != bench.code_sha256(bench.KERNEL_SRC)
+    hdr = open(bench.KERNEL_SRCS[1], encoding="utf-8").read()
+    p = tmp_path / "s.h"
+    p.write_text(hdr.replace("if (j < nd) return j;", "if (j < nd) return nd - 1 - j;", 1), encoding="utf-8")
+    assert bench.code_sha256(bench.KERNEL_SRC, str(p)) != base
+    p.write_text("// comment\n" + hdr, encoding="utf-8")
+    assert bench.code_sha256(bench.KERNEL_SRC, str(p)) == base
