@@ -83,7 +83,8 @@ def oracle_one(wl, b):
         return int(wl.num_nodes[b])
     O.verify_batch(wl.target, wl.draft, wl.dtype, wl.draft_tokens, wl.num_draft,
                    None if wl.greedy_only else wl.temperature, wl.u_accept, wl.u_sample, seqs=[b],
-                   top_k=getattr(wl, "top_k", None), top_p=getattr(wl, "top_p", None))
+                   top_k=getattr(wl, "top_k", None), top_p=getattr(wl, "top_p", None),
+                   nan_masked=getattr(wl, "top_k", None) is not None)
     return int(wl.num_draft[b])
 
 
@@ -379,7 +380,8 @@ def parity_record(wl, gpu, tol=1e-5):
     else:
         res = O.verify_batch(wl.target, wl.draft, wl.dtype, wl.draft_tokens, wl.num_draft,
                              None if wl.greedy_only else wl.temperature, wl.u_accept, wl.u_sample,
-                             top_k=getattr(wl, "top_k", None), top_p=getattr(wl, "top_p", None))
+                             top_k=getattr(wl, "top_k", None), top_p=getattr(wl, "top_p", None),
+                             nan_masked=getattr(wl, "top_k", None) is not None)
     g_all = gpu["out"].shape[1] - 1
     for b, r in enumerate(res):
         want = np.full(g_all + 1, -1)

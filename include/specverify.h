@@ -76,6 +76,10 @@ typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype_t;
 #define SPEC_ST_STOPPED 32       /* stops: the sequence emitted its end token or used up its budget */
 #define SPEC_ST_BAD_TREE 64      /* tree: a node's parent index was not below its own; it and its
                                     subtree counted as rejected */
+#define SPEC_ST_BAD_ROW 128      /* sampling: a row the call reads has no finite maximum or holds a
+                                    NaN (all -inf, a +inf or a NaN logit), so it defines no
+                                    distribution; the sequence's outputs are a well-formed step
+                                    (drafts 0..m-1, then one id) whose token is not defined */
 
 /*
  * Greedy verification (temperature 0).

@@ -77,6 +77,7 @@ ST_CLAMPED_GAMMA = 4
 ST_HISTORY_FULL = 8
 ST_STOPPED = 32
 ST_BAD_TREE = 64
+ST_BAD_ROW = 128
 
 
 def widen(row: np.ndarray, dtype: str) -> np.ndarray:
@@ -228,7 +229,7 @@ def verify_greedy_sequence(target: np.ndarray, drafts: np.ndarray, gamma: int) -
 
 def verify_sample_sequence(target: np.ndarray, draft: np.ndarray, drafts: np.ndarray,
                            gamma: int, T: float, u_accept: np.ndarray, u_sample: float,
-                           top_k: int = 0, top_p: float = 1.0) -> SequenceResult:
+                           top_k: int = 0, top_p: float = 1.0, nan_masked: bool = False) -> SequenceResult:
     """Sampling verification of one sequence ([TUT] §7.1-§7.3; [APP] Steps 3-4; [KB] §05-§06).
 
     For i = 0..gamma-1, left to right: p_i = softmax(P_i/T), q_i = softmax(Q_i/T),
@@ -236,9 +237,25 @@ def verify_sample_sequence(target: np.ndarray, draft: np.ndarray, drafts: np.nda
     m.  On a rejection the correction is drawn from max(p_m - q_m, 0)/R with u_sample; on
     full acceptance the bonus token is drawn from p_gamma with u_sample.  With top_k / top_p
     set, p and q are the truncated distributions (truncated_distribution) on both sides.
+    nan_masked: a NaN logit is read as -inf (an id that is never kept), the reading of the
+    truncated entry point, whose exact key search counts no NaN key.
     """
     V = target.shape[1]
     status = 0
+    if nan_masked:
+        target = np.where(np.isnan(target), -np.inf, target)
+        draft = np.where(np.isnan(draft), -np.inf, draft)
+    # A row whose maximum is not finite, or which holds a NaN (every logit -inf, a +inf or a
+    # NaN), has no softmax: exp(L/T - max L/T) is NaN or 0/0.  The sequence is marked
+    # ST_BAD_ROW when any row it reads (target rows 0..gamma, draft rows 0..gamma-1) is such
+    # a row; what follows is then not a defined result, and parity tests check the mark and
+    # that the step is well formed.
+    for row in list(target[: gamma + 1]) + list(draft[:gamma]):
+        if not np.isfinite(np.max(row)):
+            status |= ST_BAD_ROW
+    if status & ST_BAD_ROW:
+        nan = [math.nan] * gamma
+        return SequenceResult([0], 0, status, gamma, False, nan, list(nan), math.nan, [], math.inf)
     m = gamma
     p_d: List[float] = []
     q_d: List[float] = []
@@ -293,7 +310,7 @@ def verify_batch(target: np.ndarray, draft: Optional[np.ndarray], dtype: str,
                  draft_tokens: np.ndarray, num_draft: np.ndarray, temperature: Optional[np.ndarray],
                  u_accept: Optional[np.ndarray], u_sample: Optional[np.ndarray],
                  seqs=None, top_k: Optional[np.ndarray] = None,
-                 top_p: Optional[np.ndarray] = None) -> List[SequenceResult]:
+                 top_p: Optional[np.ndarray] = None, nan_masked: bool = False) -> List[SequenceResult]:
     """Verify every sequence (or the listed ones) of a batch.
 
     target [B, gmax+1, V], draft [B, gmax, V] (bf16 bits or float32); a sequence whose
@@ -316,7 +333,7 @@ def verify_batch(target: np.ndarray, draft: Optional[np.ndarray], dtype: str,
             Q = widen(draft[b, :g], dtype) if g > 0 else np.zeros((0, V))
             r = verify_sample_sequence(P, Q, draft_tokens[b], g, T, u_accept[b], float(u_sample[b]),
                                        0 if top_k is None else int(top_k[b]),
-                                       1.0 if top_p is None else float(top_p[b]))
+                                       1.0 if top_p is None else float(top_p[b]), nan_masked)
         r.status |= clamped
         out.append(r)
     return out

@@ -356,11 +356,12 @@ __device__ __forceinline__ void thread_stats(const Tile<E, kVec>& t, float k, fl
   run_m = mn;
 }
 
-// the warp's (max, sum) from its threads' running statistics; every lane gets the result
+// the warp's (max, sum) from its threads' running statistics; every lane gets the result.  A
+// part whose max is -inf holds no finite logit: its sum is 0, or NaN when it met a NaN logit,
+// and is carried as it is, so that a NaN anywhere in a row reaches the row's sum.
 __device__ __forceinline__ void warp_stats(float& m, float& s, float k) {
   const float M = warp_max(m);
-  float S = 0.f;
-  if (M != -INFINITY) S = warp_sum(m == -INFINITY ? 0.f : __fmul_rn(s, ex2(__fmul_rn(m - M, k))));
+  const float S = warp_sum(m == -INFINITY ? s : __fmul_rn(s, ex2(__fmul_rn(m - M, k))));
   m = M;
   s = S;
 }
@@ -926,15 +927,15 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
     const float2 p1 = lane + 32 < CL ? pp[lane + 32] : none;
     if (sq.sampling) {
       const float M = warp_max(fmaxf(p0.x, p1.x));
-      float S = 0.f;
-      if (M != -INFINITY) {
-        const float t0 = p0.x == -INFINITY ? 0.f : __fmul_rn(p0.y, ex2(__fmul_rn(p0.x - M, k)));
-        const float t1 = p1.x == -INFINITY ? 0.f : __fmul_rn(p1.y, ex2(__fmul_rn(p1.x - M, k)));
-        S = warp_sum(__fadd_rn(t0, t1));
-      }
+      // a chunk without a finite logit adds its sum as it is (0, or NaN: see warp_stats)
+      const float t0 = p0.x == -INFINITY ? p0.y : __fmul_rn(p0.y, ex2(__fmul_rn(p0.x - M, k)));
+      const float t1 = p1.x == -INFINITY ? p1.y : __fmul_rn(p1.y, ex2(__fmul_rn(p1.x - M, k)));
+      const float S = warp_sum(__fadd_rn(t0, t1));
       if (lane == 0) {
         sm.rowM[slot] = M;
         sm.rowInvS[slot] = __frcp_rn(S);
+        // no finite max, or a NaN in the row: it defines no distribution
+        if (!(isfinite(M) && isfinite(S))) atomicOr(&sm.flags_extra, SPEC_ST_BAD_ROW);
       }
     } else {
       float bv = p0.x;
@@ -1565,7 +1566,8 @@ template <bool kVec>
 __device__ unsigned long long trunc_total(const uint16_t* row, int64_t V, float k, float mk, TruncShared& ts) {
   // per thread in float, in a fixed order (so in fixed bits); in fixed point across threads
   float f = 0.f;
-  for_each_bf16<kVec>(row, V, [&](float x, uint32_t, int) { f = __fadd_rn(f, ex2(fmaf(x, k, -mk))); });
+  // a NaN logit adds nothing (fmaxf turns its NaN argument into -inf), as in the window passes
+  for_each_bf16<kVec>(row, V, [&](float x, uint32_t, int) { f = __fadd_rn(f, ex2(fmaxf(fmaf(x, k, -mk), -INFINITY))); });
   return block_sum_u64(__float2ull_rn(f * kMassUnit), ts);
 }
 
@@ -1656,7 +1658,7 @@ __device__ void trunc_search(TruncShared& ts, WindowFn window, Count count, Step
 
 // Per row: greedy rows get their argmax; sampling rows their max, threshold and kept mass.
 template <bool kVec>
-__global__ void __launch_bounds__(kThreads) trunc_rows_kernel(const Args a, const TruncArgs t, RowInfo* info,
+__global__ void __launch_bounds__(kThreads, kVec ? kMinBlocks : 1) trunc_rows_kernel(const Args a, const TruncArgs t, RowInfo* info,
                                                               int nslots) {
   __shared__ TruncShared ts;
   const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
@@ -1713,6 +1715,7 @@ __global__ void __launch_bounds__(kThreads) trunc_rows_kernel(const Args a, cons
   uint32_t kmin = 0;                       // smallest kept key (0: everything)
   unsigned long long kept = 0;             // mass of the keys >= kmin
   bool done = false;
+  bool bad = false;                        // no finite max: the row defines no distribution
   if (fused) {
     const Window win(top, kFusedWidth);
     const bool below = !dok;               // the whole row's mass is wanted
@@ -1732,7 +1735,9 @@ __global__ void __launch_bounds__(kThreads) trunc_rows_kernel(const Args a, cons
     __syncthreads();
     M = block_max_f32(fmaxf(__low2float(h), __high2float(h)), ts);
     const float mk = __fmul_rn(M, k);
-    if (key16(__float_as_uint(M) >> 16) <= top) {
+    if (!isfinite(M)) {
+      bad = done = true;
+    } else if (key16(__float_as_uint(M) >> 16) <= top) {
       // the window holds the max: its counts serve the search's first windows
       unsigned long long rest = 0, massb = 0;   // masses under both windows, of the second window
       if (below) {
@@ -1769,9 +1774,11 @@ __global__ void __launch_bounds__(kThreads) trunc_rows_kernel(const Args a, cons
       });
       M = block_max_f32(fmaxf(__low2float(h), __high2float(h)), ts);
     }
+    bad = !isfinite(M);
     const float mk = __fmul_rn(M, k);
     const uint32_t ktop = key16(__float_as_uint(M) >> 16);
-    if (!dok && !dop) {
+    if (bad) {
+    } else if (!dok && !dop) {
       kept = trunc_total<kVec>(row, V, k, mk, ts);
     } else {
       uint32_t nxt = 0;
@@ -1785,8 +1792,10 @@ __global__ void __launch_bounds__(kThreads) trunc_rows_kernel(const Args a, cons
   if (tid == 0) {
     RowInfo r;
     r.mk = mk;
-    r.invs = __frcp_rn(float(double(kept) / double(kMassUnit)));
-    r.tau = kmin == 0 ? -INFINITY : key16_value(kmin);
+    // a row without a distribution is marked by invs = 0 (otherwise invs is in (0, 1]) and
+    // keeps nothing
+    r.invs = bad ? 0.f : __frcp_rn(float(double(kept) / double(kMassUnit)));
+    r.tau = bad ? INFINITY : (kmin == 0 ? -INFINITY : key16_value(kmin));
     r.arg = 0;
     *out = r;
   }
@@ -1802,12 +1811,22 @@ __device__ PlanRec trunc_decide(const Args& a, const RowInfo* info, int nslots, 
   const RowInfo* ri = info + int64_t(b) * nslots;
   bool acc = false, valid = false;
   float p = NAN, q = NAN;
+  // the rows' records, loaded with the draft ids: lane i holds target row i and draft row i,
+  // lane g (lane 0 when g = 32) the bonus row's invs
+  RowInfo rp = {0.f, 1.f, 0.f, 0}, rq = {0.f, 1.f, 0.f, 0};
+  float binvs = 1.f;
+  if (sq.sampling) {
+    if (lane < g) {
+      rp = ri[lane];
+      rq = ri[gmax + 1 + lane];
+    }
+    if (lane == (g & 31)) binvs = ri[g].invs;
+  }
   if (lane < g) {
     const int d = __ldg(&a.draft_tokens[int64_t(b) * gmax + lane]);
     valid = d >= 0 && int64_t(d) < a.V;
     if (valid) {
       if (sq.sampling) {
-        const RowInfo rp = ri[lane], rq = ri[gmax + 1 + lane];
         const float xp = Bf16::at(target_row<Bf16>(a, b, lane), d);
         const float xq = Bf16::at(static_cast<const uint16_t*>(a.draft) + (int64_t(b) * gmax + lane) * a.V, d);
         p = xp >= rp.tau ? prob(xp, sq.k, rp.mk, rp.invs) : 0.f;
@@ -1825,6 +1844,8 @@ __device__ PlanRec trunc_decide(const Args& a, const RowInfo* info, int nslots, 
   const unsigned bad = __ballot_sync(kFull, lane < g && !valid);
   int flags = sq.flags;
   if (m < g && ((bad >> m) & 1u)) flags |= SPEC_ST_BAD_DRAFT;
+  // a row without a distribution (its record's invs is 0): target rows 0..g, draft rows 0..g-1
+  if (__any_sync(kFull, !(rp.invs > 0.f) || !(rq.invs > 0.f) || !(binvs > 0.f))) flags |= SPEC_ST_BAD_ROW;
   if (writer && a.diag) {   // gmax <= 32: lane i writes draft i's p'(d_i), q'(d_i)
     float* dg = a.diag + int64_t(b) * (2 * gmax + 1);
     if (lane < gmax) {
@@ -1875,7 +1896,7 @@ __device__ PlanRec trunc_decide(const Args& a, const RowInfo* info, int nslots, 
 // sequence's outputs), then the chunk's part of the draw; the last chunk to finish selects the
 // token and writes the outputs.
 template <bool kVec>
-__global__ void __launch_bounds__(kThreads) trunc_draw_kernel(const Args a, const Geo geo, const Work w,
+__global__ void __launch_bounds__(kThreads, kVec ? kMinBlocks : 1) trunc_draw_kernel(const Args a, const Geo geo, const Work w,
                                                               RowInfo* info, int nslots) {
   __shared__ Shared sm;
   const int64_t idx = int64_t(blockIdx.x);

@@ -19,7 +19,7 @@ SPEC_BF16 = 0
 SPEC_F32 = 1
 SPEC_MAX_GAMMA = 32
 ST_BAD_DRAFT, ST_R_ZERO, ST_CLAMPED_GAMMA, ST_HISTORY_FULL = 1, 2, 4, 8
-ST_TIMEOUT, ST_STOPPED = 16, 32
+ST_TIMEOUT, ST_STOPPED, ST_BAD_TREE, ST_BAD_ROW = 16, 32, 64, 128
 
 _lib = None
 

@@ -126,6 +126,17 @@ def compare(wl, gpu, results, seqs=None, check_probs=True):
         want = np.full(g_all + 1, -1)
         want[: len(r.tokens)] = r.tokens
         same = m == r.m and list(out) == list(want) and st == r.status
+        if r.status & O.ST_BAD_ROW:
+            # no distribution on one of the rows: the mark, and a well-formed step
+            flagged.append(b)
+            if not same:
+                differ.append(b)
+            assert st & O.ST_BAD_ROW, f"seq {b}: status gpu={st}, oracle marks a row without a distribution"
+            assert 0 <= m <= r.gamma and 0 <= out[m] < wl.V, (b, out, m)
+            assert list(out[:m]) == list(wl.draft_tokens[b, :m]), (b, out)
+            assert all(x == -1 for x in out[m + 1:]), (b, out)
+            continue
+        assert not st & O.ST_BAD_ROW, f"seq {b}: gpu marks a bad row the oracle does not see"
         if r.flagged(MARGIN_TOL):
             flagged.append(b)
             if not same:

@@ -38,7 +38,7 @@ def check(wl, top_k, top_p, max_differ=1):
     gpu = run_truncated(wl, top_k, top_p)
     res = O.verify_batch(wl.target, wl.draft, wl.dtype, wl.draft_tokens, wl.num_draft, wl.temperature,
                          wl.u_accept, wl.u_sample, top_k=None if top_k is None else np.asarray(top_k),
-                         top_p=None if top_p is None else np.asarray(top_p))
+                         top_p=None if top_p is None else np.asarray(top_p), nan_masked=True)
     n, flagged, differ = parity.compare(wl, gpu, res, check_probs=False)
     parity.record(wl.name, n, flagged, differ, entry="sample_truncated")
     assert len(differ) <= max_differ, (flagged, differ)
