@@ -99,6 +99,13 @@ def softmax_at_temperature(logits: np.ndarray, T: float) -> np.ndarray:
     return e / np.sum(e)
 
 
+def row_has_distribution(row: np.ndarray) -> bool:
+    """softmax(L/T) is defined on a row iff its max is finite and no logit is NaN: otherwise
+    exp(L/T - max L/T) is 0/0 (every logit -inf), NaN (a +inf) or NaN-poisoned (np.max returns
+    NaN when any logit is NaN)."""
+    return bool(np.isfinite(np.max(row)))
+
+
 def truncated_distribution(logits: np.ndarray, T: float, top_k: int = 0, top_p: float = 1.0):
     """p' = softmax(L/T) restricted to the ids top-k and then top-p keep, renormalised.
 
@@ -251,7 +258,7 @@ def verify_sample_sequence(target: np.ndarray, draft: np.ndarray, drafts: np.nda
     # a row; what follows is then not a defined result, and parity tests check the mark and
     # that the step is well formed.
     for row in list(target[: gamma + 1]) + list(draft[:gamma]):
-        if not np.isfinite(np.max(row)):
+        if not row_has_distribution(row):
             status |= ST_BAD_ROW
     if status & ST_BAD_ROW:
         nan = [math.nan] * gamma

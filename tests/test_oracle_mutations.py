@@ -145,6 +145,8 @@ MUTATIONS = {
     "inverse_cdf_margin_doubled": ("inverse_cdf", _icdf_margin_scaled(2.0)),
     "top_p_margin_halved": ("truncated_distribution", _top_p_margin_scaled(0.5)),
     "top_p_margin_doubled": ("truncated_distribution", _top_p_margin_scaled(2.0)),
+    "bad_row_nan_unseen": ("row_has_distribution", lambda row: bool(np.isfinite(np.nanmax(row)))),
+    "bad_row_all_neg_inf_unseen": ("row_has_distribution", lambda row: not np.isnan(np.max(row))),
 }
 
 
@@ -162,7 +164,8 @@ def _pins_pass():
               lambda: pins.check_accept_margin(cases=200, need_flips=40),
               lambda: pins.check_inverse_cdf_margin(cases=200, need_flips=60),
               lambda: pins.check_top_p_margin(cases=150, need_flips=40),
-              pins.check_flagged_uses_every_margin]
+              pins.check_flagged_uses_every_margin,
+              pins.check_rows_without_distribution, pins.check_truncated_entry_masks_nan]
     for c in checks:
         try:
             c()

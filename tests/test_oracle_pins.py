@@ -254,69 +254,10 @@ def test_flagged_uses_every_margin():
     pins.check_flagged_uses_every_margin()
 
 
+
 def test_rows_without_a_distribution_are_marked():
-    """A row the sampling step reads whose max is not finite, or which holds a NaN, defines no
-    softmax (exp(L/T - max L/T) is 0/0 or NaN): the sequence carries ST_BAD_ROW.  Rows it does
-    not read (past num_draft) and greedy sequences are not marked; ordinary rows never are."""
-    rng = np.random.default_rng(5)
-    V, g = 40, 3
-    base_t = rng.normal(0, 2, (g + 1, V))
-    base_q = base_t[:g] + rng.normal(0, 0.5, (g, V))
-    drafts = np.array([3, 7, 11])
-    u = np.array([0.3, 0.6, 0.9])
-
-    def status(t, q, gamma=g, T=1.0):
-        return O.verify_sample_sequence(t, q, drafts, gamma, T, u, 0.5).status
-
-    assert status(base_t, base_q) & O.ST_BAD_ROW == 0
-    for name, put in [("all -inf target", lambda t, q: t.__setitem__(1, -np.inf)),
-                      ("all -inf draft", lambda t, q: q.__setitem__(0, -np.inf)),
-                      ("all -inf bonus row", lambda t, q: t.__setitem__(g, -np.inf)),
-                      ("NaN logit", lambda t, q: t.__setitem__((2, 5), np.nan)),
-                      ("+inf logit", lambda t, q: q.__setitem__((1, 9), np.inf))]:
-        t, q = base_t.copy(), base_q.copy()
-        put(t, q)
-        st = status(t, q)
-        assert st & O.ST_BAD_ROW, name
-        # the same rows under truncation: marked, and the oracle does not fail on them
-        assert O.verify_sample_sequence(t, q, drafts, g, 1.0, u, 0.5, top_k=5, top_p=0.9).status & O.ST_BAD_ROW
-    # a row past num_draft is not read
-    t = base_t.copy()
-    t[3] = -np.inf
-    assert status(t, base_q, gamma=2) & O.ST_BAD_ROW == 0
-    # a greedy sequence's rows with -inf logits keep their argmax (lowest id on ties)
-    t = base_t.copy()
-    t[1] = -np.inf
-    r = O.verify_greedy_sequence(t, drafts, g)
-    assert r.status & O.ST_BAD_ROW == 0
-    # masked ids (some -inf, a finite max) are ordinary
-    t = base_t.copy()
-    t[:, ::2] = -np.inf
-    assert status(t, base_q) & O.ST_BAD_ROW == 0
+    pins.check_rows_without_distribution()
 
 
 def test_truncated_entry_masks_nan_logits():
-    """The truncated entry point's reading: a NaN logit is an id that is never kept, so a row
-    with a NaN and a finite max is ordinary there and its result equals that of the same row with
-    the NaN replaced by -inf; a row of NaN and -inf only has no finite max and is marked."""
-    rng = np.random.default_rng(6)
-    V, g = 30, 2
-    t = rng.normal(0, 2, (g + 1, V))
-    q = t[:g] + rng.normal(0, 0.5, (g, V))
-    drafts = np.array([4, 9])
-    u = np.array([0.2, 0.7])
-    tn = t.copy()
-    tn[1, 6] = np.nan
-    ti = t.copy()
-    ti[1, 6] = -np.inf
-    for k, p in [(0, 1.0), (5, 1.0), (0, 0.8), (6, 0.9)]:
-        a = O.verify_sample_sequence(tn, q, drafts, g, 1.0, u, 0.4, k, p, nan_masked=True)
-        b = O.verify_sample_sequence(ti, q, drafts, g, 1.0, u, 0.4, k, p)
-        assert a.status & O.ST_BAD_ROW == 0
-        assert (a.tokens, a.m, a.status) == (b.tokens, b.m, b.status)
-    # without the masking the NaN row has no distribution
-    assert O.verify_sample_sequence(tn, q, drafts, g, 1.0, u, 0.4).status & O.ST_BAD_ROW
-    qn = q.copy()
-    qn[0] = np.nan
-    qn[0, 2] = -np.inf
-    assert O.verify_sample_sequence(t, qn, drafts, g, 1.0, u, 0.4, 5, 0.9, nan_masked=True).status & O.ST_BAD_ROW
+    pins.check_truncated_entry_masks_nan()
