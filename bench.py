@@ -532,15 +532,17 @@ def run_native(args):
         verify = [sv.prepare_verify_greedy_commit(tgt[c], toks, nd, out, macc, kv, dkv, True, status=st,
                                                   workspace=ws, stream=stream) for c in range(ncopies)]
     elif trunc:
+        # truncated verification and the commit of the round: its two launches
         tk, tp = to_dev(wl.top_k), to_dev(wl.top_p)
-        verify = [sv.prepare_verify_sample_truncated(tgt[c], drf[c], toks, nd, temp, tk, tp, ua, us, out, macc, dg, st,
-                                                     workspace=ws, stream=stream) for c in range(ncopies)]
+        verify = [sv.prepare_verify_sample_truncated_commit(tgt[c], drf[c], toks, nd, temp, tk, tp, ua, us, out, macc,
+                                                            kv, dkv, True, diag=dg, status=st, workspace=ws,
+                                                            stream=stream) for c in range(ncopies)]
     else:
         verify = [sv.prepare_verify_sample_commit(tgt[c], drf[c], toks, nd, temp, ua, us, out, macc, kv, dkv, True,
                                                   diag=dg, status=st, workspace=ws, stream=stream)
                   for c in range(ncopies)]
-    # a separate commit launch only where no fused call exists (trees, truncated sampling)
-    fused = not (tree or trunc)
+    # a separate commit launch only where no fused call exists (trees)
+    fused = not tree
     commit = sv.prepare_commit_kv_lengths(macc, kv, dkv, True, stream=stream, gmax=g)
     step_commit = None if fused else commit
 
@@ -602,12 +604,12 @@ def run_native(args):
     value = aggregate_rate(world, rows_step, K, elapsed_ms)
     abytes = wl.algorithmic_bytes()
     peak, peak_src = measured_peak()
-    # The kernel's average launch duration.  Where a step is exactly one verify launch (the
-    # fused calls), the timed region holds nothing else: its length over the launches in it is
-    # that average, the gap to the next launch included.  Otherwise (a separate commit or stops
-    # launch in the step) the per-launch event pairs give it.  An event pair around a launch
-    # adds its own time, measured here on an empty pair.
-    one_launch_per_step = fused and launches == K
+    # The verify call's average duration.  Where a step is exactly one verify call and nothing
+    # else (the fused calls: one launch, or the truncated call's two), the timed region's length
+    # over K is that average, the gap to the next call included.  Otherwise (a separate commit
+    # launch in the step: trees) the per-launch event pairs give it.  An event pair around a
+    # launch adds its own time, measured here on an empty pair.
+    one_launch_per_step = fused and launches == K * (2 if trunc else 1)
     region_ms = elapsed_ms / K
     kern_avg_ms = region_ms if one_launch_per_step else kern_mean_ms
     achieved = abytes / (kern_avg_ms / 1e3) / 1e9
@@ -670,8 +672,9 @@ def run_native(args):
             sv.spec_verify_greedy_commit(d_in[0], d_in[1], d_in[2], out, macc, kv, None, True, status=st,
                                          workspace=ws)
         elif trunc:
-            sv.spec_verify_sample_truncated(d_in[0], d_in[1], d_in[2], d_in[3], d_in[4], tk, tp, d_in[5], d_in[6],
-                                            out, macc, dg, st, workspace=ws)
+            sv.spec_verify_sample_truncated_commit(d_in[0], d_in[1], d_in[2], d_in[3], d_in[4], tk, tp, d_in[5],
+                                                   d_in[6], out, macc, kv, None, True, diag=dg, status=st,
+                                                   workspace=ws)
         else:
             sv.spec_verify_sample_commit(d_in[0], d_in[1], d_in[2], d_in[3], d_in[4], d_in[5], d_in[6],
                                          out, macc, kv, None, True, diag=dg, status=st, workspace=ws)
@@ -721,13 +724,15 @@ def run_native(args):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": ("verify_kernel<bf16, vec, greedy> (spec_verify_tree_greedy)" if tree
-                                    else "trunc_rows + trunc_draw kernels (spec_verify_sample_truncated)"
+                                    else "trunc_rows + trunc_draw kernels with the commit (spec_verify_sample_truncated_commit)"
                                     if trunc
                                     else "verify_kernel<bf16, vec, greedy> with the commit (spec_verify_greedy_commit)"
                                     if wl.greedy_only
                                     else "verify_kernel<bf16, vec, mixed> with the commit (spec_verify_sample_commit)"),
                          "kernel_ms": kern_avg_ms,
                          "kernel_ms_source": ("timed region / launches: one verify launch per step, back to back"
+                                              if one_launch_per_step and not trunc
+                                              else "timed region / steps: one truncated call (two launches) per step"
                                               if one_launch_per_step else "mean of per-launch event pairs"),
                          "kernel_ms_mean": kern_mean_ms, "kernel_ms_median": kern_med_ms,
                          "kernel_ms_p10": kern_p10, "kernel_ms_p90": kern_p90, "kernel_ms_max": ks[-1],

@@ -322,6 +322,21 @@ int spec_verify_sample_commit(const void* target_logits, const void* draft_logit
                               int32_t* history, int32_t* committed_len, int cap, void* stream);
 
 /*
+ * spec_verify_sample_truncated followed by spec_commit_kv_lengths, fused in the same way: the
+ * thread that writes a sequence's outputs (the selector for a sampling sequence, the decision
+ * warp for a greedy one) commits it.  Same arguments as spec_verify_sample_truncated, then
+ * the commit's as for spec_verify_sample_commit; same outputs as the two separate calls.
+ */
+int spec_verify_sample_truncated_commit(const void* target_logits, const void* draft_logits, int dtype,
+                                        const int32_t* draft_tokens, const int32_t* num_draft,
+                                        const float* temperature, const int32_t* top_k, const float* top_p,
+                                        const float* u_accept, const float* u_sample, int B, int gmax, int V,
+                                        int32_t* out_tokens, int32_t* num_accepted, float* diag,
+                                        int32_t* status, void* workspace, size_t workspace_bytes,
+                                        int32_t* target_kv_len, int32_t* draft_kv_len, int correction_processed,
+                                        int32_t* history, int32_t* committed_len, int cap, void* stream);
+
+/*
  * Stops: cut each round's emit where step-by-step decoding would have stopped (tutorial
  * §5.2: nothing after an EOS in the candidate block may reach the cache; §12.3: EOS,
  * maximum length and the rejection position must agree with step-by-step decoding; card §03:

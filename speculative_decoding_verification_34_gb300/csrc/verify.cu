@@ -1857,15 +1857,20 @@ __device__ PlanRec trunc_decide(const Args& a, const RowInfo* info, int nslots, 
   PlanRec pr = {};
   if (!sq.sampling) {
     if (!writer) return pr;
+    // the round's commit, when the call carries one (lane 0), then the outputs and their
+    // history copies
+    int hist = -1, cf = 0;
+    if (lane == 0) cf = commit_apply(a, b, m, commit_load(a, b), &hist);
+    hist = __shfl_sync(kFull, hist, 0);
     for (int i = lane; i <= gmax; i += 32) {
       int v = -1;
       if (i < m) v = a.draft_tokens[int64_t(b) * gmax + i];
       else if (i == m) v = ri[m].arg;
-      a.out_tokens[int64_t(b) * (gmax + 1) + i] = v;
+      put_output(a, b, i, m, v, hist);
     }
     if (lane == 0) {
       a.num_accepted[b] = m;
-      if (a.status) a.status[b] = flags;
+      if (a.status) a.status[b] = flags | cf;
     }
     return pr;
   }
@@ -2363,7 +2368,7 @@ int verify_truncated(const void* saved, const void* target, const void* draft_lo
                      const int32_t* draft_tokens, const int32_t* num_draft, const float* temperature,
                      const int32_t* top_k, const float* top_p, const float* u_accept, const float* u_sample, int B,
                      int gmax, int V, int32_t* out_tokens, int32_t* num_accepted, float* diag, int32_t* status,
-                     void* workspace, size_t workspace_bytes, void* stream) {
+                     void* workspace, size_t workspace_bytes, void* stream, const CommitArgs* ck = nullptr) {
   if (dtype != SPEC_BF16) {
     set_error("truncated sampling takes bf16 logits");
     return SPEC_EDTYPE;
@@ -2378,6 +2383,7 @@ int verify_truncated(const void* saved, const void* target, const void* draft_lo
     return SPEC_EINVAL;
   }
   Args a = {};
+  set_commit(a, ck);
   a.saved = saved;
   a.target = target;
   a.draft = draft_logits;
@@ -2414,6 +2420,24 @@ extern "C" int spec_verify_sample_truncated(const void* target_logits, const voi
   return verify_truncated(nullptr, target_logits, draft_logits, dtype, draft_tokens, num_draft, temperature, top_k,
                           top_p, u_accept, u_sample, B, gmax, V, out_tokens, num_accepted, diag, status, workspace,
                           workspace_bytes, stream);
+}
+
+extern "C" int spec_verify_sample_truncated_commit(
+    const void* target_logits, const void* draft_logits, int dtype, const int32_t* draft_tokens,
+    const int32_t* num_draft, const float* temperature, const int32_t* top_k, const float* top_p,
+    const float* u_accept, const float* u_sample, int B, int gmax, int V, int32_t* out_tokens, int32_t* num_accepted,
+    float* diag, int32_t* status, void* workspace, size_t workspace_bytes, int32_t* target_kv_len,
+    int32_t* draft_kv_len, int correction_processed, int32_t* history, int32_t* committed_len, int cap,
+    void* stream) {
+  clear_error();
+  int rc = check_common(target_logits, dtype, draft_tokens, B, gmax, V, out_tokens, num_accepted);
+  if (rc != SPEC_OK || B == 0) return rc;
+  const CommitArgs ck = {target_kv_len, draft_kv_len, correction_processed, history, committed_len, cap};
+  rc = check_commit(ck);
+  if (rc != SPEC_OK) return rc;
+  return verify_truncated(nullptr, target_logits, draft_logits, dtype, draft_tokens, num_draft, temperature, top_k,
+                          top_p, u_accept, u_sample, B, gmax, V, out_tokens, num_accepted, diag, status, workspace,
+                          workspace_bytes, stream, &ck);
 }
 
 extern "C" int spec_verify_sample_truncated_split(const void* saved_logits, const void* block_logits,

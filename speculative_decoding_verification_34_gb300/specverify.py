@@ -68,6 +68,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.spec_verify_sample_commit.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, sz, sz, sz, vp, vp, vp, vp, vp,
                                               size_t, vp, vp, i32, vp, vp, sz, vp]
     lib.spec_verify_sample_commit.restype = i32
+    lib.spec_verify_sample_truncated_commit.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, sz, sz, vp, vp,
+                                                        vp, vp, vp, size_t, vp, vp, i32, vp, vp, sz, vp]
+    lib.spec_verify_sample_truncated_commit.restype = i32
     lib.spec_verify_sample_static.restype = i32
     lib.spec_verify_workspace_bytes.argtypes = [sz, sz, sz, i32]
     lib.spec_verify_workspace_bytes.restype = size_t
@@ -286,6 +289,51 @@ def spec_verify_sample_truncated(target_logits: torch.Tensor, draft_logits: torc
         _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
         _ptr(diag, "diag", torch.float32, (B, 2 * gmax + 1)),
         _ptr(status, "status", torch.int32, (B,)), wsp, wsn, _stream(stream)))
+
+
+def _truncated_commit_args(target_logits, draft_logits, draft_tokens, num_draft, temperature, top_k, top_p,
+                           u_accept, u_sample, out_tokens, num_accepted, diag, status, workspace, target_kv_len,
+                           draft_kv_len, correction_processed, history, committed_len, stream):
+    B, gp1, V = target_logits.shape
+    gmax = gp1 - 1
+    if draft_logits.dtype != target_logits.dtype:
+        raise TypeError("target and draft logits must have the same dtype")
+    code = _dtype_code(target_logits)
+    ws, wsp, wsn = _ws(workspace, B, gmax, V, code, target_logits.device)
+    args = (_ptr(target_logits, "target_logits"),
+            _ptr(draft_logits, "draft_logits", None, (B, gmax, V)), code,
+            _ptr(draft_tokens, "draft_tokens", torch.int32, (B, gmax)),
+            _ptr(num_draft, "num_draft", torch.int32, (B,)),
+            _ptr(temperature, "temperature", torch.float32, (B,)),
+            _ptr(top_k, "top_k", torch.int32, (B,)), _ptr(top_p, "top_p", torch.float32, (B,)),
+            _ptr(u_accept, "u_accept", torch.float32, (B, gmax)),
+            _ptr(u_sample, "u_sample", torch.float32, (B,)), B, gmax, V,
+            _ptr(out_tokens, "out_tokens", torch.int32, (B, gmax + 1)),
+            _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
+            _ptr(diag, "diag", torch.float32, (B, 2 * gmax + 1)),
+            _ptr(status, "status", torch.int32, (B,)), wsp, wsn,
+            *_commit_args(B, target_kv_len, draft_kv_len, correction_processed, history, committed_len),
+            _stream(stream))
+    return args, ws
+
+
+def spec_verify_sample_truncated_commit(target_logits: torch.Tensor, draft_logits: torch.Tensor,
+                                        draft_tokens: torch.Tensor, num_draft: Optional[torch.Tensor],
+                                        temperature: torch.Tensor, top_k: Optional[torch.Tensor],
+                                        top_p: Optional[torch.Tensor], u_accept: torch.Tensor,
+                                        u_sample: torch.Tensor, out_tokens: torch.Tensor,
+                                        num_accepted: torch.Tensor, target_kv_len: torch.Tensor,
+                                        draft_kv_len: Optional[torch.Tensor] = None,
+                                        correction_processed: bool = True, history: Optional[torch.Tensor] = None,
+                                        committed_len: Optional[torch.Tensor] = None,
+                                        diag: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                                        workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """spec_verify_sample_truncated and spec_commit_kv_lengths of the same round, fused."""
+    args, _ = _truncated_commit_args(target_logits, draft_logits, draft_tokens, num_draft, temperature, top_k,
+                                     top_p, u_accept, u_sample, out_tokens, num_accepted, diag, status, workspace,
+                                     target_kv_len, draft_kv_len, correction_processed, history, committed_len,
+                                     stream)
+    _check(load_library().spec_verify_sample_truncated_commit(*args))
 
 
 def spec_verify_sample_truncated_split(saved_logits: torch.Tensor, block_logits: Optional[torch.Tensor],
@@ -593,6 +641,20 @@ def prepare_verify_sample_truncated(target_logits, draft_logits, draft_tokens, n
     keep = (target_logits, draft_logits, draft_tokens, num_draft, temperature, top_k, top_p, u_accept,
             u_sample, out_tokens, num_accepted, diag, status, ws)
     return _Prepared(lib.spec_verify_sample_truncated, args, keep)
+
+
+def prepare_verify_sample_truncated_commit(target_logits, draft_logits, draft_tokens, num_draft, temperature,
+                                           top_k, top_p, u_accept, u_sample, out_tokens, num_accepted,
+                                           target_kv_len, draft_kv_len=None, correction_processed=True,
+                                           history=None, committed_len=None, diag=None, status=None,
+                                           workspace=None, stream=None) -> _Prepared:
+    args, ws = _truncated_commit_args(target_logits, draft_logits, draft_tokens, num_draft, temperature, top_k,
+                                      top_p, u_accept, u_sample, out_tokens, num_accepted, diag, status, workspace,
+                                      target_kv_len, draft_kv_len, correction_processed, history, committed_len,
+                                      stream)
+    keep = (target_logits, draft_logits, draft_tokens, num_draft, temperature, top_k, top_p, u_accept, u_sample,
+            out_tokens, num_accepted, diag, status, ws, target_kv_len, draft_kv_len, history, committed_len)
+    return _Prepared(load_library().spec_verify_sample_truncated_commit, args, keep)
 
 
 def prepare_verify_greedy(target_logits, draft_tokens, num_draft, out_tokens, num_accepted,

@@ -178,6 +178,7 @@ def test_binding_arity_matches_header(lib):
                  "spec_apply_stops", "spec_verify_greedy_split", "spec_verify_sample_split",
                  "spec_verify_tree_greedy", "spec_verify_sample_truncated",
                  "spec_verify_sample_truncated_split", "spec_verify_greedy_commit",
+                 "spec_verify_sample_truncated_commit",
                  "spec_verify_sample_commit"):
         m = re.search(r"\b" + name + r"\s*\(([^)]*)\)", text)
         params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
@@ -214,6 +215,13 @@ def test_fused_commit_argument_checks(lib):
         t, None, 1, h, c, cap, None)
     assert s(t=None) == 1 and s(h=FAKE) == 1
     assert s(t=None, B=0) == 0          # empty batch: nothing to check, nothing enqueued
+    tr = lambda t=FAKE, h=None, c=None, cap=0, B=4, dtype=0: lib.spec_verify_sample_truncated_commit(
+        FAKE, FAKE, dtype, FAKE, None, FAKE, None, None, FAKE, FAKE, B, 3, 100, FAKE, FAKE, None, None, FAKE, 8,
+        t, None, 1, h, c, cap, None)
+    assert tr(t=None) == 1 and tr(h=FAKE) == 1 and tr(h=FAKE, c=FAKE, cap=0) == 1
+    assert tr(t=None, B=0) == 0
+    assert tr(dtype=1) == 2 and b"bf16" in lib.spec_last_error()
     # valid commit arguments reach the workspace check (8 bytes: refused) and stop there
     assert g() == 3 and s() == 3 and b"workspace" in lib.spec_last_error()
+    assert tr() == 3 and b"workspace" in lib.spec_last_error()
     assert lib.spec_launch_count() == n0

@@ -35,7 +35,7 @@ def _host(*ts):
     return [t.cpu().numpy() for t in ts]
 
 
-@pytest.mark.parametrize("name", ["sampling", "mixed", "greedy"])
+@pytest.mark.parametrize("name", ["sampling", "mixed", "greedy", "truncated"])
 def test_fused_commit_equals_separate_calls(name):
     if name == "sampling":
         wl = W.sampling_workload("fused-s", cfg=61, seed=0, B=96, gmax=4, V=128256, dtype="bf16",
@@ -44,8 +44,15 @@ def test_fused_commit_equals_separate_calls(name):
         wl = W.sampling_workload("fused-m", cfg=62, seed=0, B=64, gmax=6, V=50000, dtype="f32",
                                  target_sigma=3.0, draft_scale=1.0, draft_sigma=1.5, temperature=0.7,
                                  num_draft=np.arange(64) % 7, greedy_mask=(np.arange(64) % 2) == 0)
+    elif name == "truncated":
+        wl = W.sampling_workload("fused-t", cfg=64, seed=0, B=48, gmax=4, V=40000, dtype="bf16",
+                                 target_sigma=3.0, draft_scale=0.8, draft_sigma=1.0, temperature=0.9,
+                                 num_draft=np.arange(48) % 5, greedy_mask=(np.arange(48) % 6) == 0)
     else:
         wl = W.greedy_planted_workload("fused-g", cfg=63, seed=0, B=64, gmax=5, V=32000, alpha=0.8)
+    trunc = name == "truncated"
+    tk = dev(np.where(np.arange(wl.B) % 3 == 0, 0, 40).astype(np.int32))
+    tp = dev(np.where(np.arange(wl.B) % 4 == 1, 1.0, 0.85).astype(np.float32))
     cap = 12
     code = sv.SPEC_BF16 if wl.dtype == "bf16" else sv.SPEC_F32
     ws = torch.zeros(sv.spec_verify_workspace_bytes(wl.B, wl.gmax, wl.V, code), dtype=torch.uint8, device="cuda")
@@ -65,7 +72,15 @@ def test_fused_commit_equals_separate_calls(name):
             else:
                 args = (tgt, dev(wl.draft), toks, nd, dev(wl.temperature), dev(wl.u_accept), dev(wl.u_sample),
                         out, m)
-                if fused:
+                targs = (tgt, dev(wl.draft), toks, nd, dev(wl.temperature), tk, tp, dev(wl.u_accept),
+                         dev(wl.u_sample), out, m)
+                if trunc and fused:
+                    sv.spec_verify_sample_truncated_commit(*targs, st["t"], st["d"], proc, st["h"], st["c"],
+                                                           diag=dg, status=status, workspace=ws)
+                elif trunc:
+                    sv.spec_verify_sample_truncated(*targs, diag=dg, status=status, workspace=ws)
+                    sv.spec_commit_kv_lengths(m, st["t"], st["d"], proc, out, st["h"], st["c"], status)
+                elif fused:
                     sv.spec_verify_sample_commit(*args, st["t"], st["d"], proc, st["h"], st["c"], diag=dg,
                                                  status=status, workspace=ws)
                 else:
