@@ -288,3 +288,38 @@ def test_workspace_reuse_across_sizes():
         res = parity.oracle_results(wl)
         _, _, differ = parity.compare(wl, gpu, res)
         assert len(differ) <= 1
+
+
+def test_batch_spanning_several_launches():
+    """A batch larger than one grid runs as several launches over consecutive sequence ranges
+    (at V = 64, gamma = 2: about 49,000 sampling sequences per launch on a 152-SM GPU, 65,535
+    greedy ones).  Every sequence's step is well formed; the sequences at both ends of every
+    launch and a sample elsewhere equal the oracle; the workspace returns to zero."""
+    B = 70000
+    wl = W.sampling_workload("multi-launch", cfg=91, seed=0, B=B, gmax=2, V=64, dtype="bf16",
+                             target_sigma=2.0, draft_scale=1.0, draft_sigma=0.7, temperature=1.0,
+                             greedy_mask=(np.arange(B) % 11) == 0)
+    n0 = sv.spec_launch_count()
+    gpu = parity.run_gpu(wl)
+    assert sv.spec_launch_count() - n0 >= 2      # the batch did not fit one grid
+    out, m = gpu["out"], gpu["m"]
+    assert ((m >= 0) & (m <= 2)).all()
+    for b in range(0, B, 997):
+        assert list(out[b, :m[b]]) == list(wl.draft_tokens[b, :m[b]]) and 0 <= out[b, m[b]] < wl.V
+    rng = np.random.default_rng(0)
+    seqs = set(range(0, 40)) | set(range(48960, 49040)) | set(range(B - 40, B))
+    seqs |= set(int(x) for x in rng.choice(B, 1200, replace=False))
+    seqs = sorted(seqs)
+    n, flagged, differ = parity.compare(wl, gpu, parity.oracle_results(wl, seqs), seqs)
+    parity.record(wl.name, n, flagged, differ, entry="sample")
+    assert len(differ) <= max(1, n // 100), differ
+    # the greedy-only kernel: 65,535 sequences per launch
+    g = W.greedy_planted_workload("multi-launch-g", cfg=92, seed=0, B=B, gmax=2, V=64, alpha=0.8)
+    n0 = sv.spec_launch_count()
+    gg = parity.run_gpu(g, mode="greedy")
+    assert sv.spec_launch_count() - n0 >= 2
+    seqs = sorted(set(range(0, 40)) | set(range(65500, 65570)) | set(range(B - 40, B)) |
+                  set(int(x) for x in rng.choice(B, 1200, replace=False)))
+    n, flagged, differ = parity.compare(g, gg, parity.oracle_results(g, seqs, mode="greedy"), seqs)
+    parity.record(g.name, n, flagged, differ, entry="greedy")
+    assert not differ
