@@ -40,8 +40,9 @@
  *  - Data-dependent problems never fault or trap the GPU: they set bits in the optional
  *    per-sequence status[B] word (see SPEC_ST_*) and a defined fallback is taken.
  *  - Limits: 0 <= B, 0 <= gmax <= SPEC_MAX_GAMMA, 1 <= V <= 2^21 (bf16) or 2^20 (fp32);
- *    a larger V, or a batch needing more than 2^31-1 thread blocks, returns SPEC_ENOSPACE.  B == 0 is a no-op that enqueues nothing and accepts
- *    null pointers (empty tensors have none).
+ *    a larger V, or a batch needing more than 2^31-1 thread blocks, returns SPEC_ENOSPACE.
+ *    B == 0 is a no-op that enqueues nothing and accepts null pointers (empty tensors have
+ *    none).
  */
 #ifndef SPECVERIFY_H
 #define SPECVERIFY_H
