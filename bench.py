@@ -525,8 +525,10 @@ def run_native(args):
     stream = torch.cuda.current_stream(device)
     ws = sv.alloc_workspace(B, g, V, sv.SPEC_BF16 if wl.dtype == "bf16" else sv.SPEC_F32, device)
     if tree:
-        verify = [sv.prepare_verify_tree_greedy(tgt[c], toks, pars, nd, out, macc, path, st, workspace=ws,
-                                                stream=stream) for c in range(ncopies)]
+        # tree verification and the commit of the round in one launch
+        verify = [sv.prepare_verify_tree_greedy_commit(tgt[c], toks, pars, nd, out, macc, kv, dkv, True,
+                                                       path_nodes=path, status=st, workspace=ws, stream=stream)
+                  for c in range(ncopies)]
     elif wl.greedy_only:
         # verification and the commit of the round in one launch
         verify = [sv.prepare_verify_greedy_commit(tgt[c], toks, nd, out, macc, kv, dkv, True, status=st,
@@ -541,8 +543,9 @@ def run_native(args):
         verify = [sv.prepare_verify_sample_commit(tgt[c], drf[c], toks, nd, temp, ua, us, out, macc, kv, dkv, True,
                                                   diag=dg, status=st, workspace=ws, stream=stream)
                   for c in range(ncopies)]
-    # a separate commit launch only where no fused call exists (trees)
-    fused = not tree
+    # every path has a fused call: a step is one verify call (a separate commit launch would
+    # only be timed where none existed)
+    fused = True
     commit = sv.prepare_commit_kv_lengths(macc, kv, dkv, True, stream=stream, gmax=g)
     step_commit = None if fused else commit
 
@@ -667,7 +670,8 @@ def run_native(args):
         for h, d in zip(h_in, d_in):
             d.copy_(h, non_blocking=True)
         if tree:
-            sv.spec_verify_tree_greedy(d_in[0], d_in[1], d_in[2], d_in[3], out, macc, path, st, workspace=ws)
+            sv.spec_verify_tree_greedy_commit(d_in[0], d_in[1], d_in[2], d_in[3], out, macc, kv, None, True,
+                                              path_nodes=path, status=st, workspace=ws)
         elif wl.greedy_only:
             sv.spec_verify_greedy_commit(d_in[0], d_in[1], d_in[2], out, macc, kv, None, True, status=st,
                                          workspace=ws)
@@ -723,7 +727,7 @@ def run_native(args):
             "sequences_per_s": world * B * K / (elapsed_ms / 1e3), "mean_emitted_per_sequence": mean_emit,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": ("verify_kernel<bf16, vec, greedy> (spec_verify_tree_greedy)" if tree
+                         "kernel": ("verify_kernel<bf16, vec, greedy> with the commit (spec_verify_tree_greedy_commit)" if tree
                                     else "trunc_rows + trunc_draw kernels with the commit (spec_verify_sample_truncated_commit)"
                                     if trunc
                                     else "verify_kernel<bf16, vec, greedy> with the commit (spec_verify_greedy_commit)"

@@ -206,6 +206,20 @@ int spec_verify_tree_greedy(const void* target_logits, int dtype, const int32_t*
                             int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * spec_verify_tree_greedy followed by spec_commit_kv_lengths (gmax = nmax), fused: the thread
+ * that writes a tree's outputs advances its lengths by the accepted path's m (+1) and appends the
+ * path's tokens to the history.  The cache entries of the nodes off the path are the caller's to
+ * drop (path_nodes lists the kept ones; card §06: trimming a length alone does not repair a
+ * tree's cache).  Commit arguments and return values as for spec_verify_sample_commit.
+ */
+int spec_verify_tree_greedy_commit(const void* target_logits, int dtype, const int32_t* node_tokens,
+                                   const int32_t* node_parents, const int32_t* num_nodes, int B, int nmax, int V,
+                                   int32_t* out_tokens, int32_t* num_accepted, int32_t* path_nodes,
+                                   int32_t* status, void* workspace, size_t workspace_bytes,
+                                   int32_t* target_kv_len, int32_t* draft_kv_len, int correction_processed,
+                                   int32_t* history, int32_t* committed_len, int cap, void* stream);
+
+/*
  * Both verify calls on the split layout of the target's logits, for engines that keep the
  * prediction saved from the last round apart from the logits of the new block, so that they
  * need not copy the two into one array first.  In the alignment table of the tutorial's §4,

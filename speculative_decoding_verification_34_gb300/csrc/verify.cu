@@ -892,8 +892,8 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
       vxq = ld_relaxed_u64(xdq);
     }
   }
-  // a greedy sequence is committed here: its lengths are loaded with the rest
-  const CommitIn cin = (tid == 0 && !sq.sampling && !a.parents) ? commit_load(a, b) : CommitIn{0, 0, 0};
+  // a greedy sequence (or tree) is committed here: its lengths are loaded with the rest
+  const CommitIn cin = (tid == 0 && !sq.sampling) ? commit_load(a, b) : CommitIn{0, 0, 0};
   // The row partials, a batch of rows at a time: every word of the batch is loaded at once (a
   // thread per word) and staged in shared memory, then one warp per row combines them, lanes
   // taking chunks c and c + 32 (at most 64 chunks).
@@ -1004,19 +1004,25 @@ __device__ void decide(const Args& a, const Geo& geo, const Work& w, const Seq<E
     }
     __syncthreads();
     const int m = sm.m;
+    if (tid == 0) {
+      // the round's commit when the call carries one: the lengths advance by the path's m
+      // (+1), the path's tokens are appended (the caller compacts its cache by path_nodes)
+      int hist;
+      const int cf = commit_apply(a, b, m, cin, &hist);
+      sm.hist = hist;
+      a.num_accepted[b] = m;
+      if (a.status) a.status[b] = sm.flags | cf;
+      w.cnt[b] = 0;
+    }
+    __syncthreads();
     for (int i = tid; i <= gmax; i += kThreads) {
       int v = -1;
       if (i < m) v = sm.ttok[sm.tpath[i]];
       else if (i == m) v = sm.rowArg[sm.tbest];
-      a.out_tokens[int64_t(b) * (gmax + 1) + i] = v;
+      put_output(a, b, i, m, v, sm.hist);
     }
     if (a.path_nodes)
       for (int i = tid; i < gmax; i += kThreads) a.path_nodes[int64_t(b) * gmax + i] = i < m ? sm.tpath[i] : -1;
-    if (tid == 0) {
-      a.num_accepted[b] = m;
-      if (a.status) a.status[b] = sm.flags;
-      w.cnt[b] = 0;
-    }
     __syncthreads();
     return;
   }
@@ -2456,11 +2462,12 @@ extern "C" int spec_verify_sample_truncated_split(const void* saved_logits, cons
                           workspace, workspace_bytes, stream);
 }
 
-extern "C" int spec_verify_tree_greedy(const void* target_logits, int dtype, const int32_t* node_tokens,
-                                       const int32_t* node_parents, const int32_t* num_nodes, int B, int nmax,
-                                       int V, int32_t* out_tokens, int32_t* num_accepted, int32_t* path_nodes,
-                                       int32_t* status, void* workspace, size_t workspace_bytes, void* stream) {
-  clear_error();
+namespace specverify {
+namespace {
+int verify_tree(const void* target_logits, int dtype, const int32_t* node_tokens, const int32_t* node_parents,
+                const int32_t* num_nodes, int B, int nmax, int V, int32_t* out_tokens, int32_t* num_accepted,
+                int32_t* path_nodes, int32_t* status, void* workspace, size_t workspace_bytes, void* stream,
+                const CommitArgs* ck) {
   if (dtype != SPEC_BF16 && dtype != SPEC_F32) {
     set_error("unknown dtype code %d", dtype);
     return SPEC_EDTYPE;
@@ -2478,7 +2485,12 @@ extern "C" int spec_verify_tree_greedy(const void* target_logits, int dtype, con
     set_error("null required pointer");
     return SPEC_EINVAL;
   }
+  if (ck) {
+    const int rc = check_commit(*ck);
+    if (rc != SPEC_OK) return rc;
+  }
   Args a = {};
+  set_commit(a, ck);
   a.target = target_logits;
   a.draft_tokens = node_tokens;
   a.parents = node_parents;
@@ -2491,6 +2503,30 @@ extern "C" int spec_verify_tree_greedy(const void* target_logits, int dtype, con
   a.num_accepted = num_accepted;
   a.status = status;
   return dispatch_on<false>(a, dtype, workspace, workspace_bytes, stream);
+}
+}  // namespace
+}  // namespace specverify
+
+extern "C" int spec_verify_tree_greedy(const void* target_logits, int dtype, const int32_t* node_tokens,
+                                       const int32_t* node_parents, const int32_t* num_nodes, int B, int nmax,
+                                       int V, int32_t* out_tokens, int32_t* num_accepted, int32_t* path_nodes,
+                                       int32_t* status, void* workspace, size_t workspace_bytes, void* stream) {
+  clear_error();
+  return verify_tree(target_logits, dtype, node_tokens, node_parents, num_nodes, B, nmax, V, out_tokens,
+                     num_accepted, path_nodes, status, workspace, workspace_bytes, stream, nullptr);
+}
+
+extern "C" int spec_verify_tree_greedy_commit(const void* target_logits, int dtype, const int32_t* node_tokens,
+                                              const int32_t* node_parents, const int32_t* num_nodes, int B,
+                                              int nmax, int V, int32_t* out_tokens, int32_t* num_accepted,
+                                              int32_t* path_nodes, int32_t* status, void* workspace,
+                                              size_t workspace_bytes, int32_t* target_kv_len, int32_t* draft_kv_len,
+                                              int correction_processed, int32_t* history, int32_t* committed_len,
+                                              int cap, void* stream) {
+  clear_error();
+  const CommitArgs ck = {target_kv_len, draft_kv_len, correction_processed, history, committed_len, cap};
+  return verify_tree(target_logits, dtype, node_tokens, node_parents, num_nodes, B, nmax, V, out_tokens,
+                     num_accepted, path_nodes, status, workspace, workspace_bytes, stream, &ck);
 }
 
 // ------------------------------------------------------------------------------------------

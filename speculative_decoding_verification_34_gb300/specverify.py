@@ -61,6 +61,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                                                        vp, vp, vp, vp, size_t, vp]
     lib.spec_verify_sample_truncated_split.restype = i32
     lib.spec_verify_tree_greedy.restype = i32
+    lib.spec_verify_tree_greedy_commit.argtypes = [vp, i32, vp, vp, vp, sz, sz, sz, vp, vp, vp, vp, vp, size_t,
+                                                   vp, vp, i32, vp, vp, sz, vp]
+    lib.spec_verify_tree_greedy_commit.restype = i32
     lib.spec_verify_sample_static.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, sz, sz, sz, vp, vp, vp, vp, vp]
     lib.spec_verify_greedy_commit.argtypes = [vp, i32, vp, vp, sz, sz, sz, vp, vp, vp, vp, size_t,
                                               vp, vp, i32, vp, vp, sz, vp]
@@ -388,6 +391,53 @@ def spec_verify_tree_greedy(target_logits: torch.Tensor, node_tokens: torch.Tens
         _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
         _ptr(path_nodes, "path_nodes", torch.int32, (B, nmax)),
         _ptr(status, "status", torch.int32, (B,)), wsp, wsn, _stream(stream)))
+
+
+def _tree_args(target_logits, node_tokens, node_parents, num_nodes, out_tokens, num_accepted, path_nodes, status,
+               workspace):
+    B, np1, V = target_logits.shape
+    nmax = np1 - 1
+    ws, wsp, wsn = _ws(workspace, B, nmax, V, _dtype_code(target_logits), target_logits.device)
+    args = (_ptr(target_logits, "target_logits"), _dtype_code(target_logits),
+            _ptr(node_tokens, "node_tokens", torch.int32, (B, nmax)),
+            _ptr(node_parents, "node_parents", torch.int32, (B, nmax)),
+            _ptr(num_nodes, "num_nodes", torch.int32, (B,)), B, nmax, V,
+            _ptr(out_tokens, "out_tokens", torch.int32, (B, nmax + 1)),
+            _ptr(num_accepted, "num_accepted", torch.int32, (B,)),
+            _ptr(path_nodes, "path_nodes", torch.int32, (B, nmax)),
+            _ptr(status, "status", torch.int32, (B,)), wsp, wsn)
+    return args, ws
+
+
+def spec_verify_tree_greedy_commit(target_logits: torch.Tensor, node_tokens: torch.Tensor,
+                                   node_parents: torch.Tensor, num_nodes: Optional[torch.Tensor],
+                                   out_tokens: torch.Tensor, num_accepted: torch.Tensor, target_kv_len: torch.Tensor,
+                                   draft_kv_len: Optional[torch.Tensor] = None, correction_processed: bool = True,
+                                   history: Optional[torch.Tensor] = None,
+                                   committed_len: Optional[torch.Tensor] = None,
+                                   path_nodes: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                                   workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """spec_verify_tree_greedy and spec_commit_kv_lengths (gmax = nmax) of the same round, fused."""
+    B = target_logits.shape[0]
+    args, _ = _tree_args(target_logits, node_tokens, node_parents, num_nodes, out_tokens, num_accepted, path_nodes,
+                         status, workspace)
+    _check(load_library().spec_verify_tree_greedy_commit(
+        *args, *_commit_args(B, target_kv_len, draft_kv_len, correction_processed, history, committed_len),
+        _stream(stream)))
+
+
+def prepare_verify_tree_greedy_commit(target_logits, node_tokens, node_parents, num_nodes, out_tokens, num_accepted,
+                                      target_kv_len, draft_kv_len=None, correction_processed=True, history=None,
+                                      committed_len=None, path_nodes=None, status=None, workspace=None,
+                                      stream=None) -> "_Prepared":
+    B = target_logits.shape[0]
+    args, ws = _tree_args(target_logits, node_tokens, node_parents, num_nodes, out_tokens, num_accepted, path_nodes,
+                          status, workspace)
+    args = args + _commit_args(B, target_kv_len, draft_kv_len, correction_processed, history, committed_len) + \
+        (_stream(stream),)
+    keep = (target_logits, node_tokens, node_parents, num_nodes, out_tokens, num_accepted, path_nodes, status, ws,
+            target_kv_len, draft_kv_len, history, committed_len)
+    return _Prepared(load_library().spec_verify_tree_greedy_commit, args, keep)
 
 
 def prepare_verify_tree_greedy(target_logits, node_tokens, node_parents, num_nodes, out_tokens, num_accepted,

@@ -178,7 +178,7 @@ def test_binding_arity_matches_header(lib):
                  "spec_apply_stops", "spec_verify_greedy_split", "spec_verify_sample_split",
                  "spec_verify_tree_greedy", "spec_verify_sample_truncated",
                  "spec_verify_sample_truncated_split", "spec_verify_greedy_commit",
-                 "spec_verify_sample_truncated_commit",
+                 "spec_verify_sample_truncated_commit", "spec_verify_tree_greedy_commit",
                  "spec_verify_sample_commit"):
         m = re.search(r"\b" + name + r"\s*\(([^)]*)\)", text)
         params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
@@ -221,7 +221,12 @@ def test_fused_commit_argument_checks(lib):
     assert tr(t=None) == 1 and tr(h=FAKE) == 1 and tr(h=FAKE, c=FAKE, cap=0) == 1
     assert tr(t=None, B=0) == 0
     assert tr(dtype=1) == 2 and b"bf16" in lib.spec_last_error()
+    tc = lambda t=FAKE, h=None, c=None, cap=0, B=4: lib.spec_verify_tree_greedy_commit(
+        FAKE, 0, FAKE, FAKE, None, B, 3, 100, FAKE, FAKE, None, None, FAKE, 8, t, None, 1, h, c, cap, None)
+    assert tc(t=None) == 1 and tc(h=FAKE) == 1 and tc(h=FAKE, c=FAKE, cap=0) == 1
+    assert tc(t=None, B=0) == 0
     # valid commit arguments reach the workspace check (8 bytes: refused) and stop there
+    assert tc() == 3 and b"workspace" in lib.spec_last_error()
     assert g() == 3 and s() == 3 and b"workspace" in lib.spec_last_error()
     assert tr() == 3 and b"workspace" in lib.spec_last_error()
     assert lib.spec_launch_count() == n0

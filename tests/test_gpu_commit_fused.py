@@ -96,3 +96,39 @@ def test_fused_commit_equals_separate_calls(name):
             assert np.array_equal(x, y), (name, proc, n)
     status = got[(True, True)][3]
     assert (status & sv.ST_HISTORY_FULL).any() and not (status & sv.ST_HISTORY_FULL).all()
+
+
+def test_fused_tree_commit_equals_separate_calls():
+    """spec_verify_tree_greedy_commit leaves what spec_verify_tree_greedy followed by
+    spec_commit_kv_lengths (gmax = nmax) leaves: tokens, path, accepted counts, status, both
+    lengths, the history (the path's tokens) and the committed lengths."""
+    tw = W.tree_workload("fused-tree", cfg=65, seed=0, B=24, nmax=15, V=32000)
+    B, n = tw.B, tw.nmax
+    cap = 20
+    ws = torch.zeros(sv.spec_verify_workspace_bytes(B, n, tw.V, sv.SPEC_BF16), dtype=torch.uint8, device="cuda")
+    tgt, toks, pars, nn = dev(tw.target), dev(tw.node_tokens), dev(tw.node_parents), dev(tw.num_nodes)
+    got = {}
+    for fused in (False, True):
+        for proc in (True, False):
+            st = _state(tw, cap, seed=6)
+            out = torch.full((B, n + 1), -7, dtype=torch.int32, device="cuda")
+            m = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+            path = torch.full((B, n), -7, dtype=torch.int32, device="cuda")
+            status = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+            if fused:
+                sv.spec_verify_tree_greedy_commit(tgt, toks, pars, nn, out, m, st["t"], st["d"], proc, st["h"],
+                                                  st["c"], path_nodes=path, status=status, workspace=ws)
+            else:
+                sv.spec_verify_tree_greedy(tgt, toks, pars, nn, out, m, path, status, workspace=ws)
+                sv.spec_commit_kv_lengths(m, st["t"], st["d"], proc, out, st["h"], st["c"], status, gmax=n)
+            torch.cuda.synchronize()
+            got[(fused, proc)] = _host(out, m, path, status, st["t"], st["d"], st["h"], st["c"])
+    assert bool((ws == 0).all())
+    names = ("out_tokens", "num_accepted", "path_nodes", "status", "target_kv_len", "draft_kv_len", "history",
+             "committed_len")
+    for proc in (True, False):
+        for name, x, y in zip(names, got[(False, proc)], got[(True, proc)]):
+            assert np.array_equal(x, y), (proc, name)
+    # the commit did something: lengths advanced where history had room
+    t0 = tw.kv_len.astype(np.int64)
+    assert (got[(True, True)][4] != t0).any()
