@@ -13,18 +13,20 @@
 //   A(b, row, c)  reads row chunk c of one row of sequence b once from HBM (128-bit loads),
 //                 one ex2 per sampled element, and writes a (max, sum 2^((x-max)k)) partial, or
 //                 an (argmax value, id) partial for greedy rows, to the workspace; the unit
-//                 whose chunk holds the row's draft id also records that logit.  The last A
-//                 unit of b to arrive (a counter) is the *decider*: it combines the partials in
-//                 a fixed order, takes the acceptance decisions, finds m, and either writes the
-//                 greedy result or publishes a plan for the final draw.
+//                 whose chunk holds the row's draft id also records that logit.  Each A unit
+//                 counts its arrival when it starts reading; the last of b to arrive is the
+//                 *decider*: once its own row is done it combines the partials in a fixed
+//                 order, takes the acceptance decisions, finds m, and either writes the greedy
+//                 result or publishes a plan for the final draw.
 //   B(b, dc)      draws on the plan: draw chunk dc of the row the last token is drawn from --
 //                 row m of p and q after a rejection, the bonus row otherwise; normally still
 //                 in L2 -- reduced to its residual and p masses.  The last draw chunk of b to
 //                 finish makes its block the *selector*: it locates the chunk holding u*R,
 //                 rescans that chunk and writes the outputs.
 //
-// No block ever has to wait for another.  A B unit may wait a short, bounded while for its
-// plan; each draw chunk then goes through a small state machine (untouched -> claimed by its B
+// No block waits for a block that has not started.  The decider waits, bounded, for the
+// partials of the A units of its sequence that arrived before it (they are running); a B unit
+// may wait a short, bounded while for its plan, then gives up; each draw chunk then goes through a small state machine (untouched -> claimed by its B
 // unit, or untouched -> given up -> taken by the decider) so that exactly one block processes
 // it whatever the timing: the decider takes the chunks whose B units gave up before the plan
 // was out, B units take the rest.  Every call returns the workspace's counters to zero.
@@ -1156,6 +1158,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
     if (!sq.slot_valid(slot, a.gmax)) return;
     if (lo < hi) fetch(t0, lo);
     if (lo + kPass < hi) fetch(t1, lo + kPass);
+    // The arrival is counted now, its round trip hidden behind the row: the unit that arrives
+    // last decides once its own row is done, and waits (bounded, in settle_word) for the
+    // partials of units that arrived before it and are still reading.  Those have arrived, so
+    // they are running: the wait never depends on a block that has not started.
+    int arrived = 0;
+    if (tid == 0) arrived = atom_add_relaxed(&w.cnt[b], 1);
     // the logit at this row's draft id, if it lies in this chunk: fetched once, up front
     const int i = slot <= a.gmax ? slot : slot - a.gmax - 1;
     bool has_d = false, no_d = false;
@@ -1205,14 +1213,14 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) verify_kernel(const Args
         p.y = __int_as_float(pi);
       }
       if (lane == 0) {
-        // published without a fence (see st_relaxed_u64); the arrival count only elects the
+        // published without a fence (see st_relaxed_u64); the arrival count only elected the
         // decider, which polls the words themselves
         if (has_d || no_d)
           st_relaxed_u64(&w.xd[int64_t(b) * geo.nslots + slot], pack_word(canon_bits(has_d ? xv : NAN), has_d ? 1u : 2u));
         st_relaxed_u64(&w.part[(int64_t(b) * geo.nslots + slot) * geo.CL + c],
                        sq.sampling ? pack_word(canon_bits(p.x), __float_as_uint(p.y))
                                    : pack_word(canon_bits(p.x), ~uint32_t(__float_as_int(p.y))));
-        sm.last = atom_add_relaxed(&w.cnt[b], 1) == geo.CL * sq.nrows() - 1;
+        sm.last = arrived == geo.CL * sq.nrows() - 1;
       }
     }
     __syncthreads();
