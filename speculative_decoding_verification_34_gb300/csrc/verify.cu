@@ -20,12 +20,14 @@
 //                 result or publishes a plan for the final draw.
 //   B(b, dc)      draws on the plan: draw chunk dc of the row the last token is drawn from --
 //                 row m of p and q after a rejection, the bonus row otherwise; normally still
-//                 in L2 -- reduced to its residual and p masses.  The last draw chunk of b to
-//                 finish makes its block the *selector*: it locates the chunk holding u*R,
-//                 rescans that chunk and writes the outputs.
+//                 in L2 -- reduced to its residual and p masses.  Each draw chunk counts its
+//                 arrival as it starts; the last of b to arrive makes its block the
+//                 *selector*: it locates the chunk holding u*R, rescans that chunk and writes
+//                 the outputs.
 //
 // No block waits for a block that has not started.  The decider waits, bounded, for the
-// partials of the A units of its sequence that arrived before it (they are running); a B unit
+// partials of the A units of its sequence that arrived before it, the selector for the masses
+// of the draw chunks that arrived before it (they are running); a B unit
 // may wait a short, bounded while for its plan, then gives up; each draw chunk then goes through a small state machine (untouched -> claimed by its B
 // unit, or untouched -> given up -> taken by the decider) so that exactly one block processes
 // it whatever the timing: the decider takes the chunks whose B units gave up before the plan
@@ -578,9 +580,10 @@ __device__ __forceinline__ uint4 vec_at(const typename E::raw* row, int64_t e, i
   }
 }
 
-// The published word at p, given a first read v of it: once it is there (it was stored before
-// its writer's arrival, which this block has seen), the slot returns to zero for the next
-// call.  Bounded: after kWaitNs the sequence is flagged SPEC_ST_TIMEOUT and 0 is used.
+// The published word at p, given a first read v of it: once it is there (its writer has counted
+// its arrival, which this block has seen, so it is running and stores the word when its part
+// is done), the slot returns to zero for the next call.  Bounded: after kWaitNs the sequence is
+// flagged SPEC_ST_TIMEOUT and 0 is used.
 // First reads of several words are issued together, then settled one by one.
 __device__ __forceinline__ uint64_t settle_word(uint64_t* p, uint64_t v, Shared& sm) {
   if (v == 0) {
@@ -831,6 +834,11 @@ __device__ void draw_chunk(const Args& a, const Geo& geo, const Work& w, const S
   const int wlen = geo.dchunk / kWarps;
   const int64_t lo = int64_t(dc) * geo.dchunk + int64_t(warp) * wlen;
   const int64_t hi = lo + wlen < a.V ? lo + wlen : a.V;
+  // the chunk's arrival is counted as it starts (the round trip hidden behind its loads): the
+  // last to arrive selects, polling (bounded) the masses of chunks that arrived before it, which
+  // are therefore being reduced
+  int arrived = 0;
+  if (tid == 0) arrived = atom_add_relaxed(&w.bdone[b], 1);
   float2 ws2 = make_float2(0.f, 0.f), ps2 = ws2;
   for (int64_t e0 = lo; e0 < hi; e0 += kStep) {
     uint4 vp[kDrawVec], vq[kDrawVec];
@@ -854,11 +862,11 @@ __device__ void draw_chunk(const Args& a, const Geo& geo, const Work& w, const S
   const float ws = warp_sum(__fadd_rn(ws2.x, ws2.y));
   const float ps = warp_sum(__fadd_rn(ps2.x, ps2.y));
   // each warp publishes its sub-range's word, (residual, -p): the sign bit of -p (p >= 0)
-  // makes it nonzero; the selector polls the words, so the arrival needs no fence
+  // makes it nonzero; the selector polls the words, so no fence orders them
   if (lane == 0)
     st_relaxed_u64(&w.mass[(int64_t(b) * geo.DCL + dc) * kWarps + warp], pack_word(__float_as_uint(ws), __float_as_uint(-ps)));
   __syncthreads();
-  if (tid == 0) sm.last = atom_add_relaxed(&w.bdone[b], 1) == geo.DCL - 1;
+  if (tid == 0) sm.last = arrived == geo.DCL - 1;
   __syncthreads();
   if (sm.last) select<E, kVec, kMixed, kTrunc>(a, geo, w, sq, pl, sm);
 }
