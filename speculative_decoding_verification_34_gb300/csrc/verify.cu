@@ -59,7 +59,7 @@ static_assert(SPEC_MAX_GAMMA < kThreads, "one output per thread");
 constexpr int kChunkTarget = 65536;            // ids per row chunk before rounding
 constexpr int kDrawChunkTarget = 16384;        // ids per draw chunk before rounding
 constexpr double kDrawWaves = 1.5;             // distance of the draw behind the rows
-constexpr long long kDeferBytes = 48LL << 20;  // draw rows deferred to the end of a call
+constexpr long long kDeferBytes = 32LL << 20;  // draw rows deferred to the end of a call
 constexpr int kMinBlocks = 4;                  // resident blocks per SM the registers allow
 constexpr int kMaxGroups = 65535;                      // grid z limit
 constexpr int kPlanWaitIters = 64;                     // optional bounded wait of a B unit (~31 us)
