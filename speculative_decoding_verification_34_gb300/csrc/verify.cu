@@ -1352,8 +1352,11 @@ __device__ __forceinline__ float key16_value(uint32_t key) {
   return __uint_as_float(bits << 16);
 }
 
+constexpr int kQueueSlots = 64;      // per warp: vectors queued for counting by the fused pass
+
 struct TruncShared {
   unsigned cnt[2][256];          // window counts: [0] a pass's window; [0], [1] the fused pass's
+  uint4 cq[kWarps][kQueueSlots]; // the fused pass's per-warp queues of vectors that reach the window
   float wm[kWarps];
   int wi[kWarps];
   unsigned long long wtot[kWarps];
@@ -1420,8 +1423,9 @@ __device__ __forceinline__ void for_each_bf16(const uint16_t* row, int64_t V, Fn
 
 // Visits every 16-byte vector of a row once: fn(v, nvalid), nvalid = the ids of v inside the
 // row (8 but at a ragged tail), eight vectors per thread per step, coalesced across the block.
-// Vectors wholly past the row are skipped.
-template <bool kVec, class Fn>
+// Vectors wholly past the row are skipped, unless kAll: then every thread calls fn the same
+// number of times (a warp can vote in fn), past the row with vectors of -inf and nvalid 0.
+template <bool kVec, class Fn, bool kAll = false>
 __device__ __forceinline__ void for_each_vec(const uint16_t* row, int64_t V, Fn fn) {
   constexpr int kVecs = 8;
   constexpr int kStep = kThreads * 8 * kVecs;
@@ -1444,7 +1448,7 @@ __device__ __forceinline__ void for_each_vec(const uint16_t* row, int64_t V, Fn 
 #pragma unroll
     for (int q = 0; q < kVecs; ++q) {
       const int64_t e = e0 + int64_t(q * kThreads + tid) * 8;
-      if (e < V) fn(v[q], V - e < 8 ? int(V - e) : 8);
+      if (kAll || e < V) fn(v[q], e >= V ? 0 : (V - e < 8 ? int(V - e) : 8));
     }
   }
 }
@@ -1607,15 +1611,65 @@ __device__ unsigned long long bins_mass(const unsigned* cnt, uint32_t hi, float 
 // fixed before the pass; with kBelow, the mass of the ids under the window relative to the
 // window's lowest value (vk = that value times k; every term is at most 1), so that no max is
 // needed during the pass.
+// A window above +0 holds only values at or above its lowest value vlo, so a vector whose max
+// is under vlo holds none of its ids.  Most vectors are such, and in the fast form the pass
+// counts only the others: each warp queues them in shared memory (`q`, kQueueSlots vectors) and
+// counts their ids 32 vectors at a time, one vector per lane.  The counts are integers, so the
+// order in which ids are counted changes no bit.
 template <bool kVec, bool kFast, bool kBelow>
 __device__ __forceinline__ void fused_pass(const uint16_t* row, int64_t V, const Window& win, float k, float vk,
-                                           unsigned* cnt, __nv_bfloat162& h, float& f) {
-  for_each_vec<kVec>(row, V, [&](const uint4& v, int nv) {
-    const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v);
-    h = __hmax2(h, __hmax2(__hmax2(p2[0], p2[1]), __hmax2(p2[2], p2[3])));
-    float unused = 0.f;
-    window_vec<kFast, kBelow>(v, nv, win, k, vk, cnt, f, unused);
-  });
+                                           unsigned* cnt, uint4* q, __nv_bfloat162& h, float& f) {
+  if constexpr (!kFast) {
+    for_each_vec<kVec>(row, V, [&](const uint4& v, int nv) {
+      const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+      h = __hmax2(h, __hmax2(__hmax2(p2[0], p2[1]), __hmax2(p2[2], p2[3])));
+      float unused = 0.f;
+      window_vec<false, kBelow>(v, nv, win, k, vk, cnt, f, unused);
+    });
+  } else {
+    static_assert(kQueueSlots == 64, "a queue holds fewer than 32 vectors between steps, 32 more per step");
+    const int lane = int(threadIdx.x) & 31;
+    const unsigned below_lane = (1u << lane) - 1u;
+    const uint32_t clast = smem_addr(cnt) + 4u * (win.width - 1u);   // bin width-1: code blo
+    const auto count8 = [&](const uint4& v) {
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t t = ((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu)) - win.blo;
+        count_if(t, win.width, clast - 4u * t);
+      }
+    };
+    unsigned head = 0, tail = 0;   // the queue's counted and written ends (the same in every lane)
+    const auto visit = [&](const uint4& v, int) {
+      const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+      const __nv_bfloat162 vm = __hmax2(__hmax2(p2[0], p2[1]), __hmax2(p2[2], p2[3]));
+      h = __hmax2(h, vm);
+      if constexpr (kBelow) {
+        // the mass under the window, id by id in id order, as window_vec takes it
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float x = __uint_as_float(((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu)) << 16);
+          f = __fadd_rn(f, x < win.vlo ? ex2(fmaf(x, k, -vk)) : 0.f);
+        }
+      }
+      // a NaN half loses to the other in __hmax2; a vector of NaN alone is never counted
+      const bool hit = fmaxf(__low2float(vm), __high2float(vm)) >= win.vlo;
+      const unsigned bal = __ballot_sync(kFull, hit);
+      if (hit) q[(tail + unsigned(__popc(bal & below_lane))) % kQueueSlots] = v;
+      tail += unsigned(__popc(bal));
+      if (tail - head >= 32u) {
+        __syncwarp();
+        count8(q[(head + unsigned(lane)) % kQueueSlots]);
+        head += 32u;
+        __syncwarp();
+      }
+    };
+    // every lane visits the same number of vectors (the ragged step's past-the-row ones too)
+    for_each_vec<kVec, decltype(visit), true>(row, V, visit);
+    __syncwarp();
+    if (unsigned(lane) < tail - head) count8(q[(head + unsigned(lane)) % kQueueSlots]);
+  }
 }
 
 // The thresholds of one row, over windows of 256 keys from key `top` (the row's max, or a key
@@ -1747,12 +1801,13 @@ __global__ void __launch_bounds__(kThreads, kVec ? kMinBlocks : 1) trunc_rows_ke
     __syncthreads();
     __nv_bfloat162 h = __floats2bfloat162_rn(-INFINITY, -INFINITY);
     float f = 0.f;
+    uint4* q = ts.cq[warp];
     if (win.fast) {
-      if (below) fused_pass<kVec, true, true>(row, V, win, k, vk, cnt, h, f);
-      else fused_pass<kVec, true, false>(row, V, win, k, vk, cnt, h, f);
+      if (below) fused_pass<kVec, true, true>(row, V, win, k, vk, cnt, q, h, f);
+      else fused_pass<kVec, true, false>(row, V, win, k, vk, cnt, q, h, f);
     } else {
-      if (below) fused_pass<kVec, false, true>(row, V, win, k, vk, cnt, h, f);
-      else fused_pass<kVec, false, false>(row, V, win, k, vk, cnt, h, f);
+      if (below) fused_pass<kVec, false, true>(row, V, win, k, vk, cnt, q, h, f);
+      else fused_pass<kVec, false, false>(row, V, win, k, vk, cnt, q, h, f);
     }
     __syncthreads();
     M = block_max_f32(fmaxf(__low2float(h), __high2float(h)), ts);
