@@ -1425,13 +1425,39 @@ __device__ __forceinline__ void for_each_bf16(const uint16_t* row, int64_t V, Fn
 // row (8 but at a ragged tail), eight vectors per thread per step, coalesced across the block.
 // Vectors wholly past the row are skipped, unless kAll: then every thread calls fn the same
 // number of times (a warp can vote in fn), past the row with vectors of -inf and nvalid 0.
+// With kAll (the fused pass, whose fn is light) the whole steps go by halves of four vectors
+// per thread, the next half's loads issued before this half is visited.
 template <bool kVec, class Fn, bool kAll = false>
 __device__ __forceinline__ void for_each_vec(const uint16_t* row, int64_t V, Fn fn) {
   constexpr int kVecs = 8;
   constexpr int kStep = kThreads * 8 * kVecs;
   const int tid = int(threadIdx.x);
   int64_t e0 = 0;
-  if constexpr (kVec) {
+  if constexpr (kVec && kAll) {
+    // whole half steps, the next one's loads in flight while this one is visited
+    constexpr int kH = kVecs / 2;
+    constexpr int kHStep = kThreads * 8 * kH;
+    if (kHStep <= V) {
+      uint4 cur[kH];
+#pragma unroll
+      for (int q = 0; q < kH; ++q) cur[q] = ld_stream(row + int64_t(q * kThreads + tid) * 8);
+      for (;;) {
+        const int64_t en = e0 + kHStep;
+        const bool more = en + kHStep <= V;
+        uint4 nxt[kH];
+        if (more) {
+#pragma unroll
+          for (int q = 0; q < kH; ++q) nxt[q] = ld_stream(row + en + int64_t(q * kThreads + tid) * 8);
+        }
+#pragma unroll
+        for (int q = 0; q < kH; ++q) fn(cur[q], 8);
+        e0 = en;
+        if (!more) break;
+#pragma unroll
+        for (int q = 0; q < kH; ++q) cur[q] = nxt[q];
+      }
+    }
+  } else if constexpr (kVec) {
     // whole steps: every vector inside the row (V is a multiple of 8 here), no checks
     for (; e0 + kStep <= V; e0 += kStep) {
       uint4 v[kVecs];
