@@ -107,8 +107,9 @@ def test_repeat_runs_are_bit_identical():
 
 @pytest.mark.parametrize("V", [40000, 151936, 262144, 5001, 270000])
 def test_row_layouts(V):
-    """Rows split over 2, 5 and 8 CTAs' shared memory, a vocabulary that is not a multiple of
-    8 (the scalar load path) and rows longer than eight slices (searched from global memory)."""
+    """Rows that end inside a step of the row pass (V = 40000, 151936, 270000), rows of whole
+    steps only (262144 = 16 steps of 16384 ids: no ragged step), and a vocabulary that is not a
+    multiple of 8 (5001: the scalar load path, a ragged last vector)."""
     wl = W.sampling_workload(f"trunc-V{V}", cfg=76, seed=5, B=6, gmax=3, V=V, dtype="bf16",
                              target_sigma=3.0, draft_scale=0.8, draft_sigma=1.0,
                              temperature=[0.8, 1.0, 0.0, 0.7, 1.2, 0.9], num_draft=[3, 3, 3, 2, 3, 0],
