@@ -1355,7 +1355,8 @@ __device__ __forceinline__ float key16_value(uint32_t key) {
 constexpr int kQueueSlots = 64;      // per warp: vectors queued for counting by the fused pass
 
 struct TruncShared {
-  unsigned cnt[2][256];          // window counts: [0] a pass's window; [0], [1] the fused pass's
+  unsigned cnt[2][256];          // window counts: [0] a pass's window (the fused pass's too); [1] is
+                                 // cleared with it and stays empty at a fused width of 256 keys
   uint4 cq[kWarps][kQueueSlots]; // the fused pass's per-warp queues of vectors that reach the window
   float wm[kWarps];
   int wi[kWarps];
@@ -1822,7 +1823,7 @@ __global__ void __launch_bounds__(kThreads, kVec ? kMinBlocks : 1) trunc_rows_ke
     const Window win(top, kFusedWidth);
     const bool below = !dok;               // the whole row's mass is wanted
     const float vk = __fmul_rn(win.vlo, k);
-    unsigned* cnt = &ts.cnt[0][0];         // [0]: keys top..top-255, [1]: the next 256
+    unsigned* cnt = &ts.cnt[0][0];         // [0]: keys top..top-255 ([1] stays empty at this width)
     for (int i = tid; i < 512; i += kThreads) cnt[i] = 0;
     __syncthreads();
     __nv_bfloat162 h = __floats2bfloat162_rn(-INFINITY, -INFINITY);
@@ -1842,7 +1843,7 @@ __global__ void __launch_bounds__(kThreads, kVec ? kMinBlocks : 1) trunc_rows_ke
       bad = done = true;
     } else if (key16(__float_as_uint(M) >> 16) <= top) {
       // the window holds the max: its counts serve the search's first windows
-      unsigned long long rest = 0, massb = 0;   // masses under both windows, of the second window
+      unsigned long long rest = 0, massb = 0;   // mass under the window; of a second window (none at this width)
       if (below) {
         // per thread from the window's lowest value to the max (a factor at most 1), then fixed point
         rest = block_sum_u64(__float2ull_rn(__fmul_rn(f, ex2(vk - mk)) * kMassUnit), ts);
